@@ -1,0 +1,1288 @@
+// Batched byte-level BPE encoding on one GB300 (sm_103a): CUDA kernels and
+// the C ABI declared in include/bpe_gb300.h.
+//
+// The method: glitch4techs, "Tokenization LLM: building an inference engine
+// in C++", sections "Technical analysis" (GPT-2-style split; each piece is
+// encoded on its own), "Byte-level encoding" (UTF-8 bytes, byte-level
+// symbols), "Byte Pair Encoding algorithm" (repeat: lowest-rank adjacent pair
+// merges, until none is left) and "Vocabulary lookup". Merges replace left to
+// right without overlap (tokenwerk, "Tokenisierung", section "Byte Pair
+// Encoding schrittweise").
+//
+// GPU design (none of it is on the pages, whose engines are CPU code):
+//   * The byte stream is cut into 4 KiB chunks, one CTA each. A CTA loads its
+//     chunk plus a 16-byte halo and a 256-byte margin into shared memory,
+//     decides for every byte whether a pre-token starts there (a local
+//     predicate equivalent to the ordered-alternative split, see
+//     starts_piece), and collects the pre-tokens that start in its chunk.
+//   * Symbols are token ids: byte b starts as byte_id[b]; a merge table maps
+//     (left_id, right_id) to its rank through an open-addressed hash table
+//     of 32-byte buckets (one L2 sector each); rank -> new_id comes from the
+//     merge rows. Because bytes(new_id) = bytes(left) || bytes(right) (checked
+//     by bpe_build), the final symbols are the vocabulary ids.
+//   * Pre-tokens of up to 64 bytes are merged by one thread each in shared
+//     memory with a flat array plus a cached rank per adjacent pair (the
+//     "Hugging Face Tokenizers v1" merge-loop rewrite: flat arrays, integer
+//     rank compare, no allocation). Longer ones are merged by the whole CTA
+//     in place in the caller's output buffer (its byte range there is free
+//     until this chunk publishes its token count).
+//   * Output positions: a single-pass chained scan (decoupled look-back) over
+//     chunk token counts; chunks take tickets in launch order so every
+//     predecessor is already running. Waits are bounded by the global timer.
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <string>
+#include <unordered_set>
+#include <vector>
+
+#include "../../include/bpe_gb300.h"
+
+#define BPE_CLASS_TABLE_STORAGE static __device__ const
+#include "class_table.inc"
+
+namespace {
+
+// ---------------------------------------------------------------- constants --
+
+constexpr int kThreads = 256;         // threads per CTA
+constexpr int kChunk = 4096;          // bytes whose pre-tokens a CTA owns
+constexpr int kMargin = 256;          // bytes after the chunk kept in shared memory
+constexpr int kHalo = 16;             // context bytes on each side of the window
+constexpr int kWin = kHalo + kChunk + kMargin + kHalo;   // window bytes
+constexpr int kWinWords = (kWin + 31) / 32;
+constexpr int kSpan = kChunk + kMargin;                  // positions with a start bit
+constexpr int kSpanWords = kSpan / 32;
+constexpr int kShortMax = 64;         // longest pre-token merged by one thread
+constexpr int kLongPerThread = 4;     // elements per thread per round of the CTA merge
+constexpr int kRound = kThreads * kLongPerThread;
+constexpr int kMaxLong = kChunk / kShortMax + 2;
+constexpr uint32_t kInf = 0xFFFFFFFFu;
+constexpr uint32_t kNone = 0xFFFFFFFFu;
+constexpr uint64_t kEmpty = ~0ull;
+constexpr uint64_t kWaitLimitNs = 20ull * 1000 * 1000 * 1000;  // 20 s
+
+// device status bits
+constexpr uint32_t kStBadInput = 1u;
+constexpr uint32_t kStTimeout = 2u;
+constexpr uint32_t kStInternal = 4u;
+constexpr uint32_t kStCapacity = 8u;
+
+// look-back descriptor: status in bits 62..63, value below
+constexpr uint64_t kDescAgg = 1ull << 62;
+constexpr uint64_t kDescIncl = 2ull << 62;
+constexpr uint64_t kDescValue = (1ull << 62) - 1;
+
+enum Cls { kO = 0, kL = 1, kN = 2, kS = 3 };
+
+__host__ __device__ inline uint32_t pair_hash(uint32_t a, uint32_t b) {
+  // MurmurHash3's 64-bit finalizer over the packed pair.
+  uint64_t x = ((uint64_t)a << 32) | b;
+  x ^= x >> 33;
+  x *= 0xFF51AFD7ED558CCDull;
+  x ^= x >> 33;
+  x *= 0xC4CEB9FE1A85EC53ull;
+  x ^= x >> 33;
+  return (uint32_t)x;
+}
+
+struct Tables {
+  const uint64_t* ht;      // 4 entries per bucket: left << 40 | right << 20 | rank
+  uint32_t hmask;          // buckets - 1
+  const int32_t* mrows;    // [n_merges][3] (left, right, new)
+  const int32_t* byte_id;  // [256]
+};
+
+struct DevSmall {
+  uint32_t status;
+  uint32_t ticket;
+  int64_t total;
+};
+
+// ------------------------------------------------------------ small helpers --
+
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lookup_rank(const Tables& T, uint32_t a, uint32_t b) {
+  const uint64_t key = ((uint64_t)a << 20) | b;
+  uint32_t bucket = pair_hash(a, b) & T.hmask;
+  for (uint32_t probe = 0; probe <= T.hmask; ++probe) {
+    const ulonglong2* p = reinterpret_cast<const ulonglong2*>(T.ht + 4ull * bucket);
+    ulonglong2 u = __ldg(p), v = __ldg(p + 1);
+    if ((u.x >> 20) == key) return (uint32_t)(u.x & 0xFFFFF);
+    if ((u.y >> 20) == key) return (uint32_t)(u.y & 0xFFFFF);
+    if ((v.x >> 20) == key) return (uint32_t)(v.x & 0xFFFFF);
+    if ((v.y >> 20) == key) return (uint32_t)(v.y & 0xFFFFF);
+    if (u.x == kEmpty || u.y == kEmpty || v.x == kEmpty || v.y == kEmpty) return kInf;
+    bucket = (bucket + 1) & T.hmask;
+  }
+  return kInf;
+}
+
+__device__ __forceinline__ int cp_class(uint32_t cp) {
+  uint32_t blk = kClassL1[cp >> 8];
+  uint32_t w = kClassL2[blk * 16 + ((cp & 255) >> 4)];
+  return (int)((w >> ((cp & 15) * 2)) & 3);
+}
+
+__device__ __forceinline__ bool is_cont(uint32_t b) { return (b & 0xC0) == 0x80; }
+
+// ------------------------------------------------------------- UTF-8 units --
+// A unit is a well-formed UTF-8 sequence (Unicode's table of well-formed byte
+// sequences) or, failing that, one byte on its own. Sequences do not cross a
+// document edge: [lo, hi) is the document of the position asked about.
+
+template <typename I>
+__device__ __forceinline__ int seq_len(const uint8_t* w, I hi, I q) {
+  uint32_t b0 = w[q];
+  if (b0 < 0x80) return 1;
+  if (b0 < 0xC2) return 0;
+  if (b0 < 0xE0) return (q + 1 < hi && is_cont(w[q + 1])) ? 2 : 0;
+  if (b0 < 0xF0) {
+    if (q + 2 >= hi) return 0;
+    uint32_t b1 = w[q + 1];
+    uint32_t lo1 = (b0 == 0xE0) ? 0xA0 : 0x80, hi1 = (b0 == 0xED) ? 0x9F : 0xBF;
+    return (b1 >= lo1 && b1 <= hi1 && is_cont(w[q + 2])) ? 3 : 0;
+  }
+  if (b0 < 0xF5) {
+    if (q + 3 >= hi) return 0;
+    uint32_t b1 = w[q + 1];
+    uint32_t lo1 = (b0 == 0xF0) ? 0x90 : 0x80, hi1 = (b0 == 0xF4) ? 0x8F : 0xBF;
+    return (b1 >= lo1 && b1 <= hi1 && is_cont(w[q + 2]) && is_cont(w[q + 3])) ? 4 : 0;
+  }
+  return 0;
+}
+
+// Start of the unit that holds byte p, and that unit's sequence length (0 for
+// a lone invalid byte).
+template <typename I>
+__device__ __forceinline__ I unit_start_of(const uint8_t* w, I lo, I hi, I p, int* len) {
+  if (is_cont(w[p])) {
+    for (int k = 1; k <= 3 && p - k >= lo; ++k) {
+      I q = p - k;
+      if (!is_cont(w[q])) {
+        int L = seq_len(w, hi, q);
+        if (L > k) { *len = L; return q; }
+        break;
+      }
+    }
+    *len = 0;
+    return p;
+  }
+  *len = seq_len(w, hi, p);
+  return p;
+}
+
+template <typename I>
+__device__ __forceinline__ int unit_class(const uint8_t* w, I q, int len) {
+  uint32_t b0 = w[q];
+  if (len == 0) return kO;
+  if (len == 1) return cp_class(b0);
+  uint32_t cp;
+  if (len == 2) cp = ((b0 & 0x1Fu) << 6) | (w[q + 1] & 0x3Fu);
+  else if (len == 3) cp = ((b0 & 0x0Fu) << 12) | ((w[q + 1] & 0x3Fu) << 6) | (w[q + 2] & 0x3Fu);
+  else cp = ((b0 & 0x07u) << 18) | ((w[q + 1] & 0x3Fu) << 12) | ((w[q + 2] & 0x3Fu) << 6) | (w[q + 3] & 0x3Fu);
+  return cp_class(cp);
+}
+
+template <typename I>
+__device__ __forceinline__ int class_at(const uint8_t* w, I lo, I hi, I p) {
+  int len;
+  I q = unit_start_of(w, lo, hi, p, &len);
+  return unit_class(w, q, len);
+}
+
+// ---------------------------------------------------------- pre-tokenizer --
+// The GPT-2-style split tries, at each position, the ordered alternatives
+//   's|'t|'re|'ve|'m|'ll|'d | ' '?L+ | ' '?N+ | ' '?O+ | S+(?!S) | S+
+// (L letter, N number, S whitespace, O anything else). Its pieces are fixed
+// by a predicate over a few neighbouring units, decided in this order for a
+// unit start i inside a document (the document start always starts a piece):
+//   B0 c[i-1] is an apostrophe that starts a piece, and c[i..] begins a
+//      contraction suffix (s t m d re ve ll): no boundary;
+//   B1 a contraction ends at i (its apostrophe starts a piece): boundary;
+//   B2 c[i] in S: boundary iff c[i-1] not in S, or c[i+1] exists and is not
+//      in S (the last whitespace before a non-space is split off);
+//   B3 otherwise: no boundary after a U+0020 (the optional space joins the
+//      run), boundary after other whitespace, else boundary iff the classes
+//      L / N / O of c[i-1] and c[i] differ.
+// An apostrophe at j starts a piece iff j is the document start or c[j-1] is
+// a letter, a number or whitespace other than U+0020.
+
+__device__ __forceinline__ bool is_stmd(uint32_t b) { return b == 's' || b == 't' || b == 'm' || b == 'd'; }
+__device__ __forceinline__ bool is_suffix2(uint32_t a, uint32_t b) {
+  return (a == 'r' && b == 'e') || (a == 'v' && b == 'e') || (a == 'l' && b == 'l');
+}
+
+template <typename I>
+__device__ __forceinline__ bool apostrophe_starts_piece(const uint8_t* w, I lo, I hi, I j) {
+  if (j == lo) return true;
+  int c = class_at(w, lo, hi, j - 1);
+  return c == kL || c == kN || (c == kS && w[j - 1] != ' ');
+}
+
+template <typename I>
+__device__ bool starts_piece(const uint8_t* w, I lo, I hi, I i) {
+  if (i == lo) return true;
+  int len;
+  if (unit_start_of(w, lo, hi, i, &len) != i) return false;
+  const int ci = unit_class(w, i, len);
+  const uint32_t bp = w[i - 1];
+  const int cprev = class_at(w, lo, hi, i - 1);
+  if (bp == '\'') {  // B0
+    const uint32_t b0 = w[i];
+    const bool suffix = is_stmd(b0) || (i + 1 < hi && is_suffix2(b0, w[i + 1]));
+    if (suffix && apostrophe_starts_piece(w, lo, hi, i - 1)) return false;
+  }
+  if (i - 2 >= lo && w[i - 2] == '\'' && is_stmd(bp) && apostrophe_starts_piece(w, lo, hi, i - 2)) return true;
+  if (i - 3 >= lo && w[i - 3] == '\'' && is_suffix2(w[i - 2], bp) && apostrophe_starts_piece(w, lo, hi, i - 3))
+    return true;
+  if (ci == kS) {  // B2
+    if (cprev != kS) return true;
+    const I e = i + (len > 0 ? len : 1);
+    return e < hi && class_at(w, lo, hi, e) != kS;
+  }
+  if (bp == ' ') return false;  // B3
+  if (cprev == kS) return true;
+  return ci != cprev;
+}
+
+// ----------------------------------------------------------- block helpers --
+
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    uint32_t o = __shfl_up_sync(0xFFFFFFFFu, v, d);
+    if (lane >= d) v += o;
+  }
+  return v;
+}
+
+// Exclusive scan over the CTA; *total gets the sum. Uses red[0..kThreads/32].
+__device__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = warp_incl_scan(v);
+  if (lane == 31) red[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t x = lane < kThreads / 32 ? red[lane] : 0;
+    uint32_t xi = warp_incl_scan(x);
+    if (lane < kThreads / 32) red[lane] = xi - x;
+    if (lane == kThreads / 32 - 1) red[kThreads / 32] = xi;
+  }
+  __syncthreads();
+  uint32_t r = red[warp] + incl - v;
+  *total = red[kThreads / 32];
+  __syncthreads();
+  return r;
+}
+
+__device__ uint32_t block_min(uint32_t v, uint32_t* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v = min(v, __shfl_xor_sync(0xFFFFFFFFu, v, d));
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  uint32_t r = red[0];
+  for (int k = 1; k < kThreads / 32; ++k) r = min(r, red[k]);
+  __syncthreads();
+  return r;
+}
+
+// Transfer functions {0,1} -> {0,1} packed as bit0 = f(0), bit1 = f(1).
+__device__ __forceinline__ uint32_t tf_apply(uint32_t f, uint32_t x) { return (f >> x) & 1u; }
+__device__ __forceinline__ uint32_t tf_then(uint32_t first, uint32_t second) {
+  return tf_apply(second, first & 1u) | (tf_apply(second, (first >> 1) & 1u) << 1);
+}
+
+// Exclusive scan of transfer functions over the CTA, applied to carry_in.
+__device__ uint32_t block_tf_input(uint32_t f, uint32_t carry_in, uint32_t* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = f;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl = tf_then(o, incl);
+  }
+  if (lane == 31) red[warp] = incl;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t acc = 2u;  // identity
+    for (int k = 0; k < kThreads / 32; ++k) {
+      uint32_t t = red[k];
+      red[k] = acc;
+      acc = tf_then(acc, t);
+    }
+  }
+  __syncthreads();
+  uint32_t excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+  if (lane == 0) excl = 2u;
+  uint32_t before = tf_then(red[warp], excl);
+  uint32_t r = tf_apply(before, carry_in);
+  __syncthreads();
+  return r;
+}
+
+// ----------------------------------------------------------- merge: short --
+// One thread, symbols and pair ranks in shared memory. rk[k] is the rank of
+// (sym[k], sym[k+1]). A step takes the lowest rank, replaces every occurrence
+// of that pair left to right without overlap, and re-probes only the pairs
+// that touch a new symbol.
+
+__device__ int merge_short(uint32_t* sym, uint32_t* rk, const uint8_t* src, int n, const Tables& T,
+                           const int32_t* byte_id) {
+  for (int k = 0; k < n; ++k) sym[k] = (uint32_t)byte_id[src[k]];
+  if (n < 2) return n;
+  for (int k = 0; k + 1 < n; ++k) rk[k] = lookup_rank(T, sym[k], sym[k + 1]);
+  for (;;) {
+    uint32_t best = kInf;
+    for (int k = 0; k + 1 < n; ++k) best = min(best, rk[k]);
+    if (best == kInf) break;
+    const uint32_t nw = (uint32_t)T.mrows[3 * best + 2];
+    int w = 0, prev_old = -1, k = 0;
+    while (k < n) {
+      uint32_t s;
+      int old;
+      if (k + 1 < n && rk[k] == best) {
+        s = nw;
+        old = -1;
+        k += 2;
+      } else {
+        s = sym[k];
+        old = k;
+        k += 1;
+      }
+      if (w > 0) {
+        uint32_t r = (old >= 0 && prev_old >= 0 && old == prev_old + 1) ? rk[prev_old] : lookup_rank(T, sym[w - 1], s);
+        rk[w - 1] = r;
+      }
+      sym[w] = s;
+      prev_old = old;
+      ++w;
+    }
+    n = w;
+    if (n < 2) break;
+  }
+  return n;
+}
+
+// ------------------------------------------------------------ merge: long --
+// The whole CTA merges one long pre-token in place in scr (its own byte range
+// of the output buffer, read and written in rounds of kRound elements; a
+// round writes only below where it read). A step is one pass: the chosen pair
+// is replaced left to right without overlap — each thread runs that scan over
+// its kLongPerThread elements for both possible "first element already
+// consumed" inputs, a CTA scan composes the results in order — and the pass
+// also probes every new adjacent pair for the next step's lowest rank.
+
+struct LongScratch {
+  uint32_t* stage;  // kRound
+  uint32_t* red;    // kThreads / 32 + 2
+  uint32_t* carry;  // 1
+};
+
+__device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, int32_t* scr, const Tables& T,
+                               const int32_t* byte_id, LongScratch L) {
+  const int tid = threadIdx.x;
+  uint32_t len = n;
+  bool first_pass = true;
+  uint32_t A = 0, B = 0, NW = 0;
+  for (;;) {
+    uint32_t W = 0, carry = 0, prev_sym = kNone, local_min = kInf;
+    for (uint32_t r0 = 0; r0 < len; r0 += kRound) {
+      uint32_t x[kLongPerThread + 1];
+#pragma unroll
+      for (int k = 0; k <= kLongPerThread; ++k) {
+        uint32_t idx = r0 + (uint32_t)tid * kLongPerThread + (uint32_t)k;
+        x[k] = kNone;
+        if (idx < len) x[k] = first_pass ? (uint32_t)byte_id[g_bytes[s + idx]] : (uint32_t)scr[idx];
+      }
+      uint32_t f = 2u;
+      if (!first_pass) {
+        f = 0;
+#pragma unroll
+        for (uint32_t in = 0; in < 2; ++in) {
+          uint32_t consumed = in;
+#pragma unroll
+          for (int k = 0; k < kLongPerThread; ++k) {
+            if (x[k] == kNone) break;
+            if (consumed) consumed = 0;
+            else if (x[k] == A && x[k + 1] == B) consumed = 1;
+          }
+          f |= consumed << in;
+        }
+      }
+      uint32_t consumed = block_tf_input(f, carry, L.red);  // also orders all reads before writes
+      uint32_t y[kLongPerThread];
+      uint32_t cnt = 0;
+#pragma unroll
+      for (int k = 0; k < kLongPerThread; ++k) {
+        if (x[k] == kNone) break;
+        if (consumed) {
+          consumed = 0;
+        } else if (!first_pass && x[k] == A && x[k + 1] == B) {
+          y[cnt++] = NW;
+          consumed = 1;
+        } else {
+          y[cnt++] = x[k];
+        }
+      }
+      if (tid == kThreads - 1) L.carry[0] = consumed;
+      uint32_t round_cnt;
+      uint32_t pos = block_excl_scan(cnt, L.red, &round_cnt);
+      for (uint32_t j = 0; j < cnt; ++j) L.stage[pos + j] = y[j];
+      __syncthreads();
+      for (uint32_t q = tid; q < round_cnt; q += kThreads) {
+        uint32_t left = q == 0 ? prev_sym : L.stage[q - 1];
+        uint32_t right = L.stage[q];
+        if (left != kNone) local_min = min(local_min, lookup_rank(T, left, right));
+        scr[W + q] = (int32_t)right;
+      }
+      if (round_cnt > 0) prev_sym = L.stage[round_cnt - 1];
+      W += round_cnt;
+      carry = L.carry[0];
+      __syncthreads();
+    }
+    len = W;
+    first_pass = false;
+    uint32_t best = block_min(local_min, L.red);
+    if (best == kInf) break;
+    A = (uint32_t)T.mrows[3 * best];
+    B = (uint32_t)T.mrows[3 * best + 1];
+    NW = (uint32_t)T.mrows[3 * best + 2];
+  }
+  __syncthreads();
+  return len;
+}
+
+// ------------------------------------------------------------------ window --
+
+struct Smem {
+  uint8_t win[kWin + 16];
+  uint32_t docbits[kWinWords];   // a document (or the area after the last one) starts here
+  uint32_t outbits[kWinWords];   // byte belongs to no document
+  uint32_t startbits[kSpanWords];
+  uint16_t span_start[kChunk + 1];
+  uint32_t span_cnt[kChunk + 1];
+  uint32_t sym[kSpan];
+  uint32_t rk[kSpan];
+  uint32_t stage[kRound];
+  int32_t byte_id[256];
+  uint16_t long_list[kMaxLong];
+  uint32_t red[kThreads / 32 + 2];
+  uint32_t carry[2];
+  int64_t chunk;
+  int64_t prefix;
+  uint32_t n_spans;
+  uint32_t n_long;
+  int64_t last_end;
+  int64_t doc_lo, doc_hi;  // document of a long pre-token that runs past the window
+};
+
+__device__ __forceinline__ bool bit_at(const uint32_t* bits, int i) { return (bits[i >> 5] >> (i & 31)) & 1u; }
+
+// Document bounds [lo, hi) around window index i: the nearest document edge at
+// or before i and the next one after i (at most kHalo away is all that is
+// read), or the window edges.
+__device__ __forceinline__ void doc_bounds(const Smem& S, int i, int* lo, int* hi) {
+  int a = i;
+  while (a > 0 && a > i - kHalo && !bit_at(S.docbits, a)) --a;
+  *lo = a;
+  int b = i + 1;
+  while (b < kWin && b <= i + kHalo && !bit_at(S.docbits, b)) ++b;
+  *hi = b;
+}
+
+// Loads the window of chunk c: bytes [c0 - kHalo, c0 + kChunk + kMargin +
+// kHalo), the document edges that fall inside it, and which bytes lie outside
+// every document. first_doc = the first document starting at or after c0.
+__device__ void load_window(Smem& S, const uint8_t* bytes, int64_t n_bytes, const int64_t* doc_offsets,
+                            int64_t n_docs, int64_t c0, int64_t first_doc) {
+  const int tid = threadIdx.x;
+  const int64_t w0 = c0 - kHalo;
+  for (int i = tid; i < kWin; i += kThreads) {
+    int64_t p = w0 + i;
+    S.win[i] = (p >= 0 && p < n_bytes) ? bytes[p] : 0;
+  }
+  for (int i = tid; i < kWinWords; i += kThreads) {
+    S.docbits[i] = 0;
+    S.outbits[i] = 0;
+  }
+  __syncthreads();
+  int64_t d_first = doc_offsets[0], d_last = doc_offsets[n_docs];
+  d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
+  d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
+  for (int i = tid; i < kWin; i += kThreads) {
+    int64_t p = w0 + i;
+    if (p < d_first || p >= d_last) atomicOr(&S.outbits[i >> 5], 1u << (i & 31));
+  }
+  // Document starts in the window: walk back from first_doc over starts in
+  // the halo, then forward.
+  int64_t k_lo = first_doc;
+  if (k_lo > n_docs) k_lo = n_docs;
+  if (k_lo < 0) k_lo = 0;
+  while (k_lo > 0 && doc_offsets[k_lo - 1] >= w0) --k_lo;
+  const int64_t w_end = w0 + kWin;
+  for (int64_t k = k_lo + tid; k <= n_docs; k += kThreads) {
+    int64_t o = doc_offsets[k];
+    if (o >= w_end) break;
+    if (o >= w0) {
+      int i = (int)(o - w0);
+      atomicOr(&S.docbits[i >> 5], 1u << (i & 31));
+    }
+  }
+  __syncthreads();
+}
+
+// Start bits for window indices [kHalo, kHalo + kSpan).
+__device__ void compute_start_bits(Smem& S) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int base = warp * 32; base < kSpan; base += kThreads) {
+    const int i = kHalo + base + lane;
+    bool b = false;
+    if (!bit_at(S.outbits, i)) {
+      int lo, hi;
+      doc_bounds(S, i, &lo, &hi);
+      b = starts_piece<int>(S.win, lo, hi, i);
+    }
+    uint32_t word = __ballot_sync(0xFFFFFFFFu, b);
+    if (lane == 0) S.startbits[base >> 5] = word;
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ kernels --
+
+// Per call: chunk descriptors cleared, first document of every chunk found,
+// offsets validated, ticket reset.
+__global__ void k_prep(const int64_t* doc_offsets, int64_t n_docs, int64_t n_bytes, int64_t n_chunks,
+                       uint64_t* desc, int64_t* first_doc, DevSmall* small) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t0 == 0) {
+    small->ticket = 0;
+    small->total = 0;
+  }
+  for (int64_t c = t0; c < n_chunks; c += stride) {
+    desc[c] = 0;
+    const int64_t target = c * kChunk;
+    int64_t lo = 0, hi = n_docs + 1;  // first k with doc_offsets[k] >= target
+    while (lo < hi) {
+      int64_t mid = (lo + hi) >> 1;
+      if (doc_offsets[mid] < target) lo = mid + 1;
+      else hi = mid;
+    }
+    first_doc[c] = lo;
+  }
+  bool bad = false;
+  for (int64_t k = t0; k <= n_docs; k += stride) {
+    int64_t o = doc_offsets[k];
+    if (o < 0 || o > n_bytes) bad = true;
+    if (k < n_docs && doc_offsets[k + 1] < o) bad = true;
+  }
+  if (bad) atomicOr(&small->status, kStBadInput);
+}
+
+struct EncodeArgs {
+  const uint8_t* bytes;
+  int64_t n_bytes;
+  const int64_t* doc_offsets;
+  int64_t n_docs;
+  int32_t* out_ids;
+  int64_t* out_offsets;
+  Tables T;
+  uint64_t* desc;
+  const int64_t* first_doc;
+  DevSmall* small;
+  int64_t n_chunks;
+};
+
+__global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  const int tid = threadIdx.x;
+
+  if (tid == 0) S.chunk = (int64_t)atomicAdd(&a.small->ticket, 1u);
+  for (int i = tid; i < 256; i += kThreads) S.byte_id[i] = a.T.byte_id[i];
+  __syncthreads();
+  const int64_t c = S.chunk;
+  const int64_t c0 = c * kChunk;
+  load_window(S, a.bytes, a.n_bytes, a.doc_offsets, a.n_docs, c0, a.first_doc[c]);
+  compute_start_bits(S);
+
+  // Pre-tokens starting in the chunk, in order. Thread t owns positions
+  // [16 t, 16 t + 16) of the chunk.
+  {
+    const uint32_t bits = (S.startbits[tid >> 1] >> ((tid & 1) * 16)) & 0xFFFFu;
+    uint32_t total;
+    uint32_t pos = block_excl_scan(__popc(bits), S.red, &total);
+    uint32_t b = bits;
+    while (b) {
+      int k = __ffs(b) - 1;
+      b &= b - 1;
+      S.span_start[pos++] = (uint16_t)(tid * 16 + k);
+    }
+    if (tid == 0) {
+      S.n_spans = total;
+      S.n_long = 0;
+      S.last_end = -1;
+    }
+  }
+  __syncthreads();
+  const uint32_t n_spans = S.n_spans;
+
+  // End of the last pre-token: the next start or document edge in the margin,
+  // or -1 when it runs past the window.
+  if (tid == 0 && n_spans > 0) {
+    int from = S.span_start[n_spans - 1] + 1;
+    int64_t end = -1;
+    for (int j = from; j < kSpan; ++j) {
+      const int i = kHalo + j;
+      if (bit_at(S.startbits, j) || bit_at(S.outbits, i) || bit_at(S.docbits, i)) {
+        end = c0 + j;
+        break;
+      }
+    }
+    S.last_end = end;
+  }
+  __syncthreads();
+
+  // Short pre-tokens: one thread each.
+  for (uint32_t j = tid; j < n_spans; j += kThreads) {
+    const int st = S.span_start[j];
+    int64_t en;
+    if (j + 1 < n_spans) en = c0 + S.span_start[j + 1];
+    else en = S.last_end;
+    const int len = en < 0 ? kSpan : (int)(en - (c0 + st));
+    if (en >= 0 && len <= kShortMax) {
+      S.span_cnt[j] = (uint32_t)merge_short(S.sym + st, S.rk + st, S.win + kHalo + st, len, a.T, S.byte_id);
+    } else {
+      uint32_t slot = atomicAdd(&S.n_long, 1u);
+      if (slot < (uint32_t)kMaxLong) S.long_list[slot] = (uint16_t)j;
+      else atomicOr(&a.small->status, kStInternal);
+      S.span_cnt[j] = 0;
+    }
+  }
+  __syncthreads();
+
+  // Long pre-tokens: the whole CTA, one at a time, in order.
+  const uint32_t n_long = min(S.n_long, (uint32_t)kMaxLong);
+  if (tid == 0 && n_long > 1) {  // sort the short list (insertion sort)
+    for (uint32_t x = 1; x < n_long; ++x) {
+      uint16_t v = S.long_list[x];
+      int y = (int)x - 1;
+      while (y >= 0 && S.long_list[y] > v) {
+        S.long_list[y + 1] = S.long_list[y];
+        --y;
+      }
+      S.long_list[y + 1] = v;
+    }
+  }
+  __syncthreads();
+  LongScratch L{S.stage, S.red, S.carry};
+  for (uint32_t x = 0; x < n_long; ++x) {
+    const uint32_t j = S.long_list[x];
+    const int64_t s = c0 + S.span_start[j];
+    int64_t e = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
+    if (e < 0) {
+      // Runs past the window: find the document it lies in, then the next
+      // pre-token start after the window.
+      if (tid == 0) {
+        int64_t lo = 0, hi = a.n_docs + 1;  // first k with doc_offsets[k] > s
+        while (lo < hi) {
+          int64_t mid = (lo + hi) >> 1;
+          if (a.doc_offsets[mid] <= s) lo = mid + 1;
+          else hi = mid;
+        }
+        int64_t k = lo - 1;
+        int64_t dlo = (k >= 0) ? a.doc_offsets[k] : 0;
+        int64_t dhi = (k >= 0 && k < a.n_docs) ? a.doc_offsets[k + 1] : s + 1;
+        if (dhi > a.n_bytes) dhi = a.n_bytes;
+        if (dlo > s) dlo = s;
+        if (dlo < 0) dlo = 0;
+        if (dhi <= s) dhi = s + 1;
+        S.doc_lo = dlo;
+        S.doc_hi = dhi;
+      }
+      __syncthreads();
+      const int64_t dlo = S.doc_lo, dhi = S.doc_hi;
+      int64_t found = dhi;
+      for (int64_t base = c0 + kSpan; base < dhi; base += kThreads) {
+        const int64_t p = base + tid;
+        bool b = p < dhi && starts_piece<int64_t>(a.bytes, dlo, dhi, p);
+        uint32_t cand = b ? (uint32_t)(p - base) : kInf;
+        uint32_t m = block_min(cand, S.red);
+        if (m != kInf) {
+          found = base + m;
+          break;
+        }
+      }
+      e = found;
+    }
+    const int64_t n = e - s;
+    if (n <= 0 || n >= (int64_t)0x7FFFFFFF) {
+      if (tid == 0) atomicOr(&a.small->status, kStInternal);
+      if (tid == 0) S.span_cnt[j] = 0;
+    } else {
+      uint32_t cnt = merge_long(a.bytes, s, (uint32_t)n, a.out_ids + s, a.T, S.byte_id, L);
+      if (tid == 0) S.span_cnt[j] = cnt;
+    }
+    __syncthreads();
+  }
+
+  // Token offsets within the chunk.
+  uint32_t agg = 0;
+  {
+    // Each thread scans a contiguous run of spans.
+    const uint32_t per = (n_spans + kThreads - 1) / kThreads;
+    const uint32_t j0 = min(n_spans, tid * per), j1 = min(n_spans, j0 + per);
+    uint32_t sum = 0;
+    for (uint32_t j = j0; j < j1; ++j) sum += S.span_cnt[j];
+    uint32_t base = block_excl_scan(sum, S.red, &agg);
+    for (uint32_t j = j0; j < j1; ++j) {
+      uint32_t v = S.span_cnt[j];
+      S.span_cnt[j] = base;
+      base += v;
+    }
+    if (tid == 0) S.span_cnt[n_spans] = agg;
+  }
+
+  // Chained scan over chunks.
+  if (tid == 0) {
+    uint64_t* desc = a.desc;
+    int64_t excl = 0;
+    if (c == 0) {
+      st_relaxed(&desc[0], kDescIncl | (uint64_t)agg);
+    } else {
+      st_relaxed(&desc[c], kDescAgg | (uint64_t)agg);
+      int64_t j = c - 1;
+      const uint64_t t_start = global_timer();
+      bool timed_out = false;
+      while (j >= 0) {
+        uint64_t d = ld_relaxed(&desc[j]);
+        if ((d & ~kDescValue) == 0) {
+          if (global_timer() - t_start > kWaitLimitNs) {
+            timed_out = true;
+            break;
+          }
+          __nanosleep(64);
+          continue;
+        }
+        excl += (int64_t)(d & kDescValue);
+        if ((d & ~kDescValue) == kDescIncl) break;
+        --j;
+      }
+      if (timed_out) atomicOr(&a.small->status, kStTimeout);
+      st_relaxed(&desc[c], kDescIncl | (uint64_t)(excl + agg));
+    }
+    S.prefix = excl;
+    if (c == a.n_chunks - 1) a.small->total = excl + agg;
+  }
+  __syncthreads();
+  const int64_t P = S.prefix;
+
+  // Long pre-tokens: move from their scratch range to their place, in order
+  // (a move lands at or below the next long pre-token's range).
+  for (uint32_t x = 0; x < n_long; ++x) {
+    const uint32_t j = S.long_list[x];
+    const int64_t s = c0 + S.span_start[j];
+    const int64_t dst = P + S.span_cnt[j];
+    const uint32_t cnt = S.span_cnt[j + 1] - S.span_cnt[j];
+    if (dst != s) {
+      for (uint32_t b0 = 0; b0 < cnt; b0 += kThreads) {
+        uint32_t q = b0 + tid;
+        int32_t v = 0;
+        if (q < cnt) v = a.out_ids[s + q];
+        __syncthreads();
+        if (q < cnt) a.out_ids[dst + q] = v;
+        __syncthreads();
+      }
+    }
+    __syncthreads();
+  }
+
+  // Short pre-tokens: ids from shared memory.
+  for (uint32_t j = tid; j < n_spans; j += kThreads) {
+    const int st = S.span_start[j];
+    bool is_long = false;
+    for (uint32_t x = 0; x < n_long; ++x) is_long |= (S.long_list[x] == j);
+    if (is_long) continue;
+    const uint32_t o = S.span_cnt[j], cnt = S.span_cnt[j + 1] - o;
+    int32_t* dst = a.out_ids + P + o;
+    for (uint32_t q = 0; q < cnt; ++q) dst[q] = (int32_t)S.sym[st + q];
+  }
+
+  // Offsets of the documents that start in this chunk.
+  {
+    int64_t k0 = a.first_doc[c];
+    for (int64_t k = k0 + tid; k <= a.n_docs; k += kThreads) {
+      const int64_t d = a.doc_offsets[k];
+      if (d >= c0 + kChunk) break;
+      if (d < c0) continue;
+      const int rel = (int)(d - c0);
+      uint32_t lo = 0, hi = n_spans;  // first span starting at or after d
+      while (lo < hi) {
+        uint32_t mid = (lo + hi) >> 1;
+        if (S.span_start[mid] < rel) lo = mid + 1;
+        else hi = mid;
+      }
+      a.out_offsets[k] = P + S.span_cnt[lo];
+    }
+  }
+}
+
+// Pre-tokenizer alone: start bits of [c0, c0 + kChunk) for chunk blockIdx.x.
+__global__ void __launch_bounds__(kThreads) k_pretokenize(const uint8_t* bytes, int64_t n_bytes,
+                                                          const int64_t* doc_offsets, int64_t n_docs,
+                                                          uint32_t* out_bits) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  const int64_t c0 = (int64_t)blockIdx.x * kChunk;
+  __shared__ int64_t s_first;
+  if (threadIdx.x == 0) {
+    int64_t lo = 0, hi = n_docs + 1;
+    while (lo < hi) {
+      int64_t mid = (lo + hi) >> 1;
+      if (doc_offsets[mid] < c0) lo = mid + 1;
+      else hi = mid;
+    }
+    s_first = lo;
+  }
+  __syncthreads();
+  load_window(S, bytes, n_bytes, doc_offsets, n_docs, c0, s_first);
+  compute_start_bits(S);
+  const int64_t n_words = (n_bytes + 31) / 32;
+  for (int w = threadIdx.x; w < kChunk / 32; w += kThreads) {
+    const int64_t gw = c0 / 32 + w;
+    if (gw < n_words) {
+      uint32_t v = S.startbits[w];
+      const int64_t first_bit = gw * 32;
+      if (first_bit + 32 > n_bytes) v &= (n_bytes - first_bit >= 32) ? 0xFFFFFFFFu : ((1u << (n_bytes - first_bit)) - 1u);
+      out_bits[gw] = v;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- decoding --
+
+constexpr int kScanBlock = 1024;
+
+__global__ void k_dec_len(const int32_t* ids, int64_t n_ids, const int64_t* voffs, int64_t n_vocab, int64_t* lens,
+                          DevSmall* small) {
+  bool bad = false;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_ids; i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t id = ids[i];
+    int64_t L = 0;
+    if (id >= 0 && id < n_vocab) L = voffs[id + 1] - voffs[id];
+    else bad = true;
+    lens[i] = L;
+  }
+  if (bad) atomicOr(&small->status, kStBadInput);
+}
+
+// In-place exclusive scan of x[0..n) in blocks of kScanBlock; block sums to sums.
+__global__ void k_scan_blocks(int64_t* x, int64_t n, int64_t* sums) {
+  __shared__ int64_t s[kScanBlock];
+  const int64_t base = (int64_t)blockIdx.x * kScanBlock;
+  for (int i = threadIdx.x; i < kScanBlock; i += blockDim.x) s[i] = (base + i < n) ? x[base + i] : 0;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int64_t acc = 0;
+    for (int i = 0; i < kScanBlock; ++i) {
+      int64_t v = s[i];
+      s[i] = acc;
+      acc += v;
+    }
+    sums[blockIdx.x] = acc;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kScanBlock; i += blockDim.x)
+    if (base + i < n) x[base + i] = s[i];
+}
+
+__global__ void k_scan_sums(int64_t* sums, int64_t n_blocks, DevSmall* small) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    int64_t acc = 0;
+    for (int64_t b = 0; b < n_blocks; ++b) {
+      int64_t v = sums[b];
+      sums[b] = acc;
+      acc += v;
+    }
+    small->total = acc;
+  }
+}
+
+__global__ void k_dec_gather(const int32_t* ids, int64_t n_ids, int64_t* offs, const int64_t* sums,
+                             const uint8_t* vbytes, const int64_t* voffs, int64_t n_vocab, uint8_t* out,
+                             int64_t cap, DevSmall* small) {
+  bool over = false;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_ids; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t o = offs[i] + sums[i / kScanBlock];
+    const int32_t id = ids[i];
+    if (id < 0 || id >= n_vocab) continue;
+    const int64_t b0 = voffs[id], L = voffs[id + 1] - b0;
+    for (int64_t q = 0; q < L; ++q) {
+      if (o + q < cap) out[o + q] = vbytes[b0 + q];
+      else over = true;
+    }
+  }
+  if (over) atomicOr(&small->status, kStCapacity);
+}
+
+__global__ void k_dec_docs(const int64_t* id_offsets, int64_t n_docs, int64_t n_ids, const int64_t* offs,
+                           const int64_t* sums, int64_t* out_offsets, DevSmall* small) {
+  bool bad = false;
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k <= n_docs; k += (int64_t)gridDim.x * blockDim.x) {
+    int64_t i = id_offsets[k];
+    if (i < 0 || i > n_ids || (k < n_docs && id_offsets[k + 1] < i)) bad = true;
+    if (i < 0) i = 0;
+    if (i > n_ids) i = n_ids;
+    int64_t first = id_offsets[0];
+    if (first < 0) first = 0;
+    if (first > n_ids) first = n_ids;
+    const int64_t at = (i < n_ids) ? offs[i] + sums[i / kScanBlock] : small->total;
+    const int64_t base = (first < n_ids) ? offs[first] + sums[first / kScanBlock] : small->total;
+    out_offsets[k] = at - base;
+  }
+  if (bad) atomicOr(&small->status, kStBadInput);
+}
+
+// ------------------------------------------------------------------- host --
+
+thread_local std::string g_err;
+
+int fail(int code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(BPE_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define CK(call)                                   \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    cudaGetDevice(&prev);
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (prev >= 0 && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+struct bpe_handle {
+  int device = 0;
+  int64_t n_merges = 0, n_vocab = 0;
+  uint64_t* d_ht = nullptr;
+  uint32_t hmask = 0;
+  int32_t* d_mrows = nullptr;
+  int32_t* d_byte_id = nullptr;
+  uint8_t* d_vbytes = nullptr;
+  int64_t* d_voffs = nullptr;
+  DevSmall* d_small = nullptr;
+  DevSmall* h_small = nullptr;  // pinned
+  void* d_ws = nullptr;
+  size_t ws_bytes = 0;
+  bool smem_set = false;
+  cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
+};
+
+namespace {
+
+int ensure_ws(bpe_handle* h, size_t need) {
+  if (need <= h->ws_bytes) return BPE_OK;
+  size_t sz = need + need / 4 + 4096;
+  if (h->d_ws) CK(cudaFree(h->d_ws));
+  h->d_ws = nullptr;
+  h->ws_bytes = 0;
+  CK(cudaMalloc(&h->d_ws, sz));
+  h->ws_bytes = sz;
+  return BPE_OK;
+}
+
+int read_status(bpe_handle* h, cudaStream_t st, DevSmall* out) {
+  CK(cudaMemcpyAsync(h->h_small, h->d_small, sizeof(DevSmall), cudaMemcpyDeviceToHost, st));
+  CK(cudaStreamSynchronize(st));
+  *out = *h->h_small;
+  if (out->status) CK(cudaMemsetAsync(&h->d_small->status, 0, sizeof(uint32_t), st));
+  return BPE_OK;
+}
+
+int status_code(uint32_t s) {
+  if (s & kStBadInput) return fail(BPE_ERR_BAD_INPUT, "offsets not monotone or outside the buffer, or an id out of range");
+  if (s & kStTimeout) return fail(BPE_ERR_TIMEOUT, "a device-side wait gave up");
+  if (s & kStCapacity) return fail(BPE_ERR_CAPACITY, "output capacity exceeded");
+  if (s & kStInternal) return fail(BPE_ERR_INTERNAL, "device-side consistency check failed");
+  return BPE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bpe_last_error(void) { return g_err.c_str(); }
+
+int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_bytes, const int64_t* vocab_offsets,
+              int64_t n_vocab, int device, bpe_handle** out) {
+  if (!out || !vocab_offsets || (n_merges > 0 && !merges) || n_merges < 0 || n_vocab < 256)
+    return fail(BPE_ERR_INVALID_ARG, "bpe_build: bad arguments");
+  *out = nullptr;
+  if (n_vocab > (1 << 20)) return fail(BPE_ERR_BAD_TABLE, "n_vocab above 2^20");
+  if (n_merges >= (1 << 20) - 1) return fail(BPE_ERR_BAD_TABLE, "n_merges above 2^20 - 2");
+  if (vocab_offsets[0] != 0) return fail(BPE_ERR_BAD_TABLE, "vocab_offsets[0] != 0");
+  for (int64_t k = 0; k < n_vocab; ++k)
+    if (vocab_offsets[k + 1] < vocab_offsets[k]) return fail(BPE_ERR_BAD_TABLE, "vocab_offsets not monotone");
+  if (vocab_offsets[n_vocab] > 0 && !vocab_bytes) return fail(BPE_ERR_INVALID_ARG, "vocab_bytes is null");
+  auto tok = [&](int64_t id) {
+    return std::string((const char*)vocab_bytes + vocab_offsets[id], (size_t)(vocab_offsets[id + 1] - vocab_offsets[id]));
+  };
+  std::vector<int32_t> byte_id(256, -1);
+  {
+    std::unordered_set<std::string> seen;
+    for (int64_t id = 0; id < n_vocab; ++id) {
+      int64_t L = vocab_offsets[id + 1] - vocab_offsets[id];
+      if (L == 0) continue;
+      std::string s = tok(id);
+      if (!seen.insert(s).second) return fail(BPE_ERR_BAD_TABLE, "two tokens have the same bytes");
+      if (L == 1) byte_id[(uint8_t)s[0]] = (int32_t)id;
+    }
+    for (int b = 0; b < 256; ++b)
+      if (byte_id[b] < 0) return fail(BPE_ERR_BAD_TABLE, "a single byte is missing from the vocabulary");
+  }
+  uint64_t nb = 1;
+  while (nb * 2 < (uint64_t)n_merges) nb <<= 1;  // at most two entries per 4-slot bucket on average
+  std::vector<uint64_t> ht(nb * 4, kEmpty);
+  {
+    std::unordered_set<uint64_t> pairs;
+    for (int64_t r = 0; r < n_merges; ++r) {
+      int32_t a = merges[3 * r], b = merges[3 * r + 1], nw = merges[3 * r + 2];
+      if (a < 0 || b < 0 || nw < 0 || a >= n_vocab || b >= n_vocab || nw >= n_vocab)
+        return fail(BPE_ERR_BAD_TABLE, "merge id out of range");
+      if (vocab_offsets[a + 1] == vocab_offsets[a] || vocab_offsets[b + 1] == vocab_offsets[b])
+        return fail(BPE_ERR_BAD_TABLE, "merge uses an unused id");
+      if (tok(nw) != tok(a) + tok(b)) return fail(BPE_ERR_BAD_TABLE, "bytes(new) != bytes(left) + bytes(right)");
+      uint64_t key = ((uint64_t)(uint32_t)a << 20) | (uint32_t)b;
+      if (!pairs.insert(key).second) return fail(BPE_ERR_BAD_TABLE, "a pair appears twice");
+      uint64_t bucket = pair_hash((uint32_t)a, (uint32_t)b) & (nb - 1);
+      for (;;) {
+        int slot = -1;
+        for (int q = 0; q < 4; ++q)
+          if (ht[bucket * 4 + q] == kEmpty) { slot = q; break; }
+        if (slot >= 0) {
+          ht[bucket * 4 + slot] = (key << 20) | (uint64_t)r;
+          break;
+        }
+        bucket = (bucket + 1) & (nb - 1);
+      }
+    }
+  }
+  int n_dev = 0;
+  CK(cudaGetDeviceCount(&n_dev));
+  if (device < 0 || device >= n_dev) return fail(BPE_ERR_INVALID_ARG, "bad device ordinal");
+  DeviceGuard g(device);
+  bpe_handle* h = new bpe_handle();
+  h->device = device;
+  h->n_merges = n_merges;
+  h->n_vocab = n_vocab;
+  h->hmask = (uint32_t)(nb - 1);
+  auto cleanup = [&](int code) {
+    bpe_destroy(h);
+    return code;
+  };
+  int rc;
+#define CKB(call)                                                   \
+  do {                                                              \
+    cudaError_t e_ = (call);                                        \
+    if (e_ != cudaSuccess) return cleanup(cuda_fail(e_, #call));    \
+  } while (0)
+  CKB(cudaMalloc(&h->d_ht, ht.size() * sizeof(uint64_t)));
+  CKB(cudaMemcpy(h->d_ht, ht.data(), ht.size() * sizeof(uint64_t), cudaMemcpyHostToDevice));
+  CKB(cudaMalloc(&h->d_mrows, (size_t)std::max<int64_t>(1, n_merges) * 3 * sizeof(int32_t)));
+  if (n_merges) CKB(cudaMemcpy(h->d_mrows, merges, (size_t)n_merges * 3 * sizeof(int32_t), cudaMemcpyHostToDevice));
+  CKB(cudaMalloc(&h->d_byte_id, 256 * sizeof(int32_t)));
+  CKB(cudaMemcpy(h->d_byte_id, byte_id.data(), 256 * sizeof(int32_t), cudaMemcpyHostToDevice));
+  const int64_t nvb = vocab_offsets[n_vocab];
+  CKB(cudaMalloc(&h->d_vbytes, (size_t)std::max<int64_t>(1, nvb)));
+  if (nvb) CKB(cudaMemcpy(h->d_vbytes, vocab_bytes, (size_t)nvb, cudaMemcpyHostToDevice));
+  CKB(cudaMalloc(&h->d_voffs, (size_t)(n_vocab + 1) * sizeof(int64_t)));
+  CKB(cudaMemcpy(h->d_voffs, vocab_offsets, (size_t)(n_vocab + 1) * sizeof(int64_t), cudaMemcpyHostToDevice));
+  CKB(cudaMalloc(&h->d_small, sizeof(DevSmall)));
+  CKB(cudaMemset(h->d_small, 0, sizeof(DevSmall)));
+  CKB(cudaMallocHost(&h->h_small, sizeof(DevSmall)));
+#undef CKB
+  (void)rc;
+  *out = h;
+  return BPE_OK;
+}
+
+int bpe_destroy(bpe_handle* h) {
+  if (!h) return fail(BPE_ERR_INVALID_ARG, "null handle");
+  DeviceGuard g(h->device);
+  cudaDeviceSynchronize();
+  cudaFree(h->d_ht);
+  cudaFree(h->d_mrows);
+  cudaFree(h->d_byte_id);
+  cudaFree(h->d_vbytes);
+  cudaFree(h->d_voffs);
+  cudaFree(h->d_small);
+  cudaFree(h->d_ws);
+  if (h->h_small) cudaFreeHost(h->h_small);
+  delete h;
+  return BPE_OK;
+}
+
+int bpe_set_timing_events(bpe_handle* h, void* ev_start, void* ev_stop) {
+  if (!h) return fail(BPE_ERR_INVALID_ARG, "null handle");
+  h->ev_start = (cudaEvent_t)ev_start;
+  h->ev_stop = (cudaEvent_t)ev_stop;
+  return BPE_OK;
+}
+
+int bpe_table_info(const bpe_handle* h, int64_t* n_merges, int64_t* n_vocab) {
+  if (!h) return fail(BPE_ERR_INVALID_ARG, "null handle");
+  if (n_merges) *n_merges = h->n_merges;
+  if (n_vocab) *n_vocab = h->n_vocab;
+  return BPE_OK;
+}
+
+int bpe_sync_status(bpe_handle* h, bpe_stream_t stream) {
+  if (!h) return fail(BPE_ERR_INVALID_ARG, "null handle");
+  DeviceGuard g(h->device);
+  DevSmall s;
+  int rc = read_status(h, (cudaStream_t)stream, &s);
+  if (rc) return rc;
+  return status_code(s.status);
+}
+
+int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
+                     int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets,
+                     int64_t* h_total_tokens, bpe_stream_t stream) {
+  if (!h || !d_doc_offsets || !d_out_offsets || n_bytes < 0 || n_docs < 0 || (n_bytes > 0 && (!d_bytes || !d_out_ids)))
+    return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch: bad arguments");
+  if (out_capacity < n_bytes) {
+    if (h_total_tokens) *h_total_tokens = n_bytes;
+    return fail(BPE_ERR_CAPACITY, "out_capacity must be at least n_bytes");
+  }
+  DeviceGuard g(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t n_chunks = n_bytes / kChunk + 1;
+  const size_t need = (size_t)n_chunks * (sizeof(uint64_t) + sizeof(int64_t));
+  int rc = ensure_ws(h, need);
+  if (rc) return rc;
+  uint64_t* desc = (uint64_t*)h->d_ws;
+  int64_t* first_doc = (int64_t*)(desc + n_chunks);
+  if (!h->smem_set) {
+    CK(cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
+    CK(cudaFuncSetAttribute(k_pretokenize, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
+    h->smem_set = true;
+  }
+  int prep_blocks = (int)std::min<int64_t>(4096, std::max<int64_t>(n_chunks, n_docs + 1) / 256 + 1);
+  k_prep<<<prep_blocks, 256, 0, st>>>(d_doc_offsets, n_docs, n_bytes, n_chunks, desc, first_doc, h->d_small);
+  CK(cudaGetLastError());
+  EncodeArgs a;
+  a.bytes = d_bytes;
+  a.n_bytes = n_bytes;
+  a.doc_offsets = d_doc_offsets;
+  a.n_docs = n_docs;
+  a.out_ids = d_out_ids;
+  a.out_offsets = d_out_offsets;
+  a.T = Tables{h->d_ht, h->hmask, h->d_mrows, h->d_byte_id};
+  a.desc = desc;
+  a.first_doc = first_doc;
+  a.small = h->d_small;
+  a.n_chunks = n_chunks;
+  if (h->ev_start) CK(cudaEventRecord(h->ev_start, st));
+  k_encode<<<(unsigned)n_chunks, kThreads, sizeof(Smem), st>>>(a);
+  CK(cudaGetLastError());
+  if (h->ev_stop) CK(cudaEventRecord(h->ev_stop, st));
+  if (h_total_tokens) {
+    DevSmall s;
+    rc = read_status(h, st, &s);
+    if (rc) return rc;
+    *h_total_tokens = s.total;
+    return status_code(s.status);
+  }
+  return BPE_OK;
+}
+
+int bpe_pretokenize_batch(const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets, int64_t n_docs,
+                          uint32_t* d_start_bits, bpe_stream_t stream) {
+  if (!d_doc_offsets || n_bytes < 0 || n_docs < 0 || (n_bytes > 0 && (!d_bytes || !d_start_bits)))
+    return fail(BPE_ERR_INVALID_ARG, "bpe_pretokenize_batch: bad arguments");
+  if (n_bytes == 0) return BPE_OK;
+  static thread_local int smem_set_dev = -1;
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  if (smem_set_dev != dev) {
+    CK(cudaFuncSetAttribute(k_pretokenize, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
+    smem_set_dev = dev;
+  }
+  const int64_t n_chunks = (n_bytes + kChunk - 1) / kChunk;
+  k_pretokenize<<<(unsigned)n_chunks, kThreads, sizeof(Smem), (cudaStream_t)stream>>>(d_bytes, n_bytes, d_doc_offsets,
+                                                                                      n_docs, d_start_bits);
+  CK(cudaGetLastError());
+  return BPE_OK;
+}
+
+int bpe_decode_batch(bpe_handle* h, const int32_t* d_ids, int64_t n_ids, const int64_t* d_id_offsets, int64_t n_docs,
+                     uint8_t* d_out_bytes, int64_t out_capacity, int64_t* d_out_byte_offsets, int64_t* h_total_bytes,
+                     bpe_stream_t stream) {
+  if (!h || !d_id_offsets || !d_out_byte_offsets || n_ids < 0 || n_docs < 0 || out_capacity < 0 ||
+      (n_ids > 0 && !d_ids) || (out_capacity > 0 && !d_out_bytes))
+    return fail(BPE_ERR_INVALID_ARG, "bpe_decode_batch: bad arguments");
+  DeviceGuard g(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t n_blocks = n_ids / kScanBlock + 1;
+  int rc = ensure_ws(h, (size_t)(n_ids + 1 + n_blocks) * sizeof(int64_t));
+  if (rc) return rc;
+  int64_t* offs = (int64_t*)h->d_ws;
+  int64_t* sums = offs + n_ids + 1;
+  const int grid = (int)std::min<int64_t>(8192, n_ids / 256 + 1);
+  k_dec_len<<<grid, 256, 0, st>>>(d_ids, n_ids, h->d_voffs, h->n_vocab, offs, h->d_small);
+  k_scan_blocks<<<(unsigned)n_blocks, 256, 0, st>>>(offs, n_ids, sums);
+  k_scan_sums<<<1, 32, 0, st>>>(sums, n_blocks, h->d_small);
+  k_dec_gather<<<grid, 256, 0, st>>>(d_ids, n_ids, offs, sums, h->d_vbytes, h->d_voffs, h->n_vocab, d_out_bytes,
+                                     out_capacity, h->d_small);
+  const int dgrid = (int)std::min<int64_t>(8192, n_docs / 256 + 1);
+  k_dec_docs<<<dgrid, 256, 0, st>>>(d_id_offsets, n_docs, n_ids, offs, sums, d_out_byte_offsets, h->d_small);
+  CK(cudaGetLastError());
+  if (h_total_bytes) {
+    DevSmall s;
+    rc = read_status(h, st, &s);
+    if (rc) return rc;
+    *h_total_bytes = s.total;
+    if (s.status) return status_code(s.status);
+    if (s.total > out_capacity) return fail(BPE_ERR_CAPACITY, "decoded bytes exceed out_capacity");
+  }
+  return BPE_OK;
+}
+
+}  // extern "C"

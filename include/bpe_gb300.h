@@ -1,0 +1,165 @@
+/*
+ * bpe_gb300.h — C ABI of the GB300 batched byte-level BPE encoder.
+ *
+ * The method (glitch4techs, "Tokenization LLM: building an inference engine
+ * in C++", sections "Technical analysis" to "Vocabulary lookup"): split each
+ * document into pre-tokens with a GPT-2-style rule, map every UTF-8 byte to
+ * its byte-level symbol, repeatedly merge the adjacent pair with the lowest
+ * merge rank until no ranked pair remains, and look the resulting symbols up
+ * in the vocabulary. A merge step replaces its pair left to right without
+ * overlap (tokenwerk, "Tokenisierung", section "Byte Pair Encoding
+ * schrittweise") and never crosses a pre-token (dothoosh, "Hugging Face
+ * Tokenizers v1 encoding up to 30x", section on how v1 works).
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* are device pointers on the handle's device; h_* are
+ *     host pointers. The caller owns every buffer passed in.
+ *   - Calls are ordered on the given stream and return once the work is
+ *     queued, except where an h_* output is requested: then the call waits
+ *     for the stream and also reports errors the kernels detected.
+ *   - A handle serves one stream at a time: calls that share a handle must not
+ *     overlap on the GPU.
+ *   - Return value: BPE_OK, or a BPE_ERR_* code; bpe_last_error() gives a
+ *     message (thread-local, valid until the next call on the thread).
+ */
+#ifndef BPE_GB300_H_
+#define BPE_GB300_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BPE_OK 0
+#define BPE_ERR_INVALID_ARG 1 /* null pointer, negative size, unknown handle */
+#define BPE_ERR_CAPACITY 2    /* an output buffer is too small */
+#define BPE_ERR_CUDA 3        /* a CUDA runtime call failed */
+#define BPE_ERR_BAD_TABLE 4   /* bpe_build: the merge table or vocabulary is inconsistent */
+#define BPE_ERR_TIMEOUT 5     /* a device-side wait gave up (no forward progress) */
+#define BPE_ERR_INTERNAL 6    /* a device-side consistency check failed */
+#define BPE_ERR_BAD_INPUT 7   /* offsets not monotone or outside the buffer, or an id out of range */
+
+typedef struct bpe_handle bpe_handle;
+typedef struct CUstream_st* bpe_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+/*
+ * bpe_build — upload a tokenizer once ("Hugging Face Tokenizers v1", closing
+ * section on GPU batch encode: the vocabulary is uploaded once).
+ *
+ *   merges        host int32[n_merges][3], rows (left_id, right_id, new_id);
+ *                 the rank of a row is its index, lower rank merges first
+ *                 (glitch4techs, section "Byte Pair Encoding algorithm").
+ *   vocab_bytes   host uint8[], the bytes of every token back to back.
+ *   vocab_offsets host int64[n_vocab + 1]; token k is
+ *                 vocab_bytes[vocab_offsets[k] .. vocab_offsets[k + 1]).
+ *                 A token with no bytes is an unused id.
+ *   device        CUDA device ordinal that owns the tables.
+ *   out           receives the new handle.
+ *
+ * Checks (BPE_ERR_BAD_TABLE): every one of the 256 single bytes is a token
+ * (byte-level base, "Tokenisierung", section "Bytes als robustes Fundament");
+ * no two tokens have the same bytes; ids are in [0, n_vocab) and n_vocab <=
+ * 2^20; no pair appears twice; bytes(new_id) == bytes(left_id) ||
+ * bytes(right_id), so the merged symbol's vocabulary entry is new_id.
+ * The handle owns device copies of the tables and a small device workspace.
+ */
+int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_bytes,
+              const int64_t* vocab_offsets, int64_t n_vocab, int device, bpe_handle** out);
+
+/*
+ * bpe_encode_batch — encode a batch of documents in one call.
+ *
+ *   d_bytes        device uint8[n_bytes], the UTF-8 input.
+ *   n_bytes        size of d_bytes.
+ *   d_doc_offsets  device int64[n_docs + 1]; document k is
+ *                  d_bytes[d_doc_offsets[k] .. d_doc_offsets[k + 1]); must be
+ *                  non-decreasing within [0, n_bytes]. Empty documents are
+ *                  allowed. Bytes outside [d_doc_offsets[0],
+ *                  d_doc_offsets[n_docs]) are ignored.
+ *   d_out_ids      device int32[out_capacity]; receives the token ids of all
+ *                  documents back to back. The call also uses it as scratch
+ *                  for long pre-tokens, so out_capacity must be >= n_bytes
+ *                  (tokens never outnumber bytes); otherwise BPE_ERR_CAPACITY
+ *                  and *h_total_tokens = n_bytes when given.
+ *   d_out_offsets  device int64[n_docs + 1]; document k's ids are
+ *                  d_out_ids[d_out_offsets[k] .. d_out_offsets[k + 1]), with
+ *                  d_out_offsets[0] = 0.
+ *   h_total_tokens host int64*, may be NULL. When given, the call waits for
+ *                  the stream, stores the total token count and returns any
+ *                  error found on the device (BPE_ERR_BAD_INPUT, _TIMEOUT,
+ *                  _INTERNAL). When NULL such errors are kept and returned by
+ *                  the next bpe_sync_status() on the handle.
+ *   stream         the CUDA stream to run on.
+ *
+ * May grow the handle's device workspace (cudaMalloc) the first time a larger
+ * batch is seen.
+ */
+int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
+                     int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets,
+                     int64_t* h_total_tokens, bpe_stream_t stream);
+
+/*
+ * bpe_pretokenize_batch — the pre-tokenizer alone: marks where pre-tokens
+ * start (glitch4techs, section "Technical analysis": the split of "Hello
+ * world!" into "Hello", " world", "!").
+ *
+ *   d_bytes, n_bytes, d_doc_offsets, n_docs   as for bpe_encode_batch.
+ *   d_start_bits   device uint32[(n_bytes + 31) / 32]; bit (i % 32) of word
+ *                  i / 32 is set iff a pre-token starts at byte i. Every
+ *                  non-empty document starts a pre-token; bytes outside the
+ *                  documents have no bit set.
+ * Needs no handle: the split depends on the text only.
+ */
+int bpe_pretokenize_batch(const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets, int64_t n_docs,
+                          uint32_t* d_start_bits, bpe_stream_t stream);
+
+/*
+ * bpe_decode_batch — token ids back to bytes: the concatenation of every
+ * token's bytes ("Tokenisierung", section "Prüfe zuerst den Roundtrip":
+ * decode(encode(text)) == text; "Hugging Face Tokenizers v1", section on the
+ * road to 1.0: bytes written straight into caller buffers). Byte-exact, no
+ * UTF-8 repair.
+ *
+ *   d_ids             device int32[n_ids].
+ *   d_id_offsets      device int64[n_docs + 1], non-decreasing in [0, n_ids].
+ *   d_out_bytes       device uint8[out_capacity].
+ *   d_out_byte_offsets device int64[n_docs + 1]; document k's bytes are
+ *                     d_out_bytes[d_out_byte_offsets[k] .. [k + 1]).
+ *   h_total_bytes     host int64*, may be NULL; when given, the call waits and
+ *                     stores the byte count; if it exceeds out_capacity the
+ *                     call returns BPE_ERR_CAPACITY (nothing past the capacity
+ *                     is written).
+ * Ids outside [0, n_vocab) decode to nothing and raise BPE_ERR_BAD_INPUT.
+ */
+int bpe_decode_batch(bpe_handle* h, const int32_t* d_ids, int64_t n_ids, const int64_t* d_id_offsets,
+                     int64_t n_docs, uint8_t* d_out_bytes, int64_t out_capacity, int64_t* d_out_byte_offsets,
+                     int64_t* h_total_bytes, bpe_stream_t stream);
+
+/*
+ * bpe_set_timing_events — measurement hook. When ev_start / ev_stop (two
+ * cudaEvent_t created by the caller on the handle's device) are non-NULL, the
+ * next bpe_encode_batch calls record ev_start right before the main encode
+ * kernel and ev_stop right after it, on the call's stream, so the caller can
+ * time that kernel alone. NULL, NULL switches it off.
+ */
+int bpe_set_timing_events(bpe_handle* h, void* ev_start, void* ev_stop);
+
+/* Waits for the stream and returns (then clears) errors the kernels of
+ * earlier calls on this handle recorded. */
+int bpe_sync_status(bpe_handle* h, bpe_stream_t stream);
+
+/* Number of merges and vocabulary size of a handle (host values). */
+int bpe_table_info(const bpe_handle* h, int64_t* n_merges, int64_t* n_vocab);
+
+/* Frees the handle's device memory. Waits for its device first. */
+int bpe_destroy(bpe_handle* h);
+
+/* Message for the last failing call on this thread. */
+const char* bpe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BPE_GB300_H_ */

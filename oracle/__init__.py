@@ -48,6 +48,8 @@ def _load():
             lib.orc_free.argtypes = [p]
             lib.orc_pretokenize.restype = i64
             lib.orc_pretokenize.argtypes = [p, i64, p, i64]
+            lib.orc_pretokenize_batch.restype = None
+            lib.orc_pretokenize_batch.argtypes = [p, p, i64, p]
             lib.orc_units.restype = i64
             lib.orc_units.argtypes = [p, i64, p, i64]
             lib.orc_class.restype = i32
@@ -84,6 +86,17 @@ def pretokenize(text) -> list[int]:
     out = np.empty(cap, dtype=np.int64)
     n = lib.orc_pretokenize(_p(b), b.size, out.ctypes.data, cap)
     return out[:n].tolist()
+
+
+def pretokenize_batch(data, offsets) -> np.ndarray:
+    """Start bits (uint32[(N + 31) // 32]) of every piece of every document."""
+    lib = _load()
+    b = _buf(data)
+    offsets = np.ascontiguousarray(offsets, dtype=np.int64)
+    bits = np.zeros(max(1, (b.size + 31) // 32), dtype=np.uint32)
+    d = b if b.size else np.zeros(1, np.uint8)
+    lib.orc_pretokenize_batch(d.ctypes.data, offsets.ctypes.data, len(offsets) - 1, bits.ctypes.data)
+    return bits
 
 
 def pieces(text) -> list[bytes]:

@@ -310,6 +310,19 @@ int64_t orc_pretokenize(const uint8_t* s, int64_t n, int64_t* starts, int64_t ca
   return (int64_t)v.size();
 }
 
+// Start bits of a batch: bit i of bits (uint32 words) is set iff a piece
+// starts at byte i; each document [doc_offsets[k], doc_offsets[k + 1]) is
+// split on its own.
+void orc_pretokenize_batch(const uint8_t* bytes, const int64_t* doc_offsets, int64_t n_docs, uint32_t* bits) {
+  for (int64_t k = 0; k < n_docs; ++k) {
+    int64_t a = doc_offsets[k], n = doc_offsets[k + 1] - a;
+    for (int64_t st : pretokenize(bytes + a, n)) {
+      int64_t i = a + st;
+      bits[i >> 5] |= 1u << (i & 31);
+    }
+  }
+}
+
 // Decoded units of a text: writes (byte offset, codepoint or -1, class) rows.
 int64_t orc_units(const uint8_t* s, int64_t n, int64_t* rows, int64_t cap) {
   Units u = units_of(s, n);
