@@ -24,8 +24,8 @@
 //     memory with a flat array plus a cached rank per adjacent pair (the
 //     "Hugging Face Tokenizers v1" merge-loop rewrite: flat arrays, integer
 //     rank compare, no allocation). Longer ones are merged by the whole CTA
-//     in place in the caller's output buffer (its byte range there is free
-//     until this chunk publishes its token count).
+//     in a device scratch pool indexed by input byte position, so every long
+//     pre-token owns the pool range of its own bytes.
 //   * Output positions: a single-pass chained scan (decoupled look-back) over
 //     chunk token counts; chunks take tickets in launch order so every
 //     predecessor is already running. Waits are bounded by the global timer.
@@ -606,7 +606,9 @@ struct EncodeArgs {
   const int64_t* doc_offsets;
   int64_t n_docs;
   int32_t* out_ids;
+  int64_t out_capacity;
   int64_t* out_offsets;
+  int32_t* pool;  // long pre-token scratch, one int32 per input byte
   Tables T;
   uint64_t* desc;
   const int64_t* first_doc;
@@ -741,7 +743,7 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
       if (tid == 0) atomicOr(&a.small->status, kStInternal);
       if (tid == 0) S.span_cnt[j] = 0;
     } else {
-      uint32_t cnt = merge_long(a.bytes, s, (uint32_t)n, a.out_ids + s, a.T, S.byte_id, L);
+      uint32_t cnt = merge_long(a.bytes, s, (uint32_t)n, a.pool + s, a.T, S.byte_id, L);
       if (tid == 0) S.span_cnt[j] = cnt;
     }
     __syncthreads();
@@ -798,24 +800,17 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
   __syncthreads();
   const int64_t P = S.prefix;
 
-  // Long pre-tokens: move from their scratch range to their place, in order
-  // (a move lands at or below the next long pre-token's range).
+  // Ids past the caller's capacity are not written; the call reports it.
+  if (tid == 0 && P + (int64_t)agg > a.out_capacity) atomicOr(&a.small->status, kStCapacity);
+
+  // Long pre-tokens: copy from their scratch range of the pool.
   for (uint32_t x = 0; x < n_long; ++x) {
     const uint32_t j = S.long_list[x];
     const int64_t s = c0 + S.span_start[j];
     const int64_t dst = P + S.span_cnt[j];
     const uint32_t cnt = S.span_cnt[j + 1] - S.span_cnt[j];
-    if (dst != s) {
-      for (uint32_t b0 = 0; b0 < cnt; b0 += kThreads) {
-        uint32_t q = b0 + tid;
-        int32_t v = 0;
-        if (q < cnt) v = a.out_ids[s + q];
-        __syncthreads();
-        if (q < cnt) a.out_ids[dst + q] = v;
-        __syncthreads();
-      }
-    }
-    __syncthreads();
+    for (uint32_t q = tid; q < cnt; q += kThreads)
+      if (dst + q < a.out_capacity) a.out_ids[dst + q] = a.pool[s + q];
   }
 
   // Short pre-tokens: ids from shared memory.
@@ -825,8 +820,9 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
     for (uint32_t x = 0; x < n_long; ++x) is_long |= (S.long_list[x] == j);
     if (is_long) continue;
     const uint32_t o = S.span_cnt[j], cnt = S.span_cnt[j + 1] - o;
-    int32_t* dst = a.out_ids + P + o;
-    for (uint32_t q = 0; q < cnt; ++q) dst[q] = (int32_t)S.sym[st + q];
+    const int64_t dst = P + o;
+    for (uint32_t q = 0; q < cnt; ++q)
+      if (dst + q < a.out_capacity) a.out_ids[dst + q] = (int32_t)S.sym[st + q];
   }
 
   // Offsets of the documents that start in this chunk.
@@ -1185,20 +1181,19 @@ int bpe_sync_status(bpe_handle* h, bpe_stream_t stream) {
 int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
                      int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets,
                      int64_t* h_total_tokens, bpe_stream_t stream) {
-  if (!h || !d_doc_offsets || !d_out_offsets || n_bytes < 0 || n_docs < 0 || (n_bytes > 0 && (!d_bytes || !d_out_ids)))
+  if (!h || !d_doc_offsets || !d_out_offsets || n_bytes < 0 || n_docs < 0 || (n_bytes > 0 && !d_bytes))
     return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch: bad arguments");
-  if (out_capacity < n_bytes) {
-    if (h_total_tokens) *h_total_tokens = n_bytes;
-    return fail(BPE_ERR_CAPACITY, "out_capacity must be at least n_bytes");
-  }
+  if (out_capacity < 0 || (out_capacity > 0 && !d_out_ids))
+    return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch: bad output buffer");
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
   const int64_t n_chunks = n_bytes / kChunk + 1;
-  const size_t need = (size_t)n_chunks * (sizeof(uint64_t) + sizeof(int64_t));
+  const size_t need = (size_t)n_chunks * (sizeof(uint64_t) + sizeof(int64_t)) + (size_t)(n_bytes + 4) * sizeof(int32_t);
   int rc = ensure_ws(h, need);
   if (rc) return rc;
   uint64_t* desc = (uint64_t*)h->d_ws;
   int64_t* first_doc = (int64_t*)(desc + n_chunks);
+  int32_t* pool = (int32_t*)(first_doc + n_chunks);
   if (!h->smem_set) {
     CK(cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
     CK(cudaFuncSetAttribute(k_pretokenize, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
@@ -1213,6 +1208,8 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
   a.doc_offsets = d_doc_offsets;
   a.n_docs = n_docs;
   a.out_ids = d_out_ids;
+  a.out_capacity = out_capacity;
+  a.pool = pool;
   a.out_offsets = d_out_offsets;
   a.T = Tables{h->d_ht, h->hmask, h->d_mrows, h->d_byte_id};
   a.desc = desc;

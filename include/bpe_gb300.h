@@ -78,10 +78,11 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
  *                  allowed. Bytes outside [d_doc_offsets[0],
  *                  d_doc_offsets[n_docs]) are ignored.
  *   d_out_ids      device int32[out_capacity]; receives the token ids of all
- *                  documents back to back. The call also uses it as scratch
- *                  for long pre-tokens, so out_capacity must be >= n_bytes
- *                  (tokens never outnumber bytes); otherwise BPE_ERR_CAPACITY
- *                  and *h_total_tokens = n_bytes when given.
+ *                  documents back to back. Tokens never outnumber bytes, so
+ *                  out_capacity >= n_bytes always suffices. Ids past
+ *                  out_capacity are not written and the call reports
+ *                  BPE_ERR_CAPACITY (through h_total_tokens, which then holds
+ *                  the count needed, or bpe_sync_status()).
  *   d_out_offsets  device int64[n_docs + 1]; document k's ids are
  *                  d_out_ids[d_out_offsets[k] .. d_out_offsets[k + 1]), with
  *                  d_out_offsets[0] = 0.
@@ -92,8 +93,10 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
  *                  the next bpe_sync_status() on the handle.
  *   stream         the CUDA stream to run on.
  *
- * May grow the handle's device workspace (cudaMalloc) the first time a larger
- * batch is seen.
+ * Workspace: the handle keeps 4 bytes per input byte (scratch for pre-tokens
+ * too long for shared memory, each using the range of its own bytes) plus 16
+ * bytes per 4 KiB chunk; it grows (cudaMalloc) the first time a larger batch
+ * is seen.
  */
 int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
                      int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets,

@@ -52,6 +52,12 @@ def assert_same_encoding(got, want, data, offsets, label=""):
         b = w_ids[w_off[k]:w_off[k + 1]]
         if a is None or not np.array_equal(a, b):
             doc = bytes(data[offsets[k]:offsets[k + 1]])
+            if a is not None:
+                n = min(len(a), len(b))
+                diff = np.nonzero(a[:n] != b[:n])[0]
+                i = int(diff[0]) if len(diff) else n
+                a, b = a[max(0, i - 5):i + 30], b[max(0, i - 5):i + 30]
+                label = f"{label} (first difference at token {i}; showing from {max(0, i - 5)})"
             raise AssertionError(f"{label}: document {k} ({len(doc)} bytes, starts {doc[:60]!r}) differs:\n"
                                  f"gpu    {None if a is None else a[:40].tolist()}\noracle {b[:40].tolist()}\n"
                                  f"offsets gpu {g_off[k]}..{g_off[k + 1]} oracle {w_off[k]}..{w_off[k + 1]}")

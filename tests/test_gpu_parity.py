@@ -237,11 +237,13 @@ def test_error_paths(bpe, tiny):
     ids = torch.zeros(16, dtype=torch.int32, device="cuda")
     out = torch.zeros(3, dtype=torch.int64, device="cuda")
     s = torch.cuda.current_stream().cuda_stream
-    # capacity below n_bytes
+    # capacity below the token count: nothing past it is written
+    ids[1:] = -5
     with pytest.raises(bpe.BpeError) as e:
         bpe.bpe_encode_batch(h, d.data_ptr(), data.size, torch.from_numpy(off).cuda().data_ptr(), 2, ids.data_ptr(),
-                             4, out.data_ptr(), True, s)
+                             1, out.data_ptr(), True, s)
     assert e.value.code == 2
+    assert (ids[1:] == -5).all()
     # offsets that go backwards are reported, not trusted
     bad = torch.tensor([0, 8, 3], dtype=torch.int64, device="cuda")
     with pytest.raises(bpe.BpeError) as e:
