@@ -129,8 +129,8 @@ def dist_env():
     return world, rank, local
 
 
-def load_workload(cfg: int, rank: int):
-    n = workloads.n_docs(cfg)
+def load_workload(cfg: int, rank: int, n_docs: int | None = None):
+    n = n_docs or workloads.n_docs(cfg)
     data, offsets = workloads.docs(cfg, rank * n, n)
     merges, vb, vo = workloads.table(cfg)
     return data, offsets, merges, vb, vo
@@ -216,7 +216,7 @@ def run_gpu(args, world, rank, local):
     __graft_entry__.build()
 
     cfg = args.cfg
-    data, offsets, merges, vb, vo = load_workload(cfg, rank)
+    data, offsets, merges, vb, vo = load_workload(cfg, rank, args.n_docs)
     n_bytes, n_docs = int(data.size), int(len(offsets) - 1)
     handle = bpe.bpe_build(merges, vb, vo, local)
     stream = torch.cuda.current_stream()
@@ -343,6 +343,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cfg", type=int, default=5, help="workload 1..5 (5 = serving batch)")
+    ap.add_argument("--n-docs", type=int, default=None, help="fewer documents (small profiling cases only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--reference-budget", type=float, default=60.0, help="total oracle seconds for --impl reference")

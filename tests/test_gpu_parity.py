@@ -110,7 +110,7 @@ def test_many_tiny_documents(bpe, tiny):
 
 
 def test_fuzz_documents(bpe, tiny):
-    from tests.test_oracle_pins import _fuzz_text
+    from tests.fuzz import fuzz_text as _fuzz_text
     h, o = tiny
     rng = random.Random(17)
     docs = [_fuzz_text(rng, rng.randint(0, 200)) for _ in range(3000)]
@@ -119,7 +119,7 @@ def test_fuzz_documents(bpe, tiny):
 
 
 def test_pretokenizer_bits_match(bpe):
-    from tests.test_oracle_pins import _fuzz_text
+    from tests.fuzz import fuzz_text as _fuzz_text
     rng = random.Random(23)
     docs = [_fuzz_text(rng, rng.randint(0, 300)) for _ in range(4000)]
     docs += [bytes(workloads.docs(c, 0, 2)[0][:200_000]) for c in (2, 3, 4)]

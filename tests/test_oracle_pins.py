@@ -111,19 +111,7 @@ def test_round_trip_page_list(cfg):
 
 regex = pytest.importorskip("regex")
 
-FUZZ_ALPHABET = ["a", "s", "t", "r", "e", "l", "v", "m", "d", "S", "1", "9", "!", ".", "'", " ", " ", " ",
-                 "\t", "\n", "\r", "é", "×", "中", "🌀", " ", " ", "\u0085", "́", "Ⅻ", "½"]
-INVALID = [b"\xff", b"\x80", b"\xc3", b"\xe4\xbd", b"\xed\xa0\x80", b"\xf0\x80\x80\x80", b"\xf4\x90\x80\x80"]
-
-
-def _fuzz_text(rng, n):
-    out = b""
-    for _ in range(n):
-        if rng.random() < 0.05:
-            out += rng.choice(INVALID)
-        else:
-            out += rng.choice(FUZZ_ALPHABET).encode()
-    return out
+from tests.fuzz import fuzz_text as _fuzz_text  # noqa: E402
 
 
 def test_pretokenize_vs_regex_fuzz():
