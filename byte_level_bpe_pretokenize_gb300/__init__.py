@@ -56,8 +56,8 @@ def build(force: bool = False, nvcc: str = "nvcc") -> str:
 _lock = threading.Lock()
 _lib = None
 
-EXPORTS = ["bpe_build", "bpe_encode_batch", "bpe_pretokenize_batch", "bpe_decode_batch", "bpe_set_timing_events",
-           "bpe_sync_status", "bpe_table_info", "bpe_destroy", "bpe_last_error"]
+EXPORTS = ["bpe_build", "bpe_encode_batch", "bpe_pretokenize_batch", "bpe_decode_batch", "bpe_set_word_cache",
+           "bpe_set_timing_events", "bpe_sync_status", "bpe_table_info", "bpe_destroy", "bpe_last_error"]
 
 
 def lib():
@@ -78,6 +78,8 @@ def lib():
             L.bpe_pretokenize_batch.argtypes = [p, i64, p, i64, p, p]
             L.bpe_decode_batch.restype = ctypes.c_int
             L.bpe_decode_batch.argtypes = [p, p, i64, p, i64, p, i64, p, p, p]
+            L.bpe_set_word_cache.restype = ctypes.c_int
+            L.bpe_set_word_cache.argtypes = [p, ctypes.c_int]
             L.bpe_set_timing_events.restype = ctypes.c_int
             L.bpe_set_timing_events.argtypes = [p, p, p]
             L.bpe_sync_status.restype = ctypes.c_int
@@ -130,6 +132,10 @@ def bpe_decode_batch(handle: int, d_ids: int, n_ids: int, d_id_offsets: int, n_d
     _check(lib().bpe_decode_batch(handle, d_ids, n_ids, d_id_offsets, n_docs, d_out_bytes, out_capacity,
                                   d_out_byte_offsets, ctypes.byref(total) if want_total else None, stream))
     return total.value if want_total else None
+
+
+def bpe_set_word_cache(handle: int, enable: bool) -> None:
+    _check(lib().bpe_set_word_cache(handle, 1 if enable else 0))
 
 
 def bpe_set_timing_events(handle: int, ev_start: int | None, ev_stop: int | None) -> None:

@@ -11,27 +11,39 @@
 //
 // GPU design (none of it is on the pages, whose engines are CPU code):
 //   * The byte stream is cut into 4 KiB chunks, one CTA each. A CTA loads its
-//     chunk plus a 16-byte halo and a 256-byte margin into shared memory,
-//     decides for every byte whether a pre-token starts there (a local
-//     predicate equivalent to the ordered-alternative split, see
-//     starts_piece), and collects the pre-tokens that start in its chunk.
+//     chunk plus a 16-byte halo and a 256-byte margin into shared memory and
+//     marks where pre-tokens start. Each thread takes 16 bytes: when they and
+//     their context are ASCII without an apostrophe, carry-free SWAR range
+//     tests give 16-bit class masks and the split rules are a dozen mask
+//     operations; otherwise a 24-byte UTF-8 unit scan builds the same masks,
+//     and apostrophes or multi-byte whitespace fall back to the per-byte
+//     predicate starts_piece.
 //   * Symbols are token ids: byte b starts as byte_id[b]; a merge table maps
 //     (left_id, right_id) to its rank through an open-addressed hash table
 //     of 32-byte buckets (one L2 sector each); rank -> new_id comes from the
 //     merge rows. Because bytes(new_id) = bytes(left) || bytes(right) (checked
 //     by bpe_build), the final symbols are the vocabulary ids.
+//   * Word cache ("Hugging Face Tokenizers v1", section on word caching: the
+//     same pre-token always gives the same ids, so a memo from pre-token bytes
+//     to ids skips the merge loop). Here the memo is filled once in bpe_build:
+//     every vocabulary string of at most 16 bytes is run through the merge
+//     kernel below, and its ids are stored under its bytes. A pre-token of at
+//     most 16 bytes that is found there takes the stored ids; any other runs
+//     the merge loop.
 //   * Pre-tokens of up to 64 bytes are merged by one thread each in shared
-//     memory with a flat array plus a cached rank per adjacent pair (the
-//     "Hugging Face Tokenizers v1" merge-loop rewrite: flat arrays, integer
-//     rank compare, no allocation). Longer ones are merged by the whole CTA
-//     in a device scratch pool indexed by input byte position, so every long
-//     pre-token owns the pool range of its own bytes.
-//   * Output positions: a single-pass chained scan (decoupled look-back) over
-//     chunk token counts; chunks take tickets in launch order so every
-//     predecessor is already running. Waits are bounded by the global timer.
+//     memory with a flat array plus a cached rank per adjacent pair (the v1
+//     merge-loop rewrite: flat arrays, integer rank compare, no allocation).
+//     Longer ones are merged by the whole CTA in a device scratch pool indexed
+//     by input byte position, so every long pre-token owns the pool range of
+//     its own bytes.
+//   * Output positions: a single-pass chained scan (decoupled look-back, one
+//     warp) over chunk token counts; chunks take tickets in launch order so
+//     every predecessor is already running. Waits are bounded by the global
+//     timer. Ids are staged in shared memory and stored coalesced.
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <string>
@@ -48,7 +60,7 @@ namespace {
 // ---------------------------------------------------------------- constants --
 
 constexpr int kThreads = 256;         // threads per CTA
-constexpr int kChunk = 4096;          // bytes whose pre-tokens a CTA owns
+constexpr int kChunk = 4096;          // bytes whose pre-tokens a CTA owns (16 per thread)
 constexpr int kMargin = 256;          // bytes after the chunk kept in shared memory
 constexpr int kHalo = 16;             // context bytes on each side of the window
 constexpr int kWin = kHalo + kChunk + kMargin + kHalo;   // window bytes
@@ -56,6 +68,8 @@ constexpr int kWinWords = (kWin + 31) / 32;
 constexpr int kSpan = kChunk + kMargin;                  // positions with a start bit
 constexpr int kSpanWords = kSpan / 32;
 constexpr int kShortMax = 64;         // longest pre-token merged by one thread
+constexpr int kCacheMaxLen = 16;      // longest pre-token looked up in the word cache
+constexpr int kCacheMaxIds = 3;       // most ids a cache entry holds
 constexpr int kLongPerThread = 4;     // elements per thread per round of the CTA merge
 constexpr int kRound = kThreads * kLongPerThread;
 constexpr int kMaxLong = kChunk / kShortMax + 2;
@@ -63,6 +77,9 @@ constexpr uint32_t kInf = 0xFFFFFFFFu;
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 constexpr uint64_t kEmpty = ~0ull;
 constexpr uint64_t kWaitLimitNs = 20ull * 1000 * 1000 * 1000;  // 20 s
+
+static_assert(kChunk == 16 * kThreads, "one 16-byte group per thread");
+static_assert(kMargin <= 16 * 16, "the margin is covered by 16 lanes of warp 0");
 
 // device status bits
 constexpr uint32_t kStBadInput = 1u;
@@ -77,15 +94,24 @@ constexpr uint64_t kDescValue = (1ull << 62) - 1;
 
 enum Cls { kO = 0, kL = 1, kN = 2, kS = 3 };
 
-__host__ __device__ inline uint32_t pair_hash(uint32_t a, uint32_t b) {
-  // MurmurHash3's 64-bit finalizer over the packed pair.
-  uint64_t x = ((uint64_t)a << 32) | b;
+__host__ __device__ inline uint64_t fmix64(uint64_t x) {
+  // MurmurHash3's 64-bit finalizer.
   x ^= x >> 33;
   x *= 0xFF51AFD7ED558CCDull;
   x ^= x >> 33;
   x *= 0xC4CEB9FE1A85EC53ull;
   x ^= x >> 33;
-  return (uint32_t)x;
+  return x;
+}
+
+__host__ __device__ inline uint32_t pair_hash(uint32_t a, uint32_t b) {
+  return (uint32_t)fmix64(((uint64_t)a << 32) | b);
+}
+
+// Word cache key: the pre-token's bytes little-endian in k0 (bytes 0..7) and
+// k1 (bytes 8..15), zero padded, plus its length.
+__host__ __device__ inline uint32_t cache_hash(uint64_t k0, uint64_t k1, uint32_t len) {
+  return (uint32_t)fmix64(k0 * 0x9E3779B97F4A7C15ull + (k1 ^ len) * 0xC2B2AE3D27D4EB4Full);
 }
 
 struct Tables {
@@ -93,6 +119,14 @@ struct Tables {
   uint32_t hmask;          // buckets - 1
   const int32_t* mrows;    // [n_merges][3] (left, right, new)
   const int32_t* byte_id;  // [256]
+};
+
+// Word cache entry, two uint4: {k0 lo, k0 hi, k1 lo, k1 hi}, {meta, id0, id1,
+// id2}; meta = len | count << 5 | 1 << 31, 0 for an empty slot.
+struct Cache {
+  const uint4* e;
+  uint32_t mask;  // slots - 1
+  int enabled;
 };
 
 struct DevSmall {
@@ -133,6 +167,25 @@ __device__ __forceinline__ uint32_t lookup_rank(const Tables& T, uint32_t a, uin
     bucket = (bucket + 1) & T.hmask;
   }
   return kInf;
+}
+
+// Number of ids (1..3) the word cache holds for a pre-token, or 0 if absent.
+__device__ __forceinline__ uint32_t cache_lookup(const Cache& C, uint64_t k0, uint64_t k1, uint32_t len,
+                                                 uint32_t* ids) {
+  uint32_t slot = cache_hash(k0, k1, len) & C.mask;
+  for (uint32_t probe = 0; probe <= C.mask; ++probe) {
+    const uint4 a = __ldg(C.e + 2 * slot), b = __ldg(C.e + 2 * slot + 1);
+    if (b.x == 0) return 0;
+    if ((b.x & 31u) == len && a.x == (uint32_t)k0 && a.y == (uint32_t)(k0 >> 32) && a.z == (uint32_t)k1 &&
+        a.w == (uint32_t)(k1 >> 32)) {
+      ids[0] = b.y;
+      ids[1] = b.z;
+      ids[2] = b.w;
+      return (b.x >> 5) & 7u;
+    }
+    slot = (slot + 1) & C.mask;
+  }
+  return 0;
 }
 
 __device__ __forceinline__ int cp_class(uint32_t cp) {
@@ -237,6 +290,7 @@ __device__ __forceinline__ bool apostrophe_starts_piece(const uint8_t* w, I lo, 
   return c == kL || c == kN || (c == kS && w[j - 1] != ' ');
 }
 
+// The predicate, one position at a time (reference form of the mask paths).
 template <typename I>
 __device__ bool starts_piece(const uint8_t* w, I lo, I hi, I i) {
   if (i == lo) return true;
@@ -261,6 +315,232 @@ __device__ bool starts_piece(const uint8_t* w, I lo, I hi, I i) {
   if (bp == ' ') return false;  // B3
   if (cprev == kS) return true;
   return ci != cprev;
+}
+
+// 0x80 in each byte of w (four ASCII bytes) that is a letter / digit /
+// whitespace / U+0020, by carry-free range tests: for an ASCII byte x,
+// x + (0x80 - lo) has bit 7 set iff x >= lo.
+struct Ascii4 {
+  uint32_t L, N, S, SP;
+};
+
+__device__ __forceinline__ Ascii4 ascii_classes(uint32_t w) {
+  const uint32_t H = 0x80808080u;
+  const uint32_t t = w | 0x20202020u;  // fold case
+  Ascii4 r;
+  r.L = (t + 0x1F1F1F1Fu) & ~(t + 0x05050505u) & H;   // 'a' .. 'z'
+  r.N = (w + 0x50505050u) & ~(w + 0x46464646u) & H;   // '0' .. '9'
+  const uint32_t y = w ^ 0x20202020u;
+  r.SP = ~(y + 0x7F7F7F7Fu) & H;                      // == 0x20
+  r.S = ((w + 0x77777777u) & ~(w + 0x72727272u) & H) | r.SP;  // 0x09 .. 0x0D or 0x20
+  return r;
+}
+
+// 0x80-per-byte mask of a word -> 4 bits (byte j -> bit j).
+__device__ __forceinline__ uint32_t movemask4(uint32_t m) { return ((m >> 7) * 0x01020408u) >> 24; }
+
+__device__ __forceinline__ bool has_byte(uint32_t w, uint32_t b) {
+  const uint32_t y = w ^ (b * 0x01010101u);
+  return ((y - 0x01010101u) & ~y & 0x80808080u) != 0;
+}
+
+struct Smem;
+__device__ __forceinline__ uint32_t bits32_at(const uint32_t* bits, int start) {
+  const int w = start >> 5, sh = start & 31;
+  return __funnelshift_r(bits[w], bits[w + 1], sh);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ window --
+
+namespace {
+
+struct Smem {
+  uint8_t win[kWin + 16];
+  uint32_t docbits[kWinWords + 2];   // a document (or the area after the last one) starts here
+  uint32_t outbits[kWinWords + 2];   // byte belongs to no document
+  uint32_t startbits[kSpanWords];
+  uint16_t span_start[kChunk + 1];
+  uint32_t span_cnt[kChunk + 1];     // token counts, then exclusive offsets
+  uint32_t sym[kSpan];               // ids of short pre-tokens, at their start position
+  union {
+    uint32_t rk[kSpan];              // pair ranks while merging short pre-tokens
+    uint32_t stage[kRound];          // long merge rounds
+    uint32_t ostage[kSpan];          // ids in output order
+  } u;
+  int32_t byte_id[256];
+  uint16_t long_list[kMaxLong];
+  uint32_t red[kThreads / 32 + 2];
+  uint32_t carry[2];
+  int64_t chunk;
+  int64_t prefix;
+  uint32_t n_spans;
+  uint32_t n_long;
+  int64_t last_end;
+  int64_t doc_lo, doc_hi;  // document of a long pre-token that runs past the window
+};
+
+__device__ __forceinline__ bool bit_at(const uint32_t* bits, int i) { return (bits[i >> 5] >> (i & 31)) & 1u; }
+
+// Document bounds [lo, hi) around window index i: the nearest document edge at
+// or before i and the next one after i (at most kHalo away is all that is
+// read), or the window edges.
+__device__ __forceinline__ void doc_bounds(const Smem& S, int i, int* lo, int* hi) {
+  int a = i;
+  while (a > 0 && a > i - kHalo && !bit_at(S.docbits, a)) --a;
+  *lo = a;
+  int b = i + 1;
+  while (b < kWin && b <= i + kHalo && !bit_at(S.docbits, b)) ++b;
+  *hi = b;
+}
+
+__device__ __forceinline__ bool starts_piece_at(const Smem& S, int i) {
+  if (bit_at(S.outbits, i)) return false;
+  int lo, hi;
+  doc_bounds(S, i, &lo, &hi);
+  return starts_piece<int>(S.win, lo, hi, i);
+}
+
+// Start bits of window positions [p0, p0 + 16), p0 a multiple of 16.
+__device__ uint32_t start_mask16(const Smem& S, int p0) {
+  const uint32_t* w32 = reinterpret_cast<const uint32_t*>(S.win);
+  const uint4 v = *reinterpret_cast<const uint4*>(S.win + p0);
+  const uint32_t wp = w32[(p0 >> 2) - 1], wn = w32[(p0 >> 2) + 4];
+  const uint32_t D17 = bits32_at(S.docbits, p0) & 0x1FFFFu;
+  const uint32_t O16 = bits32_at(S.outbits, p0) & 0xFFFFu;
+  if (O16 == 0xFFFFu) return 0;
+  const uint32_t any = v.x | v.y | v.z | v.w | wp | wn;
+  const bool apos = has_byte(wp, '\'') || has_byte(v.x, '\'') || has_byte(v.y, '\'') || has_byte(v.z, '\'') ||
+                    has_byte(v.w, '\'') || has_byte(wn, '\'');
+  if (!(any & 0x80808080u) && !apos) {
+    // ASCII: every byte is a unit.
+    const Ascii4 a0 = ascii_classes(v.x), a1 = ascii_classes(v.y), a2 = ascii_classes(v.z),
+                 a3 = ascii_classes(v.w), ap = ascii_classes(wp), an = ascii_classes(wn);
+    const uint32_t L = movemask4(a0.L) | movemask4(a1.L) << 4 | movemask4(a2.L) << 8 | movemask4(a3.L) << 12;
+    const uint32_t N = movemask4(a0.N) | movemask4(a1.N) << 4 | movemask4(a2.N) << 8 | movemask4(a3.N) << 12;
+    const uint32_t Sm = movemask4(a0.S) | movemask4(a1.S) << 4 | movemask4(a2.S) << 8 | movemask4(a3.S) << 12;
+    const uint32_t SP = movemask4(a0.SP) | movemask4(a1.SP) << 4 | movemask4(a2.SP) << 8 | movemask4(a3.SP) << 12;
+    const uint32_t Lp = (L << 1) | (ap.L >> 31), Np = (N << 1) | (ap.N >> 31);
+    const uint32_t Sp = (Sm << 1) | (ap.S >> 31), SPp = (SP << 1) | (ap.SP >> 31);
+    const uint32_t Sn = (Sm >> 1) | ((an.S >> 7) & 1u) << 15;
+    const uint32_t Dn = D17 >> 1;
+    const uint32_t B2 = Sm & (~Sp | (~Sn & ~Dn));
+    const uint32_t B3 = ~Sm & ~SPp & (Sp | (L ^ Lp) | (N ^ Np));
+    return (D17 | B2 | B3) & ~O16 & 0xFFFFu;
+  }
+  // General: scan the UTF-8 units of bytes [p0 - 7, p0 + 17). Bit k of the
+  // masks below is byte p0 - 8 + k; each byte carries its unit's class. Units
+  // starting before p0 - 8 may be misread only up to p0 - 5, and nothing
+  // before p0 - 4 is used.
+  const int base = p0 - 8;
+  const uint32_t D = bits32_at(S.docbits, base), O = bits32_at(S.outbits, base);
+  uint32_t U = 0, Lm = 0, Nm = 0, Sm = 0, SPm = 0, APm = 0, MBS = 0;
+  int rem = 0, cls = kO;
+#pragma unroll 4
+  for (int k = 1; k < 25; ++k) {
+    const int q = base + k;
+    const uint32_t b = S.win[q];
+    const uint32_t bit = 1u << k;
+    if (D & bit) rem = 0;
+    if (rem > 0) {
+      --rem;
+    } else {
+      U |= bit;
+      const uint32_t dn = (D >> (k + 1)) & 7u;  // document edges at q + 1 .. q + 3
+      const int hi = dn ? q + __ffs(dn) : q + 4;
+      const int len = seq_len(S.win, hi, q);
+      cls = unit_class(S.win, q, len);
+      rem = (len > 1 ? len : 1) - 1;
+      if (cls == kS && len > 1) MBS |= bit;
+    }
+    Lm |= cls == kL ? bit : 0u;
+    Nm |= cls == kN ? bit : 0u;
+    Sm |= cls == kS ? bit : 0u;
+    SPm |= b == 0x20u ? bit : 0u;
+    APm |= b == 0x27u ? bit : 0u;
+  }
+  const uint32_t Sp = Sm << 1, Lp = Lm << 1, Np = Nm << 1, SPp = SPm << 1;
+  const uint32_t Sn = Sm >> 1, Dn = D >> 1;
+  const uint32_t B2 = Sm & (~Sp | (~Sn & ~Dn));
+  const uint32_t B3 = ~Sm & ~SPp & (Sp | (Lm ^ Lp) | (Nm ^ Np));
+  uint32_t res = ((U & ~O & (D | B2 | B3)) >> 8) & 0xFFFFu;
+  // Contractions and multi-byte whitespace: the per-byte predicate.
+  uint32_t fix = (APm & 0x01FFFFF0u) ? 0xFFFFu : 0u;
+  fix |= (MBS >> 8) & 0xFFFFu;
+  while (fix) {
+    const int k = __ffs(fix) - 1;
+    fix &= fix - 1;
+    const uint32_t bit = 1u << k;
+    res = (res & ~bit) | (starts_piece_at(S, p0 + k) ? bit : 0u);
+  }
+  return res;
+}
+
+// Loads the window of chunk c: bytes [c0 - kHalo, c0 + kChunk + kMargin +
+// kHalo), the document edges that fall inside it, and which bytes lie outside
+// every document. first_doc = the first document starting at or after c0.
+__device__ void load_window(Smem& S, const uint8_t* bytes, int64_t n_bytes, const int64_t* doc_offsets,
+                            int64_t n_docs, int64_t c0, int64_t first_doc) {
+  const int tid = threadIdx.x;
+  const int64_t w0 = c0 - kHalo;
+  const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 15u) == 0;
+  for (int i = tid * 16; i < kWin; i += kThreads * 16) {
+    const int64_t p = w0 + i;
+    if (aligned && p >= 0 && p + 16 <= n_bytes) {
+      *reinterpret_cast<uint4*>(S.win + i) = __ldg(reinterpret_cast<const uint4*>(bytes + p));
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) S.win[i + k] = (p + k >= 0 && p + k < n_bytes) ? bytes[p + k] : 0;
+    }
+  }
+  for (int i = tid; i < kWinWords + 2; i += kThreads) {
+    S.docbits[i] = 0;
+    S.outbits[i] = 0;
+  }
+  __syncthreads();
+  int64_t d_first = doc_offsets[0], d_last = doc_offsets[n_docs];
+  d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
+  d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
+  for (int wi = tid; wi < kWinWords; wi += kThreads) {
+    uint32_t word = 0;
+    const int64_t p = w0 + (int64_t)wi * 32;
+    if (p < d_first || p + 32 > d_last) {
+      for (int k = 0; k < 32; ++k)
+        if (p + k < d_first || p + k >= d_last) word |= 1u << k;
+    }
+    S.outbits[wi] = word;
+  }
+  // Document starts in the window: walk back from first_doc over starts in
+  // the halo, then forward.
+  int64_t k_lo = first_doc;
+  if (k_lo > n_docs) k_lo = n_docs;
+  if (k_lo < 0) k_lo = 0;
+  while (k_lo > 0 && doc_offsets[k_lo - 1] >= w0) --k_lo;
+  const int64_t w_end = w0 + kWin;
+  for (int64_t k = k_lo + tid; k <= n_docs; k += kThreads) {
+    int64_t o = doc_offsets[k];
+    if (o >= w_end) break;
+    if (o >= w0) {
+      int i = (int)(o - w0);
+      atomicOr(&S.docbits[i >> 5], 1u << (i & 31));
+    }
+  }
+  __syncthreads();
+}
+
+// Start bits for window indices [kHalo, kHalo + kSpan).
+__device__ void compute_start_bits(Smem& S) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t m = start_mask16(S, kHalo + 16 * tid);
+  uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, m, 1);
+  if ((tid & 1) == 0) S.startbits[tid >> 1] = m | (hi << 16);
+  if (tid < 32) {  // the margin, 16 bytes per lane
+    uint32_t mm = lane < kMargin / 16 ? start_mask16(S, kHalo + kChunk + 16 * lane) : 0u;
+    uint32_t h2 = __shfl_down_sync(0xFFFFFFFFu, mm, 1);
+    if ((lane & 1) == 0 && lane < kMargin / 16) S.startbits[kChunk / 32 + (lane >> 1)] = mm | (h2 << 16);
+  }
+  __syncthreads();
 }
 
 // ----------------------------------------------------------- block helpers --
@@ -341,7 +621,7 @@ __device__ uint32_t block_tf_input(uint32_t f, uint32_t carry_in, uint32_t* red)
 }
 
 // ----------------------------------------------------------- merge: short --
-// One thread, symbols and pair ranks in shared memory. rk[k] is the rank of
+// One thread, symbols and pair ranks in memory it owns. rk[k] is the rank of
 // (sym[k], sym[k+1]). A step takes the lowest rank, replaces every occurrence
 // of that pair left to right without overlap, and re-probes only the pairs
 // that touch a new symbol.
@@ -384,13 +664,13 @@ __device__ int merge_short(uint32_t* sym, uint32_t* rk, const uint8_t* src, int 
 }
 
 // ------------------------------------------------------------ merge: long --
-// The whole CTA merges one long pre-token in place in scr (its own byte range
-// of the output buffer, read and written in rounds of kRound elements; a
-// round writes only below where it read). A step is one pass: the chosen pair
-// is replaced left to right without overlap — each thread runs that scan over
-// its kLongPerThread elements for both possible "first element already
-// consumed" inputs, a CTA scan composes the results in order — and the pass
-// also probes every new adjacent pair for the next step's lowest rank.
+// The whole CTA merges one long pre-token in place in scr (the pool range of
+// its own bytes, read and written in rounds of kRound elements; a round writes
+// only below where it read). A step is one pass: the chosen pair is replaced
+// left to right without overlap — each thread runs that scan over its
+// kLongPerThread elements for both possible "first element already consumed"
+// inputs, a CTA scan composes the results in order — and the pass also probes
+// every new adjacent pair for the next step's lowest rank.
 
 struct LongScratch {
   uint32_t* stage;  // kRound
@@ -472,100 +752,32 @@ __device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, in
   return len;
 }
 
-// ------------------------------------------------------------------ window --
-
-struct Smem {
-  uint8_t win[kWin + 16];
-  uint32_t docbits[kWinWords];   // a document (or the area after the last one) starts here
-  uint32_t outbits[kWinWords];   // byte belongs to no document
-  uint32_t startbits[kSpanWords];
-  uint16_t span_start[kChunk + 1];
-  uint32_t span_cnt[kChunk + 1];
-  uint32_t sym[kSpan];
-  uint32_t rk[kSpan];
-  uint32_t stage[kRound];
-  int32_t byte_id[256];
-  uint16_t long_list[kMaxLong];
-  uint32_t red[kThreads / 32 + 2];
-  uint32_t carry[2];
-  int64_t chunk;
-  int64_t prefix;
-  uint32_t n_spans;
-  uint32_t n_long;
-  int64_t last_end;
-  int64_t doc_lo, doc_hi;  // document of a long pre-token that runs past the window
-};
-
-__device__ __forceinline__ bool bit_at(const uint32_t* bits, int i) { return (bits[i >> 5] >> (i & 31)) & 1u; }
-
-// Document bounds [lo, hi) around window index i: the nearest document edge at
-// or before i and the next one after i (at most kHalo away is all that is
-// read), or the window edges.
-__device__ __forceinline__ void doc_bounds(const Smem& S, int i, int* lo, int* hi) {
-  int a = i;
-  while (a > 0 && a > i - kHalo && !bit_at(S.docbits, a)) --a;
-  *lo = a;
-  int b = i + 1;
-  while (b < kWin && b <= i + kHalo && !bit_at(S.docbits, b)) ++b;
-  *hi = b;
-}
-
-// Loads the window of chunk c: bytes [c0 - kHalo, c0 + kChunk + kMargin +
-// kHalo), the document edges that fall inside it, and which bytes lie outside
-// every document. first_doc = the first document starting at or after c0.
-__device__ void load_window(Smem& S, const uint8_t* bytes, int64_t n_bytes, const int64_t* doc_offsets,
-                            int64_t n_docs, int64_t c0, int64_t first_doc) {
-  const int tid = threadIdx.x;
-  const int64_t w0 = c0 - kHalo;
-  for (int i = tid; i < kWin; i += kThreads) {
-    int64_t p = w0 + i;
-    S.win[i] = (p >= 0 && p < n_bytes) ? bytes[p] : 0;
-  }
-  for (int i = tid; i < kWinWords; i += kThreads) {
-    S.docbits[i] = 0;
-    S.outbits[i] = 0;
-  }
-  __syncthreads();
-  int64_t d_first = doc_offsets[0], d_last = doc_offsets[n_docs];
-  d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
-  d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
-  for (int i = tid; i < kWin; i += kThreads) {
-    int64_t p = w0 + i;
-    if (p < d_first || p >= d_last) atomicOr(&S.outbits[i >> 5], 1u << (i & 31));
-  }
-  // Document starts in the window: walk back from first_doc over starts in
-  // the halo, then forward.
-  int64_t k_lo = first_doc;
-  if (k_lo > n_docs) k_lo = n_docs;
-  if (k_lo < 0) k_lo = 0;
-  while (k_lo > 0 && doc_offsets[k_lo - 1] >= w0) --k_lo;
-  const int64_t w_end = w0 + kWin;
-  for (int64_t k = k_lo + tid; k <= n_docs; k += kThreads) {
-    int64_t o = doc_offsets[k];
-    if (o >= w_end) break;
-    if (o >= w0) {
-      int i = (int)(o - w0);
-      atomicOr(&S.docbits[i >> 5], 1u << (i & 31));
+// Ids of one short pre-token (window positions [ws, ws + len)) into sym;
+// returns their count.
+__device__ __forceinline__ uint32_t encode_short(Smem& S, int st, int len, const Tables& T, const Cache& C) {
+  const int ws = kHalo + st;
+  if (C.enabled && len <= kCacheMaxLen) {
+    const uint64_t* w64 = reinterpret_cast<const uint64_t*>(S.win);
+    const int wi = ws >> 3, sh = (ws & 7) * 8;
+    const uint64_t a = w64[wi], b = w64[wi + 1], c = w64[wi + 2];
+    uint64_t k0 = sh ? (a >> sh) | (b << (64 - sh)) : a;
+    uint64_t k1 = sh ? (b >> sh) | (c << (64 - sh)) : b;
+    if (len < 8) {
+      k0 &= (1ull << (8 * len)) - 1ull;
+      k1 = 0;
+    } else if (len == 8) {
+      k1 = 0;
+    } else if (len < 16) {
+      k1 &= (1ull << (8 * (len - 8))) - 1ull;
+    }
+    uint32_t ids[kCacheMaxIds];
+    const uint32_t cnt = cache_lookup(C, k0, k1, (uint32_t)len, ids);
+    if (cnt) {
+      for (uint32_t q = 0; q < cnt; ++q) S.sym[st + q] = ids[q];
+      return cnt;
     }
   }
-  __syncthreads();
-}
-
-// Start bits for window indices [kHalo, kHalo + kSpan).
-__device__ void compute_start_bits(Smem& S) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int base = warp * 32; base < kSpan; base += kThreads) {
-    const int i = kHalo + base + lane;
-    bool b = false;
-    if (!bit_at(S.outbits, i)) {
-      int lo, hi;
-      doc_bounds(S, i, &lo, &hi);
-      b = starts_piece<int>(S.win, lo, hi, i);
-    }
-    uint32_t word = __ballot_sync(0xFFFFFFFFu, b);
-    if (lane == 0) S.startbits[base >> 5] = word;
-  }
-  __syncthreads();
+  return (uint32_t)merge_short(S.sym + st, S.u.rk + st, S.win + ws, len, T, S.byte_id);
 }
 
 // ------------------------------------------------------------------ kernels --
@@ -610,11 +822,57 @@ struct EncodeArgs {
   int64_t* out_offsets;
   int32_t* pool;  // long pre-token scratch, one int32 per input byte
   Tables T;
+  Cache C;
   uint64_t* desc;
   const int64_t* first_doc;
   DevSmall* small;
   int64_t n_chunks;
 };
+
+// Exclusive prefix of chunk c from the chained scan; called by warp 0. Lane
+// l reads the descriptor of chunk (base - l); the window slides back until an
+// inclusive prefix is found.
+__device__ int64_t look_back(uint64_t* desc, int64_t c, uint32_t agg, DevSmall* small) {
+  const int lane = threadIdx.x & 31;
+  if (c == 0) {
+    if (lane == 0) st_relaxed(&desc[0], kDescIncl | (uint64_t)agg);
+    return 0;
+  }
+  if (lane == 0) st_relaxed(&desc[c], kDescAgg | (uint64_t)agg);
+  int64_t excl = 0, base = c - 1;
+  const uint64_t t_start = global_timer();
+  bool timed_out = false;
+  for (;;) {
+    const int64_t j = base - lane;
+    const uint64_t d = j >= 0 ? ld_relaxed(&desc[j]) : kDescIncl;
+    const uint32_t ready = __ballot_sync(0xFFFFFFFFu, (d & ~kDescValue) != 0);
+    const uint32_t incl = __ballot_sync(0xFFFFFFFFu, (d & ~kDescValue) == kDescIncl);
+    // Lanes up to and including the nearest inclusive one must be ready.
+    const uint32_t need = incl ? (((incl & (0u - incl)) << 1) - 1u) : 0xFFFFFFFFu;
+    if ((ready & need) != need) {
+      bool out = false;
+      if (lane == 0) out = global_timer() - t_start > kWaitLimitNs;
+      out = __shfl_sync(0xFFFFFFFFu, out, 0);
+      if (out) {
+        timed_out = true;
+        break;
+      }
+      __nanosleep(32);
+      continue;
+    }
+    uint64_t v = (need >> lane) & 1u ? (d & kDescValue) : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    excl += (int64_t)v;
+    if (incl) break;
+    base -= 32;
+  }
+  if (lane == 0) {
+    if (timed_out) atomicOr(&small->status, kStTimeout);
+    st_relaxed(&desc[c], kDescIncl | (uint64_t)(excl + agg));
+  }
+  return excl;
+}
 
 __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -652,29 +910,36 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
 
   // End of the last pre-token: the next start or document edge in the margin,
   // or -1 when it runs past the window.
-  if (tid == 0 && n_spans > 0) {
-    int from = S.span_start[n_spans - 1] + 1;
+  if (tid < 32 && n_spans > 0) {
+    const int from = S.span_start[n_spans - 1] + 1;
     int64_t end = -1;
-    for (int j = from; j < kSpan; ++j) {
-      const int i = kHalo + j;
-      if (bit_at(S.startbits, j) || bit_at(S.outbits, i) || bit_at(S.docbits, i)) {
-        end = c0 + j;
+    for (int base = from & ~31; base < kSpan; base += 32 * 32) {
+      const int wj = (base >> 5) + tid;
+      uint32_t m = 0;
+      if (wj < kSpanWords) {
+        m = S.startbits[wj] | bits32_at(S.outbits, kHalo + wj * 32) | bits32_at(S.docbits, kHalo + wj * 32);
+        const int lo_bit = from - wj * 32;
+        if (lo_bit > 0) m = lo_bit >= 32 ? 0u : (m & (0xFFFFFFFFu << lo_bit));
+      }
+      const uint32_t any = __ballot_sync(0xFFFFFFFFu, m != 0);
+      if (any) {
+        const int first = __ffs(any) - 1;
+        const uint32_t mf = __shfl_sync(0xFFFFFFFFu, m, first);
+        end = c0 + (((base >> 5) + first) * 32 + (__ffs(mf) - 1));
         break;
       }
     }
-    S.last_end = end;
+    if (tid == 0) S.last_end = end;
   }
   __syncthreads();
 
   // Short pre-tokens: one thread each.
   for (uint32_t j = tid; j < n_spans; j += kThreads) {
     const int st = S.span_start[j];
-    int64_t en;
-    if (j + 1 < n_spans) en = c0 + S.span_start[j + 1];
-    else en = S.last_end;
+    const int64_t en = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
     const int len = en < 0 ? kSpan : (int)(en - (c0 + st));
     if (en >= 0 && len <= kShortMax) {
-      S.span_cnt[j] = (uint32_t)merge_short(S.sym + st, S.rk + st, S.win + kHalo + st, len, a.T, S.byte_id);
+      S.span_cnt[j] = encode_short(S, st, len, a.T, a.C);
     } else {
       uint32_t slot = atomicAdd(&S.n_long, 1u);
       if (slot < (uint32_t)kMaxLong) S.long_list[slot] = (uint16_t)j;
@@ -686,67 +951,69 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
 
   // Long pre-tokens: the whole CTA, one at a time, in order.
   const uint32_t n_long = min(S.n_long, (uint32_t)kMaxLong);
-  if (tid == 0 && n_long > 1) {  // sort the short list (insertion sort)
-    for (uint32_t x = 1; x < n_long; ++x) {
-      uint16_t v = S.long_list[x];
-      int y = (int)x - 1;
-      while (y >= 0 && S.long_list[y] > v) {
-        S.long_list[y + 1] = S.long_list[y];
-        --y;
-      }
-      S.long_list[y + 1] = v;
-    }
-  }
-  __syncthreads();
-  LongScratch L{S.stage, S.red, S.carry};
-  for (uint32_t x = 0; x < n_long; ++x) {
-    const uint32_t j = S.long_list[x];
-    const int64_t s = c0 + S.span_start[j];
-    int64_t e = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
-    if (e < 0) {
-      // Runs past the window: find the document it lies in, then the next
-      // pre-token start after the window.
-      if (tid == 0) {
-        int64_t lo = 0, hi = a.n_docs + 1;  // first k with doc_offsets[k] > s
-        while (lo < hi) {
-          int64_t mid = (lo + hi) >> 1;
-          if (a.doc_offsets[mid] <= s) lo = mid + 1;
-          else hi = mid;
+  if (n_long > 0) {
+    if (tid == 0 && n_long > 1) {  // sort the short list (insertion sort)
+      for (uint32_t x = 1; x < n_long; ++x) {
+        uint16_t v = S.long_list[x];
+        int y = (int)x - 1;
+        while (y >= 0 && S.long_list[y] > v) {
+          S.long_list[y + 1] = S.long_list[y];
+          --y;
         }
-        int64_t k = lo - 1;
-        int64_t dlo = (k >= 0) ? a.doc_offsets[k] : 0;
-        int64_t dhi = (k >= 0 && k < a.n_docs) ? a.doc_offsets[k + 1] : s + 1;
-        if (dhi > a.n_bytes) dhi = a.n_bytes;
-        if (dlo > s) dlo = s;
-        if (dlo < 0) dlo = 0;
-        if (dhi <= s) dhi = s + 1;
-        S.doc_lo = dlo;
-        S.doc_hi = dhi;
+        S.long_list[y + 1] = v;
       }
-      __syncthreads();
-      const int64_t dlo = S.doc_lo, dhi = S.doc_hi;
-      int64_t found = dhi;
-      for (int64_t base = c0 + kSpan; base < dhi; base += kThreads) {
-        const int64_t p = base + tid;
-        bool b = p < dhi && starts_piece<int64_t>(a.bytes, dlo, dhi, p);
-        uint32_t cand = b ? (uint32_t)(p - base) : kInf;
-        uint32_t m = block_min(cand, S.red);
-        if (m != kInf) {
-          found = base + m;
-          break;
-        }
-      }
-      e = found;
-    }
-    const int64_t n = e - s;
-    if (n <= 0 || n >= (int64_t)0x7FFFFFFF) {
-      if (tid == 0) atomicOr(&a.small->status, kStInternal);
-      if (tid == 0) S.span_cnt[j] = 0;
-    } else {
-      uint32_t cnt = merge_long(a.bytes, s, (uint32_t)n, a.pool + s, a.T, S.byte_id, L);
-      if (tid == 0) S.span_cnt[j] = cnt;
     }
     __syncthreads();
+    LongScratch L{S.u.stage, S.red, S.carry};
+    for (uint32_t x = 0; x < n_long; ++x) {
+      const uint32_t j = S.long_list[x];
+      const int64_t s = c0 + S.span_start[j];
+      int64_t e = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
+      if (e < 0) {
+        // Runs past the window: find the document it lies in, then the next
+        // pre-token start after the window.
+        if (tid == 0) {
+          int64_t lo = 0, hi = a.n_docs + 1;  // first k with doc_offsets[k] > s
+          while (lo < hi) {
+            int64_t mid = (lo + hi) >> 1;
+            if (a.doc_offsets[mid] <= s) lo = mid + 1;
+            else hi = mid;
+          }
+          int64_t k = lo - 1;
+          int64_t dlo = (k >= 0) ? a.doc_offsets[k] : 0;
+          int64_t dhi = (k >= 0 && k < a.n_docs) ? a.doc_offsets[k + 1] : s + 1;
+          if (dhi > a.n_bytes) dhi = a.n_bytes;
+          if (dlo > s) dlo = s;
+          if (dlo < 0) dlo = 0;
+          if (dhi <= s) dhi = s + 1;
+          S.doc_lo = dlo;
+          S.doc_hi = dhi;
+        }
+        __syncthreads();
+        const int64_t dlo = S.doc_lo, dhi = S.doc_hi;
+        int64_t found = dhi;
+        for (int64_t base = c0 + kSpan; base < dhi; base += kThreads) {
+          const int64_t p = base + tid;
+          bool b = p < dhi && starts_piece<int64_t>(a.bytes, dlo, dhi, p);
+          uint32_t cand = b ? (uint32_t)(p - base) : kInf;
+          uint32_t m = block_min(cand, S.red);
+          if (m != kInf) {
+            found = base + m;
+            break;
+          }
+        }
+        e = found;
+      }
+      const int64_t n = e - s;
+      if (n <= 0 || n >= (int64_t)0x7FFFFFFF) {
+        if (tid == 0) atomicOr(&a.small->status, kStInternal);
+        if (tid == 0) S.span_cnt[j] = 0;
+      } else {
+        uint32_t cnt = merge_long(a.bytes, s, (uint32_t)n, a.pool + s, a.T, S.byte_id, L);
+        if (tid == 0) S.span_cnt[j] = cnt;
+      }
+      __syncthreads();
+    }
   }
 
   // Token offsets within the chunk.
@@ -767,35 +1034,12 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
   }
 
   // Chained scan over chunks.
-  if (tid == 0) {
-    uint64_t* desc = a.desc;
-    int64_t excl = 0;
-    if (c == 0) {
-      st_relaxed(&desc[0], kDescIncl | (uint64_t)agg);
-    } else {
-      st_relaxed(&desc[c], kDescAgg | (uint64_t)agg);
-      int64_t j = c - 1;
-      const uint64_t t_start = global_timer();
-      bool timed_out = false;
-      while (j >= 0) {
-        uint64_t d = ld_relaxed(&desc[j]);
-        if ((d & ~kDescValue) == 0) {
-          if (global_timer() - t_start > kWaitLimitNs) {
-            timed_out = true;
-            break;
-          }
-          __nanosleep(64);
-          continue;
-        }
-        excl += (int64_t)(d & kDescValue);
-        if ((d & ~kDescValue) == kDescIncl) break;
-        --j;
-      }
-      if (timed_out) atomicOr(&a.small->status, kStTimeout);
-      st_relaxed(&desc[c], kDescIncl | (uint64_t)(excl + agg));
+  if (tid < 32) {
+    const int64_t excl = look_back(a.desc, c, agg, a.small);
+    if (tid == 0) {
+      S.prefix = excl;
+      if (c == a.n_chunks - 1) a.small->total = excl + agg;
     }
-    S.prefix = excl;
-    if (c == a.n_chunks - 1) a.small->total = excl + agg;
   }
   __syncthreads();
   const int64_t P = S.prefix;
@@ -803,26 +1047,39 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
   // Ids past the caller's capacity are not written; the call reports it.
   if (tid == 0 && P + (int64_t)agg > a.out_capacity) atomicOr(&a.small->status, kStCapacity);
 
-  // Long pre-tokens: copy from their scratch range of the pool.
-  for (uint32_t x = 0; x < n_long; ++x) {
-    const uint32_t j = S.long_list[x];
-    const int64_t s = c0 + S.span_start[j];
-    const int64_t dst = P + S.span_cnt[j];
-    const uint32_t cnt = S.span_cnt[j + 1] - S.span_cnt[j];
-    for (uint32_t q = tid; q < cnt; q += kThreads)
-      if (dst + q < a.out_capacity) a.out_ids[dst + q] = a.pool[s + q];
-  }
-
-  // Short pre-tokens: ids from shared memory.
-  for (uint32_t j = tid; j < n_spans; j += kThreads) {
-    const int st = S.span_start[j];
-    bool is_long = false;
-    for (uint32_t x = 0; x < n_long; ++x) is_long |= (S.long_list[x] == j);
-    if (is_long) continue;
-    const uint32_t o = S.span_cnt[j], cnt = S.span_cnt[j + 1] - o;
-    const int64_t dst = P + o;
-    for (uint32_t q = 0; q < cnt; ++q)
-      if (dst + q < a.out_capacity) a.out_ids[dst + q] = (int32_t)S.sym[st + q];
+  if (n_long == 0) {
+    // All ids are in shared memory: gather them in output order, then store
+    // them coalesced.
+    for (uint32_t j = tid; j < n_spans; j += kThreads) {
+      const int st = S.span_start[j];
+      const uint32_t o = S.span_cnt[j], cnt = S.span_cnt[j + 1] - o;
+      for (uint32_t q = 0; q < cnt; ++q) S.u.ostage[o + q] = S.sym[st + q];
+    }
+    __syncthreads();
+    const int64_t lim = a.out_capacity - P;
+    for (uint32_t q = tid; q < agg; q += kThreads)
+      if ((int64_t)q < lim) a.out_ids[P + q] = (int32_t)S.u.ostage[q];
+  } else {
+    // Long pre-tokens: copy from their scratch range of the pool.
+    for (uint32_t x = 0; x < n_long; ++x) {
+      const uint32_t j = S.long_list[x];
+      const int64_t s = c0 + S.span_start[j];
+      const int64_t dst = P + S.span_cnt[j];
+      const uint32_t cnt = S.span_cnt[j + 1] - S.span_cnt[j];
+      for (uint32_t q = tid; q < cnt; q += kThreads)
+        if (dst + q < a.out_capacity) a.out_ids[dst + q] = a.pool[s + q];
+    }
+    // Short pre-tokens: ids from shared memory.
+    for (uint32_t j = tid; j < n_spans; j += kThreads) {
+      const int st = S.span_start[j];
+      bool is_long = false;
+      for (uint32_t x = 0; x < n_long; ++x) is_long |= (S.long_list[x] == j);
+      if (is_long) continue;
+      const uint32_t o = S.span_cnt[j], cnt = S.span_cnt[j + 1] - o;
+      const int64_t dst = P + o;
+      for (uint32_t q = 0; q < cnt; ++q)
+        if (dst + q < a.out_capacity) a.out_ids[dst + q] = (int32_t)S.sym[st + q];
+    }
   }
 
   // Offsets of the documents that start in this chunk.
@@ -851,7 +1108,6 @@ __global__ void __launch_bounds__(kThreads) k_pretokenize(const uint8_t* bytes, 
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int64_t c0 = (int64_t)blockIdx.x * kChunk;
-  __shared__ int64_t s_first;
   if (threadIdx.x == 0) {
     int64_t lo = 0, hi = n_docs + 1;
     while (lo < hi) {
@@ -859,10 +1115,10 @@ __global__ void __launch_bounds__(kThreads) k_pretokenize(const uint8_t* bytes, 
       if (doc_offsets[mid] < c0) lo = mid + 1;
       else hi = mid;
     }
-    s_first = lo;
+    S.chunk = lo;
   }
   __syncthreads();
-  load_window(S, bytes, n_bytes, doc_offsets, n_docs, c0, s_first);
+  load_window(S, bytes, n_bytes, doc_offsets, n_docs, c0, S.chunk);
   compute_start_bits(S);
   const int64_t n_words = (n_bytes + 31) / 32;
   for (int w = threadIdx.x; w < kChunk / 32; w += kThreads) {
@@ -870,10 +1126,26 @@ __global__ void __launch_bounds__(kThreads) k_pretokenize(const uint8_t* bytes, 
     if (gw < n_words) {
       uint32_t v = S.startbits[w];
       const int64_t first_bit = gw * 32;
-      if (first_bit + 32 > n_bytes) v &= (n_bytes - first_bit >= 32) ? 0xFFFFFFFFu : ((1u << (n_bytes - first_bit)) - 1u);
+      if (first_bit + 32 > n_bytes) v &= (1u << (n_bytes - first_bit)) - 1u;
       out_bits[gw] = v;
     }
   }
+}
+
+// Word-cache values: the ids of each string, computed by the same merge loop
+// the encoder runs. out[4 i] = count, out[4 i + 1 .. 3] = first three ids.
+__global__ void k_cache_values(const uint8_t* strs, const int64_t* offs, int64_t n, Tables T, uint32_t* out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  uint32_t sym[kCacheMaxLen], rk[kCacheMaxLen];
+  const int len = (int)(offs[i + 1] - offs[i]);
+  if (len < 1 || len > kCacheMaxLen) {
+    out[4 * i] = 0;
+    return;
+  }
+  const int cnt = merge_short(sym, rk, strs + offs[i], len, T, T.byte_id);
+  out[4 * i] = (uint32_t)cnt;
+  for (int q = 0; q < kCacheMaxIds; ++q) out[4 * i + 1 + q] = q < cnt ? sym[q] : 0u;
 }
 
 // ---------------------------------------------------------------- decoding --
@@ -973,9 +1245,9 @@ int cuda_fail(cudaError_t e, const char* what) {
   return fail(BPE_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
-#define CK(call)                                   \
-  do {                                             \
-    cudaError_t e_ = (call);                       \
+#define CK(call)                                        \
+  do {                                                  \
+    cudaError_t e_ = (call);                            \
     if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
   } while (0)
 
@@ -1003,6 +1275,10 @@ struct bpe_handle {
   int32_t* d_byte_id = nullptr;
   uint8_t* d_vbytes = nullptr;
   int64_t* d_voffs = nullptr;
+  uint4* d_cache = nullptr;
+  uint32_t cache_mask = 0;
+  int64_t cache_entries = 0;
+  int cache_enabled = 1;
   DevSmall* d_small = nullptr;
   DevSmall* h_small = nullptr;  // pinned
   void* d_ws = nullptr;
@@ -1037,6 +1313,68 @@ int status_code(uint32_t s) {
   if (s & kStTimeout) return fail(BPE_ERR_TIMEOUT, "a device-side wait gave up");
   if (s & kStCapacity) return fail(BPE_ERR_CAPACITY, "output capacity exceeded");
   if (s & kStInternal) return fail(BPE_ERR_INTERNAL, "device-side consistency check failed");
+  return BPE_OK;
+}
+
+// Word cache: the ids of every vocabulary string of 1..16 bytes, computed on
+// the device by the merge loop, laid out as an open-addressed table (load at
+// most 1/4, linear probing).
+int build_word_cache(bpe_handle* h, const uint8_t* vocab_bytes, const int64_t* vocab_offsets, int64_t n_vocab) {
+  std::vector<uint8_t> strs;
+  std::vector<int64_t> offs{0};
+  for (int64_t id = 0; id < n_vocab; ++id) {
+    const int64_t L = vocab_offsets[id + 1] - vocab_offsets[id];
+    if (L < 1 || L > kCacheMaxLen) continue;
+    strs.insert(strs.end(), vocab_bytes + vocab_offsets[id], vocab_bytes + vocab_offsets[id + 1]);
+    offs.push_back((int64_t)strs.size());
+  }
+  const int64_t n = (int64_t)offs.size() - 1;
+  uint8_t* d_strs = nullptr;
+  int64_t* d_offs = nullptr;
+  uint32_t* d_out = nullptr;
+  std::vector<uint32_t> vals((size_t)std::max<int64_t>(1, n) * 4);
+  cudaError_t e = cudaSuccess;
+  if (n > 0) {
+    e = cudaMalloc(&d_strs, strs.size());
+    if (e == cudaSuccess) e = cudaMalloc(&d_offs, offs.size() * sizeof(int64_t));
+    if (e == cudaSuccess) e = cudaMalloc(&d_out, (size_t)n * 4 * sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemcpy(d_strs, strs.data(), strs.size(), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(d_offs, offs.data(), offs.size() * sizeof(int64_t), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) {
+      Tables T{h->d_ht, h->hmask, h->d_mrows, h->d_byte_id};
+      k_cache_values<<<(unsigned)((n + 127) / 128), 128>>>(d_strs, d_offs, n, T, d_out);
+      e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaMemcpy(vals.data(), d_out, (size_t)n * 4 * sizeof(uint32_t), cudaMemcpyDeviceToHost);
+    cudaFree(d_strs);
+    cudaFree(d_offs);
+    cudaFree(d_out);
+    if (e != cudaSuccess) return cuda_fail(e, "word cache values");
+  }
+  int64_t keep = 0;
+  for (int64_t i = 0; i < n; ++i) keep += (vals[4 * i] >= 1 && vals[4 * i] <= (uint32_t)kCacheMaxIds);
+  uint64_t slots = 16;
+  while (slots < (uint64_t)keep * 4) slots <<= 1;
+  std::vector<uint4> table(slots * 2, make_uint4(0, 0, 0, 0));
+  for (int64_t i = 0; i < n; ++i) {
+    const uint32_t cnt = vals[4 * i];
+    if (cnt < 1 || cnt > (uint32_t)kCacheMaxIds) continue;
+    const uint32_t len = (uint32_t)(offs[i + 1] - offs[i]);
+    uint64_t k0 = 0, k1 = 0;
+    for (uint32_t q = 0; q < len; ++q) {
+      const uint64_t b = strs[(size_t)offs[i] + q];
+      if (q < 8) k0 |= b << (8 * q);
+      else k1 |= b << (8 * (q - 8));
+    }
+    uint64_t slot = cache_hash(k0, k1, len) & (slots - 1);
+    while (table[slot * 2 + 1].x != 0) slot = (slot + 1) & (slots - 1);
+    table[slot * 2] = make_uint4((uint32_t)k0, (uint32_t)(k0 >> 32), (uint32_t)k1, (uint32_t)(k1 >> 32));
+    table[slot * 2 + 1] = make_uint4(len | (cnt << 5) | (1u << 31), vals[4 * i + 1], vals[4 * i + 2], vals[4 * i + 3]);
+  }
+  CK(cudaMalloc(&h->d_cache, table.size() * sizeof(uint4)));
+  CK(cudaMemcpy(h->d_cache, table.data(), table.size() * sizeof(uint4), cudaMemcpyHostToDevice));
+  h->cache_mask = (uint32_t)(slots - 1);
+  h->cache_entries = keep;
   return BPE_OK;
 }
 
@@ -1091,7 +1429,10 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
       for (;;) {
         int slot = -1;
         for (int q = 0; q < 4; ++q)
-          if (ht[bucket * 4 + q] == kEmpty) { slot = q; break; }
+          if (ht[bucket * 4 + q] == kEmpty) {
+            slot = q;
+            break;
+          }
         if (slot >= 0) {
           ht[bucket * 4 + slot] = (key << 20) | (uint64_t)r;
           break;
@@ -1113,11 +1454,10 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
     bpe_destroy(h);
     return code;
   };
-  int rc;
-#define CKB(call)                                                   \
-  do {                                                              \
-    cudaError_t e_ = (call);                                        \
-    if (e_ != cudaSuccess) return cleanup(cuda_fail(e_, #call));    \
+#define CKB(call)                                                \
+  do {                                                           \
+    cudaError_t e_ = (call);                                     \
+    if (e_ != cudaSuccess) return cleanup(cuda_fail(e_, #call)); \
   } while (0)
   CKB(cudaMalloc(&h->d_ht, ht.size() * sizeof(uint64_t)));
   CKB(cudaMemcpy(h->d_ht, ht.data(), ht.size() * sizeof(uint64_t), cudaMemcpyHostToDevice));
@@ -1134,7 +1474,8 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
   CKB(cudaMemset(h->d_small, 0, sizeof(DevSmall)));
   CKB(cudaMallocHost(&h->h_small, sizeof(DevSmall)));
 #undef CKB
-  (void)rc;
+  int rc = build_word_cache(h, vocab_bytes, vocab_offsets, n_vocab);
+  if (rc) return cleanup(rc);
   *out = h;
   return BPE_OK;
 }
@@ -1148,10 +1489,17 @@ int bpe_destroy(bpe_handle* h) {
   cudaFree(h->d_byte_id);
   cudaFree(h->d_vbytes);
   cudaFree(h->d_voffs);
+  cudaFree(h->d_cache);
   cudaFree(h->d_small);
   cudaFree(h->d_ws);
   if (h->h_small) cudaFreeHost(h->h_small);
   delete h;
+  return BPE_OK;
+}
+
+int bpe_set_word_cache(bpe_handle* h, int enable) {
+  if (!h) return fail(BPE_ERR_INVALID_ARG, "null handle");
+  h->cache_enabled = enable ? 1 : 0;
   return BPE_OK;
 }
 
@@ -1188,7 +1536,8 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
   const int64_t n_chunks = n_bytes / kChunk + 1;
-  const size_t need = (size_t)n_chunks * (sizeof(uint64_t) + sizeof(int64_t)) + (size_t)(n_bytes + 4) * sizeof(int32_t);
+  const size_t need =
+      (size_t)n_chunks * (sizeof(uint64_t) + sizeof(int64_t)) + (size_t)(n_bytes + 4) * sizeof(int32_t);
   int rc = ensure_ws(h, need);
   if (rc) return rc;
   uint64_t* desc = (uint64_t*)h->d_ws;
@@ -1196,7 +1545,6 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
   int32_t* pool = (int32_t*)(first_doc + n_chunks);
   if (!h->smem_set) {
     CK(cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
-    CK(cudaFuncSetAttribute(k_pretokenize, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
     h->smem_set = true;
   }
   int prep_blocks = (int)std::min<int64_t>(4096, std::max<int64_t>(n_chunks, n_docs + 1) / 256 + 1);
@@ -1209,9 +1557,10 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
   a.n_docs = n_docs;
   a.out_ids = d_out_ids;
   a.out_capacity = out_capacity;
-  a.pool = pool;
   a.out_offsets = d_out_offsets;
+  a.pool = pool;
   a.T = Tables{h->d_ht, h->hmask, h->d_mrows, h->d_byte_id};
+  a.C = Cache{h->d_cache, h->cache_mask, h->cache_enabled && h->d_cache != nullptr};
   a.desc = desc;
   a.first_doc = first_doc;
   a.small = h->d_small;

@@ -140,6 +140,18 @@ int bpe_decode_batch(bpe_handle* h, const int32_t* d_ids, int64_t n_ids, const i
                      int64_t* h_total_bytes, bpe_stream_t stream);
 
 /*
+ * bpe_set_word_cache — turns the handle's word cache on (default) or off.
+ * The cache is the memo of "Hugging Face Tokenizers v1" (section on word
+ * caching: a given pre-token always yields the same ids, so its ids can be
+ * looked up instead of merged). bpe_build fills it once: every vocabulary
+ * string of 1..16 bytes is run through the device merge loop and its ids
+ * (when at most 3) are stored under its bytes. During encoding a pre-token of
+ * at most 16 bytes found there takes the stored ids; every other pre-token
+ * runs the merge loop. Either setting gives identical ids.
+ */
+int bpe_set_word_cache(bpe_handle* h, int enable);
+
+/*
  * bpe_set_timing_events — measurement hook. When ev_start / ev_stop (two
  * cudaEvent_t created by the caller on the handle's device) are non-NULL, the
  * next bpe_encode_batch calls record ev_start right before the main encode

@@ -43,9 +43,14 @@ def tiny(bpe):
 
 
 def check(handle, orc, data, offsets, label="", n_bytes=None):
-    got = gpu_encode(handle, data, offsets, n_bytes)
+    """GPU ids with the word cache on and off, each equal to the oracle's."""
+    import byte_level_bpe_pretokenize_gb300 as bpe
     want = orc.encode_batch(data, offsets)
-    assert_same_encoding(got, want, data, offsets, label)
+    for cache in (True, False):
+        bpe.bpe_set_word_cache(handle, cache)
+        got = gpu_encode(handle, data, offsets, n_bytes)
+        assert_same_encoding(got, want, data, offsets, f"{label} (word cache {'on' if cache else 'off'})")
+    bpe.bpe_set_word_cache(handle, True)
     return got
 
 
