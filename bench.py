@@ -264,6 +264,22 @@ def run_gpu(args, world, rank, local):
     bpe.bpe_sync_status(handle, s_ptr)
     step_ms = t_start.elapsed_time(t_end) / args.steps
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    # Secondary: the same steps with the word cache off (every pre-token runs
+    # the merge loop), timed the same way, outside the headline region.
+    bpe.bpe_set_word_cache(handle, False)
+    step()
+    nc0, nc1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nc_steps = max(1, min(args.steps, 3))
+    torch.cuda.synchronize()
+    nc0.record(stream)
+    for _ in range(nc_steps):
+        step()
+    nc1.record(stream)
+    torch.cuda.synchronize()
+    nocache_ms = nc0.elapsed_time(nc1) / nc_steps
+    bpe.bpe_set_word_cache(handle, True)
+    bpe.bpe_sync_status(handle, s_ptr)
     if dist:
         t = torch.tensor([step_ms, kern_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -326,6 +342,9 @@ def run_gpu(args, world, rank, local):
             "e2e": {"value": round(all_bytes / e2e_s / 1e6 if world == 1 else n_bytes / e2e_s / 1e6, 3),
                     "unit": "MB/s", "h2d_bytes_per_step": n_bytes + 8 * (n_docs + 1),
                     "d2h_bytes_per_step": 4 * int(n_tokens) + 8 * (n_docs + 1)},
+            "without_word_cache": {"value": round(n_bytes / (nocache_ms / 1e3) / 1e6, 3), "unit": "MB/s",
+                                   "ms_per_step": round(nocache_ms, 4),
+                                   "hbm_frac": round(alg / (nocache_ms / 1e3) / 1e9 / peak, 4)},
             "gpu_launches": 2 * args.steps,
             "clocks": clk,
         }
