@@ -45,6 +45,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <string>
 #include <unordered_set>
@@ -135,6 +136,26 @@ struct DevSmall {
   int64_t total;
 };
 
+// Diagnostic build (-DBPE_ALIGN_CHECK): every vector or reinterpreted access
+// first checks its address; a misaligned one is recorded (site in the top
+// byte, address below) and replaced by byte loads or skipped. The normal
+// build compiles the checks away.
+#ifdef BPE_ALIGN_CHECK
+__device__ unsigned long long g_align_fault = 0;
+__device__ __forceinline__ bool aligned_ok(const void* p, uintptr_t mask, unsigned site) {
+  if (((uintptr_t)p & mask) == 0) return true;
+  atomicCAS(&g_align_fault, 0ull, ((unsigned long long)site << 56) | ((uintptr_t)p & 0xFFFFFFFFFFFFull));
+  return false;
+}
+#define BPE_ALIGNED(p, mask, site) aligned_ok((p), (mask), (site))
+#else
+#define BPE_ALIGNED(p, mask, site) true
+#endif
+
+__device__ __forceinline__ uint32_t ld_u32_bytes(const uint8_t* p) {
+  return (uint32_t)p[0] | (uint32_t)p[1] << 8 | (uint32_t)p[2] << 16 | (uint32_t)p[3] << 24;
+}
+
 // ------------------------------------------------------------ small helpers --
 
 __device__ __forceinline__ uint64_t global_timer() {
@@ -158,6 +179,7 @@ __device__ __forceinline__ uint32_t lookup_rank(const Tables& T, uint32_t a, uin
   uint32_t bucket = pair_hash(a, b) & T.hmask;
   for (uint32_t probe = 0; probe <= T.hmask; ++probe) {
     const ulonglong2* p = reinterpret_cast<const ulonglong2*>(T.ht + 4ull * bucket);
+    if (!BPE_ALIGNED(p, 15u, 7)) return kInf;
     ulonglong2 u = __ldg(p), v = __ldg(p + 1);
     if ((u.x >> 20) == key) return (uint32_t)(u.x & 0xFFFFF);
     if ((u.y >> 20) == key) return (uint32_t)(u.y & 0xFFFFF);
@@ -174,6 +196,7 @@ __device__ __forceinline__ uint32_t cache_lookup(const Cache& C, uint64_t k0, ui
                                                  uint32_t* ids) {
   uint32_t slot = cache_hash(k0, k1, len) & C.mask;
   for (uint32_t probe = 0; probe <= C.mask; ++probe) {
+    if (!BPE_ALIGNED(C.e + 2 * slot, 15u, 6)) return 0;
     const uint4 a = __ldg(C.e + 2 * slot), b = __ldg(C.e + 2 * slot + 1);
     if (b.x == 0) return 0;
     if ((b.x & 31u) == len && a.x == (uint32_t)k0 && a.y == (uint32_t)(k0 >> 32) && a.z == (uint32_t)k1 &&
@@ -405,8 +428,18 @@ __device__ __forceinline__ bool starts_piece_at(const Smem& S, int i) {
 // Start bits of window positions [p0, p0 + 16), p0 a multiple of 16.
 __device__ uint32_t start_mask16(const Smem& S, int p0) {
   const uint32_t* w32 = reinterpret_cast<const uint32_t*>(S.win);
-  const uint4 v = *reinterpret_cast<const uint4*>(S.win + p0);
-  const uint32_t wp = w32[(p0 >> 2) - 1], wn = w32[(p0 >> 2) + 4];
+  uint4 v;
+  uint32_t wp, wn;
+  if (BPE_ALIGNED(S.win + p0, 15u, 4)) {
+    v = *reinterpret_cast<const uint4*>(S.win + p0);
+    wp = w32[(p0 >> 2) - 1];
+    wn = w32[(p0 >> 2) + 4];
+  } else {
+    v = make_uint4(ld_u32_bytes(S.win + p0), ld_u32_bytes(S.win + p0 + 4), ld_u32_bytes(S.win + p0 + 8),
+                   ld_u32_bytes(S.win + p0 + 12));
+    wp = ld_u32_bytes(S.win + p0 - 4);
+    wn = ld_u32_bytes(S.win + p0 + 16);
+  }
   const uint32_t D17 = bits32_at(S.docbits, p0) & 0x1FFFFu;
   const uint32_t O16 = bits32_at(S.outbits, p0) & 0xFFFFu;
   if (O16 == 0xFFFFu) return 0;
@@ -487,7 +520,7 @@ __device__ void load_window(Smem& S, const uint8_t* bytes, int64_t n_bytes, cons
   const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 15u) == 0;
   for (int i = tid * 16; i < kWin; i += kThreads * 16) {
     const int64_t p = w0 + i;
-    if (aligned && p >= 0 && p + 16 <= n_bytes) {
+    if (aligned && p >= 0 && p + 16 <= n_bytes && BPE_ALIGNED(bytes + p, 15u, 2) && BPE_ALIGNED(S.win + i, 15u, 3)) {
       *reinterpret_cast<uint4*>(S.win + i) = __ldg(reinterpret_cast<const uint4*>(bytes + p));
     } else {
 #pragma unroll
@@ -759,7 +792,17 @@ __device__ __forceinline__ uint32_t encode_short(Smem& S, int st, int len, const
   if (C.enabled && len <= kCacheMaxLen) {
     const uint64_t* w64 = reinterpret_cast<const uint64_t*>(S.win);
     const int wi = ws >> 3, sh = (ws & 7) * 8;
-    const uint64_t a = w64[wi], b = w64[wi + 1], c = w64[wi + 2];
+    uint64_t a, b, c;
+    if (BPE_ALIGNED(w64 + wi, 7u, 5)) {
+      a = w64[wi];
+      b = w64[wi + 1];
+      c = w64[wi + 2];
+    } else {
+      const uint8_t* q = S.win + 8 * wi;
+      a = ld_u32_bytes(q) | (uint64_t)ld_u32_bytes(q + 4) << 32;
+      b = ld_u32_bytes(q + 8) | (uint64_t)ld_u32_bytes(q + 12) << 32;
+      c = ld_u32_bytes(q + 16) | (uint64_t)ld_u32_bytes(q + 20) << 32;
+    }
     uint64_t k0 = sh ? (a >> sh) | (b << (64 - sh)) : a;
     uint64_t k1 = sh ? (b >> sh) | (c << (64 - sh)) : b;
     if (len < 8) {
@@ -844,7 +887,7 @@ __device__ int64_t look_back(uint64_t* desc, int64_t c, uint32_t agg, DevSmall* 
   bool timed_out = false;
   for (;;) {
     const int64_t j = base - lane;
-    const uint64_t d = j >= 0 ? ld_relaxed(&desc[j]) : kDescIncl;
+    const uint64_t d = j >= 0 ? (BPE_ALIGNED(&desc[j], 7u, 8) ? ld_relaxed(&desc[j]) : kDescIncl) : kDescIncl;
     const uint32_t ready = __ballot_sync(0xFFFFFFFFu, (d & ~kDescValue) != 0);
     const uint32_t incl = __ballot_sync(0xFFFFFFFFu, (d & ~kDescValue) == kDescIncl);
     // Lanes up to and including the nearest inclusive one must be ready.
@@ -879,7 +922,10 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
 
-  if (tid == 0) S.chunk = (int64_t)atomicAdd(&a.small->ticket, 1u);
+  if (tid == 0) {
+    (void)BPE_ALIGNED(smem_raw, 15u, 1);
+    S.chunk = (int64_t)atomicAdd(&a.small->ticket, 1u);
+  }
   for (int i = tid; i < 256; i += kThreads) S.byte_id[i] = a.T.byte_id[i];
   __syncthreads();
   const int64_t c = S.chunk;
@@ -1309,6 +1355,16 @@ int read_status(bpe_handle* h, cudaStream_t st, DevSmall* out) {
 }
 
 int status_code(uint32_t s) {
+#ifdef BPE_ALIGN_CHECK
+  unsigned long long f = 0;
+  cudaMemcpyFromSymbol(&f, g_align_fault, sizeof(f));
+  if (f) {
+    char buf[96];
+    snprintf(buf, sizeof buf, "misaligned access at site %u, address low bits 0x%llx", (unsigned)(f >> 56),
+             f & 0xFFFFFFFFFFFFull);
+    return fail(BPE_ERR_INTERNAL, buf);
+  }
+#endif
   if (s & kStBadInput) return fail(BPE_ERR_BAD_INPUT, "offsets not monotone or outside the buffer, or an id out of range");
   if (s & kStTimeout) return fail(BPE_ERR_TIMEOUT, "a device-side wait gave up");
   if (s & kStCapacity) return fail(BPE_ERR_CAPACITY, "output capacity exceeded");
