@@ -136,25 +136,6 @@ struct DevSmall {
   int64_t total;
 };
 
-// Diagnostic build (-DBPE_ALIGN_CHECK): every vector or reinterpreted access
-// first checks its address; a misaligned one is recorded (site in the top
-// byte, address below) and replaced by byte loads or skipped. The normal
-// build compiles the checks away.
-#ifdef BPE_ALIGN_CHECK
-__device__ unsigned long long g_align_fault = 0;
-__device__ __forceinline__ bool aligned_ok(const void* p, uintptr_t mask, unsigned site) {
-  if (((uintptr_t)p & mask) == 0) return true;
-  atomicCAS(&g_align_fault, 0ull, ((unsigned long long)site << 56) | ((uintptr_t)p & 0xFFFFFFFFFFFFull));
-  return false;
-}
-#define BPE_ALIGNED(p, mask, site) aligned_ok((p), (mask), (site))
-#else
-#define BPE_ALIGNED(p, mask, site) true
-#endif
-
-__device__ __forceinline__ uint32_t ld_u32_bytes(const uint8_t* p) {
-  return (uint32_t)p[0] | (uint32_t)p[1] << 8 | (uint32_t)p[2] << 16 | (uint32_t)p[3] << 24;
-}
 
 // ------------------------------------------------------------ small helpers --
 
@@ -179,7 +160,6 @@ __device__ __forceinline__ uint32_t lookup_rank(const Tables& T, uint32_t a, uin
   uint32_t bucket = pair_hash(a, b) & T.hmask;
   for (uint32_t probe = 0; probe <= T.hmask; ++probe) {
     const ulonglong2* p = reinterpret_cast<const ulonglong2*>(T.ht + 4ull * bucket);
-    if (!BPE_ALIGNED(p, 15u, 7)) return kInf;
     ulonglong2 u = __ldg(p), v = __ldg(p + 1);
     if ((u.x >> 20) == key) return (uint32_t)(u.x & 0xFFFFF);
     if ((u.y >> 20) == key) return (uint32_t)(u.y & 0xFFFFF);
@@ -196,7 +176,6 @@ __device__ __forceinline__ uint32_t cache_lookup(const Cache& C, uint64_t k0, ui
                                                  uint32_t* ids) {
   uint32_t slot = cache_hash(k0, k1, len) & C.mask;
   for (uint32_t probe = 0; probe <= C.mask; ++probe) {
-    if (!BPE_ALIGNED(C.e + 2 * slot, 15u, 6)) return 0;
     const uint4 a = __ldg(C.e + 2 * slot), b = __ldg(C.e + 2 * slot + 1);
     if (b.x == 0) return 0;
     if ((b.x & 31u) == len && a.x == (uint32_t)k0 && a.y == (uint32_t)(k0 >> 32) && a.z == (uint32_t)k1 &&
@@ -380,7 +359,10 @@ __device__ __forceinline__ uint32_t bits32_at(const uint32_t* bits, int start) {
 namespace {
 
 struct Smem {
-  uint8_t win[kWin + 16];
+  union {
+    uint8_t win[kWin + 16];
+    uint32_t win32[(kWin + 16) / 4];
+  };
   uint32_t docbits[kWinWords + 2];   // a document (or the area after the last one) starts here
   uint32_t outbits[kWinWords + 2];   // byte belongs to no document
   uint32_t startbits[kSpanWords];
@@ -427,19 +409,15 @@ __device__ __forceinline__ bool starts_piece_at(const Smem& S, int i) {
 
 // Start bits of window positions [p0, p0 + 16), p0 a multiple of 16.
 __device__ uint32_t start_mask16(const Smem& S, int p0) {
-  const uint32_t* w32 = reinterpret_cast<const uint32_t*>(S.win);
+  // The window is read as 32-bit words only.
+  const uint32_t* w32 = S.win32;
+  const int wq = p0 >> 2;
   uint4 v;
-  uint32_t wp, wn;
-  if (BPE_ALIGNED(S.win + p0, 15u, 4)) {
-    v = *reinterpret_cast<const uint4*>(S.win + p0);
-    wp = w32[(p0 >> 2) - 1];
-    wn = w32[(p0 >> 2) + 4];
-  } else {
-    v = make_uint4(ld_u32_bytes(S.win + p0), ld_u32_bytes(S.win + p0 + 4), ld_u32_bytes(S.win + p0 + 8),
-                   ld_u32_bytes(S.win + p0 + 12));
-    wp = ld_u32_bytes(S.win + p0 - 4);
-    wn = ld_u32_bytes(S.win + p0 + 16);
-  }
+  v.x = w32[wq];
+  v.y = w32[wq + 1];
+  v.z = w32[wq + 2];
+  v.w = w32[wq + 3];
+  const uint32_t wp = w32[wq - 1], wn = w32[wq + 4];
   const uint32_t D17 = bits32_at(S.docbits, p0) & 0x1FFFFu;
   const uint32_t O16 = bits32_at(S.outbits, p0) & 0xFFFFu;
   if (O16 == 0xFFFFu) return 0;
@@ -517,11 +495,14 @@ __device__ void load_window(Smem& S, const uint8_t* bytes, int64_t n_bytes, cons
                             int64_t n_docs, int64_t c0, int64_t first_doc) {
   const int tid = threadIdx.x;
   const int64_t w0 = c0 - kHalo;
-  const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 15u) == 0;
+  // 32-bit word loads when the input is word aligned, bytes otherwise.
+  const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 3u) == 0;
+  const uint32_t* g32 = reinterpret_cast<const uint32_t*>(bytes);
   for (int i = tid * 16; i < kWin; i += kThreads * 16) {
     const int64_t p = w0 + i;
-    if (aligned && p >= 0 && p + 16 <= n_bytes && BPE_ALIGNED(bytes + p, 15u, 2) && BPE_ALIGNED(S.win + i, 15u, 3)) {
-      *reinterpret_cast<uint4*>(S.win + i) = __ldg(reinterpret_cast<const uint4*>(bytes + p));
+    if (aligned && p >= 0 && p + 16 <= n_bytes) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) S.win32[(i >> 2) + k] = __ldg(g32 + (p >> 2) + k);
     } else {
 #pragma unroll
       for (int k = 0; k < 16; ++k) S.win[i + k] = (p + k >= 0 && p + k < n_bytes) ? bytes[p + k] : 0;
@@ -790,21 +771,14 @@ __device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, in
 __device__ __forceinline__ uint32_t encode_short(Smem& S, int st, int len, const Tables& T, const Cache& C) {
   const int ws = kHalo + st;
   if (C.enabled && len <= kCacheMaxLen) {
-    const uint64_t* w64 = reinterpret_cast<const uint64_t*>(S.win);
-    const int wi = ws >> 3, sh = (ws & 7) * 8;
-    uint64_t a, b, c;
-    if (BPE_ALIGNED(w64 + wi, 7u, 5)) {
-      a = w64[wi];
-      b = w64[wi + 1];
-      c = w64[wi + 2];
-    } else {
-      const uint8_t* q = S.win + 8 * wi;
-      a = ld_u32_bytes(q) | (uint64_t)ld_u32_bytes(q + 4) << 32;
-      b = ld_u32_bytes(q + 8) | (uint64_t)ld_u32_bytes(q + 12) << 32;
-      c = ld_u32_bytes(q + 16) | (uint64_t)ld_u32_bytes(q + 20) << 32;
-    }
-    uint64_t k0 = sh ? (a >> sh) | (b << (64 - sh)) : a;
-    uint64_t k1 = sh ? (b >> sh) | (c << (64 - sh)) : b;
+    // The pre-token's 16 bytes from five 32-bit window words.
+    const int wi = ws >> 2, sh = (ws & 3) * 8;
+    const uint32_t w0 = S.win32[wi], w1 = S.win32[wi + 1], w2 = S.win32[wi + 2], w3 = S.win32[wi + 3],
+                   w4 = S.win32[wi + 4];
+    const uint32_t b0 = __funnelshift_r(w0, w1, sh), b1 = __funnelshift_r(w1, w2, sh),
+                   b2 = __funnelshift_r(w2, w3, sh), b3 = __funnelshift_r(w3, w4, sh);
+    uint64_t k0 = (uint64_t)b0 | (uint64_t)b1 << 32;
+    uint64_t k1 = (uint64_t)b2 | (uint64_t)b3 << 32;
     if (len < 8) {
       k0 &= (1ull << (8 * len)) - 1ull;
       k1 = 0;
@@ -887,7 +861,7 @@ __device__ int64_t look_back(uint64_t* desc, int64_t c, uint32_t agg, DevSmall* 
   bool timed_out = false;
   for (;;) {
     const int64_t j = base - lane;
-    const uint64_t d = j >= 0 ? (BPE_ALIGNED(&desc[j], 7u, 8) ? ld_relaxed(&desc[j]) : kDescIncl) : kDescIncl;
+    const uint64_t d = j >= 0 ? ld_relaxed(&desc[j]) : kDescIncl;
     const uint32_t ready = __ballot_sync(0xFFFFFFFFu, (d & ~kDescValue) != 0);
     const uint32_t incl = __ballot_sync(0xFFFFFFFFu, (d & ~kDescValue) == kDescIncl);
     // Lanes up to and including the nearest inclusive one must be ready.
@@ -922,10 +896,7 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
 
-  if (tid == 0) {
-    (void)BPE_ALIGNED(smem_raw, 15u, 1);
-    S.chunk = (int64_t)atomicAdd(&a.small->ticket, 1u);
-  }
+  if (tid == 0) S.chunk = (int64_t)atomicAdd(&a.small->ticket, 1u);
   for (int i = tid; i < 256; i += kThreads) S.byte_id[i] = a.T.byte_id[i];
   __syncthreads();
   const int64_t c = S.chunk;
@@ -1355,16 +1326,6 @@ int read_status(bpe_handle* h, cudaStream_t st, DevSmall* out) {
 }
 
 int status_code(uint32_t s) {
-#ifdef BPE_ALIGN_CHECK
-  unsigned long long f = 0;
-  cudaMemcpyFromSymbol(&f, g_align_fault, sizeof(f));
-  if (f) {
-    char buf[96];
-    snprintf(buf, sizeof buf, "misaligned access at site %u, address low bits 0x%llx", (unsigned)(f >> 56),
-             f & 0xFFFFFFFFFFFFull);
-    return fail(BPE_ERR_INTERNAL, buf);
-  }
-#endif
   if (s & kStBadInput) return fail(BPE_ERR_BAD_INPUT, "offsets not monotone or outside the buffer, or an id out of range");
   if (s & kStTimeout) return fail(BPE_ERR_TIMEOUT, "a device-side wait gave up");
   if (s & kStCapacity) return fail(BPE_ERR_CAPACITY, "output capacity exceeded");
@@ -1589,6 +1550,9 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
     return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch: bad arguments");
   if (out_capacity < 0 || (out_capacity > 0 && !d_out_ids))
     return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch: bad output buffer");
+  if ((reinterpret_cast<uintptr_t>(d_doc_offsets) & 7u) || (reinterpret_cast<uintptr_t>(d_out_offsets) & 7u) ||
+      (reinterpret_cast<uintptr_t>(d_out_ids) & 3u))
+    return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch: offsets must be 8-byte and ids 4-byte aligned");
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
   const int64_t n_chunks = n_bytes / kChunk + 1;
@@ -1660,6 +1624,9 @@ int bpe_decode_batch(bpe_handle* h, const int32_t* d_ids, int64_t n_ids, const i
   if (!h || !d_id_offsets || !d_out_byte_offsets || n_ids < 0 || n_docs < 0 || out_capacity < 0 ||
       (n_ids > 0 && !d_ids) || (out_capacity > 0 && !d_out_bytes))
     return fail(BPE_ERR_INVALID_ARG, "bpe_decode_batch: bad arguments");
+  if ((reinterpret_cast<uintptr_t>(d_id_offsets) & 7u) || (reinterpret_cast<uintptr_t>(d_out_byte_offsets) & 7u) ||
+      (reinterpret_cast<uintptr_t>(d_ids) & 3u))
+    return fail(BPE_ERR_INVALID_ARG, "bpe_decode_batch: offsets must be 8-byte and ids 4-byte aligned");
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
   const int64_t n_blocks = n_ids / kScanBlock + 1;
