@@ -359,10 +359,7 @@ __device__ __forceinline__ uint32_t bits32_at(const uint32_t* bits, int start) {
 namespace {
 
 struct Smem {
-  union {
-    uint8_t win[kWin + 16];
-    uint32_t win32[(kWin + 16) / 4];
-  };
+  uint8_t win[kWin + 16];
   uint32_t docbits[kWinWords + 2];   // a document (or the area after the last one) starts here
   uint32_t outbits[kWinWords + 2];   // byte belongs to no document
   uint32_t startbits[kSpanWords];
@@ -388,6 +385,20 @@ struct Smem {
 
 __device__ __forceinline__ bool bit_at(const uint32_t* bits, int i) { return (bits[i >> 5] >> (i & 31)) & 1u; }
 
+// One window byte through an explicit byte-wide shared load, so that words
+// assembled from several of them are never turned into wider loads.
+__device__ __forceinline__ uint32_t win_byte(const Smem& S, int b) {
+  uint32_t v;
+  const unsigned addr = (unsigned)__cvta_generic_to_shared(S.win + b);
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// Window bytes [b, b + 4) as a little-endian word.
+__device__ __forceinline__ uint32_t win_word(const Smem& S, int b) {
+  return win_byte(S, b) | win_byte(S, b + 1) << 8 | win_byte(S, b + 2) << 16 | win_byte(S, b + 3) << 24;
+}
+
 // Document bounds [lo, hi) around window index i: the nearest document edge at
 // or before i and the next one after i (at most kHalo away is all that is
 // read), or the window edges.
@@ -409,15 +420,13 @@ __device__ __forceinline__ bool starts_piece_at(const Smem& S, int i) {
 
 // Start bits of window positions [p0, p0 + 16), p0 a multiple of 16.
 __device__ uint32_t start_mask16(const Smem& S, int p0) {
-  // The window is read as 32-bit words only.
-  const uint32_t* w32 = S.win32;
-  const int wq = p0 >> 2;
+  // The window is read with byte loads; words are assembled in registers.
   uint4 v;
-  v.x = w32[wq];
-  v.y = w32[wq + 1];
-  v.z = w32[wq + 2];
-  v.w = w32[wq + 3];
-  const uint32_t wp = w32[wq - 1], wn = w32[wq + 4];
+  v.x = win_word(S, p0);
+  v.y = win_word(S, p0 + 4);
+  v.z = win_word(S, p0 + 8);
+  v.w = win_word(S, p0 + 12);
+  const uint32_t wp = win_word(S, p0 - 4), wn = win_word(S, p0 + 16);
   const uint32_t D17 = bits32_at(S.docbits, p0) & 0x1FFFFu;
   const uint32_t O16 = bits32_at(S.outbits, p0) & 0xFFFFu;
   if (O16 == 0xFFFFu) return 0;
@@ -502,7 +511,11 @@ __device__ void load_window(Smem& S, const uint8_t* bytes, int64_t n_bytes, cons
     const int64_t p = w0 + i;
     if (aligned && p >= 0 && p + 16 <= n_bytes) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) S.win32[(i >> 2) + k] = __ldg(g32 + (p >> 2) + k);
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t w = __ldg(g32 + (p >> 2) + k);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) S.win[i + 4 * k + q] = (uint8_t)(w >> (8 * q));
+      }
     } else {
 #pragma unroll
       for (int k = 0; k < 16; ++k) S.win[i + k] = (p + k >= 0 && p + k < n_bytes) ? bytes[p + k] : 0;
@@ -771,14 +784,9 @@ __device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, in
 __device__ __forceinline__ uint32_t encode_short(Smem& S, int st, int len, const Tables& T, const Cache& C) {
   const int ws = kHalo + st;
   if (C.enabled && len <= kCacheMaxLen) {
-    // The pre-token's 16 bytes from five 32-bit window words.
-    const int wi = ws >> 2, sh = (ws & 3) * 8;
-    const uint32_t w0 = S.win32[wi], w1 = S.win32[wi + 1], w2 = S.win32[wi + 2], w3 = S.win32[wi + 3],
-                   w4 = S.win32[wi + 4];
-    const uint32_t b0 = __funnelshift_r(w0, w1, sh), b1 = __funnelshift_r(w1, w2, sh),
-                   b2 = __funnelshift_r(w2, w3, sh), b3 = __funnelshift_r(w3, w4, sh);
-    uint64_t k0 = (uint64_t)b0 | (uint64_t)b1 << 32;
-    uint64_t k1 = (uint64_t)b2 | (uint64_t)b3 << 32;
+    // The pre-token's first 16 window bytes, little-endian.
+    uint64_t k0 = (uint64_t)win_word(S, ws) | (uint64_t)win_word(S, ws + 4) << 32;
+    uint64_t k1 = (uint64_t)win_word(S, ws + 8) | (uint64_t)win_word(S, ws + 12) << 32;
     if (len < 8) {
       k0 &= (1ull << (8 * len)) - 1ull;
       k1 = 0;
