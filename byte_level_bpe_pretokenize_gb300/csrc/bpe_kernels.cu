@@ -346,10 +346,20 @@ __device__ __forceinline__ bool has_byte(uint32_t w, uint32_t b) {
   return ((y - 0x01010101u) & ~y & 0x80808080u) != 0;
 }
 
-struct Smem;
+// A 32-bit shared-memory load the compiler must issue as written. Merging a
+// shift-or of two adjacent word loads into one load at a 2-byte offset is a
+// misaligned 32-bit shared access on the GPU (it faults), so every such
+// combination below reads its words through this.
+__device__ __forceinline__ uint32_t lds_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"((unsigned)__cvta_generic_to_shared(p)));
+  return v;
+}
+
+// Bits [start, start + 32) of a shared bit array.
 __device__ __forceinline__ uint32_t bits32_at(const uint32_t* bits, int start) {
   const int w = start >> 5, sh = start & 31;
-  return __funnelshift_r(bits[w], bits[w + 1], sh);
+  return __funnelshift_r(lds_u32(bits + w), lds_u32(bits + w + 1), sh);
 }
 
 }  // namespace
@@ -420,13 +430,14 @@ __device__ __forceinline__ bool starts_piece_at(const Smem& S, int i) {
 
 // Start bits of window positions [p0, p0 + 16), p0 a multiple of 16.
 __device__ uint32_t start_mask16(const Smem& S, int p0) {
-  // The window is read with byte loads; words are assembled in registers.
+  // Six aligned window words (p0 is a multiple of 16).
+  const uint32_t* w32 = reinterpret_cast<const uint32_t*>(S.win + p0);
   uint4 v;
-  v.x = win_word(S, p0);
-  v.y = win_word(S, p0 + 4);
-  v.z = win_word(S, p0 + 8);
-  v.w = win_word(S, p0 + 12);
-  const uint32_t wp = win_word(S, p0 - 4), wn = win_word(S, p0 + 16);
+  v.x = lds_u32(w32);
+  v.y = lds_u32(w32 + 1);
+  v.z = lds_u32(w32 + 2);
+  v.w = lds_u32(w32 + 3);
+  const uint32_t wp = lds_u32(w32 - 1), wn = lds_u32(w32 + 4);
   const uint32_t D17 = bits32_at(S.docbits, p0) & 0x1FFFFu;
   const uint32_t O16 = bits32_at(S.outbits, p0) & 0xFFFFu;
   if (O16 == 0xFFFFu) return 0;
