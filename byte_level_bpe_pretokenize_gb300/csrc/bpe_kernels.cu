@@ -859,6 +859,7 @@ struct EncodeArgs {
   int32_t* pool;  // long pre-token scratch, one int32 per input byte
   Tables T;
   Cache C;
+  const uint32_t* start_bits;  // pre-token start bitmask of all n_bytes
   uint64_t* desc;
   const int64_t* first_doc;
   DevSmall* small;
@@ -921,7 +922,15 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
   const int64_t c = S.chunk;
   const int64_t c0 = c * kChunk;
   load_window(S, a.bytes, a.n_bytes, a.doc_offsets, a.n_docs, c0, a.first_doc[c]);
-  compute_start_bits(S);
+  {
+    // Start bits of [c0, c0 + kSpan) from the split kernel's bitmask.
+    const int64_t n_words = (a.n_bytes + 31) / 32;
+    for (int w = tid; w < kSpanWords; w += kThreads) {
+      const int64_t gw = c0 / 32 + w;
+      S.startbits[w] = gw < n_words ? a.start_bits[gw] : 0u;
+    }
+    __syncthreads();
+  }
 
   // Pre-tokens starting in the chunk, in order. Thread t owns positions
   // [16 t, 16 t + 16) of the chunk.
@@ -1575,15 +1584,18 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
   const int64_t n_chunks = n_bytes / kChunk + 1;
-  const size_t need =
-      (size_t)n_chunks * (sizeof(uint64_t) + sizeof(int64_t)) + (size_t)(n_bytes + 4) * sizeof(int32_t);
+  const int64_t n_words = (n_bytes + 31) / 32;
+  const size_t need = (size_t)n_chunks * (sizeof(uint64_t) + sizeof(int64_t)) +
+                      (size_t)(n_bytes + 4) * sizeof(int32_t) + (size_t)(n_words + 4) * sizeof(uint32_t);
   int rc = ensure_ws(h, need);
   if (rc) return rc;
   uint64_t* desc = (uint64_t*)h->d_ws;
   int64_t* first_doc = (int64_t*)(desc + n_chunks);
   int32_t* pool = (int32_t*)(first_doc + n_chunks);
+  uint32_t* bits = (uint32_t*)(pool + n_bytes + 4);
   if (!h->smem_set) {
     CK(cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
+    CK(cudaFuncSetAttribute(k_pretokenize, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
     h->smem_set = true;
   }
   int prep_blocks = (int)std::min<int64_t>(4096, std::max<int64_t>(n_chunks, n_docs + 1) / 256 + 1);
@@ -1600,11 +1612,17 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
   a.pool = pool;
   a.T = Tables{h->d_ht, h->hmask, h->d_mrows, h->d_byte_id};
   a.C = Cache{h->d_cache, h->cache_mask, h->cache_enabled && h->d_cache != nullptr};
+  a.start_bits = bits;
   a.desc = desc;
   a.first_doc = first_doc;
   a.small = h->d_small;
   a.n_chunks = n_chunks;
   if (h->ev_start) CK(cudaEventRecord(h->ev_start, st));
+  if (n_bytes > 0) {
+    k_pretokenize<<<(unsigned)((n_bytes + kChunk - 1) / kChunk), kThreads, sizeof(Smem), st>>>(
+        d_bytes, n_bytes, d_doc_offsets, n_docs, bits);
+    CK(cudaGetLastError());
+  }
   k_encode<<<(unsigned)n_chunks, kThreads, sizeof(Smem), st>>>(a);
   CK(cudaGetLastError());
   if (h->ev_stop) CK(cudaEventRecord(h->ev_stop, st));
