@@ -1149,18 +1149,22 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
 // Pre-tokenizer alone: start bits of [c0, c0 + kChunk) for chunk blockIdx.x.
 __global__ void __launch_bounds__(kThreads) k_pretokenize(const uint8_t* bytes, int64_t n_bytes,
                                                           const int64_t* doc_offsets, int64_t n_docs,
-                                                          uint32_t* out_bits) {
+                                                          const int64_t* first_doc, uint32_t* out_bits) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int64_t c0 = (int64_t)blockIdx.x * kChunk;
   if (threadIdx.x == 0) {
-    int64_t lo = 0, hi = n_docs + 1;
-    while (lo < hi) {
-      int64_t mid = (lo + hi) >> 1;
-      if (doc_offsets[mid] < c0) lo = mid + 1;
-      else hi = mid;
+    if (first_doc) {
+      S.chunk = first_doc[blockIdx.x];  // from k_prep
+    } else {
+      int64_t lo = 0, hi = n_docs + 1;
+      while (lo < hi) {
+        int64_t mid = (lo + hi) >> 1;
+        if (doc_offsets[mid] < c0) lo = mid + 1;
+        else hi = mid;
+      }
+      S.chunk = lo;
     }
-    S.chunk = lo;
   }
   __syncthreads();
   load_window(S, bytes, n_bytes, doc_offsets, n_docs, c0, S.chunk);
@@ -1620,7 +1624,7 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
   if (h->ev_start) CK(cudaEventRecord(h->ev_start, st));
   if (n_bytes > 0) {
     k_pretokenize<<<(unsigned)((n_bytes + kChunk - 1) / kChunk), kThreads, sizeof(Smem), st>>>(
-        d_bytes, n_bytes, d_doc_offsets, n_docs, bits);
+        d_bytes, n_bytes, d_doc_offsets, n_docs, first_doc, bits);
     CK(cudaGetLastError());
   }
   k_encode<<<(unsigned)n_chunks, kThreads, sizeof(Smem), st>>>(a);
@@ -1650,7 +1654,7 @@ int bpe_pretokenize_batch(const uint8_t* d_bytes, int64_t n_bytes, const int64_t
   }
   const int64_t n_chunks = (n_bytes + kChunk - 1) / kChunk;
   k_pretokenize<<<(unsigned)n_chunks, kThreads, sizeof(Smem), (cudaStream_t)stream>>>(d_bytes, n_bytes, d_doc_offsets,
-                                                                                      n_docs, d_start_bits);
+                                                                                      n_docs, nullptr, d_start_bits);
   CK(cudaGetLastError());
   return BPE_OK;
 }
