@@ -74,6 +74,7 @@ constexpr int kCacheMaxIds = 3;       // most ids a cache entry holds
 constexpr int kLongPerThread = 4;     // elements per thread per round of the CTA merge
 constexpr int kRound = kThreads * kLongPerThread;
 constexpr int kMaxLong = kChunk / kShortMax + 2;
+constexpr uint32_t kMissCap = 2 * kSpanWords;  // queued word-cache misses per chunk
 constexpr uint32_t kInf = 0xFFFFFFFFu;
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 constexpr uint64_t kEmpty = ~0ull;
@@ -341,11 +342,6 @@ __device__ __forceinline__ Ascii4 ascii_classes(uint32_t w) {
 // 0x80-per-byte mask of a word -> 4 bits (byte j -> bit j).
 __device__ __forceinline__ uint32_t movemask4(uint32_t m) { return ((m >> 7) * 0x01020408u) >> 24; }
 
-__device__ __forceinline__ bool has_byte(uint32_t w, uint32_t b) {
-  const uint32_t y = w ^ (b * 0x01010101u);
-  return ((y - 0x01010101u) & ~y & 0x80808080u) != 0;
-}
-
 // A 32-bit shared-memory load the compiler must issue as written. Merging a
 // shift-or of two adjacent word loads into one load at a 2-byte offset is a
 // misaligned 32-bit shared access on the GPU (it faults), so every such
@@ -372,7 +368,10 @@ struct Smem {
   uint8_t win[kWin + 16];
   uint32_t docbits[kWinWords + 2];   // a document (or the area after the last one) starts here
   uint32_t outbits[kWinWords + 2];   // byte belongs to no document
-  uint32_t startbits[kSpanWords];
+  union {
+    uint32_t startbits[kSpanWords];
+    uint16_t missq[2 * kSpanWords];  // word-cache misses, once the start bits are consumed
+  };
   uint16_t span_start[kChunk + 1];
   uint32_t span_cnt[kChunk + 1];     // token counts, then exclusive offsets
   uint32_t sym[kSpan];               // ids of short pre-tokens, at their start position
@@ -389,6 +388,7 @@ struct Smem {
   int64_t prefix;
   uint32_t n_spans;
   uint32_t n_long;
+  uint32_t n_miss;
   int64_t last_end;
   int64_t doc_lo, doc_hi;  // document of a long pre-token that runs past the window
 };
@@ -428,44 +428,76 @@ __device__ __forceinline__ bool starts_piece_at(const Smem& S, int i) {
   return starts_piece<int>(S.win, lo, hi, i);
 }
 
+// Boundary rules on class masks. Bit k of every mask is window byte
+// p0 - 8 + k; the result is bits 8..23 (positions p0 .. p0 + 15). U marks unit
+// starts, L / N / S the class of the unit holding each byte, SP bytes equal to
+// U+0020, AP apostrophes, D document edges, O bytes outside every document.
+// B2 and B3 come from the masks directly. Contractions (B0 / B1) are resolved
+// per apostrophe: it starts a contraction when it is eligible (document start,
+// or the unit before it is a letter, a number or whitespace other than
+// U+0020) and the next one or two bytes of its document are a suffix; then
+// the byte after it gets no boundary (B0) and the byte after the suffix gets
+// one (B1).
+__device__ __forceinline__ uint32_t boundaries16(const Smem& S, int p0, uint32_t U, uint32_t L, uint32_t N,
+                                                 uint32_t Sm, uint32_t SP, uint32_t AP, uint32_t D, uint32_t O) {
+  const uint32_t Sp = Sm << 1, Lp = L << 1, Np = N << 1, SPp = SP << 1;
+  const uint32_t Sn = Sm >> 1, Dn = D >> 1;
+  const uint32_t B2 = Sm & (~Sp | (~Sn & ~Dn));
+  const uint32_t B3 = ~Sm & ~SPp & (Sp | (L ^ Lp) | (N ^ Np));
+  uint32_t base = D | B2 | B3;
+  uint32_t ap = AP & 0x007FFFE0u;  // apostrophes at bytes p0 - 3 .. p0 + 14
+  if (ap) {
+    const uint32_t prev_ok = (L | N | (Sm & ~SP)) << 1;  // bit k: byte k - 1 makes an apostrophe at k eligible
+    uint32_t B0 = 0, B1 = 0;
+    while (ap) {
+      const int k = __ffs(ap) - 1;
+      ap &= ap - 1;
+      if (!(((D | prev_ok) >> k) & 1u) || ((D >> (k + 1)) & 1u)) continue;
+      const int q = p0 - 8 + k;
+      const uint32_t b1 = S.win[q + 1];
+      if (is_stmd(b1)) {
+        B0 |= 1u << (k + 1);
+        B1 |= 1u << (k + 2);
+      } else if (!((D >> (k + 2)) & 1u) && is_suffix2(b1, S.win[q + 2])) {
+        B0 |= 1u << (k + 1);
+        B1 |= 1u << (k + 3);
+      }
+    }
+    base = (base & ~B0) | B1;
+  }
+  return ((U & ~O & base) >> 8) & 0xFFFFu;
+}
+
 // Start bits of window positions [p0, p0 + 16), p0 a multiple of 16.
 __device__ uint32_t start_mask16(const Smem& S, int p0) {
-  // Six aligned window words (p0 is a multiple of 16).
+  const uint32_t D = bits32_at(S.docbits, p0 - 8), O = bits32_at(S.outbits, p0 - 8);
+  if (((O >> 8) & 0xFFFFu) == 0xFFFFu) return 0;
+  // Six aligned window words: bytes p0 - 4 .. p0 + 19 (p0 is a multiple of 16).
   const uint32_t* w32 = reinterpret_cast<const uint32_t*>(S.win + p0);
-  uint4 v;
-  v.x = lds_u32(w32);
-  v.y = lds_u32(w32 + 1);
-  v.z = lds_u32(w32 + 2);
-  v.w = lds_u32(w32 + 3);
-  const uint32_t wp = lds_u32(w32 - 1), wn = lds_u32(w32 + 4);
-  const uint32_t D17 = bits32_at(S.docbits, p0) & 0x1FFFFu;
-  const uint32_t O16 = bits32_at(S.outbits, p0) & 0xFFFFu;
-  if (O16 == 0xFFFFu) return 0;
-  const uint32_t any = v.x | v.y | v.z | v.w | wp | wn;
-  const bool apos = has_byte(wp, '\'') || has_byte(v.x, '\'') || has_byte(v.y, '\'') || has_byte(v.z, '\'') ||
-                    has_byte(v.w, '\'') || has_byte(wn, '\'');
-  if (!(any & 0x80808080u) && !apos) {
-    // ASCII: every byte is a unit.
-    const Ascii4 a0 = ascii_classes(v.x), a1 = ascii_classes(v.y), a2 = ascii_classes(v.z),
-                 a3 = ascii_classes(v.w), ap = ascii_classes(wp), an = ascii_classes(wn);
-    const uint32_t L = movemask4(a0.L) | movemask4(a1.L) << 4 | movemask4(a2.L) << 8 | movemask4(a3.L) << 12;
-    const uint32_t N = movemask4(a0.N) | movemask4(a1.N) << 4 | movemask4(a2.N) << 8 | movemask4(a3.N) << 12;
-    const uint32_t Sm = movemask4(a0.S) | movemask4(a1.S) << 4 | movemask4(a2.S) << 8 | movemask4(a3.S) << 12;
-    const uint32_t SP = movemask4(a0.SP) | movemask4(a1.SP) << 4 | movemask4(a2.SP) << 8 | movemask4(a3.SP) << 12;
-    const uint32_t Lp = (L << 1) | (ap.L >> 31), Np = (N << 1) | (ap.N >> 31);
-    const uint32_t Sp = (Sm << 1) | (ap.S >> 31), SPp = (SP << 1) | (ap.SP >> 31);
-    const uint32_t Sn = (Sm >> 1) | ((an.S >> 7) & 1u) << 15;
-    const uint32_t Dn = D17 >> 1;
-    const uint32_t B2 = Sm & (~Sp | (~Sn & ~Dn));
-    const uint32_t B3 = ~Sm & ~SPp & (Sp | (L ^ Lp) | (N ^ Np));
-    return (D17 | B2 | B3) & ~O16 & 0xFFFFu;
+  uint32_t w[6];
+#pragma unroll
+  for (int m = 0; m < 6; ++m) w[m] = lds_u32(w32 - 1 + m);
+  if (!((w[0] | w[1] | w[2] | w[3] | w[4] | w[5]) & 0x80808080u)) {
+    // ASCII: every byte is a unit; masks for bytes p0 - 4 .. p0 + 19 land in
+    // bits 4..27.
+    uint32_t L = 0, N = 0, Sm = 0, SP = 0, AP = 0;
+#pragma unroll
+    for (int m = 0; m < 6; ++m) {
+      const Ascii4 a = ascii_classes(w[m]);
+      const uint32_t y = w[m] ^ 0x27272727u;
+      const int sh = 4 + 4 * m;
+      L |= movemask4(a.L) << sh;
+      N |= movemask4(a.N) << sh;
+      Sm |= movemask4(a.S) << sh;
+      SP |= movemask4(a.SP) << sh;
+      AP |= movemask4(~(y + 0x7F7F7F7Fu) & 0x80808080u) << sh;
+    }
+    return boundaries16(S, p0, 0xFFFFFFFFu, L, N, Sm, SP, AP, D, O);
   }
-  // General: scan the UTF-8 units of bytes [p0 - 7, p0 + 17). Bit k of the
-  // masks below is byte p0 - 8 + k; each byte carries its unit's class. Units
-  // starting before p0 - 8 may be misread only up to p0 - 5, and nothing
-  // before p0 - 4 is used.
+  // General: scan the UTF-8 units of bytes [p0 - 7, p0 + 17); each byte
+  // carries its unit's class. Units starting before p0 - 8 may be misread
+  // only up to p0 - 5, and nothing before p0 - 4 is used.
   const int base = p0 - 8;
-  const uint32_t D = bits32_at(S.docbits, base), O = bits32_at(S.outbits, base);
   uint32_t U = 0, Lm = 0, Nm = 0, Sm = 0, SPm = 0, APm = 0, MBS = 0;
   int rem = 0, cls = kO;
 #pragma unroll 4
@@ -491,14 +523,10 @@ __device__ uint32_t start_mask16(const Smem& S, int p0) {
     SPm |= b == 0x20u ? bit : 0u;
     APm |= b == 0x27u ? bit : 0u;
   }
-  const uint32_t Sp = Sm << 1, Lp = Lm << 1, Np = Nm << 1, SPp = SPm << 1;
-  const uint32_t Sn = Sm >> 1, Dn = D >> 1;
-  const uint32_t B2 = Sm & (~Sp | (~Sn & ~Dn));
-  const uint32_t B3 = ~Sm & ~SPp & (Sp | (Lm ^ Lp) | (Nm ^ Np));
-  uint32_t res = ((U & ~O & (D | B2 | B3)) >> 8) & 0xFFFFu;
-  // Contractions and multi-byte whitespace: the per-byte predicate.
-  uint32_t fix = (APm & 0x01FFFFF0u) ? 0xFFFFu : 0u;
-  fix |= (MBS >> 8) & 0xFFFFu;
+  uint32_t res = boundaries16(S, p0, U, Lm, Nm, Sm, SPm, APm, D, O);
+  // Whitespace of several bytes (B2 looks past the whole unit): the per-byte
+  // predicate.
+  uint32_t fix = (MBS >> 8) & 0xFFFFu;
   while (fix) {
     const int k = __ffs(fix) - 1;
     fix &= fix - 1;
@@ -790,30 +818,29 @@ __device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, in
   return len;
 }
 
-// Ids of one short pre-token (window positions [ws, ws + len)) into sym;
-// returns their count.
-__device__ __forceinline__ uint32_t encode_short(Smem& S, int st, int len, const Tables& T, const Cache& C) {
+// Word-cache lookup of one short pre-token (window positions [kHalo + st,
+// + len)): writes its ids to sym[st ..] and returns their count, 0 if absent.
+__device__ __forceinline__ uint32_t cache_try(Smem& S, int st, int len, const Cache& C) {
   const int ws = kHalo + st;
-  if (C.enabled && len <= kCacheMaxLen) {
-    // The pre-token's first 16 window bytes, little-endian.
-    uint64_t k0 = (uint64_t)win_word(S, ws) | (uint64_t)win_word(S, ws + 4) << 32;
-    uint64_t k1 = (uint64_t)win_word(S, ws + 8) | (uint64_t)win_word(S, ws + 12) << 32;
-    if (len < 8) {
-      k0 &= (1ull << (8 * len)) - 1ull;
-      k1 = 0;
-    } else if (len == 8) {
-      k1 = 0;
-    } else if (len < 16) {
-      k1 &= (1ull << (8 * (len - 8))) - 1ull;
-    }
-    uint32_t ids[kCacheMaxIds];
-    const uint32_t cnt = cache_lookup(C, k0, k1, (uint32_t)len, ids);
-    if (cnt) {
-      for (uint32_t q = 0; q < cnt; ++q) S.sym[st + q] = ids[q];
-      return cnt;
-    }
+  // The pre-token's first 16 window bytes, little-endian.
+  uint64_t k0 = (uint64_t)win_word(S, ws) | (uint64_t)win_word(S, ws + 4) << 32;
+  uint64_t k1 = (uint64_t)win_word(S, ws + 8) | (uint64_t)win_word(S, ws + 12) << 32;
+  if (len < 8) {
+    k0 &= (1ull << (8 * len)) - 1ull;
+    k1 = 0;
+  } else if (len == 8) {
+    k1 = 0;
+  } else if (len < 16) {
+    k1 &= (1ull << (8 * (len - 8))) - 1ull;
   }
-  return (uint32_t)merge_short(S.sym + st, S.u.rk + st, S.win + ws, len, T, S.byte_id);
+  uint32_t ids[kCacheMaxIds];
+  const uint32_t cnt = cache_lookup(C, k0, k1, (uint32_t)len, ids);
+  for (uint32_t q = 0; q < cnt; ++q) S.sym[st + q] = ids[q];
+  return cnt;
+}
+
+__device__ __forceinline__ uint32_t merge_at(Smem& S, int st, int len, const Tables& T) {
+  return (uint32_t)merge_short(S.sym + st, S.u.rk + st, S.win + kHalo + st, len, T, S.byte_id);
 }
 
 // ------------------------------------------------------------------ kernels --
@@ -947,6 +974,7 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
     if (tid == 0) {
       S.n_spans = total;
       S.n_long = 0;
+      S.n_miss = 0;
       S.last_end = -1;
     }
   }
@@ -978,18 +1006,37 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
   }
   __syncthreads();
 
-  // Short pre-tokens: one thread each.
+  // Short pre-tokens, one thread each. Word-cache hits finish here; misses
+  // are queued and merged next by all threads together, so a warp does not
+  // wait on the merge loop of a few of its lanes.
   for (uint32_t j = tid; j < n_spans; j += kThreads) {
     const int st = S.span_start[j];
     const int64_t en = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
     const int len = en < 0 ? kSpan : (int)(en - (c0 + st));
     if (en >= 0 && len <= kShortMax) {
-      S.span_cnt[j] = encode_short(S, st, len, a.T, a.C);
+      const uint32_t cnt = (a.C.enabled && len <= kCacheMaxLen) ? cache_try(S, st, len, a.C) : 0u;
+      if (cnt) {
+        S.span_cnt[j] = cnt;
+      } else {
+        const uint32_t slot = atomicAdd(&S.n_miss, 1u);
+        if (slot < kMissCap) S.missq[slot] = (uint16_t)j;
+        else S.span_cnt[j] = merge_at(S, st, len, a.T);  // queue full: merge here
+      }
     } else {
       uint32_t slot = atomicAdd(&S.n_long, 1u);
       if (slot < (uint32_t)kMaxLong) S.long_list[slot] = (uint16_t)j;
       else atomicOr(&a.small->status, kStInternal);
       S.span_cnt[j] = 0;
+    }
+  }
+  __syncthreads();
+  {
+    const uint32_t n_miss = min(S.n_miss, kMissCap);
+    for (uint32_t q = tid; q < n_miss; q += kThreads) {
+      const uint32_t j = S.missq[q];
+      const int st = S.span_start[j];
+      const int64_t en = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
+      S.span_cnt[j] = merge_at(S, st, (int)(en - (c0 + st)), a.T);
     }
   }
   __syncthreads();
