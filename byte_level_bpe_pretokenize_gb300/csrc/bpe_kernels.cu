@@ -47,6 +47,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <unordered_set>
 #include <vector>
@@ -1476,6 +1477,49 @@ int build_word_cache(bpe_handle* h, const uint8_t* vocab_bytes, const int64_t* v
 
 }  // namespace
 
+// ---------------------------------------------- fixed scratch of the no-alloc encode --
+// bpe_encode_batch_noalloc keeps its scratch (look-back descriptors, first
+// document of each chunk, long pre-token pool, start bitmask) in one array of
+// static device memory per device instead of the handle's workspace. Regions
+// start on 256-byte boundaries and are sized for kNoAllocMaxBytes input bytes.
+namespace {
+constexpr int64_t kNoAllocMaxBytes = int64_t(4) << 20;
+constexpr int64_t kNoAllocChunks = kNoAllocMaxBytes / kChunk + 1;
+constexpr size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr size_t kNoAllocFirstDocOff = round256((size_t)kNoAllocChunks * sizeof(uint64_t));
+constexpr size_t kNoAllocPoolOff = kNoAllocFirstDocOff + round256((size_t)kNoAllocChunks * sizeof(int64_t));
+constexpr size_t kNoAllocBitsOff = kNoAllocPoolOff + round256((size_t)(kNoAllocMaxBytes + 4) * sizeof(int32_t));
+constexpr size_t kNoAllocScratchBytes =
+    kNoAllocBitsOff + round256((size_t)((kNoAllocMaxBytes + 31) / 32 + 4) * sizeof(uint32_t));
+static_assert(kNoAllocScratchBytes < (size_t(17) << 20), "the fixed scratch stays below 17 MiB");
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+unsigned char* g_noalloc_base[kNoAllocMaxDevices] = {};
+
+// Once per device, with that device current: the scratch address and the
+// shared-memory opt-in of the two kernels. Later calls only read the table.
+int noalloc_setup(int dev, unsigned char** base) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch_noalloc: device ordinal above 63");
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_base[dev]) {
+    void* p = nullptr;
+    CK(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+    if (reinterpret_cast<uintptr_t>(p) & 255u)
+      return fail(BPE_ERR_INTERNAL, "bpe_encode_batch_noalloc: scratch not 256-byte aligned");
+    CK(cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
+    CK(cudaFuncSetAttribute(k_pretokenize, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
+    g_noalloc_base[dev] = static_cast<unsigned char*>(p);
+  }
+  *base = g_noalloc_base[dev];
+  return BPE_OK;
+}
+}  // namespace
+
 extern "C" {
 
 const char* bpe_last_error(void) { return g_err.c_str(); }
@@ -1677,6 +1721,68 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
   k_encode<<<(unsigned)n_chunks, kThreads, sizeof(Smem), st>>>(a);
   CK(cudaGetLastError());
   if (h->ev_stop) CK(cudaEventRecord(h->ev_stop, st));
+  if (h_total_tokens) {
+    DevSmall s;
+    rc = read_status(h, st, &s);
+    if (rc) return rc;
+    *h_total_tokens = s.total;
+    return status_code(s.status);
+  }
+  return BPE_OK;
+}
+
+int bpe_encode_batch_noalloc(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
+                             int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets,
+                             int64_t* h_total_tokens, bpe_stream_t stream) {
+  if (!h || !d_doc_offsets || !d_out_offsets || n_bytes < 0 || n_docs < 0 || (n_bytes > 0 && !d_bytes))
+    return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch_noalloc: bad arguments");
+  if (out_capacity < 0 || (out_capacity > 0 && !d_out_ids))
+    return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch_noalloc: bad output buffer");
+  if ((reinterpret_cast<uintptr_t>(d_doc_offsets) & 7u) || (reinterpret_cast<uintptr_t>(d_out_offsets) & 7u) ||
+      (reinterpret_cast<uintptr_t>(d_out_ids) & 3u))
+    return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch_noalloc: offsets must be 8-byte and ids 4-byte aligned");
+  if (n_bytes > kNoAllocMaxBytes)
+    return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch_noalloc: n_bytes = " + std::to_string(n_bytes) +
+                                         " is above its fixed scratch limit of " + std::to_string(kNoAllocMaxBytes) +
+                                         " bytes (4 MiB); encode larger batches with bpe_encode_batch");
+  DeviceGuard g(h->device);
+  unsigned char* base = nullptr;
+  int rc = noalloc_setup(h->device, &base);
+  if (rc) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t n_chunks = n_bytes / kChunk + 1;
+  uint64_t* desc = reinterpret_cast<uint64_t*>(base);
+  int64_t* first_doc = reinterpret_cast<int64_t*>(base + kNoAllocFirstDocOff);
+  int32_t* pool = reinterpret_cast<int32_t*>(base + kNoAllocPoolOff);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(base + kNoAllocBitsOff);
+  // k_prep zeroes the look-back descriptors and the handle's ticket and token
+  // count; every other scratch word is written before it is read.
+  int prep_blocks = (int)std::min<int64_t>(4096, std::max<int64_t>(n_chunks, n_docs + 1) / 256 + 1);
+  k_prep<<<prep_blocks, 256, 0, st>>>(d_doc_offsets, n_docs, n_bytes, n_chunks, desc, first_doc, h->d_small);
+  CK(cudaGetLastError());
+  EncodeArgs a;
+  a.bytes = d_bytes;
+  a.n_bytes = n_bytes;
+  a.doc_offsets = d_doc_offsets;
+  a.n_docs = n_docs;
+  a.out_ids = d_out_ids;
+  a.out_capacity = out_capacity;
+  a.out_offsets = d_out_offsets;
+  a.pool = pool;
+  a.T = Tables{h->d_ht, h->hmask, h->d_mrows, h->d_byte_id};
+  a.C = Cache{h->d_cache, h->cache_mask, h->cache_enabled && h->d_cache != nullptr};
+  a.start_bits = bits;
+  a.desc = desc;
+  a.first_doc = first_doc;
+  a.small = h->d_small;
+  a.n_chunks = n_chunks;
+  if (n_bytes > 0) {
+    k_pretokenize<<<(unsigned)((n_bytes + kChunk - 1) / kChunk), kThreads, sizeof(Smem), st>>>(
+        d_bytes, n_bytes, d_doc_offsets, n_docs, first_doc, bits);
+    CK(cudaGetLastError());
+  }
+  k_encode<<<(unsigned)n_chunks, kThreads, sizeof(Smem), st>>>(a);
+  CK(cudaGetLastError());
   if (h_total_tokens) {
     DevSmall s;
     rc = read_status(h, st, &s);

@@ -103,6 +103,40 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
                      int64_t* h_total_tokens, bpe_stream_t stream);
 
 /*
+ * bpe_encode_batch_noalloc — bpe_encode_batch with fixed scratch: the same
+ * arguments, kernels and results, but the call allocates no device memory.
+ * The pages have no counterpart; this is a library-level variant for callers
+ * that cannot allocate at encode time: a serving loop whose latency cannot
+ * absorb the device-wide wait of the cudaFree that bpe_encode_batch issues
+ * when its workspace grows, or a process that must fix its device memory
+ * footprint before it starts taking requests.
+ *
+ *   Limit: n_bytes <= 4 MiB (4,194,304). A larger batch is rejected with
+ *   BPE_ERR_INVALID_ARG before anything is queued; split it or use
+ *   bpe_encode_batch. n_docs is not limited by the scratch.
+ *   Scratch: one 16.8 MB array of static device memory per device (reserved
+ *   when the library's module is loaded on that device, not by this call),
+ *   holding the look-back descriptors, each 4 KiB chunk's first document, the
+ *   pool for pre-tokens too long for shared memory and the pre-token start
+ *   bitmask. The call's first kernel zeroes what must start at zero (the
+ *   look-back descriptors and the handle's ticket and token count); every
+ *   other scratch word is written before it is read.
+ *   Set-up: the first call on each device looks up the scratch address
+ *   (cudaGetSymbolAddress) and sets the kernels' shared-memory limit, with the
+ *   handle's device current; make that first call before any stream capture.
+ *   Races: the scratch is shared by every call of this function on a device,
+ *   whatever the handle, stream or host thread. Two calls in flight on one
+ *   device at the same time overwrite each other's scratch and give wrong ids;
+ *   order them on one stream (or wait between them). Calls of bpe_encode_batch
+ *   do not touch this scratch.
+ * Errors as for bpe_encode_batch. Timing events (bpe_set_timing_events) are
+ * not recorded by this call.
+ */
+int bpe_encode_batch_noalloc(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
+                             int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets,
+                             int64_t* h_total_tokens, bpe_stream_t stream);
+
+/*
  * bpe_pretokenize_batch — the pre-tokenizer alone: marks where pre-tokens
  * start (glitch4techs, section "Technical analysis": the split of "Hello
  * world!" into "Hello", " world", "!").
