@@ -75,14 +75,17 @@ constexpr int kCacheMaxIds = 3;       // most ids a cache entry holds
 constexpr int kLongPerThread = 4;     // elements per thread per round of the CTA merge
 constexpr int kRound = kThreads * kLongPerThread;
 constexpr int kMaxLong = kChunk / kShortMax + 2;
-constexpr uint32_t kMissCap = 2 * kSpanWords;  // queued word-cache misses per chunk
+constexpr uint32_t kMissShortCap = 3 * kSpanWords / 2;  // queued word-cache misses of <= 16 bytes
+constexpr uint32_t kMissMedCap = kSpanWords / 2;        // ... and of 17..kShortMax bytes
+constexpr uint32_t kReprobe = 0xFFFFFFFEu;              // pair rank still to be looked up
 constexpr uint32_t kInf = 0xFFFFFFFFu;
 constexpr uint32_t kNone = 0xFFFFFFFFu;
-constexpr uint64_t kEmpty = ~0ull;
+constexpr uint32_t kEmptySlot = 0xFFFFFFFFu;  // left id of an unused pair-table slot
 constexpr uint64_t kWaitLimitNs = 20ull * 1000 * 1000 * 1000;  // 20 s
 
 static_assert(kChunk == 16 * kThreads, "one 16-byte group per thread");
 static_assert(kMargin <= 16 * 16, "the margin is covered by 16 lanes of warp 0");
+static_assert(kShortMax <= 64 && kCacheMaxLen <= 16, "group merges hold 2 symbols per lane");
 
 // device status bits
 constexpr uint32_t kStBadInput = 1u;
@@ -118,7 +121,7 @@ __host__ __device__ inline uint32_t cache_hash(uint64_t k0, uint64_t k1, uint32_
 }
 
 struct Tables {
-  const uint64_t* ht;      // 4 entries per bucket: left << 40 | right << 20 | rank
+  const uint4* ht;         // 2 entries per 32-byte bucket: {left, right, rank, new_id}
   uint32_t hmask;          // buckets - 1
   const int32_t* mrows;    // [n_merges][3] (left, right, new)
   const int32_t* byte_id;  // [256]
@@ -157,20 +160,28 @@ __device__ __forceinline__ void st_relaxed(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-__device__ __forceinline__ uint32_t lookup_rank(const Tables& T, uint32_t a, uint32_t b) {
-  const uint64_t key = ((uint64_t)a << 20) | b;
+// Rank of the pair (a, b), kInf if it is not a merge; *nw gets the merged id.
+__device__ __forceinline__ uint32_t lookup_pair(const Tables& T, uint32_t a, uint32_t b, uint32_t* nw) {
   uint32_t bucket = pair_hash(a, b) & T.hmask;
   for (uint32_t probe = 0; probe <= T.hmask; ++probe) {
-    const ulonglong2* p = reinterpret_cast<const ulonglong2*>(T.ht + 4ull * bucket);
-    ulonglong2 u = __ldg(p), v = __ldg(p + 1);
-    if ((u.x >> 20) == key) return (uint32_t)(u.x & 0xFFFFF);
-    if ((u.y >> 20) == key) return (uint32_t)(u.y & 0xFFFFF);
-    if ((v.x >> 20) == key) return (uint32_t)(v.x & 0xFFFFF);
-    if ((v.y >> 20) == key) return (uint32_t)(v.y & 0xFFFFF);
-    if (u.x == kEmpty || u.y == kEmpty || v.x == kEmpty || v.y == kEmpty) return kInf;
+    const uint4 u = __ldg(T.ht + 2ull * bucket), v = __ldg(T.ht + 2ull * bucket + 1);
+    if (u.x == a && u.y == b) {
+      *nw = u.w;
+      return u.z;
+    }
+    if (v.x == a && v.y == b) {
+      *nw = v.w;
+      return v.z;
+    }
+    if (u.x == kEmptySlot || v.x == kEmptySlot) return kInf;
     bucket = (bucket + 1) & T.hmask;
   }
   return kInf;
+}
+
+__device__ __forceinline__ uint32_t lookup_rank(const Tables& T, uint32_t a, uint32_t b) {
+  uint32_t nw;
+  return lookup_pair(T, a, b, &nw);
 }
 
 // Number of ids (1..3) the word cache holds for a pre-token, or 0 if absent.
@@ -365,19 +376,25 @@ __device__ __forceinline__ uint32_t bits32_at(const uint32_t* bits, int start) {
 
 namespace {
 
+// A warp's scratch while its lanes merge pre-tokens in groups (merge_group).
+struct GroupScratch {
+  uint32_t sym[64], rank[64], nw[64];
+};
+
 struct Smem {
   uint8_t win[kWin + 16];
   uint32_t docbits[kWinWords + 2];   // a document (or the area after the last one) starts here
   uint32_t outbits[kWinWords + 2];   // byte belongs to no document
   union {
     uint32_t startbits[kSpanWords];
-    uint16_t missq[2 * kSpanWords];  // word-cache misses, once the start bits are consumed
+    uint16_t missq[kMissShortCap + kMissMedCap];  // word-cache misses, once the start bits are consumed
   };
   uint16_t span_start[kChunk + 1];
   uint32_t span_cnt[kChunk + 1];     // token counts, then exclusive offsets
   uint32_t sym[kSpan];               // ids of short pre-tokens, at their start position
   union {
-    uint32_t rk[kSpan];              // pair ranks while merging short pre-tokens
+    uint32_t rk[kSpan];              // pair ranks while one thread merges a short pre-token
+    GroupScratch grp[kThreads / 32]; // one per warp while lane groups merge cache misses
     uint32_t stage[kRound];          // long merge rounds
     uint32_t ostage[kSpan];          // ids in output order
   } u;
@@ -389,7 +406,8 @@ struct Smem {
   int64_t prefix;
   uint32_t n_spans;
   uint32_t n_long;
-  uint32_t n_miss;
+  uint32_t n_miss;                   // queued misses of <= 16 bytes
+  uint32_t n_miss_m;                 // queued misses of 17..kShortMax bytes
   int64_t last_end;
   int64_t doc_lo, doc_hi;  // document of a long pre-token that runs past the window
 };
@@ -730,6 +748,92 @@ __device__ int merge_short(uint32_t* sym, uint32_t* rk, const uint8_t* src, int 
   return n;
 }
 
+// ------------------------------------------------------ merge: lane group --
+// G lanes of a warp (G = 8 or 32) merge one pre-token of n <= 2 G symbols
+// together. Lane g holds positions g and g + G: the symbol, and the rank and
+// merged id of the pair that starts there. A step takes the group's lowest
+// rank and marks every position where that pair starts. Two marks are
+// adjacent only when both symbols of the pair are equal; a left-to-right scan
+// without overlap then keeps the first mark of each such run and every second
+// one after it, which is computed for all positions at once from the run
+// starts (bit masks of up to 64 positions). The merged symbols are written
+// compacted to the warp's scratch and only the pairs that touch a merged
+// symbol are looked up again. All 32 lanes call this together; a group with
+// n == 0 idles. The final ids go to out[0 .. count).
+template <int G>
+__device__ uint32_t merge_group(GroupScratch& W, const uint8_t* src, uint32_t n, const Tables& T,
+                                const int32_t* byte_id, uint32_t* out) {
+  static_assert(G == 8 || G == 32, "group of 8 or 32 lanes");
+  const int lane = threadIdx.x & 31;
+  const int g = lane & (G - 1);
+  const int goff = lane & ~(G - 1);
+  const uint32_t gbits = G == 32 ? 0xFFFFFFFFu : ((1u << G) - 1u);
+  uint32_t* ws = W.sym + (lane / G) * 2 * G;
+  uint32_t* wr = W.rank + (lane / G) * 2 * G;
+  uint32_t* ww = W.nw + (lane / G) * 2 * G;
+  const uint32_t p0 = (uint32_t)g, p1 = (uint32_t)(g + G);
+
+  uint32_t s0 = p0 < n ? (uint32_t)byte_id[src[p0]] : kNone;
+  uint32_t s1 = p1 < n ? (uint32_t)byte_id[src[p1]] : kNone;
+  ws[p0] = s0;
+  ws[p1] = s1;
+  __syncwarp();
+  uint32_t w0 = 0, w1 = 0;
+  uint32_t r0 = p0 + 1 < n ? lookup_pair(T, s0, ws[p0 + 1], &w0) : kInf;
+  uint32_t r1 = p1 + 1 < n ? lookup_pair(T, s1, ws[p1 + 1], &w1) : kInf;
+  uint32_t cnt = n;
+  for (;;) {
+    uint32_t best = min(r0, r1);
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) best = min(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+    const bool go = best != kInf;
+    if (!__any_sync(0xFFFFFFFFu, go)) break;
+    const bool o0 = go && r0 == best, o1 = go && r1 == best;
+    const uint32_t b0 = (__ballot_sync(0xFFFFFFFFu, o0) >> goff) & gbits;
+    const uint32_t b1 = (__ballot_sync(0xFFFFFFFFu, o1) >> goff) & gbits;
+    const uint64_t M = (uint64_t)b0 | ((uint64_t)b1 << G);
+    const uint32_t any = b0 | b1;
+    const uint32_t nwb = __shfl_sync(0xFFFFFFFFu, o0 ? w0 : w1, goff + (any ? __ffs(any) - 1 : 0));
+    const uint64_t E = 0x5555555555555555ull;  // even positions
+    const uint64_t run_start = M & ~(M << 1);
+    const uint64_t even_runs = M & ~(M + (run_start & E));  // runs that start at an even position
+    const uint64_t take = (even_runs & E) | (M & ~even_runs & ~E);
+    const uint64_t valid = cnt >= 64 ? ~0ull : ((1ull << cnt) - 1ull);
+    const uint64_t keep = valid & ~(take << 1);
+    __syncwarp();  // every lane has read the scratch before it is rewritten
+    if (go) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t p = h ? p1 : p0;
+        if ((keep >> p) & 1ull) {
+          const uint32_t ni = (uint32_t)__popcll(keep & ((1ull << p) - 1ull));
+          const bool tp = (take >> p) & 1ull;
+          const uint32_t q = tp ? p + 2 : p + 1;  // next kept position
+          const bool tq = q < 64 && ((take >> q) & 1ull);
+          ws[ni] = tp ? nwb : (h ? s1 : s0);
+          wr[ni] = (tp || tq) ? kReprobe : (h ? r1 : r0);
+          ww[ni] = h ? w1 : w0;
+        }
+      }
+      cnt = (uint32_t)__popcll(keep);
+    }
+    __syncwarp();
+    if (go) {  // a finished group keeps its registers
+      s0 = p0 < cnt ? ws[p0] : kNone;
+      s1 = p1 < cnt ? ws[p1] : kNone;
+      r0 = p0 + 1 < cnt ? wr[p0] : kInf;
+      r1 = p1 + 1 < cnt ? wr[p1] : kInf;
+      w0 = ww[p0];
+      w1 = ww[p1];
+      if (r0 == kReprobe) r0 = lookup_pair(T, s0, ws[p0 + 1], &w0);
+      if (r1 == kReprobe) r1 = lookup_pair(T, s1, ws[p1 + 1], &w1);
+    }
+  }
+  if (p0 < cnt) out[p0] = s0;
+  if (p1 < cnt) out[p1] = s1;
+  return cnt;
+}
+
 // ------------------------------------------------------------ merge: long --
 // The whole CTA merges one long pre-token in place in scr (the pool range of
 // its own bytes, read and written in rounds of kRound elements; a round writes
@@ -976,6 +1080,7 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
       S.n_spans = total;
       S.n_long = 0;
       S.n_miss = 0;
+      S.n_miss_m = 0;
       S.last_end = -1;
     }
   }
@@ -1018,10 +1123,14 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
       const uint32_t cnt = (a.C.enabled && len <= kCacheMaxLen) ? cache_try(S, st, len, a.C) : 0u;
       if (cnt) {
         S.span_cnt[j] = cnt;
-      } else {
+      } else if (len <= kCacheMaxLen) {
         const uint32_t slot = atomicAdd(&S.n_miss, 1u);
-        if (slot < kMissCap) S.missq[slot] = (uint16_t)j;
+        if (slot < kMissShortCap) S.missq[slot] = (uint16_t)j;
         else S.span_cnt[j] = merge_at(S, st, len, a.T);  // queue full: merge here
+      } else {
+        const uint32_t slot = atomicAdd(&S.n_miss_m, 1u);
+        if (slot < kMissMedCap) S.missq[kMissShortCap + slot] = (uint16_t)j;
+        else S.span_cnt[j] = merge_at(S, st, len, a.T);
       }
     } else {
       uint32_t slot = atomicAdd(&S.n_long, 1u);
@@ -1032,12 +1141,35 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
   }
   __syncthreads();
   {
-    const uint32_t n_miss = min(S.n_miss, kMissCap);
-    for (uint32_t q = tid; q < n_miss; q += kThreads) {
-      const uint32_t j = S.missq[q];
-      const int st = S.span_start[j];
-      const int64_t en = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
-      S.span_cnt[j] = merge_at(S, st, (int)(en - (c0 + st)), a.T);
+    // Queued misses: up to 16 bytes by groups of 8 lanes, longer ones by a
+    // warp each.
+    GroupScratch& W = S.u.grp[tid >> 5];
+    const uint32_t n_short = min(S.n_miss, kMissShortCap), n_med = min(S.n_miss_m, kMissMedCap);
+    for (uint32_t q0 = 0; q0 < n_short; q0 += kThreads / 8) {
+      const uint32_t q = q0 + (uint32_t)(tid >> 3);
+      uint32_t j = 0, n = 0;
+      int st = 0;
+      if (q < n_short) {
+        j = S.missq[q];
+        st = S.span_start[j];
+        const int64_t en = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
+        n = (uint32_t)(en - (c0 + st));
+      }
+      const uint32_t cnt = merge_group<8>(W, S.win + kHalo + st, n, a.T, S.byte_id, S.sym + st);
+      if (q < n_short && (tid & 7) == 0) S.span_cnt[j] = cnt;
+    }
+    for (uint32_t q0 = 0; q0 < n_med; q0 += kThreads / 32) {
+      const uint32_t q = q0 + (uint32_t)(tid >> 5);
+      uint32_t j = 0, n = 0;
+      int st = 0;
+      if (q < n_med) {
+        j = S.missq[kMissShortCap + q];
+        st = S.span_start[j];
+        const int64_t en = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
+        n = (uint32_t)(en - (c0 + st));
+      }
+      const uint32_t cnt = merge_group<32>(W, S.win + kHalo + st, n, a.T, S.byte_id, S.sym + st);
+      if (q < n_med && (tid & 31) == 0) S.span_cnt[j] = cnt;
     }
   }
   __syncthreads();
@@ -1366,7 +1498,7 @@ struct DeviceGuard {
 struct bpe_handle {
   int device = 0;
   int64_t n_merges = 0, n_vocab = 0;
-  uint64_t* d_ht = nullptr;
+  uint4* d_ht = nullptr;
   uint32_t hmask = 0;
   int32_t* d_mrows = nullptr;
   int32_t* d_byte_id = nullptr;
@@ -1413,17 +1545,24 @@ int status_code(uint32_t s) {
   return BPE_OK;
 }
 
-// Word cache: the ids of every vocabulary string of 1..16 bytes, computed on
-// the device by the merge loop, laid out as an open-addressed table (load at
-// most 1/4, linear probing).
+// Word cache: the ids of every vocabulary string of 1..16 bytes, and of
+// every vocabulary string that starts with a space with that space removed
+// (the same word at the start of a line or document), computed on the device
+// by the merge loop, laid out as an open-addressed table (load at most 1/4,
+// linear probing).
 int build_word_cache(bpe_handle* h, const uint8_t* vocab_bytes, const int64_t* vocab_offsets, int64_t n_vocab) {
   std::vector<uint8_t> strs;
   std::vector<int64_t> offs{0};
+  std::unordered_set<std::string> keys;
+  auto add = [&](const uint8_t* b, int64_t L) {
+    if (L < 1 || L > kCacheMaxLen || !keys.insert(std::string((const char*)b, (size_t)L)).second) return;
+    strs.insert(strs.end(), b, b + L);
+    offs.push_back((int64_t)strs.size());
+  };
+  for (int64_t id = 0; id < n_vocab; ++id) add(vocab_bytes + vocab_offsets[id], vocab_offsets[id + 1] - vocab_offsets[id]);
   for (int64_t id = 0; id < n_vocab; ++id) {
     const int64_t L = vocab_offsets[id + 1] - vocab_offsets[id];
-    if (L < 1 || L > kCacheMaxLen) continue;
-    strs.insert(strs.end(), vocab_bytes + vocab_offsets[id], vocab_bytes + vocab_offsets[id + 1]);
-    offs.push_back((int64_t)strs.size());
+    if (L >= 2 && vocab_bytes[vocab_offsets[id]] == ' ') add(vocab_bytes + vocab_offsets[id] + 1, L - 1);
   }
   const int64_t n = (int64_t)offs.size() - 1;
   uint8_t* d_strs = nullptr;
@@ -1552,8 +1691,8 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
       if (byte_id[b] < 0) return fail(BPE_ERR_BAD_TABLE, "a single byte is missing from the vocabulary");
   }
   uint64_t nb = 1;
-  while (nb * 2 < (uint64_t)n_merges) nb <<= 1;  // at most two entries per 4-slot bucket on average
-  std::vector<uint64_t> ht(nb * 4, kEmpty);
+  while (nb < (uint64_t)n_merges) nb <<= 1;  // at most one entry per 2-slot bucket on average
+  std::vector<uint4> ht(nb * 2, make_uint4(kEmptySlot, kEmptySlot, kInf, 0));
   {
     std::unordered_set<uint64_t> pairs;
     for (int64_t r = 0; r < n_merges; ++r) {
@@ -1568,13 +1707,13 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
       uint64_t bucket = pair_hash((uint32_t)a, (uint32_t)b) & (nb - 1);
       for (;;) {
         int slot = -1;
-        for (int q = 0; q < 4; ++q)
-          if (ht[bucket * 4 + q] == kEmpty) {
+        for (int q = 0; q < 2; ++q)
+          if (ht[bucket * 2 + q].x == kEmptySlot) {
             slot = q;
             break;
           }
         if (slot >= 0) {
-          ht[bucket * 4 + slot] = (key << 20) | (uint64_t)r;
+          ht[bucket * 2 + slot] = make_uint4((uint32_t)a, (uint32_t)b, (uint32_t)r, (uint32_t)nw);
           break;
         }
         bucket = (bucket + 1) & (nb - 1);
@@ -1599,8 +1738,8 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
     cudaError_t e_ = (call);                                     \
     if (e_ != cudaSuccess) return cleanup(cuda_fail(e_, #call)); \
   } while (0)
-  CKB(cudaMalloc(&h->d_ht, ht.size() * sizeof(uint64_t)));
-  CKB(cudaMemcpy(h->d_ht, ht.data(), ht.size() * sizeof(uint64_t), cudaMemcpyHostToDevice));
+  CKB(cudaMalloc(&h->d_ht, ht.size() * sizeof(uint4)));
+  CKB(cudaMemcpy(h->d_ht, ht.data(), ht.size() * sizeof(uint4), cudaMemcpyHostToDevice));
   CKB(cudaMalloc(&h->d_mrows, (size_t)std::max<int64_t>(1, n_merges) * 3 * sizeof(int32_t)));
   if (n_merges) CKB(cudaMemcpy(h->d_mrows, merges, (size_t)n_merges * 3 * sizeof(int32_t), cudaMemcpyHostToDevice));
   CKB(cudaMalloc(&h->d_byte_id, 256 * sizeof(int32_t)));
