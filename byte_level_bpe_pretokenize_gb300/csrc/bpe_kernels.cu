@@ -100,24 +100,26 @@ constexpr uint64_t kDescValue = (1ull << 62) - 1;
 
 enum Cls { kO = 0, kL = 1, kN = 2, kS = 3 };
 
-__host__ __device__ inline uint64_t fmix64(uint64_t x) {
-  // MurmurHash3's 64-bit finalizer.
-  x ^= x >> 33;
-  x *= 0xFF51AFD7ED558CCDull;
-  x ^= x >> 33;
-  x *= 0xC4CEB9FE1A85EC53ull;
-  x ^= x >> 33;
-  return x;
+// 32-bit hashing: odd multipliers combine the words, then a xor-shift /
+// multiply finalizer (the "lowbias32" constants of Chris Wellons' hash
+// prospector) spreads them over the low bits the tables index with.
+__host__ __device__ inline uint32_t mix32(uint32_t h) {
+  h ^= h >> 16;
+  h *= 0x7FEB352Du;
+  h ^= h >> 15;
+  h *= 0x846CA68Bu;
+  h ^= h >> 16;
+  return h;
 }
 
 __host__ __device__ inline uint32_t pair_hash(uint32_t a, uint32_t b) {
-  return (uint32_t)fmix64(((uint64_t)a << 32) | b);
+  return mix32(a * 0x9E3779B1u + b * 0x85EBCA77u);
 }
 
-// Word cache key: the pre-token's bytes little-endian in k0 (bytes 0..7) and
-// k1 (bytes 8..15), zero padded, plus its length.
-__host__ __device__ inline uint32_t cache_hash(uint64_t k0, uint64_t k1, uint32_t len) {
-  return (uint32_t)fmix64(k0 * 0x9E3779B97F4A7C15ull + (k1 ^ len) * 0xC2B2AE3D27D4EB4Full);
+// Word cache key: the pre-token's bytes little-endian in x0..x3 (bytes 0..15),
+// zero padded, plus its length.
+__host__ __device__ inline uint32_t cache_hash(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3, uint32_t len) {
+  return mix32(x0 * 0x9E3779B1u + x1 * 0x85EBCA77u + x2 * 0xC2B2AE3Du + x3 * 0x27D4EB2Fu + len);
 }
 
 struct Tables {
@@ -182,25 +184,6 @@ __device__ __forceinline__ uint32_t lookup_pair(const Tables& T, uint32_t a, uin
 __device__ __forceinline__ uint32_t lookup_rank(const Tables& T, uint32_t a, uint32_t b) {
   uint32_t nw;
   return lookup_pair(T, a, b, &nw);
-}
-
-// Number of ids (1..3) the word cache holds for a pre-token, or 0 if absent.
-__device__ __forceinline__ uint32_t cache_lookup(const Cache& C, uint64_t k0, uint64_t k1, uint32_t len,
-                                                 uint32_t* ids) {
-  uint32_t slot = cache_hash(k0, k1, len) & C.mask;
-  for (uint32_t probe = 0; probe <= C.mask; ++probe) {
-    const uint4 a = __ldg(C.e + 2 * slot), b = __ldg(C.e + 2 * slot + 1);
-    if (b.x == 0) return 0;
-    if ((b.x & 31u) == len && a.x == (uint32_t)k0 && a.y == (uint32_t)(k0 >> 32) && a.z == (uint32_t)k1 &&
-        a.w == (uint32_t)(k1 >> 32)) {
-      ids[0] = b.y;
-      ids[1] = b.z;
-      ids[2] = b.w;
-      return (b.x >> 5) & 7u;
-    }
-    slot = (slot + 1) & C.mask;
-  }
-  return 0;
 }
 
 __device__ __forceinline__ int cp_class(uint32_t cp) {
@@ -381,7 +364,9 @@ struct GroupScratch {
   uint32_t sym[64], rank[64], nw[64];
 };
 
-struct Smem {
+// What the split needs: the window and its document and start bit masks. The
+// split kernel's shared memory is only this; the encode kernel's extends it.
+struct SplitSmem {
   uint8_t win[kWin + 16];
   uint32_t docbits[kWinWords + 2];   // a document (or the area after the last one) starts here
   uint32_t outbits[kWinWords + 2];   // byte belongs to no document
@@ -389,6 +374,10 @@ struct Smem {
     uint32_t startbits[kSpanWords];
     uint16_t missq[kMissShortCap + kMissMedCap];  // word-cache misses, once the start bits are consumed
   };
+  int64_t chunk;
+};
+
+struct Smem : SplitSmem {
   uint16_t span_start[kChunk + 1];
   uint32_t span_cnt[kChunk + 1];     // token counts, then exclusive offsets
   uint32_t sym[kSpan];               // ids of short pre-tokens, at their start position
@@ -402,8 +391,8 @@ struct Smem {
   uint16_t long_list[kMaxLong];
   uint32_t red[kThreads / 32 + 2];
   uint32_t carry[2];
-  int64_t chunk;
   int64_t prefix;
+  uint32_t agg;                      // the chunk's token count
   uint32_t n_spans;
   uint32_t n_long;
   uint32_t n_miss;                   // queued misses of <= 16 bytes
@@ -412,26 +401,18 @@ struct Smem {
   int64_t doc_lo, doc_hi;  // document of a long pre-token that runs past the window
 };
 
+// Barrier of the kThreads threads that split and merge (named barrier 1). The
+// encode kernel's extra look-back warp never takes part in it.
+__device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void named_arrive(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
 __device__ __forceinline__ bool bit_at(const uint32_t* bits, int i) { return (bits[i >> 5] >> (i & 31)) & 1u; }
-
-// One window byte through an explicit byte-wide shared load, so that words
-// assembled from several of them are never turned into wider loads.
-__device__ __forceinline__ uint32_t win_byte(const Smem& S, int b) {
-  uint32_t v;
-  const unsigned addr = (unsigned)__cvta_generic_to_shared(S.win + b);
-  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
-// Window bytes [b, b + 4) as a little-endian word.
-__device__ __forceinline__ uint32_t win_word(const Smem& S, int b) {
-  return win_byte(S, b) | win_byte(S, b + 1) << 8 | win_byte(S, b + 2) << 16 | win_byte(S, b + 3) << 24;
-}
 
 // Document bounds [lo, hi) around window index i: the nearest document edge at
 // or before i and the next one after i (at most kHalo away is all that is
 // read), or the window edges.
-__device__ __forceinline__ void doc_bounds(const Smem& S, int i, int* lo, int* hi) {
+__device__ __forceinline__ void doc_bounds(const SplitSmem& S, int i, int* lo, int* hi) {
   int a = i;
   while (a > 0 && a > i - kHalo && !bit_at(S.docbits, a)) --a;
   *lo = a;
@@ -440,7 +421,7 @@ __device__ __forceinline__ void doc_bounds(const Smem& S, int i, int* lo, int* h
   *hi = b;
 }
 
-__device__ __forceinline__ bool starts_piece_at(const Smem& S, int i) {
+__device__ __forceinline__ bool starts_piece_at(const SplitSmem& S, int i) {
   if (bit_at(S.outbits, i)) return false;
   int lo, hi;
   doc_bounds(S, i, &lo, &hi);
@@ -457,7 +438,7 @@ __device__ __forceinline__ bool starts_piece_at(const Smem& S, int i) {
 // U+0020) and the next one or two bytes of its document are a suffix; then
 // the byte after it gets no boundary (B0) and the byte after the suffix gets
 // one (B1).
-__device__ __forceinline__ uint32_t boundaries16(const Smem& S, int p0, uint32_t U, uint32_t L, uint32_t N,
+__device__ __forceinline__ uint32_t boundaries16(const SplitSmem& S, int p0, uint32_t U, uint32_t L, uint32_t N,
                                                  uint32_t Sm, uint32_t SP, uint32_t AP, uint32_t D, uint32_t O) {
   const uint32_t Sp = Sm << 1, Lp = L << 1, Np = N << 1, SPp = SP << 1;
   const uint32_t Sn = Sm >> 1, Dn = D >> 1;
@@ -488,7 +469,7 @@ __device__ __forceinline__ uint32_t boundaries16(const Smem& S, int p0, uint32_t
 }
 
 // Start bits of window positions [p0, p0 + 16), p0 a multiple of 16.
-__device__ uint32_t start_mask16(const Smem& S, int p0) {
+__device__ uint32_t start_mask16(const SplitSmem& S, int p0) {
   const uint32_t D = bits32_at(S.docbits, p0 - 8), O = bits32_at(S.outbits, p0 - 8);
   if (((O >> 8) & 0xFFFFu) == 0xFFFFu) return 0;
   // Six aligned window words: bytes p0 - 4 .. p0 + 19 (p0 is a multiple of 16).
@@ -558,7 +539,7 @@ __device__ uint32_t start_mask16(const Smem& S, int p0) {
 // Loads the window of chunk c: bytes [c0 - kHalo, c0 + kChunk + kMargin +
 // kHalo), the document edges that fall inside it, and which bytes lie outside
 // every document. first_doc = the first document starting at or after c0.
-__device__ void load_window(Smem& S, const uint8_t* bytes, int64_t n_bytes, const int64_t* doc_offsets,
+__device__ void load_window(SplitSmem& S, const uint8_t* bytes, int64_t n_bytes, const int64_t* doc_offsets,
                             int64_t n_docs, int64_t c0, int64_t first_doc) {
   const int tid = threadIdx.x;
   const int64_t w0 = c0 - kHalo;
@@ -583,7 +564,7 @@ __device__ void load_window(Smem& S, const uint8_t* bytes, int64_t n_bytes, cons
     S.docbits[i] = 0;
     S.outbits[i] = 0;
   }
-  __syncthreads();
+  cta_sync();
   int64_t d_first = doc_offsets[0], d_last = doc_offsets[n_docs];
   d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
   d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
@@ -611,11 +592,55 @@ __device__ void load_window(Smem& S, const uint8_t* bytes, int64_t n_bytes, cons
       atomicOr(&S.docbits[i >> 5], 1u << (i & 31));
     }
   }
-  __syncthreads();
+  cta_sync();
+}
+
+// The encode kernel's window of chunk c: the bytes (as load_window), which
+// bytes lie outside every document (from the first and last document
+// offsets alone: documents are contiguous, so every other document edge is a
+// pre-token start) and the split kernel's start bits of [c0, c0 + kSpan).
+__device__ void load_encode_window(SplitSmem& S, const uint8_t* bytes, int64_t n_bytes, const int64_t* doc_offsets,
+                                   int64_t n_docs, const uint32_t* start_bits, int64_t c0) {
+  const int tid = threadIdx.x;
+  const int64_t w0 = c0 - kHalo;
+  int64_t d_first = __ldg(doc_offsets), d_last = __ldg(doc_offsets + n_docs);
+  const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 3u) == 0;
+  const uint32_t* g32 = reinterpret_cast<const uint32_t*>(bytes);
+  for (int i = tid * 16; i < kWin; i += kThreads * 16) {
+    const int64_t p = w0 + i;
+    if (aligned && p >= 0 && p + 16 <= n_bytes) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t w = __ldg(g32 + (p >> 2) + k);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) S.win[i + 4 * k + q] = (uint8_t)(w >> (8 * q));
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) S.win[i + k] = (p + k >= 0 && p + k < n_bytes) ? bytes[p + k] : 0;
+    }
+  }
+  const int64_t n_words = (n_bytes + 31) / 32;
+  for (int w = tid; w < kSpanWords; w += kThreads) {
+    const int64_t gw = c0 / 32 + w;
+    S.startbits[w] = gw < n_words ? __ldg(start_bits + gw) : 0u;
+  }
+  d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
+  d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
+  for (int wi = tid; wi < kWinWords + 2; wi += kThreads) {
+    uint32_t word = 0;
+    const int64_t p = w0 + (int64_t)wi * 32;
+    if (p < d_first || p + 32 > d_last) {
+      for (int k = 0; k < 32; ++k)
+        if (p + k < d_first || p + k >= d_last) word |= 1u << k;
+    }
+    S.outbits[wi] = word;
+  }
+  cta_sync();
 }
 
 // Start bits for window indices [kHalo, kHalo + kSpan).
-__device__ void compute_start_bits(Smem& S) {
+__device__ void compute_start_bits(SplitSmem& S) {
   const int tid = threadIdx.x, lane = tid & 31;
   uint32_t m = start_mask16(S, kHalo + 16 * tid);
   uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, m, 1);
@@ -625,7 +650,7 @@ __device__ void compute_start_bits(Smem& S) {
     uint32_t h2 = __shfl_down_sync(0xFFFFFFFFu, mm, 1);
     if ((lane & 1) == 0 && lane < kMargin / 16) S.startbits[kChunk / 32 + (lane >> 1)] = mm | (h2 << 16);
   }
-  __syncthreads();
+  cta_sync();
 }
 
 // ----------------------------------------------------------- block helpers --
@@ -645,17 +670,17 @@ __device__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total) 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t incl = warp_incl_scan(v);
   if (lane == 31) red[warp] = incl;
-  __syncthreads();
+  cta_sync();
   if (warp == 0) {
     uint32_t x = lane < kThreads / 32 ? red[lane] : 0;
     uint32_t xi = warp_incl_scan(x);
     if (lane < kThreads / 32) red[lane] = xi - x;
     if (lane == kThreads / 32 - 1) red[kThreads / 32] = xi;
   }
-  __syncthreads();
+  cta_sync();
   uint32_t r = red[warp] + incl - v;
   *total = red[kThreads / 32];
-  __syncthreads();
+  cta_sync();
   return r;
 }
 
@@ -664,10 +689,10 @@ __device__ uint32_t block_min(uint32_t v, uint32_t* red) {
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) v = min(v, __shfl_xor_sync(0xFFFFFFFFu, v, d));
   if (lane == 0) red[warp] = v;
-  __syncthreads();
+  cta_sync();
   uint32_t r = red[0];
   for (int k = 1; k < kThreads / 32; ++k) r = min(r, red[k]);
-  __syncthreads();
+  cta_sync();
   return r;
 }
 
@@ -687,7 +712,7 @@ __device__ uint32_t block_tf_input(uint32_t f, uint32_t carry_in, uint32_t* red)
     if (lane >= d) incl = tf_then(o, incl);
   }
   if (lane == 31) red[warp] = incl;
-  __syncthreads();
+  cta_sync();
   if (threadIdx.x == 0) {
     uint32_t acc = 2u;  // identity
     for (int k = 0; k < kThreads / 32; ++k) {
@@ -696,12 +721,12 @@ __device__ uint32_t block_tf_input(uint32_t f, uint32_t carry_in, uint32_t* red)
       acc = tf_then(acc, t);
     }
   }
-  __syncthreads();
+  cta_sync();
   uint32_t excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
   if (lane == 0) excl = 2u;
   uint32_t before = tf_then(red[warp], excl);
   uint32_t r = tf_apply(before, carry_in);
-  __syncthreads();
+  cta_sync();
   return r;
 }
 
@@ -899,7 +924,7 @@ __device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, in
       uint32_t round_cnt;
       uint32_t pos = block_excl_scan(cnt, L.red, &round_cnt);
       for (uint32_t j = 0; j < cnt; ++j) L.stage[pos + j] = y[j];
-      __syncthreads();
+      cta_sync();
       for (uint32_t q = tid; q < round_cnt; q += kThreads) {
         uint32_t left = q == 0 ? prev_sym : L.stage[q - 1];
         uint32_t right = L.stage[q];
@@ -909,7 +934,7 @@ __device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, in
       if (round_cnt > 0) prev_sym = L.stage[round_cnt - 1];
       W += round_cnt;
       carry = L.carry[0];
-      __syncthreads();
+      cta_sync();
     }
     len = W;
     first_pass = false;
@@ -919,29 +944,55 @@ __device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, in
     B = (uint32_t)T.mrows[3 * best + 1];
     NW = (uint32_t)T.mrows[3 * best + 2];
   }
-  __syncthreads();
+  cta_sync();
   return len;
 }
 
-// Word-cache lookup of one short pre-token (window positions [kHalo + st,
-// + len)): writes its ids to sym[st ..] and returns their count, 0 if absent.
-__device__ __forceinline__ uint32_t cache_try(Smem& S, int st, int len, const Cache& C) {
+// Word-cache key of a short pre-token (window positions [kHalo + st, + len)):
+// its bytes as four little-endian words, zero past len, read with aligned
+// 32-bit shared loads and funnel shifts.
+struct CacheKey {
+  uint32_t x0, x1, x2, x3, len, slot;
+};
+
+__device__ __forceinline__ CacheKey cache_key(const Smem& S, int st, int len, const Cache& C) {
   const int ws = kHalo + st;
-  // The pre-token's first 16 window bytes, little-endian.
-  uint64_t k0 = (uint64_t)win_word(S, ws) | (uint64_t)win_word(S, ws + 4) << 32;
-  uint64_t k1 = (uint64_t)win_word(S, ws + 8) | (uint64_t)win_word(S, ws + 12) << 32;
-  if (len < 8) {
-    k0 &= (1ull << (8 * len)) - 1ull;
-    k1 = 0;
-  } else if (len == 8) {
-    k1 = 0;
-  } else if (len < 16) {
-    k1 &= (1ull << (8 * (len - 8))) - 1ull;
+  const uint32_t* wv = reinterpret_cast<const uint32_t*>(S.win) + (ws >> 2);
+  const uint32_t sh = (uint32_t)(ws & 3) * 8u;
+  const uint32_t a0 = lds_u32(wv), a1 = lds_u32(wv + 1), a2 = lds_u32(wv + 2), a3 = lds_u32(wv + 3),
+                 a4 = lds_u32(wv + 4);
+  auto keep = [len](int k) {
+    const int nb = len - 4 * k;
+    return nb >= 4 ? 0xFFFFFFFFu : (nb <= 0 ? 0u : ((1u << (8 * nb)) - 1u));
+  };
+  CacheKey K;
+  K.x0 = __funnelshift_r(a0, a1, sh) & keep(0);
+  K.x1 = __funnelshift_r(a1, a2, sh) & keep(1);
+  K.x2 = __funnelshift_r(a2, a3, sh) & keep(2);
+  K.x3 = __funnelshift_r(a3, a4, sh) & keep(3);
+  K.len = (uint32_t)len;
+  K.slot = cache_hash(K.x0, K.x1, K.x2, K.x3, K.len) & C.mask;
+  return K;
+}
+
+// Count of ids (1..3) for key K given the entry {ea, eb} at its first slot
+// (loaded by the caller), 0 when absent; the ids go to ids[0..2].
+__device__ __forceinline__ uint32_t cache_resolve(const Cache& C, const CacheKey& K, uint4 ea, uint4 eb,
+                                                  uint32_t* ids) {
+  uint32_t slot = K.slot;
+  for (uint32_t probe = 0; probe <= C.mask; ++probe) {
+    if (eb.x == 0) return 0;
+    if ((eb.x & 31u) == K.len && ea.x == K.x0 && ea.y == K.x1 && ea.z == K.x2 && ea.w == K.x3) {
+      ids[0] = eb.y;
+      ids[1] = eb.z;
+      ids[2] = eb.w;
+      return (eb.x >> 5) & 7u;
+    }
+    slot = (slot + 1) & C.mask;
+    ea = __ldg(C.e + 2 * slot);
+    eb = __ldg(C.e + 2 * slot + 1);
   }
-  uint32_t ids[kCacheMaxIds];
-  const uint32_t cnt = cache_lookup(C, k0, k1, (uint32_t)len, ids);
-  for (uint32_t q = 0; q < cnt; ++q) S.sym[st + q] = ids[q];
-  return cnt;
+  return 0;
 }
 
 __device__ __forceinline__ uint32_t merge_at(Smem& S, int st, int len, const Tables& T) {
@@ -998,20 +1049,16 @@ struct EncodeArgs {
   int64_t n_chunks;
 };
 
-// Exclusive prefix of chunk c from the chained scan; called by warp 0. Lane
-// l reads the descriptor of chunk (base - l); the window slides back until an
-// inclusive prefix is found.
-__device__ int64_t look_back(uint64_t* desc, int64_t c, uint32_t agg, DevSmall* small) {
+// Exclusive prefix of chunk c from the chained scan, by the look-back warp
+// while the other warps encode the chunk. Lane l reads the descriptor of
+// chunk (base - l); the window slides back until an inclusive prefix is found.
+// A wait that makes no progress for kWaitLimitNs sets the timeout status and
+// returns what was summed so far.
+__device__ int64_t look_back(const uint64_t* desc, int64_t c, DevSmall* small) {
   const int lane = threadIdx.x & 31;
-  if (c == 0) {
-    if (lane == 0) st_relaxed(&desc[0], kDescIncl | (uint64_t)agg);
-    return 0;
-  }
-  if (lane == 0) st_relaxed(&desc[c], kDescAgg | (uint64_t)agg);
   int64_t excl = 0, base = c - 1;
   const uint64_t t_start = global_timer();
-  bool timed_out = false;
-  for (;;) {
+  while (base >= 0) {
     const int64_t j = base - lane;
     const uint64_t d = j >= 0 ? ld_relaxed(&desc[j]) : kDescIncl;
     const uint32_t ready = __ballot_sync(0xFFFFFFFFu, (d & ~kDescValue) != 0);
@@ -1023,10 +1070,10 @@ __device__ int64_t look_back(uint64_t* desc, int64_t c, uint32_t agg, DevSmall* 
       if (lane == 0) out = global_timer() - t_start > kWaitLimitNs;
       out = __shfl_sync(0xFFFFFFFFu, out, 0);
       if (out) {
-        timed_out = true;
+        if (lane == 0) atomicOr(&small->status, kStTimeout);
         break;
       }
-      __nanosleep(32);
+      __nanosleep(64);
       continue;
     }
     uint64_t v = (need >> lane) & 1u ? (d & kDescValue) : 0;
@@ -1036,33 +1083,42 @@ __device__ int64_t look_back(uint64_t* desc, int64_t c, uint32_t agg, DevSmall* 
     if (incl) break;
     base -= 32;
   }
-  if (lane == 0) {
-    if (timed_out) atomicOr(&small->status, kStTimeout);
-    st_relaxed(&desc[c], kDescIncl | (uint64_t)(excl + agg));
-  }
   return excl;
 }
 
-__global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
+// Launched with kThreads + 32 threads: warps 0..7 encode chunk c, warp 8
+// finds the chunk's output offset meanwhile (named barriers 2 and 3 hand the
+// chunk's token count to it and the offset back).
+constexpr int kEncodeThreads = kThreads + 32;
+
+__global__ void __launch_bounds__(kEncodeThreads) k_encode(EncodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
 
   if (tid == 0) S.chunk = (int64_t)atomicAdd(&a.small->ticket, 1u);
-  for (int i = tid; i < 256; i += kThreads) S.byte_id[i] = a.T.byte_id[i];
+  for (int i = tid; i < 256; i += kEncodeThreads) S.byte_id[i] = a.T.byte_id[i];
   __syncthreads();
   const int64_t c = S.chunk;
   const int64_t c0 = c * kChunk;
-  load_window(S, a.bytes, a.n_bytes, a.doc_offsets, a.n_docs, c0, a.first_doc[c]);
-  {
-    // Start bits of [c0, c0 + kSpan) from the split kernel's bitmask.
-    const int64_t n_words = (a.n_bytes + 31) / 32;
-    for (int w = tid; w < kSpanWords; w += kThreads) {
-      const int64_t gw = c0 / 32 + w;
-      S.startbits[w] = gw < n_words ? a.start_bits[gw] : 0u;
+  if (tid >= kThreads) {  // the look-back warp
+    const int64_t excl = look_back(a.desc, c, a.small);
+    named_sync(2, kEncodeThreads);  // the chunk's token count is in S.agg
+    if (tid == kThreads) {
+      const uint32_t agg = S.agg;
+      st_relaxed(&a.desc[c], kDescIncl | (uint64_t)(excl + agg));
+      S.prefix = excl;
+      if (c == a.n_chunks - 1) a.small->total = excl + agg;
     }
-    __syncthreads();
+    __syncwarp();
+    named_arrive(3, kEncodeThreads);
+    return;
   }
+  // The first document starting at or after c0 and, ahead of their use at
+  // the end, the offsets of the first kThreads documents from there on.
+  const int64_t k_first = __ldg(a.first_doc + c);
+  const int64_t d_mine = k_first + tid <= a.n_docs ? __ldg(a.doc_offsets + k_first + tid) : INT64_MAX;
+  load_encode_window(S, a.bytes, a.n_bytes, a.doc_offsets, a.n_docs, a.start_bits, c0);
 
   // Pre-tokens starting in the chunk, in order. Thread t owns positions
   // [16 t, 16 t + 16) of the chunk.
@@ -1084,7 +1140,7 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
       S.last_end = -1;
     }
   }
-  __syncthreads();
+  cta_sync();
   const uint32_t n_spans = S.n_spans;
 
   // End of the last pre-token: the next start or document edge in the margin,
@@ -1096,7 +1152,7 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
       const int wj = (base >> 5) + tid;
       uint32_t m = 0;
       if (wj < kSpanWords) {
-        m = S.startbits[wj] | bits32_at(S.outbits, kHalo + wj * 32) | bits32_at(S.docbits, kHalo + wj * 32);
+        m = S.startbits[wj] | bits32_at(S.outbits, kHalo + wj * 32);
         const int lo_bit = from - wj * 32;
         if (lo_bit > 0) m = lo_bit >= 32 ? 0u : (m & (0xFFFFFFFFu << lo_bit));
       }
@@ -1110,36 +1166,64 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
     }
     if (tid == 0) S.last_end = end;
   }
-  __syncthreads();
+  cta_sync();
 
-  // Short pre-tokens, one thread each. Word-cache hits finish here; misses
-  // are queued and merged next by all threads together, so a warp does not
-  // wait on the merge loop of a few of its lanes.
-  for (uint32_t j = tid; j < n_spans; j += kThreads) {
-    const int st = S.span_start[j];
-    const int64_t en = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
-    const int len = en < 0 ? kSpan : (int)(en - (c0 + st));
-    if (en >= 0 && len <= kShortMax) {
-      const uint32_t cnt = (a.C.enabled && len <= kCacheMaxLen) ? cache_try(S, st, len, a.C) : 0u;
-      if (cnt) {
-        S.span_cnt[j] = cnt;
-      } else if (len <= kCacheMaxLen) {
-        const uint32_t slot = atomicAdd(&S.n_miss, 1u);
-        if (slot < kMissShortCap) S.missq[slot] = (uint16_t)j;
-        else S.span_cnt[j] = merge_at(S, st, len, a.T);  // queue full: merge here
-      } else {
-        const uint32_t slot = atomicAdd(&S.n_miss_m, 1u);
-        if (slot < kMissMedCap) S.missq[kMissShortCap + slot] = (uint16_t)j;
-        else S.span_cnt[j] = merge_at(S, st, len, a.T);
+  // Short pre-tokens, one thread each, two per round with their word-cache
+  // probes in flight together. Hits finish here; misses are queued and
+  // merged next by lane groups, so a warp does not wait on the merge loop of
+  // a few of its lanes.
+  for (uint32_t j0 = tid; j0 < n_spans; j0 += 2 * kThreads) {
+    int st[2], len[2];
+    bool shortp[2], probe[2];
+    CacheKey K[2];
+    uint4 ea[2], eb[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t j = j0 + (uint32_t)h * kThreads;
+      st[h] = 0;
+      len[h] = 0;
+      shortp[h] = probe[h] = false;
+      if (j < n_spans) {
+        st[h] = S.span_start[j];
+        const int64_t en = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
+        len[h] = en < 0 ? kSpan : (int)(en - (c0 + st[h]));
+        shortp[h] = en >= 0 && len[h] <= kShortMax;
+        probe[h] = shortp[h] && a.C.enabled && len[h] <= kCacheMaxLen;
       }
-    } else {
-      uint32_t slot = atomicAdd(&S.n_long, 1u);
-      if (slot < (uint32_t)kMaxLong) S.long_list[slot] = (uint16_t)j;
-      else atomicOr(&a.small->status, kStInternal);
-      S.span_cnt[j] = 0;
+      if (probe[h]) {
+        K[h] = cache_key(S, st[h], len[h], a.C);
+        ea[h] = __ldg(a.C.e + 2 * K[h].slot);
+        eb[h] = __ldg(a.C.e + 2 * K[h].slot + 1);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t j = j0 + (uint32_t)h * kThreads;
+      if (j >= n_spans) continue;
+      if (shortp[h]) {
+        uint32_t ids[kCacheMaxIds];
+        const uint32_t cnt = probe[h] ? cache_resolve(a.C, K[h], ea[h], eb[h], ids) : 0u;
+        if (cnt) {
+          for (uint32_t q = 0; q < cnt; ++q) S.sym[st[h] + q] = ids[q];
+          S.span_cnt[j] = cnt;
+        } else if (len[h] <= kCacheMaxLen) {
+          const uint32_t slot = atomicAdd(&S.n_miss, 1u);
+          if (slot < kMissShortCap) S.missq[slot] = (uint16_t)j;
+          else S.span_cnt[j] = merge_at(S, st[h], len[h], a.T);  // queue full: merge here
+        } else {
+          const uint32_t slot = atomicAdd(&S.n_miss_m, 1u);
+          if (slot < kMissMedCap) S.missq[kMissShortCap + slot] = (uint16_t)j;
+          else S.span_cnt[j] = merge_at(S, st[h], len[h], a.T);
+        }
+      } else {
+        const uint32_t slot = atomicAdd(&S.n_long, 1u);
+        if (slot < (uint32_t)kMaxLong) S.long_list[slot] = (uint16_t)j;
+        else atomicOr(&a.small->status, kStInternal);
+        S.span_cnt[j] = 0;
+      }
     }
   }
-  __syncthreads();
+  cta_sync();
   {
     // Queued misses: up to 16 bytes by groups of 8 lanes, longer ones by a
     // warp each.
@@ -1172,7 +1256,7 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
       if (q < n_med && (tid & 31) == 0) S.span_cnt[j] = cnt;
     }
   }
-  __syncthreads();
+  cta_sync();
 
   // Long pre-tokens: the whole CTA, one at a time, in order.
   const uint32_t n_long = min(S.n_long, (uint32_t)kMaxLong);
@@ -1188,7 +1272,7 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
         S.long_list[y + 1] = v;
       }
     }
-    __syncthreads();
+    cta_sync();
     LongScratch L{S.u.stage, S.red, S.carry};
     for (uint32_t x = 0; x < n_long; ++x) {
       const uint32_t j = S.long_list[x];
@@ -1214,7 +1298,7 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
           S.doc_lo = dlo;
           S.doc_hi = dhi;
         }
-        __syncthreads();
+        cta_sync();
         const int64_t dlo = S.doc_lo, dhi = S.doc_hi;
         int64_t found = dhi;
         for (int64_t base = c0 + kSpan; base < dhi; base += kThreads) {
@@ -1237,7 +1321,7 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
         uint32_t cnt = merge_long(a.bytes, s, (uint32_t)n, a.pool + s, a.T, S.byte_id, L);
         if (tid == 0) S.span_cnt[j] = cnt;
       }
-      __syncthreads();
+      cta_sync();
     }
   }
 
@@ -1257,30 +1341,30 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
     }
     if (tid == 0) S.span_cnt[n_spans] = agg;
   }
+  cta_sync();
 
-  // Chained scan over chunks.
-  if (tid < 32) {
-    const int64_t excl = look_back(a.desc, c, agg, a.small);
-    if (tid == 0) {
-      S.prefix = excl;
-      if (c == a.n_chunks - 1) a.small->total = excl + agg;
+  // Hand the chunk's token count to the look-back warp (and publish it for
+  // later chunks), stage the ids in output order, then take the offset.
+  if (tid == 0) {
+    S.agg = agg;
+    st_relaxed(&a.desc[c], kDescAgg | (uint64_t)agg);
+  }
+  named_arrive(2, kEncodeThreads);
+  if (n_long == 0) {
+    for (uint32_t j = tid; j < n_spans; j += kThreads) {
+      const int st = S.span_start[j];
+      const uint32_t o = S.span_cnt[j], cnt = S.span_cnt[j + 1] - o;
+      for (uint32_t q = 0; q < cnt; ++q) S.u.ostage[o + q] = S.sym[st + q];
     }
   }
-  __syncthreads();
+  named_sync(3, kEncodeThreads);
   const int64_t P = S.prefix;
 
   // Ids past the caller's capacity are not written; the call reports it.
   if (tid == 0 && P + (int64_t)agg > a.out_capacity) atomicOr(&a.small->status, kStCapacity);
 
   if (n_long == 0) {
-    // All ids are in shared memory: gather them in output order, then store
-    // them coalesced.
-    for (uint32_t j = tid; j < n_spans; j += kThreads) {
-      const int st = S.span_start[j];
-      const uint32_t o = S.span_cnt[j], cnt = S.span_cnt[j + 1] - o;
-      for (uint32_t q = 0; q < cnt; ++q) S.u.ostage[o + q] = S.sym[st + q];
-    }
-    __syncthreads();
+    // All ids are in shared memory, in output order: store them coalesced.
     const int64_t lim = a.out_capacity - P;
     for (uint32_t q = tid; q < agg; q += kThreads)
       if ((int64_t)q < lim) a.out_ids[P + q] = (int32_t)S.u.ostage[q];
@@ -1309,9 +1393,8 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
 
   // Offsets of the documents that start in this chunk.
   {
-    int64_t k0 = a.first_doc[c];
-    for (int64_t k = k0 + tid; k <= a.n_docs; k += kThreads) {
-      const int64_t d = a.doc_offsets[k];
+    for (int64_t k = k_first + tid; k <= a.n_docs; k += kThreads) {
+      const int64_t d = k == k_first + tid ? d_mine : a.doc_offsets[k];
       if (d >= c0 + kChunk) break;
       if (d < c0) continue;
       const int rel = (int)(d - c0);
@@ -1330,8 +1413,7 @@ __global__ void __launch_bounds__(kThreads) k_encode(EncodeArgs a) {
 __global__ void __launch_bounds__(kThreads) k_pretokenize(const uint8_t* bytes, int64_t n_bytes,
                                                           const int64_t* doc_offsets, int64_t n_docs,
                                                           const int64_t* first_doc, uint32_t* out_bits) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  __shared__ SplitSmem S;
   const int64_t c0 = (int64_t)blockIdx.x * kChunk;
   if (threadIdx.x == 0) {
     if (first_doc) {
@@ -1602,7 +1684,8 @@ int build_word_cache(bpe_handle* h, const uint8_t* vocab_bytes, const int64_t* v
       if (q < 8) k0 |= b << (8 * q);
       else k1 |= b << (8 * (q - 8));
     }
-    uint64_t slot = cache_hash(k0, k1, len) & (slots - 1);
+    uint64_t slot =
+        cache_hash((uint32_t)k0, (uint32_t)(k0 >> 32), (uint32_t)k1, (uint32_t)(k1 >> 32), len) & (slots - 1);
     while (table[slot * 2 + 1].x != 0) slot = (slot + 1) & (slots - 1);
     table[slot * 2] = make_uint4((uint32_t)k0, (uint32_t)(k0 >> 32), (uint32_t)k1, (uint32_t)(k1 >> 32));
     table[slot * 2 + 1] = make_uint4(len | (cnt << 5) | (1u << 31), vals[4 * i + 1], vals[4 * i + 2], vals[4 * i + 3]);
@@ -1651,7 +1734,6 @@ int noalloc_setup(int dev, unsigned char** base) {
     if (reinterpret_cast<uintptr_t>(p) & 255u)
       return fail(BPE_ERR_INTERNAL, "bpe_encode_batch_noalloc: scratch not 256-byte aligned");
     CK(cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
-    CK(cudaFuncSetAttribute(k_pretokenize, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
     g_noalloc_base[dev] = static_cast<unsigned char*>(p);
   }
   *base = g_noalloc_base[dev];
@@ -1829,7 +1911,6 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
   uint32_t* bits = (uint32_t*)(pool + n_bytes + 4);
   if (!h->smem_set) {
     CK(cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
-    CK(cudaFuncSetAttribute(k_pretokenize, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
     h->smem_set = true;
   }
   int prep_blocks = (int)std::min<int64_t>(4096, std::max<int64_t>(n_chunks, n_docs + 1) / 256 + 1);
@@ -1853,11 +1934,11 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
   a.n_chunks = n_chunks;
   if (h->ev_start) CK(cudaEventRecord(h->ev_start, st));
   if (n_bytes > 0) {
-    k_pretokenize<<<(unsigned)((n_bytes + kChunk - 1) / kChunk), kThreads, sizeof(Smem), st>>>(
+    k_pretokenize<<<(unsigned)((n_bytes + kChunk - 1) / kChunk), kThreads, 0, st>>>(
         d_bytes, n_bytes, d_doc_offsets, n_docs, first_doc, bits);
     CK(cudaGetLastError());
   }
-  k_encode<<<(unsigned)n_chunks, kThreads, sizeof(Smem), st>>>(a);
+  k_encode<<<(unsigned)n_chunks, kEncodeThreads, sizeof(Smem), st>>>(a);
   CK(cudaGetLastError());
   if (h->ev_stop) CK(cudaEventRecord(h->ev_stop, st));
   if (h_total_tokens) {
@@ -1916,11 +1997,11 @@ int bpe_encode_batch_noalloc(bpe_handle* h, const uint8_t* d_bytes, int64_t n_by
   a.small = h->d_small;
   a.n_chunks = n_chunks;
   if (n_bytes > 0) {
-    k_pretokenize<<<(unsigned)((n_bytes + kChunk - 1) / kChunk), kThreads, sizeof(Smem), st>>>(
+    k_pretokenize<<<(unsigned)((n_bytes + kChunk - 1) / kChunk), kThreads, 0, st>>>(
         d_bytes, n_bytes, d_doc_offsets, n_docs, first_doc, bits);
     CK(cudaGetLastError());
   }
-  k_encode<<<(unsigned)n_chunks, kThreads, sizeof(Smem), st>>>(a);
+  k_encode<<<(unsigned)n_chunks, kEncodeThreads, sizeof(Smem), st>>>(a);
   CK(cudaGetLastError());
   if (h_total_tokens) {
     DevSmall s;
@@ -1937,15 +2018,8 @@ int bpe_pretokenize_batch(const uint8_t* d_bytes, int64_t n_bytes, const int64_t
   if (!d_doc_offsets || n_bytes < 0 || n_docs < 0 || (n_bytes > 0 && (!d_bytes || !d_start_bits)))
     return fail(BPE_ERR_INVALID_ARG, "bpe_pretokenize_batch: bad arguments");
   if (n_bytes == 0) return BPE_OK;
-  static thread_local int smem_set_dev = -1;
-  int dev = 0;
-  CK(cudaGetDevice(&dev));
-  if (smem_set_dev != dev) {
-    CK(cudaFuncSetAttribute(k_pretokenize, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
-    smem_set_dev = dev;
-  }
   const int64_t n_chunks = (n_bytes + kChunk - 1) / kChunk;
-  k_pretokenize<<<(unsigned)n_chunks, kThreads, sizeof(Smem), (cudaStream_t)stream>>>(d_bytes, n_bytes, d_doc_offsets,
+  k_pretokenize<<<(unsigned)n_chunks, kThreads, 0, (cudaStream_t)stream>>>(d_bytes, n_bytes, d_doc_offsets,
                                                                                       n_docs, nullptr, d_start_bits);
   CK(cudaGetLastError());
   return BPE_OK;
