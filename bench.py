@@ -129,11 +129,32 @@ def dist_env():
     return world, rank, local
 
 
-def load_workload(cfg: int, rank: int, n_docs: int | None = None):
+def shard(cfg: int, rank: int, n_docs: int | None = None) -> tuple[int, int]:
+    """(first document, count) a rank encodes: every rank takes a full
+    workload's worth of its own documents of the same generator (weak
+    scaling; no data is exchanged between ranks)."""
     n = n_docs or workloads.n_docs(cfg)
-    data, offsets = workloads.docs(cfg, rank * n, n)
+    return rank * n, n
+
+
+def load_workload(cfg: int, rank: int, n_docs: int | None = None):
+    first, n = shard(cfg, rank, n_docs)
+    data, offsets = workloads.docs(cfg, first, n)
     merges, vb, vo = workloads.table(cfg)
     return data, offsets, merges, vb, vo
+
+
+def reduce_ranks(dist, device, times: list[float], counts: list[float]) -> tuple[list[float], list[float]]:
+    """Max over ranks of each time, sum over ranks of each count (a no-op
+    without a process group)."""
+    if dist is None:
+        return list(times), list(counts)
+    import torch
+    t = torch.tensor(times, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    c = torch.tensor(counts, dtype=torch.float64, device=device)
+    dist.all_reduce(c, op=dist.ReduceOp.SUM)
+    return t.tolist(), c.tolist()
 
 
 def algorithmic_bytes(n_bytes: int, n_docs: int, n_tokens: int) -> int:
@@ -280,15 +301,6 @@ def run_gpu(args, world, rank, local):
     nocache_ms = nc0.elapsed_time(nc1) / nc_steps
     bpe.bpe_set_word_cache(handle, True)
     bpe.bpe_sync_status(handle, s_ptr)
-    if dist:
-        t = torch.tensor([step_ms, kern_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, kern_ms = float(t[0]), float(t[1])
-        tot = torch.tensor([n_bytes, n_tokens], device=dev, dtype=torch.float64)
-        dist.all_reduce(tot)
-        all_bytes, all_tokens = float(tot[0]), float(tot[1])
-    else:
-        all_bytes, all_tokens = float(n_bytes), float(n_tokens)
 
     # End to end through the public call: pinned host input, H2D, encode
     # (waits for the count), D2H of ids and offsets.
@@ -307,6 +319,8 @@ def run_gpu(args, world, rank, local):
         h_out.copy_(d_out, non_blocking=True)
         torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - e0) / e2e_steps
+    (step_ms, kern_ms, e2e_s), (all_bytes, all_tokens, all_docs) = reduce_ranks(
+        dist, dev, [step_ms, kern_ms, e2e_s], [n_bytes, n_tokens, n_docs])
 
     out = None
     if rank == 0:
@@ -333,13 +347,13 @@ def run_gpu(args, world, rank, local):
             "hbm_gbs_achieved": round(achieved, 2),
             "config": {"workload": workloads.NAMES[cfg], "n_docs": n_docs, "n_bytes": n_bytes,
                        "tokens": int(n_tokens), "merges": int(len(merges)), "n_vocab": int(len(vo) - 1),
-                       "l2": "inputs (1 GiB) larger than L2; no flush", "parallelism": f"replicas x{world}"},
+                       "l2": (f"inputs ({n_bytes / 2**20:.0f} MiB) larger than L2 (129 MB); no flush" if n_bytes > 129e6 else f"inputs ({n_bytes / 2**20:.0f} MiB) fit in L2: a profiling case, not a bench number"), "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                         "kernel": "k_encode", "kernel_ms": round(kern_ms, 4),
+                         "kernel": "k_pretokenize+k_encode", "kernel_ms": round(kern_ms, 4),
                          "algorithmic_bytes_per_launch": alg, "traffic": traffic_from_profile()},
             "cpu_baseline": cpu,
-            "e2e": {"value": round(all_bytes / e2e_s / 1e6 if world == 1 else n_bytes / e2e_s / 1e6, 3),
+            "e2e": {"value": round(all_bytes / e2e_s / 1e6, 3),
                     "unit": "MB/s", "h2d_bytes_per_step": n_bytes + 8 * (n_docs + 1),
                     "d2h_bytes_per_step": 4 * int(n_tokens) + 8 * (n_docs + 1)},
             "without_word_cache": {"value": round(n_bytes / (nocache_ms / 1e3) / 1e6, 3), "unit": "MB/s",
