@@ -382,10 +382,8 @@ struct Smem : SplitSmem {
   uint32_t span_cnt[kChunk + 1];     // token counts, then exclusive offsets
   uint32_t sym[kSpan];               // ids of short pre-tokens, at their start position
   union {
-    uint32_t rk[kSpan];              // pair ranks while one thread merges a short pre-token
     GroupScratch grp[kThreads / 32]; // one per warp while lane groups merge cache misses
     uint32_t stage[kRound];          // long merge rounds
-    uint32_t ostage[kSpan];          // ids in output order
   } u;
   int32_t byte_id[256];
   uint16_t long_list[kMaxLong];
@@ -406,6 +404,8 @@ struct Smem : SplitSmem {
 __device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void named_arrive(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+static_assert(4 * (sizeof(Smem) + 1024) <= 228 * 1024, "four encode CTAs fit in an SM's shared memory");
 
 __device__ __forceinline__ bool bit_at(const uint32_t* bits, int i) { return (bits[i >> 5] >> (i & 31)) & 1u; }
 
@@ -995,8 +995,11 @@ __device__ __forceinline__ uint32_t cache_resolve(const Cache& C, const CacheKey
   return 0;
 }
 
+// One thread merges a short pre-token in place (used when the miss queue is
+// full or the word cache is off); its pair ranks live in local memory.
 __device__ __forceinline__ uint32_t merge_at(Smem& S, int st, int len, const Tables& T) {
-  return (uint32_t)merge_short(S.sym + st, S.u.rk + st, S.win + kHalo + st, len, T, S.byte_id);
+  uint32_t rk[kShortMax];
+  return (uint32_t)merge_short(S.sym + st, rk, S.win + kHalo + st, len, T, S.byte_id);
 }
 
 // ------------------------------------------------------------------ kernels --
@@ -1091,7 +1094,7 @@ __device__ int64_t look_back(const uint64_t* desc, int64_t c, DevSmall* small) {
 // chunk's token count to it and the offset back).
 constexpr int kEncodeThreads = kThreads + 32;
 
-__global__ void __launch_bounds__(kEncodeThreads) k_encode(EncodeArgs a) {
+__global__ void __launch_bounds__(kEncodeThreads, 4) k_encode(EncodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
@@ -1350,13 +1353,6 @@ __global__ void __launch_bounds__(kEncodeThreads) k_encode(EncodeArgs a) {
     st_relaxed(&a.desc[c], kDescAgg | (uint64_t)agg);
   }
   named_arrive(2, kEncodeThreads);
-  if (n_long == 0) {
-    for (uint32_t j = tid; j < n_spans; j += kThreads) {
-      const int st = S.span_start[j];
-      const uint32_t o = S.span_cnt[j], cnt = S.span_cnt[j + 1] - o;
-      for (uint32_t q = 0; q < cnt; ++q) S.u.ostage[o + q] = S.sym[st + q];
-    }
-  }
   named_sync(3, kEncodeThreads);
   const int64_t P = S.prefix;
 
@@ -1364,10 +1360,25 @@ __global__ void __launch_bounds__(kEncodeThreads) k_encode(EncodeArgs a) {
   if (tid == 0 && P + (int64_t)agg > a.out_capacity) atomicOr(&a.small->status, kStCapacity);
 
   if (n_long == 0) {
-    // All ids are in shared memory, in output order: store them coalesced.
+    // All ids are in shared memory, each span's at its start position. Warp w
+    // stores output positions [agg w / 8, agg (w + 1) / 8), a lane per
+    // position, coalesced: the span holding position o is the last one whose
+    // offset is at most o. Every span has at least one id, so a lane's next
+    // position (32 further) lies at most 32 spans further.
+    const int warp = tid >> 5, lane = tid & 31;
+    const uint32_t lo = (uint32_t)((uint64_t)agg * warp / (kThreads / 32));
+    const uint32_t hi = (uint32_t)((uint64_t)agg * (warp + 1) / (kThreads / 32));
     const int64_t lim = a.out_capacity - P;
-    for (uint32_t q = tid; q < agg; q += kThreads)
-      if ((int64_t)q < lim) a.out_ids[P + q] = (int32_t)S.u.ostage[q];
+    uint32_t jl = 0, jh = n_spans;  // span_cnt[jl] <= o < span_cnt[jh] (span_cnt[n_spans] = agg)
+    for (uint32_t o = lo + lane; o < hi; o += 32) {
+      while (jh - jl > 1) {
+        const uint32_t mid = (jl + jh) >> 1;
+        if (S.span_cnt[mid] <= o) jl = mid;
+        else jh = mid;
+      }
+      if ((int64_t)o < lim) a.out_ids[P + o] = (int32_t)S.sym[S.span_start[jl] + (o - S.span_cnt[jl])];
+      jh = min(n_spans, jl + 33);
+    }
   } else {
     // Long pre-tokens: copy from their scratch range of the pool.
     for (uint32_t x = 0; x < n_long; ++x) {
