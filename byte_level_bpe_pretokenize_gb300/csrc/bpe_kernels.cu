@@ -366,7 +366,7 @@ struct GroupScratch {
 
 // What the split needs: the window and its document and start bit masks. The
 // split kernel's shared memory is only this; the encode kernel's extends it.
-struct SplitSmem {
+struct __align__(16) SplitSmem {
   uint8_t win[kWin + 16];
   uint32_t docbits[kWinWords + 2];   // a document (or the area after the last one) starts here
   uint32_t outbits[kWinWords + 2];   // byte belongs to no document
@@ -395,7 +395,8 @@ struct Smem : SplitSmem {
   uint32_t n_long;
   uint32_t n_miss;                   // queued misses of <= 16 bytes
   uint32_t n_miss_m;                 // queued misses of 17..kShortMax bytes
-  int64_t last_end;
+  int64_t last_end;                  // end of the chunk's last pre-token, -1 past the window
+  int last_end_rel;                  // the same relative to the chunk start
   int64_t doc_lo, doc_hi;  // document of a long pre-token that runs past the window
 };
 
@@ -542,33 +543,33 @@ __device__ uint32_t start_mask16(const SplitSmem& S, int p0) {
 __device__ void load_window(SplitSmem& S, const uint8_t* bytes, int64_t n_bytes, const int64_t* doc_offsets,
                             int64_t n_docs, int64_t c0, int64_t first_doc) {
   const int tid = threadIdx.x;
-  const int64_t w0 = c0 - kHalo;
-  // 32-bit word loads when the input is word aligned, bytes otherwise.
-  const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 3u) == 0;
-  const uint32_t* g32 = reinterpret_cast<const uint32_t*>(bytes);
+  const int64_t w0 = c0 - kHalo, w_end = w0 + kWin;
+  // Every load is issued before the first barrier: the bytes, the first and
+  // last document offsets, and the offsets of the documents from 32 before
+  // first_doc on (one per thread; more only when documents are tiny).
+  int64_t d_first = __ldg(doc_offsets), d_last = __ldg(doc_offsets + n_docs);
+  int64_t k_lo = first_doc - 32;
+  if (k_lo > n_docs) k_lo = n_docs;
+  if (k_lo < 0) k_lo = 0;
+  const int64_t o_before = k_lo > 0 ? __ldg(doc_offsets + k_lo - 1) : INT64_MIN;
+  const int64_t o_mine = k_lo + tid <= n_docs ? __ldg(doc_offsets + k_lo + tid) : INT64_MAX;
+  // 16-byte loads and stores when the input is 16-byte aligned (window
+  // offsets are multiples of 16), bytes otherwise.
+  const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 15u) == 0;
   for (int i = tid * 16; i < kWin; i += kThreads * 16) {
     const int64_t p = w0 + i;
     if (aligned && p >= 0 && p + 16 <= n_bytes) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t w = __ldg(g32 + (p >> 2) + k);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) S.win[i + 4 * k + q] = (uint8_t)(w >> (8 * q));
-      }
+      *reinterpret_cast<uint4*>(S.win + i) = __ldg(reinterpret_cast<const uint4*>(bytes + p));
     } else {
 #pragma unroll
       for (int k = 0; k < 16; ++k) S.win[i + k] = (p + k >= 0 && p + k < n_bytes) ? bytes[p + k] : 0;
     }
   }
-  for (int i = tid; i < kWinWords + 2; i += kThreads) {
-    S.docbits[i] = 0;
-    S.outbits[i] = 0;
-  }
+  for (int i = tid; i < kWinWords + 2; i += kThreads) S.docbits[i] = 0;
   cta_sync();
-  int64_t d_first = doc_offsets[0], d_last = doc_offsets[n_docs];
   d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
   d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
-  for (int wi = tid; wi < kWinWords; wi += kThreads) {
+  for (int wi = tid; wi < kWinWords + 2; wi += kThreads) {
     uint32_t word = 0;
     const int64_t p = w0 + (int64_t)wi * 32;
     if (p < d_first || p + 32 > d_last) {
@@ -577,18 +578,26 @@ __device__ void load_window(SplitSmem& S, const uint8_t* bytes, int64_t n_bytes,
     }
     S.outbits[wi] = word;
   }
-  // Document starts in the window: walk back from first_doc over starts in
-  // the halo, then forward.
-  int64_t k_lo = first_doc;
-  if (k_lo > n_docs) k_lo = n_docs;
-  if (k_lo < 0) k_lo = 0;
-  while (k_lo > 0 && doc_offsets[k_lo - 1] >= w0) --k_lo;
-  const int64_t w_end = w0 + kWin;
-  for (int64_t k = k_lo + tid; k <= n_docs; k += kThreads) {
-    int64_t o = doc_offsets[k];
-    if (o >= w_end) break;
-    if (o >= w0) {
-      int i = (int)(o - w0);
+  // Document starts in the window.
+  if (o_mine >= w0 && o_mine < w_end) {
+    const int i = (int)(o_mine - w0);
+    atomicOr(&S.docbits[i >> 5], 1u << (i & 31));
+  }
+  if (o_mine < w_end) {  // tiny documents: more than kThreads - 32 start in the window
+    for (int64_t k = k_lo + tid + kThreads; k <= n_docs; k += kThreads) {
+      const int64_t o = doc_offsets[k];
+      if (o >= w_end) break;
+      if (o >= w0) {
+        const int i = (int)(o - w0);
+        atomicOr(&S.docbits[i >> 5], 1u << (i & 31));
+      }
+    }
+  }
+  if (tid == 0 && o_before >= w0) {  // more than 32 documents start in the left halo
+    for (int64_t k = k_lo - 1; k >= 0; --k) {
+      const int64_t o = doc_offsets[k];
+      if (o < w0) break;
+      const int i = (int)(o - w0);
       atomicOr(&S.docbits[i >> 5], 1u << (i & 31));
     }
   }
@@ -604,17 +613,13 @@ __device__ void load_encode_window(SplitSmem& S, const uint8_t* bytes, int64_t n
   const int tid = threadIdx.x;
   const int64_t w0 = c0 - kHalo;
   int64_t d_first = __ldg(doc_offsets), d_last = __ldg(doc_offsets + n_docs);
-  const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 3u) == 0;
-  const uint32_t* g32 = reinterpret_cast<const uint32_t*>(bytes);
+  // 16-byte loads and stores when the input is 16-byte aligned (window
+  // offsets are multiples of 16), bytes otherwise.
+  const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 15u) == 0;
   for (int i = tid * 16; i < kWin; i += kThreads * 16) {
     const int64_t p = w0 + i;
     if (aligned && p >= 0 && p + 16 <= n_bytes) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t w = __ldg(g32 + (p >> 2) + k);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) S.win[i + 4 * k + q] = (uint8_t)(w >> (8 * q));
-      }
+      *reinterpret_cast<uint4*>(S.win + i) = __ldg(reinterpret_cast<const uint4*>(bytes + p));
     } else {
 #pragma unroll
       for (int k = 0; k < 16; ++k) S.win[i + k] = (p + k >= 0 && p + k < n_bytes) ? bytes[p + k] : 0;
@@ -1061,6 +1066,7 @@ __device__ int64_t look_back(const uint64_t* desc, int64_t c, DevSmall* small) {
   const int lane = threadIdx.x & 31;
   int64_t excl = 0, base = c - 1;
   const uint64_t t_start = global_timer();
+  uint32_t sleep_ns = 64;
   while (base >= 0) {
     const int64_t j = base - lane;
     const uint64_t d = j >= 0 ? ld_relaxed(&desc[j]) : kDescIncl;
@@ -1076,9 +1082,11 @@ __device__ int64_t look_back(const uint64_t* desc, int64_t c, DevSmall* small) {
         if (lane == 0) atomicOr(&small->status, kStTimeout);
         break;
       }
-      __nanosleep(64);
+      __nanosleep(sleep_ns);
+      sleep_ns = min(2u * sleep_ns, 1024u);
       continue;
     }
+    sleep_ns = 64;
     uint64_t v = (need >> lane) & 1u ? (d & kDescValue) : 0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
@@ -1140,36 +1148,32 @@ __global__ void __launch_bounds__(kEncodeThreads, 4) k_encode(EncodeArgs a) {
       S.n_long = 0;
       S.n_miss = 0;
       S.n_miss_m = 0;
-      S.last_end = -1;
+      if (total == 0) {
+        S.last_end = -1;
+        S.last_end_rel = -1;
+      }
+    }
+    // The thread holding the chunk's last start finds where that pre-token
+    // ends: the next start, or the first byte outside every document, in the
+    // window; -1 when it runs past the window.
+    if (bits != 0 && pos == total) {
+      const int from = tid * 16 + (31 - __clz(bits)) + 1;
+      int end = -1;
+      for (int wj = from >> 5; wj < kSpanWords; ++wj) {
+        uint32_t m = S.startbits[wj] | bits32_at(S.outbits, kHalo + wj * 32);
+        if (wj == (from >> 5)) m &= 0xFFFFFFFFu << (from & 31);
+        if (m) {
+          end = wj * 32 + __ffs(m) - 1;
+          break;
+        }
+      }
+      S.last_end_rel = end;
+      S.last_end = end < 0 ? -1 : c0 + end;
     }
   }
   cta_sync();
   const uint32_t n_spans = S.n_spans;
-
-  // End of the last pre-token: the next start or document edge in the margin,
-  // or -1 when it runs past the window.
-  if (tid < 32 && n_spans > 0) {
-    const int from = S.span_start[n_spans - 1] + 1;
-    int64_t end = -1;
-    for (int base = from & ~31; base < kSpan; base += 32 * 32) {
-      const int wj = (base >> 5) + tid;
-      uint32_t m = 0;
-      if (wj < kSpanWords) {
-        m = S.startbits[wj] | bits32_at(S.outbits, kHalo + wj * 32);
-        const int lo_bit = from - wj * 32;
-        if (lo_bit > 0) m = lo_bit >= 32 ? 0u : (m & (0xFFFFFFFFu << lo_bit));
-      }
-      const uint32_t any = __ballot_sync(0xFFFFFFFFu, m != 0);
-      if (any) {
-        const int first = __ffs(any) - 1;
-        const uint32_t mf = __shfl_sync(0xFFFFFFFFu, m, first);
-        end = c0 + (((base >> 5) + first) * 32 + (__ffs(mf) - 1));
-        break;
-      }
-    }
-    if (tid == 0) S.last_end = end;
-  }
-  cta_sync();
+  const int last_end = S.last_end_rel;
 
   // Short pre-tokens, one thread each, two per round with their word-cache
   // probes in flight together. Hits finish here; misses are queued and
@@ -1188,8 +1192,8 @@ __global__ void __launch_bounds__(kEncodeThreads, 4) k_encode(EncodeArgs a) {
       shortp[h] = probe[h] = false;
       if (j < n_spans) {
         st[h] = S.span_start[j];
-        const int64_t en = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
-        len[h] = en < 0 ? kSpan : (int)(en - (c0 + st[h]));
+        const int en = (j + 1 < n_spans) ? (int)S.span_start[j + 1] : last_end;
+        len[h] = en < 0 ? kSpan : en - st[h];
         shortp[h] = en >= 0 && len[h] <= kShortMax;
         probe[h] = shortp[h] && a.C.enabled && len[h] <= kCacheMaxLen;
       }
@@ -1239,8 +1243,7 @@ __global__ void __launch_bounds__(kEncodeThreads, 4) k_encode(EncodeArgs a) {
       if (q < n_short) {
         j = S.missq[q];
         st = S.span_start[j];
-        const int64_t en = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
-        n = (uint32_t)(en - (c0 + st));
+        n = (uint32_t)(((j + 1 < n_spans) ? (int)S.span_start[j + 1] : last_end) - st);
       }
       const uint32_t cnt = merge_group<8>(W, S.win + kHalo + st, n, a.T, S.byte_id, S.sym + st);
       if (q < n_short && (tid & 7) == 0) S.span_cnt[j] = cnt;
@@ -1252,8 +1255,7 @@ __global__ void __launch_bounds__(kEncodeThreads, 4) k_encode(EncodeArgs a) {
       if (q < n_med) {
         j = S.missq[kMissShortCap + q];
         st = S.span_start[j];
-        const int64_t en = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
-        n = (uint32_t)(en - (c0 + st));
+        n = (uint32_t)(((j + 1 < n_spans) ? (int)S.span_start[j + 1] : last_end) - st);
       }
       const uint32_t cnt = merge_group<32>(W, S.win + kHalo + st, n, a.T, S.byte_id, S.sym + st);
       if (q < n_med && (tid & 31) == 0) S.span_cnt[j] = cnt;
@@ -1329,15 +1331,16 @@ __global__ void __launch_bounds__(kEncodeThreads, 4) k_encode(EncodeArgs a) {
   }
 
   // Token offsets within the chunk.
+  // Each thread scans a contiguous run of spans [run0, run1); it also stores
+  // their ids at the end, so consecutive threads write consecutive ranges.
   uint32_t agg = 0;
+  const uint32_t per = (n_spans + kThreads - 1) / kThreads;
+  const uint32_t run0 = min(n_spans, tid * per), run1 = min(n_spans, run0 + per);
   {
-    // Each thread scans a contiguous run of spans.
-    const uint32_t per = (n_spans + kThreads - 1) / kThreads;
-    const uint32_t j0 = min(n_spans, tid * per), j1 = min(n_spans, j0 + per);
     uint32_t sum = 0;
-    for (uint32_t j = j0; j < j1; ++j) sum += S.span_cnt[j];
+    for (uint32_t j = run0; j < run1; ++j) sum += S.span_cnt[j];
     uint32_t base = block_excl_scan(sum, S.red, &agg);
-    for (uint32_t j = j0; j < j1; ++j) {
+    for (uint32_t j = run0; j < run1; ++j) {
       uint32_t v = S.span_cnt[j];
       S.span_cnt[j] = base;
       base += v;
@@ -1359,47 +1362,27 @@ __global__ void __launch_bounds__(kEncodeThreads, 4) k_encode(EncodeArgs a) {
   // Ids past the caller's capacity are not written; the call reports it.
   if (tid == 0 && P + (int64_t)agg > a.out_capacity) atomicOr(&a.small->status, kStCapacity);
 
-  if (n_long == 0) {
-    // All ids are in shared memory, each span's at its start position. Warp w
-    // stores output positions [agg w / 8, agg (w + 1) / 8), a lane per
-    // position, coalesced: the span holding position o is the last one whose
-    // offset is at most o. Every span has at least one id, so a lane's next
-    // position (32 further) lies at most 32 spans further.
-    const int warp = tid >> 5, lane = tid & 31;
-    const uint32_t lo = (uint32_t)((uint64_t)agg * warp / (kThreads / 32));
-    const uint32_t hi = (uint32_t)((uint64_t)agg * (warp + 1) / (kThreads / 32));
+  // Ids of short pre-tokens from shared memory, each thread its own run.
+  {
     const int64_t lim = a.out_capacity - P;
-    uint32_t jl = 0, jh = n_spans;  // span_cnt[jl] <= o < span_cnt[jh] (span_cnt[n_spans] = agg)
-    for (uint32_t o = lo + lane; o < hi; o += 32) {
-      while (jh - jl > 1) {
-        const uint32_t mid = (jl + jh) >> 1;
-        if (S.span_cnt[mid] <= o) jl = mid;
-        else jh = mid;
-      }
-      if ((int64_t)o < lim) a.out_ids[P + o] = (int32_t)S.sym[S.span_start[jl] + (o - S.span_cnt[jl])];
-      jh = min(n_spans, jl + 33);
-    }
-  } else {
-    // Long pre-tokens: copy from their scratch range of the pool.
-    for (uint32_t x = 0; x < n_long; ++x) {
-      const uint32_t j = S.long_list[x];
-      const int64_t s = c0 + S.span_start[j];
-      const int64_t dst = P + S.span_cnt[j];
-      const uint32_t cnt = S.span_cnt[j + 1] - S.span_cnt[j];
-      for (uint32_t q = tid; q < cnt; q += kThreads)
-        if (dst + q < a.out_capacity) a.out_ids[dst + q] = a.pool[s + q];
-    }
-    // Short pre-tokens: ids from shared memory.
-    for (uint32_t j = tid; j < n_spans; j += kThreads) {
-      const int st = S.span_start[j];
+    for (uint32_t j = run0; j < run1; ++j) {
       bool is_long = false;
       for (uint32_t x = 0; x < n_long; ++x) is_long |= (S.long_list[x] == j);
       if (is_long) continue;
+      const int st = S.span_start[j];
       const uint32_t o = S.span_cnt[j], cnt = S.span_cnt[j + 1] - o;
-      const int64_t dst = P + o;
       for (uint32_t q = 0; q < cnt; ++q)
-        if (dst + q < a.out_capacity) a.out_ids[dst + q] = (int32_t)S.sym[st + q];
+        if ((int64_t)(o + q) < lim) a.out_ids[P + o + q] = (int32_t)S.sym[st + q];
     }
+  }
+  // Long pre-tokens: the CTA copies each from its scratch range of the pool.
+  for (uint32_t x = 0; x < n_long; ++x) {
+    const uint32_t j = S.long_list[x];
+    const int64_t s = c0 + S.span_start[j];
+    const int64_t dst = P + S.span_cnt[j];
+    const uint32_t cnt = S.span_cnt[j + 1] - S.span_cnt[j];
+    for (uint32_t q = tid; q < cnt; q += kThreads)
+      if (dst + q < a.out_capacity) a.out_ids[dst + q] = a.pool[s + q];
   }
 
   // Offsets of the documents that start in this chunk.
@@ -1426,10 +1409,11 @@ __global__ void __launch_bounds__(kThreads) k_pretokenize(const uint8_t* bytes, 
                                                           const int64_t* first_doc, uint32_t* out_bits) {
   __shared__ SplitSmem S;
   const int64_t c0 = (int64_t)blockIdx.x * kChunk;
-  if (threadIdx.x == 0) {
-    if (first_doc) {
-      S.chunk = first_doc[blockIdx.x];  // from k_prep
-    } else {
+  int64_t k_first;
+  if (first_doc) {
+    k_first = __ldg(first_doc + blockIdx.x);  // from k_prep
+  } else {  // no k_prep: the first document at or after c0 by binary search
+    if (threadIdx.x == 0) {
       int64_t lo = 0, hi = n_docs + 1;
       while (lo < hi) {
         int64_t mid = (lo + hi) >> 1;
@@ -1438,9 +1422,10 @@ __global__ void __launch_bounds__(kThreads) k_pretokenize(const uint8_t* bytes, 
       }
       S.chunk = lo;
     }
+    __syncthreads();
+    k_first = S.chunk;
   }
-  __syncthreads();
-  load_window(S, bytes, n_bytes, doc_offsets, n_docs, c0, S.chunk);
+  load_window(S, bytes, n_bytes, doc_offsets, n_docs, c0, k_first);
   compute_start_bits(S);
   const int64_t n_words = (n_bytes + 31) / 32;
   for (int w = threadIdx.x; w < kChunk / 32; w += kThreads) {
