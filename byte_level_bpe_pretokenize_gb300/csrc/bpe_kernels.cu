@@ -1623,10 +1623,11 @@ int status_code(uint32_t s) {
   return BPE_OK;
 }
 
-// Word cache: the ids of every vocabulary string of 1..16 bytes, and of
-// every vocabulary string that starts with a space with that space removed
-// (the same word at the start of a line or document), computed on the device
-// by the merge loop, laid out as an open-addressed table (load at most 1/4,
+// Word cache: the ids of every vocabulary string of 1..16 bytes, of every
+// vocabulary string that starts with a space with that space removed (the
+// same word at the start of a line or document), and of every prefix of
+// those (a word cut off by the end of a document), computed on the device by
+// the merge loop, laid out as an open-addressed table (load at most 1/4,
 // linear probing).
 int build_word_cache(bpe_handle* h, const uint8_t* vocab_bytes, const int64_t* vocab_offsets, int64_t n_vocab) {
   std::vector<uint8_t> strs;
@@ -1641,6 +1642,11 @@ int build_word_cache(bpe_handle* h, const uint8_t* vocab_bytes, const int64_t* v
   for (int64_t id = 0; id < n_vocab; ++id) {
     const int64_t L = vocab_offsets[id + 1] - vocab_offsets[id];
     if (L >= 2 && vocab_bytes[vocab_offsets[id]] == ' ') add(vocab_bytes + vocab_offsets[id] + 1, L - 1);
+  }
+  // Prefixes of all of the above (a word cut off by the end of a document).
+  for (int64_t i = 0, n0 = (int64_t)offs.size() - 1; i < n0; ++i) {
+    const std::string w(strs.begin() + offs[i], strs.begin() + offs[i + 1]);  // copy: add() grows strs
+    for (size_t L = 1; L < w.size(); ++L) add(reinterpret_cast<const uint8_t*>(w.data()), (int64_t)L);
   }
   const int64_t n = (int64_t)offs.size() - 1;
   uint8_t* d_strs = nullptr;

@@ -177,13 +177,14 @@ int bpe_decode_batch(bpe_handle* h, const int32_t* d_ids, int64_t n_ids, const i
  * bpe_set_word_cache — turns the handle's word cache on (default) or off.
  * The cache is the memo of "Hugging Face Tokenizers v1" (section on word
  * caching: a given pre-token always yields the same ids, so its ids can be
- * looked up instead of merged). bpe_build fills it once: every vocabulary
- * string of 1..16 bytes, and every vocabulary string that starts with a space
- * with the space removed (the word at the start of a line or document), is
- * run through the device merge loop and its ids (when at most 3) are stored
- * under its bytes. During encoding a pre-token of
- * at most 16 bytes found there takes the stored ids; every other pre-token
- * runs the merge loop. Either setting gives identical ids.
+ * looked up instead of merged). bpe_build fills it once with strings of
+ * 1..16 bytes: every vocabulary string, every vocabulary string that starts
+ * with a space with the space removed (the word at the start of a line or
+ * document), and every prefix of those (a word cut off by the end of a
+ * document). Each is run through the device merge loop and its ids (when at
+ * most 3) are stored under its bytes. During encoding a pre-token of at most
+ * 16 bytes found there takes the stored ids; every other pre-token runs the
+ * merge loop. Either setting gives identical ids.
  */
 int bpe_set_word_cache(bpe_handle* h, int enable);
 
