@@ -81,7 +81,6 @@ constexpr uint32_t kReprobe = 0xFFFFFFFEu;              // pair rank still to be
 constexpr uint32_t kInf = 0xFFFFFFFFu;
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 constexpr uint32_t kEmptySlot = 0xFFFFFFFFu;  // left id of an unused pair-table slot
-constexpr uint64_t kWaitLimitNs = 20ull * 1000 * 1000 * 1000;  // 20 s
 
 static_assert(kChunk == 16 * kThreads, "one 16-byte group per thread");
 static_assert(kMargin <= 16 * 16, "the margin is covered by 16 lanes of warp 0");
@@ -93,10 +92,9 @@ constexpr uint32_t kStTimeout = 2u;
 constexpr uint32_t kStInternal = 4u;
 constexpr uint32_t kStCapacity = 8u;
 
-// look-back descriptor: status in bits 62..63, value below
-constexpr uint64_t kDescAgg = 1ull << 62;
-constexpr uint64_t kDescIncl = 2ull << 62;
-constexpr uint64_t kDescValue = (1ull << 62) - 1;
+// Staged output: chunk c's ids of short pre-tokens go to stage[c kStage ..]
+// in order (long pre-tokens keep theirs in the pool at their own bytes).
+constexpr int kStage = kChunk + kShortMax;
 
 enum Cls { kO = 0, kL = 1, kN = 2, kS = 3 };
 
@@ -139,28 +137,12 @@ struct Cache {
 
 struct DevSmall {
   uint32_t status;
-  uint32_t ticket;
+  uint32_t rec_used;  // u32 words of long pre-token records handed out this call
   int64_t total;
 };
 
 
 // ------------------------------------------------------------ small helpers --
-
-__device__ __forceinline__ uint64_t global_timer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ uint64_t ld_relaxed(const uint64_t* p) {
-  uint64_t v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_relaxed(uint64_t* p, uint64_t v) {
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
 
 // Rank of the pair (a, b), kInf if it is not a merge; *nw gets the merged id.
 __device__ __forceinline__ uint32_t lookup_pair(const Tables& T, uint32_t a, uint32_t b, uint32_t* nw) {
@@ -400,11 +382,8 @@ struct Smem : SplitSmem {
   int64_t doc_lo, doc_hi;  // document of a long pre-token that runs past the window
 };
 
-// Barrier of the kThreads threads that split and merge (named barrier 1). The
-// encode kernel's extra look-back warp never takes part in it.
+// Barrier of the kThreads threads of a CTA (named barrier 1).
 __device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
-__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-__device__ __forceinline__ void named_arrive(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 static_assert(4 * (sizeof(Smem) + 1024) <= 228 * 1024, "four encode CTAs fit in an SM's shared memory");
 
@@ -1009,18 +988,18 @@ __device__ __forceinline__ uint32_t merge_at(Smem& S, int st, int len, const Tab
 
 // ------------------------------------------------------------------ kernels --
 
-// Per call: chunk descriptors cleared, first document of every chunk found,
-// offsets validated, ticket reset.
+// Per call: first document of every chunk found (first_doc[n_chunks] =
+// n_docs + 1), offsets validated, record counter and token count reset.
 __global__ void k_prep(const int64_t* doc_offsets, int64_t n_docs, int64_t n_bytes, int64_t n_chunks,
-                       uint64_t* desc, int64_t* first_doc, DevSmall* small) {
+                       int64_t* first_doc, DevSmall* small) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t0 == 0) {
-    small->ticket = 0;
+    small->rec_used = 0;
     small->total = 0;
+    first_doc[n_chunks] = n_docs + 1;
   }
   for (int64_t c = t0; c < n_chunks; c += stride) {
-    desc[c] = 0;
     const int64_t target = c * kChunk;
     int64_t lo = 0, hi = n_docs + 1;  // first k with doc_offsets[k] >= target
     while (lo < hi) {
@@ -1044,87 +1023,31 @@ struct EncodeArgs {
   int64_t n_bytes;
   const int64_t* doc_offsets;
   int64_t n_docs;
-  int32_t* out_ids;
-  int64_t out_capacity;
   int64_t* out_offsets;
   int32_t* pool;  // long pre-token scratch, one int32 per input byte
   Tables T;
   Cache C;
   const uint32_t* start_bits;  // pre-token start bitmask of all n_bytes
-  uint64_t* desc;
+  uint32_t* stage;             // [n_chunks][kStage] ids of short pre-tokens
+  uint64_t* chunk_meta;        // per chunk: token count | (record index + 1) << 32
+  uint32_t* rec;               // long pre-token records
+  uint64_t rec_cap;            // u32 words of rec
   const int64_t* first_doc;
   DevSmall* small;
   int64_t n_chunks;
 };
 
-// Exclusive prefix of chunk c from the chained scan, by the look-back warp
-// while the other warps encode the chunk. Lane l reads the descriptor of
-// chunk (base - l); the window slides back until an inclusive prefix is found.
-// A wait that makes no progress for kWaitLimitNs sets the timeout status and
-// returns what was summed so far.
-__device__ int64_t look_back(const uint64_t* desc, int64_t c, DevSmall* small) {
-  const int lane = threadIdx.x & 31;
-  int64_t excl = 0, base = c - 1;
-  const uint64_t t_start = global_timer();
-  uint32_t sleep_ns = 64;
-  while (base >= 0) {
-    const int64_t j = base - lane;
-    const uint64_t d = j >= 0 ? ld_relaxed(&desc[j]) : kDescIncl;
-    const uint32_t ready = __ballot_sync(0xFFFFFFFFu, (d & ~kDescValue) != 0);
-    const uint32_t incl = __ballot_sync(0xFFFFFFFFu, (d & ~kDescValue) == kDescIncl);
-    // Lanes up to and including the nearest inclusive one must be ready.
-    const uint32_t need = incl ? (((incl & (0u - incl)) << 1) - 1u) : 0xFFFFFFFFu;
-    if ((ready & need) != need) {
-      bool out = false;
-      if (lane == 0) out = global_timer() - t_start > kWaitLimitNs;
-      out = __shfl_sync(0xFFFFFFFFu, out, 0);
-      if (out) {
-        if (lane == 0) atomicOr(&small->status, kStTimeout);
-        break;
-      }
-      __nanosleep(sleep_ns);
-      sleep_ns = min(2u * sleep_ns, 1024u);
-      continue;
-    }
-    sleep_ns = 64;
-    uint64_t v = (need >> lane) & 1u ? (d & kDescValue) : 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    excl += (int64_t)v;
-    if (incl) break;
-    base -= 32;
-  }
-  return excl;
-}
-
-// Launched with kThreads + 32 threads: warps 0..7 encode chunk c, warp 8
-// finds the chunk's output offset meanwhile (named barriers 2 and 3 hand the
-// chunk's token count to it and the offset back).
-constexpr int kEncodeThreads = kThreads + 32;
-
-__global__ void __launch_bounds__(kEncodeThreads, 4) k_encode(EncodeArgs a) {
+// Encodes chunk blockIdx.x without waiting on any other chunk: its ids go to
+// its stage region (short pre-tokens) or stay in the pool (long ones, listed
+// in a record), its count to chunk_meta, and its documents' offsets are
+// written relative to the chunk. k_chunk_scan and k_compact finish the call.
+__global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
-
-  if (tid == 0) S.chunk = (int64_t)atomicAdd(&a.small->ticket, 1u);
-  for (int i = tid; i < 256; i += kEncodeThreads) S.byte_id[i] = a.T.byte_id[i];
-  __syncthreads();
-  const int64_t c = S.chunk;
+  for (int i = tid; i < 256; i += kThreads) S.byte_id[i] = a.T.byte_id[i];
+  const int64_t c = blockIdx.x;
   const int64_t c0 = c * kChunk;
-  if (tid >= kThreads) {  // the look-back warp
-    const int64_t excl = look_back(a.desc, c, a.small);
-    named_sync(2, kEncodeThreads);  // the chunk's token count is in S.agg
-    if (tid == kThreads) {
-      const uint32_t agg = S.agg;
-      st_relaxed(&a.desc[c], kDescIncl | (uint64_t)(excl + agg));
-      S.prefix = excl;
-      if (c == a.n_chunks - 1) a.small->total = excl + agg;
-    }
-    __syncwarp();
-    named_arrive(3, kEncodeThreads);
-    return;
-  }
   // The first document starting at or after c0 and, ahead of their use at
   // the end, the offsets of the first kThreads documents from there on.
   const int64_t k_first = __ldg(a.first_doc + c);
@@ -1349,43 +1272,53 @@ __global__ void __launch_bounds__(kEncodeThreads, 4) k_encode(EncodeArgs a) {
   }
   cta_sync();
 
-  // Hand the chunk's token count to the look-back warp (and publish it for
-  // later chunks), stage the ids in output order, then take the offset.
+  // Long pre-tokens: one record block per chunk, {n_long, then per long
+  // pre-token {offset in the chunk, first byte (low, high 32 bits), count}}.
   if (tid == 0) {
-    S.agg = agg;
-    st_relaxed(&a.desc[c], kDescAgg | (uint64_t)agg);
+    uint64_t meta = agg;
+    if (n_long > 0) {
+      const uint32_t words = 1 + 4 * n_long;
+      const uint32_t r = atomicAdd(&a.small->rec_used, words);
+      if ((uint64_t)r + words <= a.rec_cap) {
+        a.rec[r] = n_long;
+        for (uint32_t x = 0; x < n_long; ++x) {
+          const uint32_t j = S.long_list[x];
+          const uint64_t s = (uint64_t)(c0 + S.span_start[j]);
+          uint32_t* e = a.rec + r + 1 + 4 * x;
+          e[0] = S.span_cnt[j];
+          e[1] = (uint32_t)s;
+          e[2] = (uint32_t)(s >> 32);
+          e[3] = S.span_cnt[j + 1] - S.span_cnt[j];
+        }
+        meta |= (uint64_t)(r + 1) << 32;
+      } else {
+        atomicOr(&a.small->status, kStInternal);
+      }
+    }
+    a.chunk_meta[c] = meta;
   }
-  named_arrive(2, kEncodeThreads);
-  named_sync(3, kEncodeThreads);
-  const int64_t P = S.prefix;
 
-  // Ids past the caller's capacity are not written; the call reports it.
-  if (tid == 0 && P + (int64_t)agg > a.out_capacity) atomicOr(&a.small->status, kStCapacity);
-
-  // Ids of short pre-tokens from shared memory, each thread its own run.
+  // Ids of short pre-tokens to the chunk's stage region, each thread its own
+  // run, in output order without the long pre-tokens' ids.
   {
-    const int64_t lim = a.out_capacity - P;
+    uint32_t* stage = a.stage + c * kStage;
     for (uint32_t j = run0; j < run1; ++j) {
       bool is_long = false;
-      for (uint32_t x = 0; x < n_long; ++x) is_long |= (S.long_list[x] == j);
+      uint32_t long_before = 0;
+      for (uint32_t x = 0; x < n_long; ++x) {
+        const uint32_t lj = S.long_list[x];
+        is_long |= lj == j;
+        if (lj < j) long_before += S.span_cnt[lj + 1] - S.span_cnt[lj];
+      }
       if (is_long) continue;
       const int st = S.span_start[j];
-      const uint32_t o = S.span_cnt[j], cnt = S.span_cnt[j + 1] - o;
-      for (uint32_t q = 0; q < cnt; ++q)
-        if ((int64_t)(o + q) < lim) a.out_ids[P + o + q] = (int32_t)S.sym[st + q];
+      const uint32_t o = S.span_cnt[j] - long_before, cnt = S.span_cnt[j + 1] - S.span_cnt[j];
+      for (uint32_t q = 0; q < cnt; ++q) stage[o + q] = S.sym[st + q];
     }
   }
-  // Long pre-tokens: the CTA copies each from its scratch range of the pool.
-  for (uint32_t x = 0; x < n_long; ++x) {
-    const uint32_t j = S.long_list[x];
-    const int64_t s = c0 + S.span_start[j];
-    const int64_t dst = P + S.span_cnt[j];
-    const uint32_t cnt = S.span_cnt[j + 1] - S.span_cnt[j];
-    for (uint32_t q = tid; q < cnt; q += kThreads)
-      if (dst + q < a.out_capacity) a.out_ids[dst + q] = a.pool[s + q];
-  }
 
-  // Offsets of the documents that start in this chunk.
+  // Offsets of the documents that start in this chunk, relative to the
+  // chunk's first id (k_compact adds the chunk's offset).
   {
     for (int64_t k = k_first + tid; k <= a.n_docs; k += kThreads) {
       const int64_t d = k == k_first + tid ? d_mine : a.doc_offsets[k];
@@ -1398,9 +1331,121 @@ __global__ void __launch_bounds__(kEncodeThreads, 4) k_encode(EncodeArgs a) {
         if (S.span_start[mid] < rel) lo = mid + 1;
         else hi = mid;
       }
-      a.out_offsets[k] = P + S.span_cnt[lo];
+      a.out_offsets[k] = S.span_cnt[lo];
     }
   }
+}
+
+// Exclusive prefix sum of the chunks' token counts in two levels: k_scan_tiles
+// scans tiles of kScanThreads chunks (coalesced, one chunk per thread) into
+// chunk_off and writes each tile's total; k_scan_tile_sums (one CTA) turns
+// the tile totals into exclusive tile offsets and small->total. k_compact
+// adds the two.
+constexpr int kScanThreads = 1024;
+
+__device__ uint64_t block_excl_scan64(uint64_t v, uint64_t* red, uint64_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint64_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) red[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint64_t x = lane < (int)(blockDim.x >> 5) ? red[lane] : 0;
+    uint64_t xi = x;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint64_t o = __shfl_up_sync(0xFFFFFFFFu, xi, d);
+      if (lane >= d) xi += o;
+    }
+    red[lane] = xi - x;
+    if (lane == 31) red[32] = xi;
+  }
+  __syncthreads();
+  const uint64_t r = red[warp] + incl - v;
+  *total = red[32];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kScanThreads) k_scan_tiles(const uint64_t* chunk_meta, int64_t n_chunks,
+                                                             uint64_t* chunk_off, uint64_t* tile_sum) {
+  __shared__ uint64_t red[33];
+  const int64_t c = (int64_t)blockIdx.x * kScanThreads + threadIdx.x;
+  const uint64_t v = c < n_chunks ? (chunk_meta[c] & 0xFFFFFFFFull) : 0;
+  uint64_t total;
+  const uint64_t e = block_excl_scan64(v, red, &total);
+  if (c < n_chunks) chunk_off[c] = e;
+  if (threadIdx.x == 0) tile_sum[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(kScanThreads) k_scan_tile_sums(uint64_t* tile_sum, int64_t n_tiles, DevSmall* small) {
+  __shared__ uint64_t red[33];
+  uint64_t carry = 0;
+  for (int64_t base = 0; base < n_tiles; base += kScanThreads) {
+    const int64_t t = base + threadIdx.x;
+    const uint64_t v = t < n_tiles ? tile_sum[t] : 0;
+    uint64_t total;
+    const uint64_t e = block_excl_scan64(v, red, &total);
+    if (t < n_tiles) tile_sum[t] = carry + e;
+    carry += total;
+  }
+  if (threadIdx.x == 0) small->total = (int64_t)carry;
+}
+
+// One warp per chunk: chunk c's ids to their place in out_ids (short
+// pre-tokens from the stage region, long ones from the pool, in order) and
+// its documents' offsets made absolute. Ids past out_capacity are not written.
+constexpr int kCompactWarps = 8;
+
+__global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const uint32_t* stage, const int32_t* pool,
+                                                                const uint64_t* chunk_meta, const uint64_t* chunk_off,
+                                                                const uint64_t* tile_off, const uint32_t* rec,
+                                                                const int64_t* first_doc, int64_t n_chunks,
+                                                                int64_t n_docs, int32_t* out_ids, int64_t out_capacity,
+                                                                int64_t* out_offsets, DevSmall* small) {
+  const int lane = threadIdx.x & 31;
+  const int64_t c = (int64_t)blockIdx.x * kCompactWarps + (threadIdx.x >> 5);
+  if (c >= n_chunks) return;
+  const uint64_t meta = chunk_meta[c];
+  const uint32_t cnt = (uint32_t)meta;
+  const uint32_t r1 = (uint32_t)(meta >> 32);  // record index + 1, 0 without long pre-tokens
+  const int64_t P = (int64_t)(chunk_off[c] + tile_off[c / kScanThreads]);
+  const uint32_t* src = stage + c * kStage;
+  if (lane == 0 && P + (int64_t)cnt > out_capacity) atomicOr(&small->status, kStCapacity);
+  const int64_t lim = out_capacity - P;
+  if (r1 == 0) {
+    for (uint32_t q = lane; q < cnt; q += 32)
+      if ((int64_t)q < lim) out_ids[P + q] = (int32_t)src[q];
+  } else {
+    const uint32_t* R = rec + (r1 - 1);
+    const uint32_t n_long = R[0];
+    for (uint32_t q = lane; q < cnt; q += 32) {
+      if ((int64_t)q >= lim) break;
+      uint32_t shift = 0;
+      int32_t v = 0;
+      bool from_long = false;
+      for (uint32_t x = 0; x < n_long; ++x) {
+        const uint32_t off = R[1 + 4 * x], lc = R[4 + 4 * x];
+        if (q >= off + lc) {
+          shift += lc;
+        } else {
+          if (q >= off) {
+            const uint64_t s = (uint64_t)R[2 + 4 * x] | ((uint64_t)R[3 + 4 * x] << 32);
+            v = pool[s + (q - off)];
+            from_long = true;
+          }
+          break;
+        }
+      }
+      out_ids[P + q] = from_long ? v : (int32_t)src[q - shift];
+    }
+  }
+  const int64_t k_hi = first_doc[c + 1] < n_docs + 1 ? first_doc[c + 1] : n_docs + 1;
+  for (int64_t k = first_doc[c] + lane; k < k_hi; k += 32) out_offsets[k] += P;
 }
 
 // Pre-tokenizer alone: start bits of [c0, c0 + kChunk) for chunk blockIdx.x.
@@ -1701,21 +1746,84 @@ int build_word_cache(bpe_handle* h, const uint8_t* vocab_bytes, const int64_t* v
 
 }  // namespace
 
+// -------------------------------------------------------- encode workspace --
+// Regions of the per-call workspace, each starting on a 256-byte boundary:
+// first document per chunk (+1 sentinel), chunk metadata and offsets, tile
+// offsets of the chunk scan, long pre-token records, the start bitmask, the
+// stage regions and the pool.
+namespace {
+constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsSizes {
+  size_t first_doc, chunk_meta, chunk_off, tile_off, rec, bits, stage, pool, total;
+  uint64_t rec_cap;  // u32 words: a header per chunk and 4 words per long pre-token
+};
+
+constexpr WsSizes ws_sizes(int64_t n_bytes) {
+  const int64_t n_chunks = n_bytes / kChunk + 1, n_words = (n_bytes + 31) / 32;
+  WsSizes z{};
+  z.rec_cap = (uint64_t)(n_chunks + 4 * (n_bytes / (kShortMax + 1) + n_chunks) + 16);
+  z.first_doc = align256((size_t)(n_chunks + 1) * sizeof(int64_t));
+  z.chunk_meta = align256((size_t)n_chunks * sizeof(uint64_t));
+  z.chunk_off = align256((size_t)n_chunks * sizeof(uint64_t));
+  z.tile_off = align256((size_t)(n_chunks / kScanThreads + 1) * sizeof(uint64_t));
+  z.rec = align256((size_t)z.rec_cap * sizeof(uint32_t));
+  z.bits = align256((size_t)(n_words + 4) * sizeof(uint32_t));
+  z.stage = align256((size_t)n_chunks * kStage * sizeof(uint32_t));
+  z.pool = align256((size_t)(n_bytes + 4) * sizeof(int32_t));
+  z.total = z.first_doc + z.chunk_meta + z.chunk_off + z.tile_off + z.rec + z.bits + z.stage + z.pool;
+  return z;
+}
+
+struct Ws {
+  int64_t* first_doc;
+  uint64_t* chunk_meta;
+  uint64_t* chunk_off;
+  uint64_t* tile_off;
+  uint32_t* rec;
+  uint64_t rec_cap;
+  uint32_t* bits;
+  uint32_t* stage;
+  int32_t* pool;
+};
+
+Ws ws_carve(unsigned char* base, int64_t n_bytes) {
+  const WsSizes z = ws_sizes(n_bytes);
+  Ws w;
+  w.first_doc = reinterpret_cast<int64_t*>(base);
+  base += z.first_doc;
+  w.chunk_meta = reinterpret_cast<uint64_t*>(base);
+  base += z.chunk_meta;
+  w.chunk_off = reinterpret_cast<uint64_t*>(base);
+  base += z.chunk_off;
+  w.tile_off = reinterpret_cast<uint64_t*>(base);
+  base += z.tile_off;
+  w.rec = reinterpret_cast<uint32_t*>(base);
+  w.rec_cap = z.rec_cap;
+  base += z.rec;
+  w.bits = reinterpret_cast<uint32_t*>(base);
+  base += z.bits;
+  w.stage = reinterpret_cast<uint32_t*>(base);
+  base += z.stage;
+  w.pool = reinterpret_cast<int32_t*>(base);
+  return w;
+}
+
+// The per-call kernels: k_prep, the split, the encode, the chunk scan and the
+// compaction, on stream st. ev_start / ev_stop (may be null) bracket all but
+// k_prep.
+int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
+                  int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets, cudaStream_t st,
+                  cudaEvent_t ev_start, cudaEvent_t ev_stop);
+}  // namespace
+
 // ---------------------------------------------- fixed scratch of the no-alloc encode --
-// bpe_encode_batch_noalloc keeps its scratch (look-back descriptors, first
-// document of each chunk, long pre-token pool, start bitmask) in one array of
-// static device memory per device instead of the handle's workspace. Regions
-// start on 256-byte boundaries and are sized for kNoAllocMaxBytes input bytes.
+// bpe_encode_batch_noalloc keeps its workspace in one array of static device
+// memory per device, sized for kNoAllocMaxBytes input bytes.
 namespace {
 constexpr int64_t kNoAllocMaxBytes = int64_t(4) << 20;
-constexpr int64_t kNoAllocChunks = kNoAllocMaxBytes / kChunk + 1;
-constexpr size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
-constexpr size_t kNoAllocFirstDocOff = round256((size_t)kNoAllocChunks * sizeof(uint64_t));
-constexpr size_t kNoAllocPoolOff = kNoAllocFirstDocOff + round256((size_t)kNoAllocChunks * sizeof(int64_t));
-constexpr size_t kNoAllocBitsOff = kNoAllocPoolOff + round256((size_t)(kNoAllocMaxBytes + 4) * sizeof(int32_t));
-constexpr size_t kNoAllocScratchBytes =
-    kNoAllocBitsOff + round256((size_t)((kNoAllocMaxBytes + 31) / 32 + 4) * sizeof(uint32_t));
-static_assert(kNoAllocScratchBytes < (size_t(17) << 20), "the fixed scratch stays below 17 MiB");
+constexpr size_t kNoAllocScratchBytes = ws_sizes(kNoAllocMaxBytes).total;
+static_assert(kNoAllocScratchBytes < (size_t(36) << 20), "the fixed scratch stays below 36 MiB");
 }  // namespace
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -1739,6 +1847,53 @@ int noalloc_setup(int dev, unsigned char** base) {
     g_noalloc_base[dev] = static_cast<unsigned char*>(p);
   }
   *base = g_noalloc_base[dev];
+  return BPE_OK;
+}
+}  // namespace
+
+namespace {
+int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
+                  int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets, cudaStream_t st,
+                  cudaEvent_t ev_start, cudaEvent_t ev_stop) {
+  const int64_t n_chunks = n_bytes / kChunk + 1;
+  const int prep_blocks = (int)std::min<int64_t>(4096, std::max<int64_t>(n_chunks, n_docs + 1) / 256 + 1);
+  k_prep<<<prep_blocks, 256, 0, st>>>(d_doc_offsets, n_docs, n_bytes, n_chunks, w.first_doc, h->d_small);
+  CK(cudaGetLastError());
+  EncodeArgs a;
+  a.bytes = d_bytes;
+  a.n_bytes = n_bytes;
+  a.doc_offsets = d_doc_offsets;
+  a.n_docs = n_docs;
+  a.pool = w.pool;
+  a.T = Tables{h->d_ht, h->hmask, h->d_mrows, h->d_byte_id};
+  a.C = Cache{h->d_cache, h->cache_mask, h->cache_enabled && h->d_cache != nullptr};
+  a.start_bits = w.bits;
+  a.stage = w.stage;
+  a.chunk_meta = w.chunk_meta;
+  a.rec = w.rec;
+  a.rec_cap = w.rec_cap;
+  a.first_doc = w.first_doc;
+  a.small = h->d_small;
+  a.n_chunks = n_chunks;
+  a.out_offsets = d_out_offsets;
+  if (ev_start) CK(cudaEventRecord(ev_start, st));
+  if (n_bytes > 0) {
+    k_pretokenize<<<(unsigned)((n_bytes + kChunk - 1) / kChunk), kThreads, 0, st>>>(d_bytes, n_bytes, d_doc_offsets,
+                                                                                   n_docs, w.first_doc, w.bits);
+    CK(cudaGetLastError());
+  }
+  k_encode<<<(unsigned)n_chunks, kThreads, sizeof(Smem), st>>>(a);
+  CK(cudaGetLastError());
+  const int64_t n_tiles = (n_chunks + kScanThreads - 1) / kScanThreads;
+  k_scan_tiles<<<(unsigned)n_tiles, kScanThreads, 0, st>>>(w.chunk_meta, n_chunks, w.chunk_off, w.tile_off);
+  CK(cudaGetLastError());
+  k_scan_tile_sums<<<1, kScanThreads, 0, st>>>(w.tile_off, n_tiles, h->d_small);
+  CK(cudaGetLastError());
+  k_compact<<<(unsigned)((n_chunks + kCompactWarps - 1) / kCompactWarps), 32 * kCompactWarps, 0, st>>>(
+      w.stage, w.pool, w.chunk_meta, w.chunk_off, w.tile_off, w.rec, w.first_doc, n_chunks, n_docs, d_out_ids,
+      out_capacity, d_out_offsets, h->d_small);
+  CK(cudaGetLastError());
+  if (ev_stop) CK(cudaEventRecord(ev_stop, st));
   return BPE_OK;
 }
 }  // namespace
@@ -1901,48 +2056,15 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
     return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch: offsets must be 8-byte and ids 4-byte aligned");
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
-  const int64_t n_chunks = n_bytes / kChunk + 1;
-  const int64_t n_words = (n_bytes + 31) / 32;
-  const size_t need = (size_t)n_chunks * (sizeof(uint64_t) + sizeof(int64_t)) +
-                      (size_t)(n_bytes + 4) * sizeof(int32_t) + (size_t)(n_words + 4) * sizeof(uint32_t);
-  int rc = ensure_ws(h, need);
+  int rc = ensure_ws(h, ws_sizes(n_bytes).total);
   if (rc) return rc;
-  uint64_t* desc = (uint64_t*)h->d_ws;
-  int64_t* first_doc = (int64_t*)(desc + n_chunks);
-  int32_t* pool = (int32_t*)(first_doc + n_chunks);
-  uint32_t* bits = (uint32_t*)(pool + n_bytes + 4);
   if (!h->smem_set) {
     CK(cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
     h->smem_set = true;
   }
-  int prep_blocks = (int)std::min<int64_t>(4096, std::max<int64_t>(n_chunks, n_docs + 1) / 256 + 1);
-  k_prep<<<prep_blocks, 256, 0, st>>>(d_doc_offsets, n_docs, n_bytes, n_chunks, desc, first_doc, h->d_small);
-  CK(cudaGetLastError());
-  EncodeArgs a;
-  a.bytes = d_bytes;
-  a.n_bytes = n_bytes;
-  a.doc_offsets = d_doc_offsets;
-  a.n_docs = n_docs;
-  a.out_ids = d_out_ids;
-  a.out_capacity = out_capacity;
-  a.out_offsets = d_out_offsets;
-  a.pool = pool;
-  a.T = Tables{h->d_ht, h->hmask, h->d_mrows, h->d_byte_id};
-  a.C = Cache{h->d_cache, h->cache_mask, h->cache_enabled && h->d_cache != nullptr};
-  a.start_bits = bits;
-  a.desc = desc;
-  a.first_doc = first_doc;
-  a.small = h->d_small;
-  a.n_chunks = n_chunks;
-  if (h->ev_start) CK(cudaEventRecord(h->ev_start, st));
-  if (n_bytes > 0) {
-    k_pretokenize<<<(unsigned)((n_bytes + kChunk - 1) / kChunk), kThreads, 0, st>>>(
-        d_bytes, n_bytes, d_doc_offsets, n_docs, first_doc, bits);
-    CK(cudaGetLastError());
-  }
-  k_encode<<<(unsigned)n_chunks, kEncodeThreads, sizeof(Smem), st>>>(a);
-  CK(cudaGetLastError());
-  if (h->ev_stop) CK(cudaEventRecord(h->ev_stop, st));
+  rc = launch_encode(h, ws_carve(static_cast<unsigned char*>(h->d_ws), n_bytes), d_bytes, n_bytes, d_doc_offsets,
+                     n_docs, d_out_ids, out_capacity, d_out_offsets, st, h->ev_start, h->ev_stop);
+  if (rc) return rc;
   if (h_total_tokens) {
     DevSmall s;
     rc = read_status(h, st, &s);
@@ -1972,39 +2094,9 @@ int bpe_encode_batch_noalloc(bpe_handle* h, const uint8_t* d_bytes, int64_t n_by
   int rc = noalloc_setup(h->device, &base);
   if (rc) return rc;
   cudaStream_t st = (cudaStream_t)stream;
-  const int64_t n_chunks = n_bytes / kChunk + 1;
-  uint64_t* desc = reinterpret_cast<uint64_t*>(base);
-  int64_t* first_doc = reinterpret_cast<int64_t*>(base + kNoAllocFirstDocOff);
-  int32_t* pool = reinterpret_cast<int32_t*>(base + kNoAllocPoolOff);
-  uint32_t* bits = reinterpret_cast<uint32_t*>(base + kNoAllocBitsOff);
-  // k_prep zeroes the look-back descriptors and the handle's ticket and token
-  // count; every other scratch word is written before it is read.
-  int prep_blocks = (int)std::min<int64_t>(4096, std::max<int64_t>(n_chunks, n_docs + 1) / 256 + 1);
-  k_prep<<<prep_blocks, 256, 0, st>>>(d_doc_offsets, n_docs, n_bytes, n_chunks, desc, first_doc, h->d_small);
-  CK(cudaGetLastError());
-  EncodeArgs a;
-  a.bytes = d_bytes;
-  a.n_bytes = n_bytes;
-  a.doc_offsets = d_doc_offsets;
-  a.n_docs = n_docs;
-  a.out_ids = d_out_ids;
-  a.out_capacity = out_capacity;
-  a.out_offsets = d_out_offsets;
-  a.pool = pool;
-  a.T = Tables{h->d_ht, h->hmask, h->d_mrows, h->d_byte_id};
-  a.C = Cache{h->d_cache, h->cache_mask, h->cache_enabled && h->d_cache != nullptr};
-  a.start_bits = bits;
-  a.desc = desc;
-  a.first_doc = first_doc;
-  a.small = h->d_small;
-  a.n_chunks = n_chunks;
-  if (n_bytes > 0) {
-    k_pretokenize<<<(unsigned)((n_bytes + kChunk - 1) / kChunk), kThreads, 0, st>>>(
-        d_bytes, n_bytes, d_doc_offsets, n_docs, first_doc, bits);
-    CK(cudaGetLastError());
-  }
-  k_encode<<<(unsigned)n_chunks, kEncodeThreads, sizeof(Smem), st>>>(a);
-  CK(cudaGetLastError());
+  rc = launch_encode(h, ws_carve(base, n_bytes), d_bytes, n_bytes, d_doc_offsets, n_docs, d_out_ids, out_capacity,
+                     d_out_offsets, st, nullptr, nullptr);
+  if (rc) return rc;
   if (h_total_tokens) {
     DevSmall s;
     rc = read_status(h, st, &s);
