@@ -11,35 +11,41 @@
 //
 // GPU design (none of it is on the pages, whose engines are CPU code):
 //   * The byte stream is cut into 4 KiB chunks, one CTA each. A CTA loads its
-//     chunk plus a 16-byte halo and a 256-byte margin into shared memory and
-//     marks where pre-tokens start. Each thread takes 16 bytes: when they and
-//     their context are ASCII without an apostrophe, carry-free SWAR range
-//     tests give 16-bit class masks and the split rules are a dozen mask
-//     operations; otherwise a 24-byte UTF-8 unit scan builds the same masks,
-//     and apostrophes or multi-byte whitespace fall back to the per-byte
-//     predicate starts_piece.
-//   * Symbols are token ids: byte b starts as byte_id[b]; a merge table maps
-//     (left_id, right_id) to its rank through an open-addressed hash table
-//     of 32-byte buckets (one L2 sector each); rank -> new_id comes from the
-//     merge rows. Because bytes(new_id) = bytes(left) || bytes(right) (checked
+//     chunk plus a 16-byte halo and a 256-byte margin into shared memory.
+//   * Split (k_pretokenize). Each thread takes 16 bytes.
+//     - When they and their context are ASCII, carry-free SWAR range tests
+//       give 16-bit class masks, and the split rules are a dozen mask
+//       operations; each apostrophe resolves its contraction in place.
+//     - Otherwise a 24-byte UTF-8 unit scan builds the same masks from a
+//       two-level codepoint class table.
+//     - Multi-byte whitespace falls back to the per-byte predicate
+//       starts_piece.
+//     - Output: a start bitmask in global memory.
+//   * Symbols are token ids: byte b starts as byte_id[b]. An open-addressed
+//     pair table of 32-byte buckets maps (left_id, right_id) to {rank,
+//     new_id}. Because bytes(new_id) = bytes(left) || bytes(right) (checked
 //     by bpe_build), the final symbols are the vocabulary ids.
 //   * Word cache ("Hugging Face Tokenizers v1", section on word caching: the
 //     same pre-token always gives the same ids, so a memo from pre-token bytes
-//     to ids skips the merge loop). Here the memo is filled once in bpe_build:
-//     every vocabulary string of at most 16 bytes is run through the merge
-//     kernel below, and its ids are stored under its bytes. A pre-token of at
-//     most 16 bytes that is found there takes the stored ids; any other runs
-//     the merge loop.
-//   * Pre-tokens of up to 64 bytes are merged by one thread each in shared
-//     memory with a flat array plus a cached rank per adjacent pair (the v1
-//     merge-loop rewrite: flat arrays, integer rank compare, no allocation).
-//     Longer ones are merged by the whole CTA in a device scratch pool indexed
-//     by input byte position, so every long pre-token owns the pool range of
-//     its own bytes.
-//   * Output positions: a single-pass chained scan (decoupled look-back, one
-//     warp) over chunk token counts; chunks take tickets in launch order so
-//     every predecessor is already running. Waits are bounded by the global
-//     timer. Ids are staged in shared memory and stored coalesced.
+//     to ids skips the merge loop).
+//     - bpe_build fills it once, by running the merge kernel below on strings
+//       of at most 16 bytes: vocabulary strings, space-stripped vocabulary
+//       words and prefixes of both.
+//     - A pre-token found there takes the stored ids.
+//   * Encode (k_encode):
+//     - Pre-tokens of up to 64 bytes get one thread each for the cache probe.
+//     - Misses are queued and merged by lane groups: 8 lanes up to 16 bytes,
+//       a warp up to 64. Each step is a group-wide minimum, a ballot of the
+//       pair's positions and a run-parity mask for the non-overlapping
+//       left-to-right choice.
+//     - Longer pre-tokens are merged by the whole CTA in a device pool indexed
+//       by input byte, so each owns the pool range of its own bytes.
+//   * Output without waits between CTAs:
+//     - each chunk writes its ids to a stage region of its own (long
+//       pre-tokens' stay in the pool, listed in a record block), its token
+//       count, and its documents' offsets relative to the chunk;
+//     - a two-level scan gives the chunk offsets;
+//     - k_compact moves every chunk's ids into place, a warp per chunk.
 
 #include <cuda_runtime.h>
 

@@ -36,7 +36,7 @@ extern "C" {
 #define BPE_ERR_CAPACITY 2    /* an output buffer is too small */
 #define BPE_ERR_CUDA 3        /* a CUDA runtime call failed */
 #define BPE_ERR_BAD_TABLE 4   /* bpe_build: the merge table or vocabulary is inconsistent */
-#define BPE_ERR_TIMEOUT 5     /* a device-side wait gave up (no forward progress) */
+#define BPE_ERR_TIMEOUT 5     /* a device-side wait gave up (no current kernel waits) */
 #define BPE_ERR_INTERNAL 6    /* a device-side consistency check failed */
 #define BPE_ERR_BAD_INPUT 7   /* offsets not monotone or outside the buffer, or an id out of range */
 
@@ -88,15 +88,20 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
  *                  d_out_offsets[0] = 0.
  *   h_total_tokens host int64*, may be NULL. When given, the call waits for
  *                  the stream, stores the total token count and returns any
- *                  error found on the device (BPE_ERR_BAD_INPUT, _TIMEOUT,
- *                  _INTERNAL). When NULL such errors are kept and returned by
+ *                  error found on the device (BPE_ERR_BAD_INPUT, _INTERNAL,
+ *                  _CAPACITY). When NULL such errors are kept and returned by
  *                  the next bpe_sync_status() on the handle.
  *   stream         the CUDA stream to run on.
  *
- * Workspace: the handle keeps 4 bytes per input byte (scratch for pre-tokens
- * too long for shared memory, each using the range of its own bytes) plus 16
- * bytes per 4 KiB chunk; it grows (cudaMalloc) the first time a larger batch
- * is seen.
+ * Workspace: the handle keeps about 8.3 bytes per input byte:
+ *   - a pool of 4 bytes per input byte (scratch for pre-tokens too long for
+ *     shared memory, each using the range of its own bytes);
+ *   - a stage of about 4 bytes per input byte (each 4 KiB chunk's ids, before
+ *     the chunk offsets are known);
+ *   - the start bitmask (1 bit per byte);
+ *   - records of long pre-tokens and a few words per chunk.
+ * The workspace grows (cudaFree of the old one, then cudaMalloc) the first
+ * time a larger batch is seen. No kernel of the call waits on another CTA.
  */
 int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
                      int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets,
@@ -114,13 +119,17 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
  *   Limit: n_bytes <= 4 MiB (4,194,304). A larger batch is rejected with
  *   BPE_ERR_INVALID_ARG before anything is queued; split it or use
  *   bpe_encode_batch. n_docs is not limited by the scratch.
- *   Scratch: one 16.8 MB array of static device memory per device (reserved
- *   when the library's module is loaded on that device, not by this call),
- *   holding the look-back descriptors, each 4 KiB chunk's first document, the
- *   pool for pre-tokens too long for shared memory and the pre-token start
- *   bitmask. The call's first kernel zeroes what must start at zero (the
- *   look-back descriptors and the handle's ticket and token count); every
- *   other scratch word is written before it is read.
+ *   Scratch: one 35 MB array of static device memory per device (reserved
+ *   when the library's module is loaded on that device, not by this call).
+ *   It holds bpe_encode_batch's workspace for a 4 MiB batch:
+ *     - each 4 KiB chunk's first document, token count and offset;
+ *     - the records of long pre-tokens;
+ *     - the pre-token start bitmask;
+ *     - the per-chunk stage of ids;
+ *     - the pool for pre-tokens too long for shared memory.
+ *   The call's first kernel zeroes what must start at zero (the handle's
+ *   record counter and token count); every other scratch word is written
+ *   before it is read.
  *   Set-up: the first call on each device looks up the scratch address
  *   (cudaGetSymbolAddress) and sets the kernels' shared-memory limit, with the
  *   handle's device current; make that first call before any stream capture.
@@ -189,11 +198,13 @@ int bpe_decode_batch(bpe_handle* h, const int32_t* d_ids, int64_t n_ids, const i
 int bpe_set_word_cache(bpe_handle* h, int enable);
 
 /*
- * bpe_set_timing_events — measurement hook. When ev_start / ev_stop (two
- * cudaEvent_t created by the caller on the handle's device) are non-NULL, the
- * next bpe_encode_batch calls record ev_start right before the main encode
- * kernel and ev_stop right after it, on the call's stream, so the caller can
- * time that kernel alone. NULL, NULL switches it off.
+ * bpe_set_timing_events — measurement hook. ev_start and ev_stop are two
+ * cudaEvent_t created by the caller on the handle's device. When they are
+ * non-NULL, the next bpe_encode_batch calls record them on the call's stream:
+ *   - ev_start right after the first (bookkeeping) kernel;
+ *   - ev_stop right after the last kernel.
+ * So the caller times the split, encode, scan and compaction kernels together.
+ * NULL, NULL switches it off.
  */
 int bpe_set_timing_events(bpe_handle* h, void* ev_start, void* ev_stop);
 
