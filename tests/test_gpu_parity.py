@@ -177,6 +177,22 @@ def test_random_tables_including_non_monotone(bpe, seed):
     bpe.bpe_destroy(h)
 
 
+def test_token_made_by_two_rules(bpe):
+    # "abc" is made both by (ab, c) and by (a, bc): the miss path must not
+    # assume one rule per token. Ranks put either split first.
+    for order in ([(b"a", b"b"), (b"b", b"c"), (b"ab", b"c"), (b"a", b"bc")],
+                  [(b"b", b"c"), (b"a", b"b"), (b"a", b"bc"), (b"ab", b"c"), (b"abc", b"abc")]):
+        ids = [256, 257, 258, 258] + ([259] if len(order) > 4 else [])
+        m, vb, vo = table_from_pairs(order, ids=ids)
+        h, o = bpe.bpe_build(m, vb, vo, 0), oracle.Oracle(m, vb, vo)
+        rng = random.Random(len(order))
+        docs = [bytes(rng.choice(b"abc  x") for _ in range(rng.randint(0, 40))) for _ in range(400)]
+        docs += [b"abc" * 30, b" abcabc", b"aabbcc", b"abcabcabc"]
+        data, off = batch(docs)
+        check(h, o, data, off, f"two rules for one token ({len(order)} rows)")
+        bpe.bpe_destroy(h)
+
+
 def test_non_identity_ids(bpe):
     # Byte tokens and merged tokens at arbitrary ids (not b and 256 + k).
     pairs = [(b"h", b"e"), (b"he", b"l"), (b"hel", b"l"), (b" ", b"w"), (b"l", b"o")]
