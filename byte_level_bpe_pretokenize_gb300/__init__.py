@@ -6,7 +6,8 @@ no CPU fallback; loading fails loudly when the library is missing.
 
 Low level: ``bpe_build``, ``bpe_encode_batch``, ``bpe_encode_batch_noalloc``,
 ``bpe_pretokenize_batch``, ``bpe_decode_batch``, ``bpe_sync_status``,
-``bpe_destroy`` take device pointers as integers, exactly like the C calls.
+``bpe_destroy`` take device pointers as integers, exactly like the C calls;
+``bpe_encode_batch_host`` takes host pointers.
 High level: ``Tokenizer`` takes torch CUDA tensors and the current stream.
 """
 from __future__ import annotations
@@ -56,7 +57,7 @@ def build(force: bool = False, nvcc: str = "nvcc") -> str:
 _lock = threading.Lock()
 _lib = None
 
-EXPORTS = ["bpe_build", "bpe_encode_batch", "bpe_encode_batch_noalloc", "bpe_pretokenize_batch", "bpe_decode_batch", "bpe_set_word_cache",
+EXPORTS = ["bpe_build", "bpe_encode_batch", "bpe_encode_batch_host", "bpe_encode_batch_noalloc", "bpe_pretokenize_batch", "bpe_decode_batch", "bpe_set_word_cache",
            "bpe_set_timing_events", "bpe_sync_status", "bpe_table_info", "bpe_destroy", "bpe_last_error"]
 
 
@@ -74,6 +75,8 @@ def lib():
             L.bpe_build.argtypes = [p, i64, p, p, i64, ctypes.c_int, ctypes.POINTER(p)]
             L.bpe_encode_batch.restype = ctypes.c_int
             L.bpe_encode_batch.argtypes = [p, p, i64, p, i64, p, i64, p, p, p]
+            L.bpe_encode_batch_host.restype = ctypes.c_int
+            L.bpe_encode_batch_host.argtypes = [p, p, i64, p, i64, p, i64, p, p, p]
             L.bpe_encode_batch_noalloc.restype = ctypes.c_int
             L.bpe_encode_batch_noalloc.argtypes = [p, p, i64, p, i64, p, i64, p, p, p]
             L.bpe_pretokenize_batch.restype = ctypes.c_int
@@ -120,6 +123,17 @@ def bpe_encode_batch(handle: int, d_bytes: int, n_bytes: int, d_doc_offsets: int
     total = ctypes.c_int64(-1)
     _check(lib().bpe_encode_batch(handle, d_bytes, n_bytes, d_doc_offsets, n_docs, d_out_ids, out_capacity,
                                   d_out_offsets, ctypes.byref(total) if want_total else None, stream))
+    return total.value if want_total else None
+
+
+def bpe_encode_batch_host(handle: int, h_bytes: int, n_bytes: int, h_doc_offsets: int, n_docs: int,
+                          h_out_ids: int, out_capacity: int, h_out_offsets: int, want_total: bool,
+                          stream: int) -> int | None:
+    """bpe_encode_batch on host buffers (pointers as integers; page-locked
+    for overlap): copies in, encodes and copies out in a pipeline of slices."""
+    total = ctypes.c_int64(-1)
+    _check(lib().bpe_encode_batch_host(handle, h_bytes, n_bytes, h_doc_offsets, n_docs, h_out_ids, out_capacity,
+                                       h_out_offsets, ctypes.byref(total) if want_total else None, stream))
     return total.value if want_total else None
 
 

@@ -1506,6 +1506,13 @@ __global__ void k_cache_values(const uint8_t* strs, const int64_t* offs, int64_t
   for (int q = 0; q < kCacheMaxIds; ++q) out[4 * i + 1 + q] = q < cnt ? sym[q] : 0u;
 }
 
+// x[0..n) += delta (document offsets of one slice of a host batch: to the
+// slice's bytes before encoding, to the whole batch's ids after).
+__global__ void k_offsets_shift(int64_t* x, int64_t n, int64_t delta) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    x[i] += delta;
+}
+
 // ---------------------------------------------------------------- decoding --
 
 constexpr int kScanBlock = 1024;
@@ -1643,6 +1650,18 @@ struct bpe_handle {
   size_t ws_bytes = 0;
   bool smem_set = false;
   cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
+  // bpe_encode_batch_host: two slots of device buffers, copy streams, events
+  struct HostSlot {
+    uint8_t* bytes = nullptr;
+    int64_t* offs = nullptr;
+    int32_t* ids = nullptr;
+    int64_t* out_offs = nullptr;
+    cudaEvent_t in = nullptr, done = nullptr, free = nullptr;
+  } slot[2];
+  int64_t slot_bytes = 0, slot_docs = 0;  // capacity of each slot
+  cudaStream_t s_h2d = nullptr, s_d2h = nullptr;
+  int64_t* h_totals = nullptr;  // pinned, one per slice
+  int64_t h_totals_cap = 0;
 };
 
 namespace {
@@ -2016,6 +2035,18 @@ int bpe_destroy(bpe_handle* h) {
   cudaFree(h->d_cache);
   cudaFree(h->d_small);
   cudaFree(h->d_ws);
+  for (auto& sl : h->slot) {
+    cudaFree(sl.bytes);
+    cudaFree(sl.offs);
+    cudaFree(sl.ids);
+    cudaFree(sl.out_offs);
+    if (sl.in) cudaEventDestroy(sl.in);
+    if (sl.done) cudaEventDestroy(sl.done);
+    if (sl.free) cudaEventDestroy(sl.free);
+  }
+  if (h->s_h2d) cudaStreamDestroy(h->s_h2d);
+  if (h->s_d2h) cudaStreamDestroy(h->s_d2h);
+  if (h->h_totals) cudaFreeHost(h->h_totals);
   if (h->h_small) cudaFreeHost(h->h_small);
   delete h;
   return BPE_OK;
@@ -2110,6 +2141,137 @@ int bpe_encode_batch_noalloc(bpe_handle* h, const uint8_t* d_bytes, int64_t n_by
     *h_total_tokens = s.total;
     return status_code(s.status);
   }
+  return BPE_OK;
+}
+
+int bpe_encode_batch_host(bpe_handle* h, const uint8_t* h_bytes, int64_t n_bytes, const int64_t* h_doc_offsets,
+                          int64_t n_docs, int32_t* h_out_ids, int64_t out_capacity, int64_t* h_out_offsets,
+                          int64_t* h_total_tokens, bpe_stream_t stream) {
+  if (!h || !h_doc_offsets || !h_out_offsets || n_bytes < 0 || n_docs < 0 || (n_bytes > 0 && !h_bytes))
+    return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch_host: bad arguments");
+  if (out_capacity < 0 || (out_capacity > 0 && !h_out_ids))
+    return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch_host: bad output buffer");
+  const int64_t b_first = h_doc_offsets[0], b_last = h_doc_offsets[n_docs];
+  if (b_first < 0 || b_last < b_first || b_last > n_bytes)
+    return fail(BPE_ERR_BAD_INPUT, "bpe_encode_batch_host: first or last document offset outside the buffer");
+  DeviceGuard g(h->device);
+  cudaStream_t cs = (cudaStream_t)stream;
+  // Slices of whole documents, about (b_last - b_first) / 8 bytes each but at
+  // least 4 MiB; a document longer than that is a slice of its own.
+  const int64_t target = std::max<int64_t>(int64_t(4) << 20, (b_last - b_first + 7) / 8);
+  std::vector<int64_t> cut{0};
+  while (cut.back() < n_docs) {
+    const int64_t d0 = cut.back(), want = h_doc_offsets[d0] + target;
+    int64_t lo = d0 + 1, hi = n_docs;  // last doc boundary at or below want, at least one document
+    while (lo < hi) {
+      const int64_t mid = (lo + hi + 1) / 2;
+      if (h_doc_offsets[mid] <= want) lo = mid;
+      else hi = mid - 1;
+    }
+    const int64_t a = h_doc_offsets[d0], b = h_doc_offsets[lo];
+    if (b < a || b > b_last) return fail(BPE_ERR_BAD_INPUT, "bpe_encode_batch_host: offsets not monotone");
+    cut.push_back(lo);
+  }
+  const int64_t n_slices = std::max<int64_t>(1, (int64_t)cut.size() - 1);
+  if (cut.size() == 1) cut.push_back(0);  // no documents: one empty slice
+  int64_t max_bytes = 0, max_docs = 0;
+  for (int64_t j = 0; j < n_slices; ++j) {
+    max_bytes = std::max(max_bytes, h_doc_offsets[cut[j + 1]] - h_doc_offsets[cut[j]]);
+    max_docs = std::max(max_docs, cut[j + 1] - cut[j]);
+  }
+  // Buffers, streams and events, grown or made on first need.
+  if (max_bytes > h->slot_bytes || max_docs > h->slot_docs) {
+    CK(cudaDeviceSynchronize());
+    const int64_t nb = std::max(max_bytes, h->slot_bytes), nd = std::max(max_docs, h->slot_docs);
+    for (auto& sl : h->slot) {
+      cudaFree(sl.bytes);
+      cudaFree(sl.offs);
+      cudaFree(sl.ids);
+      cudaFree(sl.out_offs);
+      sl.bytes = nullptr;
+      sl.offs = sl.out_offs = nullptr;
+      sl.ids = nullptr;
+    }
+    h->slot_bytes = h->slot_docs = 0;
+    for (auto& sl : h->slot) {
+      CK(cudaMalloc(&sl.bytes, (size_t)std::max<int64_t>(16, nb)));
+      CK(cudaMalloc(&sl.offs, (size_t)(nd + 1) * sizeof(int64_t)));
+      CK(cudaMalloc(&sl.ids, (size_t)std::max<int64_t>(1, nb) * sizeof(int32_t)));
+      CK(cudaMalloc(&sl.out_offs, (size_t)(nd + 1) * sizeof(int64_t)));
+    }
+    h->slot_bytes = nb;
+    h->slot_docs = nd;
+  }
+  for (auto& sl : h->slot) {
+    if (!sl.in) CK(cudaEventCreateWithFlags(&sl.in, cudaEventDisableTiming));
+    if (!sl.done) CK(cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming));
+    if (!sl.free) CK(cudaEventCreateWithFlags(&sl.free, cudaEventDisableTiming));
+  }
+  if (!h->s_h2d) CK(cudaStreamCreateWithFlags(&h->s_h2d, cudaStreamNonBlocking));
+  if (!h->s_d2h) CK(cudaStreamCreateWithFlags(&h->s_d2h, cudaStreamNonBlocking));
+  if (n_slices > h->h_totals_cap) {
+    if (h->h_totals) CK(cudaFreeHost(h->h_totals));
+    h->h_totals = nullptr;
+    h->h_totals_cap = 0;
+    CK(cudaMallocHost(&h->h_totals, (size_t)n_slices * sizeof(int64_t)));
+    h->h_totals_cap = n_slices;
+  }
+  int rc = ensure_ws(h, ws_sizes(h->slot_bytes).total);
+  if (rc) return rc;
+  if (!h->smem_set) {
+    CK(cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
+    h->smem_set = true;
+  }
+  // Slice j: upload (stream h2d) -> encode (the caller's stream) -> count to
+  // the host -> shift offsets, download (stream d2h). Slot j % 2 is reused by
+  // slice j + 2 once slice j's download is done.
+  auto issue_in = [&](int64_t j) -> int {
+    auto& sl = h->slot[j % 2];
+    const int64_t d0 = cut[j], nd = cut[j + 1] - d0, b0 = h_doc_offsets[d0], nb = h_doc_offsets[cut[j + 1]] - b0;
+    if (j >= 2) CK(cudaStreamWaitEvent(h->s_h2d, sl.free, 0));
+    if (nb > 0) CK(cudaMemcpyAsync(sl.bytes, h_bytes + b0, (size_t)nb, cudaMemcpyHostToDevice, h->s_h2d));
+    CK(cudaMemcpyAsync(sl.offs, h_doc_offsets + d0, (size_t)(nd + 1) * sizeof(int64_t), cudaMemcpyHostToDevice,
+                       h->s_h2d));
+    CK(cudaEventRecord(sl.in, h->s_h2d));
+    CK(cudaStreamWaitEvent(cs, sl.in, 0));
+    k_offsets_shift<<<(unsigned)std::min<int64_t>(1024, nd / 256 + 1), 256, 0, cs>>>(sl.offs, nd + 1, -b0);
+    CK(cudaGetLastError());
+    int r = launch_encode(h, ws_carve(static_cast<unsigned char*>(h->d_ws), nb), sl.bytes, nb, sl.offs, nd, sl.ids,
+                          nb, sl.out_offs, cs, nullptr, nullptr);
+    if (r) return r;
+    CK(cudaMemcpyAsync(h->h_totals + j, &h->d_small->total, sizeof(int64_t), cudaMemcpyDeviceToHost, cs));
+    CK(cudaEventRecord(sl.done, cs));
+    return BPE_OK;
+  };
+  for (int64_t j = 0; j < std::min<int64_t>(2, n_slices); ++j)
+    if ((rc = issue_in(j))) return rc;
+  int64_t base = 0;
+  for (int64_t j = 0; j < n_slices; ++j) {
+    auto& sl = h->slot[j % 2];
+    const int64_t d0 = cut[j], nd = cut[j + 1] - d0;
+    CK(cudaEventSynchronize(sl.done));
+    const int64_t tot = h->h_totals[j];
+    CK(cudaStreamWaitEvent(h->s_d2h, sl.done, 0));
+    k_offsets_shift<<<(unsigned)std::min<int64_t>(1024, nd / 256 + 1), 256, 0, h->s_d2h>>>(sl.out_offs, nd + 1, base);
+    CK(cudaGetLastError());
+    const int64_t fit = std::max<int64_t>(0, std::min(tot, out_capacity - base));
+    if (fit > 0)
+      CK(cudaMemcpyAsync(h_out_ids + base, sl.ids, (size_t)fit * sizeof(int32_t), cudaMemcpyDeviceToHost, h->s_d2h));
+    const int64_t n_out = nd + (j == n_slices - 1 ? 1 : 0);  // the next slice writes its first offset
+    if (n_out > 0)
+      CK(cudaMemcpyAsync(h_out_offsets + d0, sl.out_offs, (size_t)n_out * sizeof(int64_t), cudaMemcpyDeviceToHost,
+                         h->s_d2h));
+    CK(cudaEventRecord(sl.free, h->s_d2h));
+    base += tot;
+    if (j + 2 < n_slices && (rc = issue_in(j + 2))) return rc;
+  }
+  CK(cudaStreamSynchronize(h->s_d2h));
+  DevSmall s;
+  rc = read_status(h, cs, &s);
+  if (rc) return rc;
+  if (h_total_tokens) *h_total_tokens = base;
+  if (s.status) return status_code(s.status);
+  if (base > out_capacity) return fail(BPE_ERR_CAPACITY, "output capacity exceeded");
   return BPE_OK;
 }
 

@@ -108,6 +108,44 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
                      int64_t* h_total_tokens, bpe_stream_t stream);
 
 /*
+ * bpe_encode_batch_host — bpe_encode_batch on host buffers. It does the whole
+ * round trip and returns when the ids and offsets are in host memory. The
+ * pages have no counterpart: the v1 engine of "Hugging Face Tokenizers v1"
+ * runs on the CPU.
+ *
+ * Arguments are those of bpe_encode_batch, but host pointers (h_bytes,
+ * h_doc_offsets, h_out_ids, h_out_offsets). Use page-locked memory
+ * (cudaMallocHost) for overlap; pageable memory works but copies serialise.
+ *
+ * Pipeline:
+ *   - The batch is cut on document boundaries into about 8 slices of at least
+ *     4 MiB each; a longer document is a slice of its own.
+ *   - Slice j's bytes and offsets are copied in on a copy stream of the handle.
+ *   - Slice j is encoded on `stream`.
+ *   - Slice j-1's ids and offsets are copied out on a second copy stream.
+ *   - Two slots of device buffers alternate.
+ *
+ * Each slice's token count is read on the host (through page-locked memory)
+ * before its ids are copied out, so exactly the ids are moved. The offsets
+ * are made absolute on the device.
+ *
+ * Results equal those of bpe_encode_batch on the same batch.
+ *
+ * Memory: the handle keeps two slots of (slice bytes + 4 B per slice byte +
+ * 16 B per slice document) and bpe_encode_batch's workspace for one slice.
+ * It grows the first time a larger slice is seen.
+ *
+ * Errors: BPE_ERR_BAD_INPUT when the first or last offset is outside the
+ * buffer or the slice edges are not monotone (checked on the host), and as
+ * for bpe_encode_batch otherwise. BPE_ERR_CAPACITY when the ids do not fit
+ * (*h_total_tokens then holds the count needed; ids past out_capacity are
+ * not written).
+ */
+int bpe_encode_batch_host(bpe_handle* h, const uint8_t* h_bytes, int64_t n_bytes, const int64_t* h_doc_offsets,
+                          int64_t n_docs, int32_t* h_out_ids, int64_t out_capacity, int64_t* h_out_offsets,
+                          int64_t* h_total_tokens, bpe_stream_t stream);
+
+/*
  * bpe_encode_batch_noalloc — bpe_encode_batch with fixed scratch: the same
  * arguments, kernels and results, but the call allocates no device memory.
  * The pages have no counterpart; this is a library-level variant for callers
