@@ -78,6 +78,7 @@ constexpr int kSpanWords = kSpan / 32;
 constexpr int kShortMax = 64;         // longest pre-token merged by one thread
 constexpr int kCacheMaxLen = 16;      // longest pre-token looked up in the word cache
 constexpr int kCacheMaxIds = 3;       // most ids a cache entry holds
+constexpr int kProbeRound = 3;        // word-cache probes a thread has in flight
 constexpr int kLongPerThread = 4;     // elements per thread per round of the CTA merge
 constexpr int kRound = kThreads * kLongPerThread;
 constexpr int kMaxLong = kChunk / kShortMax + 2;
@@ -358,14 +359,13 @@ struct __align__(16) SplitSmem {
   uint8_t win[kWin + 16];
   uint32_t docbits[kWinWords + 2];   // a document (or the area after the last one) starts here
   uint32_t outbits[kWinWords + 2];   // byte belongs to no document
-  union {
-    uint32_t startbits[kSpanWords];
-    uint16_t missq[kMissShortCap + kMissMedCap];  // word-cache misses, once the start bits are consumed
-  };
+  uint32_t startbits[kSpanWords];
   int64_t chunk;
 };
 
 struct Smem : SplitSmem {
+  uint16_t missq[kMissShortCap + kMissMedCap];  // queued word-cache misses
+  uint16_t grp_pos[kThreads];        // pre-tokens starting before chunk byte 16 t
   uint16_t span_start[kChunk + 1];
   uint32_t span_cnt[kChunk + 1];     // token counts, then exclusive offsets
   uint32_t sym[kSpan];               // ids of short pre-tokens, at their start position
@@ -945,7 +945,7 @@ struct CacheKey {
   uint32_t x0, x1, x2, x3, len, slot;
 };
 
-__device__ __forceinline__ CacheKey cache_key(const Smem& S, int st, int len, const Cache& C) {
+__device__ __forceinline__ CacheKey cache_key_words(const Smem& S, int st, int len) {
   const int ws = kHalo + st;
   const uint32_t* wv = reinterpret_cast<const uint32_t*>(S.win) + (ws >> 2);
   const uint32_t sh = (uint32_t)(ws & 3) * 8u;
@@ -961,6 +961,12 @@ __device__ __forceinline__ CacheKey cache_key(const Smem& S, int st, int len, co
   K.x2 = __funnelshift_r(a2, a3, sh) & keep(2);
   K.x3 = __funnelshift_r(a3, a4, sh) & keep(3);
   K.len = (uint32_t)len;
+  K.slot = 0;
+  return K;
+}
+
+__device__ __forceinline__ CacheKey cache_key(const Smem& S, int st, int len, const Cache& C) {
+  CacheKey K = cache_key_words(S, st, len);
   K.slot = cache_hash(K.x0, K.x1, K.x2, K.x3, K.len) & C.mask;
   return K;
 }
@@ -1066,6 +1072,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
     const uint32_t bits = (S.startbits[tid >> 1] >> ((tid & 1) * 16)) & 0xFFFFu;
     uint32_t total;
     uint32_t pos = block_excl_scan(__popc(bits), S.red, &total);
+    S.grp_pos[tid] = (uint16_t)pos;
     uint32_t b = bits;
     while (b) {
       int k = __ffs(b) - 1;
@@ -1104,56 +1111,60 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
   const uint32_t n_spans = S.n_spans;
   const int last_end = S.last_end_rel;
 
-  // Short pre-tokens, one thread each, two per round with their word-cache
-  // probes in flight together. Hits finish here; misses are queued and
-  // merged next by lane groups, so a warp does not wait on the merge loop of
-  // a few of its lanes.
-  for (uint32_t j0 = tid; j0 < n_spans; j0 += 2 * kThreads) {
-    int st[2], len[2];
-    bool shortp[2], probe[2];
-    CacheKey K[2];
-    uint4 ea[2], eb[2];
+  // Short pre-tokens, one thread each, kProbeRound per round with their
+  // word-cache probes in flight together (a thread keeps only each probe's
+  // slot and entry; the key is read again from the window to compare). Hits
+  // finish here; misses are queued and merged next by lane groups, so a warp
+  // does not wait on the merge loop of a few of its lanes.
+  for (uint32_t j0 = tid; j0 < n_spans; j0 += kProbeRound * kThreads) {
+    int st[kProbeRound], len[kProbeRound];
+    uint32_t slot[kProbeRound];
+    uint4 ea[kProbeRound], eb[kProbeRound];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < kProbeRound; ++h) {
       const uint32_t j = j0 + (uint32_t)h * kThreads;
       st[h] = 0;
-      len[h] = 0;
-      shortp[h] = probe[h] = false;
+      len[h] = -1;  // -1: no pre-token; > kShortMax: long
+      slot[h] = kNone;
       if (j < n_spans) {
         st[h] = S.span_start[j];
         const int en = (j + 1 < n_spans) ? (int)S.span_start[j + 1] : last_end;
         len[h] = en < 0 ? kSpan : en - st[h];
-        shortp[h] = en >= 0 && len[h] <= kShortMax;
-        probe[h] = shortp[h] && a.C.enabled && len[h] <= kCacheMaxLen;
-      }
-      if (probe[h]) {
-        K[h] = cache_key(S, st[h], len[h], a.C);
-        ea[h] = __ldg(a.C.e + 2 * K[h].slot);
-        eb[h] = __ldg(a.C.e + 2 * K[h].slot + 1);
+        if (len[h] <= kCacheMaxLen && a.C.enabled) {
+          const CacheKey K = cache_key(S, st[h], len[h], a.C);
+          slot[h] = K.slot;
+          ea[h] = __ldg(a.C.e + 2 * K.slot);
+          eb[h] = __ldg(a.C.e + 2 * K.slot + 1);
+        }
       }
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < kProbeRound; ++h) {
       const uint32_t j = j0 + (uint32_t)h * kThreads;
-      if (j >= n_spans) continue;
-      if (shortp[h]) {
+      if (len[h] < 0) continue;
+      if (len[h] <= kShortMax) {
         uint32_t ids[kCacheMaxIds];
-        const uint32_t cnt = probe[h] ? cache_resolve(a.C, K[h], ea[h], eb[h], ids) : 0u;
+        uint32_t cnt = 0;
+        if (slot[h] != kNone) {
+          CacheKey K = cache_key_words(S, st[h], len[h]);
+          K.slot = slot[h];
+          cnt = cache_resolve(a.C, K, ea[h], eb[h], ids);
+        }
         if (cnt) {
           for (uint32_t q = 0; q < cnt; ++q) S.sym[st[h] + q] = ids[q];
           S.span_cnt[j] = cnt;
         } else if (len[h] <= kCacheMaxLen) {
-          const uint32_t slot = atomicAdd(&S.n_miss, 1u);
-          if (slot < kMissShortCap) S.missq[slot] = (uint16_t)j;
+          const uint32_t qs = atomicAdd(&S.n_miss, 1u);
+          if (qs < kMissShortCap) S.missq[qs] = (uint16_t)j;
           else S.span_cnt[j] = merge_at(S, st[h], len[h], a.T);  // queue full: merge here
         } else {
-          const uint32_t slot = atomicAdd(&S.n_miss_m, 1u);
-          if (slot < kMissMedCap) S.missq[kMissShortCap + slot] = (uint16_t)j;
+          const uint32_t qm = atomicAdd(&S.n_miss_m, 1u);
+          if (qm < kMissMedCap) S.missq[kMissShortCap + qm] = (uint16_t)j;
           else S.span_cnt[j] = merge_at(S, st[h], len[h], a.T);
         }
       } else {
-        const uint32_t slot = atomicAdd(&S.n_long, 1u);
-        if (slot < (uint32_t)kMaxLong) S.long_list[slot] = (uint16_t)j;
+        const uint32_t ql = atomicAdd(&S.n_long, 1u);
+        if (ql < (uint32_t)kMaxLong) S.long_list[ql] = (uint16_t)j;
         else atomicOr(&a.small->status, kStInternal);
         S.span_cnt[j] = 0;
       }
@@ -1330,14 +1341,11 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
       const int64_t d = k == k_first + tid ? d_mine : a.doc_offsets[k];
       if (d >= c0 + kChunk) break;
       if (d < c0) continue;
-      const int rel = (int)(d - c0);
-      uint32_t lo = 0, hi = n_spans;  // first span starting at or after d
-      while (lo < hi) {
-        uint32_t mid = (lo + hi) >> 1;
-        if (S.span_start[mid] < rel) lo = mid + 1;
-        else hi = mid;
-      }
-      a.out_offsets[k] = S.span_cnt[lo];
+      // the first pre-token starting at or after d: those before d's 16-byte
+      // group, plus the group's starts before d
+      const int rel = (int)(d - c0), t = rel >> 4;
+      const uint32_t gbits = (S.startbits[t >> 1] >> ((t & 1) * 16)) & ((1u << (rel & 15)) - 1u);
+      a.out_offsets[k] = S.span_cnt[S.grp_pos[t] + __popc(gbits)];
     }
   }
 }
@@ -1424,8 +1432,19 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const uint32_t* 
   if (lane == 0 && P + (int64_t)cnt > out_capacity) atomicOr(&small->status, kStCapacity);
   const int64_t lim = out_capacity - P;
   if (r1 == 0) {
-    for (uint32_t q = lane; q < cnt; q += 32)
-      if ((int64_t)q < lim) out_ids[P + q] = (int32_t)src[q];
+    for (uint32_t q0 = 0; q0 < cnt; q0 += 128) {  // four loads in flight per lane
+      uint32_t v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t q = q0 + 32 * u + lane;
+        v[u] = q < cnt ? src[q] : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t q = q0 + 32 * u + lane;
+        if (q < cnt && (int64_t)q < lim) out_ids[P + q] = (int32_t)v[u];
+      }
+    }
   } else {
     const uint32_t* R = rec + (r1 - 1);
     const uint32_t n_long = R[0];
