@@ -78,7 +78,7 @@ constexpr int kSpanWords = kSpan / 32;
 constexpr int kShortMax = 64;         // longest pre-token merged by one thread
 constexpr int kCacheMaxLen = 16;      // longest pre-token looked up in the word cache
 constexpr int kCacheMaxIds = 3;       // most ids a cache entry holds
-constexpr int kProbeRound = 3;        // word-cache probes a thread has in flight
+constexpr int kProbeRound = 2;        // word-cache probes a thread has in flight
 constexpr int kLongPerThread = 4;     // elements per thread per round of the CTA merge
 constexpr int kRound = kThreads * kLongPerThread;
 constexpr int kMaxLong = kChunk / kShortMax + 2;
@@ -951,15 +951,15 @@ __device__ __forceinline__ CacheKey cache_key_words(const Smem& S, int st, int l
   const uint32_t sh = (uint32_t)(ws & 3) * 8u;
   const uint32_t a0 = lds_u32(wv), a1 = lds_u32(wv + 1), a2 = lds_u32(wv + 2), a3 = lds_u32(wv + 3),
                  a4 = lds_u32(wv + 4);
-  auto keep = [len](int k) {
-    const int nb = len - 4 * k;
-    return nb >= 4 ? 0xFFFFFFFFu : (nb <= 0 ? 0u : ((1u << (8 * nb)) - 1u));
-  };
+  // bytes at or past len are zeroed: a 64-bit mask per half (len <= 16)
+  const uint32_t nbit = 8u * (uint32_t)len;
+  const uint64_t m_lo = nbit >= 64 ? ~0ull : (1ull << nbit) - 1ull;
+  const uint64_t m_hi = nbit <= 64 ? 0ull : (nbit >= 128 ? ~0ull : (1ull << (nbit - 64)) - 1ull);
   CacheKey K;
-  K.x0 = __funnelshift_r(a0, a1, sh) & keep(0);
-  K.x1 = __funnelshift_r(a1, a2, sh) & keep(1);
-  K.x2 = __funnelshift_r(a2, a3, sh) & keep(2);
-  K.x3 = __funnelshift_r(a3, a4, sh) & keep(3);
+  K.x0 = __funnelshift_r(a0, a1, sh) & (uint32_t)m_lo;
+  K.x1 = __funnelshift_r(a1, a2, sh) & (uint32_t)(m_lo >> 32);
+  K.x2 = __funnelshift_r(a2, a3, sh) & (uint32_t)m_hi;
+  K.x3 = __funnelshift_r(a3, a4, sh) & (uint32_t)(m_hi >> 32);
   K.len = (uint32_t)len;
   K.slot = 0;
   return K;
@@ -1118,23 +1118,22 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
   // does not wait on the merge loop of a few of its lanes.
   for (uint32_t j0 = tid; j0 < n_spans; j0 += kProbeRound * kThreads) {
     int st[kProbeRound], len[kProbeRound];
-    uint32_t slot[kProbeRound];
+    CacheKey K[kProbeRound];
     uint4 ea[kProbeRound], eb[kProbeRound];
 #pragma unroll
     for (int h = 0; h < kProbeRound; ++h) {
       const uint32_t j = j0 + (uint32_t)h * kThreads;
       st[h] = 0;
       len[h] = -1;  // -1: no pre-token; > kShortMax: long
-      slot[h] = kNone;
+      K[h].slot = kNone;
       if (j < n_spans) {
         st[h] = S.span_start[j];
         const int en = (j + 1 < n_spans) ? (int)S.span_start[j + 1] : last_end;
         len[h] = en < 0 ? kSpan : en - st[h];
         if (len[h] <= kCacheMaxLen && a.C.enabled) {
-          const CacheKey K = cache_key(S, st[h], len[h], a.C);
-          slot[h] = K.slot;
-          ea[h] = __ldg(a.C.e + 2 * K.slot);
-          eb[h] = __ldg(a.C.e + 2 * K.slot + 1);
+          K[h] = cache_key(S, st[h], len[h], a.C);
+          ea[h] = __ldg(a.C.e + 2 * K[h].slot);
+          eb[h] = __ldg(a.C.e + 2 * K[h].slot + 1);
         }
       }
     }
@@ -1144,12 +1143,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
       if (len[h] < 0) continue;
       if (len[h] <= kShortMax) {
         uint32_t ids[kCacheMaxIds];
-        uint32_t cnt = 0;
-        if (slot[h] != kNone) {
-          CacheKey K = cache_key_words(S, st[h], len[h]);
-          K.slot = slot[h];
-          cnt = cache_resolve(a.C, K, ea[h], eb[h], ids);
-        }
+        const uint32_t cnt = K[h].slot != kNone ? cache_resolve(a.C, K[h], ea[h], eb[h], ids) : 0u;
         if (cnt) {
           for (uint32_t q = 0; q < cnt; ++q) S.sym[st[h] + q] = ids[q];
           S.span_cnt[j] = cnt;
