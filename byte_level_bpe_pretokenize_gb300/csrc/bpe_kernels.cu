@@ -361,6 +361,7 @@ struct __align__(16) SplitSmem {
   uint32_t outbits[kWinWords + 2];   // byte belongs to no document
   uint32_t startbits[kSpanWords];
   int64_t chunk;
+  int more_docs;  // more documents start in the window (or chunk) than one per thread
 };
 
 struct Smem : SplitSmem {
@@ -551,6 +552,7 @@ __device__ void load_window(SplitSmem& S, const uint8_t* bytes, int64_t n_bytes,
     }
   }
   for (int i = tid; i < kWinWords + 2; i += kThreads) S.docbits[i] = 0;
+  if (tid == kThreads - 1) S.more_docs = o_mine < w_end;
   cta_sync();
   d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
   d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
@@ -568,7 +570,7 @@ __device__ void load_window(SplitSmem& S, const uint8_t* bytes, int64_t n_bytes,
     const int i = (int)(o_mine - w0);
     atomicOr(&S.docbits[i >> 5], 1u << (i & 31));
   }
-  if (o_mine < w_end) {  // tiny documents: more than kThreads - 32 start in the window
+  if (S.more_docs && o_mine < w_end) {  // tiny documents: more than kThreads - 32 start in the window
     for (int64_t k = k_lo + tid + kThreads; k <= n_docs; k += kThreads) {
       const int64_t o = doc_offsets[k];
       if (o >= w_end) break;
@@ -1064,6 +1066,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
   // the end, the offsets of the first kThreads documents from there on.
   const int64_t k_first = __ldg(a.first_doc + c);
   const int64_t d_mine = k_first + tid <= a.n_docs ? __ldg(a.doc_offsets + k_first + tid) : INT64_MAX;
+  if (tid == kThreads - 1) S.more_docs = d_mine < c0 + kChunk;  // more than kThreads documents start here
   load_encode_window(S, a.bytes, a.n_bytes, a.doc_offsets, a.n_docs, a.start_bits, c0);
 
   // Pre-tokens starting in the chunk, in order. Thread t owns positions
@@ -1331,15 +1334,18 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
   // Offsets of the documents that start in this chunk, relative to the
   // chunk's first id (k_compact adds the chunk's offset).
   {
+    const bool more = S.more_docs;
     for (int64_t k = k_first + tid; k <= a.n_docs; k += kThreads) {
       const int64_t d = k == k_first + tid ? d_mine : a.doc_offsets[k];
       if (d >= c0 + kChunk) break;
-      if (d < c0) continue;
+      if (d >= c0) {
       // the first pre-token starting at or after d: those before d's 16-byte
       // group, plus the group's starts before d
-      const int rel = (int)(d - c0), t = rel >> 4;
-      const uint32_t gbits = (S.startbits[t >> 1] >> ((t & 1) * 16)) & ((1u << (rel & 15)) - 1u);
-      a.out_offsets[k] = S.span_cnt[S.grp_pos[t] + __popc(gbits)];
+        const int rel = (int)(d - c0), t = rel >> 4;
+        const uint32_t gbits = (S.startbits[t >> 1] >> ((t & 1) * 16)) & ((1u << (rel & 15)) - 1u);
+        a.out_offsets[k] = S.span_cnt[S.grp_pos[t] + __popc(gbits)];
+      }
+      if (!more) break;
     }
   }
 }
