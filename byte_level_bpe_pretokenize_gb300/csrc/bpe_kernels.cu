@@ -90,7 +90,6 @@ constexpr uint32_t kNone = 0xFFFFFFFFu;
 constexpr uint32_t kEmptySlot = 0xFFFFFFFFu;  // left id of an unused pair-table slot
 
 static_assert(kChunk == 16 * kThreads, "one 16-byte group per thread");
-static_assert(kMargin <= 16 * 16, "the margin is covered by 16 lanes of warp 0");
 static_assert(kShortMax <= 64 && kCacheMaxLen <= 16, "group merges hold 2 symbols per lane");
 
 // device status bits
@@ -631,17 +630,13 @@ __device__ void load_encode_window(SplitSmem& S, const uint8_t* bytes, int64_t n
   cta_sync();
 }
 
-// Start bits for window indices [kHalo, kHalo + kSpan).
+// Start bits of the chunk, window indices [kHalo, kHalo + kChunk) (the encode
+// kernel takes the margin's from the next chunk's output).
 __device__ void compute_start_bits(SplitSmem& S) {
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   uint32_t m = start_mask16(S, kHalo + 16 * tid);
   uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, m, 1);
   if ((tid & 1) == 0) S.startbits[tid >> 1] = m | (hi << 16);
-  if (tid < 32) {  // the margin, 16 bytes per lane
-    uint32_t mm = lane < kMargin / 16 ? start_mask16(S, kHalo + kChunk + 16 * lane) : 0u;
-    uint32_t h2 = __shfl_down_sync(0xFFFFFFFFu, mm, 1);
-    if ((lane & 1) == 0 && lane < kMargin / 16) S.startbits[kChunk / 32 + (lane >> 1)] = mm | (h2 << 16);
-  }
   cta_sync();
 }
 
