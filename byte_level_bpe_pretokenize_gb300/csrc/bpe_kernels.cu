@@ -1664,14 +1664,16 @@ struct bpe_handle {
   size_t ws_bytes = 0;
   bool smem_set = false;
   cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
-  // bpe_encode_batch_host: two slots of device buffers, copy streams, events
+  // bpe_encode_batch_host: kHostSlots slots of device buffers, copy streams,
+  // events
+  static constexpr int kHostSlots = 3;
   struct HostSlot {
     uint8_t* bytes = nullptr;
     int64_t* offs = nullptr;
     int32_t* ids = nullptr;
     int64_t* out_offs = nullptr;
     cudaEvent_t in = nullptr, done = nullptr, free = nullptr;
-  } slot[2];
+  } slot[kHostSlots];
   int64_t slot_bytes = 0, slot_docs = 0;  // capacity of each slot
   cudaStream_t s_h2d = nullptr, s_d2h = nullptr;
   int64_t* h_totals = nullptr;  // pinned, one per slice
@@ -2170,9 +2172,9 @@ int bpe_encode_batch_host(bpe_handle* h, const uint8_t* h_bytes, int64_t n_bytes
     return fail(BPE_ERR_BAD_INPUT, "bpe_encode_batch_host: first or last document offset outside the buffer");
   DeviceGuard g(h->device);
   cudaStream_t cs = (cudaStream_t)stream;
-  // Slices of whole documents, about (b_last - b_first) / 8 bytes each but at
+  // Slices of whole documents, about (b_last - b_first) / 12 bytes each but at
   // least 4 MiB; a document longer than that is a slice of its own.
-  const int64_t target = std::max<int64_t>(int64_t(4) << 20, (b_last - b_first + 7) / 8);
+  const int64_t target = std::max<int64_t>(int64_t(4) << 20, (b_last - b_first + 11) / 12);
   std::vector<int64_t> cut{0};
   while (cut.back() < n_docs) {
     const int64_t d0 = cut.back(), want = h_doc_offsets[d0] + target;
@@ -2237,12 +2239,13 @@ int bpe_encode_batch_host(bpe_handle* h, const uint8_t* h_bytes, int64_t n_bytes
     h->smem_set = true;
   }
   // Slice j: upload (stream h2d) -> encode (the caller's stream) -> count to
-  // the host -> shift offsets, download (stream d2h). Slot j % 2 is reused by
-  // slice j + 2 once slice j's download is done.
+  // the host -> shift offsets, download (stream d2h). Slot j % kHostSlots is
+  // reused by slice j + kHostSlots once slice j's download is done.
+  constexpr int NS = bpe_handle::kHostSlots;
   auto issue_in = [&](int64_t j) -> int {
-    auto& sl = h->slot[j % 2];
+    auto& sl = h->slot[j % NS];
     const int64_t d0 = cut[j], nd = cut[j + 1] - d0, b0 = h_doc_offsets[d0], nb = h_doc_offsets[cut[j + 1]] - b0;
-    if (j >= 2) CK(cudaStreamWaitEvent(h->s_h2d, sl.free, 0));
+    if (j >= NS) CK(cudaStreamWaitEvent(h->s_h2d, sl.free, 0));
     if (nb > 0) CK(cudaMemcpyAsync(sl.bytes, h_bytes + b0, (size_t)nb, cudaMemcpyHostToDevice, h->s_h2d));
     CK(cudaMemcpyAsync(sl.offs, h_doc_offsets + d0, (size_t)(nd + 1) * sizeof(int64_t), cudaMemcpyHostToDevice,
                        h->s_h2d));
@@ -2257,11 +2260,11 @@ int bpe_encode_batch_host(bpe_handle* h, const uint8_t* h_bytes, int64_t n_bytes
     CK(cudaEventRecord(sl.done, cs));
     return BPE_OK;
   };
-  for (int64_t j = 0; j < std::min<int64_t>(2, n_slices); ++j)
+  for (int64_t j = 0; j < std::min<int64_t>(NS, n_slices); ++j)
     if ((rc = issue_in(j))) return rc;
   int64_t base = 0;
   for (int64_t j = 0; j < n_slices; ++j) {
-    auto& sl = h->slot[j % 2];
+    auto& sl = h->slot[j % NS];
     const int64_t d0 = cut[j], nd = cut[j + 1] - d0;
     CK(cudaEventSynchronize(sl.done));
     const int64_t tot = h->h_totals[j];
@@ -2277,7 +2280,7 @@ int bpe_encode_batch_host(bpe_handle* h, const uint8_t* h_bytes, int64_t n_bytes
                          h->s_d2h));
     CK(cudaEventRecord(sl.free, h->s_d2h));
     base += tot;
-    if (j + 2 < n_slices && (rc = issue_in(j + 2))) return rc;
+    if (j + NS < n_slices && (rc = issue_in(j + NS))) return rc;
   }
   CK(cudaStreamSynchronize(h->s_d2h));
   DevSmall s;
