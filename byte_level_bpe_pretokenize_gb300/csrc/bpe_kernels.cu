@@ -354,14 +354,24 @@ struct GroupScratch {
 
 // What the split needs: the window and its document and start bit masks. The
 // split kernel's shared memory is only this; the encode kernel's extends it.
-struct __align__(16) SplitSmem {
-  uint8_t win[kWin + 16];
-  uint32_t docbits[kWinWords + 2];   // a document (or the area after the last one) starts here
-  uint32_t outbits[kWinWords + 2];   // byte belongs to no document
-  uint32_t startbits[kSpanWords];
+template <int CHUNK, int AFTER>
+struct __align__(16) WindowSmem {
+  static constexpr int kLen = kHalo + CHUNK + AFTER + kHalo;  // window bytes
+  static constexpr int kWords = (kLen + 31) / 32;
+  uint8_t win[kLen + 16];
+  uint32_t docbits[kWords + 2];   // a document (or the area after the last one) starts here
+  uint32_t outbits[kWords + 2];   // byte belongs to no document
+  uint32_t startbits[(CHUNK + AFTER) / 32];
   int64_t chunk;
   int more_docs;  // more documents start in the window (or chunk) than one per thread
 };
+
+// The encode kernel's window: a chunk plus the margin.
+using SplitSmem = WindowSmem<kChunk, kMargin>;
+static_assert(SplitSmem::kLen == kWin && SplitSmem::kWords == kWinWords, "encode window");
+// The split kernel's window: 32 bytes per thread.
+constexpr int kSplitChunk = 32 * kThreads;
+using SplitWin = WindowSmem<kSplitChunk, kHalo>;
 
 struct Smem : SplitSmem {
   uint16_t missq[kMissShortCap + kMissMedCap];  // queued word-cache misses
@@ -398,24 +408,33 @@ __device__ __forceinline__ bool bit_at(const uint32_t* bits, int i) { return (bi
 // Document bounds [lo, hi) around window index i: the nearest document edge at
 // or before i and the next one after i (at most kHalo away is all that is
 // read), or the window edges.
-__device__ __forceinline__ void doc_bounds(const SplitSmem& S, int i, int* lo, int* hi) {
+template <class SS>
+__device__ __forceinline__ void doc_bounds(const SS& S, int i, int* lo, int* hi) {
   int a = i;
   while (a > 0 && a > i - kHalo && !bit_at(S.docbits, a)) --a;
   *lo = a;
   int b = i + 1;
-  while (b < kWin && b <= i + kHalo && !bit_at(S.docbits, b)) ++b;
+  while (b < SS::kLen && b <= i + kHalo && !bit_at(S.docbits, b)) ++b;
   *hi = b;
 }
 
-__device__ __forceinline__ bool starts_piece_at(const SplitSmem& S, int i) {
+template <class SS>
+__device__ __forceinline__ bool starts_piece_at(const SS& S, int i) {
   if (bit_at(S.outbits, i)) return false;
   int lo, hi;
   doc_bounds(S, i, &lo, &hi);
   return starts_piece<int>(S.win, lo, hi, i);
 }
 
+// Bits [start, start + 64) of a shared bit array.
+__device__ __forceinline__ uint64_t bits64_at(const uint32_t* bits, int start) {
+  const int w = start >> 5, sh = start & 31;
+  const uint32_t a = lds_u32(bits + w), b = lds_u32(bits + w + 1), c = lds_u32(bits + w + 2);
+  return (uint64_t)__funnelshift_r(a, b, sh) | (uint64_t)__funnelshift_r(b, c, sh) << 32;
+}
+
 // Boundary rules on class masks. Bit k of every mask is window byte
-// p0 - 8 + k; the result is bits 8..23 (positions p0 .. p0 + 15). U marks unit
+// p0 - 8 + k; the result is bits 8..39 (positions p0 .. p0 + 31). U marks unit
 // starts, L / N / S the class of the unit holding each byte, SP bytes equal to
 // U+0020, AP apostrophes, D document edges, O bytes outside every document.
 // B2 and B3 come from the masks directly. Contractions (B0 / B1) are resolved
@@ -424,95 +443,100 @@ __device__ __forceinline__ bool starts_piece_at(const SplitSmem& S, int i) {
 // U+0020) and the next one or two bytes of its document are a suffix; then
 // the byte after it gets no boundary (B0) and the byte after the suffix gets
 // one (B1).
-__device__ __forceinline__ uint32_t boundaries16(const SplitSmem& S, int p0, uint32_t U, uint32_t L, uint32_t N,
-                                                 uint32_t Sm, uint32_t SP, uint32_t AP, uint32_t D, uint32_t O) {
-  const uint32_t Sp = Sm << 1, Lp = L << 1, Np = N << 1, SPp = SP << 1;
-  const uint32_t Sn = Sm >> 1, Dn = D >> 1;
-  const uint32_t B2 = Sm & (~Sp | (~Sn & ~Dn));
-  const uint32_t B3 = ~Sm & ~SPp & (Sp | (L ^ Lp) | (N ^ Np));
-  uint32_t base = D | B2 | B3;
-  uint32_t ap = AP & 0x007FFFE0u;  // apostrophes at bytes p0 - 3 .. p0 + 14
+template <class SS>
+__device__ __forceinline__ uint32_t boundaries32(const SS& S, int p0, uint64_t U, uint64_t L, uint64_t N,
+                                                 uint64_t Sm, uint64_t SP, uint64_t AP, uint64_t D, uint64_t O) {
+  const uint64_t Sp = Sm << 1, Lp = L << 1, Np = N << 1, SPp = SP << 1;
+  const uint64_t Sn = Sm >> 1, Dn = D >> 1;
+  const uint64_t B2 = Sm & (~Sp | (~Sn & ~Dn));
+  const uint64_t B3 = ~Sm & ~SPp & (Sp | (L ^ Lp) | (N ^ Np));
+  uint64_t base = D | B2 | B3;
+  uint64_t ap = AP & 0x7FFFFFFFE0ull;  // apostrophes at bytes p0 - 3 .. p0 + 30
   if (ap) {
-    const uint32_t prev_ok = (L | N | (Sm & ~SP)) << 1;  // bit k: byte k - 1 makes an apostrophe at k eligible
-    uint32_t B0 = 0, B1 = 0;
+    const uint64_t prev_ok = (L | N | (Sm & ~SP)) << 1;  // bit k: byte k - 1 makes an apostrophe at k eligible
+    uint64_t B0 = 0, B1 = 0;
     while (ap) {
-      const int k = __ffs(ap) - 1;
+      const int k = __ffsll((long long)ap) - 1;
       ap &= ap - 1;
       if (!(((D | prev_ok) >> k) & 1u) || ((D >> (k + 1)) & 1u)) continue;
       const int q = p0 - 8 + k;
       const uint32_t b1 = S.win[q + 1];
       if (is_stmd(b1)) {
-        B0 |= 1u << (k + 1);
-        B1 |= 1u << (k + 2);
+        B0 |= 1ull << (k + 1);
+        B1 |= 1ull << (k + 2);
       } else if (!((D >> (k + 2)) & 1u) && is_suffix2(b1, S.win[q + 2])) {
-        B0 |= 1u << (k + 1);
-        B1 |= 1u << (k + 3);
+        B0 |= 1ull << (k + 1);
+        B1 |= 1ull << (k + 3);
       }
     }
     base = (base & ~B0) | B1;
   }
-  return ((U & ~O & base) >> 8) & 0xFFFFu;
+  return (uint32_t)((U & ~O & base) >> 8);
 }
 
-// Start bits of window positions [p0, p0 + 16), p0 a multiple of 16.
-__device__ uint32_t start_mask16(const SplitSmem& S, int p0) {
-  const uint32_t D = bits32_at(S.docbits, p0 - 8), O = bits32_at(S.outbits, p0 - 8);
-  if (((O >> 8) & 0xFFFFu) == 0xFFFFu) return 0;
-  // Six aligned window words: bytes p0 - 4 .. p0 + 19 (p0 is a multiple of 16).
+// Start bits of window positions [p0, p0 + 32), p0 a multiple of 16.
+template <class SS>
+__device__ uint32_t start_mask32(const SS& S, int p0) {
+  const uint64_t D = bits64_at(S.docbits, p0 - 8), O = bits64_at(S.outbits, p0 - 8);
+  if ((uint32_t)(O >> 8) == 0xFFFFFFFFu) return 0;
+  // Ten aligned window words: bytes p0 - 4 .. p0 + 35.
   const uint32_t* w32 = reinterpret_cast<const uint32_t*>(S.win + p0);
-  uint32_t w[6];
+  uint32_t w[10], any = 0;
 #pragma unroll
-  for (int m = 0; m < 6; ++m) w[m] = lds_u32(w32 - 1 + m);
-  if (!((w[0] | w[1] | w[2] | w[3] | w[4] | w[5]) & 0x80808080u)) {
-    // ASCII: every byte is a unit; masks for bytes p0 - 4 .. p0 + 19 land in
-    // bits 4..27.
-    uint32_t L = 0, N = 0, Sm = 0, SP = 0, AP = 0;
+  for (int m = 0; m < 10; ++m) {
+    w[m] = lds_u32(w32 - 1 + m);
+    any |= w[m];
+  }
+  if (!(any & 0x80808080u)) {
+    // ASCII: every byte is a unit; masks for bytes p0 - 4 .. p0 + 35 land in
+    // bits 4..43.
+    uint64_t L = 0, N = 0, Sm = 0, SP = 0, AP = 0;
 #pragma unroll
-    for (int m = 0; m < 6; ++m) {
+    for (int m = 0; m < 10; ++m) {
       const Ascii4 a = ascii_classes(w[m]);
       const uint32_t y = w[m] ^ 0x27272727u;
       const int sh = 4 + 4 * m;
-      L |= movemask4(a.L) << sh;
-      N |= movemask4(a.N) << sh;
-      Sm |= movemask4(a.S) << sh;
-      SP |= movemask4(a.SP) << sh;
-      AP |= movemask4(~(y + 0x7F7F7F7Fu) & 0x80808080u) << sh;
+      L |= (uint64_t)movemask4(a.L) << sh;
+      N |= (uint64_t)movemask4(a.N) << sh;
+      Sm |= (uint64_t)movemask4(a.S) << sh;
+      SP |= (uint64_t)movemask4(a.SP) << sh;
+      AP |= (uint64_t)movemask4(~(y + 0x7F7F7F7Fu) & 0x80808080u) << sh;
     }
-    return boundaries16(S, p0, 0xFFFFFFFFu, L, N, Sm, SP, AP, D, O);
+    return boundaries32(S, p0, ~0ull, L, N, Sm, SP, AP, D, O);
   }
-  // General: scan the UTF-8 units of bytes [p0 - 7, p0 + 17); each byte
+  // General: scan the UTF-8 units of bytes [p0 - 7, p0 + 33); each byte
   // carries its unit's class. Units starting before p0 - 8 may be misread
   // only up to p0 - 5, and nothing before p0 - 4 is used.
   const int base = p0 - 8;
-  uint32_t U = 0, Lm = 0, Nm = 0, Sm = 0, SPm = 0, APm = 0, MBS = 0;
+  uint64_t U = 0, Lm = 0, Nm = 0, Sm = 0, SPm = 0, APm = 0, MBS = 0;
   int rem = 0, cls = kO;
 #pragma unroll 4
-  for (int k = 1; k < 25; ++k) {
+  for (int k = 1; k < 41; ++k) {
     const int q = base + k;
     const uint32_t b = S.win[q];
-    const uint32_t bit = 1u << k;
+    const uint64_t bit = 1ull << k;
     if (D & bit) rem = 0;
     if (rem > 0) {
       --rem;
     } else {
       U |= bit;
-      const uint32_t dn = (D >> (k + 1)) & 7u;  // document edges at q + 1 .. q + 3
+      const uint32_t dn = (uint32_t)(D >> (k + 1)) & 7u;  // document edges at q + 1 .. q + 3
       const int hi = dn ? q + __ffs(dn) : q + 4;
       const int len = seq_len(S.win, hi, q);
       cls = unit_class(S.win, q, len);
       rem = (len > 1 ? len : 1) - 1;
       if (cls == kS && len > 1) MBS |= bit;
     }
-    Lm |= cls == kL ? bit : 0u;
-    Nm |= cls == kN ? bit : 0u;
-    Sm |= cls == kS ? bit : 0u;
-    SPm |= b == 0x20u ? bit : 0u;
-    APm |= b == 0x27u ? bit : 0u;
+    Lm |= cls == kL ? bit : 0ull;
+    Nm |= cls == kN ? bit : 0ull;
+    Sm |= cls == kS ? bit : 0ull;
+    SPm |= b == 0x20u ? bit : 0ull;
+    APm |= b == 0x27u ? bit : 0ull;
   }
-  uint32_t res = boundaries16(S, p0, U, Lm, Nm, Sm, SPm, APm, D, O);
+  uint32_t res = boundaries32(S, p0, U, Lm, Nm, Sm, SPm, APm, D, O);
   // Whitespace of several bytes (B2 looks past the whole unit): the per-byte
   // predicate.
-  uint32_t fix = (MBS >> 8) & 0xFFFFu;
+  uint32_t fix = (uint32_t)(MBS >> 8);
   while (fix) {
     const int k = __ffs(fix) - 1;
     fix &= fix - 1;
@@ -525,10 +549,11 @@ __device__ uint32_t start_mask16(const SplitSmem& S, int p0) {
 // Loads the window of chunk c: bytes [c0 - kHalo, c0 + kChunk + kMargin +
 // kHalo), the document edges that fall inside it, and which bytes lie outside
 // every document. first_doc = the first document starting at or after c0.
-__device__ void load_window(SplitSmem& S, const uint8_t* bytes, int64_t n_bytes, const int64_t* doc_offsets,
+template <class SS>
+__device__ void load_window(SS& S, const uint8_t* bytes, int64_t n_bytes, const int64_t* doc_offsets,
                             int64_t n_docs, int64_t c0, int64_t first_doc) {
   const int tid = threadIdx.x;
-  const int64_t w0 = c0 - kHalo, w_end = w0 + kWin;
+  const int64_t w0 = c0 - kHalo, w_end = w0 + SS::kLen;
   // Every load is issued before the first barrier: the bytes, the first and
   // last document offsets, and the offsets of the documents from 32 before
   // first_doc on (one per thread; more only when documents are tiny).
@@ -541,7 +566,7 @@ __device__ void load_window(SplitSmem& S, const uint8_t* bytes, int64_t n_bytes,
   // 16-byte loads and stores when the input is 16-byte aligned (window
   // offsets are multiples of 16), bytes otherwise.
   const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 15u) == 0;
-  for (int i = tid * 16; i < kWin; i += kThreads * 16) {
+  for (int i = tid * 16; i < SS::kLen; i += kThreads * 16) {
     const int64_t p = w0 + i;
     if (aligned && p >= 0 && p + 16 <= n_bytes) {
       *reinterpret_cast<uint4*>(S.win + i) = __ldg(reinterpret_cast<const uint4*>(bytes + p));
@@ -550,12 +575,12 @@ __device__ void load_window(SplitSmem& S, const uint8_t* bytes, int64_t n_bytes,
       for (int k = 0; k < 16; ++k) S.win[i + k] = (p + k >= 0 && p + k < n_bytes) ? bytes[p + k] : 0;
     }
   }
-  for (int i = tid; i < kWinWords + 2; i += kThreads) S.docbits[i] = 0;
+  for (int i = tid; i < SS::kWords + 2; i += kThreads) S.docbits[i] = 0;
   if (tid == kThreads - 1) S.more_docs = o_mine < w_end;
   cta_sync();
   d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
   d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
-  for (int wi = tid; wi < kWinWords + 2; wi += kThreads) {
+  for (int wi = tid; wi < SS::kWords + 2; wi += kThreads) {
     uint32_t word = 0;
     const int64_t p = w0 + (int64_t)wi * 32;
     if (p < d_first || p + 32 > d_last) {
@@ -630,13 +655,11 @@ __device__ void load_encode_window(SplitSmem& S, const uint8_t* bytes, int64_t n
   cta_sync();
 }
 
-// Start bits of the chunk, window indices [kHalo, kHalo + kChunk) (the encode
-// kernel takes the margin's from the next chunk's output).
-__device__ void compute_start_bits(SplitSmem& S) {
-  const int tid = threadIdx.x;
-  uint32_t m = start_mask16(S, kHalo + 16 * tid);
-  uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, m, 1);
-  if ((tid & 1) == 0) S.startbits[tid >> 1] = m | (hi << 16);
+// Start bits of the split kernel's chunk: thread t takes window positions
+// [kHalo + 32 t, + 32), one start bit word (the encode kernel takes its
+// margin's start bits from the next chunk's output).
+__device__ void compute_start_bits(SplitWin& S) {
+  S.startbits[threadIdx.x] = start_mask32(S, kHalo + 32 * (int)threadIdx.x);
   cta_sync();
 }
 
@@ -1468,15 +1491,16 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const uint32_t* 
   for (int64_t k = first_doc[c] + lane; k < k_hi; k += 32) out_offsets[k] += P;
 }
 
-// Pre-tokenizer alone: start bits of [c0, c0 + kChunk) for chunk blockIdx.x.
+// Pre-tokenizer alone: start bits of [c0, c0 + kSplitChunk) for chunk
+// blockIdx.x (first_doc, when given, is indexed by 4 KiB chunk).
 __global__ void __launch_bounds__(kThreads) k_pretokenize(const uint8_t* bytes, int64_t n_bytes,
                                                           const int64_t* doc_offsets, int64_t n_docs,
                                                           const int64_t* first_doc, uint32_t* out_bits) {
-  __shared__ SplitSmem S;
-  const int64_t c0 = (int64_t)blockIdx.x * kChunk;
+  __shared__ SplitWin S;
+  const int64_t c0 = (int64_t)blockIdx.x * kSplitChunk;
   int64_t k_first;
   if (first_doc) {
-    k_first = __ldg(first_doc + blockIdx.x);  // from k_prep
+    k_first = __ldg(first_doc + (int64_t)blockIdx.x * (kSplitChunk / kChunk));  // from k_prep
   } else {  // no k_prep: the first document at or after c0 by binary search
     if (threadIdx.x == 0) {
       int64_t lo = 0, hi = n_docs + 1;
@@ -1493,7 +1517,7 @@ __global__ void __launch_bounds__(kThreads) k_pretokenize(const uint8_t* bytes, 
   load_window(S, bytes, n_bytes, doc_offsets, n_docs, c0, k_first);
   compute_start_bits(S);
   const int64_t n_words = (n_bytes + 31) / 32;
-  for (int w = threadIdx.x; w < kChunk / 32; w += kThreads) {
+  for (int w = threadIdx.x; w < kSplitChunk / 32; w += kThreads) {
     const int64_t gw = c0 / 32 + w;
     if (gw < n_words) {
       uint32_t v = S.startbits[w];
@@ -1919,7 +1943,7 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
   a.out_offsets = d_out_offsets;
   if (ev_start) CK(cudaEventRecord(ev_start, st));
   if (n_bytes > 0) {
-    k_pretokenize<<<(unsigned)((n_bytes + kChunk - 1) / kChunk), kThreads, 0, st>>>(d_bytes, n_bytes, d_doc_offsets,
+    k_pretokenize<<<(unsigned)((n_bytes + kSplitChunk - 1) / kSplitChunk), kThreads, 0, st>>>(d_bytes, n_bytes, d_doc_offsets,
                                                                                    n_docs, w.first_doc, w.bits);
     CK(cudaGetLastError());
   }
@@ -2297,7 +2321,7 @@ int bpe_pretokenize_batch(const uint8_t* d_bytes, int64_t n_bytes, const int64_t
   if (!d_doc_offsets || n_bytes < 0 || n_docs < 0 || (n_bytes > 0 && (!d_bytes || !d_start_bits)))
     return fail(BPE_ERR_INVALID_ARG, "bpe_pretokenize_batch: bad arguments");
   if (n_bytes == 0) return BPE_OK;
-  const int64_t n_chunks = (n_bytes + kChunk - 1) / kChunk;
+  const int64_t n_chunks = (n_bytes + kSplitChunk - 1) / kSplitChunk;
   k_pretokenize<<<(unsigned)n_chunks, kThreads, 0, (cudaStream_t)stream>>>(d_bytes, n_bytes, d_doc_offsets,
                                                                                       n_docs, nullptr, d_start_bits);
   CK(cudaGetLastError());
