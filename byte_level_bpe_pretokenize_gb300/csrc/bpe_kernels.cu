@@ -79,6 +79,9 @@ constexpr int kShortMax = 64;         // longest pre-token merged by one thread
 constexpr int kCacheMaxLen = 16;      // longest pre-token looked up in the word cache
 constexpr int kCacheMaxIds = 3;       // most ids a cache entry holds
 constexpr int kProbeRound = 2;        // word-cache probes a thread has in flight
+constexpr uint32_t kMaxDefer = 160;   // cache misses per chunk handed to k_misses
+constexpr uint32_t kMissMark = 1u << 31;   // span_cnt: a cache miss, its byte length below
+constexpr uint16_t kDeferFlag = 0x8000;    // span_start: the miss goes to k_misses
 constexpr int kLongPerThread = 4;     // elements per thread per round of the CTA merge
 constexpr int kRound = kThreads * kLongPerThread;
 constexpr int kMaxLong = kChunk / kShortMax + 2;
@@ -145,6 +148,7 @@ struct DevSmall {
   uint32_t status;
   uint32_t rec_used;  // u32 words of long pre-token records handed out this call
   int64_t total;
+  uint32_t q_short, q_med;  // cache misses queued for k_misses (<= 16 bytes, longer)
 };
 
 
@@ -393,6 +397,7 @@ struct Smem : SplitSmem {
   uint32_t n_long;
   uint32_t n_miss;                   // queued misses of <= 16 bytes
   uint32_t n_miss_m;                 // queued misses of 17..kShortMax bytes
+  uint32_t q_base_s, q_base_m;       // the chunk's first entries in the k_misses queue
   int64_t last_end;                  // end of the chunk's last pre-token, -1 past the window
   int last_end_rel;                  // the same relative to the chunk start
   int64_t doc_lo, doc_hi;  // document of a long pre-token that runs past the window
@@ -1029,6 +1034,8 @@ __global__ void k_prep(const int64_t* doc_offsets, int64_t n_docs, int64_t n_byt
   if (t0 == 0) {
     small->rec_used = 0;
     small->total = 0;
+    small->q_short = 0;
+    small->q_med = 0;
     first_doc[n_chunks] = n_docs + 1;
   }
   for (int64_t c = t0; c < n_chunks; c += stride) {
@@ -1064,6 +1071,10 @@ struct EncodeArgs {
   uint64_t* chunk_meta;        // per chunk: token count | (record index + 1) << 32
   uint32_t* rec;               // long pre-token records
   uint64_t rec_cap;            // u32 words of rec
+  uint32_t* def_n;             // per chunk: cache misses handed to k_misses
+  uint32_t* def_rec;           // [n_chunks][kMaxDefer][3] their records
+  uint64_t* queue;             // (chunk << 8 | slot): short misses from the front, longer from the back
+  uint64_t queue_cap;
   const int64_t* first_doc;
   DevSmall* small;
   int64_t n_chunks;
@@ -1168,20 +1179,61 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
         if (cnt) {
           for (uint32_t q = 0; q < cnt; ++q) S.sym[st[h] + q] = ids[q];
           S.span_cnt[j] = cnt;
-        } else if (len[h] <= kCacheMaxLen) {
-          const uint32_t qs = atomicAdd(&S.n_miss, 1u);
-          if (qs < kMissShortCap) S.missq[qs] = (uint16_t)j;
-          else S.span_cnt[j] = merge_at(S, st[h], len[h], a.T);  // queue full: merge here
         } else {
-          const uint32_t qm = atomicAdd(&S.n_miss_m, 1u);
-          if (qm < kMissMedCap) S.missq[kMissShortCap + qm] = (uint16_t)j;
-          else S.span_cnt[j] = merge_at(S, st[h], len[h], a.T);
+          S.span_cnt[j] = kMissMark | (uint32_t)len[h];
         }
       } else {
         const uint32_t ql = atomicAdd(&S.n_long, 1u);
         if (ql < (uint32_t)kMaxLong) S.long_list[ql] = (uint16_t)j;
         else atomicOr(&a.small->status, kStInternal);
         S.span_cnt[j] = 0;
+      }
+    }
+  }
+  cta_sync();
+  // Cache misses. When the chunk's slots suffice they all go to k_misses:
+  // each keeps its byte length of ids reserved (ids never outnumber bytes),
+  // the chunk records it and moves on. Otherwise they are merged here by lane
+  // groups. Each thread owns a contiguous run of spans [run0, run1), in this
+  // and every later step.
+  const uint32_t per = (n_spans + kThreads - 1) / kThreads;
+  const uint32_t run0 = min(n_spans, tid * per), run1 = min(n_spans, run0 + per);
+  uint32_t def_before, def_total;  // packed: misses of <= 16 bytes | longer ones << 16
+  {
+    uint32_t mine = 0;
+    for (uint32_t j = run0; j < run1; ++j) {
+      const uint32_t v = S.span_cnt[j];
+      if (v & kMissMark) mine += (v & 0xFFu) <= (uint32_t)kCacheMaxLen ? 1u : 0x10000u;
+    }
+    def_before = block_excl_scan(mine, S.red, &def_total);
+  }
+  const uint32_t n_def = (def_total & 0xFFFFu) + (def_total >> 16);
+  const bool defer = a.queue != nullptr && n_def <= kMaxDefer;
+  if (defer) {
+    if (tid == 0 && n_def) {
+      S.q_base_s = atomicAdd(&a.small->q_short, def_total & 0xFFFFu);
+      S.q_base_m = atomicAdd(&a.small->q_med, def_total >> 16);
+    }
+    for (uint32_t j = run0; j < run1; ++j) {
+      const uint32_t v = S.span_cnt[j];
+      if (v & kMissMark) {
+        S.span_start[j] |= kDeferFlag;
+        S.span_cnt[j] = v & 0xFFu;  // reserved
+      }
+    }
+  } else {
+    for (uint32_t j = run0; j < run1; ++j) {
+      const uint32_t v = S.span_cnt[j];
+      if (!(v & kMissMark)) continue;
+      const int len = (int)(v & 0xFFu), st = S.span_start[j];
+      if (len <= kCacheMaxLen) {
+        const uint32_t qs = atomicAdd(&S.n_miss, 1u);
+        if (qs < kMissShortCap) S.missq[qs] = (uint16_t)j;
+        else S.span_cnt[j] = merge_at(S, st, len, a.T);  // queue full: merge here
+      } else {
+        const uint32_t qm = atomicAdd(&S.n_miss_m, 1u);
+        if (qm < kMissMedCap) S.missq[kMissShortCap + qm] = (uint16_t)j;
+        else S.span_cnt[j] = merge_at(S, st, len, a.T);
       }
     }
   }
@@ -1198,7 +1250,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
       if (q < n_short) {
         j = S.missq[q];
         st = S.span_start[j];
-        n = (uint32_t)(((j + 1 < n_spans) ? (int)S.span_start[j + 1] : last_end) - st);
+        n = (uint32_t)(((j + 1 < n_spans) ? (int)(S.span_start[j + 1] & ~kDeferFlag) : last_end) - st);
       }
       const uint32_t cnt = merge_group<8>(W, S.win + kHalo + st, n, a.T, S.byte_id, S.sym + st);
       if (q < n_short && (tid & 7) == 0) S.span_cnt[j] = cnt;
@@ -1210,7 +1262,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
       if (q < n_med) {
         j = S.missq[kMissShortCap + q];
         st = S.span_start[j];
-        n = (uint32_t)(((j + 1 < n_spans) ? (int)S.span_start[j + 1] : last_end) - st);
+        n = (uint32_t)(((j + 1 < n_spans) ? (int)(S.span_start[j + 1] & ~kDeferFlag) : last_end) - st);
       }
       const uint32_t cnt = merge_group<32>(W, S.win + kHalo + st, n, a.T, S.byte_id, S.sym + st);
       if (q < n_med && (tid & 31) == 0) S.span_cnt[j] = cnt;
@@ -1236,8 +1288,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
     LongScratch L{S.u.stage, S.red, S.carry};
     for (uint32_t x = 0; x < n_long; ++x) {
       const uint32_t j = S.long_list[x];
-      const int64_t s = c0 + S.span_start[j];
-      int64_t e = (j + 1 < n_spans) ? c0 + S.span_start[j + 1] : S.last_end;
+      const int64_t s = c0 + (S.span_start[j] & ~kDeferFlag);
+      int64_t e = (j + 1 < n_spans) ? c0 + (S.span_start[j + 1] & ~kDeferFlag) : S.last_end;
       if (e < 0) {
         // Runs past the window: find the document it lies in, then the next
         // pre-token start after the window.
@@ -1289,8 +1341,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
   // Each thread scans a contiguous run of spans [run0, run1); it also stores
   // their ids at the end, so consecutive threads write consecutive ranges.
   uint32_t agg = 0;
-  const uint32_t per = (n_spans + kThreads - 1) / kThreads;
-  const uint32_t run0 = min(n_spans, tid * per), run1 = min(n_spans, run0 + per);
   {
     uint32_t sum = 0;
     for (uint32_t j = run0; j < run1; ++j) sum += S.span_cnt[j];
@@ -1315,7 +1365,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
         a.rec[r] = n_long;
         for (uint32_t x = 0; x < n_long; ++x) {
           const uint32_t j = S.long_list[x];
-          const uint64_t s = (uint64_t)(c0 + S.span_start[j]);
+          const uint64_t s = (uint64_t)(c0 + (S.span_start[j] & ~kDeferFlag));
           uint32_t* e = a.rec + r + 1 + 4 * x;
           e[0] = S.span_cnt[j];
           e[1] = (uint32_t)s;
@@ -1328,12 +1378,17 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
       }
     }
     a.chunk_meta[c] = meta;
+    if (a.def_n) a.def_n[c] = defer ? n_def : 0u;
   }
 
   // Ids of short pre-tokens to the chunk's stage region, each thread its own
-  // run, in output order without the long pre-tokens' ids.
+  // run, in output order without the long pre-tokens' ids. A deferred miss
+  // leaves its reserved range to k_misses and gets a record
+  // {offset in the chunk, start | reserved << 12 | stage offset << 19, ids}
+  // in slot order (= span order) and a queue entry.
   {
     uint32_t* stage = a.stage + c * kStage;
+    uint32_t ds = def_before & 0xFFFFu, dm = def_before >> 16;
     for (uint32_t j = run0; j < run1; ++j) {
       bool is_long = false;
       uint32_t long_before = 0;
@@ -1343,8 +1398,20 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
         if (lj < j) long_before += S.span_cnt[lj + 1] - S.span_cnt[lj];
       }
       if (is_long) continue;
-      const int st = S.span_start[j];
+      const uint32_t raw = S.span_start[j];
+      const int st = (int)(raw & ~(uint32_t)kDeferFlag);
       const uint32_t o = S.span_cnt[j] - long_before, cnt = S.span_cnt[j + 1] - S.span_cnt[j];
+      if (raw & kDeferFlag) {
+        const uint32_t slot = ds + dm;
+        uint32_t* R = a.def_rec + ((uint64_t)c * kMaxDefer + slot) * 3;
+        R[0] = S.span_cnt[j];
+        R[1] = (uint32_t)st | cnt << 12 | o << 19;
+        R[2] = cnt;
+        const uint64_t e = (uint64_t)c << 8 | slot;
+        if (cnt <= (uint32_t)kCacheMaxLen) a.queue[S.q_base_s + ds++] = e;
+        else a.queue[a.queue_cap - 1 - (S.q_base_m + dm++)] = e;
+        continue;
+      }
       for (uint32_t q = 0; q < cnt; ++q) stage[o + q] = S.sym[st + q];
     }
   }
@@ -1364,6 +1431,68 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
         a.out_offsets[k] = S.span_cnt[S.grp_pos[t] + __popc(gbits)];
       }
       if (!more) break;
+    }
+  }
+}
+
+// Cache misses that k_encode handed over, merged across the whole GPU: a
+// queue entry (chunk << 8 | slot) names a record {offset, start | reserved <<
+// 12 | stage offset << 19, ids}. Misses of up to 16 bytes go to groups of 8
+// lanes, longer ones to a warp (merge_group). Each writes its ids into its
+// reserved stage range, the count into its record, and gives the unused part
+// of the reservation back to the chunk's count.
+__global__ void __launch_bounds__(kThreads) k_misses(const uint8_t* bytes, const uint64_t* queue, uint64_t queue_cap,
+                                                     const DevSmall* small, uint32_t* def_rec, uint32_t* stage,
+                                                     uint64_t* chunk_meta, Tables T) {
+  __shared__ GroupScratch grp[kThreads / 32];
+  __shared__ int32_t byte_id[256];
+  for (int i = threadIdx.x; i < 256; i += kThreads) byte_id[i] = T.byte_id[i];
+  __syncthreads();
+  const uint32_t n_short = small->q_short, n_med = small->q_med;
+  const int lane = threadIdx.x & 31;
+  GroupScratch& W = grp[threadIdx.x >> 5];
+  auto run = [&](uint64_t e, bool on, auto merge) {
+    const uint64_t c = e >> 8;
+    uint32_t* R = def_rec + (c * kMaxDefer + (e & 0xFFu)) * 3;
+    const uint32_t w = on ? R[1] : 0u;
+    const uint32_t st = w & 0xFFFu, n = on ? (w >> 12) & 0x7Fu : 0u, so = w >> 19;
+    const uint32_t cnt = merge(W, bytes + c * kChunk + st, n, stage + c * kStage + so);
+    return cnt;
+  };
+  {
+    const uint64_t groups = (uint64_t)gridDim.x * (kThreads / 8), g = (uint64_t)blockIdx.x * (kThreads / 8) + (threadIdx.x >> 3);
+    for (uint64_t q0 = 0; q0 < n_short; q0 += groups) {
+      const uint64_t q = q0 + g;
+      const bool on = q < n_short;
+      const uint64_t e = on ? queue[q] : 0;
+      const uint32_t cnt = run(e, on, [&](GroupScratch& G, const uint8_t* src, uint32_t n, uint32_t* out) {
+        return merge_group<8>(G, src, n, T, byte_id, out);
+      });
+      if (on && (lane & 7) == 0) {
+        const uint64_t c = e >> 8;
+        uint32_t* R = def_rec + (c * kMaxDefer + (e & 0xFFu)) * 3;
+        const uint32_t reserved = (R[1] >> 12) & 0x7Fu;
+        R[2] = cnt;
+        atomicAdd(reinterpret_cast<unsigned long long*>(chunk_meta + c), 0ull - (unsigned long long)(reserved - cnt));
+      }
+    }
+  }
+  {
+    const uint64_t warps = (uint64_t)gridDim.x * (kThreads / 32), wi = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    for (uint64_t q0 = 0; q0 < n_med; q0 += warps) {
+      const uint64_t q = q0 + wi;
+      const bool on = q < n_med;
+      const uint64_t e = on ? queue[queue_cap - 1 - q] : 0;
+      const uint32_t cnt = run(e, on, [&](GroupScratch& G, const uint8_t* src, uint32_t n, uint32_t* out) {
+        return merge_group<32>(G, src, n, T, byte_id, out);
+      });
+      if (on && lane == 0) {
+        const uint64_t c = e >> 8;
+        uint32_t* R = def_rec + (c * kMaxDefer + (e & 0xFFu)) * 3;
+        const uint32_t reserved = (R[1] >> 12) & 0x7Fu;
+        R[2] = cnt;
+        atomicAdd(reinterpret_cast<unsigned long long*>(chunk_meta + c), 0ull - (unsigned long long)(reserved - cnt));
+      }
     }
   }
 }
@@ -1436,6 +1565,7 @@ constexpr int kCompactWarps = 8;
 __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const uint32_t* stage, const int32_t* pool,
                                                                 const uint64_t* chunk_meta, const uint64_t* chunk_off,
                                                                 const uint64_t* tile_off, const uint32_t* rec,
+                                                                const uint32_t* def_n, const uint32_t* def_rec,
                                                                 const int64_t* first_doc, int64_t n_chunks,
                                                                 int64_t n_docs, int32_t* out_ids, int64_t out_capacity,
                                                                 int64_t* out_offsets, DevSmall* small) {
@@ -1449,7 +1579,44 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const uint32_t* 
   const uint32_t* src = stage + c * kStage;
   if (lane == 0 && P + (int64_t)cnt > out_capacity) atomicOr(&small->status, kStCapacity);
   const int64_t lim = out_capacity - P;
-  if (r1 == 0) {
+  const uint32_t nd = def_n ? def_n[c] : 0u;
+  const uint32_t* D = def_rec + (uint64_t)c * kMaxDefer * 3;
+  if (nd > 0) {
+    // Deferred misses: output position q maps to u in the chunk's reserved
+    // layout by adding the unused reservations of the misses before it
+    // (records in span order), then to the pool (long pre-tokens) or the
+    // stage (everything else, long pre-tokens' ids left out).
+    const uint32_t* R = r1 ? rec + (r1 - 1) : nullptr;
+    const uint32_t n_long = R ? R[0] : 0u;
+    uint32_t d = 0, gap = 0;  // per lane: misses passed and their unused ids
+    for (uint32_t q = lane; q < cnt; q += 32) {
+      if ((int64_t)q >= lim) break;
+      while (d < nd) {
+        const uint32_t U = D[3 * d], res = (D[3 * d + 1] >> 12) & 0x7Fu, used = D[3 * d + 2];
+        if (q + gap < U + used) break;
+        gap += res - used;
+        ++d;
+      }
+      const uint32_t u = q + gap;
+      uint32_t shift = 0;
+      int32_t v = 0;
+      bool from_long = false;
+      for (uint32_t x = 0; x < n_long; ++x) {
+        const uint32_t off = R[1 + 4 * x], lc = R[4 + 4 * x];
+        if (u >= off + lc) {
+          shift += lc;
+        } else {
+          if (u >= off) {
+            const uint64_t sp = (uint64_t)R[2 + 4 * x] | ((uint64_t)R[3 + 4 * x] << 32);
+            v = pool[sp + (u - off)];
+            from_long = true;
+          }
+          break;
+        }
+      }
+      out_ids[P + q] = from_long ? v : (int32_t)src[u - shift];
+    }
+  } else if (r1 == 0) {
     for (uint32_t q0 = 0; q0 < cnt; q0 += 128) {  // four loads in flight per lane
       uint32_t v[4];
 #pragma unroll
@@ -1488,7 +1655,17 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const uint32_t* 
     }
   }
   const int64_t k_hi = first_doc[c + 1] < n_docs + 1 ? first_doc[c + 1] : n_docs + 1;
-  for (int64_t k = first_doc[c] + lane; k < k_hi; k += 32) out_offsets[k] += P;
+  for (int64_t k = first_doc[c] + lane; k < k_hi; k += 32) {
+    // k_encode wrote the offset in the reserved layout: take back the unused
+    // reservations of the misses before it
+    const int64_t o = out_offsets[k];
+    int64_t fix = 0;
+    for (uint32_t d = 0; d < nd; ++d) {
+      if ((int64_t)D[3 * d] >= o) break;
+      fix += (int64_t)((D[3 * d + 1] >> 12) & 0x7Fu) - (int64_t)D[3 * d + 2];
+    }
+    out_offsets[k] = o - fix + P;
+  }
 }
 
 // Pre-tokenizer alone: start bits of [c0, c0 + kSplitChunk) for chunk
@@ -1820,7 +1997,7 @@ namespace {
 constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsSizes {
-  size_t first_doc, chunk_meta, chunk_off, tile_off, rec, bits, stage, pool, total;
+  size_t first_doc, chunk_meta, chunk_off, tile_off, rec, def_n, def_rec, queue, bits, stage, pool, total;
   uint64_t rec_cap;  // u32 words: a header per chunk and 4 words per long pre-token
 };
 
@@ -1833,10 +2010,14 @@ constexpr WsSizes ws_sizes(int64_t n_bytes) {
   z.chunk_off = align256((size_t)n_chunks * sizeof(uint64_t));
   z.tile_off = align256((size_t)(n_chunks / kScanThreads + 1) * sizeof(uint64_t));
   z.rec = align256((size_t)z.rec_cap * sizeof(uint32_t));
+  z.def_n = align256((size_t)n_chunks * sizeof(uint32_t));
+  z.def_rec = align256((size_t)n_chunks * kMaxDefer * 3 * sizeof(uint32_t));
+  z.queue = align256((size_t)n_chunks * kMaxDefer * sizeof(uint64_t));
   z.bits = align256((size_t)(n_words + 4) * sizeof(uint32_t));
   z.stage = align256((size_t)n_chunks * kStage * sizeof(uint32_t));
   z.pool = align256((size_t)(n_bytes + 4) * sizeof(int32_t));
-  z.total = z.first_doc + z.chunk_meta + z.chunk_off + z.tile_off + z.rec + z.bits + z.stage + z.pool;
+  z.total = z.first_doc + z.chunk_meta + z.chunk_off + z.tile_off + z.rec + z.def_n + z.def_rec + z.queue + z.bits +
+            z.stage + z.pool;
   return z;
 }
 
@@ -1847,6 +2028,10 @@ struct Ws {
   uint64_t* tile_off;
   uint32_t* rec;
   uint64_t rec_cap;
+  uint32_t* def_n;
+  uint32_t* def_rec;
+  uint64_t* queue;
+  uint64_t queue_cap;
   uint32_t* bits;
   uint32_t* stage;
   int32_t* pool;
@@ -1866,6 +2051,13 @@ Ws ws_carve(unsigned char* base, int64_t n_bytes) {
   w.rec = reinterpret_cast<uint32_t*>(base);
   w.rec_cap = z.rec_cap;
   base += z.rec;
+  w.def_n = reinterpret_cast<uint32_t*>(base);
+  base += z.def_n;
+  w.def_rec = reinterpret_cast<uint32_t*>(base);
+  base += z.def_rec;
+  w.queue = reinterpret_cast<uint64_t*>(base);
+  w.queue_cap = (uint64_t)(n_bytes / kChunk + 1) * kMaxDefer;
+  base += z.queue;
   w.bits = reinterpret_cast<uint32_t*>(base);
   base += z.bits;
   w.stage = reinterpret_cast<uint32_t*>(base);
@@ -1888,7 +2080,7 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
 namespace {
 constexpr int64_t kNoAllocMaxBytes = int64_t(4) << 20;
 constexpr size_t kNoAllocScratchBytes = ws_sizes(kNoAllocMaxBytes).total;
-static_assert(kNoAllocScratchBytes < (size_t(36) << 20), "the fixed scratch stays below 36 MiB");
+static_assert(kNoAllocScratchBytes < (size_t(40) << 20), "the fixed scratch stays below 40 MiB");
 }  // namespace
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -1937,6 +2129,10 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
   a.chunk_meta = w.chunk_meta;
   a.rec = w.rec;
   a.rec_cap = w.rec_cap;
+  a.def_n = w.def_n;
+  a.def_rec = w.def_rec;
+  a.queue = w.queue;
+  a.queue_cap = w.queue_cap;
   a.first_doc = w.first_doc;
   a.small = h->d_small;
   a.n_chunks = n_chunks;
@@ -1949,14 +2145,17 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
   }
   k_encode<<<(unsigned)n_chunks, kThreads, sizeof(Smem), st>>>(a);
   CK(cudaGetLastError());
+  k_misses<<<(unsigned)std::min<int64_t>(8 * 152, n_chunks), kThreads, 0, st>>>(d_bytes, w.queue, w.queue_cap, h->d_small,
+                                                                            w.def_rec, w.stage, w.chunk_meta, a.T);
+  CK(cudaGetLastError());
   const int64_t n_tiles = (n_chunks + kScanThreads - 1) / kScanThreads;
   k_scan_tiles<<<(unsigned)n_tiles, kScanThreads, 0, st>>>(w.chunk_meta, n_chunks, w.chunk_off, w.tile_off);
   CK(cudaGetLastError());
   k_scan_tile_sums<<<1, kScanThreads, 0, st>>>(w.tile_off, n_tiles, h->d_small);
   CK(cudaGetLastError());
   k_compact<<<(unsigned)((n_chunks + kCompactWarps - 1) / kCompactWarps), 32 * kCompactWarps, 0, st>>>(
-      w.stage, w.pool, w.chunk_meta, w.chunk_off, w.tile_off, w.rec, w.first_doc, n_chunks, n_docs, d_out_ids,
-      out_capacity, d_out_offsets, h->d_small);
+      w.stage, w.pool, w.chunk_meta, w.chunk_off, w.tile_off, w.rec, w.def_n, w.def_rec, w.first_doc, n_chunks, n_docs,
+      d_out_ids, out_capacity, d_out_offsets, h->d_small);
   CK(cudaGetLastError());
   if (ev_stop) CK(cudaEventRecord(ev_stop, st));
   return BPE_OK;
