@@ -362,7 +362,7 @@ def run_gpu(args, world, rank, local):
             "without_word_cache": {"value": round(n_bytes / (nocache_ms / 1e3) / 1e6, 3), "unit": "MB/s",
                                    "ms_per_step": round(nocache_ms, 4),
                                    "hbm_frac": round(alg / (nocache_ms / 1e3) / 1e9 / peak, 4)},
-            "gpu_launches": 6 * args.steps,
+            "gpu_launches": 7 * args.steps,
             "clocks": clk,
         }
         print(json.dumps(out), flush=True)

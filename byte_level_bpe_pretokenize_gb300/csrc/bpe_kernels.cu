@@ -803,7 +803,7 @@ __device__ int merge_short(uint32_t* sym, uint32_t* rk, const uint8_t* src, int 
 template <int G>
 __device__ uint32_t merge_group(GroupScratch& W, const uint8_t* src, uint32_t n, const Tables& T,
                                 const int32_t* byte_id, uint32_t* out) {
-  static_assert(G == 8 || G == 32, "group of 8 or 32 lanes");
+  static_assert(G == 4 || G == 8 || G == 32, "group of 4, 8 or 32 lanes");
   const int lane = threadIdx.x & 31;
   const int g = lane & (G - 1);
   const int goff = lane & ~(G - 1);
@@ -1441,7 +1441,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
 // lanes, longer ones to a warp (merge_group). Each writes its ids into its
 // reserved stage range, the count into its record, and gives the unused part
 // of the reservation back to the chunk's count.
-__global__ void __launch_bounds__(kThreads) k_misses(const uint8_t* bytes, const uint64_t* queue, uint64_t queue_cap,
+constexpr int kMissBlocksPerSm = 6;  // resident at once (40 registers a thread)
+__global__ void __launch_bounds__(kThreads, kMissBlocksPerSm) k_misses(const uint8_t* bytes, const uint64_t* queue, uint64_t queue_cap,
                                                      const DevSmall* small, uint32_t* def_rec, uint32_t* stage,
                                                      uint64_t* chunk_meta, Tables T) {
   __shared__ GroupScratch grp[kThreads / 32];
@@ -1459,12 +1460,33 @@ __global__ void __launch_bounds__(kThreads) k_misses(const uint8_t* bytes, const
     const uint32_t cnt = merge(W, bytes + c * kChunk + st, n, stage + c * kStage + so);
     return cnt;
   };
+  // Misses of up to 16 bytes: those of up to 8 by groups of 4 lanes in a
+  // first pass, the others by groups of 8 in a second (each pass skips the
+  // other's entries).
+  {
+    const uint64_t groups = (uint64_t)gridDim.x * (kThreads / 4), g = (uint64_t)blockIdx.x * (kThreads / 4) + (threadIdx.x >> 2);
+    for (uint64_t q0 = 0; q0 < n_short; q0 += groups) {
+      const uint64_t q = q0 + g;
+      uint64_t e = q < n_short ? queue[q] : 0;
+      const bool on = q < n_short && ((def_rec[((e >> 8) * kMaxDefer + (e & 0xFFu)) * 3 + 1] >> 12) & 0x7Fu) <= 8u;
+      const uint32_t cnt = run(e, on, [&](GroupScratch& G, const uint8_t* src, uint32_t n, uint32_t* out) {
+        return merge_group<4>(G, src, n, T, byte_id, out);
+      });
+      if (on && (lane & 3) == 0) {
+        const uint64_t c = e >> 8;
+        uint32_t* R = def_rec + (c * kMaxDefer + (e & 0xFFu)) * 3;
+        const uint32_t reserved = (R[1] >> 12) & 0x7Fu;
+        R[2] = cnt;
+        atomicAdd(reinterpret_cast<unsigned long long*>(chunk_meta + c), 0ull - (unsigned long long)(reserved - cnt));
+      }
+    }
+  }
   {
     const uint64_t groups = (uint64_t)gridDim.x * (kThreads / 8), g = (uint64_t)blockIdx.x * (kThreads / 8) + (threadIdx.x >> 3);
     for (uint64_t q0 = 0; q0 < n_short; q0 += groups) {
       const uint64_t q = q0 + g;
-      const bool on = q < n_short;
-      const uint64_t e = on ? queue[q] : 0;
+      uint64_t e = q < n_short ? queue[q] : 0;
+      const bool on = q < n_short && ((def_rec[((e >> 8) * kMaxDefer + (e & 0xFFu)) * 3 + 1] >> 12) & 0x7Fu) > 8u;
       const uint32_t cnt = run(e, on, [&](GroupScratch& G, const uint8_t* src, uint32_t n, uint32_t* out) {
         return merge_group<8>(G, src, n, T, byte_id, out);
       });
@@ -1581,14 +1603,80 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const uint32_t* 
   const int64_t lim = out_capacity - P;
   const uint32_t nd = def_n ? def_n[c] : 0u;
   const uint32_t* D = def_rec + (uint64_t)c * kMaxDefer * 3;
-  if (nd > 0) {
-    // Deferred misses: output position q maps to u in the chunk's reserved
-    // layout by adding the unused reservations of the misses before it
-    // (records in span order), then to the pool (long pre-tokens) or the
-    // stage (everything else, long pre-tokens' ids left out).
-    const uint32_t* R = r1 ? rec + (r1 - 1) : nullptr;
-    const uint32_t n_long = R ? R[0] : 0u;
-    uint32_t d = 0, gap = 0;  // per lane: misses passed and their unused ids
+  // Deferred misses left holes in the chunk's ids (reserved ids they did not
+  // use). Output position q is reserved-layout position q + gap(q), gap(q)
+  // the holes before it. Miss d's ids end at output position
+  // E_d = U_d + used_d - (holes of the misses before d), strictly increasing
+  // in d, and gap(q) is the holes of the misses with E_d <= q. For up to 32
+  // misses lane d holds E_d and the inclusive sum of holes (Gi); with more,
+  // each lane walks the records.
+  const bool in_lanes = nd <= 32;
+  uint32_t E = 0xFFFFFFFFu, Gi = 0, Ud = 0xFFFFFFFFu;
+  if (in_lanes) {
+    uint32_t hole = 0;
+    if ((uint32_t)lane < nd) {
+      Ud = D[3 * lane];
+      const uint32_t used = D[3 * lane + 2];
+      hole = ((D[3 * lane + 1] >> 12) & 0x7Fu) - used;
+      E = Ud + used;
+    }
+    Gi = hole;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, Gi, o);
+      if (lane >= o) Gi += t;
+    }
+    if ((uint32_t)lane < nd) E -= Gi - hole;
+  }
+  // gap for q = base + lane (all lanes together; in_lanes only)
+  auto gap_at = [&](uint32_t base) -> uint32_t {
+    const uint32_t rel = E - base;
+    const uint32_t win = __reduce_or_sync(0xFFFFFFFFu, rel < 32u ? 1u << rel : 0u);
+    const uint32_t j = __popc(__ballot_sync(0xFFFFFFFFu, E < base)) + __popc(win & ((2u << lane) - 1u));
+    const uint32_t g = __shfl_sync(0xFFFFFFFFu, Gi, (int)(j ? j - 1 : 0));
+    return j ? g : 0u;
+  };
+  const uint32_t* R = r1 ? rec + (r1 - 1) : nullptr;
+  const uint32_t n_long = R ? R[0] : 0u;
+  // reserved-layout position u to the id (pool for long pre-tokens, else the
+  // stage without the long pre-tokens' ids)
+  auto id_at = [&](uint32_t u) -> int32_t {
+    uint32_t shift = 0;
+    for (uint32_t x = 0; x < n_long; ++x) {
+      const uint32_t off = R[1 + 4 * x], lc = R[4 + 4 * x];
+      if (u < off) break;
+      if (u < off + lc) {
+        const uint64_t sp = (uint64_t)R[2 + 4 * x] | ((uint64_t)R[3 + 4 * x] << 32);
+        return pool[sp + (u - off)];
+      }
+      shift += lc;
+    }
+    return (int32_t)src[u - shift];
+  };
+  if (in_lanes && r1 == 0) {
+    constexpr int kUnroll = 8;  // loads in flight per lane
+    for (uint32_t q0 = 0; q0 < cnt; q0 += 32 * kUnroll) {
+      uint32_t v[kUnroll];
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) {
+        const uint32_t base = q0 + 32 * k, q = base + lane;
+        const uint32_t gap = nd ? gap_at(base) : 0u;
+        v[k] = q < cnt ? src[q + gap] : 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) {
+        const uint32_t q = q0 + 32 * k + lane;
+        if (q < cnt && (int64_t)q < lim) out_ids[P + q] = (int32_t)v[k];
+      }
+    }
+  } else if (in_lanes) {
+    for (uint32_t q0 = 0; q0 < cnt; q0 += 32) {
+      const uint32_t q = q0 + lane;
+      const uint32_t gap = nd ? gap_at(q0) : 0u;
+      if (q < cnt && (int64_t)q < lim) out_ids[P + q] = id_at(q + gap);
+    }
+  } else {
+    uint32_t d = 0, gap = 0;  // per lane: misses passed and their holes
     for (uint32_t q = lane; q < cnt; q += 32) {
       if ((int64_t)q >= lim) break;
       while (d < nd) {
@@ -1597,74 +1685,35 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const uint32_t* 
         gap += res - used;
         ++d;
       }
-      const uint32_t u = q + gap;
-      uint32_t shift = 0;
-      int32_t v = 0;
-      bool from_long = false;
-      for (uint32_t x = 0; x < n_long; ++x) {
-        const uint32_t off = R[1 + 4 * x], lc = R[4 + 4 * x];
-        if (u >= off + lc) {
-          shift += lc;
-        } else {
-          if (u >= off) {
-            const uint64_t sp = (uint64_t)R[2 + 4 * x] | ((uint64_t)R[3 + 4 * x] << 32);
-            v = pool[sp + (u - off)];
-            from_long = true;
-          }
-          break;
-        }
-      }
-      out_ids[P + q] = from_long ? v : (int32_t)src[u - shift];
-    }
-  } else if (r1 == 0) {
-    for (uint32_t q0 = 0; q0 < cnt; q0 += 128) {  // four loads in flight per lane
-      uint32_t v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t q = q0 + 32 * u + lane;
-        v[u] = q < cnt ? src[q] : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t q = q0 + 32 * u + lane;
-        if (q < cnt && (int64_t)q < lim) out_ids[P + q] = (int32_t)v[u];
-      }
-    }
-  } else {
-    const uint32_t* R = rec + (r1 - 1);
-    const uint32_t n_long = R[0];
-    for (uint32_t q = lane; q < cnt; q += 32) {
-      if ((int64_t)q >= lim) break;
-      uint32_t shift = 0;
-      int32_t v = 0;
-      bool from_long = false;
-      for (uint32_t x = 0; x < n_long; ++x) {
-        const uint32_t off = R[1 + 4 * x], lc = R[4 + 4 * x];
-        if (q >= off + lc) {
-          shift += lc;
-        } else {
-          if (q >= off) {
-            const uint64_t s = (uint64_t)R[2 + 4 * x] | ((uint64_t)R[3 + 4 * x] << 32);
-            v = pool[s + (q - off)];
-            from_long = true;
-          }
-          break;
-        }
-      }
-      out_ids[P + q] = from_long ? v : (int32_t)src[q - shift];
+      out_ids[P + q] = id_at(q + gap);
     }
   }
+  // Document offsets: k_encode wrote them in the reserved layout; take back
+  // the holes of the misses that start before each (U_d is increasing: a
+  // search over the lanes, or a walk over the records).
+  const int64_t k_lo = first_doc[c];
   const int64_t k_hi = first_doc[c + 1] < n_docs + 1 ? first_doc[c + 1] : n_docs + 1;
-  for (int64_t k = first_doc[c] + lane; k < k_hi; k += 32) {
-    // k_encode wrote the offset in the reserved layout: take back the unused
-    // reservations of the misses before it
-    const int64_t o = out_offsets[k];
+  for (int64_t k0 = k_lo; k0 < k_hi; k0 += 32) {
+    const int64_t k = k0 + lane;
+    const int64_t o = k < k_hi ? out_offsets[k] : 0;
     int64_t fix = 0;
-    for (uint32_t d = 0; d < nd; ++d) {
-      if ((int64_t)D[3 * d] >= o) break;
-      fix += (int64_t)((D[3 * d + 1] >> 12) & 0x7Fu) - (int64_t)D[3 * d + 2];
+    if (in_lanes) {
+      uint32_t j = 0;  // misses with U_d < o: first among lanes 0..30, then lane 31
+#pragma unroll
+      for (uint32_t step = 16; step > 0; step >>= 1) {
+        const uint32_t u = __shfl_sync(0xFFFFFFFFu, Ud, (int)(j + step - 1));
+        if ((int64_t)u < o) j += step;
+      }
+      if ((int64_t)__shfl_sync(0xFFFFFFFFu, Ud, (int)j) < o) ++j;
+      const uint32_t g = __shfl_sync(0xFFFFFFFFu, Gi, (int)(j ? j - 1 : 0));
+      fix = j ? g : 0;
+    } else {
+      for (uint32_t d = 0; d < nd; ++d) {
+        if ((int64_t)D[3 * d] >= o) break;
+        fix += (int64_t)((D[3 * d + 1] >> 12) & 0x7Fu) - (int64_t)D[3 * d + 2];
+      }
     }
-    out_offsets[k] = o - fix + P;
+    if (k < k_hi) out_offsets[k] = o - fix + P;
   }
 }
 
@@ -1848,6 +1897,7 @@ struct DeviceGuard {
 
 struct bpe_handle {
   int device = 0;
+  int n_sms = 1;  // multiprocessors of the device (grids of persistent kernels)
   int64_t n_merges = 0, n_vocab = 0;
   uint4* d_ht = nullptr;
   uint32_t hmask = 0;
@@ -2145,8 +2195,9 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
   }
   k_encode<<<(unsigned)n_chunks, kThreads, sizeof(Smem), st>>>(a);
   CK(cudaGetLastError());
-  k_misses<<<(unsigned)std::min<int64_t>(8 * 152, n_chunks), kThreads, 0, st>>>(d_bytes, w.queue, w.queue_cap, h->d_small,
-                                                                            w.def_rec, w.stage, w.chunk_meta, a.T);
+  const unsigned miss_grid = (unsigned)std::min<int64_t>((int64_t)kMissBlocksPerSm * h->n_sms, n_chunks);
+  k_misses<<<miss_grid, kThreads, 0, st>>>(d_bytes, w.queue, w.queue_cap, h->d_small,
+                                      w.def_rec, w.stage, w.chunk_meta, a.T);
   CK(cudaGetLastError());
   const int64_t n_tiles = (n_chunks + kScanThreads - 1) / kScanThreads;
   k_scan_tiles<<<(unsigned)n_tiles, kScanThreads, 0, st>>>(w.chunk_meta, n_chunks, w.chunk_off, w.tile_off);
@@ -2241,6 +2292,7 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
     cudaError_t e_ = (call);                                     \
     if (e_ != cudaSuccess) return cleanup(cuda_fail(e_, #call)); \
   } while (0)
+  CKB(cudaDeviceGetAttribute(&h->n_sms, cudaDevAttrMultiProcessorCount, device));
   CKB(cudaMalloc(&h->d_ht, ht.size() * sizeof(uint4)));
   CKB(cudaMemcpy(h->d_ht, ht.data(), ht.size() * sizeof(uint4), cudaMemcpyHostToDevice));
   CKB(cudaMalloc(&h->d_mrows, (size_t)std::max<int64_t>(1, n_merges) * 3 * sizeof(int32_t)));
