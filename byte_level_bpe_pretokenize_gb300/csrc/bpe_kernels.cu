@@ -148,7 +148,7 @@ struct DevSmall {
   uint32_t status;
   uint32_t rec_used;  // u32 words of long pre-token records handed out this call
   int64_t total;
-  uint32_t q_short, q_med;  // cache misses queued for k_misses (<= 16 bytes, longer)
+  uint32_t q_n;  // cache misses queued for k_misses
 };
 
 
@@ -389,7 +389,7 @@ struct Smem : SplitSmem {
   } u;
   int32_t byte_id[256];
   uint16_t long_list[kMaxLong];
-  uint32_t red[kThreads / 32 + 2];
+  uint32_t red[2 * (kThreads / 32 + 1)];
   uint32_t carry[2];
   int64_t prefix;
   uint32_t agg;                      // the chunk's token count
@@ -397,7 +397,8 @@ struct Smem : SplitSmem {
   uint32_t n_long;
   uint32_t n_miss;                   // queued misses of <= 16 bytes
   uint32_t n_miss_m;                 // queued misses of 17..kShortMax bytes
-  uint32_t q_base_s, q_base_m;       // the chunk's first entries in the k_misses queue
+  uint32_t n_def;                    // word-cache misses (all lengths)
+  uint32_t q_base;                   // the chunk's first entry in the k_misses queue
   int64_t last_end;                  // end of the chunk's last pre-token, -1 past the window
   int last_end_rel;                  // the same relative to the chunk start
   int64_t doc_lo, doc_hi;  // document of a long pre-token that runs past the window
@@ -697,6 +698,38 @@ __device__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total) 
   *total = red[kThreads / 32];
   cta_sync();
   return r;
+}
+
+// Two exclusive scans over the CTA with one set of barriers; uses
+// red[0 .. 2 (kThreads/32 + 1)).
+__device__ void block_excl_scan2(uint32_t v, uint32_t u, uint32_t* red, uint32_t* ev, uint32_t* eu, uint32_t* tv,
+                                 uint32_t* tu) {
+  constexpr int kW = kThreads / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t iv = warp_incl_scan(v), iu = warp_incl_scan(u);
+  if (lane == 31) {
+    red[warp] = iv;
+    red[kW + 1 + warp] = iu;
+  }
+  cta_sync();
+  if (warp == 0) {
+    const uint32_t x = lane < kW ? red[lane] : 0, y = lane < kW ? red[kW + 1 + lane] : 0;
+    const uint32_t xi = warp_incl_scan(x), yi = warp_incl_scan(y);
+    if (lane < kW) {
+      red[lane] = xi - x;
+      red[kW + 1 + lane] = yi - y;
+    }
+    if (lane == kW - 1) {
+      red[kW] = xi;
+      red[2 * kW + 1] = yi;
+    }
+  }
+  cta_sync();
+  *ev = red[warp] + iv - v;
+  *eu = red[kW + 1 + warp] + iu - u;
+  *tv = red[kW];
+  *tu = red[2 * kW + 1];
+  cta_sync();
 }
 
 __device__ uint32_t block_min(uint32_t v, uint32_t* red) {
@@ -1034,8 +1067,7 @@ __global__ void k_prep(const int64_t* doc_offsets, int64_t n_docs, int64_t n_byt
   if (t0 == 0) {
     small->rec_used = 0;
     small->total = 0;
-    small->q_short = 0;
-    small->q_med = 0;
+    small->q_n = 0;
     first_doc[n_chunks] = n_docs + 1;
   }
   for (int64_t c = t0; c < n_chunks; c += stride) {
@@ -1073,8 +1105,7 @@ struct EncodeArgs {
   uint64_t rec_cap;            // u32 words of rec
   uint32_t* def_n;             // per chunk: cache misses handed to k_misses
   uint32_t* def_rec;           // [n_chunks][kMaxDefer][3] their records
-  uint64_t* queue;             // (chunk << 8 | slot): short misses from the front, longer from the back
-  uint64_t queue_cap;
+  uint64_t* queue;             // (chunk << 8 | slot) of each deferred miss
   const int64_t* first_doc;
   DevSmall* small;
   int64_t n_chunks;
@@ -1095,7 +1126,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
   // the end, the offsets of the first kThreads documents from there on.
   const int64_t k_first = __ldg(a.first_doc + c);
   const int64_t d_mine = k_first + tid <= a.n_docs ? __ldg(a.doc_offsets + k_first + tid) : INT64_MAX;
-  if (tid == kThreads - 1) S.more_docs = d_mine < c0 + kChunk;  // more than kThreads documents start here
   load_encode_window(S, a.bytes, a.n_bytes, a.doc_offsets, a.n_docs, a.start_bits, c0);
 
   // Pre-tokens starting in the chunk, in order. Thread t owns positions
@@ -1116,6 +1146,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
       S.n_long = 0;
       S.n_miss = 0;
       S.n_miss_m = 0;
+      S.n_def = 0;
       if (total == 0) {
         S.last_end = -1;
         S.last_end_rel = -1;
@@ -1148,6 +1179,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
   // slot and entry; the key is read again from the window to compare). Hits
   // finish here; misses are queued and merged next by lane groups, so a warp
   // does not wait on the merge loop of a few of its lanes.
+  uint32_t my_misses = 0;
   for (uint32_t j0 = tid; j0 < n_spans; j0 += kProbeRound * kThreads) {
     int st[kProbeRound], len[kProbeRound];
     CacheKey K[kProbeRound];
@@ -1181,6 +1213,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
           S.span_cnt[j] = cnt;
         } else {
           S.span_cnt[j] = kMissMark | (uint32_t)len[h];
+          ++my_misses;
         }
       } else {
         const uint32_t ql = atomicAdd(&S.n_long, 1u);
@@ -1190,38 +1223,21 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
       }
     }
   }
+  my_misses = __reduce_add_sync(0xFFFFFFFFu, my_misses);
+  if ((tid & 31) == 0 && my_misses) atomicAdd(&S.n_def, my_misses);
   cta_sync();
   // Cache misses. When the chunk's slots suffice they all go to k_misses:
-  // each keeps its byte length of ids reserved (ids never outnumber bytes),
-  // the chunk records it and moves on. Otherwise they are merged here by lane
-  // groups. Each thread owns a contiguous run of spans [run0, run1), in this
-  // and every later step.
+  // each keeps its byte length of ids reserved (ids never outnumber bytes)
+  // and gets a record and a queue entry with the chunk's ids further on.
+  // Otherwise they are merged here by lane groups. Each thread owns a
+  // contiguous run of spans [run0, run1), in this and every later step.
   const uint32_t per = (n_spans + kThreads - 1) / kThreads;
   const uint32_t run0 = min(n_spans, tid * per), run1 = min(n_spans, run0 + per);
-  uint32_t def_before, def_total;  // packed: misses of <= 16 bytes | longer ones << 16
-  {
-    uint32_t mine = 0;
-    for (uint32_t j = run0; j < run1; ++j) {
-      const uint32_t v = S.span_cnt[j];
-      if (v & kMissMark) mine += (v & 0xFFu) <= (uint32_t)kCacheMaxLen ? 1u : 0x10000u;
-    }
-    def_before = block_excl_scan(mine, S.red, &def_total);
-  }
-  const uint32_t n_def = (def_total & 0xFFFFu) + (def_total >> 16);
+  const uint32_t n_def = S.n_def;
   const bool defer = a.queue != nullptr && n_def <= kMaxDefer;
-  if (defer) {
-    if (tid == 0 && n_def) {
-      S.q_base_s = atomicAdd(&a.small->q_short, def_total & 0xFFFFu);
-      S.q_base_m = atomicAdd(&a.small->q_med, def_total >> 16);
-    }
-    for (uint32_t j = run0; j < run1; ++j) {
-      const uint32_t v = S.span_cnt[j];
-      if (v & kMissMark) {
-        S.span_start[j] |= kDeferFlag;
-        S.span_cnt[j] = v & 0xFFu;  // reserved
-      }
-    }
-  } else {
+  uint32_t q_base = 0;  // thread 0: the chunk's queue entries, needed only once its ids are written
+  if (defer && tid == 0 && n_def) q_base = atomicAdd(&a.small->q_n, n_def);
+  if (!defer) {
     for (uint32_t j = run0; j < run1; ++j) {
       const uint32_t v = S.span_cnt[j];
       if (!(v & kMissMark)) continue;
@@ -1236,39 +1252,39 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
         else S.span_cnt[j] = merge_at(S, st, len, a.T);
       }
     }
-  }
-  cta_sync();
-  {
-    // Queued misses: up to 16 bytes by groups of 8 lanes, longer ones by a
-    // warp each.
-    GroupScratch& W = S.u.grp[tid >> 5];
-    const uint32_t n_short = min(S.n_miss, kMissShortCap), n_med = min(S.n_miss_m, kMissMedCap);
-    for (uint32_t q0 = 0; q0 < n_short; q0 += kThreads / 8) {
-      const uint32_t q = q0 + (uint32_t)(tid >> 3);
-      uint32_t j = 0, n = 0;
-      int st = 0;
-      if (q < n_short) {
-        j = S.missq[q];
-        st = S.span_start[j];
-        n = (uint32_t)(((j + 1 < n_spans) ? (int)(S.span_start[j + 1] & ~kDeferFlag) : last_end) - st);
+    cta_sync();
+    {
+      // Queued misses: up to 16 bytes by groups of 8 lanes, longer ones by a
+      // warp each.
+      GroupScratch& W = S.u.grp[tid >> 5];
+      const uint32_t n_short = min(S.n_miss, kMissShortCap), n_med = min(S.n_miss_m, kMissMedCap);
+      for (uint32_t q0 = 0; q0 < n_short; q0 += kThreads / 8) {
+        const uint32_t q = q0 + (uint32_t)(tid >> 3);
+        uint32_t j = 0, n = 0;
+        int st = 0;
+        if (q < n_short) {
+          j = S.missq[q];
+          st = S.span_start[j];
+          n = (uint32_t)(((j + 1 < n_spans) ? (int)(S.span_start[j + 1] & ~kDeferFlag) : last_end) - st);
+        }
+        const uint32_t cnt = merge_group<8>(W, S.win + kHalo + st, n, a.T, S.byte_id, S.sym + st);
+        if (q < n_short && (tid & 7) == 0) S.span_cnt[j] = cnt;
       }
-      const uint32_t cnt = merge_group<8>(W, S.win + kHalo + st, n, a.T, S.byte_id, S.sym + st);
-      if (q < n_short && (tid & 7) == 0) S.span_cnt[j] = cnt;
-    }
-    for (uint32_t q0 = 0; q0 < n_med; q0 += kThreads / 32) {
-      const uint32_t q = q0 + (uint32_t)(tid >> 5);
-      uint32_t j = 0, n = 0;
-      int st = 0;
-      if (q < n_med) {
-        j = S.missq[kMissShortCap + q];
-        st = S.span_start[j];
-        n = (uint32_t)(((j + 1 < n_spans) ? (int)(S.span_start[j + 1] & ~kDeferFlag) : last_end) - st);
+      for (uint32_t q0 = 0; q0 < n_med; q0 += kThreads / 32) {
+        const uint32_t q = q0 + (uint32_t)(tid >> 5);
+        uint32_t j = 0, n = 0;
+        int st = 0;
+        if (q < n_med) {
+          j = S.missq[kMissShortCap + q];
+          st = S.span_start[j];
+          n = (uint32_t)(((j + 1 < n_spans) ? (int)(S.span_start[j + 1] & ~kDeferFlag) : last_end) - st);
+        }
+        const uint32_t cnt = merge_group<32>(W, S.win + kHalo + st, n, a.T, S.byte_id, S.sym + st);
+        if (q < n_med && (tid & 31) == 0) S.span_cnt[j] = cnt;
       }
-      const uint32_t cnt = merge_group<32>(W, S.win + kHalo + st, n, a.T, S.byte_id, S.sym + st);
-      if (q < n_med && (tid & 31) == 0) S.span_cnt[j] = cnt;
     }
+    cta_sync();
   }
-  cta_sync();
 
   // Long pre-tokens: the whole CTA, one at a time, in order.
   const uint32_t n_long = min(S.n_long, (uint32_t)kMaxLong);
@@ -1337,20 +1353,35 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
     }
   }
 
-  // Token offsets within the chunk.
-  // Each thread scans a contiguous run of spans [run0, run1); it also stores
-  // their ids at the end, so consecutive threads write consecutive ranges.
-  uint32_t agg = 0;
+  // Token offsets within the chunk, and the deferred misses' slots (in span
+  // order). Each thread scans a contiguous run of spans [run0, run1); it also
+  // stores their ids at the end, so consecutive threads write consecutive
+  // ranges. A deferred miss counts its reserved ids and is flagged.
+  uint32_t agg = 0, slot = 0;
   {
-    uint32_t sum = 0;
-    for (uint32_t j = run0; j < run1; ++j) sum += S.span_cnt[j];
-    uint32_t base = block_excl_scan(sum, S.red, &agg);
+    uint32_t sum = 0, nm = 0;
+    for (uint32_t j = run0; j < run1; ++j) {
+      const uint32_t v = S.span_cnt[j];
+      const bool miss = v & kMissMark;
+      sum += miss ? v & 0xFFu : v;
+      nm += miss;
+    }
+    if (tid == kThreads - 1) S.more_docs = d_mine < c0 + kChunk;  // more than kThreads documents start here
+    uint32_t base, def_all;
+    block_excl_scan2(sum, nm, S.red, &base, &slot, &agg, &def_all);
     for (uint32_t j = run0; j < run1; ++j) {
       uint32_t v = S.span_cnt[j];
+      if (v & kMissMark) {
+        v &= 0xFFu;
+        S.span_start[j] |= kDeferFlag;
+      }
       S.span_cnt[j] = base;
       base += v;
     }
-    if (tid == 0) S.span_cnt[n_spans] = agg;
+    if (tid == 0) {
+      S.span_cnt[n_spans] = agg;
+      S.q_base = q_base;
+    }
   }
   cta_sync();
 
@@ -1388,7 +1419,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
   // in slot order (= span order) and a queue entry.
   {
     uint32_t* stage = a.stage + c * kStage;
-    uint32_t ds = def_before & 0xFFFFu, dm = def_before >> 16;
     for (uint32_t j = run0; j < run1; ++j) {
       bool is_long = false;
       uint32_t long_before = 0;
@@ -1402,14 +1432,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
       const int st = (int)(raw & ~(uint32_t)kDeferFlag);
       const uint32_t o = S.span_cnt[j] - long_before, cnt = S.span_cnt[j + 1] - S.span_cnt[j];
       if (raw & kDeferFlag) {
-        const uint32_t slot = ds + dm;
         uint32_t* R = a.def_rec + ((uint64_t)c * kMaxDefer + slot) * 3;
         R[0] = S.span_cnt[j];
         R[1] = (uint32_t)st | cnt << 12 | o << 19;
         R[2] = cnt;
-        const uint64_t e = (uint64_t)c << 8 | slot;
-        if (cnt <= (uint32_t)kCacheMaxLen) a.queue[S.q_base_s + ds++] = e;
-        else a.queue[a.queue_cap - 1 - (S.q_base_m + dm++)] = e;
+        a.queue[S.q_base + slot] = (uint64_t)c << 8 | slot;
+        ++slot;
         continue;
       }
       for (uint32_t q = 0; q < cnt; ++q) stage[o + q] = S.sym[st + q];
@@ -1437,85 +1465,63 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
 
 // Cache misses that k_encode handed over, merged across the whole GPU: a
 // queue entry (chunk << 8 | slot) names a record {offset, start | reserved <<
-// 12 | stage offset << 19, ids}. Misses of up to 16 bytes go to groups of 8
-// lanes, longer ones to a warp (merge_group). Each writes its ids into its
-// reserved stage range, the count into its record, and gives the unused part
-// of the reservation back to the chunk's count.
+// 12 | stage offset << 19, ids}, reserved = the miss's byte length. A warp
+// takes 32 entries at a time, one per lane, and merges them in rounds:
+// groups of 4 lanes take misses of up to 8 bytes while at least 8 are left,
+// groups of 8 the rest of those up to 16 bytes, the whole warp each longer
+// one (merge_group). Each writes its ids into its reserved stage range, the
+// count into its record, and gives the unused part of the reservation back to
+// the chunk's count.
 constexpr int kMissBlocksPerSm = 6;  // resident at once (40 registers a thread)
-__global__ void __launch_bounds__(kThreads, kMissBlocksPerSm) k_misses(const uint8_t* bytes, const uint64_t* queue, uint64_t queue_cap,
-                                                     const DevSmall* small, uint32_t* def_rec, uint32_t* stage,
-                                                     uint64_t* chunk_meta, Tables T) {
+__global__ void __launch_bounds__(kThreads, kMissBlocksPerSm) k_misses(const uint8_t* bytes, const uint64_t* queue,
+                                                                       const DevSmall* small, uint32_t* def_rec,
+                                                                       uint32_t* stage, uint64_t* chunk_meta,
+                                                                       Tables T) {
   __shared__ GroupScratch grp[kThreads / 32];
   __shared__ int32_t byte_id[256];
   for (int i = threadIdx.x; i < 256; i += kThreads) byte_id[i] = T.byte_id[i];
   __syncthreads();
-  const uint32_t n_short = small->q_short, n_med = small->q_med;
+  const uint32_t n_q = small->q_n;
   const int lane = threadIdx.x & 31;
   GroupScratch& W = grp[threadIdx.x >> 5];
-  auto run = [&](uint64_t e, bool on, auto merge) {
-    const uint64_t c = e >> 8;
-    uint32_t* R = def_rec + (c * kMaxDefer + (e & 0xFFu)) * 3;
-    const uint32_t w = on ? R[1] : 0u;
-    const uint32_t st = w & 0xFFFu, n = on ? (w >> 12) & 0x7Fu : 0u, so = w >> 19;
-    const uint32_t cnt = merge(W, bytes + c * kChunk + st, n, stage + c * kStage + so);
-    return cnt;
-  };
-  // Misses of up to 16 bytes: those of up to 8 by groups of 4 lanes in a
-  // first pass, the others by groups of 8 in a second (each pass skips the
-  // other's entries).
-  {
-    const uint64_t groups = (uint64_t)gridDim.x * (kThreads / 4), g = (uint64_t)blockIdx.x * (kThreads / 4) + (threadIdx.x >> 2);
-    for (uint64_t q0 = 0; q0 < n_short; q0 += groups) {
-      const uint64_t q = q0 + g;
-      uint64_t e = q < n_short ? queue[q] : 0;
-      const bool on = q < n_short && ((def_rec[((e >> 8) * kMaxDefer + (e & 0xFFu)) * 3 + 1] >> 12) & 0x7Fu) <= 8u;
-      const uint32_t cnt = run(e, on, [&](GroupScratch& G, const uint8_t* src, uint32_t n, uint32_t* out) {
-        return merge_group<4>(G, src, n, T, byte_id, out);
-      });
-      if (on && (lane & 3) == 0) {
-        const uint64_t c = e >> 8;
-        uint32_t* R = def_rec + (c * kMaxDefer + (e & 0xFFu)) * 3;
-        const uint32_t reserved = (R[1] >> 12) & 0x7Fu;
-        R[2] = cnt;
-        atomicAdd(reinterpret_cast<unsigned long long*>(chunk_meta + c), 0ull - (unsigned long long)(reserved - cnt));
-      }
+  const uint64_t warps = (uint64_t)gridDim.x * (kThreads / 32);
+  for (uint64_t q0 = ((uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * 32; q0 < n_q; q0 += warps * 32) {
+    uint64_t e = 0;
+    uint32_t w = 0;
+    if (q0 + lane < n_q) {
+      e = queue[q0 + lane];
+      w = def_rec[((e >> 8) * kMaxDefer + (e & 0xFFu)) * 3 + 1];
     }
-  }
-  {
-    const uint64_t groups = (uint64_t)gridDim.x * (kThreads / 8), g = (uint64_t)blockIdx.x * (kThreads / 8) + (threadIdx.x >> 3);
-    for (uint64_t q0 = 0; q0 < n_short; q0 += groups) {
-      const uint64_t q = q0 + g;
-      uint64_t e = q < n_short ? queue[q] : 0;
-      const bool on = q < n_short && ((def_rec[((e >> 8) * kMaxDefer + (e & 0xFFu)) * 3 + 1] >> 12) & 0x7Fu) > 8u;
-      const uint32_t cnt = run(e, on, [&](GroupScratch& G, const uint8_t* src, uint32_t n, uint32_t* out) {
-        return merge_group<8>(G, src, n, T, byte_id, out);
-      });
-      if (on && (lane & 7) == 0) {
-        const uint64_t c = e >> 8;
-        uint32_t* R = def_rec + (c * kMaxDefer + (e & 0xFFu)) * 3;
-        const uint32_t reserved = (R[1] >> 12) & 0x7Fu;
-        R[2] = cnt;
-        atomicAdd(reinterpret_cast<unsigned long long*>(chunk_meta + c), 0ull - (unsigned long long)(reserved - cnt));
+    const uint32_t len = (w >> 12) & 0x7Fu;  // 0: no entry
+    uint32_t m4 = __ballot_sync(0xFFFFFFFFu, len != 0 && len <= 8u);
+    uint32_t m8 = __ballot_sync(0xFFFFFFFFu, len > 8u && len <= (uint32_t)kCacheMaxLen);
+    uint32_t m32 = __ballot_sync(0xFFFFFFFFu, len > (uint32_t)kCacheMaxLen);
+    // One round: group g of G lanes takes the g-th entry of *mask (none past
+    // its end); the round's entries leave the mask.
+    auto round = [&](uint32_t* mask, auto merge, int G) {
+      const int g = lane / G;
+      uint32_t mm = *mask;
+      for (int x = 0; x < g; ++x) mm &= mm - 1u;
+      const bool on = mm != 0;
+      const int src = on ? __ffs(mm) - 1 : 0;
+      for (int x = 0; x < 32 / G; ++x) *mask &= *mask - 1u;
+      const uint64_t ge = __shfl_sync(0xFFFFFFFFu, e, src);
+      const uint32_t gw = __shfl_sync(0xFFFFFFFFu, w, src);
+      const uint64_t c = ge >> 8;
+      const uint32_t n = on ? (gw >> 12) & 0x7Fu : 0u;
+      const uint32_t cnt = merge(bytes + c * kChunk + (gw & 0xFFFu), n, stage + c * kStage + (gw >> 19));
+      if (on && (lane & (G - 1)) == 0) {
+        def_rec[(c * kMaxDefer + (ge & 0xFFu)) * 3 + 2] = cnt;
+        atomicAdd(reinterpret_cast<unsigned long long*>(chunk_meta + c), 0ull - (unsigned long long)(n - cnt));
       }
-    }
-  }
-  {
-    const uint64_t warps = (uint64_t)gridDim.x * (kThreads / 32), wi = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-    for (uint64_t q0 = 0; q0 < n_med; q0 += warps) {
-      const uint64_t q = q0 + wi;
-      const bool on = q < n_med;
-      const uint64_t e = on ? queue[queue_cap - 1 - q] : 0;
-      const uint32_t cnt = run(e, on, [&](GroupScratch& G, const uint8_t* src, uint32_t n, uint32_t* out) {
-        return merge_group<32>(G, src, n, T, byte_id, out);
-      });
-      if (on && lane == 0) {
-        const uint64_t c = e >> 8;
-        uint32_t* R = def_rec + (c * kMaxDefer + (e & 0xFFu)) * 3;
-        const uint32_t reserved = (R[1] >> 12) & 0x7Fu;
-        R[2] = cnt;
-        atomicAdd(reinterpret_cast<unsigned long long*>(chunk_meta + c), 0ull - (unsigned long long)(reserved - cnt));
-      }
-    }
+    };
+    while (__popc(m4) >= 8)
+      round(&m4, [&](const uint8_t* src, uint32_t n, uint32_t* out) { return merge_group<4>(W, src, n, T, byte_id, out); }, 4);
+    m8 |= m4;
+    while (m8)
+      round(&m8, [&](const uint8_t* src, uint32_t n, uint32_t* out) { return merge_group<8>(W, src, n, T, byte_id, out); }, 8);
+    while (m32)
+      round(&m32, [&](const uint8_t* src, uint32_t n, uint32_t* out) { return merge_group<32>(W, src, n, T, byte_id, out); }, 32);
   }
 }
 
@@ -2081,7 +2087,6 @@ struct Ws {
   uint32_t* def_n;
   uint32_t* def_rec;
   uint64_t* queue;
-  uint64_t queue_cap;
   uint32_t* bits;
   uint32_t* stage;
   int32_t* pool;
@@ -2106,7 +2111,6 @@ Ws ws_carve(unsigned char* base, int64_t n_bytes) {
   w.def_rec = reinterpret_cast<uint32_t*>(base);
   base += z.def_rec;
   w.queue = reinterpret_cast<uint64_t*>(base);
-  w.queue_cap = (uint64_t)(n_bytes / kChunk + 1) * kMaxDefer;
   base += z.queue;
   w.bits = reinterpret_cast<uint32_t*>(base);
   base += z.bits;
@@ -2182,7 +2186,6 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
   a.def_n = w.def_n;
   a.def_rec = w.def_rec;
   a.queue = w.queue;
-  a.queue_cap = w.queue_cap;
   a.first_doc = w.first_doc;
   a.small = h->d_small;
   a.n_chunks = n_chunks;
@@ -2196,7 +2199,7 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
   k_encode<<<(unsigned)n_chunks, kThreads, sizeof(Smem), st>>>(a);
   CK(cudaGetLastError());
   const unsigned miss_grid = (unsigned)std::min<int64_t>((int64_t)kMissBlocksPerSm * h->n_sms, n_chunks);
-  k_misses<<<miss_grid, kThreads, 0, st>>>(d_bytes, w.queue, w.queue_cap, h->d_small,
+  k_misses<<<miss_grid, kThreads, 0, st>>>(d_bytes, w.queue, h->d_small,
                                       w.def_rec, w.stage, w.chunk_meta, a.T);
   CK(cudaGetLastError());
   const int64_t n_tiles = (n_chunks + kScanThreads - 1) / kScanThreads;
