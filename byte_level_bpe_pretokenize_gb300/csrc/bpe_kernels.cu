@@ -339,6 +339,18 @@ __device__ __forceinline__ uint32_t lds_u32(const uint32_t* p) {
   return v;
 }
 
+// Asynchronous global-to-shared copies (16 or 4 bytes, both addresses aligned
+// to the size): a thread issues all of its copies before it waits for any.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((unsigned)__cvta_generic_to_shared(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((unsigned)__cvta_generic_to_shared(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Bits [start, start + 32) of a shared bit array.
 __device__ __forceinline__ uint32_t bits32_at(const uint32_t* bits, int start) {
   const int w = start >> 5, sh = start & 31;
@@ -367,7 +379,7 @@ struct __align__(16) WindowSmem {
   uint32_t outbits[kWords + 2];   // byte belongs to no document
   uint32_t startbits[(CHUNK + AFTER) / 32];
   int64_t chunk;
-  int more_docs;  // more documents start in the window (or chunk) than one per thread
+  int more_docs;  // more documents start in the window than one per thread
 };
 
 // The encode kernel's window: a chunk plus the margin.
@@ -560,29 +572,30 @@ __device__ void load_window(SS& S, const uint8_t* bytes, int64_t n_bytes, const 
                             int64_t n_docs, int64_t c0, int64_t first_doc) {
   const int tid = threadIdx.x;
   const int64_t w0 = c0 - kHalo, w_end = w0 + SS::kLen;
-  // Every load is issued before the first barrier: the bytes, the first and
-  // last document offsets, and the offsets of the documents from 32 before
-  // first_doc on (one per thread; more only when documents are tiny).
+  // Every load is issued before the first barrier: the bytes (asynchronous
+  // 16-byte copies when the input is 16-byte aligned, window offsets being
+  // multiples of 16; bytes otherwise), the first and last document offsets,
+  // and the offsets of the documents from 32 before first_doc on (one per
+  // thread; more only when documents are tiny).
+  const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 15u) == 0;
+  for (int i = tid * 16; i < SS::kLen; i += kThreads * 16) {
+    const int64_t p = w0 + i;
+    if (aligned && p >= 0 && p + 16 <= n_bytes) {
+      cp_async16(S.win + i, bytes + p);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) S.win[i + k] = (p + k >= 0 && p + k < n_bytes) ? bytes[p + k] : 0;
+    }
+  }
   int64_t d_first = __ldg(doc_offsets), d_last = __ldg(doc_offsets + n_docs);
   int64_t k_lo = first_doc - 32;
   if (k_lo > n_docs) k_lo = n_docs;
   if (k_lo < 0) k_lo = 0;
   const int64_t o_before = k_lo > 0 ? __ldg(doc_offsets + k_lo - 1) : INT64_MIN;
   const int64_t o_mine = k_lo + tid <= n_docs ? __ldg(doc_offsets + k_lo + tid) : INT64_MAX;
-  // 16-byte loads and stores when the input is 16-byte aligned (window
-  // offsets are multiples of 16), bytes otherwise.
-  const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 15u) == 0;
-  for (int i = tid * 16; i < SS::kLen; i += kThreads * 16) {
-    const int64_t p = w0 + i;
-    if (aligned && p >= 0 && p + 16 <= n_bytes) {
-      *reinterpret_cast<uint4*>(S.win + i) = __ldg(reinterpret_cast<const uint4*>(bytes + p));
-    } else {
-#pragma unroll
-      for (int k = 0; k < 16; ++k) S.win[i + k] = (p + k >= 0 && p + k < n_bytes) ? bytes[p + k] : 0;
-    }
-  }
   for (int i = tid; i < SS::kWords + 2; i += kThreads) S.docbits[i] = 0;
   if (tid == kThreads - 1) S.more_docs = o_mine < w_end;
+  cp_async_wait_all();
   cta_sync();
   d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
   d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
@@ -629,14 +642,14 @@ __device__ void load_encode_window(SplitSmem& S, const uint8_t* bytes, int64_t n
                                    int64_t n_docs, const uint32_t* start_bits, int64_t c0) {
   const int tid = threadIdx.x;
   const int64_t w0 = c0 - kHalo;
-  int64_t d_first = __ldg(doc_offsets), d_last = __ldg(doc_offsets + n_docs);
-  // 16-byte loads and stores when the input is 16-byte aligned (window
-  // offsets are multiples of 16), bytes otherwise.
+  // Asynchronous 16-byte copies when the input is 16-byte aligned (window
+  // offsets are multiples of 16), bytes otherwise; the start bits as 4-byte
+  // copies.
   const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 15u) == 0;
   for (int i = tid * 16; i < kWin; i += kThreads * 16) {
     const int64_t p = w0 + i;
     if (aligned && p >= 0 && p + 16 <= n_bytes) {
-      *reinterpret_cast<uint4*>(S.win + i) = __ldg(reinterpret_cast<const uint4*>(bytes + p));
+      cp_async16(S.win + i, bytes + p);
     } else {
 #pragma unroll
       for (int k = 0; k < 16; ++k) S.win[i + k] = (p + k >= 0 && p + k < n_bytes) ? bytes[p + k] : 0;
@@ -645,8 +658,10 @@ __device__ void load_encode_window(SplitSmem& S, const uint8_t* bytes, int64_t n
   const int64_t n_words = (n_bytes + 31) / 32;
   for (int w = tid; w < kSpanWords; w += kThreads) {
     const int64_t gw = c0 / 32 + w;
-    S.startbits[w] = gw < n_words ? __ldg(start_bits + gw) : 0u;
+    if (gw < n_words) cp_async4(&S.startbits[w], start_bits + gw);
+    else S.startbits[w] = 0u;
   }
+  int64_t d_first = __ldg(doc_offsets), d_last = __ldg(doc_offsets + n_docs);
   d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
   d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
   for (int wi = tid; wi < kWinWords + 2; wi += kThreads) {
@@ -658,6 +673,7 @@ __device__ void load_encode_window(SplitSmem& S, const uint8_t* bytes, int64_t n
     }
     S.outbits[wi] = word;
   }
+  cp_async_wait_all();
   cta_sync();
 }
 
@@ -1122,11 +1138,14 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
   for (int i = tid; i < 256; i += kThreads) S.byte_id[i] = a.T.byte_id[i];
   const int64_t c = blockIdx.x;
   const int64_t c0 = c * kChunk;
-  // The first document starting at or after c0 and, ahead of their use at
-  // the end, the offsets of the first kThreads documents from there on.
+  // The first document starting at or after c0 (its load overlaps the
+  // window's) and, ahead of their use at the end, the offsets of the
+  // kThreads documents from there on and of the last of them (more
+  // documents start in the chunk when it does).
   const int64_t k_first = __ldg(a.first_doc + c);
-  const int64_t d_mine = k_first + tid <= a.n_docs ? __ldg(a.doc_offsets + k_first + tid) : INT64_MAX;
   load_encode_window(S, a.bytes, a.n_bytes, a.doc_offsets, a.n_docs, a.start_bits, c0);
+  const int64_t d_mine = k_first + tid <= a.n_docs ? __ldg(a.doc_offsets + k_first + tid) : INT64_MAX;
+  const int64_t d_more = k_first + kThreads - 1 <= a.n_docs ? __ldg(a.doc_offsets + k_first + kThreads - 1) : INT64_MAX;
 
   // Pre-tokens starting in the chunk, in order. Thread t owns positions
   // [16 t, 16 t + 16) of the chunk.
@@ -1366,7 +1385,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
       sum += miss ? v & 0xFFu : v;
       nm += miss;
     }
-    if (tid == kThreads - 1) S.more_docs = d_mine < c0 + kChunk;  // more than kThreads documents start here
     uint32_t base, def_all;
     block_excl_scan2(sum, nm, S.red, &base, &slot, &agg, &def_all);
     for (uint32_t j = run0; j < run1; ++j) {
@@ -1447,7 +1465,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
   // Offsets of the documents that start in this chunk, relative to the
   // chunk's first id (k_compact adds the chunk's offset).
   {
-    const bool more = S.more_docs;
+    const bool more = d_more < c0 + kChunk;
     for (int64_t k = k_first + tid; k <= a.n_docs; k += kThreads) {
       const int64_t d = k == k_first + tid ? d_mine : a.doc_offsets[k];
       if (d >= c0 + kChunk) break;
