@@ -461,6 +461,30 @@ __device__ __forceinline__ uint64_t bits64_at(const uint32_t* bits, int start) {
 // U+0020) and the next one or two bytes of its document are a suffix; then
 // the byte after it gets no boundary (B0) and the byte after the suffix gets
 // one (B1).
+// Contractions for the eligible apostrophes in cand (same bit layout): the
+// byte after the apostrophe loses its boundary (B0) and the byte after the
+// suffix gets one (B1).
+template <class SS>
+__device__ __forceinline__ uint64_t contractions(const SS& S, int p0, uint64_t cand, uint64_t D, uint64_t base) {
+  uint64_t B0 = 0, B1 = 0;
+  while (cand) {
+    const int k = __ffsll((long long)cand) - 1;
+    cand &= cand - 1;
+    const int q = p0 - 8 + k;
+    const uint32_t b1 = S.win[q + 1];
+    if (is_stmd(b1)) {
+      B0 |= 1ull << (k + 1);
+      B1 |= 1ull << (k + 2);
+    } else if (!((D >> (k + 2)) & 1u) && is_suffix2(b1, S.win[q + 2])) {
+      B0 |= 1ull << (k + 1);
+      B1 |= 1ull << (k + 3);
+    }
+  }
+  return (base & ~B0) | B1;
+}
+
+constexpr uint64_t kApostropheBits = 0x7FFFFFFFE0ull;  // apostrophes at bytes p0 - 3 .. p0 + 30 matter
+
 template <class SS>
 __device__ __forceinline__ uint32_t boundaries32(const SS& S, int p0, uint64_t U, uint64_t L, uint64_t N,
                                                  uint64_t Sm, uint64_t SP, uint64_t AP, uint64_t D, uint64_t O) {
@@ -469,27 +493,74 @@ __device__ __forceinline__ uint32_t boundaries32(const SS& S, int p0, uint64_t U
   const uint64_t B2 = Sm & (~Sp | (~Sn & ~Dn));
   const uint64_t B3 = ~Sm & ~SPp & (Sp | (L ^ Lp) | (N ^ Np));
   uint64_t base = D | B2 | B3;
-  uint64_t ap = AP & 0x7FFFFFFFE0ull;  // apostrophes at bytes p0 - 3 .. p0 + 30
-  if (ap) {
-    const uint64_t prev_ok = (L | N | (Sm & ~SP)) << 1;  // bit k: byte k - 1 makes an apostrophe at k eligible
-    uint64_t B0 = 0, B1 = 0;
-    while (ap) {
-      const int k = __ffsll((long long)ap) - 1;
-      ap &= ap - 1;
-      if (!(((D | prev_ok) >> k) & 1u) || ((D >> (k + 1)) & 1u)) continue;
-      const int q = p0 - 8 + k;
-      const uint32_t b1 = S.win[q + 1];
-      if (is_stmd(b1)) {
-        B0 |= 1ull << (k + 1);
-        B1 |= 1ull << (k + 2);
-      } else if (!((D >> (k + 2)) & 1u) && is_suffix2(b1, S.win[q + 2])) {
-        B0 |= 1ull << (k + 1);
-        B1 |= 1ull << (k + 3);
-      }
-    }
-    base = (base & ~B0) | B1;
-  }
+  const uint64_t prev_ok = (L | N | (Sm & ~SP)) << 1;  // bit k: byte k - 1 makes an apostrophe at k eligible
+  const uint64_t cand = AP & kApostropheBits & (D | prev_ok) & ~(D >> 1);
+  if (cand) base = contractions(S, p0, cand, D, base);
   return (uint32_t)((U & ~O & base) >> 8);
+}
+
+// The same rules for bytes p0 - 4 .. p0 + 35 read as ASCII (word m of w32 =
+// bytes p0 - 4 + 4 m), computed per byte on 0x80-per-byte masks (a byte's
+// neighbours are a funnel shift away) and turned into bits once:
+// base = D | X | B3 | (Y & ~Dn) with X = S & ~Sp and Y = S & ~Sn the two
+// halves of B2, and C the apostrophes whose previous byte makes them
+// eligible. *any gets the OR of the ten words: the result holds only if none
+// has a byte >= 0x80.
+template <class SS>
+__device__ __forceinline__ uint32_t ascii_starts32(const SS& S, int p0, const uint32_t* w32, uint64_t D, uint64_t O,
+                                                   uint32_t* any) {
+  uint32_t wv[10];
+#pragma unroll
+  for (int m = 0; m < 10; ++m) wv[m] = lds_u32(w32 + m);
+  Ascii4 prev = ascii_classes(wv[0]), cur = ascii_classes(wv[1]);
+  uint32_t all = wv[0] | wv[1];
+  // eligible apostrophes of word 0 (bytes p0 - 3 .. p0 - 1 are the ones used)
+  uint32_t e_prev = prev.L | prev.N | (prev.S & ~prev.SP);
+  const uint32_t c0 = movemask4(~((wv[0] ^ 0x27272727u) + 0x7F7F7F7Fu) & 0x80808080u & __funnelshift_l(0u, e_prev, 8));
+  uint32_t z = 0, y = 0, c = 0, zlo = 0, ylo = 0, clo = 0;
+#pragma unroll
+  for (int m = 1; m <= 8; ++m) {
+    all |= wv[m + 1];
+    const Ascii4 next = ascii_classes(wv[m + 1]);
+    const uint32_t Sp = __funnelshift_l(prev.S, cur.S, 8), Lp = __funnelshift_l(prev.L, cur.L, 8),
+                   Np = __funnelshift_l(prev.N, cur.N, 8), SPp = __funnelshift_l(prev.SP, cur.SP, 8),
+                   Sn = __funnelshift_r(cur.S, next.S, 8);
+    const uint32_t B3 = ~cur.S & ~SPp & (Sp | (cur.L ^ Lp) | (cur.N ^ Np));
+    const uint32_t Z = (cur.S & ~Sp) | B3, Y = cur.S & ~Sn;
+    const uint32_t E = cur.L | cur.N | (cur.S & ~cur.SP);
+    const uint32_t C = ~((wv[m] ^ 0x27272727u) + 0x7F7F7F7Fu) & 0x80808080u & __funnelshift_l(e_prev, E, 8);
+    e_prev = E;
+    if (m & 1) {
+      zlo = Z >> 7;
+      ylo = Y >> 7;
+      clo = C >> 7;
+    } else {
+      // bytes of words m - 1 and m: bits 0..3 and 4..7 of the product's top
+      // byte (the other partial products stay below bit 24), placed in byte
+      // (m - 2) / 2 of the result
+      const int i = (m - 2) / 2;
+      const uint32_t sel = (0x3210u & ~(0xFu << (4 * i))) | (7u << (4 * i));
+      z = __byte_perm(z, (zlo | (Z >> 3)) * 0x01020408u, sel);
+      y = __byte_perm(y, (ylo | (Y >> 3)) * 0x01020408u, sel);
+      c = __byte_perm(c, (clo | (C >> 3)) * 0x01020408u, sel);
+    }
+    prev = cur;
+    cur = next;
+  }
+  *any = all;
+  uint32_t base = (uint32_t)(D >> 8) | z | (y & ~(uint32_t)(D >> 9));
+  // Contractions: eligible apostrophes, and apostrophes at a document start;
+  // none followed by a document start.
+  uint64_t cand = ((uint64_t)c << 8) | ((uint64_t)c0 << 4);
+  uint64_t dap = D & kApostropheBits;
+  while (dap) {
+    const int k = __ffsll((long long)dap) - 1;
+    dap &= dap - 1;
+    if (S.win[p0 - 8 + k] == 0x27u) cand |= 1ull << k;
+  }
+  cand &= kApostropheBits & ~(D >> 1);
+  if (cand) base = (uint32_t)(contractions(S, p0, cand, D, (uint64_t)base << 8) >> 8);
+  return base & ~(uint32_t)(O >> 8);
 }
 
 // Start bits of window positions [p0, p0 + 32), p0 a multiple of 16.
@@ -497,31 +568,11 @@ template <class SS>
 __device__ uint32_t start_mask32(const SS& S, int p0) {
   const uint64_t D = bits64_at(S.docbits, p0 - 8), O = bits64_at(S.outbits, p0 - 8);
   if ((uint32_t)(O >> 8) == 0xFFFFFFFFu) return 0;
-  // Ten aligned window words: bytes p0 - 4 .. p0 + 35.
-  const uint32_t* w32 = reinterpret_cast<const uint32_t*>(S.win + p0);
-  uint32_t w[10], any = 0;
-#pragma unroll
-  for (int m = 0; m < 10; ++m) {
-    w[m] = lds_u32(w32 - 1 + m);
-    any |= w[m];
-  }
-  if (!(any & 0x80808080u)) {
-    // ASCII: every byte is a unit; masks for bytes p0 - 4 .. p0 + 35 land in
-    // bits 4..43.
-    uint64_t L = 0, N = 0, Sm = 0, SP = 0, AP = 0;
-#pragma unroll
-    for (int m = 0; m < 10; ++m) {
-      const Ascii4 a = ascii_classes(w[m]);
-      const uint32_t y = w[m] ^ 0x27272727u;
-      const int sh = 4 + 4 * m;
-      L |= (uint64_t)movemask4(a.L) << sh;
-      N |= (uint64_t)movemask4(a.N) << sh;
-      Sm |= (uint64_t)movemask4(a.S) << sh;
-      SP |= (uint64_t)movemask4(a.SP) << sh;
-      AP |= (uint64_t)movemask4(~(y + 0x7F7F7F7Fu) & 0x80808080u) << sh;
-    }
-    return boundaries32(S, p0, ~0ull, L, N, Sm, SP, AP, D, O);
-  }
+  // Ten aligned window words: bytes p0 - 4 .. p0 + 35. ASCII: every byte is a
+  // unit.
+  uint32_t any;
+  const uint32_t ascii = ascii_starts32(S, p0, reinterpret_cast<const uint32_t*>(S.win + p0) - 1, D, O, &any);
+  if (!(any & 0x80808080u)) return ascii;
   // General: scan the UTF-8 units of bytes [p0 - 7, p0 + 33); each byte
   // carries its unit's class. Units starting before p0 - 8 may be misread
   // only up to p0 - 5, and nothing before p0 - 4 is used.
