@@ -69,7 +69,7 @@ namespace {
 
 constexpr int kThreads = 256;         // threads per CTA
 constexpr int kChunk = 4096;          // bytes whose pre-tokens a CTA owns (16 per thread)
-constexpr int kMargin = 256;          // bytes after the chunk kept in shared memory
+constexpr int kMargin = 64;           // bytes after the chunk kept in shared memory (a short pre-token ends there)
 constexpr int kHalo = 16;             // context bytes on each side of the window
 constexpr int kWin = kHalo + kChunk + kMargin + kHalo;   // window bytes
 constexpr int kWinWords = (kWin + 31) / 32;
@@ -80,7 +80,7 @@ constexpr int kCacheMaxLen = 16;      // longest pre-token looked up in the word
 constexpr int kCacheMaxIds = 3;       // most ids a cache entry holds
 constexpr int kProbeRound = 2;        // word-cache probes a thread has in flight
 constexpr uint32_t kMaxDefer = 160;   // cache misses per chunk handed to k_misses
-constexpr uint32_t kMissMark = 1u << 31;   // span_cnt: a cache miss, its byte length below
+constexpr uint16_t kMissMark = 0x8000;     // span_cnt: a cache miss, its byte length below
 constexpr uint16_t kDeferFlag = 0x8000;    // span_start: the miss goes to k_misses
 constexpr int kLongPerThread = 4;     // elements per thread per round of the CTA merge
 constexpr int kRound = kThreads * kLongPerThread;
@@ -363,19 +363,23 @@ __device__ __forceinline__ uint32_t bits32_at(const uint32_t* bits, int start) {
 
 namespace {
 
+// Warps of an encode CTA that merge the cache misses it keeps (the rest wait).
+constexpr int kMergeWarps = 4;
+
 // A warp's scratch while its lanes merge pre-tokens in groups (merge_group).
 struct GroupScratch {
   uint32_t sym[64], rank[64], nw[64];
 };
 
 // What the split needs: the window and its document and start bit masks. The
-// split kernel's shared memory is only this; the encode kernel's extends it.
-template <int CHUNK, int AFTER>
+// split kernel's shared memory is only this; the encode kernel's extends it
+// (and keeps no document starts: every document edge is a pre-token start).
+template <int CHUNK, int AFTER, bool DOCS>
 struct __align__(16) WindowSmem {
   static constexpr int kLen = kHalo + CHUNK + AFTER + kHalo;  // window bytes
   static constexpr int kWords = (kLen + 31) / 32;
   uint8_t win[kLen + 16];
-  uint32_t docbits[kWords + 2];   // a document (or the area after the last one) starts here
+  uint32_t docbits[DOCS ? kWords + 2 : 1];  // a document (or the area after the last one) starts here
   uint32_t outbits[kWords + 2];   // byte belongs to no document
   uint32_t startbits[(CHUNK + AFTER) / 32];
   int64_t chunk;
@@ -383,24 +387,27 @@ struct __align__(16) WindowSmem {
 };
 
 // The encode kernel's window: a chunk plus the margin.
-using SplitSmem = WindowSmem<kChunk, kMargin>;
+using SplitSmem = WindowSmem<kChunk, kMargin, false>;
 static_assert(SplitSmem::kLen == kWin && SplitSmem::kWords == kWinWords, "encode window");
 // The split kernel's window: 32 bytes per thread.
 constexpr int kSplitChunk = 32 * kThreads;
-using SplitWin = WindowSmem<kSplitChunk, kHalo>;
+using SplitWin = WindowSmem<kSplitChunk, kHalo, true>;
 
 struct Smem : SplitSmem {
   uint16_t missq[kMissShortCap + kMissMedCap];  // queued word-cache misses
   uint16_t grp_pos[kThreads];        // pre-tokens starting before chunk byte 16 t
   uint16_t span_start[kChunk + 1];
-  uint32_t span_cnt[kChunk + 1];     // token counts, then exclusive offsets
+  // token counts (long pre-tokens 0, a miss kMissMark | length), then
+  // exclusive offsets without the long pre-tokens' ids
+  uint16_t span_cnt[kChunk + 1];
   uint32_t sym[kSpan];               // ids of short pre-tokens, at their start position
   union {
-    GroupScratch grp[kThreads / 32]; // one per warp while lane groups merge cache misses
+    GroupScratch grp[kMergeWarps];   // one per merging warp while lane groups merge cache misses
     uint32_t stage[kRound];          // long merge rounds
   } u;
   int32_t byte_id[256];
   uint16_t long_list[kMaxLong];
+  uint32_t long_cnt[kMaxLong];       // ids of each long pre-token, in long_list order
   uint32_t red[2 * (kThreads / 32 + 1)];
   uint32_t carry[2];
   int64_t prefix;
@@ -416,10 +423,12 @@ struct Smem : SplitSmem {
   int64_t doc_lo, doc_hi;  // document of a long pre-token that runs past the window
 };
 
+constexpr int kEncodeCtasPerSm = 5;  // resident encode CTAs (shared memory and 48 registers a thread)
+
 // Barrier of the kThreads threads of a CTA (named barrier 1).
 __device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
 
-static_assert(4 * (sizeof(Smem) + 1024) <= 228 * 1024, "four encode CTAs fit in an SM's shared memory");
+static_assert(kEncodeCtasPerSm * (sizeof(Smem) + 1024) <= 228 * 1024, "the encode CTAs fit in an SM's shared memory");
 
 __device__ __forceinline__ bool bit_at(const uint32_t* bits, int i) { return (bits[i >> 5] >> (i & 31)) & 1u; }
 
@@ -1182,7 +1191,7 @@ struct EncodeArgs {
 // its stage region (short pre-tokens) or stay in the pool (long ones, listed
 // in a record), its count to chunk_meta, and its documents' offsets are
 // written relative to the chunk. k_chunk_scan and k_compact finish the call.
-__global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
+__global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
@@ -1323,12 +1332,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
       }
     }
     cta_sync();
-    {
-      // Queued misses: up to 16 bytes by groups of 8 lanes, longer ones by a
-      // warp each.
+    if (tid < 32 * kMergeWarps) {
+      // Queued misses, by the first kMergeWarps warps: up to 16 bytes by
+      // groups of 8 lanes, longer ones by a warp each.
       GroupScratch& W = S.u.grp[tid >> 5];
       const uint32_t n_short = min(S.n_miss, kMissShortCap), n_med = min(S.n_miss_m, kMissMedCap);
-      for (uint32_t q0 = 0; q0 < n_short; q0 += kThreads / 8) {
+      for (uint32_t q0 = 0; q0 < n_short; q0 += 4 * kMergeWarps) {
         const uint32_t q = q0 + (uint32_t)(tid >> 3);
         uint32_t j = 0, n = 0;
         int st = 0;
@@ -1340,7 +1349,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
         const uint32_t cnt = merge_group<8>(W, S.win + kHalo + st, n, a.T, S.byte_id, S.sym + st);
         if (q < n_short && (tid & 7) == 0) S.span_cnt[j] = cnt;
       }
-      for (uint32_t q0 = 0; q0 < n_med; q0 += kThreads / 32) {
+      for (uint32_t q0 = 0; q0 < n_med; q0 += kMergeWarps) {
         const uint32_t q = q0 + (uint32_t)(tid >> 5);
         uint32_t j = 0, n = 0;
         int st = 0;
@@ -1414,19 +1423,21 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
       const int64_t n = e - s;
       if (n <= 0 || n >= (int64_t)0x7FFFFFFF) {
         if (tid == 0) atomicOr(&a.small->status, kStInternal);
-        if (tid == 0) S.span_cnt[j] = 0;
+        if (tid == 0) S.long_cnt[x] = 0;
       } else {
         uint32_t cnt = merge_long(a.bytes, s, (uint32_t)n, a.pool + s, a.T, S.byte_id, L);
-        if (tid == 0) S.span_cnt[j] = cnt;
+        if (tid == 0) S.long_cnt[x] = cnt;
       }
       cta_sync();
     }
   }
 
-  // Token offsets within the chunk, and the deferred misses' slots (in span
-  // order). Each thread scans a contiguous run of spans [run0, run1); it also
-  // stores their ids at the end, so consecutive threads write consecutive
-  // ranges. A deferred miss counts its reserved ids and is flagged.
+  // Token offsets within the chunk without the long pre-tokens' ids (= stage
+  // offsets; a long pre-token counts 0 here), and the deferred misses' slots
+  // (in span order). Each thread scans a contiguous run of spans [run0,
+  // run1); it also stores their ids at the end, so consecutive threads write
+  // consecutive ranges. A deferred miss counts its reserved ids and is
+  // flagged.
   uint32_t agg = 0, slot = 0;
   {
     uint32_t sum = 0, nm = 0;
@@ -1444,11 +1455,11 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
         v &= 0xFFu;
         S.span_start[j] |= kDeferFlag;
       }
-      S.span_cnt[j] = base;
+      S.span_cnt[j] = (uint16_t)base;
       base += v;
     }
     if (tid == 0) {
-      S.span_cnt[n_spans] = agg;
+      S.span_cnt[n_spans] = (uint16_t)agg;
       S.q_base = q_base;
     }
   }
@@ -1456,21 +1467,26 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
 
   // Long pre-tokens: one record block per chunk, {n_long, then per long
   // pre-token {offset in the chunk, first byte (low, high 32 bits), count}}.
+  // Offsets in the chunk count every id before: the stage offset plus the
+  // ids of the long pre-tokens before.
   if (tid == 0) {
     uint64_t meta = agg;
+    for (uint32_t x = 0; x < n_long; ++x) meta += S.long_cnt[x];
     if (n_long > 0) {
       const uint32_t words = 1 + 4 * n_long;
       const uint32_t r = atomicAdd(&a.small->rec_used, words);
       if ((uint64_t)r + words <= a.rec_cap) {
         a.rec[r] = n_long;
+        uint32_t long_before = 0;
         for (uint32_t x = 0; x < n_long; ++x) {
           const uint32_t j = S.long_list[x];
           const uint64_t s = (uint64_t)(c0 + (S.span_start[j] & ~kDeferFlag));
           uint32_t* e = a.rec + r + 1 + 4 * x;
-          e[0] = S.span_cnt[j];
+          e[0] = S.span_cnt[j] + long_before;
           e[1] = (uint32_t)s;
           e[2] = (uint32_t)(s >> 32);
-          e[3] = S.span_cnt[j + 1] - S.span_cnt[j];
+          e[3] = S.long_cnt[x];
+          long_before += S.long_cnt[x];
         }
         meta |= (uint64_t)(r + 1) << 32;
       } else {
@@ -1494,15 +1510,15 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
       for (uint32_t x = 0; x < n_long; ++x) {
         const uint32_t lj = S.long_list[x];
         is_long |= lj == j;
-        if (lj < j) long_before += S.span_cnt[lj + 1] - S.span_cnt[lj];
+        if (lj < j) long_before += S.long_cnt[x];
       }
       if (is_long) continue;
       const uint32_t raw = S.span_start[j];
       const int st = (int)(raw & ~(uint32_t)kDeferFlag);
-      const uint32_t o = S.span_cnt[j] - long_before, cnt = S.span_cnt[j + 1] - S.span_cnt[j];
+      const uint32_t o = S.span_cnt[j], cnt = (uint32_t)S.span_cnt[j + 1] - o;
       if (raw & kDeferFlag) {
         uint32_t* R = a.def_rec + ((uint64_t)c * kMaxDefer + slot) * 3;
-        R[0] = S.span_cnt[j];
+        R[0] = o + long_before;
         R[1] = (uint32_t)st | cnt << 12 | o << 19;
         R[2] = cnt;
         a.queue[S.q_base + slot] = (uint64_t)c << 8 | slot;
@@ -1525,7 +1541,11 @@ __global__ void __launch_bounds__(kThreads, 4) k_encode(EncodeArgs a) {
       // group, plus the group's starts before d
         const int rel = (int)(d - c0), t = rel >> 4;
         const uint32_t gbits = (S.startbits[t >> 1] >> ((t & 1) * 16)) & ((1u << (rel & 15)) - 1u);
-        a.out_offsets[k] = S.span_cnt[S.grp_pos[t] + __popc(gbits)];
+        const uint32_t r = S.grp_pos[t] + __popc(gbits);
+        int64_t o = S.span_cnt[r];
+        for (uint32_t x = 0; x < n_long; ++x)
+          if (S.long_list[x] < r) o += S.long_cnt[x];
+        a.out_offsets[k] = o;
       }
       if (!more) break;
     }
