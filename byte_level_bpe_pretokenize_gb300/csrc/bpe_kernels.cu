@@ -2105,8 +2105,10 @@ int build_word_cache(bpe_handle* h, const uint8_t* vocab_bytes, const int64_t* v
   }
   int64_t keep = 0;
   for (int64_t i = 0; i < n; ++i) keep += (vals[4 * i] >= 1 && vals[4 * i] <= (uint32_t)kCacheMaxIds);
+  // load factor at most 1/8: a probe that meets another key at the home slot
+  // costs the whole warp a second round trip
   uint64_t slots = 16;
-  while (slots < (uint64_t)keep * 4) slots <<= 1;
+  while (slots < (uint64_t)keep * 8) slots <<= 1;
   std::vector<uint4> table(slots * 2, make_uint4(0, 0, 0, 0));
   for (int64_t i = 0; i < n; ++i) {
     const uint32_t cnt = vals[4 * i];

@@ -93,11 +93,13 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
  *                  the next bpe_sync_status() on the handle.
  *   stream         the CUDA stream to run on.
  *
- * Workspace: the handle keeps about 8.3 bytes per input byte:
+ * Workspace: the handle keeps about 9.2 bytes per input byte:
  *   - a pool of 4 bytes per input byte (scratch for pre-tokens too long for
  *     shared memory, each using the range of its own bytes);
  *   - a stage of about 4 bytes per input byte (each 4 KiB chunk's ids, before
  *     the chunk offsets are known);
+ *   - records and a queue for the word-cache misses each chunk hands to the
+ *     GPU-wide miss merge (about 0.8 bytes per input byte);
  *   - the start bitmask (1 bit per byte);
  *   - records of long pre-tokens and a few words per chunk.
  * The workspace grows (cudaFree of the old one, then cudaMalloc) the first
@@ -158,11 +160,12 @@ int bpe_encode_batch_host(bpe_handle* h, const uint8_t* h_bytes, int64_t n_bytes
  *   Limit: n_bytes <= 4 MiB (4,194,304). A larger batch is rejected with
  *   BPE_ERR_INVALID_ARG before anything is queued; split it or use
  *   bpe_encode_batch. n_docs is not limited by the scratch.
- *   Scratch: one 35 MB array of static device memory per device (reserved
+ *   Scratch: one 38.7 MB array of static device memory per device (reserved
  *   when the library's module is loaded on that device, not by this call).
  *   It holds bpe_encode_batch's workspace for a 4 MiB batch:
  *     - each 4 KiB chunk's first document, token count and offset;
  *     - the records of long pre-tokens;
+ *     - the records and queue of deferred word-cache misses;
  *     - the pre-token start bitmask;
  *     - the per-chunk stage of ids;
  *     - the pool for pre-tokens too long for shared memory.
@@ -242,7 +245,8 @@ int bpe_set_word_cache(bpe_handle* h, int enable);
  * non-NULL, the next bpe_encode_batch calls record them on the call's stream:
  *   - ev_start right after the first (bookkeeping) kernel;
  *   - ev_stop right after the last kernel.
- * So the caller times the split, encode, scan and compaction kernels together.
+ * So the caller times the split, encode, miss-merge, scan and compaction
+ * kernels together.
  * NULL, NULL switches it off.
  */
 int bpe_set_timing_events(bpe_handle* h, void* ev_start, void* ev_stop);
