@@ -351,6 +351,14 @@ __device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// A 64-bit read-only global load issued where it stands (not merged with an
+// earlier load of the same word, whose register would then stay live).
+__device__ __forceinline__ int64_t ldg_fresh(const int64_t* p) {
+  int64_t v;
+  asm volatile("ld.global.nc.s64 %0, [%1];" : "=l"(v) : "l"(p));
+  return v;
+}
+
 // Bits [start, start + 32) of a shared bit array.
 __device__ __forceinline__ uint32_t bits32_at(const uint32_t* bits, int start) {
   const int w = start >> 5, sh = start & 31;
@@ -1075,8 +1083,10 @@ __device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, in
 // Word-cache key of a short pre-token (window positions [kHalo + st, + len)):
 // its bytes as four little-endian words, zero past len, read with aligned
 // 32-bit shared loads and funnel shifts.
+// A pre-token's cache key words: its bytes little-endian in x0..x3, zero
+// padded (the length travels separately).
 struct CacheKey {
-  uint32_t x0, x1, x2, x3, len, slot;
+  uint32_t x0, x1, x2, x3;
 };
 
 __device__ __forceinline__ CacheKey cache_key_words(const Smem& S, int st, int len) {
@@ -1094,31 +1104,28 @@ __device__ __forceinline__ CacheKey cache_key_words(const Smem& S, int st, int l
   K.x1 = __funnelshift_r(a1, a2, sh) & (uint32_t)(m_lo >> 32);
   K.x2 = __funnelshift_r(a2, a3, sh) & (uint32_t)m_hi;
   K.x3 = __funnelshift_r(a3, a4, sh) & (uint32_t)(m_hi >> 32);
-  K.len = (uint32_t)len;
-  K.slot = 0;
   return K;
 }
 
-__device__ __forceinline__ CacheKey cache_key(const Smem& S, int st, int len, const Cache& C) {
-  CacheKey K = cache_key_words(S, st, len);
-  K.slot = cache_hash(K.x0, K.x1, K.x2, K.x3, K.len) & C.mask;
-  return K;
+__device__ __forceinline__ uint32_t cache_slot(const CacheKey& K, uint32_t len, const Cache& C) {
+  return cache_hash(K.x0, K.x1, K.x2, K.x3, len) & C.mask;
 }
 
-// Count of ids (1..3) for key K given the entry {ea, eb} at its first slot
-// (loaded by the caller), 0 when absent; the ids go to ids[0..2].
-__device__ __forceinline__ uint32_t cache_resolve(const Cache& C, const CacheKey& K, uint4 ea, uint4 eb,
+// Count of ids (1..3) for key K of len bytes given the entry {ea, eb} at its
+// home slot (loaded by the caller), 0 when absent; the ids go to ids[0..2].
+// The home slot is recomputed only when the probe goes on past it.
+__device__ __forceinline__ uint32_t cache_resolve(const Cache& C, const CacheKey& K, uint32_t len, uint4 ea, uint4 eb,
                                                   uint32_t* ids) {
-  uint32_t slot = K.slot;
+  uint32_t slot = kNone;
   for (uint32_t probe = 0; probe <= C.mask; ++probe) {
     if (eb.x == 0) return 0;
-    if ((eb.x & 31u) == K.len && ea.x == K.x0 && ea.y == K.x1 && ea.z == K.x2 && ea.w == K.x3) {
+    if ((eb.x & 31u) == len && ea.x == K.x0 && ea.y == K.x1 && ea.z == K.x2 && ea.w == K.x3) {
       ids[0] = eb.y;
       ids[1] = eb.z;
       ids[2] = eb.w;
       return (eb.x >> 5) & 7u;
     }
-    slot = (slot + 1) & C.mask;
+    slot = ((slot == kNone ? cache_slot(K, len, C) : slot) + 1) & C.mask;
     ea = __ldg(C.e + 2 * slot);
     eb = __ldg(C.e + 2 * slot + 1);
   }
@@ -1252,6 +1259,10 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
   cta_sync();
   const uint32_t n_spans = S.n_spans;
   const int last_end = S.last_end_rel;
+  // The document offsets have arrived by now: keep them relative to the
+  // chunk (-1 before it, kChunk from its end on) to spare registers.
+  const int d_rel = d_mine < c0 ? -1 : (d_mine >= c0 + kChunk ? kChunk : (int)(d_mine - c0));
+  const bool more = d_more < c0 + kChunk;
 
   // Short pre-tokens, one thread each, kProbeRound per round with their
   // word-cache probes in flight together (a thread keeps only each probe's
@@ -1260,38 +1271,43 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
   // does not wait on the merge loop of a few of its lanes.
   uint32_t my_misses = 0;
   for (uint32_t j0 = tid; j0 < n_spans; j0 += kProbeRound * kThreads) {
-    int st[kProbeRound], len[kProbeRound];
+    // per probe: start | length << 12 | present << 30 | probed << 31 (a
+    // length above kShortMax: long)
+    uint32_t sl[kProbeRound];
     CacheKey K[kProbeRound];
     uint4 ea[kProbeRound], eb[kProbeRound];
 #pragma unroll
     for (int h = 0; h < kProbeRound; ++h) {
       const uint32_t j = j0 + (uint32_t)h * kThreads;
-      st[h] = 0;
-      len[h] = -1;  // -1: no pre-token; > kShortMax: long
-      K[h].slot = kNone;
+      sl[h] = 0;
       if (j < n_spans) {
-        st[h] = S.span_start[j];
+        const int st = S.span_start[j];
         const int en = (j + 1 < n_spans) ? (int)S.span_start[j + 1] : last_end;
-        len[h] = en < 0 ? kSpan : en - st[h];
-        if (len[h] <= kCacheMaxLen && a.C.enabled) {
-          K[h] = cache_key(S, st[h], len[h], a.C);
-          ea[h] = __ldg(a.C.e + 2 * K[h].slot);
-          eb[h] = __ldg(a.C.e + 2 * K[h].slot + 1);
+        const int len = en < 0 ? kSpan : en - st;
+        sl[h] = (uint32_t)st | (uint32_t)len << 12 | 1u << 30;
+        if (len <= kCacheMaxLen && a.C.enabled) {
+          K[h] = cache_key_words(S, st, len);
+          const uint32_t slot = cache_slot(K[h], (uint32_t)len, a.C);
+          ea[h] = __ldg(a.C.e + 2 * slot);
+          eb[h] = __ldg(a.C.e + 2 * slot + 1);
+          sl[h] |= 1u << 31;
         }
       }
     }
 #pragma unroll
     for (int h = 0; h < kProbeRound; ++h) {
       const uint32_t j = j0 + (uint32_t)h * kThreads;
-      if (len[h] < 0) continue;
-      if (len[h] <= kShortMax) {
+      if (!(sl[h] & (1u << 30))) continue;
+      const int st = (int)(sl[h] & 0xFFFu);
+      const uint32_t len = (sl[h] >> 12) & 0x3FFFu;
+      if (len <= (uint32_t)kShortMax) {
         uint32_t ids[kCacheMaxIds];
-        const uint32_t cnt = K[h].slot != kNone ? cache_resolve(a.C, K[h], ea[h], eb[h], ids) : 0u;
+        const uint32_t cnt = (sl[h] >> 31) ? cache_resolve(a.C, K[h], len, ea[h], eb[h], ids) : 0u;
         if (cnt) {
-          for (uint32_t q = 0; q < cnt; ++q) S.sym[st[h] + q] = ids[q];
+          for (uint32_t q = 0; q < cnt; ++q) S.sym[st + q] = ids[q];
           S.span_cnt[j] = cnt;
         } else {
-          S.span_cnt[j] = kMissMark | (uint32_t)len[h];
+          S.span_cnt[j] = kMissMark | len;
           ++my_misses;
         }
       } else {
@@ -1497,6 +1513,9 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
     if (a.def_n) a.def_n[c] = defer ? n_def : 0u;
   }
 
+  // The chunk's first document again, for the document offsets at the end.
+  const int64_t k_first_end = ldg_fresh(a.first_doc + c);
+
   // Ids of short pre-tokens to the chunk's stage region, each thread its own
   // run, in output order without the long pre-tokens' ids. A deferred miss
   // leaves its reserved range to k_misses and gets a record
@@ -1532,9 +1551,8 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
   // Offsets of the documents that start in this chunk, relative to the
   // chunk's first id (k_compact adds the chunk's offset).
   {
-    const bool more = d_more < c0 + kChunk;
-    for (int64_t k = k_first + tid; k <= a.n_docs; k += kThreads) {
-      const int64_t d = k == k_first + tid ? d_mine : a.doc_offsets[k];
+    for (int64_t k = k_first_end + tid; k <= a.n_docs; k += kThreads) {
+      const int64_t d = k == k_first_end + tid ? c0 + d_rel : a.doc_offsets[k];
       if (d >= c0 + kChunk) break;
       if (d >= c0) {
       // the first pre-token starting at or after d: those before d's 16-byte
