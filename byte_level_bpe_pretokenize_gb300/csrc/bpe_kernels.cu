@@ -1544,7 +1544,13 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
         ++slot;
         continue;
       }
-      for (uint32_t q = 0; q < cnt; ++q) stage[o + q] = S.sym[st + q];
+      if (cnt <= (uint32_t)kCacheMaxIds) {  // a cache hit: at most three ids, without a loop
+#pragma unroll
+        for (uint32_t q = 0; q < (uint32_t)kCacheMaxIds; ++q)
+          if (q < cnt) stage[o + q] = S.sym[st + q];
+      } else {
+        for (uint32_t q = 0; q < cnt; ++q) stage[o + q] = S.sym[st + q];
+      }
     }
   }
 
