@@ -178,6 +178,44 @@ __device__ __forceinline__ uint32_t lookup_rank(const Tables& T, uint32_t a, uin
   return lookup_pair(T, a, b, &nw);
 }
 
+// The rest of lookup_pair once the home bucket {u, v} of (a, b) is loaded.
+__device__ __forceinline__ uint32_t lookup_pair_from(const Tables& T, uint32_t a, uint32_t b, uint32_t bucket, uint4 u,
+                                                     uint4 v, uint32_t* nw) {
+  for (uint32_t probe = 0; probe <= T.hmask; ++probe) {
+    if (u.x == a && u.y == b) {
+      *nw = u.w;
+      return u.z;
+    }
+    if (v.x == a && v.y == b) {
+      *nw = v.w;
+      return v.z;
+    }
+    if (u.x == kEmptySlot || v.x == kEmptySlot) return kInf;
+    bucket = (bucket + 1) & T.hmask;
+    u = __ldg(T.ht + 2ull * bucket);
+    v = __ldg(T.ht + 2ull * bucket + 1);
+  }
+  return kInf;
+}
+
+// Two pair lookups with both home buckets in flight together; a pair with
+// a == kNone is skipped (rank kInf).
+__device__ __forceinline__ void lookup_pair2(const Tables& T, uint32_t a1, uint32_t b1, uint32_t a2, uint32_t b2,
+                                             uint32_t* r1, uint32_t* w1, uint32_t* r2, uint32_t* w2) {
+  const uint32_t k1 = pair_hash(a1, b1) & T.hmask, k2 = pair_hash(a2, b2) & T.hmask;
+  uint4 u1 = make_uint4(0, 0, 0, 0), v1 = u1, u2 = u1, v2 = u1;
+  if (a1 != kNone) {
+    u1 = __ldg(T.ht + 2ull * k1);
+    v1 = __ldg(T.ht + 2ull * k1 + 1);
+  }
+  if (a2 != kNone) {
+    u2 = __ldg(T.ht + 2ull * k2);
+    v2 = __ldg(T.ht + 2ull * k2 + 1);
+  }
+  *r1 = a1 != kNone ? lookup_pair_from(T, a1, b1, k1, u1, v1, w1) : kInf;
+  *r2 = a2 != kNone ? lookup_pair_from(T, a2, b2, k2, u2, v2, w2) : kInf;
+}
+
 __device__ __forceinline__ int cp_class(uint32_t cp) {
   uint32_t blk = kClassL1[cp >> 8];
   uint32_t w = kClassL2[blk * 16 + ((cp & 255) >> 4)];
@@ -1304,7 +1342,9 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
         uint32_t ids[kCacheMaxIds];
         const uint32_t cnt = (sl[h] >> 31) ? cache_resolve(a.C, K[h], len, ea[h], eb[h], ids) : 0u;
         if (cnt) {
-          for (uint32_t q = 0; q < cnt; ++q) S.sym[st + q] = ids[q];
+#pragma unroll
+          for (uint32_t q = 0; q < (uint32_t)kCacheMaxIds; ++q)
+            if (q < cnt) S.sym[st + q] = ids[q];
           S.span_cnt[j] = cnt;
         } else {
           S.span_cnt[j] = kMissMark | len;
@@ -1579,18 +1619,75 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
 // Cache misses that k_encode handed over, merged across the whole GPU: a
 // queue entry (chunk << 8 | slot) names a record {offset, start | reserved <<
 // 12 | stage offset << 19, ids}, reserved = the miss's byte length. A warp
-// takes 32 entries at a time, one per lane, and merges them in rounds:
-// groups of 4 lanes take misses of up to 8 bytes while at least 8 are left,
-// groups of 8 the rest of those up to 16 bytes, the whole warp each longer
-// one (merge_group). Each writes its ids into its reserved stage range, the
+// takes 32 entries at a time, one per lane. A lane merges its own miss of up
+// to 8 bytes (merge_thread); then, in rounds, groups of 8 lanes take the
+// misses of 9 to 16 bytes and the whole warp each longer one (merge_group). Each writes its ids into its reserved stage range, the
 // count into its record, and gives the unused part of the reservation back to
 // the chunk's count.
-constexpr int kMissBlocksPerSm = 6;  // resident at once (40 registers a thread)
+// One thread merges a pre-token of n <= 8 bytes: symbols, pair ranks and
+// merged ids in its own column of shared memory (x[i * kThreads], so the
+// threads of a warp use distinct banks). A step takes the lowest rank,
+// replaces its occurrences left to right without overlap while compacting,
+// and looks up again only the pairs next to a merged symbol, two at a time.
+// The final ids go to out[0 .. count).
+constexpr int kTinyMax = 8;
+struct TinyScratch {
+  uint32_t sy[kTinyMax * kThreads], rk[kTinyMax * kThreads], nw[kTinyMax * kThreads];
+};
+
+__device__ uint32_t merge_thread(TinyScratch& Z, const uint8_t* src, uint32_t n, const Tables& T,
+                                 const int32_t* byte_id, uint32_t* out) {
+  uint32_t* sy = Z.sy + threadIdx.x;
+  uint32_t* rk = Z.rk + threadIdx.x;
+  uint32_t* nw = Z.nw + threadIdx.x;
+  for (uint32_t i = 0; i < n; ++i) sy[i * kThreads] = (uint32_t)byte_id[src[i]];
+  uint32_t redo = n > 1 ? (1u << (n - 1)) - 1u : 0u;  // pairs to look up
+  for (;;) {
+    while (redo) {
+      const uint32_t p1 = __ffs(redo) - 1;
+      redo &= redo - 1;
+      const uint32_t p2 = redo ? __ffs(redo) - 1 : kNone;
+      redo &= redo - 1;
+      uint32_t r1, w1, r2 = kInf, w2 = 0;
+      lookup_pair2(T, sy[p1 * kThreads], sy[(p1 + 1) * kThreads], p2 != kNone ? sy[p2 * kThreads] : kNone,
+                   p2 != kNone ? sy[(p2 + 1) * kThreads] : 0u, &r1, &w1, &r2, &w2);
+      rk[p1 * kThreads] = r1;
+      nw[p1 * kThreads] = w1;
+      if (p2 != kNone) {
+        rk[p2 * kThreads] = r2;
+        nw[p2 * kThreads] = w2;
+      }
+    }
+    uint32_t best = kInf;
+    for (uint32_t i = 0; i + 1 < n; ++i) best = min(best, rk[i * kThreads]);
+    if (best == kInf) break;
+    uint32_t m = 0;
+    for (uint32_t i = 0; i < n; ++m) {
+      if (i + 1 < n && rk[i * kThreads] == best) {
+        sy[m * kThreads] = nw[i * kThreads];
+        redo |= (1u << m) | (m ? 1u << (m - 1) : 0u);  // the merged symbol's pairs
+        i += 2;
+      } else {
+        sy[m * kThreads] = sy[i * kThreads];
+        rk[m * kThreads] = rk[i * kThreads];
+        nw[m * kThreads] = nw[i * kThreads];
+        i += 1;
+      }
+    }
+    n = m;
+    redo &= n > 1 ? (1u << (n - 1)) - 1u : 0u;
+  }
+  for (uint32_t i = 0; i < n; ++i) out[i] = sy[i * kThreads];
+  return n;
+}
+
+constexpr int kMissBlocksPerSm = 5;  // resident at once (48 registers a thread)
 __global__ void __launch_bounds__(kThreads, kMissBlocksPerSm) k_misses(const uint8_t* bytes, const uint64_t* queue,
                                                                        const DevSmall* small, uint32_t* def_rec,
                                                                        uint32_t* stage, uint64_t* chunk_meta,
                                                                        Tables T) {
   __shared__ GroupScratch grp[kThreads / 32];
+  __shared__ TinyScratch tiny;
   __shared__ int32_t byte_id[256];
   for (int i = threadIdx.x; i < 256; i += kThreads) byte_id[i] = T.byte_id[i];
   __syncthreads();
@@ -1628,9 +1725,14 @@ __global__ void __launch_bounds__(kThreads, kMissBlocksPerSm) k_misses(const uin
         atomicAdd(reinterpret_cast<unsigned long long*>(chunk_meta + c), 0ull - (unsigned long long)(n - cnt));
       }
     };
-    while (__popc(m4) >= 8)
-      round(&m4, [&](const uint8_t* src, uint32_t n, uint32_t* out) { return merge_group<4>(W, src, n, T, byte_id, out); }, 4);
-    m8 |= m4;
+    if ((m4 >> lane) & 1u) {  // up to 8 bytes: each lane its own
+      const uint64_t c = e >> 8;
+      const uint32_t cnt = merge_thread(tiny, bytes + c * kChunk + (w & 0xFFFu), len, T, byte_id,
+                                        stage + c * kStage + (w >> 19));
+      def_rec[(c * kMaxDefer + (e & 0xFFu)) * 3 + 2] = cnt;
+      atomicAdd(reinterpret_cast<unsigned long long*>(chunk_meta + c), 0ull - (unsigned long long)(len - cnt));
+    }
+    __syncwarp();
     while (m8)
       round(&m8, [&](const uint8_t* src, uint32_t n, uint32_t* out) { return merge_group<8>(W, src, n, T, byte_id, out); }, 8);
     while (m32)
