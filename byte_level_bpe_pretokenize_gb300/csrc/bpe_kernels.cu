@@ -785,10 +785,10 @@ __device__ void load_encode_window(SplitSmem& S, const uint8_t* bytes, int64_t n
 
 // Start bits of the split kernel's chunk: thread t takes window positions
 // [kHalo + 32 t, + 32), one start bit word (the encode kernel takes its
-// margin's start bits from the next chunk's output).
+// margin's start bits from the next chunk's output). Each thread stores its
+// own word afterwards, so no barrier follows.
 __device__ void compute_start_bits(SplitWin& S) {
   S.startbits[threadIdx.x] = start_mask32(S, kHalo + 32 * (int)threadIdx.x);
-  cta_sync();
 }
 
 // ----------------------------------------------------------- block helpers --
@@ -804,6 +804,9 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
 }
 
 // Exclusive scan over the CTA; *total gets the sum. Uses red[0..kThreads/32].
+// SYNC_AFTER = false leaves out the closing barrier that lets red be written
+// again: for callers that pass another barrier before their next use of red.
+template <bool SYNC_AFTER = true>
 __device__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t incl = warp_incl_scan(v);
@@ -818,12 +821,13 @@ __device__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total) 
   cta_sync();
   uint32_t r = red[warp] + incl - v;
   *total = red[kThreads / 32];
-  cta_sync();
+  if (SYNC_AFTER) cta_sync();
   return r;
 }
 
 // Two exclusive scans over the CTA with one set of barriers; uses
-// red[0 .. 2 (kThreads/32 + 1)).
+// red[0 .. 2 (kThreads/32 + 1)). The caller passes another barrier before
+// its next use of red.
 __device__ void block_excl_scan2(uint32_t v, uint32_t u, uint32_t* red, uint32_t* ev, uint32_t* eu, uint32_t* tv,
                                  uint32_t* tu) {
   constexpr int kW = kThreads / 32;
@@ -851,7 +855,6 @@ __device__ void block_excl_scan2(uint32_t v, uint32_t u, uint32_t* red, uint32_t
   *eu = red[kW + 1 + warp] + iu - u;
   *tv = red[kW];
   *tu = red[2 * kW + 1];
-  cta_sync();
 }
 
 __device__ uint32_t block_min(uint32_t v, uint32_t* red) {
@@ -1257,7 +1260,7 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
   {
     const uint32_t bits = (S.startbits[tid >> 1] >> ((tid & 1) * 16)) & 0xFFFFu;
     uint32_t total;
-    uint32_t pos = block_excl_scan(__popc(bits), S.red, &total);
+    uint32_t pos = block_excl_scan<false>(__popc(bits), S.red, &total);
     S.grp_pos[tid] = (uint16_t)pos;
     uint32_t b = bits;
     while (b) {
