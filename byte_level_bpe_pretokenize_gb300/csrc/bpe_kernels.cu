@@ -803,31 +803,32 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
   return v;
 }
 
-// Exclusive scan over the CTA; *total gets the sum. Uses red[0..kThreads/32].
-// SYNC_AFTER = false leaves out the closing barrier that lets red be written
-// again: for callers that pass another barrier before their next use of red.
+// Exclusive scan over the CTA; *total gets the sum. One barrier: each warp
+// posts its total to red[0..kThreads/32) and every thread adds up the totals
+// of the warps before its own. SYNC_AFTER = false leaves out the closing
+// barrier that lets red be written again: for callers that pass another
+// barrier before their next use of red.
 template <bool SYNC_AFTER = true>
 __device__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t incl = warp_incl_scan(v);
+  const uint32_t incl = warp_incl_scan(v);
   if (lane == 31) red[warp] = incl;
   cta_sync();
-  if (warp == 0) {
-    uint32_t x = lane < kThreads / 32 ? red[lane] : 0;
-    uint32_t xi = warp_incl_scan(x);
-    if (lane < kThreads / 32) red[lane] = xi - x;
-    if (lane == kThreads / 32 - 1) red[kThreads / 32] = xi;
+  uint32_t before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const uint32_t x = red[w];
+    before += w < warp ? x : 0u;
+    all += x;
   }
-  cta_sync();
-  uint32_t r = red[warp] + incl - v;
-  *total = red[kThreads / 32];
+  *total = all;
   if (SYNC_AFTER) cta_sync();
-  return r;
+  return before + incl - v;
 }
 
-// Two exclusive scans over the CTA with one set of barriers; uses
-// red[0 .. 2 (kThreads/32 + 1)). The caller passes another barrier before
-// its next use of red.
+// Two exclusive scans over the CTA with one barrier; uses
+// red[0 .. 2 kThreads/32). The caller passes another barrier before its next
+// use of red.
 __device__ void block_excl_scan2(uint32_t v, uint32_t u, uint32_t* red, uint32_t* ev, uint32_t* eu, uint32_t* tv,
                                  uint32_t* tu) {
   constexpr int kW = kThreads / 32;
@@ -835,26 +836,22 @@ __device__ void block_excl_scan2(uint32_t v, uint32_t u, uint32_t* red, uint32_t
   const uint32_t iv = warp_incl_scan(v), iu = warp_incl_scan(u);
   if (lane == 31) {
     red[warp] = iv;
-    red[kW + 1 + warp] = iu;
+    red[kW + warp] = iu;
   }
   cta_sync();
-  if (warp == 0) {
-    const uint32_t x = lane < kW ? red[lane] : 0, y = lane < kW ? red[kW + 1 + lane] : 0;
-    const uint32_t xi = warp_incl_scan(x), yi = warp_incl_scan(y);
-    if (lane < kW) {
-      red[lane] = xi - x;
-      red[kW + 1 + lane] = yi - y;
-    }
-    if (lane == kW - 1) {
-      red[kW] = xi;
-      red[2 * kW + 1] = yi;
-    }
+  uint32_t bv = 0, bu = 0, av = 0, au = 0;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) {
+    const uint32_t x = red[w], y = red[kW + w];
+    bv += w < warp ? x : 0u;
+    bu += w < warp ? y : 0u;
+    av += x;
+    au += y;
   }
-  cta_sync();
-  *ev = red[warp] + iv - v;
-  *eu = red[kW + 1 + warp] + iu - u;
-  *tv = red[kW];
-  *tu = red[2 * kW + 1];
+  *ev = bv + iv - v;
+  *eu = bu + iu - u;
+  *tv = av;
+  *tu = au;
 }
 
 __device__ uint32_t block_min(uint32_t v, uint32_t* red) {
