@@ -429,7 +429,6 @@ struct __align__(16) WindowSmem {
   uint32_t outbits[kWords + 2];   // byte belongs to no document
   uint32_t startbits[(CHUNK + AFTER) / 32];
   int64_t chunk;
-  int more_docs;  // more documents start in the window than one per thread
 };
 
 // The encode kernel's window: a chunk plus the margin.
@@ -678,6 +677,15 @@ __device__ void load_window(SS& S, const uint8_t* bytes, int64_t n_bytes, const 
                             int64_t n_docs, int64_t c0, int64_t first_doc) {
   const int tid = threadIdx.x;
   const int64_t w0 = c0 - kHalo, w_end = w0 + SS::kLen;
+  // Positions relative to the window fit in 32 bits: the input's start and
+  // end and the first and last document offsets, clamped to [-1, kBits]
+  // (kBits: every position the bit masks hold).
+  constexpr int kBits = (SS::kWords + 2) * 32;
+  auto rel = [&](int64_t x) -> int {
+    const int64_t r = x - w0;
+    return r < -1 ? -1 : (r > kBits ? kBits : (int)r);
+  };
+  const int r_0 = rel(0), r_n = rel(n_bytes);  // window bytes [r_0, r_n) exist
   // Every load is issued before the first barrier: the bytes (asynchronous
   // 16-byte copies when the input is 16-byte aligned, window offsets being
   // multiples of 16; bytes otherwise), the first and last document offsets,
@@ -685,12 +693,11 @@ __device__ void load_window(SS& S, const uint8_t* bytes, int64_t n_bytes, const 
   // thread; more only when documents are tiny).
   const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 15u) == 0;
   for (int i = tid * 16; i < SS::kLen; i += kThreads * 16) {
-    const int64_t p = w0 + i;
-    if (aligned && p >= 0 && p + 16 <= n_bytes) {
-      cp_async16(S.win + i, bytes + p);
+    if (aligned && i >= r_0 && i + 16 <= r_n) {
+      cp_async16(S.win + i, bytes + (w0 + i));
     } else {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) S.win[i + k] = (p + k >= 0 && p + k < n_bytes) ? bytes[p + k] : 0;
+      for (int k = 0; k < 16; ++k) S.win[i + k] = (i + k >= r_0 && i + k < r_n) ? bytes[w0 + i + k] : 0;
     }
   }
   int64_t d_first = __ldg(doc_offsets), d_last = __ldg(doc_offsets + n_docs);
@@ -699,18 +706,21 @@ __device__ void load_window(SS& S, const uint8_t* bytes, int64_t n_bytes, const 
   if (k_lo < 0) k_lo = 0;
   const int64_t o_before = k_lo > 0 ? __ldg(doc_offsets + k_lo - 1) : INT64_MIN;
   const int64_t o_mine = k_lo + tid <= n_docs ? __ldg(doc_offsets + k_lo + tid) : INT64_MAX;
+  // the last of those (every thread reads it: no barrier waits on the load)
+  const int64_t o_last =
+      k_lo + kThreads - 1 <= n_docs ? __ldg(doc_offsets + k_lo + kThreads - 1) : INT64_MAX;
   for (int i = tid; i < SS::kWords + 2; i += kThreads) S.docbits[i] = 0;
-  if (tid == kThreads - 1) S.more_docs = o_mine < w_end;
   cp_async_wait_all();
   cta_sync();
   d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
   d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
+  const int r_first = rel(d_first), r_last = rel(d_last);
   for (int wi = tid; wi < SS::kWords + 2; wi += kThreads) {
     uint32_t word = 0;
-    const int64_t p = w0 + (int64_t)wi * 32;
-    if (p < d_first || p + 32 > d_last) {
+    const int p = wi * 32;
+    if (p < r_first || p + 32 > r_last) {
       for (int k = 0; k < 32; ++k)
-        if (p + k < d_first || p + k >= d_last) word |= 1u << k;
+        if (p + k < r_first || p + k >= r_last) word |= 1u << k;
     }
     S.outbits[wi] = word;
   }
@@ -719,7 +729,7 @@ __device__ void load_window(SS& S, const uint8_t* bytes, int64_t n_bytes, const 
     const int i = (int)(o_mine - w0);
     atomicOr(&S.docbits[i >> 5], 1u << (i & 31));
   }
-  if (S.more_docs && o_mine < w_end) {  // tiny documents: more than kThreads - 32 start in the window
+  if (o_last < w_end && o_mine < w_end) {  // tiny documents: more than kThreads - 32 start in the window
     for (int64_t k = k_lo + tid + kThreads; k <= n_docs; k += kThreads) {
       const int64_t o = doc_offsets[k];
       if (o >= w_end) break;
@@ -748,17 +758,24 @@ __device__ void load_encode_window(SplitSmem& S, const uint8_t* bytes, int64_t n
                                    int64_t n_docs, const uint32_t* start_bits, int64_t c0) {
   const int tid = threadIdx.x;
   const int64_t w0 = c0 - kHalo;
+  // Window-relative positions in 32 bits, clamped to [-1, kBits] (as in
+  // load_window).
+  constexpr int kBits = (kWinWords + 2) * 32;
+  auto rel = [&](int64_t x) -> int {
+    const int64_t r = x - w0;
+    return r < -1 ? -1 : (r > kBits ? kBits : (int)r);
+  };
+  const int r_0 = rel(0), r_n = rel(n_bytes);  // window bytes [r_0, r_n) exist
   // Asynchronous 16-byte copies when the input is 16-byte aligned (window
   // offsets are multiples of 16), bytes otherwise; the start bits as 4-byte
   // copies.
   const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 15u) == 0;
   for (int i = tid * 16; i < kWin; i += kThreads * 16) {
-    const int64_t p = w0 + i;
-    if (aligned && p >= 0 && p + 16 <= n_bytes) {
-      cp_async16(S.win + i, bytes + p);
+    if (aligned && i >= r_0 && i + 16 <= r_n) {
+      cp_async16(S.win + i, bytes + (w0 + i));
     } else {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) S.win[i + k] = (p + k >= 0 && p + k < n_bytes) ? bytes[p + k] : 0;
+      for (int k = 0; k < 16; ++k) S.win[i + k] = (i + k >= r_0 && i + k < r_n) ? bytes[w0 + i + k] : 0;
     }
   }
   const int64_t n_words = (n_bytes + 31) / 32;
@@ -770,12 +787,13 @@ __device__ void load_encode_window(SplitSmem& S, const uint8_t* bytes, int64_t n
   int64_t d_first = __ldg(doc_offsets), d_last = __ldg(doc_offsets + n_docs);
   d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
   d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
+  const int r_first = rel(d_first), r_last = rel(d_last);
   for (int wi = tid; wi < kWinWords + 2; wi += kThreads) {
     uint32_t word = 0;
-    const int64_t p = w0 + (int64_t)wi * 32;
-    if (p < d_first || p + 32 > d_last) {
+    const int p = wi * 32;
+    if (p < r_first || p + 32 > r_last) {
       for (int k = 0; k < 32; ++k)
-        if (p + k < d_first || p + k >= d_last) word |= 1u << k;
+        if (p + k < r_first || p + k >= r_last) word |= 1u << k;
     }
     S.outbits[wi] = word;
   }
