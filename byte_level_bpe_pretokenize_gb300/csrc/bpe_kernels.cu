@@ -2016,6 +2016,13 @@ __global__ void k_offsets_shift(int64_t* x, int64_t n, int64_t delta) {
     x[i] += delta;
 }
 
+// The call's token count into page-locked host memory, written by the GPU:
+// a copy on the encode stream would queue behind the large downloads on the
+// same copy engine and hold up the next slice's kernels.
+__global__ void k_total_to_host(const DevSmall* small, int64_t* h_dst) {
+  if (threadIdx.x == 0) *reinterpret_cast<volatile int64_t*>(h_dst) = small->total;
+}
+
 // ---------------------------------------------------------------- decoding --
 
 constexpr int kScanBlock = 1024;
@@ -2156,7 +2163,7 @@ struct bpe_handle {
   cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
   // bpe_encode_batch_host: kHostSlots slots of device buffers, copy streams,
   // events
-  static constexpr int kHostSlots = 3;
+  static constexpr int kHostSlots = 4;
   struct HostSlot {
     uint8_t* bytes = nullptr;
     int64_t* offs = nullptr;
@@ -2167,6 +2174,7 @@ struct bpe_handle {
   int64_t slot_bytes = 0, slot_docs = 0;  // capacity of each slot
   cudaStream_t s_h2d = nullptr, s_d2h = nullptr;
   int64_t* h_totals = nullptr;  // pinned, one per slice
+  int64_t* d_totals = nullptr;  // the same memory as the device addresses it
   int64_t h_totals_cap = 0;
 };
 
@@ -2685,12 +2693,18 @@ int bpe_encode_batch_host(bpe_handle* h, const uint8_t* h_bytes, int64_t n_bytes
     return fail(BPE_ERR_BAD_INPUT, "bpe_encode_batch_host: first or last document offset outside the buffer");
   DeviceGuard g(h->device);
   cudaStream_t cs = (cudaStream_t)stream;
-  // Slices of whole documents, about (b_last - b_first) / 12 bytes each but at
-  // least 4 MiB; a document longer than that is a slice of its own.
-  const int64_t target = std::max<int64_t>(int64_t(4) << 20, (b_last - b_first + 11) / 12);
+  // Slices of whole documents, about T = (b_last - b_first) / 12 bytes each.
+  // The first three ramp up (T/8, T/4, T/2) and the last ones halve down to
+  // T/8, so the first encode starts, and the last download ends, soon after
+  // the copies begin and end. No slice is asked for less than 4 MiB; a
+  // document longer than its slice is a slice of its own.
+  const int64_t T = std::max<int64_t>(int64_t(4) << 20, (b_last - b_first + 11) / 12);
   std::vector<int64_t> cut{0};
   while (cut.back() < n_docs) {
-    const int64_t d0 = cut.back(), want = h_doc_offsets[d0] + target;
+    const int64_t j = (int64_t)cut.size() - 1, d0 = cut.back(), rest = b_last - h_doc_offsets[d0];
+    int64_t target = j < 3 ? T >> (3 - j) : (rest > 2 * T ? T : (rest > T / 4 ? rest / 2 : rest));
+    target = std::max<int64_t>(target, int64_t(4) << 20);
+    const int64_t want = h_doc_offsets[d0] + target;
     int64_t lo = d0 + 1, hi = n_docs;  // last doc boundary at or below want, at least one document
     while (lo < hi) {
       const int64_t mid = (lo + hi + 1) / 2;
@@ -2743,6 +2757,7 @@ int bpe_encode_batch_host(bpe_handle* h, const uint8_t* h_bytes, int64_t n_bytes
     h->h_totals = nullptr;
     h->h_totals_cap = 0;
     CK(cudaMallocHost(&h->h_totals, (size_t)n_slices * sizeof(int64_t)));
+    CK(cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->d_totals), h->h_totals, 0));
     h->h_totals_cap = n_slices;
   }
   int rc = ensure_ws(h, ws_sizes(h->slot_bytes).total);
@@ -2769,7 +2784,8 @@ int bpe_encode_batch_host(bpe_handle* h, const uint8_t* h_bytes, int64_t n_bytes
     int r = launch_encode(h, ws_carve(static_cast<unsigned char*>(h->d_ws), nb), sl.bytes, nb, sl.offs, nd, sl.ids,
                           nb, sl.out_offs, cs, nullptr, nullptr);
     if (r) return r;
-    CK(cudaMemcpyAsync(h->h_totals + j, &h->d_small->total, sizeof(int64_t), cudaMemcpyDeviceToHost, cs));
+    k_total_to_host<<<1, 32, 0, cs>>>(h->d_small, h->d_totals + j);
+    CK(cudaGetLastError());
     CK(cudaEventRecord(sl.done, cs));
     return BPE_OK;
   };

@@ -120,21 +120,23 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
  * (cudaMallocHost) for overlap; pageable memory works but copies serialise.
  *
  * Pipeline:
- *   - The batch is cut on document boundaries into about 12 slices of at
- *     least 4 MiB each; a longer document is a slice of its own.
+ *   - The batch is cut on document boundaries into slices of about 1/12 of
+ *     it (at least 4 MiB); the first and last few are smaller, so encoding
+ *     starts and the last copy-out ends soon after the copies start and end.
+ *     A document longer than its slice is a slice of its own.
  *   - Slice j's bytes and offsets are copied in on a copy stream of the handle.
  *   - Slice j is encoded on `stream`.
  *   - Slice j-1's ids and offsets are copied out on a second copy stream.
- *   - Three slots of device buffers rotate, so the next slice's upload does
- *     not wait on the previous slice's download.
+ *   - Four slots of device buffers rotate, so a slice's upload does not wait
+ *     on the download of the slice before.
  *
- * Each slice's token count is read on the host (through page-locked memory)
- * before its ids are copied out, so exactly the ids are moved. The offsets
- * are made absolute on the device.
+ * Each slice's token count is written by a kernel into page-locked host
+ * memory and read on the host before its ids are copied out, so exactly the
+ * ids are moved. The offsets are made absolute on the device.
  *
  * Results equal those of bpe_encode_batch on the same batch.
  *
- * Memory: the handle keeps three slots of (slice bytes + 4 B per slice byte +
+ * Memory: the handle keeps four slots of (slice bytes + 4 B per slice byte +
  * 16 B per slice document) and bpe_encode_batch's workspace for one slice.
  * It grows the first time a larger slice is seen.
  *
