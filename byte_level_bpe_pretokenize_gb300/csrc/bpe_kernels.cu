@@ -155,10 +155,19 @@ struct DevSmall {
 // ------------------------------------------------------------ small helpers --
 
 // Rank of the pair (a, b), kInf if it is not a merge; *nw gets the merged id.
+// One 32-byte read-only load (a pair bucket or a word-cache entry; both
+// tables are 32-byte aligned) as a single 256-bit access.
+__device__ __forceinline__ void ldg32(const uint4* p, uint4& lo, uint4& hi) {
+  asm("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+      : "l"(p));
+}
+
 __device__ __forceinline__ uint32_t lookup_pair(const Tables& T, uint32_t a, uint32_t b, uint32_t* nw) {
   uint32_t bucket = pair_hash(a, b) & T.hmask;
   for (uint32_t probe = 0; probe <= T.hmask; ++probe) {
-    const uint4 u = __ldg(T.ht + 2ull * bucket), v = __ldg(T.ht + 2ull * bucket + 1);
+    uint4 u, v;
+    ldg32(T.ht + 2ull * bucket, u, v);
     if (u.x == a && u.y == b) {
       *nw = u.w;
       return u.z;
@@ -192,8 +201,7 @@ __device__ __forceinline__ uint32_t lookup_pair_from(const Tables& T, uint32_t a
     }
     if (u.x == kEmptySlot || v.x == kEmptySlot) return kInf;
     bucket = (bucket + 1) & T.hmask;
-    u = __ldg(T.ht + 2ull * bucket);
-    v = __ldg(T.ht + 2ull * bucket + 1);
+    ldg32(T.ht + 2ull * bucket, u, v);
   }
   return kInf;
 }
@@ -205,12 +213,10 @@ __device__ __forceinline__ void lookup_pair2(const Tables& T, uint32_t a1, uint3
   const uint32_t k1 = pair_hash(a1, b1) & T.hmask, k2 = pair_hash(a2, b2) & T.hmask;
   uint4 u1 = make_uint4(0, 0, 0, 0), v1 = u1, u2 = u1, v2 = u1;
   if (a1 != kNone) {
-    u1 = __ldg(T.ht + 2ull * k1);
-    v1 = __ldg(T.ht + 2ull * k1 + 1);
+    ldg32(T.ht + 2ull * k1, u1, v1);
   }
   if (a2 != kNone) {
-    u2 = __ldg(T.ht + 2ull * k2);
-    v2 = __ldg(T.ht + 2ull * k2 + 1);
+    ldg32(T.ht + 2ull * k2, u2, v2);
   }
   *r1 = a1 != kNone ? lookup_pair_from(T, a1, b1, k1, u1, v1, w1) : kInf;
   *r2 = a2 != kNone ? lookup_pair_from(T, a2, b2, k2, u2, v2, w2) : kInf;
@@ -1182,8 +1188,7 @@ __device__ __forceinline__ uint32_t cache_resolve(const Cache& C, const CacheKey
       return (eb.x >> 5) & 7u;
     }
     slot = ((slot == kNone ? cache_slot(K, len, C) : slot) + 1) & C.mask;
-    ea = __ldg(C.e + 2 * slot);
-    eb = __ldg(C.e + 2 * slot + 1);
+    ldg32(C.e + 2 * slot, ea, eb);
   }
   return 0;
 }
@@ -1344,8 +1349,7 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
         if (len <= kCacheMaxLen && a.C.enabled) {
           K[h] = cache_key_words(S, st, len);
           const uint32_t slot = cache_slot(K[h], (uint32_t)len, a.C);
-          ea[h] = __ldg(a.C.e + 2 * slot);
-          eb[h] = __ldg(a.C.e + 2 * slot + 1);
+          ldg32(a.C.e + 2 * slot, ea[h], eb[h]);
           sl[h] |= 1u << 31;
         }
       }
