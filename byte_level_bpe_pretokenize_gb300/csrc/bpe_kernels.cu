@@ -982,7 +982,7 @@ __device__ int merge_short(uint32_t* sym, uint32_t* rk, const uint8_t* src, int 
 template <int G>
 __device__ uint32_t merge_group(GroupScratch& W, const uint8_t* src, uint32_t n, const Tables& T,
                                 const int32_t* byte_id, uint32_t* out) {
-  static_assert(G == 4 || G == 8 || G == 32, "group of 4, 8 or 32 lanes");
+  static_assert(G == 4 || G == 8 || G == 16 || G == 32, "group of 4, 8, 16 or 32 lanes");
   const int lane = threadIdx.x & 31;
   const int g = lane & (G - 1);
   const int goff = lane & ~(G - 1);
@@ -1643,7 +1643,8 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
 // 12 | stage offset << 19, ids}, reserved = the miss's byte length. A warp
 // takes 32 entries at a time, one per lane. A lane merges its own miss of up
 // to 8 bytes (merge_thread); then, in rounds, groups of 8 lanes take the
-// misses of 9 to 16 bytes and the whole warp each longer one (merge_group). Each writes its ids into its reserved stage range, the
+// misses of 9 to 16 bytes, groups of 16 those of 17 to 32, and the whole warp
+// each longer one (merge_group). Each writes its ids into its reserved stage range, the
 // count into its record, and gives the unused part of the reservation back to
 // the chunk's count.
 // One thread merges a pre-token of n <= 8 bytes: symbols, pair ranks and
@@ -1727,7 +1728,8 @@ __global__ void __launch_bounds__(kThreads, kMissBlocksPerSm) k_misses(const uin
     const uint32_t len = (w >> 12) & 0x7Fu;  // 0: no entry
     uint32_t m4 = __ballot_sync(0xFFFFFFFFu, len != 0 && len <= 8u);
     uint32_t m8 = __ballot_sync(0xFFFFFFFFu, len > 8u && len <= (uint32_t)kCacheMaxLen);
-    uint32_t m32 = __ballot_sync(0xFFFFFFFFu, len > (uint32_t)kCacheMaxLen);
+    uint32_t m16 = __ballot_sync(0xFFFFFFFFu, len > (uint32_t)kCacheMaxLen && len <= 32u);
+    uint32_t m32 = __ballot_sync(0xFFFFFFFFu, len > 32u);
     // One round: group g of G lanes takes the g-th entry of *mask (none past
     // its end); the round's entries leave the mask.
     auto round = [&](uint32_t* mask, auto merge, int G) {
@@ -1757,6 +1759,8 @@ __global__ void __launch_bounds__(kThreads, kMissBlocksPerSm) k_misses(const uin
     __syncwarp();
     while (m8)
       round(&m8, [&](const uint8_t* src, uint32_t n, uint32_t* out) { return merge_group<8>(W, src, n, T, byte_id, out); }, 8);
+    while (m16)
+      round(&m16, [&](const uint8_t* src, uint32_t n, uint32_t* out) { return merge_group<16>(W, src, n, T, byte_id, out); }, 16);
     while (m32)
       round(&m32, [&](const uint8_t* src, uint32_t n, uint32_t* out) { return merge_group<32>(W, src, n, T, byte_id, out); }, 32);
   }
