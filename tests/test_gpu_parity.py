@@ -222,6 +222,29 @@ def test_non_identity_ids(bpe):
     bpe.bpe_destroy(h)
 
 
+@pytest.mark.parametrize("p_miss", [0.12, 0.15, 0.17, 0.19, 0.25])
+def test_miss_density_around_deferral_limit(bpe, p_miss):
+    # Common words (word-cache hits) mixed with random letter strings (misses)
+    # so that 4 KiB chunks hold from about 120 to about 200 misses: chunks
+    # on both sides of the 160 a chunk hands to the GPU-wide miss merge.
+    h, o = _pair(bpe, workloads.table(5))
+    rng = random.Random(int(p_miss * 1000))
+    common = [b" the", b" of", b" and", b" to", b" in", b" is", b" that", b" for", b" it", b" was"]
+    letters = b"bcdfghjklmnpqrstvwxz"
+    docs = []
+    for _ in range(16):
+        words = []
+        while sum(len(w) for w in words) < 4000:
+            if rng.random() < p_miss:
+                words.append(b" " + bytes(rng.choice(letters) for _ in range(rng.randint(4, 12))))
+            else:
+                words.append(rng.choice(common))
+        docs.append(b"".join(words))
+    data, off = batch(docs)
+    check(h, o, data, off, f"miss density {p_miss}")
+    bpe.bpe_destroy(h)
+
+
 @pytest.mark.parametrize("cfg", [2, 3, 4, 5])
 def test_workload_slices(bpe, cfg):
     h, o = _pair(bpe, workloads.table(cfg))
