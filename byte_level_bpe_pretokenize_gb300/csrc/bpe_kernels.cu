@@ -55,6 +55,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <type_traits>
 #include <unordered_set>
 #include <vector>
 
@@ -997,6 +998,9 @@ __device__ uint32_t merge_group(GroupScratch& W, const uint8_t* src, uint32_t n,
   ws[p0] = s0;
   ws[p1] = s1;
   __syncwarp();
+  // masks of the group's positions: 32 bits while they fit
+  using Mask = typename std::conditional<(2 * G <= 32), uint32_t, uint64_t>::type;
+  constexpr int kMaskBits = 8 * (int)sizeof(Mask);
   uint32_t w0 = 0, w1 = 0;
   uint32_t r0 = p0 + 1 < n ? lookup_pair(T, s0, ws[p0 + 1], &w0) : kInf;
   uint32_t r1 = p1 + 1 < n ? lookup_pair(T, s1, ws[p1 + 1], &w1) : kInf;
@@ -1010,31 +1014,31 @@ __device__ uint32_t merge_group(GroupScratch& W, const uint8_t* src, uint32_t n,
     const bool o0 = go && r0 == best, o1 = go && r1 == best;
     const uint32_t b0 = (__ballot_sync(0xFFFFFFFFu, o0) >> goff) & gbits;
     const uint32_t b1 = (__ballot_sync(0xFFFFFFFFu, o1) >> goff) & gbits;
-    const uint64_t M = (uint64_t)b0 | ((uint64_t)b1 << G);
+    const Mask M = (Mask)b0 | ((Mask)b1 << G);
     const uint32_t any = b0 | b1;
     const uint32_t nwb = __shfl_sync(0xFFFFFFFFu, o0 ? w0 : w1, goff + (any ? __ffs(any) - 1 : 0));
-    const uint64_t E = 0x5555555555555555ull;  // even positions
-    const uint64_t run_start = M & ~(M << 1);
-    const uint64_t even_runs = M & ~(M + (run_start & E));  // runs that start at an even position
-    const uint64_t take = (even_runs & E) | (M & ~even_runs & ~E);
-    const uint64_t valid = cnt >= 64 ? ~0ull : ((1ull << cnt) - 1ull);
-    const uint64_t keep = valid & ~(take << 1);
+    const Mask E = (Mask)0x5555555555555555ull;  // even positions
+    const Mask run_start = M & ~(M << 1);
+    const Mask even_runs = M & ~(M + (run_start & E));  // runs that start at an even position
+    const Mask take = (even_runs & E) | (M & ~even_runs & ~E);
+    const Mask valid = cnt >= (uint32_t)kMaskBits ? ~(Mask)0 : (((Mask)1 << cnt) - 1);
+    const Mask keep = valid & ~(take << 1);
     __syncwarp();  // every lane has read the scratch before it is rewritten
     if (go) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t p = h ? p1 : p0;
-        if ((keep >> p) & 1ull) {
-          const uint32_t ni = (uint32_t)__popcll(keep & ((1ull << p) - 1ull));
-          const bool tp = (take >> p) & 1ull;
+        if ((keep >> p) & 1) {
+          const uint32_t ni = (uint32_t)__popcll((uint64_t)(keep & (((Mask)1 << p) - 1)));
+          const bool tp = (take >> p) & 1;
           const uint32_t q = tp ? p + 2 : p + 1;  // next kept position
-          const bool tq = q < 64 && ((take >> q) & 1ull);
+          const bool tq = q < (uint32_t)kMaskBits && ((take >> q) & 1);
           ws[ni] = tp ? nwb : (h ? s1 : s0);
           wr[ni] = (tp || tq) ? kReprobe : (h ? r1 : r0);
           ww[ni] = h ? w1 : w0;
         }
       }
-      cnt = (uint32_t)__popcll(keep);
+      cnt = (uint32_t)__popcll((uint64_t)keep);
     }
     __syncwarp();
     if (go) {  // a finished group keeps its registers
