@@ -1262,7 +1262,9 @@ struct EncodeArgs {
 // Encodes chunk blockIdx.x without waiting on any other chunk: its ids go to
 // its stage region (short pre-tokens) or stay in the pool (long ones, listed
 // in a record), its count to chunk_meta, and its documents' offsets are
-// written relative to the chunk. k_chunk_scan and k_compact finish the call.
+// written relative to the chunk. Its cache misses either get reserved stage
+// ranges that k_misses fills, or are merged here. k_scan_tiles,
+// k_scan_tile_sums and k_compact finish the call.
 __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
@@ -1330,10 +1332,11 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
   const bool more = d_more < c0 + kChunk;
 
   // Short pre-tokens, one thread each, kProbeRound per round with their
-  // word-cache probes in flight together (a thread keeps only each probe's
-  // slot and entry; the key is read again from the window to compare). Hits
-  // finish here; misses are queued and merged next by lane groups, so a warp
-  // does not wait on the merge loop of a few of its lanes.
+  // word-cache probes in flight together (a thread keeps each probe's key
+  // words, entry and one word of start, length and flags; the slot is
+  // recomputed only if the probe goes past it). Hits finish here; misses are
+  // marked and counted, and handled next, so a warp does not wait on the
+  // merge loop of a few of its lanes.
   uint32_t my_misses = 0;
   for (uint32_t j0 = tid; j0 < n_spans; j0 += kProbeRound * kThreads) {
     // per probe: start | length << 12 | present << 30 | probed << 31 (a
@@ -2400,7 +2403,7 @@ std::mutex g_noalloc_mu;
 unsigned char* g_noalloc_base[kNoAllocMaxDevices] = {};
 
 // Once per device, with that device current: the scratch address and the
-// shared-memory opt-in of the two kernels. Later calls only read the table.
+// encode kernel's shared-memory opt-in. Later calls only read the table.
 int noalloc_setup(int dev, unsigned char** base) {
   if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch_noalloc: device ordinal above 63");
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
