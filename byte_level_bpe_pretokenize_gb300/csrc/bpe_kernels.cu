@@ -1838,7 +1838,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_tile_sums(uint64_t* tile_
 // its documents' offsets made absolute. Ids past out_capacity are not written.
 constexpr int kCompactWarps = 8;
 
-__global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const uint32_t* stage, const int32_t* pool,
+__global__ void __launch_bounds__(32 * kCompactWarps, 8) k_compact(const uint32_t* stage, const int32_t* pool,
                                                                 const uint64_t* chunk_meta, const uint64_t* chunk_off,
                                                                 const uint64_t* tile_off, const uint32_t* rec,
                                                                 const uint32_t* def_n, const uint32_t* def_rec,
