@@ -1269,7 +1269,6 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
-  for (int i = tid; i < 256; i += kThreads) S.byte_id[i] = a.T.byte_id[i];
   const int64_t c = blockIdx.x;
   const int64_t c0 = c * kChunk;
   // The first document starting at or after c0 (its load overlaps the
@@ -1402,6 +1401,9 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
   uint32_t q_base = 0;  // thread 0: the chunk's queue entries, needed only once its ids are written
   if (defer && tid == 0 && n_def) q_base = atomicAdd(&a.small->q_n, n_def);
   if (!defer) {
+    // the byte -> symbol map, for the merges (loaded only when a chunk merges)
+    for (int i = tid; i < 256; i += kThreads) S.byte_id[i] = a.T.byte_id[i];
+    cta_sync();
     for (uint32_t j = run0; j < run1; ++j) {
       const uint32_t v = S.span_cnt[j];
       if (!(v & kMissMark)) continue;
@@ -1453,6 +1455,7 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
   // Long pre-tokens: the whole CTA, one at a time, in order.
   const uint32_t n_long = min(S.n_long, (uint32_t)kMaxLong);
   if (n_long > 0) {
+    for (int i = tid; i < 256; i += kThreads) S.byte_id[i] = a.T.byte_id[i];
     if (tid == 0 && n_long > 1) {  // sort the short list (insertion sort)
       for (uint32_t x = 1; x < n_long; ++x) {
         uint16_t v = S.long_list[x];
