@@ -1271,14 +1271,13 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
   const int tid = threadIdx.x;
   const int64_t c = blockIdx.x;
   const int64_t c0 = c * kChunk;
-  // The first document starting at or after c0 (its load overlaps the
-  // window's) and, ahead of their use at the end, the offsets of the
-  // kThreads documents from there on and of the last of them (more
-  // documents start in the chunk when it does).
-  const int64_t k_first = __ldg(a.first_doc + c);
+  // The documents starting in the chunk are k_first .. k_next - 1 (k_prep's
+  // first document of this chunk and of the next; the loads overlap the
+  // window's). Ahead of their use at the end, the offsets of the first
+  // kThreads of them, one per thread.
+  const int64_t k_first = __ldg(a.first_doc + c), k_next = __ldg(a.first_doc + c + 1);
   load_encode_window(S, a.bytes, a.n_bytes, a.doc_offsets, a.n_docs, a.start_bits, c0);
-  const int64_t d_mine = k_first + tid <= a.n_docs ? __ldg(a.doc_offsets + k_first + tid) : INT64_MAX;
-  const int64_t d_more = k_first + kThreads - 1 <= a.n_docs ? __ldg(a.doc_offsets + k_first + kThreads - 1) : INT64_MAX;
+  const int64_t d_mine = k_first + tid < k_next ? __ldg(a.doc_offsets + k_first + tid) : c0;
 
   // Pre-tokens starting in the chunk, in order. Thread t owns positions
   // [16 t, 16 t + 16) of the chunk.
@@ -1325,10 +1324,9 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
   cta_sync();
   const uint32_t n_spans = S.n_spans;
   const int last_end = S.last_end_rel;
-  // The document offsets have arrived by now: keep them relative to the
-  // chunk (-1 before it, kChunk from its end on) to spare registers.
-  const int d_rel = d_mine < c0 ? -1 : (d_mine >= c0 + kChunk ? kChunk : (int)(d_mine - c0));
-  const bool more = d_more < c0 + kChunk;
+  // The document offset has arrived by now: keep it relative to the chunk
+  // (-1 outside it, which only malformed offsets give) to spare registers.
+  const int d_rel = d_mine < c0 || d_mine >= c0 + kChunk ? -1 : (int)(d_mine - c0);
 
   // Short pre-tokens, one thread each, kProbeRound per round with their
   // word-cache probes in flight together (a thread keeps each probe's key
@@ -1585,8 +1583,8 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
     if (a.def_n) a.def_n[c] = defer ? n_def : 0u;
   }
 
-  // The chunk's first document again, for the document offsets at the end.
-  const int64_t k_first_end = ldg_fresh(a.first_doc + c);
+  // The chunk's documents again, for their offsets at the end.
+  const int64_t k_first_end = ldg_fresh(a.first_doc + c), k_next_end = ldg_fresh(a.first_doc + c + 1);
 
   // Ids of short pre-tokens to the chunk's stage region, each thread its own
   // run, in output order without the long pre-tokens' ids. A deferred miss
@@ -1629,10 +1627,9 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
   // Offsets of the documents that start in this chunk, relative to the
   // chunk's first id (k_compact adds the chunk's offset).
   {
-    for (int64_t k = k_first_end + tid; k <= a.n_docs; k += kThreads) {
-      const int64_t d = k == k_first_end + tid ? c0 + d_rel : a.doc_offsets[k];
-      if (d >= c0 + kChunk) break;
-      if (d >= c0) {
+    for (int64_t k = k_first_end + tid; k < k_next_end; k += kThreads) {
+      const int64_t d = k == k_first_end + tid ? (d_rel < 0 ? -1 : c0 + d_rel) : a.doc_offsets[k];
+      if (d >= c0 && d < c0 + kChunk) {
       // the first pre-token starting at or after d: those before d's 16-byte
       // group, plus the group's starts before d
         const int rel = (int)(d - c0), t = rel >> 4;
@@ -1643,7 +1640,6 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
           if (S.long_list[x] < r) o += S.long_cnt[x];
         a.out_offsets[k] = o;
       }
-      if (!more) break;
     }
   }
 }
