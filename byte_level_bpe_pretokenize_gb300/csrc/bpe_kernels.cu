@@ -711,7 +711,7 @@ __device__ void load_window(SS& S, const uint8_t* bytes, int64_t n_bytes, const 
   int64_t k_lo = first_doc - 32;
   if (k_lo > n_docs) k_lo = n_docs;
   if (k_lo < 0) k_lo = 0;
-  const int64_t o_before = k_lo > 0 ? __ldg(doc_offsets + k_lo - 1) : INT64_MIN;
+  const int64_t o_before = tid == 0 && k_lo > 0 ? __ldg(doc_offsets + k_lo - 1) : INT64_MIN;  // thread 0's test below
   const int64_t o_mine = k_lo + tid <= n_docs ? __ldg(doc_offsets + k_lo + tid) : INT64_MAX;
   // the last of those (every thread reads it: no barrier waits on the load)
   const int64_t o_last =
@@ -791,18 +791,21 @@ __device__ void load_encode_window(SplitSmem& S, const uint8_t* bytes, int64_t n
     if (gw < n_words) cp_async4(&S.startbits[w], start_bits + gw);
     else S.startbits[w] = 0u;
   }
-  int64_t d_first = __ldg(doc_offsets), d_last = __ldg(doc_offsets + n_docs);
-  d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
-  d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
-  const int r_first = rel(d_first), r_last = rel(d_last);
-  for (int wi = tid; wi < kWinWords + 2; wi += kThreads) {
+  // Which bytes lie outside every document: one word per thread, so only
+  // those threads read the first and last document offsets.
+  static_assert(kWinWords + 2 <= kThreads, "one out-of-document word per thread");
+  if (tid < kWinWords + 2) {
+    int64_t d_first = __ldg(doc_offsets), d_last = __ldg(doc_offsets + n_docs);
+    d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
+    d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
+    const int r_first = rel(d_first), r_last = rel(d_last);
     uint32_t word = 0;
-    const int p = wi * 32;
+    const int p = tid * 32;
     if (p < r_first || p + 32 > r_last) {
       for (int k = 0; k < 32; ++k)
         if (p + k < r_first || p + k >= r_last) word |= 1u << k;
     }
-    S.outbits[wi] = word;
+    S.outbits[tid] = word;
   }
   cp_async_wait_all();
   cta_sync();
