@@ -396,13 +396,6 @@ __device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// A 64-bit read-only global load issued where it stands (not merged with an
-// earlier load of the same word, whose register would then stay live).
-__device__ __forceinline__ int64_t ldg_fresh(const int64_t* p) {
-  int64_t v;
-  asm volatile("ld.global.nc.s64 %0, [%1];" : "=l"(v) : "l"(p));
-  return v;
-}
 
 // Bits [start, start + 32) of a shared bit array.
 __device__ __forceinline__ uint32_t bits32_at(const uint32_t* bits, int start) {
@@ -460,6 +453,7 @@ struct Smem : SplitSmem {
   int32_t byte_id[256];
   uint16_t long_list[kMaxLong];
   uint32_t long_cnt[kMaxLong];       // ids of each long pre-token, in long_list order
+  int64_t doc_k0, doc_k1;            // the documents starting in the chunk: [doc_k0, doc_k1)
   uint32_t red[2 * (kThreads / 32 + 1)];
   uint32_t carry[2];
   int64_t prefix;
@@ -1301,6 +1295,8 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
       S.n_miss = 0;
       S.n_miss_m = 0;
       S.n_def = 0;
+      S.doc_k0 = k_first;
+      S.doc_k1 = k_next;
       if (total == 0) {
         S.last_end = -1;
         S.last_end_rel = -1;
@@ -1586,8 +1582,9 @@ __global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArg
     if (a.def_n) a.def_n[c] = defer ? n_def : 0u;
   }
 
-  // The chunk's documents again, for their offsets at the end.
-  const int64_t k_first_end = ldg_fresh(a.first_doc + c), k_next_end = ldg_fresh(a.first_doc + c + 1);
+  // The chunk's documents again (kept in shared memory, not in registers),
+  // for their offsets at the end.
+  const int64_t k_first_end = S.doc_k0, k_next_end = S.doc_k1;
 
   // Ids of short pre-tokens to the chunk's stage region, each thread its own
   // run, in output order without the long pre-tokens' ids. A deferred miss
