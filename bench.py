@@ -32,7 +32,9 @@ sys.path.insert(0, ROOT)
 import workloads  # noqa: E402
 
 METRIC = "encoded input MB/s and tokens/s on 1 GB300; achieved HBM GB/s vs peak"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_encode_serving_batch.md")
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic_serving_batch.json")
+KERNEL_SPAN = "k_prep..k_compact"
+LAUNCHES_PER_CALL = 7
 KERNEL_SRC = os.path.join(ROOT, "byte_level_bpe_pretokenize_gb300", "csrc", "bpe_kernels.cu")
 
 
@@ -49,21 +51,19 @@ def peaks():
 
 
 def traffic_from_profile():
-    """dram bytes per launch of the encode kernel from the committed ncu
-    summary, when it was taken on the current kernel source."""
-    if not os.path.exists(PROFILE_SUMMARY):
-        return None
-    kv = {}
-    for line in open(PROFILE_SUMMARY):
-        if line.startswith("- ") and ":" in line:
-            k, v = line[2:].split(":", 1)
-            kv[k.strip()] = v.strip().strip("`")
-    if kv.get("kernel_source_sha256_16") != kernel_hash():
+    """DRAM bytes per full call of the timed kernels, from the committed ncu
+    summary (profiles/traffic_serving_batch.json), when it was taken on the
+    current kernel source; None otherwise."""
+    if not os.path.exists(TRAFFIC_JSON):
         return None
     try:
-        return int(float(kv["dram_bytes_per_full_launch"]))
-    except (KeyError, ValueError):
+        d = json.load(open(TRAFFIC_JSON))
+    except (OSError, ValueError):
         return None
+    if d.get("kernel_source_sha256_16") != kernel_hash():
+        return None
+    v = d.get("dram_bytes_per_full_call")
+    return int(v) if v is not None else None
 
 
 class ClockSampler:
@@ -163,9 +163,9 @@ def algorithmic_bytes(n_bytes: int, n_docs: int, n_tokens: int) -> int:
 
 
 def oracle_sample(cfg: int, data, offsets, merges, vb, vo, budget_s: float, gpu_ids=None, gpu_off=None):
-    """Time the oracle on whole documents from the start of the batch until
-    about budget_s of CPU time; optionally check those documents against the
-    GPU output."""
+    """Time the single-threaded oracle on whole documents from the start of
+    the batch until about budget_s of CPU time; optionally check those
+    documents against the GPU output."""
     import oracle
     o = oracle.Oracle(merges, vb, vo)
     n_docs = len(offsets) - 1
@@ -188,39 +188,113 @@ def oracle_sample(cfg: int, data, offsets, merges, vb, vo, budget_s: float, gpu_
     return {"docs": done, "bytes": nbytes, "tokens": ntok, "seconds": t_used, "mismatched_groups": mismatch}
 
 
+def slice_docs(offsets: np.ndarray, max_bytes: int) -> int:
+    """Number of whole documents from the start whose bytes fit in max_bytes."""
+    return max(1, int(np.searchsorted(offsets, offsets[0] + max_bytes, side="right")) - 1)
+
+
 def run_reference(args, world, rank):
+    """The reference arm: the oracle on every host core (one pinned process
+    per physical core over byte-balanced document shards), each step a
+    bounded slice of the same workload."""
     if rank != 0:
         return
+    from oracle import sharded
     cfg = args.cfg
     n = workloads.n_docs(cfg)
-    # A bounded sample per step: the first documents of the batch.
-    lens = workloads.doc_lengths(cfg, 0, min(n, 200_000))
-    data, offsets = workloads.docs(cfg, 0, len(lens))
+    lens = workloads.doc_lengths(cfg, 0, min(n, 600_000))
+    offs = np.zeros(len(lens) + 1, dtype=np.int64)
+    np.cumsum(lens, out=offs[1:])
+    k = min(len(lens), slice_docs(offs, args.reference_slice_mib << 20))
+    data, offsets = workloads.docs(cfg, 0, k)
     merges, vb, vo = workloads.table(cfg)
-    per_step = max(0.5, args.reference_budget / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_sample(cfg, data, offsets, merges, vb, vo, per_step)
-    rates, trates, samples = [], [], []
+        sharded.encode(merges, vb, vo, data, offsets)
+    walls, tok = [], 0
+    r = None
     for _ in range(args.steps):
-        s = oracle_sample(cfg, data, offsets, merges, vb, vo, per_step)
-        rates.append(s["bytes"] / s["seconds"] / 1e6)
-        trates.append(s["tokens"] / s["seconds"])
-        samples.append(s)
-    v = statistics.median(rates)
+        r = sharded.encode(merges, vb, vo, data, offsets)
+        walls.append(r["wall_s"])
+        tok = len(r["ids"])
+    wall = statistics.median(walls)
+    v = data.size / wall / 1e6
+    sample = (f"first {k} documents ({data.size} bytes) of the workload per step, on {r['procs']} pinned "
+              f"single-threaded oracle processes ({r['cpu_model']})")
     out = {
         "impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "MB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(1000 * statistics.median([s["seconds"] for s in samples]), 3),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * wall, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "tokens_per_s": round(statistics.median(trates), 1),
-        "config": {"workload": workloads.NAMES[cfg], "n_docs_sampled": samples[-1]["docs"],
-                   "bytes_sampled": samples[-1]["bytes"], "merges": int(len(merges))},
-        "cpu_baseline": {"value": round(v, 3), "unit": "MB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"first {samples[-1]['docs']} documents ({samples[-1]['bytes']} bytes) of the "
-                                   f"workload per step, single-threaded"},
+        "tokens_per_s": round(tok / wall, 1),
+        "config": {"workload": workloads.NAMES[cfg], "n_docs_sampled": k, "bytes_sampled": int(data.size),
+                   "merges": int(len(merges))},
+        "cpu_baseline": {"value": round(v, 3), "unit": "MB/s", "cores": r["procs"], "kind": "oracle",
+                         "sample": sample, "cpu_model": r["cpu_model"]},
         "e2e": {"value": round(v, 3), "unit": "MB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
+
+
+class Encoder:
+    """One workload resident on the GPU with its handle and output buffers."""
+
+    def __init__(self, bpe, cfg, dev, local, rank=0, n_docs=None):
+        import torch
+        self.bpe, self.cfg = bpe, cfg
+        self.data, self.offsets, self.merges, self.vb, self.vo = load_workload(cfg, rank, n_docs)
+        self.n_bytes, self.n_docs = int(self.data.size), int(len(self.offsets) - 1)
+        self.handle = bpe.bpe_build(self.merges, self.vb, self.vo, local)
+        self.stream = torch.cuda.current_stream()
+        self.d_data = torch.from_numpy(self.data).to(dev)
+        self.d_off = torch.from_numpy(self.offsets).to(dev)
+        self.d_ids = torch.empty(max(1, self.n_bytes), dtype=torch.int32, device=dev)
+        self.d_out = torch.empty(self.n_docs + 1, dtype=torch.int64, device=dev)
+        self.n_tokens = self.step(True)
+
+    def step(self, want_total=False):
+        return self.bpe.bpe_encode_batch(self.handle, self.d_data.data_ptr(), self.n_bytes, self.d_off.data_ptr(),
+                                         self.n_docs, self.d_ids.data_ptr(), self.n_bytes, self.d_out.data_ptr(),
+                                         want_total, self.stream.cuda_stream)
+
+    def time_calls(self, steps, warmup):
+        """CUDA-event time (ms) of each of `steps` calls after `warmup`."""
+        import torch
+        for _ in range(warmup):
+            self.step()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            a.record(self.stream)
+            self.step()
+            b.record(self.stream)
+        torch.cuda.synchronize()
+        self.bpe.bpe_sync_status(self.handle, self.stream.cuda_stream)
+        return [a.elapsed_time(b) for a, b in ev]
+
+    def result(self):
+        return self.d_ids[:self.n_tokens].cpu().numpy(), self.d_out.cpu().numpy()
+
+    def close(self):
+        self.bpe.bpe_destroy(self.handle)
+
+
+def config_line(enc: "Encoder", ms: float, peak: float) -> dict:
+    alg = algorithmic_bytes(enc.n_bytes, enc.n_docs, enc.n_tokens)
+    return {"workload": workloads.NAMES[enc.cfg], "n_docs": enc.n_docs, "n_bytes": enc.n_bytes,
+            "tokens": int(enc.n_tokens), "merges": int(len(enc.merges)), "ms_per_call": round(ms, 4),
+            "input_mb_per_s": round(enc.n_bytes / (ms / 1e3) / 1e6, 3),
+            "tokens_per_s": round(enc.n_tokens / (ms / 1e3), 1),
+            "hbm_gbs_achieved": round(alg / (ms / 1e3) / 1e9, 2), "frac": round(alg / (ms / 1e3) / 1e9 / peak, 4),
+            "algorithmic_bytes": alg}
+
+
+def parity_line(enc: "Encoder", gpu_ids, gpu_off) -> tuple[dict, dict]:
+    """The whole batch through the all-core oracle, compared id for id."""
+    from oracle import sharded
+    r = sharded.encode(enc.merges, enc.vb, enc.vo, enc.data, enc.offsets)
+    same = bool(np.array_equal(gpu_ids, r["ids"]) and np.array_equal(gpu_off, r["offsets"]))
+    line = {"fnv1a64_gpu": f"{workloads.fnv1a64(gpu_ids):016x}", "fnv1a64_oracle": f"{workloads.fnv1a64(r['ids']):016x}",
+            "docs_compared": enc.n_docs, "identical": same}
+    return line, r
 
 
 def run_gpu(args, world, rank, local):
@@ -237,27 +311,15 @@ def run_gpu(args, world, rank, local):
     __graft_entry__.build()
 
     cfg = args.cfg
-    data, offsets, merges, vb, vo = load_workload(cfg, rank, args.n_docs)
-    n_bytes, n_docs = int(data.size), int(len(offsets) - 1)
-    handle = bpe.bpe_build(merges, vb, vo, local)
-    stream = torch.cuda.current_stream()
+    enc = Encoder(bpe, cfg, dev, local, rank, args.n_docs)
+    handle, stream, n_bytes, n_docs, n_tokens = enc.handle, enc.stream, enc.n_bytes, enc.n_docs, enc.n_tokens
     s_ptr = stream.cuda_stream
-
-    d_data = torch.from_numpy(data).to(dev)
-    d_off = torch.from_numpy(offsets).to(dev)
-    d_ids = torch.empty(n_bytes, dtype=torch.int32, device=dev)
-    d_out = torch.empty(n_docs + 1, dtype=torch.int64, device=dev)
-
-    def step(want_total=False):
-        return bpe.bpe_encode_batch(handle, d_data.data_ptr(), n_bytes, d_off.data_ptr(), n_docs, d_ids.data_ptr(),
-                                    n_bytes, d_out.data_ptr(), want_total, s_ptr)
-
-    n_tokens = step(True)
+    data, offsets = enc.data, enc.offsets
     for _ in range(max(0, args.warmup - 1)):
-        step()
+        enc.step()
     bpe.bpe_sync_status(handle, s_ptr)
 
-    # Timed region: K steps; the encode kernel is timed by its own event pair.
+    # Timed region: K steps; the encode kernels are timed by their own event pair.
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a, b in ev:  # materialise the CUDA events
         a.record(stream)
@@ -275,7 +337,7 @@ def run_gpu(args, world, rank, local):
     t_start.record(stream)
     for a, b in ev:
         bpe.bpe_set_timing_events(handle, a.cuda_event, b.cuda_event)
-        step()
+        enc.step()
     t_end.record(stream)
     bpe.bpe_set_timing_events(handle, None, None)
     torch.cuda.synchronize()
@@ -286,21 +348,11 @@ def run_gpu(args, world, rank, local):
     step_ms = t_start.elapsed_time(t_end) / args.steps
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
 
-    # Secondary: the same steps with the word cache off (every pre-token runs
+    # Secondary: the same calls with the word cache off (every pre-token runs
     # the merge loop), timed the same way, outside the headline region.
     bpe.bpe_set_word_cache(handle, False)
-    step()
-    nc0, nc1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    nc_steps = max(1, min(args.steps, 3))
-    torch.cuda.synchronize()
-    nc0.record(stream)
-    for _ in range(nc_steps):
-        step()
-    nc1.record(stream)
-    torch.cuda.synchronize()
-    nocache_ms = nc0.elapsed_time(nc1) / nc_steps
+    nocache_ms = statistics.median(enc.time_calls(max(1, min(args.steps, 3)), 1))
     bpe.bpe_set_word_cache(handle, True)
-    bpe.bpe_sync_status(handle, s_ptr)
 
     # End to end through the C ABI's host-buffer call: page-locked host input,
     # copies in, encode and copies out of ids and offsets, pipelined in slices
@@ -322,6 +374,7 @@ def run_gpu(args, world, rank, local):
     for _ in range(e2e_steps):
         host_step()
     e2e_s = (time.perf_counter() - e0) / e2e_steps
+    del h_data, h_off, h_ids, h_out
     (step_ms, kern_ms, e2e_s), (all_bytes, all_tokens, all_docs) = reduce_ranks(
         dist, dev, [step_ms, kern_ms, e2e_s], [n_bytes, n_tokens, n_docs])
 
@@ -331,11 +384,38 @@ def run_gpu(args, world, rank, local):
         alg = algorithmic_bytes(n_bytes, n_docs, n_tokens)
         achieved = alg / (kern_ms / 1e3) / 1e9
         value = all_bytes / (step_ms / 1e3) / 1e6
-        cpu = None
-        if world == 1 and not args.no_cpu_baseline:
-            g_ids = d_ids[:n_tokens].cpu().numpy()
-            g_off = d_out.cpu().numpy()
-            s = oracle_sample(cfg, data, offsets, merges, vb, vo, args.cpu_budget, g_ids, g_off)
+        cpu, configs = None, None
+        if world == 1 and args.n_docs is None and not args.no_configs:
+            # The other workloads, one at a time (median of >= 10 calls after
+            # 3 warm-up calls), then every workload compared whole with the
+            # oracle on all host cores.
+            configs = {}
+            head_ids, head_off = enc.result()
+            for c in (1, 2, 3, 4):
+                e = Encoder(bpe, c, dev, local)
+                ms = statistics.median(e.time_calls(max(10, min(args.steps, 20)), 3))
+                configs[f"C{c}"] = config_line(e, ms, peak)
+                if not args.no_cpu_baseline:
+                    ids_c, off_c = e.result()
+                    configs[f"C{c}"]["parity"], _ = parity_line(e, ids_c, off_c)
+                e.close()
+                del e
+                torch.cuda.empty_cache()
+            configs[f"C{cfg}"] = config_line(enc, kern_ms, peak)
+            if not args.no_cpu_baseline:
+                par, r = parity_line(enc, head_ids, head_off)
+                configs[f"C{cfg}"]["parity"] = par
+                cpu = {"value": round(n_bytes / r["wall_s"] / 1e6, 3), "unit": "MB/s", "cores": r["procs"],
+                       "kind": "oracle",
+                       "sample": f"the whole batch ({n_docs} documents, {n_bytes} bytes) on {r['procs']} pinned "
+                                 f"single-threaded oracle processes over byte-balanced document shards "
+                                 f"({r['cpu_s']:.0f} CPU-seconds)",
+                       "cpu_model": r["cpu_model"], "physical_cores": r["cores"],
+                       "tokens_per_s": round(len(r["ids"]) / r["wall_s"], 1),
+                       "parity_vs_gpu": "identical" if par["identical"] else "differs"}
+        elif world == 1 and not args.no_cpu_baseline:
+            g_ids, g_off = enc.result()
+            s = oracle_sample(cfg, data, offsets, enc.merges, enc.vb, enc.vo, args.cpu_budget, g_ids, g_off)
             cpu = {"value": round(s["bytes"] / s["seconds"] / 1e6, 3), "unit": "MB/s", "cores": 1,
                    "kind": "oracle",
                    "sample": f"first {s['docs']} documents ({s['bytes']} bytes) of the same batch, single-threaded",
@@ -349,11 +429,11 @@ def run_gpu(args, world, rank, local):
             "tokens_per_s": round(all_tokens / (step_ms / 1e3), 1),
             "hbm_gbs_achieved": round(achieved, 2),
             "config": {"workload": workloads.NAMES[cfg], "n_docs": n_docs, "n_bytes": n_bytes,
-                       "tokens": int(n_tokens), "merges": int(len(merges)), "n_vocab": int(len(vo) - 1),
+                       "tokens": int(n_tokens), "merges": int(len(enc.merges)), "n_vocab": int(len(enc.vo) - 1),
                        "l2": (f"inputs ({n_bytes / 2**20:.0f} MiB) larger than L2 (129 MB); no flush" if n_bytes > 129e6 else f"inputs ({n_bytes / 2**20:.0f} MiB) fit in L2: a profiling case, not a bench number"), "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                         "kernel": "k_pretokenize..k_compact", "kernel_ms": round(kern_ms, 4),
+                         "kernel": KERNEL_SPAN, "kernel_ms": round(kern_ms, 4),
                          "algorithmic_bytes_per_launch": alg, "traffic": traffic_from_profile()},
             "cpu_baseline": cpu,
             "e2e": {"value": round(all_bytes / e2e_s / 1e6, 3),
@@ -362,11 +442,12 @@ def run_gpu(args, world, rank, local):
             "without_word_cache": {"value": round(n_bytes / (nocache_ms / 1e3) / 1e6, 3), "unit": "MB/s",
                                    "ms_per_step": round(nocache_ms, 4),
                                    "hbm_frac": round(alg / (nocache_ms / 1e3) / 1e9 / peak, 4)},
-            "gpu_launches": 7 * args.steps,
+            "configs": configs,
+            "gpu_launches": LAUNCHES_PER_CALL * args.steps,
             "clocks": clk,
         }
         print(json.dumps(out), flush=True)
-    bpe.bpe_destroy(handle)
+    enc.close()
     if dist:
         dist.destroy_process_group()
     return out
@@ -382,7 +463,9 @@ def main():
     ap.add_argument("--n-docs", type=int, default=None, help="fewer documents (small profiling cases only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
-    ap.add_argument("--reference-budget", type=float, default=60.0, help="total oracle seconds for --impl reference")
+    ap.add_argument("--reference-slice-mib", type=int, default=64,
+                    help="MiB of whole documents per --impl reference step")
+    ap.add_argument("--no-configs", action="store_true", help="headline workload only (no C1-C4 lines, no full parity)")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":

@@ -79,6 +79,8 @@ def _load():
                 getattr(lib, f).argtypes = [ctypes.c_int]
             lib.wl_word.restype = ctypes.c_int
             lib.wl_word.argtypes = [ctypes.c_int, ctypes.c_char_p]
+            lib.wl_fnv1a64.restype = ctypes.c_uint64
+            lib.wl_fnv1a64.argtypes = [p, i64, ctypes.c_uint64]
             _lib = lib
     return _lib
 
@@ -165,6 +167,21 @@ def train(text: np.ndarray, merges: int) -> np.ndarray:
     out = np.empty((max(merges, 1), 3), dtype=np.int32)
     k = lib.wl_train(_ptr(text) if text.size else 0, text.size, merges, _ptr(out))
     return out[:k].copy()
+
+
+FNV64_BASIS = 0xCBF29CE484222325
+
+
+def fnv1a64(a: np.ndarray, h: int = FNV64_BASIS) -> int:
+    """FNV-1a 64 digest of an array's bytes (little-endian), continuing from h.
+
+    A checksum to compare id streams between implementations; it is not part
+    of any encoding.
+    """
+    a = np.ascontiguousarray(a)
+    if a.size == 0:
+        return h
+    return int(_load().wl_fnv1a64(a.ctypes.data, a.nbytes, h))
 
 
 def vocab_from_merges(merges: np.ndarray):

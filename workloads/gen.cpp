@@ -497,4 +497,15 @@ int64_t wl_train(const uint8_t* corpus, int64_t n, int64_t n_merges, int32_t* me
   return t.run(n_merges, merges_out);
 }
 
+// FNV-1a 64 over n bytes, continuing from state h (start with
+// 0xcbf29ce484222325). A digest for comparing id streams, not part of any
+// encoding: offset basis and prime are the published FNV-1a 64 parameters.
+uint64_t wl_fnv1a64(const uint8_t* p, int64_t n, uint64_t h) {
+  for (int64_t i = 0; i < n; ++i) {
+    h ^= p[i];
+    h *= 0x100000001b3ull;
+  }
+  return h;
+}
+
 }  // extern "C"
