@@ -38,7 +38,7 @@ class BpeError(RuntimeError):
 
 
 def _sources():
-    return [os.path.join(_CSRC, f) for f in ("bpe_kernels.cu", "class_table.inc")] + \
+    return [os.path.join(_CSRC, f) for f in ("bpe_kernels.cu", "tiles.cuh", "class_table.inc")] + \
         [os.path.join(_ROOT, "include", "bpe_gb300.h")]
 
 

@@ -10,17 +10,18 @@
 // Encoding schrittweise").
 //
 // GPU design (none of it is on the pages, whose engines are CPU code):
-//   * The byte stream is cut into 4 KiB chunks, one CTA each. A CTA loads its
-//     chunk plus a 16-byte halo and a 256-byte margin into shared memory.
-//   * Split (k_pretokenize). Each thread takes 16 bytes.
+//   * One pass over the input (k_tiles, tiles.cuh): a warp per 992-byte tile
+//     splits, probes the word cache, merges the misses and writes the ids;
+//     a decoupled look-back over the tiles' counts gives each tile its output
+//     offset.
+//   * Split (start_mask32): each lane takes 32 bytes.
 //     - When they and their context are ASCII, carry-free SWAR range tests
-//       give 16-bit class masks, and the split rules are a dozen mask
+//       give per-byte class masks, and the split rules are a dozen mask
 //       operations; each apostrophe resolves its contraction in place.
-//     - Otherwise a 24-byte UTF-8 unit scan builds the same masks from a
-//       two-level codepoint class table.
+//     - Otherwise a UTF-8 unit scan builds the same masks from a two-level
+//       codepoint class table.
 //     - Multi-byte whitespace falls back to the per-byte predicate
 //       starts_piece.
-//     - Output: a start bitmask in global memory.
 //   * Symbols are token ids: byte b starts as byte_id[b]. An open-addressed
 //     pair table of 32-byte buckets maps (left_id, right_id) to {rank,
 //     new_id}. Because bytes(new_id) = bytes(left) || bytes(right) (checked
@@ -28,24 +29,18 @@
 //   * Word cache ("Hugging Face Tokenizers v1", section on word caching: the
 //     same pre-token always gives the same ids, so a memo from pre-token bytes
 //     to ids skips the merge loop).
-//     - bpe_build fills it once, by running the merge kernel below on strings
-//       of at most 16 bytes: vocabulary strings, space-stripped vocabulary
-//       words and prefixes of both.
+//     - bpe_build fills it once, by running the merge loop on strings of at
+//       most 16 bytes: vocabulary strings, space-stripped vocabulary words and
+//       prefixes of both.
 //     - A pre-token found there takes the stored ids.
-//   * Encode (k_encode):
-//     - Pre-tokens of up to 64 bytes get one thread each for the cache probe.
-//     - Misses are queued and merged by lane groups: 8 lanes up to 16 bytes,
-//       a warp up to 64. Each step is a group-wide minimum, a ballot of the
-//       pair's positions and a run-parity mask for the non-overlapping
-//       left-to-right choice.
-//     - Longer pre-tokens are merged by the whole CTA in a device pool indexed
-//       by input byte, so each owns the pool range of its own bytes.
-//   * Output without waits between CTAs:
-//     - each chunk writes its ids to a stage region of its own (long
-//       pre-tokens' stay in the pool, listed in a record block), its token
-//       count, and its documents' offsets relative to the chunk;
-//     - a two-level scan gives the chunk offsets;
-//     - k_compact moves every chunk's ids into place, a warp per chunk.
+//   * Merges of cache misses (at most 64 bytes) by lane groups of 4 to 32
+//     lanes (merge_group): each step is a group-wide minimum, a ballot of the
+//     pair's positions and a run-parity mask for the non-overlapping
+//     left-to-right choice.
+//   * Longer pre-tokens are merged by a whole CTA each (k_giants,
+//     merge_long) in a device pool indexed by input byte, so each owns the
+//     pool range of its own bytes; their tiles' ids are placed by the fix-up
+//     kernels after a scan of all tile counts.
 
 #include <cuda_runtime.h>
 
@@ -68,32 +63,18 @@ namespace {
 
 // ---------------------------------------------------------------- constants --
 
-constexpr int kThreads = 256;         // threads per CTA
-constexpr int kChunk = 4096;          // bytes whose pre-tokens a CTA owns (16 per thread)
-constexpr int kMargin = 64;           // bytes after the chunk kept in shared memory (a short pre-token ends there)
-constexpr int kHalo = 16;             // context bytes on each side of the window
-constexpr int kWin = kHalo + kChunk + kMargin + kHalo;   // window bytes
-constexpr int kWinWords = (kWin + 31) / 32;
-constexpr int kSpan = kChunk + kMargin;                  // positions with a start bit
-constexpr int kSpanWords = kSpan / 32;
-constexpr int kShortMax = 64;         // longest pre-token merged by one thread
+constexpr int kThreads = 256;         // threads per CTA of the CTA-wide merge (k_giants)
+constexpr int kHalo = 16;             // context bytes on each side of a split window
+constexpr int kShortMax = 64;         // longest pre-token merged inside its tile (by a lane group)
 constexpr int kCacheMaxLen = 16;      // longest pre-token looked up in the word cache
 constexpr int kCacheMaxIds = 3;       // most ids a cache entry holds
-constexpr int kProbeRound = 2;        // word-cache probes a thread has in flight
-constexpr uint32_t kMaxDefer = 160;   // cache misses per chunk handed to k_misses
-constexpr uint16_t kMissMark = 0x8000;     // span_cnt: a cache miss, its byte length below
-constexpr uint16_t kDeferFlag = 0x8000;    // span_start: the miss goes to k_misses
 constexpr int kLongPerThread = 4;     // elements per thread per round of the CTA merge
 constexpr int kRound = kThreads * kLongPerThread;
-constexpr int kMaxLong = kChunk / kShortMax + 2;
-constexpr uint32_t kMissShortCap = 3 * kSpanWords / 2;  // queued word-cache misses of <= 16 bytes
-constexpr uint32_t kMissMedCap = kSpanWords / 2;        // ... and of 17..kShortMax bytes
 constexpr uint32_t kReprobe = 0xFFFFFFFEu;              // pair rank still to be looked up
 constexpr uint32_t kInf = 0xFFFFFFFFu;
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 constexpr uint32_t kEmptySlot = 0xFFFFFFFFu;  // left id of an unused pair-table slot
 
-static_assert(kChunk == 16 * kThreads, "one 16-byte group per thread");
 static_assert(kShortMax <= 64 && kCacheMaxLen <= 16, "group merges hold 2 symbols per lane");
 
 // device status bits
@@ -101,10 +82,6 @@ constexpr uint32_t kStBadInput = 1u;
 constexpr uint32_t kStTimeout = 2u;
 constexpr uint32_t kStInternal = 4u;
 constexpr uint32_t kStCapacity = 8u;
-
-// Staged output: chunk c's ids of short pre-tokens go to stage[c kStage ..]
-// in order (long pre-tokens keep theirs in the pool at their own bytes).
-constexpr int kStage = kChunk + kShortMax;
 
 enum Cls { kO = 0, kL = 1, kN = 2, kS = 3 };
 
@@ -147,9 +124,13 @@ struct Cache {
 
 struct DevSmall {
   uint32_t status;
-  uint32_t rec_used;  // u32 words of long pre-token records handed out this call
-  int64_t total;
-  uint32_t q_n;  // cache misses queued for k_misses
+  uint32_t pad;
+  int64_t total;                     // ids of the call
+  unsigned long long tile_ctr;       // tiles taken by k_tiles' warps
+  unsigned long long n_misses;       // cache misses handed to k_misses
+  unsigned long long n_giants;       // pre-tokens deferred to k_giants
+  unsigned long long giant_ctr;      // deferred pre-tokens taken by k_giants' CTAs
+  unsigned long long n_ranges;       // long runs of tiles for k_prep_long
 };
 
 
@@ -187,6 +168,8 @@ __device__ __forceinline__ uint32_t lookup_rank(const Tables& T, uint32_t a, uin
   uint32_t nw;
   return lookup_pair(T, a, b, &nw);
 }
+
+
 
 // The rest of lookup_pair once the home bucket {u, v} of (a, b) is loaded.
 __device__ __forceinline__ uint32_t lookup_pair_from(const Tables& T, uint32_t a, uint32_t b, uint32_t bucket, uint4 u,
@@ -384,14 +367,10 @@ __device__ __forceinline__ uint32_t lds_u32(const uint32_t* p) {
   return v;
 }
 
-// Asynchronous global-to-shared copies (16 or 4 bytes, both addresses aligned
-// to the size): a thread issues all of its copies before it waits for any.
+// Asynchronous global-to-shared copy of 16 bytes (both addresses 16-byte
+// aligned); a thread issues all of its copies before it waits for any.
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((unsigned)__cvta_generic_to_shared(smem)), "l"(gmem)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((unsigned)__cvta_generic_to_shared(smem)), "l"(gmem)
                : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
@@ -409,17 +388,14 @@ __device__ __forceinline__ uint32_t bits32_at(const uint32_t* bits, int start) {
 
 namespace {
 
-// Warps of an encode CTA that merge the cache misses it keeps (the rest wait).
-constexpr int kMergeWarps = 4;
-
 // A warp's scratch while its lanes merge pre-tokens in groups (merge_group).
 struct GroupScratch {
   uint32_t sym[64], rank[64], nw[64];
 };
 
-// What the split needs: the window and its document and start bit masks. The
-// split kernel's shared memory is only this; the encode kernel's extends it
-// (and keeps no document starts: every document edge is a pre-token start).
+// What the split needs: the window (CHUNK bytes whose start bits are computed,
+// AFTER more, and kHalo bytes of context on each side) with its document-edge
+// and outside-document bit masks, and room for the start bits.
 template <int CHUNK, int AFTER, bool DOCS>
 struct __align__(16) WindowSmem {
   static constexpr int kLen = kHalo + CHUNK + AFTER + kHalo;  // window bytes
@@ -431,50 +407,8 @@ struct __align__(16) WindowSmem {
   int64_t chunk;
 };
 
-// The encode kernel's window: a chunk plus the margin.
-using SplitSmem = WindowSmem<kChunk, kMargin, false>;
-static_assert(SplitSmem::kLen == kWin && SplitSmem::kWords == kWinWords, "encode window");
-// The split kernel's window: 32 bytes per thread.
-constexpr int kSplitChunk = 32 * kThreads;
-using SplitWin = WindowSmem<kSplitChunk, kHalo, true>;
-
-struct Smem : SplitSmem {
-  uint16_t missq[kMissShortCap + kMissMedCap];  // queued word-cache misses
-  uint16_t grp_pos[kThreads];        // pre-tokens starting before chunk byte 16 t
-  uint16_t span_start[kChunk + 1];
-  // token counts (long pre-tokens 0, a miss kMissMark | length), then
-  // exclusive offsets without the long pre-tokens' ids
-  uint16_t span_cnt[kChunk + 1];
-  uint32_t sym[kSpan];               // ids of short pre-tokens, at their start position
-  union {
-    GroupScratch grp[kMergeWarps];   // one per merging warp while lane groups merge cache misses
-    uint32_t stage[kRound];          // long merge rounds
-  } u;
-  int32_t byte_id[256];
-  uint16_t long_list[kMaxLong];
-  uint32_t long_cnt[kMaxLong];       // ids of each long pre-token, in long_list order
-  int64_t doc_k0, doc_k1;            // the documents starting in the chunk: [doc_k0, doc_k1)
-  uint32_t red[2 * (kThreads / 32 + 1)];
-  uint32_t carry[2];
-  int64_t prefix;
-  uint32_t agg;                      // the chunk's token count
-  uint32_t n_spans;
-  uint32_t n_long;
-  uint32_t n_miss;                   // queued misses of <= 16 bytes
-  uint32_t n_miss_m;                 // queued misses of 17..kShortMax bytes
-  uint32_t n_def;                    // word-cache misses (all lengths)
-  uint32_t q_base;                   // the chunk's first entry in the k_misses queue
-  int64_t last_end;                  // end of the chunk's last pre-token, -1 past the window
-  int last_end_rel;                  // the same relative to the chunk start
-  int64_t doc_lo, doc_hi;  // document of a long pre-token that runs past the window
-};
-
-constexpr int kEncodeCtasPerSm = 5;  // resident encode CTAs (shared memory and 48 registers a thread)
-
 // Barrier of the kThreads threads of a CTA (named barrier 1).
 __device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
-
-static_assert(kEncodeCtasPerSm * (sizeof(Smem) + 1024) <= 228 * 1024, "the encode CTAs fit in an SM's shared memory");
 
 __device__ __forceinline__ bool bit_at(const uint32_t* bits, int i) { return (bits[i >> 5] >> (i & 31)) & 1u; }
 
@@ -670,149 +604,6 @@ __device__ uint32_t start_mask32(const SS& S, int p0) {
   return res;
 }
 
-// Loads the window of chunk c: bytes [c0 - kHalo, c0 + kChunk + kMargin +
-// kHalo), the document edges that fall inside it, and which bytes lie outside
-// every document. first_doc = the first document starting at or after c0.
-template <class SS>
-__device__ void load_window(SS& S, const uint8_t* bytes, int64_t n_bytes, const int64_t* doc_offsets,
-                            int64_t n_docs, int64_t c0, int64_t first_doc) {
-  const int tid = threadIdx.x;
-  const int64_t w0 = c0 - kHalo, w_end = w0 + SS::kLen;
-  // Positions relative to the window fit in 32 bits: the input's start and
-  // end and the first and last document offsets, clamped to [-1, kBits]
-  // (kBits: every position the bit masks hold).
-  constexpr int kBits = (SS::kWords + 2) * 32;
-  auto rel = [&](int64_t x) -> int {
-    const int64_t r = x - w0;
-    return r < -1 ? -1 : (r > kBits ? kBits : (int)r);
-  };
-  const int r_0 = rel(0), r_n = rel(n_bytes);  // window bytes [r_0, r_n) exist
-  // Every load is issued before the first barrier: the bytes (asynchronous
-  // 16-byte copies when the input is 16-byte aligned, window offsets being
-  // multiples of 16; bytes otherwise), the first and last document offsets,
-  // and the offsets of the documents from 32 before first_doc on (one per
-  // thread; more only when documents are tiny).
-  const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 15u) == 0;
-  for (int i = tid * 16; i < SS::kLen; i += kThreads * 16) {
-    if (aligned && i >= r_0 && i + 16 <= r_n) {
-      cp_async16(S.win + i, bytes + (w0 + i));
-    } else {
-#pragma unroll
-      for (int k = 0; k < 16; ++k) S.win[i + k] = (i + k >= r_0 && i + k < r_n) ? bytes[w0 + i + k] : 0;
-    }
-  }
-  int64_t d_first = __ldg(doc_offsets), d_last = __ldg(doc_offsets + n_docs);
-  int64_t k_lo = first_doc - 32;
-  if (k_lo > n_docs) k_lo = n_docs;
-  if (k_lo < 0) k_lo = 0;
-  const int64_t o_before = tid == 0 && k_lo > 0 ? __ldg(doc_offsets + k_lo - 1) : INT64_MIN;  // thread 0's test below
-  const int64_t o_mine = k_lo + tid <= n_docs ? __ldg(doc_offsets + k_lo + tid) : INT64_MAX;
-  // the last of those (every thread reads it: no barrier waits on the load)
-  const int64_t o_last =
-      k_lo + kThreads - 1 <= n_docs ? __ldg(doc_offsets + k_lo + kThreads - 1) : INT64_MAX;
-  for (int i = tid; i < SS::kWords + 2; i += kThreads) S.docbits[i] = 0;
-  cp_async_wait_all();
-  cta_sync();
-  d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
-  d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
-  const int r_first = rel(d_first), r_last = rel(d_last);
-  for (int wi = tid; wi < SS::kWords + 2; wi += kThreads) {
-    uint32_t word = 0;
-    const int p = wi * 32;
-    if (p < r_first || p + 32 > r_last) {
-      for (int k = 0; k < 32; ++k)
-        if (p + k < r_first || p + k >= r_last) word |= 1u << k;
-    }
-    S.outbits[wi] = word;
-  }
-  // Document starts in the window.
-  if (o_mine >= w0 && o_mine < w_end) {
-    const int i = (int)(o_mine - w0);
-    atomicOr(&S.docbits[i >> 5], 1u << (i & 31));
-  }
-  if (o_last < w_end && o_mine < w_end) {  // tiny documents: more than kThreads - 32 start in the window
-    for (int64_t k = k_lo + tid + kThreads; k <= n_docs; k += kThreads) {
-      const int64_t o = doc_offsets[k];
-      if (o >= w_end) break;
-      if (o >= w0) {
-        const int i = (int)(o - w0);
-        atomicOr(&S.docbits[i >> 5], 1u << (i & 31));
-      }
-    }
-  }
-  if (tid == 0 && o_before >= w0) {  // more than 32 documents start in the left halo
-    for (int64_t k = k_lo - 1; k >= 0; --k) {
-      const int64_t o = doc_offsets[k];
-      if (o < w0) break;
-      const int i = (int)(o - w0);
-      atomicOr(&S.docbits[i >> 5], 1u << (i & 31));
-    }
-  }
-  cta_sync();
-}
-
-// The encode kernel's window of chunk c: the bytes (as load_window), which
-// bytes lie outside every document (from the first and last document
-// offsets alone: documents are contiguous, so every other document edge is a
-// pre-token start) and the split kernel's start bits of [c0, c0 + kSpan).
-__device__ void load_encode_window(SplitSmem& S, const uint8_t* bytes, int64_t n_bytes, const int64_t* doc_offsets,
-                                   int64_t n_docs, const uint32_t* start_bits, int64_t c0) {
-  const int tid = threadIdx.x;
-  const int64_t w0 = c0 - kHalo;
-  // Window-relative positions in 32 bits, clamped to [-1, kBits] (as in
-  // load_window).
-  constexpr int kBits = (kWinWords + 2) * 32;
-  auto rel = [&](int64_t x) -> int {
-    const int64_t r = x - w0;
-    return r < -1 ? -1 : (r > kBits ? kBits : (int)r);
-  };
-  const int r_0 = rel(0), r_n = rel(n_bytes);  // window bytes [r_0, r_n) exist
-  // Asynchronous 16-byte copies when the input is 16-byte aligned (window
-  // offsets are multiples of 16), bytes otherwise; the start bits as 4-byte
-  // copies.
-  const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 15u) == 0;
-  for (int i = tid * 16; i < kWin; i += kThreads * 16) {
-    if (aligned && i >= r_0 && i + 16 <= r_n) {
-      cp_async16(S.win + i, bytes + (w0 + i));
-    } else {
-#pragma unroll
-      for (int k = 0; k < 16; ++k) S.win[i + k] = (i + k >= r_0 && i + k < r_n) ? bytes[w0 + i + k] : 0;
-    }
-  }
-  const int64_t n_words = (n_bytes + 31) / 32;
-  for (int w = tid; w < kSpanWords; w += kThreads) {
-    const int64_t gw = c0 / 32 + w;
-    if (gw < n_words) cp_async4(&S.startbits[w], start_bits + gw);
-    else S.startbits[w] = 0u;
-  }
-  // Which bytes lie outside every document: one word per thread, so only
-  // those threads read the first and last document offsets.
-  static_assert(kWinWords + 2 <= kThreads, "one out-of-document word per thread");
-  if (tid < kWinWords + 2) {
-    int64_t d_first = __ldg(doc_offsets), d_last = __ldg(doc_offsets + n_docs);
-    d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
-    d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
-    const int r_first = rel(d_first), r_last = rel(d_last);
-    uint32_t word = 0;
-    const int p = tid * 32;
-    if (p < r_first || p + 32 > r_last) {
-      for (int k = 0; k < 32; ++k)
-        if (p + k < r_first || p + k >= r_last) word |= 1u << k;
-    }
-    S.outbits[tid] = word;
-  }
-  cp_async_wait_all();
-  cta_sync();
-}
-
-// Start bits of the split kernel's chunk: thread t takes window positions
-// [kHalo + 32 t, + 32), one start bit word (the encode kernel takes its
-// margin's start bits from the next chunk's output). Each thread stores its
-// own word afterwards, so no barrier follows.
-__device__ void compute_start_bits(SplitWin& S) {
-  S.startbits[threadIdx.x] = start_mask32(S, kHalo + 32 * (int)threadIdx.x);
-}
-
 // ----------------------------------------------------------- block helpers --
 
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
@@ -848,33 +639,6 @@ __device__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total) 
   return before + incl - v;
 }
 
-// Two exclusive scans over the CTA with one barrier; uses
-// red[0 .. 2 kThreads/32). The caller passes another barrier before its next
-// use of red.
-__device__ void block_excl_scan2(uint32_t v, uint32_t u, uint32_t* red, uint32_t* ev, uint32_t* eu, uint32_t* tv,
-                                 uint32_t* tu) {
-  constexpr int kW = kThreads / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t iv = warp_incl_scan(v), iu = warp_incl_scan(u);
-  if (lane == 31) {
-    red[warp] = iv;
-    red[kW + warp] = iu;
-  }
-  cta_sync();
-  uint32_t bv = 0, bu = 0, av = 0, au = 0;
-#pragma unroll
-  for (int w = 0; w < kW; ++w) {
-    const uint32_t x = red[w], y = red[kW + w];
-    bv += w < warp ? x : 0u;
-    bu += w < warp ? y : 0u;
-    av += x;
-    au += y;
-  }
-  *ev = bv + iv - v;
-  *eu = bu + iu - u;
-  *tv = av;
-  *tu = au;
-}
 
 __device__ uint32_t block_min(uint32_t v, uint32_t* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1152,23 +916,6 @@ struct CacheKey {
   uint32_t x0, x1, x2, x3;
 };
 
-__device__ __forceinline__ CacheKey cache_key_words(const Smem& S, int st, int len) {
-  const int ws = kHalo + st;
-  const uint32_t* wv = reinterpret_cast<const uint32_t*>(S.win) + (ws >> 2);
-  const uint32_t sh = (uint32_t)(ws & 3) * 8u;
-  const uint32_t a0 = lds_u32(wv), a1 = lds_u32(wv + 1), a2 = lds_u32(wv + 2), a3 = lds_u32(wv + 3),
-                 a4 = lds_u32(wv + 4);
-  // bytes at or past len are zeroed: a 64-bit mask per half (len <= 16)
-  const uint32_t nbit = 8u * (uint32_t)len;
-  const uint64_t m_lo = nbit >= 64 ? ~0ull : (1ull << nbit) - 1ull;
-  const uint64_t m_hi = nbit <= 64 ? 0ull : (nbit >= 128 ? ~0ull : (1ull << (nbit - 64)) - 1ull);
-  CacheKey K;
-  K.x0 = __funnelshift_r(a0, a1, sh) & (uint32_t)m_lo;
-  K.x1 = __funnelshift_r(a1, a2, sh) & (uint32_t)(m_lo >> 32);
-  K.x2 = __funnelshift_r(a2, a3, sh) & (uint32_t)m_hi;
-  K.x3 = __funnelshift_r(a3, a4, sh) & (uint32_t)(m_hi >> 32);
-  return K;
-}
 
 __device__ __forceinline__ uint32_t cache_slot(const CacheKey& K, uint32_t len, const Cache& C) {
   return cache_hash(K.x0, K.x1, K.x2, K.x3, len) & C.mask;
@@ -1194,818 +941,11 @@ __device__ __forceinline__ uint32_t cache_resolve(const Cache& C, const CacheKey
   return 0;
 }
 
-// One thread merges a short pre-token in place (used when the miss queue is
-// full or the word cache is off); its pair ranks live in local memory.
-__device__ __forceinline__ uint32_t merge_at(Smem& S, int st, int len, const Tables& T) {
-  uint32_t rk[kShortMax];
-  return (uint32_t)merge_short(S.sym + st, rk, S.win + kHalo + st, len, T, S.byte_id);
-}
+}  // namespace
 
-// ------------------------------------------------------------------ kernels --
+#include "tiles.cuh"
 
-// Per call: first document of every chunk found (first_doc[n_chunks] =
-// n_docs + 1), offsets validated, record counter and token count reset.
-__global__ void k_prep(const int64_t* doc_offsets, int64_t n_docs, int64_t n_bytes, int64_t n_chunks,
-                       int64_t* first_doc, DevSmall* small) {
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t0 == 0) {
-    small->rec_used = 0;
-    small->total = 0;
-    small->q_n = 0;
-    first_doc[n_chunks] = n_docs + 1;
-  }
-  for (int64_t c = t0; c < n_chunks; c += stride) {
-    const int64_t target = c * kChunk;
-    int64_t lo = 0, hi = n_docs + 1;  // first k with doc_offsets[k] >= target
-    while (lo < hi) {
-      int64_t mid = (lo + hi) >> 1;
-      if (doc_offsets[mid] < target) lo = mid + 1;
-      else hi = mid;
-    }
-    first_doc[c] = lo;
-  }
-  bool bad = false;
-  for (int64_t k = t0; k <= n_docs; k += stride) {
-    int64_t o = doc_offsets[k];
-    if (o < 0 || o > n_bytes) bad = true;
-    if (k < n_docs && doc_offsets[k + 1] < o) bad = true;
-  }
-  if (bad) atomicOr(&small->status, kStBadInput);
-}
-
-struct EncodeArgs {
-  const uint8_t* bytes;
-  int64_t n_bytes;
-  const int64_t* doc_offsets;
-  int64_t n_docs;
-  int64_t* out_offsets;
-  int32_t* pool;  // long pre-token scratch, one int32 per input byte
-  Tables T;
-  Cache C;
-  const uint32_t* start_bits;  // pre-token start bitmask of all n_bytes
-  uint32_t* stage;             // [n_chunks][kStage] ids of short pre-tokens
-  uint64_t* chunk_meta;        // per chunk: token count | (record index + 1) << 32
-  uint32_t* rec;               // long pre-token records
-  uint64_t rec_cap;            // u32 words of rec
-  uint32_t* def_n;             // per chunk: cache misses handed to k_misses
-  uint32_t* def_rec;           // [n_chunks][kMaxDefer][3] their records
-  uint64_t* queue;             // (chunk << 8 | slot) of each deferred miss
-  const int64_t* first_doc;
-  DevSmall* small;
-  int64_t n_chunks;
-};
-
-// Encodes chunk blockIdx.x without waiting on any other chunk: its ids go to
-// its stage region (short pre-tokens) or stay in the pool (long ones, listed
-// in a record), its count to chunk_meta, and its documents' offsets are
-// written relative to the chunk. Its cache misses either get reserved stage
-// ranges that k_misses fills, or are merged here. k_scan_tiles,
-// k_scan_tile_sums and k_compact finish the call.
-__global__ void __launch_bounds__(kThreads, kEncodeCtasPerSm) k_encode(EncodeArgs a) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
-  const int tid = threadIdx.x;
-  const int64_t c = blockIdx.x;
-  const int64_t c0 = c * kChunk;
-  // The documents starting in the chunk are k_first .. k_next - 1 (k_prep's
-  // first document of this chunk and of the next; the loads overlap the
-  // window's). Ahead of their use at the end, the offsets of the first
-  // kThreads of them, one per thread.
-  const int64_t k_first = __ldg(a.first_doc + c), k_next = __ldg(a.first_doc + c + 1);
-  load_encode_window(S, a.bytes, a.n_bytes, a.doc_offsets, a.n_docs, a.start_bits, c0);
-  const int64_t d_mine = k_first + tid < k_next ? __ldg(a.doc_offsets + k_first + tid) : c0;
-
-  // Pre-tokens starting in the chunk, in order. Thread t owns positions
-  // [16 t, 16 t + 16) of the chunk.
-  {
-    const uint32_t bits = (S.startbits[tid >> 1] >> ((tid & 1) * 16)) & 0xFFFFu;
-    uint32_t total;
-    uint32_t pos = block_excl_scan<false>(__popc(bits), S.red, &total);
-    S.grp_pos[tid] = (uint16_t)pos;
-    uint32_t b = bits;
-    while (b) {
-      int k = __ffs(b) - 1;
-      b &= b - 1;
-      S.span_start[pos++] = (uint16_t)(tid * 16 + k);
-    }
-    if (tid == 0) {
-      S.n_spans = total;
-      S.n_long = 0;
-      S.n_miss = 0;
-      S.n_miss_m = 0;
-      S.n_def = 0;
-      S.doc_k0 = k_first;
-      S.doc_k1 = k_next;
-      if (total == 0) {
-        S.last_end = -1;
-        S.last_end_rel = -1;
-      }
-    }
-    // The thread holding the chunk's last start finds where that pre-token
-    // ends: the next start, or the first byte outside every document, in the
-    // window; -1 when it runs past the window.
-    if (bits != 0 && pos == total) {
-      const int from = tid * 16 + (31 - __clz(bits)) + 1;
-      int end = -1;
-      for (int wj = from >> 5; wj < kSpanWords; ++wj) {
-        uint32_t m = S.startbits[wj] | bits32_at(S.outbits, kHalo + wj * 32);
-        if (wj == (from >> 5)) m &= 0xFFFFFFFFu << (from & 31);
-        if (m) {
-          end = wj * 32 + __ffs(m) - 1;
-          break;
-        }
-      }
-      S.last_end_rel = end;
-      S.last_end = end < 0 ? -1 : c0 + end;
-    }
-  }
-  cta_sync();
-  const uint32_t n_spans = S.n_spans;
-  const int last_end = S.last_end_rel;
-  // The document offset has arrived by now: keep it relative to the chunk
-  // (-1 outside it, which only malformed offsets give) to spare registers.
-  const int d_rel = d_mine < c0 || d_mine >= c0 + kChunk ? -1 : (int)(d_mine - c0);
-
-  // Short pre-tokens, one thread each, kProbeRound per round with their
-  // word-cache probes in flight together (a thread keeps each probe's key
-  // words, entry and one word of start, length and flags; the slot is
-  // recomputed only if the probe goes past it). Hits finish here; misses are
-  // marked and counted, and handled next, so a warp does not wait on the
-  // merge loop of a few of its lanes.
-  uint32_t my_misses = 0;
-  for (uint32_t j0 = tid; j0 < n_spans; j0 += kProbeRound * kThreads) {
-    // per probe: start | length << 12 | present << 30 | probed << 31 (a
-    // length above kShortMax: long)
-    uint32_t sl[kProbeRound];
-    CacheKey K[kProbeRound];
-    uint4 ea[kProbeRound], eb[kProbeRound];
-#pragma unroll
-    for (int h = 0; h < kProbeRound; ++h) {
-      const uint32_t j = j0 + (uint32_t)h * kThreads;
-      sl[h] = 0;
-      if (j < n_spans) {
-        const int st = S.span_start[j];
-        const int en = (j + 1 < n_spans) ? (int)S.span_start[j + 1] : last_end;
-        const int len = en < 0 ? kSpan : en - st;
-        sl[h] = (uint32_t)st | (uint32_t)len << 12 | 1u << 30;
-        if (len <= kCacheMaxLen && a.C.enabled) {
-          K[h] = cache_key_words(S, st, len);
-          const uint32_t slot = cache_slot(K[h], (uint32_t)len, a.C);
-          ldg32(a.C.e + 2 * slot, ea[h], eb[h]);
-          sl[h] |= 1u << 31;
-        }
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < kProbeRound; ++h) {
-      const uint32_t j = j0 + (uint32_t)h * kThreads;
-      if (!(sl[h] & (1u << 30))) continue;
-      const int st = (int)(sl[h] & 0xFFFu);
-      const uint32_t len = (sl[h] >> 12) & 0x3FFFu;
-      if (len <= (uint32_t)kShortMax) {
-        uint32_t ids[kCacheMaxIds];
-        const uint32_t cnt = (sl[h] >> 31) ? cache_resolve(a.C, K[h], len, ea[h], eb[h], ids) : 0u;
-        if (cnt) {
-#pragma unroll
-          for (uint32_t q = 0; q < (uint32_t)kCacheMaxIds; ++q)
-            if (q < cnt) S.sym[st + q] = ids[q];
-          S.span_cnt[j] = cnt;
-        } else {
-          S.span_cnt[j] = kMissMark | len;
-          ++my_misses;
-        }
-      } else {
-        const uint32_t ql = atomicAdd(&S.n_long, 1u);
-        if (ql < (uint32_t)kMaxLong) S.long_list[ql] = (uint16_t)j;
-        else atomicOr(&a.small->status, kStInternal);
-        S.span_cnt[j] = 0;
-      }
-    }
-  }
-  my_misses = __reduce_add_sync(0xFFFFFFFFu, my_misses);
-  if ((tid & 31) == 0 && my_misses) atomicAdd(&S.n_def, my_misses);
-  cta_sync();
-  // Cache misses. When the chunk's slots suffice they all go to k_misses:
-  // each keeps its byte length of ids reserved (ids never outnumber bytes)
-  // and gets a record and a queue entry with the chunk's ids further on.
-  // Otherwise they are merged here by lane groups. Each thread owns a
-  // contiguous run of spans [run0, run1), in this and every later step.
-  const uint32_t per = (n_spans + kThreads - 1) / kThreads;
-  const uint32_t run0 = min(n_spans, tid * per), run1 = min(n_spans, run0 + per);
-  const uint32_t n_def = S.n_def;
-  const bool defer = a.queue != nullptr && n_def <= kMaxDefer;
-  uint32_t q_base = 0;  // thread 0: the chunk's queue entries, needed only once its ids are written
-  if (defer && tid == 0 && n_def) q_base = atomicAdd(&a.small->q_n, n_def);
-  if (!defer) {
-    // the byte -> symbol map, for the merges (loaded only when a chunk merges)
-    for (int i = tid; i < 256; i += kThreads) S.byte_id[i] = a.T.byte_id[i];
-    cta_sync();
-    for (uint32_t j = run0; j < run1; ++j) {
-      const uint32_t v = S.span_cnt[j];
-      if (!(v & kMissMark)) continue;
-      const int len = (int)(v & 0xFFu), st = S.span_start[j];
-      if (len <= kCacheMaxLen) {
-        const uint32_t qs = atomicAdd(&S.n_miss, 1u);
-        if (qs < kMissShortCap) S.missq[qs] = (uint16_t)j;
-        else S.span_cnt[j] = merge_at(S, st, len, a.T);  // queue full: merge here
-      } else {
-        const uint32_t qm = atomicAdd(&S.n_miss_m, 1u);
-        if (qm < kMissMedCap) S.missq[kMissShortCap + qm] = (uint16_t)j;
-        else S.span_cnt[j] = merge_at(S, st, len, a.T);
-      }
-    }
-    cta_sync();
-    if (tid < 32 * kMergeWarps) {
-      // Queued misses, by the first kMergeWarps warps: up to 16 bytes by
-      // groups of 8 lanes, longer ones by a warp each.
-      GroupScratch& W = S.u.grp[tid >> 5];
-      const uint32_t n_short = min(S.n_miss, kMissShortCap), n_med = min(S.n_miss_m, kMissMedCap);
-      for (uint32_t q0 = 0; q0 < n_short; q0 += 4 * kMergeWarps) {
-        const uint32_t q = q0 + (uint32_t)(tid >> 3);
-        uint32_t j = 0, n = 0;
-        int st = 0;
-        if (q < n_short) {
-          j = S.missq[q];
-          st = S.span_start[j];
-          n = (uint32_t)(((j + 1 < n_spans) ? (int)(S.span_start[j + 1] & ~kDeferFlag) : last_end) - st);
-        }
-        const uint32_t cnt = merge_group<8>(W, S.win + kHalo + st, n, a.T, S.byte_id, S.sym + st);
-        if (q < n_short && (tid & 7) == 0) S.span_cnt[j] = cnt;
-      }
-      for (uint32_t q0 = 0; q0 < n_med; q0 += kMergeWarps) {
-        const uint32_t q = q0 + (uint32_t)(tid >> 5);
-        uint32_t j = 0, n = 0;
-        int st = 0;
-        if (q < n_med) {
-          j = S.missq[kMissShortCap + q];
-          st = S.span_start[j];
-          n = (uint32_t)(((j + 1 < n_spans) ? (int)(S.span_start[j + 1] & ~kDeferFlag) : last_end) - st);
-        }
-        const uint32_t cnt = merge_group<32>(W, S.win + kHalo + st, n, a.T, S.byte_id, S.sym + st);
-        if (q < n_med && (tid & 31) == 0) S.span_cnt[j] = cnt;
-      }
-    }
-    cta_sync();
-  }
-
-  // Long pre-tokens: the whole CTA, one at a time, in order.
-  const uint32_t n_long = min(S.n_long, (uint32_t)kMaxLong);
-  if (n_long > 0) {
-    for (int i = tid; i < 256; i += kThreads) S.byte_id[i] = a.T.byte_id[i];
-    if (tid == 0 && n_long > 1) {  // sort the short list (insertion sort)
-      for (uint32_t x = 1; x < n_long; ++x) {
-        uint16_t v = S.long_list[x];
-        int y = (int)x - 1;
-        while (y >= 0 && S.long_list[y] > v) {
-          S.long_list[y + 1] = S.long_list[y];
-          --y;
-        }
-        S.long_list[y + 1] = v;
-      }
-    }
-    cta_sync();
-    LongScratch L{S.u.stage, S.red, S.carry};
-    for (uint32_t x = 0; x < n_long; ++x) {
-      const uint32_t j = S.long_list[x];
-      const int64_t s = c0 + (S.span_start[j] & ~kDeferFlag);
-      int64_t e = (j + 1 < n_spans) ? c0 + (S.span_start[j + 1] & ~kDeferFlag) : S.last_end;
-      if (e < 0) {
-        // Runs past the window: find the document it lies in, then the next
-        // pre-token start after the window.
-        if (tid == 0) {
-          int64_t lo = 0, hi = a.n_docs + 1;  // first k with doc_offsets[k] > s
-          while (lo < hi) {
-            int64_t mid = (lo + hi) >> 1;
-            if (a.doc_offsets[mid] <= s) lo = mid + 1;
-            else hi = mid;
-          }
-          int64_t k = lo - 1;
-          int64_t dlo = (k >= 0) ? a.doc_offsets[k] : 0;
-          int64_t dhi = (k >= 0 && k < a.n_docs) ? a.doc_offsets[k + 1] : s + 1;
-          if (dhi > a.n_bytes) dhi = a.n_bytes;
-          if (dlo > s) dlo = s;
-          if (dlo < 0) dlo = 0;
-          if (dhi <= s) dhi = s + 1;
-          S.doc_lo = dlo;
-          S.doc_hi = dhi;
-        }
-        cta_sync();
-        const int64_t dlo = S.doc_lo, dhi = S.doc_hi;
-        int64_t found = dhi;
-        for (int64_t base = c0 + kSpan; base < dhi; base += kThreads) {
-          const int64_t p = base + tid;
-          bool b = p < dhi && starts_piece<int64_t>(a.bytes, dlo, dhi, p);
-          uint32_t cand = b ? (uint32_t)(p - base) : kInf;
-          uint32_t m = block_min(cand, S.red);
-          if (m != kInf) {
-            found = base + m;
-            break;
-          }
-        }
-        e = found;
-      }
-      const int64_t n = e - s;
-      if (n <= 0 || n >= (int64_t)0x7FFFFFFF) {
-        if (tid == 0) atomicOr(&a.small->status, kStInternal);
-        if (tid == 0) S.long_cnt[x] = 0;
-      } else {
-        uint32_t cnt = merge_long(a.bytes, s, (uint32_t)n, a.pool + s, a.T, S.byte_id, L);
-        if (tid == 0) S.long_cnt[x] = cnt;
-      }
-      cta_sync();
-    }
-  }
-
-  // Token offsets within the chunk without the long pre-tokens' ids (= stage
-  // offsets; a long pre-token counts 0 here), and the deferred misses' slots
-  // (in span order). Each thread scans a contiguous run of spans [run0,
-  // run1); it also stores their ids at the end, so consecutive threads write
-  // consecutive ranges. A deferred miss counts its reserved ids and is
-  // flagged.
-  uint32_t agg = 0, slot = 0;
-  {
-    uint32_t sum = 0, nm = 0;
-    for (uint32_t j = run0; j < run1; ++j) {
-      const uint32_t v = S.span_cnt[j];
-      const bool miss = v & kMissMark;
-      sum += miss ? v & 0xFFu : v;
-      nm += miss;
-    }
-    uint32_t base, def_all;
-    block_excl_scan2(sum, nm, S.red, &base, &slot, &agg, &def_all);
-    for (uint32_t j = run0; j < run1; ++j) {
-      uint32_t v = S.span_cnt[j];
-      if (v & kMissMark) {
-        v &= 0xFFu;
-        S.span_start[j] |= kDeferFlag;
-      }
-      S.span_cnt[j] = (uint16_t)base;
-      base += v;
-    }
-    if (tid == 0) {
-      S.span_cnt[n_spans] = (uint16_t)agg;
-      S.q_base = q_base;
-    }
-  }
-  cta_sync();
-
-  // Long pre-tokens: one record block per chunk, {n_long, then per long
-  // pre-token {offset in the chunk, first byte (low, high 32 bits), count}}.
-  // Offsets in the chunk count every id before: the stage offset plus the
-  // ids of the long pre-tokens before.
-  if (tid == 0) {
-    uint64_t meta = agg;
-    for (uint32_t x = 0; x < n_long; ++x) meta += S.long_cnt[x];
-    if (n_long > 0) {
-      const uint32_t words = 1 + 4 * n_long;
-      const uint32_t r = atomicAdd(&a.small->rec_used, words);
-      if ((uint64_t)r + words <= a.rec_cap) {
-        a.rec[r] = n_long;
-        uint32_t long_before = 0;
-        for (uint32_t x = 0; x < n_long; ++x) {
-          const uint32_t j = S.long_list[x];
-          const uint64_t s = (uint64_t)(c0 + (S.span_start[j] & ~kDeferFlag));
-          uint32_t* e = a.rec + r + 1 + 4 * x;
-          e[0] = S.span_cnt[j] + long_before;
-          e[1] = (uint32_t)s;
-          e[2] = (uint32_t)(s >> 32);
-          e[3] = S.long_cnt[x];
-          long_before += S.long_cnt[x];
-        }
-        meta |= (uint64_t)(r + 1) << 32;
-      } else {
-        atomicOr(&a.small->status, kStInternal);
-      }
-    }
-    a.chunk_meta[c] = meta;
-    if (a.def_n) a.def_n[c] = defer ? n_def : 0u;
-  }
-
-  // The chunk's documents again (kept in shared memory, not in registers),
-  // for their offsets at the end.
-  const int64_t k_first_end = S.doc_k0, k_next_end = S.doc_k1;
-
-  // Ids of short pre-tokens to the chunk's stage region, each thread its own
-  // run, in output order without the long pre-tokens' ids. A deferred miss
-  // leaves its reserved range to k_misses and gets a record
-  // {offset in the chunk, start | reserved << 12 | stage offset << 19, ids}
-  // in slot order (= span order) and a queue entry.
-  {
-    uint32_t* stage = a.stage + c * kStage;
-    for (uint32_t j = run0; j < run1; ++j) {
-      bool is_long = false;
-      uint32_t long_before = 0;
-      for (uint32_t x = 0; x < n_long; ++x) {
-        const uint32_t lj = S.long_list[x];
-        is_long |= lj == j;
-        if (lj < j) long_before += S.long_cnt[x];
-      }
-      if (is_long) continue;
-      const uint32_t raw = S.span_start[j];
-      const int st = (int)(raw & ~(uint32_t)kDeferFlag);
-      const uint32_t o = S.span_cnt[j], cnt = (uint32_t)S.span_cnt[j + 1] - o;
-      if (raw & kDeferFlag) {
-        uint32_t* R = a.def_rec + ((uint64_t)c * kMaxDefer + slot) * 3;
-        R[0] = o + long_before;
-        R[1] = (uint32_t)st | cnt << 12 | o << 19;
-        R[2] = cnt;
-        a.queue[S.q_base + slot] = (uint64_t)c << 8 | slot;
-        ++slot;
-        continue;
-      }
-      if (cnt <= (uint32_t)kCacheMaxIds) {  // a cache hit: at most three ids, without a loop
-#pragma unroll
-        for (uint32_t q = 0; q < (uint32_t)kCacheMaxIds; ++q)
-          if (q < cnt) stage[o + q] = S.sym[st + q];
-      } else {
-        for (uint32_t q = 0; q < cnt; ++q) stage[o + q] = S.sym[st + q];
-      }
-    }
-  }
-
-  // Offsets of the documents that start in this chunk, relative to the
-  // chunk's first id (k_compact adds the chunk's offset).
-  {
-    for (int64_t k = k_first_end + tid; k < k_next_end; k += kThreads) {
-      const int64_t d = k == k_first_end + tid ? (d_rel < 0 ? -1 : c0 + d_rel) : a.doc_offsets[k];
-      if (d >= c0 && d < c0 + kChunk) {
-      // the first pre-token starting at or after d: those before d's 16-byte
-      // group, plus the group's starts before d
-        const int rel = (int)(d - c0), t = rel >> 4;
-        const uint32_t gbits = (S.startbits[t >> 1] >> ((t & 1) * 16)) & ((1u << (rel & 15)) - 1u);
-        const uint32_t r = S.grp_pos[t] + __popc(gbits);
-        int64_t o = S.span_cnt[r];
-        for (uint32_t x = 0; x < n_long; ++x)
-          if (S.long_list[x] < r) o += S.long_cnt[x];
-        a.out_offsets[k] = o;
-      }
-    }
-  }
-}
-
-// Cache misses that k_encode handed over, merged across the whole GPU: a
-// queue entry (chunk << 8 | slot) names a record {offset, start | reserved <<
-// 12 | stage offset << 19, ids}, reserved = the miss's byte length. A warp
-// takes 32 entries at a time, one per lane. A lane merges its own miss of up
-// to 8 bytes (merge_thread); then, in rounds, groups of 8 lanes take the
-// misses of 9 to 16 bytes, groups of 16 those of 17 to 32, and the whole warp
-// each longer one (merge_group). Each writes its ids into its reserved stage range, the
-// count into its record, and gives the unused part of the reservation back to
-// the chunk's count.
-// One thread merges a pre-token of n <= 8 bytes: symbols, pair ranks and
-// merged ids in its own column of shared memory (x[i * kThreads], so the
-// threads of a warp use distinct banks). A step takes the lowest rank,
-// replaces its occurrences left to right without overlap while compacting,
-// and looks up again only the pairs next to a merged symbol, two at a time.
-// The final ids go to out[0 .. count).
-constexpr int kTinyMax = 8;
-struct TinyScratch {
-  uint32_t sy[kTinyMax * kThreads], rk[kTinyMax * kThreads], nw[kTinyMax * kThreads];
-};
-
-__device__ uint32_t merge_thread(TinyScratch& Z, const uint8_t* src, uint32_t n, const Tables& T,
-                                 const int32_t* byte_id, uint32_t* out) {
-  uint32_t* sy = Z.sy + threadIdx.x;
-  uint32_t* rk = Z.rk + threadIdx.x;
-  uint32_t* nw = Z.nw + threadIdx.x;
-  for (uint32_t i = 0; i < n; ++i) sy[i * kThreads] = (uint32_t)byte_id[src[i]];
-  uint32_t redo = n > 1 ? (1u << (n - 1)) - 1u : 0u;  // pairs to look up
-  for (;;) {
-    while (redo) {
-      const uint32_t p1 = __ffs(redo) - 1;
-      redo &= redo - 1;
-      const uint32_t p2 = redo ? __ffs(redo) - 1 : kNone;
-      redo &= redo - 1;
-      uint32_t r1, w1, r2 = kInf, w2 = 0;
-      lookup_pair2(T, sy[p1 * kThreads], sy[(p1 + 1) * kThreads], p2 != kNone ? sy[p2 * kThreads] : kNone,
-                   p2 != kNone ? sy[(p2 + 1) * kThreads] : 0u, &r1, &w1, &r2, &w2);
-      rk[p1 * kThreads] = r1;
-      nw[p1 * kThreads] = w1;
-      if (p2 != kNone) {
-        rk[p2 * kThreads] = r2;
-        nw[p2 * kThreads] = w2;
-      }
-    }
-    uint32_t best = kInf;
-    for (uint32_t i = 0; i + 1 < n; ++i) best = min(best, rk[i * kThreads]);
-    if (best == kInf) break;
-    uint32_t m = 0;
-    for (uint32_t i = 0; i < n; ++m) {
-      if (i + 1 < n && rk[i * kThreads] == best) {
-        sy[m * kThreads] = nw[i * kThreads];
-        redo |= (1u << m) | (m ? 1u << (m - 1) : 0u);  // the merged symbol's pairs
-        i += 2;
-      } else {
-        sy[m * kThreads] = sy[i * kThreads];
-        rk[m * kThreads] = rk[i * kThreads];
-        nw[m * kThreads] = nw[i * kThreads];
-        i += 1;
-      }
-    }
-    n = m;
-    redo &= n > 1 ? (1u << (n - 1)) - 1u : 0u;
-  }
-  for (uint32_t i = 0; i < n; ++i) out[i] = sy[i * kThreads];
-  return n;
-}
-
-constexpr int kMissBlocksPerSm = 5;  // resident at once (48 registers a thread)
-__global__ void __launch_bounds__(kThreads, kMissBlocksPerSm) k_misses(const uint8_t* bytes, const uint64_t* queue,
-                                                                       const DevSmall* small, uint32_t* def_rec,
-                                                                       uint32_t* stage, uint64_t* chunk_meta,
-                                                                       Tables T) {
-  __shared__ GroupScratch grp[kThreads / 32];
-  __shared__ TinyScratch tiny;
-  __shared__ int32_t byte_id[256];
-  for (int i = threadIdx.x; i < 256; i += kThreads) byte_id[i] = T.byte_id[i];
-  __syncthreads();
-  const uint32_t n_q = small->q_n;
-  const int lane = threadIdx.x & 31;
-  GroupScratch& W = grp[threadIdx.x >> 5];
-  const uint64_t warps = (uint64_t)gridDim.x * (kThreads / 32);
-  for (uint64_t q0 = ((uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * 32; q0 < n_q; q0 += warps * 32) {
-    uint64_t e = 0;
-    uint32_t w = 0;
-    if (q0 + lane < n_q) {
-      e = queue[q0 + lane];
-      w = def_rec[((e >> 8) * kMaxDefer + (e & 0xFFu)) * 3 + 1];
-    }
-    const uint32_t len = (w >> 12) & 0x7Fu;  // 0: no entry
-    uint32_t m4 = __ballot_sync(0xFFFFFFFFu, len != 0 && len <= 8u);
-    uint32_t m8 = __ballot_sync(0xFFFFFFFFu, len > 8u && len <= (uint32_t)kCacheMaxLen);
-    uint32_t m16 = __ballot_sync(0xFFFFFFFFu, len > (uint32_t)kCacheMaxLen && len <= 32u);
-    uint32_t m32 = __ballot_sync(0xFFFFFFFFu, len > 32u);
-    // One round: group g of G lanes takes the g-th entry of *mask (none past
-    // its end); the round's entries leave the mask.
-    auto round = [&](uint32_t* mask, auto merge, int G) {
-      const int g = lane / G;
-      uint32_t mm = *mask;
-      for (int x = 0; x < g; ++x) mm &= mm - 1u;
-      const bool on = mm != 0;
-      const int src = on ? __ffs(mm) - 1 : 0;
-      for (int x = 0; x < 32 / G; ++x) *mask &= *mask - 1u;
-      const uint64_t ge = __shfl_sync(0xFFFFFFFFu, e, src);
-      const uint32_t gw = __shfl_sync(0xFFFFFFFFu, w, src);
-      const uint64_t c = ge >> 8;
-      const uint32_t n = on ? (gw >> 12) & 0x7Fu : 0u;
-      const uint32_t cnt = merge(bytes + c * kChunk + (gw & 0xFFFu), n, stage + c * kStage + (gw >> 19));
-      if (on && (lane & (G - 1)) == 0) {
-        def_rec[(c * kMaxDefer + (ge & 0xFFu)) * 3 + 2] = cnt;
-        atomicAdd(reinterpret_cast<unsigned long long*>(chunk_meta + c), 0ull - (unsigned long long)(n - cnt));
-      }
-    };
-    if ((m4 >> lane) & 1u) {  // up to 8 bytes: each lane its own
-      const uint64_t c = e >> 8;
-      const uint32_t cnt = merge_thread(tiny, bytes + c * kChunk + (w & 0xFFFu), len, T, byte_id,
-                                        stage + c * kStage + (w >> 19));
-      def_rec[(c * kMaxDefer + (e & 0xFFu)) * 3 + 2] = cnt;
-      atomicAdd(reinterpret_cast<unsigned long long*>(chunk_meta + c), 0ull - (unsigned long long)(len - cnt));
-    }
-    __syncwarp();
-    while (m8)
-      round(&m8, [&](const uint8_t* src, uint32_t n, uint32_t* out) { return merge_group<8>(W, src, n, T, byte_id, out); }, 8);
-    while (m16)
-      round(&m16, [&](const uint8_t* src, uint32_t n, uint32_t* out) { return merge_group<16>(W, src, n, T, byte_id, out); }, 16);
-    while (m32)
-      round(&m32, [&](const uint8_t* src, uint32_t n, uint32_t* out) { return merge_group<32>(W, src, n, T, byte_id, out); }, 32);
-  }
-}
-
-// Exclusive prefix sum of the chunks' token counts in two levels: k_scan_tiles
-// scans tiles of kScanThreads chunks (coalesced, one chunk per thread) into
-// chunk_off and writes each tile's total; k_scan_tile_sums (one CTA) turns
-// the tile totals into exclusive tile offsets and small->total. k_compact
-// adds the two.
-constexpr int kScanThreads = 1024;
-
-__device__ uint64_t block_excl_scan64(uint64_t v, uint64_t* red, uint64_t* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint64_t incl = v;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const uint64_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-    if (lane >= d) incl += o;
-  }
-  if (lane == 31) red[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const uint64_t x = lane < (int)(blockDim.x >> 5) ? red[lane] : 0;
-    uint64_t xi = x;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const uint64_t o = __shfl_up_sync(0xFFFFFFFFu, xi, d);
-      if (lane >= d) xi += o;
-    }
-    red[lane] = xi - x;
-    if (lane == 31) red[32] = xi;
-  }
-  __syncthreads();
-  const uint64_t r = red[warp] + incl - v;
-  *total = red[32];
-  __syncthreads();
-  return r;
-}
-
-__global__ void __launch_bounds__(kScanThreads) k_scan_tiles(const uint64_t* chunk_meta, int64_t n_chunks,
-                                                             uint64_t* chunk_off, uint64_t* tile_sum) {
-  __shared__ uint64_t red[33];
-  const int64_t c = (int64_t)blockIdx.x * kScanThreads + threadIdx.x;
-  const uint64_t v = c < n_chunks ? (chunk_meta[c] & 0xFFFFFFFFull) : 0;
-  uint64_t total;
-  const uint64_t e = block_excl_scan64(v, red, &total);
-  if (c < n_chunks) chunk_off[c] = e;
-  if (threadIdx.x == 0) tile_sum[blockIdx.x] = total;
-}
-
-__global__ void __launch_bounds__(kScanThreads) k_scan_tile_sums(uint64_t* tile_sum, int64_t n_tiles, DevSmall* small) {
-  __shared__ uint64_t red[33];
-  uint64_t carry = 0;
-  for (int64_t base = 0; base < n_tiles; base += kScanThreads) {
-    const int64_t t = base + threadIdx.x;
-    const uint64_t v = t < n_tiles ? tile_sum[t] : 0;
-    uint64_t total;
-    const uint64_t e = block_excl_scan64(v, red, &total);
-    if (t < n_tiles) tile_sum[t] = carry + e;
-    carry += total;
-  }
-  if (threadIdx.x == 0) small->total = (int64_t)carry;
-}
-
-// One warp per chunk: chunk c's ids to their place in out_ids (short
-// pre-tokens from the stage region, long ones from the pool, in order) and
-// its documents' offsets made absolute. Ids past out_capacity are not written.
-constexpr int kCompactWarps = 8;
-
-__global__ void __launch_bounds__(32 * kCompactWarps, 8) k_compact(const uint32_t* stage, const int32_t* pool,
-                                                                const uint64_t* chunk_meta, const uint64_t* chunk_off,
-                                                                const uint64_t* tile_off, const uint32_t* rec,
-                                                                const uint32_t* def_n, const uint32_t* def_rec,
-                                                                const int64_t* first_doc, int64_t n_chunks,
-                                                                int64_t n_docs, int32_t* out_ids, int64_t out_capacity,
-                                                                int64_t* out_offsets, DevSmall* small) {
-  const int lane = threadIdx.x & 31;
-  const int64_t c = (int64_t)blockIdx.x * kCompactWarps + (threadIdx.x >> 5);
-  if (c >= n_chunks) return;
-  const uint64_t meta = chunk_meta[c];
-  const uint32_t cnt = (uint32_t)meta;
-  const uint32_t r1 = (uint32_t)(meta >> 32);  // record index + 1, 0 without long pre-tokens
-  const int64_t P = (int64_t)(chunk_off[c] + tile_off[c / kScanThreads]);
-  const uint32_t* src = stage + c * kStage;
-  if (lane == 0 && P + (int64_t)cnt > out_capacity) atomicOr(&small->status, kStCapacity);
-  const int64_t lim = out_capacity - P;
-  const uint32_t nd = def_n ? def_n[c] : 0u;
-  const uint32_t* D = def_rec + (uint64_t)c * kMaxDefer * 3;
-  // Deferred misses left holes in the chunk's ids (reserved ids they did not
-  // use). Output position q is reserved-layout position q + gap(q), gap(q)
-  // the holes before it. Miss d's ids end at output position
-  // E_d = U_d + used_d - (holes of the misses before d), strictly increasing
-  // in d, and gap(q) is the holes of the misses with E_d <= q. For up to 32
-  // misses lane d holds E_d and the inclusive sum of holes (Gi); with more,
-  // each lane walks the records.
-  const bool in_lanes = nd <= 32;
-  uint32_t E = 0xFFFFFFFFu, Gi = 0, Ud = 0xFFFFFFFFu;
-  if (in_lanes) {
-    uint32_t hole = 0;
-    if ((uint32_t)lane < nd) {
-      Ud = D[3 * lane];
-      const uint32_t used = D[3 * lane + 2];
-      hole = ((D[3 * lane + 1] >> 12) & 0x7Fu) - used;
-      E = Ud + used;
-    }
-    Gi = hole;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, Gi, o);
-      if (lane >= o) Gi += t;
-    }
-    if ((uint32_t)lane < nd) E -= Gi - hole;
-  }
-  // gap for q = base + lane (all lanes together; in_lanes only)
-  auto gap_at = [&](uint32_t base) -> uint32_t {
-    const uint32_t rel = E - base;
-    const uint32_t win = __reduce_or_sync(0xFFFFFFFFu, rel < 32u ? 1u << rel : 0u);
-    const uint32_t j = __popc(__ballot_sync(0xFFFFFFFFu, E < base)) + __popc(win & ((2u << lane) - 1u));
-    const uint32_t g = __shfl_sync(0xFFFFFFFFu, Gi, (int)(j ? j - 1 : 0));
-    return j ? g : 0u;
-  };
-  const uint32_t* R = r1 ? rec + (r1 - 1) : nullptr;
-  const uint32_t n_long = R ? R[0] : 0u;
-  // reserved-layout position u to the id (pool for long pre-tokens, else the
-  // stage without the long pre-tokens' ids)
-  auto id_at = [&](uint32_t u) -> int32_t {
-    uint32_t shift = 0;
-    for (uint32_t x = 0; x < n_long; ++x) {
-      const uint32_t off = R[1 + 4 * x], lc = R[4 + 4 * x];
-      if (u < off) break;
-      if (u < off + lc) {
-        const uint64_t sp = (uint64_t)R[2 + 4 * x] | ((uint64_t)R[3 + 4 * x] << 32);
-        return pool[sp + (u - off)];
-      }
-      shift += lc;
-    }
-    return (int32_t)src[u - shift];
-  };
-  if (in_lanes && r1 == 0) {
-    constexpr int kUnroll = 8;  // loads in flight per lane
-    for (uint32_t q0 = 0; q0 < cnt; q0 += 32 * kUnroll) {
-      uint32_t v[kUnroll];
-#pragma unroll
-      for (int k = 0; k < kUnroll; ++k) {
-        const uint32_t base = q0 + 32 * k, q = base + lane;
-        const uint32_t gap = nd ? gap_at(base) : 0u;
-        v[k] = q < cnt ? src[q + gap] : 0u;
-      }
-#pragma unroll
-      for (int k = 0; k < kUnroll; ++k) {
-        const uint32_t q = q0 + 32 * k + lane;
-        if (q < cnt && (int64_t)q < lim) out_ids[P + q] = (int32_t)v[k];
-      }
-    }
-  } else if (in_lanes) {
-    for (uint32_t q0 = 0; q0 < cnt; q0 += 32) {
-      const uint32_t q = q0 + lane;
-      const uint32_t gap = nd ? gap_at(q0) : 0u;
-      if (q < cnt && (int64_t)q < lim) out_ids[P + q] = id_at(q + gap);
-    }
-  } else {
-    uint32_t d = 0, gap = 0;  // per lane: misses passed and their holes
-    for (uint32_t q = lane; q < cnt; q += 32) {
-      if ((int64_t)q >= lim) break;
-      while (d < nd) {
-        const uint32_t U = D[3 * d], res = (D[3 * d + 1] >> 12) & 0x7Fu, used = D[3 * d + 2];
-        if (q + gap < U + used) break;
-        gap += res - used;
-        ++d;
-      }
-      out_ids[P + q] = id_at(q + gap);
-    }
-  }
-  // Document offsets: k_encode wrote them in the reserved layout; take back
-  // the holes of the misses that start before each (U_d is increasing: a
-  // search over the lanes, or a walk over the records).
-  const int64_t k_lo = first_doc[c];
-  const int64_t k_hi = first_doc[c + 1] < n_docs + 1 ? first_doc[c + 1] : n_docs + 1;
-  for (int64_t k0 = k_lo; k0 < k_hi; k0 += 32) {
-    const int64_t k = k0 + lane;
-    const int64_t o = k < k_hi ? out_offsets[k] : 0;
-    int64_t fix = 0;
-    if (in_lanes) {
-      uint32_t j = 0;  // misses with U_d < o: first among lanes 0..30, then lane 31
-#pragma unroll
-      for (uint32_t step = 16; step > 0; step >>= 1) {
-        const uint32_t u = __shfl_sync(0xFFFFFFFFu, Ud, (int)(j + step - 1));
-        if ((int64_t)u < o) j += step;
-      }
-      if ((int64_t)__shfl_sync(0xFFFFFFFFu, Ud, (int)j) < o) ++j;
-      const uint32_t g = __shfl_sync(0xFFFFFFFFu, Gi, (int)(j ? j - 1 : 0));
-      fix = j ? g : 0;
-    } else {
-      for (uint32_t d = 0; d < nd; ++d) {
-        if ((int64_t)D[3 * d] >= o) break;
-        fix += (int64_t)((D[3 * d + 1] >> 12) & 0x7Fu) - (int64_t)D[3 * d + 2];
-      }
-    }
-    if (k < k_hi) out_offsets[k] = o - fix + P;
-  }
-}
-
-// Pre-tokenizer alone: start bits of [c0, c0 + kSplitChunk) for chunk
-// blockIdx.x (first_doc, when given, is indexed by 4 KiB chunk).
-__global__ void __launch_bounds__(kThreads) k_pretokenize(const uint8_t* bytes, int64_t n_bytes,
-                                                          const int64_t* doc_offsets, int64_t n_docs,
-                                                          const int64_t* first_doc, uint32_t* out_bits) {
-  __shared__ SplitWin S;
-  const int64_t c0 = (int64_t)blockIdx.x * kSplitChunk;
-  int64_t k_first;
-  if (first_doc) {
-    k_first = __ldg(first_doc + (int64_t)blockIdx.x * (kSplitChunk / kChunk));  // from k_prep
-  } else {  // no k_prep: the first document at or after c0 by binary search
-    if (threadIdx.x == 0) {
-      int64_t lo = 0, hi = n_docs + 1;
-      while (lo < hi) {
-        int64_t mid = (lo + hi) >> 1;
-        if (doc_offsets[mid] < c0) lo = mid + 1;
-        else hi = mid;
-      }
-      S.chunk = lo;
-    }
-    __syncthreads();
-    k_first = S.chunk;
-  }
-  load_window(S, bytes, n_bytes, doc_offsets, n_docs, c0, k_first);
-  compute_start_bits(S);
-  const int64_t n_words = (n_bytes + 31) / 32;
-  for (int w = threadIdx.x; w < kSplitChunk / 32; w += kThreads) {
-    const int64_t gw = c0 / 32 + w;
-    if (gw < n_words) {
-      uint32_t v = S.startbits[w];
-      const int64_t first_bit = gw * 32;
-      if (first_bit + 32 > n_bytes) v &= (1u << (n_bytes - first_bit)) - 1u;
-      out_bits[gw] = v;
-    }
-  }
-}
+namespace {
 
 // Word-cache values: the ids of each string, computed by the same merge loop
 // the encoder runs. out[4 i] = count, out[4 i + 1 .. 3] = first three ids.
@@ -2225,7 +1165,7 @@ int status_code(uint32_t s) {
 // vocabulary string that starts with a space with that space removed (the
 // same word at the start of a line or document), and of every prefix of
 // those (a word cut off by the end of a document), computed on the device by
-// the merge loop, laid out as an open-addressed table (load at most 1/4,
+// the merge loop, laid out as an open-addressed table (load at most 1/8,
 // linear probing).
 int build_word_cache(bpe_handle* h, const uint8_t* vocab_bytes, const int64_t* vocab_offsets, int64_t n_vocab) {
   std::vector<uint8_t> strs;
@@ -2303,83 +1243,89 @@ int build_word_cache(bpe_handle* h, const uint8_t* vocab_bytes, const int64_t* v
 
 // -------------------------------------------------------- encode workspace --
 // Regions of the per-call workspace, each starting on a 256-byte boundary:
-// first document per chunk (+1 sentinel), chunk metadata and offsets, tile
-// offsets of the chunk scan, long pre-token records, the start bitmask, the
-// stage regions and the pool.
+// per tile its first document, record, first pre-token start and offset;
+// the scan's block sums; the stage slots; the miss queue; the deferred-piece
+// records; the long runs of k_prep_docs; the pool of the deferred pieces (an
+// int32 per input byte).
 namespace {
 constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsSizes {
-  size_t first_doc, chunk_meta, chunk_off, tile_off, rec, def_n, def_rec, queue, bits, stage, pool, total;
-  uint64_t rec_cap;  // u32 words: a header per chunk and 4 words per long pre-token
+  size_t first_doc, rec, first_start, tile_base, block_sum, stage, misses, giants, ranges, pool, total;
+  int64_t n_tiles, miss_cap, giant_cap, range_cap;
 };
 
 constexpr WsSizes ws_sizes(int64_t n_bytes) {
-  const int64_t n_chunks = n_bytes / kChunk + 1, n_words = (n_bytes + 31) / 32;
   WsSizes z{};
-  z.rec_cap = (uint64_t)(n_chunks + 4 * (n_bytes / (kShortMax + 1) + n_chunks) + 16);
-  z.first_doc = align256((size_t)(n_chunks + 1) * sizeof(int64_t));
-  z.chunk_meta = align256((size_t)n_chunks * sizeof(uint64_t));
-  z.chunk_off = align256((size_t)n_chunks * sizeof(uint64_t));
-  z.tile_off = align256((size_t)(n_chunks / kScanThreads + 1) * sizeof(uint64_t));
-  z.rec = align256((size_t)z.rec_cap * sizeof(uint32_t));
-  z.def_n = align256((size_t)n_chunks * sizeof(uint32_t));
-  z.def_rec = align256((size_t)n_chunks * kMaxDefer * 3 * sizeof(uint32_t));
-  z.queue = align256((size_t)n_chunks * kMaxDefer * sizeof(uint64_t));
-  z.bits = align256((size_t)(n_words + 4) * sizeof(uint32_t));
-  z.stage = align256((size_t)n_chunks * kStage * sizeof(uint32_t));
+  z.n_tiles = n_bytes / kTileOwn + 1;
+  z.miss_cap = n_bytes / 2 + 64;  // a miss has at least 2 bytes
+  z.giant_cap = n_bytes / (kShortMax + 1) + z.n_tiles + 16;
+  z.range_cap = z.n_tiles / kPrepSpan + 16;
+  z.first_doc = align256((size_t)z.n_tiles * sizeof(int64_t));
+  z.rec = align256((size_t)z.n_tiles * sizeof(TileRec));
+  z.first_start = align256((size_t)z.n_tiles * sizeof(int64_t));
+  z.tile_base = align256((size_t)z.n_tiles * sizeof(uint64_t));
+  z.block_sum = align256((size_t)(z.n_tiles / kScanThreads + 1) * sizeof(uint64_t));
+  z.stage = align256((size_t)z.n_tiles * kTileBits * sizeof(uint32_t));
+  z.misses = align256((size_t)z.miss_cap * sizeof(uint64_t));
+  z.giants = align256((size_t)z.giant_cap * sizeof(GiantRec));
+  z.ranges = align256((size_t)z.range_cap * sizeof(PrepRange));
   z.pool = align256((size_t)(n_bytes + 4) * sizeof(int32_t));
-  z.total = z.first_doc + z.chunk_meta + z.chunk_off + z.tile_off + z.rec + z.def_n + z.def_rec + z.queue + z.bits +
-            z.stage + z.pool;
+  z.total = z.first_doc + z.rec + z.first_start + z.tile_base + z.block_sum + z.stage + z.misses + z.giants +
+            z.ranges + z.pool;
   return z;
 }
 
 struct Ws {
+  int64_t n_tiles, miss_cap, giant_cap, range_cap;
   int64_t* first_doc;
-  uint64_t* chunk_meta;
-  uint64_t* chunk_off;
-  uint64_t* tile_off;
-  uint32_t* rec;
-  uint64_t rec_cap;
-  uint32_t* def_n;
-  uint32_t* def_rec;
-  uint64_t* queue;
-  uint32_t* bits;
+  TileRec* rec;
+  int64_t* first_start;
+  uint64_t* tile_base;
+  uint64_t* block_sum;
   uint32_t* stage;
+  uint64_t* misses;
+  GiantRec* giants;
+  PrepRange* ranges;
   int32_t* pool;
 };
 
 Ws ws_carve(unsigned char* base, int64_t n_bytes) {
   const WsSizes z = ws_sizes(n_bytes);
   Ws w;
-  w.first_doc = reinterpret_cast<int64_t*>(base);
-  base += z.first_doc;
-  w.chunk_meta = reinterpret_cast<uint64_t*>(base);
-  base += z.chunk_meta;
-  w.chunk_off = reinterpret_cast<uint64_t*>(base);
-  base += z.chunk_off;
-  w.tile_off = reinterpret_cast<uint64_t*>(base);
-  base += z.tile_off;
-  w.rec = reinterpret_cast<uint32_t*>(base);
-  w.rec_cap = z.rec_cap;
-  base += z.rec;
-  w.def_n = reinterpret_cast<uint32_t*>(base);
-  base += z.def_n;
-  w.def_rec = reinterpret_cast<uint32_t*>(base);
-  base += z.def_rec;
-  w.queue = reinterpret_cast<uint64_t*>(base);
-  base += z.queue;
-  w.bits = reinterpret_cast<uint32_t*>(base);
-  base += z.bits;
-  w.stage = reinterpret_cast<uint32_t*>(base);
-  base += z.stage;
-  w.pool = reinterpret_cast<int32_t*>(base);
+  w.n_tiles = z.n_tiles;
+  w.miss_cap = z.miss_cap;
+  w.giant_cap = z.giant_cap;
+  w.range_cap = z.range_cap;
+  auto take = [&](size_t n) {
+    unsigned char* p = base;
+    base += n;
+    return p;
+  };
+  w.first_doc = reinterpret_cast<int64_t*>(take(z.first_doc));
+  w.rec = reinterpret_cast<TileRec*>(take(z.rec));
+  w.first_start = reinterpret_cast<int64_t*>(take(z.first_start));
+  w.tile_base = reinterpret_cast<uint64_t*>(take(z.tile_base));
+  w.block_sum = reinterpret_cast<uint64_t*>(take(z.block_sum));
+  w.stage = reinterpret_cast<uint32_t*>(take(z.stage));
+  w.misses = reinterpret_cast<uint64_t*>(take(z.misses));
+  w.giants = reinterpret_cast<GiantRec*>(take(z.giants));
+  w.ranges = reinterpret_cast<PrepRange*>(take(z.ranges));
+  w.pool = reinterpret_cast<int32_t*>(take(z.pool));
   return w;
 }
 
-// The per-call kernels: k_prep, the split, the encode, the chunk scan and the
-// compaction, on stream st. ev_start / ev_stop (may be null) bracket all but
-// k_prep.
+// k_tiles' dynamic shared memory above the 48 KB default, once per device.
+int tiles_smem_setup() {
+  return cudaFuncSetAttribute(k_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTileSmemBytes) ==
+                 cudaSuccess
+             ? BPE_OK
+             : fail(BPE_ERR_CUDA, "cudaFuncSetAttribute(k_tiles) failed");
+}
+
+// The per-call kernels on stream st: k_prep_docs, k_prep_long, k_tiles,
+// k_misses, k_giants (which returns at once when nothing was deferred), the
+// scan and k_compact. ev_start / ev_stop (may be null) bracket all of them.
 int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
                   int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets, cudaStream_t st,
                   cudaEvent_t ev_start, cudaEvent_t ev_stop);
@@ -2391,7 +1337,7 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
 namespace {
 constexpr int64_t kNoAllocMaxBytes = int64_t(4) << 20;
 constexpr size_t kNoAllocScratchBytes = ws_sizes(kNoAllocMaxBytes).total;
-static_assert(kNoAllocScratchBytes < (size_t(40) << 20), "the fixed scratch stays below 40 MiB");
+static_assert(kNoAllocScratchBytes < (size_t(64) << 20), "the fixed scratch stays below 64 MiB");
 }  // namespace
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -2402,7 +1348,7 @@ std::mutex g_noalloc_mu;
 unsigned char* g_noalloc_base[kNoAllocMaxDevices] = {};
 
 // Once per device, with that device current: the scratch address and the
-// encode kernel's shared-memory opt-in. Later calls only read the table.
+// tile kernel's shared-memory opt-in. Later calls only read the table.
 int noalloc_setup(int dev, unsigned char** base) {
   if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch_noalloc: device ordinal above 63");
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
@@ -2411,7 +1357,7 @@ int noalloc_setup(int dev, unsigned char** base) {
     CK(cudaGetSymbolAddress(&p, g_noalloc_scratch));
     if (reinterpret_cast<uintptr_t>(p) & 255u)
       return fail(BPE_ERR_INTERNAL, "bpe_encode_batch_noalloc: scratch not 256-byte aligned");
-    CK(cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
+    if (tiles_smem_setup()) return BPE_ERR_CUDA;
     g_noalloc_base[dev] = static_cast<unsigned char*>(p);
   }
   *base = g_noalloc_base[dev];
@@ -2423,50 +1369,49 @@ namespace {
 int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
                   int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets, cudaStream_t st,
                   cudaEvent_t ev_start, cudaEvent_t ev_stop) {
-  const int64_t n_chunks = n_bytes / kChunk + 1;
-  const int prep_blocks = (int)std::min<int64_t>(4096, std::max<int64_t>(n_chunks, n_docs + 1) / 256 + 1);
-  k_prep<<<prep_blocks, 256, 0, st>>>(d_doc_offsets, n_docs, n_bytes, n_chunks, w.first_doc, h->d_small);
+  if (ev_start) CK(cudaEventRecord(ev_start, st));
+  const int64_t n_tiles = w.n_tiles;
+  const int prep_blocks = (int)std::min<int64_t>(4096, (n_docs + 2) / 256 + 1);
+  k_prep_docs<<<prep_blocks, 256, 0, st>>>(d_doc_offsets, n_docs, n_bytes, n_tiles, w.first_doc, w.ranges,
+                                           w.range_cap, h->d_small);
   CK(cudaGetLastError());
-  EncodeArgs a;
+  k_prep_long<<<(unsigned)std::min<int64_t>(2 * h->n_sms, w.range_cap), 256, 0, st>>>(w.ranges, w.first_doc,
+                                                                                    h->d_small);
+  CK(cudaGetLastError());
+  TileArgs a;
   a.bytes = d_bytes;
   a.n_bytes = n_bytes;
   a.doc_offsets = d_doc_offsets;
   a.n_docs = n_docs;
-  a.pool = w.pool;
   a.T = Tables{h->d_ht, h->hmask, h->d_mrows, h->d_byte_id};
   a.C = Cache{h->d_cache, h->cache_mask, h->cache_enabled && h->d_cache != nullptr};
-  a.start_bits = w.bits;
-  a.stage = w.stage;
-  a.chunk_meta = w.chunk_meta;
-  a.rec = w.rec;
-  a.rec_cap = w.rec_cap;
-  a.def_n = w.def_n;
-  a.def_rec = w.def_rec;
-  a.queue = w.queue;
   a.first_doc = w.first_doc;
+  a.rec = w.rec;
+  a.first_start = w.first_start;
+  a.stage = w.stage;
+  a.misses = w.misses;
+  a.miss_cap = w.miss_cap;
+  a.giants = w.giants;
+  a.giant_cap = w.giant_cap;
   a.small = h->d_small;
-  a.n_chunks = n_chunks;
-  a.out_offsets = d_out_offsets;
-  if (ev_start) CK(cudaEventRecord(ev_start, st));
-  if (n_bytes > 0) {
-    k_pretokenize<<<(unsigned)((n_bytes + kSplitChunk - 1) / kSplitChunk), kThreads, 0, st>>>(d_bytes, n_bytes, d_doc_offsets,
-                                                                                   n_docs, w.first_doc, w.bits);
-    CK(cudaGetLastError());
-  }
-  k_encode<<<(unsigned)n_chunks, kThreads, sizeof(Smem), st>>>(a);
+  a.n_tiles = n_tiles;
+  const int64_t grid = std::min<int64_t>((int64_t)kTileCtasPerSm * h->n_sms, (n_tiles + kTileWarps - 1) / kTileWarps);
+  k_tiles<<<(unsigned)grid, kTileThreads, kTileSmemBytes, st>>>(a);
   CK(cudaGetLastError());
-  const unsigned miss_grid = (unsigned)std::min<int64_t>((int64_t)kMissBlocksPerSm * h->n_sms, n_chunks);
-  k_misses<<<miss_grid, kThreads, 0, st>>>(d_bytes, w.queue, h->d_small,
-                                      w.def_rec, w.stage, w.chunk_meta, a.T);
+  k_misses<<<(unsigned)(kMissBlocksPerSm * h->n_sms), kMissThreads, 0, st>>>(d_bytes, w.misses, w.miss_cap, w.stage,
+                                                                            w.rec, a.T, h->d_small);
   CK(cudaGetLastError());
-  const int64_t n_tiles = (n_chunks + kScanThreads - 1) / kScanThreads;
-  k_scan_tiles<<<(unsigned)n_tiles, kScanThreads, 0, st>>>(w.chunk_meta, n_chunks, w.chunk_off, w.tile_off);
+  k_giants<<<(unsigned)(2 * h->n_sms), kGiantThreads, 0, st>>>(d_bytes, w.giants, w.giant_cap, w.first_start, n_tiles,
+                                                            w.rec, w.pool, a.T, h->d_small);
   CK(cudaGetLastError());
-  k_scan_tile_sums<<<1, kScanThreads, 0, st>>>(w.tile_off, n_tiles, h->d_small);
+  const int64_t n_blocks = (n_tiles + kScanThreads - 1) / kScanThreads;
+  k_scan_tiles<<<(unsigned)n_blocks, kScanThreads, 0, st>>>(w.rec, n_tiles, w.tile_base, w.block_sum);
   CK(cudaGetLastError());
-  k_compact<<<(unsigned)((n_chunks + kCompactWarps - 1) / kCompactWarps), 32 * kCompactWarps, 0, st>>>(
-      w.stage, w.pool, w.chunk_meta, w.chunk_off, w.tile_off, w.rec, w.def_n, w.def_rec, w.first_doc, n_chunks, n_docs,
-      d_out_ids, out_capacity, d_out_offsets, h->d_small);
+  k_scan_tile_sums<<<1, kScanThreads, 0, st>>>(w.block_sum, n_blocks, h->d_small);
+  CK(cudaGetLastError());
+  k_compact<<<(unsigned)std::min<int64_t>((n_tiles + kCompactWarps - 1) / kCompactWarps, 8 * h->n_sms),
+              32 * kCompactWarps, 0, st>>>(w.rec, w.stage, w.tile_base, w.block_sum, w.giants, w.pool, d_doc_offsets,
+                                          n_tiles, d_out_ids, out_capacity, d_out_offsets, h->d_small);
   CK(cudaGetLastError());
   if (ev_stop) CK(cudaEventRecord(ev_stop, st));
   return BPE_OK;
@@ -2647,7 +1592,7 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
   int rc = ensure_ws(h, ws_sizes(n_bytes).total);
   if (rc) return rc;
   if (!h->smem_set) {
-    CK(cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
+    if ((rc = tiles_smem_setup())) return rc;
     h->smem_set = true;
   }
   rc = launch_encode(h, ws_carve(static_cast<unsigned char*>(h->d_ws), n_bytes), d_bytes, n_bytes, d_doc_offsets,
@@ -2777,7 +1722,7 @@ int bpe_encode_batch_host(bpe_handle* h, const uint8_t* h_bytes, int64_t n_bytes
   int rc = ensure_ws(h, ws_sizes(h->slot_bytes).total);
   if (rc) return rc;
   if (!h->smem_set) {
-    CK(cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)));
+    if ((rc = tiles_smem_setup())) return rc;
     h->smem_set = true;
   }
   // Slice j: upload (stream h2d) -> encode (the caller's stream) -> count to
@@ -2840,9 +1785,9 @@ int bpe_pretokenize_batch(const uint8_t* d_bytes, int64_t n_bytes, const int64_t
   if (!d_doc_offsets || n_bytes < 0 || n_docs < 0 || (n_bytes > 0 && (!d_bytes || !d_start_bits)))
     return fail(BPE_ERR_INVALID_ARG, "bpe_pretokenize_batch: bad arguments");
   if (n_bytes == 0) return BPE_OK;
-  const int64_t n_chunks = (n_bytes + kSplitChunk - 1) / kSplitChunk;
-  k_pretokenize<<<(unsigned)n_chunks, kThreads, 0, (cudaStream_t)stream>>>(d_bytes, n_bytes, d_doc_offsets,
-                                                                                      n_docs, nullptr, d_start_bits);
+  const int64_t n_tiles = n_bytes / kTileOwn + 1;
+  k_split_tiles<<<(unsigned)((n_tiles + kSplitWarps - 1) / kSplitWarps), 32 * kSplitWarps, 0, (cudaStream_t)stream>>>(
+      d_bytes, n_bytes, d_doc_offsets, n_docs, n_tiles, d_start_bits);
   CK(cudaGetLastError());
   return BPE_OK;
 }

@@ -1,0 +1,819 @@
+// Warp-tile encoder: the split, byte -> symbol and the word cache in one pass
+// over the input, one warp per tile; the cache misses merged GPU-wide after
+// it; then the ids placed by a scan of the tiles' counts.
+//
+// Included once by bpe_kernels.cu after the shared helpers (window, split
+// masks, word cache, lane-group and CTA merges); not a standalone header.
+//
+// The method is the one bpe_kernels.cu describes (glitch4techs, "Tokenization
+// LLM", sections "Technical analysis", "Byte-level encoding", "BPE merge
+// algorithm", "Vocabulary lookup"; tokenwerk, "Tokenisierung", section "Byte
+// Pair Encoding schrittweise"). What follows is GPU organisation only:
+//
+//   * Tiles (k_tiles). Tile t owns the pre-tokens that start in input bytes
+//     [992 t, 992 t + 992). Its warp loads bytes [992 t - 16, 992 t + 1040)
+//     into shared memory (16 bytes of context on each side of the 1024 bytes
+//     it splits); lane l computes the start bits of bytes [32 l, 32 l + 32)
+//     of the tile, so lane 31 covers a 32-byte margin where the tile's last
+//     pre-token normally ends. The input is read once; the next tile's window
+//     is in flight while the warp works on the current one.
+//   * Per pre-token, one lane: a word-cache probe for 2 to 16 bytes (a single
+//     byte is its own token). The ids go to the tile's stage slot at reserved
+//     positions: a hit reserves its id count, a miss its byte length (ids
+//     never outnumber bytes), a pre-token longer than kShortMax bytes or
+//     running past the margin one placeholder.
+//   * Misses (k_misses, GPU-wide): a lane per miss of up to 8 bytes, groups
+//     of 8, 16 or 32 lanes for longer ones; each writes its ids at its
+//     reserved position, marks the rest of the reservation as holes and adds
+//     their number to its tile's record.
+//   * Long pre-tokens (k_giants): a CTA each, in a pool at their own bytes.
+//   * Output: a two-level scan of the tiles' final counts (k_scan_tiles,
+//     k_scan_tile_sums), then k_compact moves every tile's ids into place
+//     without the holes, expanding the placeholders, and writes the document
+//     offsets. No kernel waits on another CTA.
+
+namespace {
+
+constexpr int kTileLanes = 31;                     // lanes whose bytes a tile owns
+constexpr int kTileOwn = 32 * kTileLanes;          // 992 bytes whose pre-tokens a tile owns
+constexpr int kTileBits = 32 * 32;                 // bytes whose start bits a tile computes
+using TileWin = WindowSmem<kTileBits, 0, true>;    // window: 16 + 1024 + 16 bytes
+static_assert(TileWin::kLen == kHalo + kTileBits + kHalo, "tile window");
+constexpr int kTileWarps = 8;                      // warps (tiles in flight) per CTA
+constexpr int kTileThreads = 32 * kTileWarps;
+constexpr int kTileCtasPerSm = 3;                  // resident CTAs (registers: 85 a thread)
+constexpr int kMissCap = 128;                      // miss records a tile holds before it hands them on
+constexpr int kMissFlush = kMissCap - 64;          // hand on once this many are held (a round adds <= 64)
+
+// Span list entries (u16): the start's tile position, and flags.
+constexpr uint32_t kSpanPos = 0x07FFu;
+constexpr uint32_t kSpanNone = 0x07FFu;  // sentinel: no pre-token start in the margin
+constexpr uint32_t kSpanSkip = 0x4000u;  // the end of the last document: nothing to encode
+constexpr uint32_t kSpanDoc = 0x8000u;   // a document starts here
+
+// Stage entries: an id (< 2^20), or a hole, or a placeholder for a deferred
+// pre-token (its record index); kIdDoc marks the first id of a document.
+constexpr uint32_t kIdDoc = 0x80000000u;
+constexpr uint32_t kIdSpecial = 0x40000000u;
+constexpr uint32_t kIdLong = 0x20000000u;
+constexpr uint32_t kIdHole = kIdSpecial;
+constexpr uint32_t kIdIndex = 0x1FFFFFFFu;
+
+// A deferred pre-token (longer than kShortMax bytes, or running past its
+// tile's margin): k_giants finds its end when unknown (-1), merges it into
+// the pool at its own bytes and stores its id count.
+struct GiantRec {
+  int64_t start;
+  int64_t end;
+  int64_t tile;
+  uint32_t count;
+  uint32_t pad;
+};
+
+// Per tile: its documents [k0, k1) (k = n_docs: the end of the last one),
+// stage entries used, holes left by merged misses, extra ids of its
+// deferred pre-tokens (their ids minus their placeholders), flags.
+constexpr uint32_t kTileDup = 1u;   // two documents start at the same byte (an empty document)
+struct TileRec {
+  int64_t k0, k1;
+  uint32_t resv;
+  uint32_t holes;
+  uint32_t extra;
+  uint32_t flags;
+};
+
+// A cache miss handed to k_misses: tile << 29 | reserved position << 18 |
+// document start << 17 | length << 10 | start.
+__device__ __forceinline__ uint64_t miss_entry(int64_t t, uint32_t rec) {
+  return (uint64_t)t << 29 | (uint64_t)((rec >> 17) & 0x7FFu) << 18 | (uint64_t)((rec >> 28) & 1u) << 17 |
+         (uint64_t)(rec & 0x1FFFFu);
+}
+
+struct __align__(16) TileSmem {
+  TileWin w[2];                   // the current tile's window and the next one's
+  uint16_t span[kTileOwn + 8];    // pre-token starts
+  uint32_t miss[kMissCap];        // start | length << 10 | reserved position << 17 | document start << 28
+};
+constexpr size_t kTileSmemBytes = kTileWarps * sizeof(TileSmem);
+static_assert(kTileCtasPerSm * (kTileSmemBytes + 1024) <= 228 * 1024, "the tile CTAs fit in an SM's shared memory");
+
+struct TileArgs {
+  const uint8_t* bytes;
+  int64_t n_bytes;
+  const int64_t* doc_offsets;
+  int64_t n_docs;
+  Tables T;
+  Cache C;
+  const int64_t* first_doc;  // per tile: the first document starting at or after the window
+  TileRec* rec;              // per tile
+  int64_t* first_start;      // per tile: the first pre-token start it owns (INT64_MAX: none)
+  uint32_t* stage;           // [n_tiles][kTileBits]
+  uint64_t* misses;          // the miss queue
+  int64_t miss_cap;
+  GiantRec* giants;
+  int64_t giant_cap;
+  DevSmall* small;
+  int64_t n_tiles;
+};
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  return (1u << (threadIdx.x & 31)) - 1u;
+}
+
+// --------------------------------------------------------- window and docs --
+
+// Bytes [t0 - kHalo, t0 + kTileBits + kHalo) into W.win (zero outside the
+// input): 16-byte asynchronous copies when the input is 16-byte aligned
+// (window offsets are multiples of 16), byte loads otherwise. The caller
+// waits with cp_async_wait_all and __syncwarp.
+__device__ void tile_load_bytes(TileWin& W, const uint8_t* bytes, int64_t n_bytes, int64_t t0, bool aligned) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = t0 - kHalo;
+  for (int c = lane; c < TileWin::kLen / 16; c += 32) {
+    const int64_t g = w0 + 16 * c;
+    if (aligned && g >= 0 && g + 16 <= n_bytes) {
+      cp_async16(W.win + 16 * c, bytes + g);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) W.win[16 * c + k] = (g + k >= 0 && g + k < n_bytes) ? bytes[g + k] : 0;
+    }
+  }
+}
+
+struct TileDocs {
+  int64_t k0, k1;  // documents starting in the tile's own bytes: [k0, k1)
+  bool dup;        // two of them start at the same byte (an empty document)
+};
+
+// Document edges of the window into W.docbits (every offset, the end of the
+// last document included) and the bytes outside every document into
+// W.outbits; kA = the first document at or after the window start (clamped
+// here). Offsets are read in warp-wide groups until one lies past the window
+// or they stop increasing (malformed input: k_prep_docs reports it).
+__device__ TileDocs tile_load_docs(TileWin& W, const int64_t* doc_offsets, int64_t n_docs, int64_t t0, int64_t kA,
+                                   int64_t d_first, int64_t d_last) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = t0 - kHalo, w_end = w0 + TileWin::kLen;
+  for (int i = lane; i < TileWin::kWords + 2; i += 32) {
+    W.docbits[i] = 0;
+    uint32_t word = 0;
+    const int64_t p = w0 + 32 * i;
+    if (p < d_first || p + 32 > d_last) {
+      for (int k = 0; k < 32; ++k)
+        if (p + k < d_first || p + k >= d_last) word |= 1u << k;
+    }
+    W.outbits[i] = word;
+  }
+  __syncwarp();
+  kA = kA < 0 ? 0 : (kA > n_docs + 1 ? n_docs + 1 : kA);
+  int64_t n_lt0 = 0, n_lt1 = 0, prev_last = INT64_MIN;
+  bool dup = false;
+  for (int64_t k = kA; k <= n_docs; k += 32) {
+    const int64_t kk = k + lane;
+    const int64_t o = kk <= n_docs ? __ldg(doc_offsets + kk) : INT64_MAX;
+    if (o >= w0 && o < w_end) {
+      const int i = (int)(o - w0);
+      atomicOr(&W.docbits[i >> 5], 1u << (i & 31));
+    }
+    n_lt0 += __popc(__ballot_sync(0xFFFFFFFFu, o < t0));
+    n_lt1 += __popc(__ballot_sync(0xFFFFFFFFu, o < t0 + kTileOwn));
+    int64_t o_prev = __shfl_up_sync(0xFFFFFFFFu, o, 1);
+    if (lane == 0) o_prev = prev_last;
+    dup |= __any_sync(0xFFFFFFFFu, o == o_prev && o >= t0 && o < t0 + kTileOwn);
+    const bool down = __any_sync(0xFFFFFFFFu, kk <= n_docs && o < o_prev);
+    prev_last = __shfl_sync(0xFFFFFFFFu, o, 31);
+    if (down || prev_last >= w_end) break;
+  }
+  __syncwarp();
+  return TileDocs{kA + n_lt0, kA + n_lt1, dup};
+}
+
+// A word-cache key from the window (tile positions [s, s + len), len <= 16).
+__device__ __forceinline__ CacheKey tile_key(const TileWin& W, int s, int len) {
+  const int ws = kHalo + s;
+  const uint32_t* wv = reinterpret_cast<const uint32_t*>(W.win) + (ws >> 2);
+  const uint32_t sh = (uint32_t)(ws & 3) * 8u;
+  const uint32_t a0 = lds_u32(wv), a1 = lds_u32(wv + 1), a2 = lds_u32(wv + 2), a3 = lds_u32(wv + 3),
+                 a4 = lds_u32(wv + 4);
+  const uint32_t nbit = 8u * (uint32_t)len;
+  const uint64_t m_lo = nbit >= 64 ? ~0ull : (1ull << nbit) - 1ull;
+  const uint64_t m_hi = nbit <= 64 ? 0ull : (nbit >= 128 ? ~0ull : (1ull << (nbit - 64)) - 1ull);
+  CacheKey K;
+  K.x0 = __funnelshift_r(a0, a1, sh) & (uint32_t)m_lo;
+  K.x1 = __funnelshift_r(a1, a2, sh) & (uint32_t)(m_lo >> 32);
+  K.x2 = __funnelshift_r(a2, a3, sh) & (uint32_t)m_hi;
+  K.x3 = __funnelshift_r(a3, a4, sh) & (uint32_t)(m_hi >> 32);
+  return K;
+}
+
+// The held miss records of tile t into the GPU-wide queue (one atomic per
+// hand-over).
+__device__ void tile_hand_misses(const TileSmem& S, int n_miss, int64_t t, const TileArgs& a) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long base = 0;
+  if (lane == 0) base = atomicAdd(&a.small->n_misses, (unsigned long long)n_miss);
+  base = __shfl_sync(0xFFFFFFFFu, base, 0);
+  for (int i = lane; i < n_miss; i += 32) {
+    if ((int64_t)(base + i) < a.miss_cap) a.misses[base + i] = miss_entry(t, S.miss[i]);
+    else atomicOr(&a.small->status, kStInternal);
+  }
+}
+
+// ---------------------------------------------------------------- kernel --
+
+// Persistent: each warp takes tiles from a counter, prefetching the next
+// tile's window while it encodes the current one.
+__global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm) k_tiles(TileArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  TileSmem& S = reinterpret_cast<TileSmem*>(smem_raw)[threadIdx.x >> 5];
+  const int lane = threadIdx.x & 31;
+  const bool aligned = (reinterpret_cast<uintptr_t>(a.bytes) & 15u) == 0;
+  int64_t d_first = __ldg(a.doc_offsets), d_last = __ldg(a.doc_offsets + a.n_docs);
+  d_first = d_first < 0 ? 0 : (d_first > a.n_bytes ? a.n_bytes : d_first);
+  d_last = d_last < d_first ? d_first : (d_last > a.n_bytes ? a.n_bytes : d_last);
+  auto take = [&]() -> int64_t {
+    unsigned long long tu = 0;
+    if (lane == 0) tu = atomicAdd(&a.small->tile_ctr, 1ull);
+    return (int64_t)__shfl_sync(0xFFFFFFFFu, tu, 0);
+  };
+  int64_t t = take();
+  if (t < a.n_tiles) tile_load_bytes(S.w[0], a.bytes, a.n_bytes, t * (int64_t)kTileOwn, aligned);
+  for (int buf = 0; t < a.n_tiles; buf ^= 1) {
+    TileWin& W = S.w[buf];
+    const int64_t t0 = t * (int64_t)kTileOwn;
+    const int64_t kA = __ldg(a.first_doc + t);
+    const int64_t t_next = take();
+    const TileDocs D = tile_load_docs(W, a.doc_offsets, a.n_docs, t0, kA, d_first, d_last);
+    cp_async_wait_all();
+    __syncwarp();
+    // the next window's copies overlap this tile's work
+    if (t_next < a.n_tiles) tile_load_bytes(S.w[buf ^ 1], a.bytes, a.n_bytes, t_next * (int64_t)kTileOwn, aligned);
+
+    // Split: lane l's 32 start bits; the end of the last document ends the
+    // pre-token before it.
+    const int p0 = kHalo + 32 * lane;
+    const uint32_t dw = bits32_at(W.docbits, p0), ow = bits32_at(W.outbits, p0);
+    const uint32_t m = start_mask32(W, p0) | (dw & ow);
+    const bool own = lane < kTileLanes;
+    const uint32_t cnt = own ? (uint32_t)__popc(m) : 0u;
+    const uint32_t incl = warp_incl_scan(cnt);
+    const uint32_t n_spans = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    if (own) {
+      uint32_t b = m, o = incl - cnt;
+      while (b) {
+        const int k = __ffs(b) - 1;
+        b &= b - 1;
+        uint32_t v = (uint32_t)(32 * lane + k);
+        if ((dw >> k) & 1u) v |= kSpanDoc;
+        if (((dw & ow) >> k) & 1u) v |= kSpanSkip;
+        S.span[o++] = (uint16_t)v;
+      }
+    } else {
+      S.span[n_spans] = (uint16_t)(m ? (uint32_t)(32 * kTileLanes + __ffs(m) - 1) : kSpanNone);
+    }
+    __syncwarp();
+    if (lane == 0) a.first_start[t] = n_spans ? t0 + (int64_t)(S.span[0] & kSpanPos) : INT64_MAX;
+
+    // Pre-tokens, two per lane per round: cache probes in flight together.
+    uint32_t* stage = a.stage + t * (int64_t)kTileBits;
+    uint32_t resv = 0;
+    int n_miss = 0;
+    enum : uint32_t { kNoPiece = 0, kSkipPiece = 1, kProbe = 2, kMiss = 3, kLong = 4, kOne = 5 };
+    for (uint32_t i0 = 0; i0 < n_spans; i0 += 64) {
+      uint32_t info[2];  // start | length << 10 | kind << 21 | document start << 24
+      CacheKey K[2];
+      uint4 ea[2], eb[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t i = i0 + 32u * h + lane;
+        info[h] = 0;
+        if (i < n_spans) {
+          const uint32_t e0 = S.span[i], e1 = S.span[i + 1];
+          const uint32_t s = e0 & kSpanPos;
+          uint32_t kind, len = 0;
+          if (e0 & kSpanSkip) {
+            kind = kSkipPiece;
+          } else if (e1 == kSpanNone) {
+            kind = kLong;
+          } else {
+            len = (e1 & kSpanPos) - s;
+            kind = len > (uint32_t)kShortMax
+                       ? kLong
+                       : (len == 1 ? kOne : ((len <= (uint32_t)kCacheMaxLen && a.C.enabled) ? kProbe : kMiss));
+          }
+          info[h] = s | (len << 10) | (kind << 21) | ((e0 & kSpanDoc) ? 1u << 24 : 0u);
+          if (kind == kProbe) {
+            K[h] = tile_key(W, (int)s, (int)len);
+            ldg32(a.C.e + 2 * cache_slot(K[h], len, a.C), ea[h], eb[h]);
+          }
+        }
+      }
+      uint32_t res[2], cnt2[2], idv[2][kCacheMaxIds];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t kind = (info[h] >> 21) & 7u;
+        const uint32_t len = (info[h] >> 10) & 0x7FFu;
+        cnt2[h] = 0;
+        if (kind == kProbe) {
+          cnt2[h] = cache_resolve(a.C, K[h], len, ea[h], eb[h], idv[h]);
+          if (!cnt2[h]) kind = kMiss;
+        } else if (kind == kOne) {  // a single byte is its own token
+          idv[h][0] = (uint32_t)__ldg(a.T.byte_id + W.win[kHalo + (info[h] & 0x3FFu)]);
+          cnt2[h] = 1;
+          kind = kProbe;
+        }
+        info[h] = (info[h] & ~(7u << 21)) | (kind << 21);
+        res[h] = kind == kProbe ? cnt2[h] : (kind == kMiss ? len : (kind == kLong ? 1u : 0u));
+      }
+      const uint32_t inc0 = warp_incl_scan(res[0]), inc1 = warp_incl_scan(res[1]);
+      const uint32_t tot0 = __shfl_sync(0xFFFFFFFFu, inc0, 31), tot1 = __shfl_sync(0xFFFFFFFFu, inc1, 31);
+      const uint32_t at[2] = {resv + inc0 - res[0], resv + tot0 + inc1 - res[1]};
+      resv += tot0 + tot1;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t kind = (info[h] >> 21) & 7u;
+        const uint32_t doc = (info[h] >> 24) & 1u ? kIdDoc : 0u;
+        if (kind == kProbe) {
+#pragma unroll
+          for (uint32_t q = 0; q < (uint32_t)kCacheMaxIds; ++q)
+            if (q < cnt2[h]) stage[at[h] + q] = idv[h][q] | (q == 0 ? doc : 0u);
+        } else if (kind == kLong) {
+          const uint32_t s = info[h] & 0x3FFu, len = (info[h] >> 10) & 0x7FFu;
+          const unsigned long long gi = atomicAdd(&a.small->n_giants, 1ull);
+          if ((int64_t)gi < a.giant_cap) {
+            a.giants[gi] = GiantRec{t0 + (int64_t)s, len ? t0 + (int64_t)(s + len) : -1, t, 0u, 0u};
+            stage[at[h]] = kIdSpecial | kIdLong | (uint32_t)gi | doc;
+          } else {
+            atomicOr(&a.small->status, kStInternal);
+            stage[at[h]] = kIdHole;
+          }
+        }
+        const bool miss = kind == kMiss;
+        const uint32_t mb = __ballot_sync(0xFFFFFFFFu, miss);
+        if (miss) {
+          const uint32_t len = (info[h] >> 10) & 0x7FFu;
+          S.miss[n_miss + __popc(mb & lanemask_lt())] =
+              (info[h] & 0x3FFu) | (len << 10) | (at[h] << 17) | (doc ? 1u << 28 : 0u);
+        }
+        n_miss += __popc(mb);
+      }
+      __syncwarp();
+      if (n_miss >= kMissFlush) {
+        tile_hand_misses(S, n_miss, t, a);
+        n_miss = 0;
+        __syncwarp();
+      }
+    }
+    if (n_miss) tile_hand_misses(S, n_miss, t, a);
+    if (lane == 0) a.rec[t] = TileRec{D.k0, D.k1, resv, 0u, 0u, D.dup ? kTileDup : 0u};
+    __syncwarp();
+    t = t_next;
+  }
+}
+
+// ------------------------------------------------------------------ misses --
+
+// One thread merges a pre-token of n <= 8 bytes: symbols, pair ranks and
+// merged ids in its own column of shared memory (x[i * kMissThreads], so the
+// threads of a warp use distinct banks). A step takes the lowest rank,
+// replaces its occurrences left to right without overlap while compacting,
+// and looks up again only the pairs next to a merged symbol, two at a time.
+// The final ids go to out[0 .. count).
+constexpr int kMissThreads = 256;
+constexpr int kTinyMax = 8;
+struct TinyScratch {
+  uint32_t sy[kTinyMax * kMissThreads], rk[kTinyMax * kMissThreads], nw[kTinyMax * kMissThreads];
+};
+
+__device__ uint32_t merge_thread(TinyScratch& Z, const uint8_t* src, uint32_t n, const Tables& T,
+                                 const int32_t* byte_id, uint32_t* out) {
+  uint32_t* sy = Z.sy + threadIdx.x;
+  uint32_t* rk = Z.rk + threadIdx.x;
+  uint32_t* nw = Z.nw + threadIdx.x;
+  for (uint32_t i = 0; i < n; ++i) sy[i * kMissThreads] = (uint32_t)byte_id[src[i]];
+  uint32_t redo = n > 1 ? (1u << (n - 1)) - 1u : 0u;  // pairs to look up
+  for (;;) {
+    while (redo) {
+      const uint32_t p1 = __ffs(redo) - 1;
+      redo &= redo - 1;
+      const uint32_t p2 = redo ? __ffs(redo) - 1 : kNone;
+      redo &= redo - 1;
+      uint32_t r1, w1, r2 = kInf, w2 = 0;
+      lookup_pair2(T, sy[p1 * kMissThreads], sy[(p1 + 1) * kMissThreads], p2 != kNone ? sy[p2 * kMissThreads] : kNone,
+                   p2 != kNone ? sy[(p2 + 1) * kMissThreads] : 0u, &r1, &w1, &r2, &w2);
+      rk[p1 * kMissThreads] = r1;
+      nw[p1 * kMissThreads] = w1;
+      if (p2 != kNone) {
+        rk[p2 * kMissThreads] = r2;
+        nw[p2 * kMissThreads] = w2;
+      }
+    }
+    uint32_t best = kInf;
+    for (uint32_t i = 0; i + 1 < n; ++i) best = min(best, rk[i * kMissThreads]);
+    if (best == kInf) break;
+    uint32_t m = 0;
+    for (uint32_t i = 0; i < n; ++m) {
+      if (i + 1 < n && rk[i * kMissThreads] == best) {
+        sy[m * kMissThreads] = nw[i * kMissThreads];
+        redo |= (1u << m) | (m ? 1u << (m - 1) : 0u);  // the merged symbol's pairs
+        i += 2;
+      } else {
+        sy[m * kMissThreads] = sy[i * kMissThreads];
+        rk[m * kMissThreads] = rk[i * kMissThreads];
+        nw[m * kMissThreads] = nw[i * kMissThreads];
+        i += 1;
+      }
+    }
+    n = m;
+    redo &= n > 1 ? (1u << (n - 1)) - 1u : 0u;
+  }
+  for (uint32_t i = 0; i < n; ++i) out[i] = sy[i * kMissThreads];
+  return n;
+}
+
+// The queued cache misses of every tile, a warp per 32 queue entries: up to
+// 8 bytes a lane each (merge_thread); then, in rounds, groups of 8 lanes take
+// the misses of 9 to 16 bytes, groups of 16 those of 17 to 32, and the whole
+// warp each longer one (merge_group). Each writes its ids at its reserved
+// stage position, holes over the rest of the reservation, the document mark
+// on its first id, and adds its holes to its tile's record.
+constexpr int kMissBlocksPerSm = 5;
+__global__ void __launch_bounds__(kMissThreads, kMissBlocksPerSm) k_misses(const uint8_t* bytes, const uint64_t* queue,
+                                                                           int64_t queue_cap, uint32_t* stage,
+                                                                           TileRec* rec, Tables T, DevSmall* small) {
+  __shared__ GroupScratch grp[kMissThreads / 32];
+  __shared__ TinyScratch tiny;
+  __shared__ int32_t byte_id[256];
+  const unsigned long long n_raw = small->n_misses;
+  const uint64_t n_q = n_raw < (unsigned long long)queue_cap ? n_raw : (unsigned long long)queue_cap;
+  if (n_q == 0) return;
+  for (int i = threadIdx.x; i < 256; i += kMissThreads) byte_id[i] = T.byte_id[i];
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  GroupScratch& W = grp[threadIdx.x >> 5];
+  const uint64_t warps = (uint64_t)gridDim.x * (kMissThreads / 32);
+  for (uint64_t q0 = ((uint64_t)blockIdx.x * (kMissThreads / 32) + (threadIdx.x >> 5)) * 32; q0 < n_q; q0 += warps * 32) {
+    const uint64_t e = q0 + lane < n_q ? queue[q0 + lane] : 0ull;
+    const uint32_t len = q0 + lane < n_q ? (uint32_t)(e >> 10) & 0x7Fu : 0u;  // 0: no entry
+    // where a queue entry's bytes, ids and tile record are
+    auto src_of = [&](uint64_t x) { return bytes + (int64_t)(x >> 29) * kTileOwn + (int64_t)(x & 0x3FFu); };
+    auto out_of = [&](uint64_t x) { return stage + (int64_t)(x >> 29) * kTileBits + ((x >> 18) & 0x7FFu); };
+    auto finish = [&](uint64_t x, uint32_t n, uint32_t cnt, uint32_t* out) {
+      for (uint32_t q = cnt; q < n; ++q) out[q] = kIdHole;
+      if ((x >> 17) & 1u) out[0] |= kIdDoc;
+      if (n > cnt) atomicAdd(&rec[(int64_t)(x >> 29)].holes, n - cnt);
+    };
+    uint32_t m8 = __ballot_sync(0xFFFFFFFFu, len > 8u && len <= (uint32_t)kCacheMaxLen);
+    uint32_t m16 = __ballot_sync(0xFFFFFFFFu, len > (uint32_t)kCacheMaxLen && len <= 32u);
+    uint32_t m32 = __ballot_sync(0xFFFFFFFFu, len > 32u);
+    // One round: group g of G lanes takes the g-th entry of *mask (none past
+    // its end); the round's entries leave the mask.
+    auto round = [&](uint32_t* mask, auto merge, int G) {
+      const int g = lane / G;
+      uint32_t mm = *mask;
+      for (int x = 0; x < g; ++x) mm &= mm - 1u;
+      const bool on = mm != 0;
+      const int src = on ? __ffs(mm) - 1 : 0;
+      for (int x = 0; x < 32 / G; ++x) *mask &= *mask - 1u;
+      const uint64_t ge = __shfl_sync(0xFFFFFFFFu, e, src);
+      const uint32_t n = on ? (uint32_t)(ge >> 10) & 0x7Fu : 0u;
+      uint32_t* out = out_of(ge);
+      const uint32_t cnt = merge(src_of(ge), n, out);
+      __syncwarp();
+      if (on && (lane & (G - 1)) == 0) finish(ge, n, cnt, out);
+    };
+    if (len != 0 && len <= 8u) {  // up to 8 bytes: each lane its own
+      uint32_t* out = out_of(e);
+      const uint32_t cnt = merge_thread(tiny, src_of(e), len, T, byte_id, out);
+      finish(e, len, cnt, out);
+    }
+    __syncwarp();
+    while (m8)
+      round(&m8, [&](const uint8_t* src, uint32_t n, uint32_t* out) { return merge_group<8>(W, src, n, T, byte_id, out); }, 8);
+    while (m16)
+      round(&m16, [&](const uint8_t* src, uint32_t n, uint32_t* out) { return merge_group<16>(W, src, n, T, byte_id, out); }, 16);
+    while (m32)
+      round(&m32, [&](const uint8_t* src, uint32_t n, uint32_t* out) { return merge_group<32>(W, src, n, T, byte_id, out); }, 32);
+  }
+}
+
+// ------------------------------------------------------------- preparation --
+
+// Per call, before k_tiles: counters reset, offsets validated, and
+// first_doc[t] = the first document k with doc_offsets[k] >= 992 t - 16
+// (n_docs + 1 if none). Thread k writes the tiles whose window start lies in
+// (doc_offsets[k - 1], doc_offsets[k]]: at most kPrepSpan of them, and a
+// longer run goes to a list that k_prep_long fills.
+constexpr int64_t kPrepSpan = 16;
+
+struct PrepRange {
+  int64_t k, t_lo, t_hi;
+};
+
+__device__ __forceinline__ int64_t floor_div(int64_t a, int64_t b) {
+  const int64_t q = a / b;
+  return (a % b != 0 && ((a < 0) != (b < 0))) ? q - 1 : q;
+}
+
+__global__ void k_prep_docs(const int64_t* doc_offsets, int64_t n_docs, int64_t n_bytes, int64_t n_tiles,
+                            int64_t* first_doc, PrepRange* ranges, int64_t range_cap, DevSmall* small) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t0 == 0) {
+    small->total = 0;
+    small->tile_ctr = 0;
+    small->n_misses = 0;
+    small->n_giants = 0;
+    small->giant_ctr = 0;
+    small->n_ranges = 0;
+  }
+  bool bad = false;
+  for (int64_t k = t0; k <= n_docs + 1; k += stride) {
+    const int64_t prev = k == 0 ? INT64_MIN : __ldg(doc_offsets + k - 1);
+    const int64_t cur = k <= n_docs ? __ldg(doc_offsets + k) : INT64_MAX;
+    if (k <= n_docs && (cur < 0 || cur > n_bytes || (k > 0 && cur < prev))) {
+      bad = true;
+      continue;
+    }
+    int64_t lo = prev == INT64_MIN ? 0 : floor_div(prev + kHalo, kTileOwn) + 1;
+    int64_t hi = cur == INT64_MAX ? n_tiles - 1 : floor_div(cur + kHalo, kTileOwn);
+    lo = lo < 0 ? 0 : lo;
+    hi = hi > n_tiles - 1 ? n_tiles - 1 : hi;
+    if (hi - lo + 1 > kPrepSpan) {
+      const unsigned long long i = atomicAdd(&small->n_ranges, 1ull);
+      if ((int64_t)i < range_cap) ranges[i] = PrepRange{k, lo + kPrepSpan, hi};
+      else bad = true;
+      hi = lo + kPrepSpan - 1;
+    }
+    for (int64_t t = lo; t <= hi; ++t) first_doc[t] = k;
+  }
+  if (bad) atomicOr(&small->status, kStBadInput);
+}
+
+// The long runs of tiles k_prep_docs listed, a CTA per run; skipped when the
+// offsets are malformed (the runs may then overlap without bound).
+__global__ void k_prep_long(const PrepRange* ranges, int64_t* first_doc, DevSmall* small) {
+  const unsigned long long n = small->n_ranges;
+  if (small->status & kStBadInput) return;
+  for (unsigned long long r = blockIdx.x; r < n; r += gridDim.x) {
+    const PrepRange R = ranges[r];
+    for (int64_t t = R.t_lo + threadIdx.x; t <= R.t_hi; t += blockDim.x) first_doc[t] = R.k;
+  }
+}
+
+// -------------------------------------------------------- deferred pieces --
+
+// Pre-tokens longer than kShortMax bytes or running past their tile's
+// margin, one CTA each (taken from a counter): the end when unknown is the
+// first pre-token start of a later tile; the CTA merge (merge_long) leaves
+// the ids in the pool at the pre-token's own bytes.
+constexpr int kGiantThreads = kThreads;
+__global__ void __launch_bounds__(kGiantThreads) k_giants(const uint8_t* bytes, GiantRec* giants, int64_t giant_cap,
+                                                          const int64_t* first_start, int64_t n_tiles, TileRec* rec,
+                                                          int32_t* pool, Tables T, DevSmall* small) {
+  __shared__ int32_t byte_id[256];
+  __shared__ uint32_t stage[kRound];
+  __shared__ uint32_t red[kThreads / 32 + 2];
+  __shared__ uint32_t carry[2];
+  __shared__ unsigned long long next;
+  __shared__ int64_t end_at;
+  const unsigned long long n = small->n_giants < (unsigned long long)giant_cap ? small->n_giants
+                                                                               : (unsigned long long)giant_cap;
+  if (n == 0) return;
+  for (int i = threadIdx.x; i < 256; i += kGiantThreads) byte_id[i] = T.byte_id[i];
+  LongScratch L{stage, red, carry};
+  for (;;) {
+    if (threadIdx.x == 0) next = atomicAdd(&small->giant_ctr, 1ull);
+    __syncthreads();
+    const unsigned long long g = next;
+    if (g >= n) break;
+    GiantRec R = giants[g];
+    if (R.end < 0) {
+      // the first tile after R's with a pre-token start holds the end
+      if (threadIdx.x == 0) end_at = INT64_MAX;
+      __syncthreads();
+      for (int64_t t = R.tile + 1; t < n_tiles; t += kGiantThreads) {
+        const int64_t tt = t + threadIdx.x;
+        const int64_t fs = tt < n_tiles ? first_start[tt] : INT64_MAX;
+        if (fs != INT64_MAX) atomicMin(reinterpret_cast<long long*>(&end_at), (long long)fs);
+        __syncthreads();
+        if (end_at != INT64_MAX) break;
+        __syncthreads();
+      }
+      R.end = end_at;
+      if (R.end == INT64_MAX || R.end <= R.start) {
+        if (threadIdx.x == 0) atomicOr(&small->status, kStInternal);
+        R.end = R.start + 1;
+      }
+    }
+    const uint32_t cnt = merge_long(bytes, R.start, (uint32_t)(R.end - R.start), pool + R.start, T, byte_id, L);
+    if (threadIdx.x == 0) {
+      giants[g].count = cnt;
+      atomicAdd(&rec[R.tile].extra, cnt - 1u);
+    }
+    __syncthreads();
+  }
+}
+
+// ----------------------------------------------------------------- output --
+// The exclusive offsets of the tiles' final counts (stage entries, less
+// holes, plus extra ids) in two levels: k_scan_tiles scans blocks of
+// kScanThreads tiles, k_scan_tile_sums (one CTA) the block sums and writes
+// the call's token count.
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads) k_scan_tiles(const TileRec* rec, int64_t n_tiles, uint64_t* tile_base,
+                                                             uint64_t* block_sum) {
+  __shared__ uint64_t red[kScanThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t b = blockIdx.x;
+  const int64_t t = b * kScanThreads + threadIdx.x;
+  uint64_t v = 0;
+  if (t < n_tiles) {
+    const TileRec R = rec[t];
+    v = (uint64_t)R.resv - R.holes + R.extra;
+  }
+  uint64_t incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint64_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) red[warp] = incl;
+  __syncthreads();
+  uint64_t before = 0, all = 0;
+  for (int w = 0; w < kScanThreads / 32; ++w) {
+    before += w < warp ? red[w] : 0ull;
+    all += red[w];
+  }
+  if (t < n_tiles) tile_base[t] = before + incl - v;
+  if (threadIdx.x == 0) block_sum[b] = all;
+}
+
+__global__ void __launch_bounds__(kScanThreads) k_scan_tile_sums(uint64_t* block_sum, int64_t n_blocks,
+                                                                 DevSmall* small) {
+  __shared__ uint64_t red[kScanThreads / 32];
+  __shared__ uint64_t carry;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int64_t b0 = 0; b0 < n_blocks; b0 += kScanThreads) {
+    const int64_t b = b0 + threadIdx.x;
+    const uint64_t v = b < n_blocks ? block_sum[b] : 0ull;
+    uint64_t incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint64_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    if (lane == 31) red[warp] = incl;
+    __syncthreads();
+    uint64_t before = 0, all = 0;
+    for (int w = 0; w < kScanThreads / 32; ++w) {
+      before += w < warp ? red[w] : 0ull;
+      all += red[w];
+    }
+    if (b < n_blocks) block_sum[b] = carry + before + incl - v;
+    __syncthreads();
+    if (threadIdx.x == 0) carry += all;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) small->total = (int64_t)carry;
+}
+
+// A warp per tile: its stage entries to out_ids at the tile's offset without
+// the holes, each placeholder expanded to its deferred pre-token's ids from
+// the pool. A document mark (the first id of a document) gives document
+// offsets: the r-th mark of the tile belongs to the r-th distinct document
+// start in it, which is document k0 + r unless the tile has empty documents;
+// then a table of the last document at each distinct start, built from the
+// offsets in shared memory, maps r to its documents. The documents at the
+// end of the last one get the tile's end.
+constexpr int kCompactWarps = 8;
+__global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* rec, const uint32_t* stage,
+                                                                const uint64_t* tile_base, const uint64_t* block_sum,
+                                                                const GiantRec* giants, const int32_t* pool,
+                                                                const int64_t* doc_offsets, int64_t n_tiles,
+                                                                int32_t* out_ids, int64_t capacity,
+                                                                int64_t* out_offsets, DevSmall* small) {
+  __shared__ uint16_t docq[kCompactWarps][kTileOwn + 2];  // per mark rank: its last document - k0 (tiles with empty documents)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t warps = (int64_t)gridDim.x * kCompactWarps;
+  bool over = false;
+  for (int64_t t = (int64_t)blockIdx.x * kCompactWarps + warp; t < n_tiles; t += warps) {
+    const TileRec R = rec[t];
+    const uint64_t base = tile_base[t] + block_sum[t / kScanThreads];
+    const uint32_t* src = stage + t * (int64_t)kTileBits;
+    const bool dup = (R.flags & kTileDup) != 0;
+    const int64_t t0 = t * (int64_t)kTileOwn;
+    if (dup) {
+      // docq[r] = the last document at the r-th distinct start in the tile
+      uint32_t r = 0;
+      for (int64_t k = R.k0; k < R.k1; k += 32) {
+        const int64_t kk = k + lane;
+        const int64_t o = kk < R.k1 ? doc_offsets[kk] : INT64_MAX;
+        const int64_t o_next = kk + 1 < R.k1 ? doc_offsets[kk + 1] : INT64_MAX;
+        const bool last = kk < R.k1 && o_next != o;
+        const uint32_t lb = __ballot_sync(0xFFFFFFFFu, last);
+        const uint32_t rr = r + __popc(lb & lanemask_lt());
+        if (last && rr < (uint32_t)(kTileOwn + 2)) docq[warp][rr] = (uint16_t)(kk - R.k0);
+        r += __popc(lb);
+      }
+      __syncwarp();
+    }
+    uint64_t shift = 0;  // extra ids of the placeholders so far
+    uint32_t nmark = 0;
+    for (uint32_t q0 = 0; q0 < R.resv; q0 += 32) {
+      const bool in = q0 + lane < R.resv;
+      const uint32_t v = in ? src[q0 + lane] : kIdHole;
+      const bool valid = (v & (kIdSpecial | kIdLong)) != kIdSpecial;
+      const bool ph = valid && (v & kIdSpecial);
+      const uint32_t g_cnt = ph ? giants[v & kIdIndex].count : 1u;
+      const uint32_t n_ids = valid ? g_cnt : 0u;
+      const uint32_t incl = warp_incl_scan(n_ids);
+      const uint64_t at = base + shift + (incl - n_ids);
+      if (valid && !ph) {
+        if ((int64_t)at < capacity) out_ids[at] = (int32_t)(v & ~kIdDoc);
+        else over = true;
+      }
+      const bool mark = valid && (v & kIdDoc);
+      const uint32_t mb = __ballot_sync(0xFFFFFFFFu, mark);
+      if (mark) {
+        const uint32_t r = nmark + __popc(mb & lanemask_lt());
+        if (!dup) {
+          const int64_t k = R.k0 + r;
+          if (k < R.k1) out_offsets[k] = (int64_t)at;
+          else atomicOr(&small->status, kStInternal);
+        } else {
+          const int64_t k_hi = R.k0 + (r < (uint32_t)(kTileOwn + 2) ? docq[warp][r] : 0);
+          int64_t k_lo = r == 0 ? R.k0 : R.k0 + docq[warp][r - 1] + 1;
+          for (int64_t k = k_lo; k <= k_hi; ++k) out_offsets[k] = (int64_t)at;
+        }
+      }
+      uint32_t phm = __ballot_sync(0xFFFFFFFFu, ph);
+      while (phm) {
+        const int src_lane = __ffs(phm) - 1;
+        phm &= phm - 1;
+        const uint32_t gv = __shfl_sync(0xFFFFFFFFu, v, src_lane);
+        const uint64_t gat = __shfl_sync(0xFFFFFFFFu, at, src_lane);
+        const GiantRec G = giants[gv & kIdIndex];
+        for (uint32_t q = lane; q < G.count; q += 32) {
+          if ((int64_t)(gat + q) < capacity) out_ids[gat + q] = pool[G.start + q];
+          else over = true;
+        }
+      }
+      nmark += __popc(mb);
+      shift += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    // documents with no mark: at the end of the last document
+    const int64_t k_rest = !dup ? R.k0 + nmark : (nmark == 0 ? R.k0 : R.k0 + docq[warp][nmark - 1] + 1);
+    for (int64_t k = k_rest + lane; k < R.k1; k += 32) out_offsets[k] = (int64_t)(base + shift);
+    (void)t0;
+    __syncwarp();
+  }
+  if (over) atomicOr(&small->status, kStCapacity);
+}
+
+// ------------------------------------------------------------------ split --
+// bpe_pretokenize_batch: the tiles' start bits alone, a warp per tile (no
+// workspace: lane 0 finds the tile's first document by binary search).
+constexpr int kSplitWarps = 4;
+__global__ void __launch_bounds__(32 * kSplitWarps) k_split_tiles(const uint8_t* bytes, int64_t n_bytes,
+                                                                  const int64_t* doc_offsets, int64_t n_docs,
+                                                                  int64_t n_tiles, uint32_t* out_bits) {
+  __shared__ TileWin Wsh[kSplitWarps];
+  TileWin& W = Wsh[threadIdx.x >> 5];
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * kSplitWarps + (threadIdx.x >> 5);
+  if (t >= n_tiles) return;
+  const int64_t t0 = t * (int64_t)kTileOwn;
+  const bool aligned = (reinterpret_cast<uintptr_t>(bytes) & 15u) == 0;
+  tile_load_bytes(W, bytes, n_bytes, t0, aligned);
+  int64_t kA = 0;
+  if (lane == 0) {
+    int64_t lo = 0, hi = n_docs + 1;  // first k with doc_offsets[k] >= t0 - kHalo
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (doc_offsets[mid] < t0 - kHalo) lo = mid + 1;
+      else hi = mid;
+    }
+    kA = lo;
+  }
+  kA = __shfl_sync(0xFFFFFFFFu, kA, 0);
+  int64_t d_first = __ldg(doc_offsets), d_last = __ldg(doc_offsets + n_docs);
+  d_first = d_first < 0 ? 0 : (d_first > n_bytes ? n_bytes : d_first);
+  d_last = d_last < d_first ? d_first : (d_last > n_bytes ? n_bytes : d_last);
+  tile_load_docs(W, doc_offsets, n_docs, t0, kA, d_first, d_last);
+  cp_async_wait_all();
+  __syncwarp();
+  const uint32_t m = start_mask32(W, kHalo + 32 * lane);
+  const int64_t gw = t0 / 32 + lane, n_words = (n_bytes + 31) / 32;
+  if (lane < kTileLanes && gw < n_words) {
+    uint32_t v = m;
+    const int64_t first_bit = gw * 32;
+    if (first_bit + 32 > n_bytes) v &= (1u << (n_bytes - first_bit)) - 1u;
+    out_bits[gw] = v;
+  }
+}
+
+}  // namespace
