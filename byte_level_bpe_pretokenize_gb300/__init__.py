@@ -58,7 +58,8 @@ _lock = threading.Lock()
 _lib = None
 
 EXPORTS = ["bpe_build", "bpe_encode_batch", "bpe_encode_batch_host", "bpe_encode_batch_noalloc", "bpe_pretokenize_batch", "bpe_decode_batch", "bpe_set_word_cache",
-           "bpe_set_timing_events", "bpe_sync_status", "bpe_table_info", "bpe_destroy", "bpe_last_error"]
+           "bpe_set_timing_events", "bpe_sync_status", "bpe_table_info", "bpe_table_monotone", "bpe_merges_monotone",
+           "bpe_destroy", "bpe_last_error"]
 
 
 def lib():
@@ -91,6 +92,10 @@ def lib():
             L.bpe_sync_status.argtypes = [p, p]
             L.bpe_table_info.restype = ctypes.c_int
             L.bpe_table_info.argtypes = [p, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+            L.bpe_table_monotone.restype = ctypes.c_int
+            L.bpe_table_monotone.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
+            L.bpe_merges_monotone.restype = ctypes.c_int
+            L.bpe_merges_monotone.argtypes = [p, i64, i64, ctypes.POINTER(ctypes.c_int)]
             L.bpe_destroy.restype = ctypes.c_int
             L.bpe_destroy.argtypes = [p]
             L.bpe_last_error.restype = ctypes.c_char_p
@@ -181,6 +186,20 @@ def bpe_table_info(handle: int) -> tuple[int, int]:
     a, b = ctypes.c_int64(), ctypes.c_int64()
     _check(lib().bpe_table_info(handle, ctypes.byref(a), ctypes.byref(b)))
     return a.value, b.value
+
+
+def bpe_table_monotone(handle: int) -> bool:
+    m = ctypes.c_int()
+    _check(lib().bpe_table_monotone(handle, ctypes.byref(m)))
+    return bool(m.value)
+
+
+def bpe_merges_monotone(merges, n_vocab: int) -> bool:
+    """Host-only: whether every merge's operands are bytes or made by lower ranks."""
+    mm = np.ascontiguousarray(np.asarray(merges, dtype=np.int32).reshape(-1, 3))
+    out = ctypes.c_int()
+    _check(lib().bpe_merges_monotone(mm.ctypes.data if mm.size else None, len(mm), n_vocab, ctypes.byref(out)))
+    return bool(out.value)
 
 
 def bpe_destroy(handle: int) -> None:

@@ -921,25 +921,6 @@ __device__ __forceinline__ uint32_t cache_slot(const CacheKey& K, uint32_t len, 
   return cache_hash(K.x0, K.x1, K.x2, K.x3, len) & C.mask;
 }
 
-// Count of ids (1..3) for key K of len bytes given the entry {ea, eb} at its
-// home slot (loaded by the caller), 0 when absent; the ids go to ids[0..2].
-// The home slot is recomputed only when the probe goes on past it.
-__device__ __forceinline__ uint32_t cache_resolve(const Cache& C, const CacheKey& K, uint32_t len, uint4 ea, uint4 eb,
-                                                  uint32_t* ids) {
-  uint32_t slot = kNone;
-  for (uint32_t probe = 0; probe <= C.mask; ++probe) {
-    if (eb.x == 0) return 0;
-    if ((eb.x & 31u) == len && ea.x == K.x0 && ea.y == K.x1 && ea.z == K.x2 && ea.w == K.x3) {
-      ids[0] = eb.y;
-      ids[1] = eb.z;
-      ids[2] = eb.w;
-      return (eb.x >> 5) & 7u;
-    }
-    slot = ((slot == kNone ? cache_slot(K, len, C) : slot) + 1) & C.mask;
-    ldg32(C.e + 2 * slot, ea, eb);
-  }
-  return 0;
-}
 
 }  // namespace
 
@@ -1099,6 +1080,7 @@ struct bpe_handle {
   int device = 0;
   int n_sms = 1;  // multiprocessors of the device (grids of persistent kernels)
   int64_t n_merges = 0, n_vocab = 0;
+  int monotone = 1;  // every merge's operands are made by lower ranks (bpe_merges_monotone)
   uint4* d_ht = nullptr;
   uint32_t hmask = 0;
   int32_t* d_mrows = nullptr;
@@ -1487,6 +1469,7 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
   h->device = device;
   h->n_merges = n_merges;
   h->n_vocab = n_vocab;
+  bpe_merges_monotone(merges, n_merges, n_vocab, &h->monotone);
   h->hmask = (uint32_t)(nb - 1);
   auto cleanup = [&](int code) {
     bpe_destroy(h);
@@ -1565,6 +1548,35 @@ int bpe_table_info(const bpe_handle* h, int64_t* n_merges, int64_t* n_vocab) {
   if (!h) return fail(BPE_ERR_INVALID_ARG, "null handle");
   if (n_merges) *n_merges = h->n_merges;
   if (n_vocab) *n_vocab = h->n_vocab;
+  return BPE_OK;
+}
+
+int bpe_table_monotone(const bpe_handle* h, int* monotone) {
+  if (!h || !monotone) return fail(BPE_ERR_INVALID_ARG, "bpe_table_monotone: bad arguments");
+  *monotone = h->monotone;
+  return BPE_OK;
+}
+
+int bpe_merges_monotone(const int32_t* merges, int64_t n_merges, int64_t n_vocab, int* monotone) {
+  if (!monotone || n_merges < 0 || n_vocab < 0 || (n_merges > 0 && !merges))
+    return fail(BPE_ERR_INVALID_ARG, "bpe_merges_monotone: bad arguments");
+  // made[id]: the lowest rank whose merge makes id (-1: a single byte or an
+  // id no merge makes, which counts as present from the start)
+  std::vector<int64_t> made((size_t)n_vocab, -1);
+  for (int64_t r = n_merges - 1; r >= 0; --r) {
+    const int32_t nw = merges[3 * r + 2];
+    if (nw < 0 || nw >= n_vocab) return fail(BPE_ERR_BAD_TABLE, "bpe_merges_monotone: merge id out of range");
+    made[(size_t)nw] = r;
+  }
+  int ok = 1;
+  for (int64_t r = 0; r < n_merges && ok; ++r) {
+    for (int q = 0; q < 2; ++q) {
+      const int32_t id = merges[3 * r + q];
+      if (id < 0 || id >= n_vocab) return fail(BPE_ERR_BAD_TABLE, "bpe_merges_monotone: merge id out of range");
+      if (made[(size_t)id] >= r) ok = 0;
+    }
+  }
+  *monotone = ok;
   return BPE_OK;
 }
 

@@ -188,6 +188,116 @@ __device__ TileDocs tile_load_docs(TileWin& W, const int64_t* doc_offsets, int64
   return TileDocs{kA + n_lt0, kA + n_lt1, dup};
 }
 
+// ------------------------------------------------------------- ASCII split --
+// Start bits of window positions [p0, p0 + 32) (p0 a multiple of 16) when
+// bytes p0 - 4 .. p0 + 35 are all ASCII; returns false otherwise (the caller
+// then takes start_mask32, which handles every input). The rules are those of
+// start_mask32 (B0..B3 of the split predicate) on 32-bit masks in byte order:
+//   * per word, carry-free SWAR range tests give 0x80 in each byte that is a
+//     letter, a digit, whitespace or U+0020;
+//   * a multiply gathers those bits: for flag words a (bytes 0..3) and b
+//     (bytes 4..7), ((a >> 4) | b) * 0x204081 has the eight flags in byte
+//     order in bits 24..31 (each partial product lands on its own bit);
+//   * B2 = S & (~prev S | (~next S & ~next doc start)), B3 = ~S & ~prev U+0020
+//     & (prev S | class change among letter / digit / other), plus the
+//     document starts, minus the bytes outside every document;
+//   * each apostrophe at p0 - 3 .. p0 + 31 then resolves its contraction:
+//     when it is eligible (a document start, or after a letter, a digit or
+//     whitespace other than U+0020) and one of s t m d (or re ve ll) follows
+//     in its document, the byte after it loses its start (B0) and the byte
+//     after the suffix gets one (B1).
+__device__ __forceinline__ uint4 lds_u128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"((unsigned)__cvta_generic_to_shared(p)));
+  return v;
+}
+
+struct Flags4 {
+  uint32_t L, N, S, SP;
+};
+
+__device__ __forceinline__ Flags4 ascii_flags(uint32_t w) {
+  const uint32_t H = 0x80808080u;
+  const uint32_t t = w | 0x20202020u;  // fold case
+  Flags4 f;
+  f.L = (t + 0x1F1F1F1Fu) & ~(t + 0x05050505u) & H;   // 'a' .. 'z'
+  f.N = (w + 0x50505050u) & ~(w + 0x46464646u) & H;   // '0' .. '9'
+  f.SP = ~((w ^ 0x20202020u) + 0x7F7F7F7Fu) & H;      // == 0x20
+  f.S = ((w + 0x77777777u) & ~(w + 0x72727272u) & H) | f.SP;  // 0x09 .. 0x0D or 0x20
+  return f;
+}
+
+// Eight 0x80 flags of words a, b -> 8 bits in byte order, in bits 24..31.
+__device__ __forceinline__ uint32_t gather8(uint32_t a, uint32_t b) { return ((a >> 4) | b) * 0x00204081u; }
+// Bits 24..31 of p0..p3 -> one word (p0's in byte 0).
+__device__ __forceinline__ uint32_t gather32(uint32_t p0, uint32_t p1, uint32_t p2, uint32_t p3) {
+  return __byte_perm(__byte_perm(p0, p1, 0x0073u), __byte_perm(p2, p3, 0x0073u), 0x5410u);
+}
+
+__device__ __forceinline__ bool ascii_letter(uint32_t b) { return (uint32_t)((b | 0x20u) - 'a') < 26u; }
+__device__ __forceinline__ bool ascii_digit(uint32_t b) { return (uint32_t)(b - '0') < 10u; }
+__device__ __forceinline__ bool ascii_space(uint32_t b) { return b == 0x20u || (uint32_t)(b - 9u) < 5u; }
+
+template <class SS>
+__device__ __forceinline__ bool ascii_split32(const SS& W, int p0, uint32_t* out) {
+  const uint4 a = lds_u128(W.win + p0), b = lds_u128(W.win + p0 + 16);
+  const uint32_t wp = lds_u32(reinterpret_cast<const uint32_t*>(W.win + p0) - 1);
+  const uint32_t wn = lds_u32(reinterpret_cast<const uint32_t*>(W.win + p0 + 32));
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  if ((a.x | a.y | a.z | a.w | b.x | b.y | b.z | b.w | wp | wn) & 0x80808080u) return false;
+  Flags4 f[8];
+  uint32_t apos = 0;  // nonzero: an apostrophe among bytes p0 - 3 .. p0 + 31
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    f[m] = ascii_flags(w[m]);
+    const uint32_t x = w[m] ^ 0x27272727u;
+    apos |= (x - 0x01010101u) & ~x;
+  }
+  {
+    const uint32_t x = (wp ^ 0x27272727u) | 0xFFu;  // bytes p0 - 3 .. p0 - 1
+    apos |= (x - 0x01010101u) & ~x;
+  }
+  const uint32_t L = gather32(gather8(f[0].L, f[1].L), gather8(f[2].L, f[3].L), gather8(f[4].L, f[5].L),
+                              gather8(f[6].L, f[7].L));
+  const uint32_t N = gather32(gather8(f[0].N, f[1].N), gather8(f[2].N, f[3].N), gather8(f[4].N, f[5].N),
+                              gather8(f[6].N, f[7].N));
+  const uint32_t S = gather32(gather8(f[0].S, f[1].S), gather8(f[2].S, f[3].S), gather8(f[4].S, f[5].S),
+                              gather8(f[6].S, f[7].S));
+  const uint32_t SP = gather32(gather8(f[0].SP, f[1].SP), gather8(f[2].SP, f[3].SP), gather8(f[4].SP, f[5].SP),
+                               gather8(f[6].SP, f[7].SP));
+  // the byte before (p0 - 1) and after (p0 + 32)
+  const uint32_t bp = wp >> 24, bn = wn & 0xFFu;
+  const uint32_t pL = (L << 1) | (ascii_letter(bp) ? 1u : 0u), pN = (N << 1) | (ascii_digit(bp) ? 1u : 0u);
+  const uint32_t pS = (S << 1) | (ascii_space(bp) ? 1u : 0u), pSP = (SP << 1) | (bp == 0x20u ? 1u : 0u);
+  const uint32_t nS = (S >> 1) | (ascii_space(bn) ? 0x80000000u : 0u);
+  const uint32_t D = bits32_at(W.docbits, p0), nD = bits32_at(W.docbits, p0 + 1);
+  const uint32_t B2 = S & (~pS | (~nS & ~nD));
+  const uint32_t B3 = ~S & ~pSP & (pS | (L ^ pL) | (N ^ pN));
+  uint32_t base = B2 | B3 | D;
+  if (apos & 0x80808080u) {
+    // contractions, one apostrophe at a time (positions relative to p0)
+    for (int j = -3; j < 32; ++j) {
+      if (W.win[p0 + j] != 0x27u) continue;
+      const int q = p0 + j;
+      const bool at_start = bit_at(W.docbits, q);
+      const uint32_t c = W.win[q - 1];
+      const bool eligible = at_start || ascii_letter(c) || ascii_digit(c) || (ascii_space(c) && c != 0x20u);
+      if (!eligible || bit_at(W.docbits, q + 1)) continue;
+      const uint32_t s1 = W.win[q + 1];
+      int k = 0;
+      if (s1 == 's' || s1 == 't' || s1 == 'm' || s1 == 'd') k = 1;
+      else if (!bit_at(W.docbits, q + 2) && is_suffix2(s1, W.win[q + 2])) k = 2;
+      if (!k) continue;
+      if (j + 1 >= 0 && j + 1 < 32) base &= ~(1u << (j + 1));
+      if (j + 1 + k >= 0 && j + 1 + k < 32) base |= 1u << (j + 1 + k);
+    }
+  }
+  *out = base & ~bits32_at(W.outbits, p0);
+  return true;
+}
+
 // A word-cache key from the window (tile positions [s, s + len), len <= 16).
 __device__ __forceinline__ CacheKey tile_key(const TileWin& W, int s, int len) {
   const int ws = kHalo + s;
@@ -195,15 +305,47 @@ __device__ __forceinline__ CacheKey tile_key(const TileWin& W, int s, int len) {
   const uint32_t sh = (uint32_t)(ws & 3) * 8u;
   const uint32_t a0 = lds_u32(wv), a1 = lds_u32(wv + 1), a2 = lds_u32(wv + 2), a3 = lds_u32(wv + 3),
                  a4 = lds_u32(wv + 4);
-  const uint32_t nbit = 8u * (uint32_t)len;
-  const uint64_t m_lo = nbit >= 64 ? ~0ull : (1ull << nbit) - 1ull;
-  const uint64_t m_hi = nbit <= 64 ? 0ull : (nbit >= 128 ? ~0ull : (1ull << (nbit - 64)) - 1ull);
+  // word k keeps its low min(max(8 len - 32 k, 0), 32) bits: the top word of
+  // (0 : ~0) shifted left by that many (the shift clamps at 32)
+  const int nbit = 8 * len;
   CacheKey K;
-  K.x0 = __funnelshift_r(a0, a1, sh) & (uint32_t)m_lo;
-  K.x1 = __funnelshift_r(a1, a2, sh) & (uint32_t)(m_lo >> 32);
-  K.x2 = __funnelshift_r(a2, a3, sh) & (uint32_t)m_hi;
-  K.x3 = __funnelshift_r(a3, a4, sh) & (uint32_t)(m_hi >> 32);
+  K.x0 = __funnelshift_r(a0, a1, sh) & __funnelshift_lc(~0u, 0u, (uint32_t)nbit);
+  K.x1 = __funnelshift_r(a1, a2, sh) & __funnelshift_lc(~0u, 0u, (uint32_t)max(nbit - 32, 0));
+  K.x2 = __funnelshift_r(a2, a3, sh) & __funnelshift_lc(~0u, 0u, (uint32_t)max(nbit - 64, 0));
+  K.x3 = __funnelshift_r(a3, a4, sh) & __funnelshift_lc(~0u, 0u, (uint32_t)max(nbit - 96, 0));
   return K;
+}
+
+// Count of ids (1..3) for key K of len bytes given the entry {ea, eb} at its
+// home slot, 0 when the key is absent; the ids go to ids[0..2]. The home slot
+// settles almost every probe (the table is at most 1/8 full); the rest of the
+// probe chain is kept out of line.
+__device__ __noinline__ uint32_t cache_probe_chain(const Cache& C, const CacheKey& K, uint32_t len, uint32_t* ids) {
+  uint32_t slot = cache_slot(K, len, C);
+  for (uint32_t probe = 0; probe < C.mask; ++probe) {
+    slot = (slot + 1) & C.mask;
+    uint4 ea, eb;
+    ldg32(C.e + 2 * slot, ea, eb);
+    if (eb.x == 0) return 0;
+    if ((eb.x & 31u) == len && ea.x == K.x0 && ea.y == K.x1 && ea.z == K.x2 && ea.w == K.x3) {
+      ids[0] = eb.y;
+      ids[1] = eb.z;
+      ids[2] = eb.w;
+      return (eb.x >> 5) & 7u;
+    }
+  }
+  return 0;
+}
+
+__device__ __forceinline__ uint32_t tile_resolve(const Cache& C, const CacheKey& K, uint32_t len, const uint4& ea,
+                                                 const uint4& eb, uint32_t* ids) {
+  const bool same = (eb.x & 31u) == len && ((ea.x ^ K.x0) | (ea.y ^ K.x1) | (ea.z ^ K.x2) | (ea.w ^ K.x3)) == 0;
+  ids[0] = eb.y;
+  ids[1] = eb.z;
+  ids[2] = eb.w;
+  if (same) return (eb.x >> 5) & 7u;
+  if (eb.x == 0) return 0;
+  return cache_probe_chain(C, K, len, ids);
 }
 
 // The held miss records of tile t into the GPU-wide queue (one atomic per
@@ -253,7 +395,9 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm) k_tiles(TileArgs
     // pre-token before it.
     const int p0 = kHalo + 32 * lane;
     const uint32_t dw = bits32_at(W.docbits, p0), ow = bits32_at(W.outbits, p0);
-    const uint32_t m = start_mask32(W, p0) | (dw & ow);
+    uint32_t m;
+    if (!ascii_split32(W, p0, &m)) m = start_mask32(W, p0);
+    m |= dw & ow;
     const bool own = lane < kTileLanes;
     const uint32_t cnt = own ? (uint32_t)__popc(m) : 0u;
     const uint32_t incl = warp_incl_scan(cnt);
@@ -315,7 +459,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm) k_tiles(TileArgs
         const uint32_t len = (info[h] >> 10) & 0x7FFu;
         cnt2[h] = 0;
         if (kind == kProbe) {
-          cnt2[h] = cache_resolve(a.C, K[h], len, ea[h], eb[h], idv[h]);
+          cnt2[h] = tile_resolve(a.C, K[h], len, ea[h], eb[h], idv[h]);
           if (!cnt2[h]) kind = kMiss;
         } else if (kind == kOne) {  // a single byte is its own token
           idv[h][0] = (uint32_t)__ldg(a.T.byte_id + W.win[kHalo + (info[h] & 0x3FFu)]);
@@ -683,13 +827,14 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_tile_sums(uint64_t* block
 
 // A warp per tile: its stage entries to out_ids at the tile's offset without
 // the holes, each placeholder expanded to its deferred pre-token's ids from
-// the pool. A document mark (the first id of a document) gives document
+// the pool. The stage is read with streaming loads (it is not read again). A document mark (the first id of a document) gives document
 // offsets: the r-th mark of the tile belongs to the r-th distinct document
 // start in it, which is document k0 + r unless the tile has empty documents;
 // then a table of the last document at each distinct start, built from the
 // offsets in shared memory, maps r to its documents. The documents at the
 // end of the last one get the tile's end.
 constexpr int kCompactWarps = 8;
+constexpr int kCompactChunks = 8;  // stage chunks of 32 entries a lane loads before it processes any
 __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* rec, const uint32_t* stage,
                                                                 const uint64_t* tile_base, const uint64_t* block_sum,
                                                                 const GiantRec* giants, const int32_t* pool,
@@ -701,11 +846,16 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* r
   const int64_t warps = (int64_t)gridDim.x * kCompactWarps;
   bool over = false;
   for (int64_t t = (int64_t)blockIdx.x * kCompactWarps + warp; t < n_tiles; t += warps) {
+    // Every load of the tile is issued before any result is used: the record,
+    // the offset and the first kCompactChunks chunks of the stage slot (a slot
+    // is always kTileBits entries, so the loads stay inside it).
+    const uint32_t* src = stage + t * (int64_t)kTileBits;
+    uint32_t v[kCompactChunks];
+#pragma unroll
+    for (int c = 0; c < kCompactChunks; ++c) v[c] = __ldcs(src + 32 * c + lane);
     const TileRec R = rec[t];
     const uint64_t base = tile_base[t] + block_sum[t / kScanThreads];
-    const uint32_t* src = stage + t * (int64_t)kTileBits;
     const bool dup = (R.flags & kTileDup) != 0;
-    const int64_t t0 = t * (int64_t)kTileOwn;
     if (dup) {
       // docq[r] = the last document at the r-th distinct start in the tile
       uint32_t r = 0;
@@ -721,22 +871,22 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* r
       }
       __syncwarp();
     }
-    uint64_t shift = 0;  // extra ids of the placeholders so far
+    uint64_t shift = 0;  // ids placed so far
     uint32_t nmark = 0;
-    for (uint32_t q0 = 0; q0 < R.resv; q0 += 32) {
+    auto chunk = [&](uint32_t q0, uint32_t x) {
       const bool in = q0 + lane < R.resv;
-      const uint32_t v = in ? src[q0 + lane] : kIdHole;
-      const bool valid = (v & (kIdSpecial | kIdLong)) != kIdSpecial;
-      const bool ph = valid && (v & kIdSpecial);
-      const uint32_t g_cnt = ph ? giants[v & kIdIndex].count : 1u;
+      const uint32_t e = in ? x : kIdHole;
+      const bool valid = (e & (kIdSpecial | kIdLong)) != kIdSpecial;
+      const bool ph = valid && (e & kIdSpecial);
+      const uint32_t g_cnt = ph ? giants[e & kIdIndex].count : 1u;
       const uint32_t n_ids = valid ? g_cnt : 0u;
       const uint32_t incl = warp_incl_scan(n_ids);
       const uint64_t at = base + shift + (incl - n_ids);
       if (valid && !ph) {
-        if ((int64_t)at < capacity) out_ids[at] = (int32_t)(v & ~kIdDoc);
+        if ((int64_t)at < capacity) out_ids[at] = (int32_t)(e & ~kIdDoc);
         else over = true;
       }
-      const bool mark = valid && (v & kIdDoc);
+      const bool mark = valid && (e & kIdDoc);
       const uint32_t mb = __ballot_sync(0xFFFFFFFFu, mark);
       if (mark) {
         const uint32_t r = nmark + __popc(mb & lanemask_lt());
@@ -746,7 +896,7 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* r
           else atomicOr(&small->status, kStInternal);
         } else {
           const int64_t k_hi = R.k0 + (r < (uint32_t)(kTileOwn + 2) ? docq[warp][r] : 0);
-          int64_t k_lo = r == 0 ? R.k0 : R.k0 + docq[warp][r - 1] + 1;
+          const int64_t k_lo = r == 0 ? R.k0 : R.k0 + docq[warp][r - 1] + 1;
           for (int64_t k = k_lo; k <= k_hi; ++k) out_offsets[k] = (int64_t)at;
         }
       }
@@ -754,7 +904,7 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* r
       while (phm) {
         const int src_lane = __ffs(phm) - 1;
         phm &= phm - 1;
-        const uint32_t gv = __shfl_sync(0xFFFFFFFFu, v, src_lane);
+        const uint32_t gv = __shfl_sync(0xFFFFFFFFu, e, src_lane);
         const uint64_t gat = __shfl_sync(0xFFFFFFFFu, at, src_lane);
         const GiantRec G = giants[gv & kIdIndex];
         for (uint32_t q = lane; q < G.count; q += 32) {
@@ -764,11 +914,14 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* r
       }
       nmark += __popc(mb);
       shift += __shfl_sync(0xFFFFFFFFu, incl, 31);
-    }
+    };
+#pragma unroll
+    for (int c = 0; c < kCompactChunks; ++c)
+      if (32u * c < R.resv) chunk(32u * c, v[c]);
+    for (uint32_t q0 = 32u * kCompactChunks; q0 < R.resv; q0 += 32) chunk(q0, __ldcs(src + q0 + lane));
     // documents with no mark: at the end of the last document
     const int64_t k_rest = !dup ? R.k0 + nmark : (nmark == 0 ? R.k0 : R.k0 + docq[warp][nmark - 1] + 1);
     for (int64_t k = k_rest + lane; k < R.k1; k += 32) out_offsets[k] = (int64_t)(base + shift);
-    (void)t0;
     __syncwarp();
   }
   if (over) atomicOr(&small->status, kStCapacity);
@@ -806,7 +959,8 @@ __global__ void __launch_bounds__(32 * kSplitWarps) k_split_tiles(const uint8_t*
   tile_load_docs(W, doc_offsets, n_docs, t0, kA, d_first, d_last);
   cp_async_wait_all();
   __syncwarp();
-  const uint32_t m = start_mask32(W, kHalo + 32 * lane);
+  uint32_t m;
+  if (!ascii_split32(W, kHalo + 32 * lane, &m)) m = start_mask32(W, kHalo + 32 * lane);
   const int64_t gw = t0 / 32 + lane, n_words = (n_bytes + 31) / 32;
   if (lane < kTileLanes && gw < n_words) {
     uint32_t v = m;

@@ -93,15 +93,15 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
  *                  the next bpe_sync_status() on the handle.
  *   stream         the CUDA stream to run on.
  *
- * Workspace: the handle keeps about 9.2 bytes per input byte:
- *   - a pool of 4 bytes per input byte (scratch for pre-tokens too long for
- *     shared memory, each using the range of its own bytes);
- *   - a stage of about 4 bytes per input byte (each 4 KiB chunk's ids, before
- *     the chunk offsets are known);
- *   - records and a queue for the word-cache misses each chunk hands to the
- *     GPU-wide miss merge (about 0.8 bytes per input byte);
- *   - the start bitmask (1 bit per byte);
- *   - records of long pre-tokens and a few words per chunk.
+ * Workspace: the handle keeps about 12.6 bytes per input byte:
+ *   - a stage of 4.1 bytes per input byte (each 992-byte tile's ids at their
+ *     reserved positions, before the tiles' offsets are known);
+ *   - a queue of 4 bytes per input byte for the word-cache misses the tiles
+ *     hand to the GPU-wide miss merge (a miss has at least 2 bytes);
+ *   - a pool of 4 bytes per input byte (scratch for pre-tokens longer than
+ *     64 bytes, each using the range of its own bytes);
+ *   - about 48 bytes per tile (first document, record, first pre-token start,
+ *     offset) and records of the long pre-tokens.
  * The workspace grows (cudaFree of the old one, then cudaMalloc) the first
  * time a larger batch is seen. No kernel of the call waits on another CTA.
  */
@@ -162,18 +162,16 @@ int bpe_encode_batch_host(bpe_handle* h, const uint8_t* h_bytes, int64_t n_bytes
  *   Limit: n_bytes <= 4 MiB (4,194,304). A larger batch is rejected with
  *   BPE_ERR_INVALID_ARG before anything is queued; split it or use
  *   bpe_encode_batch. n_docs is not limited by the scratch.
- *   Scratch: one 38.7 MB array of static device memory per device (reserved
- *   when the library's module is loaded on that device, not by this call).
- *   It holds bpe_encode_batch's workspace for a 4 MiB batch:
- *     - each 4 KiB chunk's first document, token count and offset;
- *     - the records of long pre-tokens;
- *     - the records and queue of deferred word-cache misses;
- *     - the pre-token start bitmask;
- *     - the per-chunk stage of ids;
- *     - the pool for pre-tokens too long for shared memory.
+ *   Scratch: one array of about 53 MB of static device memory per device
+ *   (reserved when the library's module is loaded on that device, not by
+ *   this call). It holds bpe_encode_batch's workspace for a 4 MiB batch:
+ *     - each tile's first document, record, first pre-token start and offset;
+ *     - the stage of ids;
+ *     - the queue of word-cache misses;
+ *     - the records and the pool of long pre-tokens.
  *   The call's first kernel zeroes what must start at zero (the handle's
- *   record counter and token count); every other scratch word is written
- *   before it is read.
+ *   counters and token count); every other scratch word is written before it
+ *   is read.
  *   Set-up: the first call on each device looks up the scratch address
  *   (cudaGetSymbolAddress) and sets the kernels' shared-memory limit, with the
  *   handle's device current; make that first call before any stream capture.
@@ -259,6 +257,27 @@ int bpe_sync_status(bpe_handle* h, bpe_stream_t stream);
 
 /* Number of merges and vocabulary size of a handle (host values). */
 int bpe_table_info(const bpe_handle* h, int64_t* n_merges, int64_t* n_vocab);
+
+/*
+ * bpe_merges_monotone — whether a merge table is monotone: every merge's two
+ * operands are single bytes, or ids that a merge of lower rank makes (so a
+ * merge can only apply once its operands can exist). A trainer that merges
+ * the most frequent pair of the current symbols ("Tokenisierung", section
+ * "Byte Pair Encoding schrittweise") always writes monotone tables. On those,
+ * replacing every occurrence of the lowest-rank pair per step (this library)
+ * and replacing its leftmost occurrence per step give the same ids; on a
+ * non-monotone table they can differ (for "abab" with (ab, a) at rank 0 and
+ * (a, b) at rank 1 this library gives [ab, ab]).
+ *
+ *   merges, n_merges, n_vocab   as for bpe_build (host memory).
+ *   monotone                    receives 1 or 0.
+ * Host-only: needs no GPU and no handle. BPE_ERR_BAD_TABLE for an id outside
+ * [0, n_vocab).
+ */
+int bpe_merges_monotone(const int32_t* merges, int64_t n_merges, int64_t n_vocab, int* monotone);
+
+/* bpe_merges_monotone of the table a handle was built from. */
+int bpe_table_monotone(const bpe_handle* h, int* monotone);
 
 /* Frees the handle's device memory. Waits for its device first. */
 int bpe_destroy(bpe_handle* h);

@@ -110,3 +110,22 @@ def test_workload_tables_pass_host_checks(bpe):
         m, vb, vo = workloads.table(cfg)
         rc = _build_code(bpe, m, vb, vo)
         assert rc in (0, 3)  # OK on a GPU machine, CUDA error without a device
+
+
+def test_merges_monotone_host_only(bpe):
+    # "Tokenisierung", section "Byte Pair Encoding schrittweise": a trainer
+    # merges pairs of the symbols that exist, so its tables are monotone.
+    m, vb, vo = table_from_pairs([(b"a", b"b"), (b"ab", b"a")])
+    assert bpe.bpe_merges_monotone(m, len(vo) - 1)
+    # the abab example: (ab, a) at rank 0 uses "ab", which rank 1 makes
+    m, vb, vo = table_from_pairs([(b"ab", b"a"), (b"a", b"b")], ids=[257, 256])
+    assert not bpe.bpe_merges_monotone(m, len(vo) - 1)
+    assert bpe.bpe_merges_monotone(np.zeros((0, 3), np.int32), 256)
+    merges, _, vo5 = workloads.table(5)
+    assert bpe.bpe_merges_monotone(merges, len(vo5) - 1)
+    # a token made by two rules counts from its lowest rank
+    m, vb, vo = table_from_pairs([(b"a", b"b"), (b"b", b"c"), (b"ab", b"c"), (b"a", b"bc"), (b"abc", b"a")],
+                                 ids=[256, 257, 258, 258, 259])
+    assert bpe.bpe_merges_monotone(m, len(vo) - 1)
+    with pytest.raises(bpe.BpeError):
+        bpe.bpe_merges_monotone(np.array([[1, 2, 999]], np.int32), 300)
