@@ -11,12 +11,12 @@
 // Pair Encoding schrittweise"). What follows is GPU organisation only:
 //
 //   * Tiles (k_tiles). Tile t owns the pre-tokens that start in input bytes
-//     [992 t, 992 t + 992). Its warp loads bytes [992 t - 16, 992 t + 1040)
-//     into shared memory (16 bytes of context on each side of the 1024 bytes
-//     it splits); lane l computes the start bits of bytes [32 l, 32 l + 32)
-//     of the tile, so lane 31 covers a 32-byte margin where the tile's last
-//     pre-token normally ends. The input is read once; the next tile's window
-//     is in flight while the warp works on the current one.
+//     [2016 t, 2016 t + 2016). Its warp loads bytes [2016 t - 16, 2016 t +
+//     2064) into shared memory (16 bytes of context on each side of the 2048
+//     bytes it splits); lane l computes the start bits of bytes [32 l, 32 l +
+//     32) and [1024 + 32 l, 1024 + 32 l + 32) of the tile, so lane 31's second
+//     word covers a 32-byte margin where the tile's last pre-token normally
+//     ends. The input is read once.
 //   * Per pre-token, one lane: a word-cache probe for 2 to 16 bytes (a single
 //     byte is its own token). The ids go to the tile's stage slot at reserved
 //     positions: a hit reserves its id count, a miss its byte length (ids
@@ -34,10 +34,10 @@
 
 namespace {
 
-constexpr int kTileLanes = 31;                     // lanes whose bytes a tile owns
-constexpr int kTileOwn = 32 * kTileLanes;          // 992 bytes whose pre-tokens a tile owns
-constexpr int kTileBits = 32 * 32;                 // bytes whose start bits a tile computes
-using TileWin = WindowSmem<kTileBits, 0, true>;    // window: 16 + 1024 + 16 bytes
+constexpr int kTileWords = 64;                     // 32-byte start-bit words a tile computes (two per lane)
+constexpr int kTileOwn = 32 * (kTileWords - 1);    // 2016 bytes whose pre-tokens a tile owns
+constexpr int kTileBits = 32 * kTileWords;         // 2048 bytes whose start bits a tile computes
+using TileWin = WindowSmem<kTileBits, 0, true>;    // window: 16 + 2048 + 16 bytes
 static_assert(TileWin::kLen == kHalo + kTileBits + kHalo, "tile window");
 constexpr int kTileWarps = 8;                      // warps (tiles in flight) per CTA
 constexpr int kTileThreads = 32 * kTileWarps;
@@ -82,17 +82,15 @@ struct TileRec {
   uint32_t flags;
 };
 
-// A cache miss handed to k_misses: tile << 29 | reserved position << 18 |
-// document start << 17 | length << 10 | start.
-__device__ __forceinline__ uint64_t miss_entry(int64_t t, uint32_t rec) {
-  return (uint64_t)t << 29 | (uint64_t)((rec >> 17) & 0x7FFu) << 18 | (uint64_t)((rec >> 28) & 1u) << 17 |
-         (uint64_t)(rec & 0x1FFFFu);
-}
+// A tile's held miss record (u32): start | length << 11 | reserved position
+// << 18 | document start << 29. Handed to k_misses as tile << 30 | the record.
+constexpr int kMissLenShift = 11, kMissAtShift = 18, kMissDocShift = 29;
+__device__ __forceinline__ uint64_t miss_entry(int64_t t, uint32_t rec) { return (uint64_t)t << 30 | rec; }
 
 struct __align__(16) TileSmem {
-  TileWin w[2];                   // the current tile's window and the next one's
+  TileWin w;                      // the tile's window
   uint16_t span[kTileOwn + 8];    // pre-token starts
-  uint32_t miss[kMissCap];        // start | length << 10 | reserved position << 17 | document start << 28
+  uint32_t miss[kMissCap];        // held miss records
 };
 constexpr size_t kTileSmemBytes = kTileWarps * sizeof(TileSmem);
 static_assert(kTileCtasPerSm * (kTileSmemBytes + 1024) <= 228 * 1024, "the tile CTAs fit in an SM's shared memory");
@@ -120,6 +118,20 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return (1u << (threadIdx.x & 31)) - 1u;
 }
 
+// Inclusive warp scan: each step adds the value d lanes below, using the
+// valid-source predicate of shfl.sync.up instead of a lane comparison.
+__device__ __forceinline__ uint32_t warp_scan_incl(uint32_t v) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    asm("{\n\t.reg .pred p;\n\t.reg .u32 r;\n\t"
+        "shfl.sync.up.b32 r|p, %0, %1, 0, 0xffffffff;\n\t"
+        "@p add.u32 %0, %0, r;\n\t}"
+        : "+r"(v)
+        : "r"(d));
+  }
+  return v;
+}
+
 // --------------------------------------------------------- window and docs --
 
 // Bytes [t0 - kHalo, t0 + kTileBits + kHalo) into W.win (zero outside the
@@ -129,6 +141,14 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 __device__ void tile_load_bytes(TileWin& W, const uint8_t* bytes, int64_t n_bytes, int64_t t0, bool aligned) {
   const int lane = threadIdx.x & 31;
   const int64_t w0 = t0 - kHalo;
+  if (aligned && w0 >= 0 && w0 + TileWin::kLen <= n_bytes) {  // the whole window exists (every tile but the edges)
+    static_assert(TileWin::kLen == 130 * 16, "four copies per lane and two more");
+    const uint8_t* g = bytes + w0 + 16 * lane;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) cp_async16(W.win + 512 * c + 16 * lane, g + 512 * c);
+    if (lane < 2) cp_async16(W.win + 2048 + 16 * lane, g + 2048);
+    return;
+  }
   for (int c = lane; c < TileWin::kLen / 16; c += 32) {
     const int64_t g = w0 + 16 * c;
     if (aligned && g >= 0 && g + 16 <= n_bytes) {
@@ -154,11 +174,12 @@ __device__ TileDocs tile_load_docs(TileWin& W, const int64_t* doc_offsets, int64
                                    int64_t d_first, int64_t d_last) {
   const int lane = threadIdx.x & 31;
   const int64_t w0 = t0 - kHalo, w_end = w0 + TileWin::kLen;
+  const bool inside = w0 >= d_first && w0 + 32 * (TileWin::kWords + 2) <= d_last;  // no byte outside the documents
   for (int i = lane; i < TileWin::kWords + 2; i += 32) {
     W.docbits[i] = 0;
     uint32_t word = 0;
     const int64_t p = w0 + 32 * i;
-    if (p < d_first || p + 32 > d_last) {
+    if (!inside && (p < d_first || p + 32 > d_last)) {
       for (int k = 0; k < 32; ++k)
         if (p + k < d_first || p + k >= d_last) word |= 1u << k;
     }
@@ -277,9 +298,17 @@ __device__ __forceinline__ bool ascii_split32(const SS& W, int p0, uint32_t* out
   const uint32_t B3 = ~S & ~pSP & (pS | (L ^ pL) | (N ^ pN));
   uint32_t base = B2 | B3 | D;
   if (apos & 0x80808080u) {
-    // contractions, one apostrophe at a time (positions relative to p0)
-    for (int j = -3; j < 32; ++j) {
-      if (W.win[p0 + j] != 0x27u) continue;
+    // contractions, one apostrophe at a time: bit k of A is byte p0 - 3 + k
+    uint32_t fa[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) fa[m] = ~((w[m] ^ 0x27272727u) + 0x7F7F7F7Fu) & 0x80808080u;
+    const uint32_t own = gather32(gather8(fa[0], fa[1]), gather8(fa[2], fa[3]), gather8(fa[4], fa[5]),
+                                  gather8(fa[6], fa[7]));
+    const uint32_t before = movemask4(~((wp ^ 0x27272727u) + 0x7F7F7F7Fu) & 0x80808080u) >> 1;  // bytes p0-3..p0-1
+    uint64_t A = ((uint64_t)own << 3) | before;
+    while (A) {
+      const int j = __ffsll((long long)A) - 1 - 3;
+      A &= A - 1;
       const int q = p0 + j;
       const bool at_start = bit_at(W.docbits, q);
       const uint32_t c = W.win[q - 1];
@@ -363,57 +392,60 @@ __device__ void tile_hand_misses(const TileSmem& S, int n_miss, int64_t t, const
 
 // ---------------------------------------------------------------- kernel --
 
-// Persistent: each warp takes tiles from a counter, prefetching the next
-// tile's window while it encodes the current one.
+// Persistent: each warp takes tiles from a counter.
 __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm) k_tiles(TileArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   TileSmem& S = reinterpret_cast<TileSmem*>(smem_raw)[threadIdx.x >> 5];
+  TileWin& W = S.w;
   const int lane = threadIdx.x & 31;
   const bool aligned = (reinterpret_cast<uintptr_t>(a.bytes) & 15u) == 0;
   int64_t d_first = __ldg(a.doc_offsets), d_last = __ldg(a.doc_offsets + a.n_docs);
   d_first = d_first < 0 ? 0 : (d_first > a.n_bytes ? a.n_bytes : d_first);
   d_last = d_last < d_first ? d_first : (d_last > a.n_bytes ? a.n_bytes : d_last);
-  auto take = [&]() -> int64_t {
+  for (;;) {
     unsigned long long tu = 0;
     if (lane == 0) tu = atomicAdd(&a.small->tile_ctr, 1ull);
-    return (int64_t)__shfl_sync(0xFFFFFFFFu, tu, 0);
-  };
-  int64_t t = take();
-  if (t < a.n_tiles) tile_load_bytes(S.w[0], a.bytes, a.n_bytes, t * (int64_t)kTileOwn, aligned);
-  for (int buf = 0; t < a.n_tiles; buf ^= 1) {
-    TileWin& W = S.w[buf];
+    const int64_t t = (int64_t)__shfl_sync(0xFFFFFFFFu, tu, 0);
+    if (t >= a.n_tiles) break;
     const int64_t t0 = t * (int64_t)kTileOwn;
-    const int64_t kA = __ldg(a.first_doc + t);
-    const int64_t t_next = take();
-    const TileDocs D = tile_load_docs(W, a.doc_offsets, a.n_docs, t0, kA, d_first, d_last);
+    tile_load_bytes(W, a.bytes, a.n_bytes, t0, aligned);
+    const TileDocs D = tile_load_docs(W, a.doc_offsets, a.n_docs, t0, __ldg(a.first_doc + t), d_first, d_last);
     cp_async_wait_all();
     __syncwarp();
-    // the next window's copies overlap this tile's work
-    if (t_next < a.n_tiles) tile_load_bytes(S.w[buf ^ 1], a.bytes, a.n_bytes, t_next * (int64_t)kTileOwn, aligned);
 
-    // Split: lane l's 32 start bits; the end of the last document ends the
-    // pre-token before it.
-    const int p0 = kHalo + 32 * lane;
-    const uint32_t dw = bits32_at(W.docbits, p0), ow = bits32_at(W.outbits, p0);
-    uint32_t m;
-    if (!ascii_split32(W, p0, &m)) m = start_mask32(W, p0);
-    m |= dw & ow;
-    const bool own = lane < kTileLanes;
-    const uint32_t cnt = own ? (uint32_t)__popc(m) : 0u;
-    const uint32_t incl = warp_incl_scan(cnt);
-    const uint32_t n_spans = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    if (own) {
-      uint32_t b = m, o = incl - cnt;
+    // Split: lane l's two words of 32 start bits (tile bytes 32 l and 1024 +
+    // 32 l); the end of the last document ends the pre-token before it.
+    uint32_t m[2], dw[2], dso[2];
+#pragma unroll
+    for (int hw = 0; hw < 2; ++hw) {
+      const int p0 = kHalo + 1024 * hw + 32 * lane;
+      dw[hw] = bits32_at(W.docbits, p0);
+      dso[hw] = dw[hw] & bits32_at(W.outbits, p0);
+      if (!ascii_split32(W, p0, &m[hw])) m[hw] = start_mask32(W, p0);
+      m[hw] |= dso[hw];
+    }
+    const bool own1 = lane < 31;  // lane 31's second word is the margin
+    const uint32_t c0 = __popc(m[0]), c1 = own1 ? __popc(m[1]) : 0u;
+    const uint32_t incl = warp_scan_incl(c0 | c1 << 16);
+    const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const uint32_t n_spans = (tot & 0xFFFFu) + (tot >> 16);
+#pragma unroll
+    for (int hw = 0; hw < 2; ++hw) {
+      if (hw == 1 && !own1) continue;
+      uint32_t b = m[hw];
+      uint32_t o = hw == 0 ? (incl & 0xFFFFu) - c0 : (tot & 0xFFFFu) + (incl >> 16) - c1;
       while (b) {
         const int k = __ffs(b) - 1;
         b &= b - 1;
-        uint32_t v = (uint32_t)(32 * lane + k);
-        if ((dw >> k) & 1u) v |= kSpanDoc;
-        if (((dw & ow) >> k) & 1u) v |= kSpanSkip;
+        uint32_t v = (uint32_t)(1024 * hw + 32 * lane + k);
+        if ((dw[hw] >> k) & 1u) v |= kSpanDoc;
+        if ((dso[hw] >> k) & 1u) v |= kSpanSkip;
         S.span[o++] = (uint16_t)v;
       }
-    } else {
-      S.span[n_spans] = (uint16_t)(m ? (uint32_t)(32 * kTileLanes + __ffs(m) - 1) : kSpanNone);
+    }
+    if (lane == 31) {
+      S.span[n_spans] = (uint16_t)(m[1] ? (uint32_t)(kTileOwn + __ffs(m[1]) - 1) : kSpanNone);
+      S.span[n_spans + 1] = (uint16_t)kSpanNone;
     }
     __syncwarp();
     if (lane == 0) a.first_start[t] = n_spans ? t0 + (int64_t)(S.span[0] & kSpanPos) : INT64_MAX;
@@ -422,83 +454,75 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm) k_tiles(TileArgs
     uint32_t* stage = a.stage + t * (int64_t)kTileBits;
     uint32_t resv = 0;
     int n_miss = 0;
-    enum : uint32_t { kNoPiece = 0, kSkipPiece = 1, kProbe = 2, kMiss = 3, kLong = 4, kOne = 5 };
+    enum : uint32_t { kNoPiece = 0, kProbe = 2, kMiss = 3, kLong = 4, kOne = 5 };
     for (uint32_t i0 = 0; i0 < n_spans; i0 += 64) {
-      uint32_t info[2];  // start | length << 10 | kind << 21 | document start << 24
+      // Two slots per lane: i = i0 + lane and i0 + 32 + lane. Everything but
+      // the rare cases is computed for every lane without branches (a slot
+      // past the list reads the sentinel and is made no piece).
+      uint32_t s[2], len[2], kind[2], doc[2];
       CacheKey K[2];
       uint4 ea[2], eb[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t i = i0 + 32u * h + lane;
-        info[h] = 0;
-        if (i < n_spans) {
-          const uint32_t e0 = S.span[i], e1 = S.span[i + 1];
-          const uint32_t s = e0 & kSpanPos;
-          uint32_t kind, len = 0;
-          if (e0 & kSpanSkip) {
-            kind = kSkipPiece;
-          } else if (e1 == kSpanNone) {
-            kind = kLong;
-          } else {
-            len = (e1 & kSpanPos) - s;
-            kind = len > (uint32_t)kShortMax
-                       ? kLong
-                       : (len == 1 ? kOne : ((len <= (uint32_t)kCacheMaxLen && a.C.enabled) ? kProbe : kMiss));
-          }
-          info[h] = s | (len << 10) | (kind << 21) | ((e0 & kSpanDoc) ? 1u << 24 : 0u);
-          if (kind == kProbe) {
-            K[h] = tile_key(W, (int)s, (int)len);
-            ldg32(a.C.e + 2 * cache_slot(K[h], len, a.C), ea[h], eb[h]);
-          }
-        }
+        const uint32_t ic = min(i, n_spans);
+        const uint32_t e0 = S.span[ic], e1 = S.span[ic + 1];
+        s[h] = e0 & kSpanPos;
+        len[h] = (e1 & kSpanPos) - s[h];
+        doc[h] = (e0 & kSpanDoc) ? kIdDoc : 0u;
+        const bool valid = i < n_spans && !(e0 & kSpanSkip);
+        const bool lng = e1 == kSpanNone || len[h] > (uint32_t)kShortMax;
+        kind[h] = !valid ? kNoPiece
+                         : (lng ? kLong
+                                : (len[h] == 1 ? kOne
+                                               : ((len[h] <= (uint32_t)kCacheMaxLen && a.C.enabled) ? kProbe : kMiss)));
+        K[h] = tile_key(W, (int)s[h], (int)min(len[h], (uint32_t)kCacheMaxLen));
+        const uint32_t slot = cache_slot(K[h], len[h], a.C);
+        ldg32(a.C.e + 2 * slot, ea[h], eb[h]);  // every lane: no branch (the slot is in range; unused unless probed)
       }
-      uint32_t res[2], cnt2[2], idv[2][kCacheMaxIds];
+      uint32_t cnt[2], idv[2][kCacheMaxIds];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t kind = (info[h] >> 21) & 7u;
-        const uint32_t len = (info[h] >> 10) & 0x7FFu;
-        cnt2[h] = 0;
-        if (kind == kProbe) {
-          cnt2[h] = tile_resolve(a.C, K[h], len, ea[h], eb[h], idv[h]);
-          if (!cnt2[h]) kind = kMiss;
-        } else if (kind == kOne) {  // a single byte is its own token
-          idv[h][0] = (uint32_t)__ldg(a.T.byte_id + W.win[kHalo + (info[h] & 0x3FFu)]);
-          cnt2[h] = 1;
-          kind = kProbe;
+        cnt[h] = 0;
+        if (kind[h] == kProbe) {
+          cnt[h] = tile_resolve(a.C, K[h], len[h], ea[h], eb[h], idv[h]);
+          if (!cnt[h]) kind[h] = kMiss;
+        } else if (kind[h] == kOne) {  // a single byte is its own token
+          idv[h][0] = (uint32_t)__ldg(a.T.byte_id + W.win[kHalo + s[h]]);
+          cnt[h] = 1;
+          kind[h] = kProbe;
         }
-        info[h] = (info[h] & ~(7u << 21)) | (kind << 21);
-        res[h] = kind == kProbe ? cnt2[h] : (kind == kMiss ? len : (kind == kLong ? 1u : 0u));
       }
-      const uint32_t inc0 = warp_incl_scan(res[0]), inc1 = warp_incl_scan(res[1]);
-      const uint32_t tot0 = __shfl_sync(0xFFFFFFFFu, inc0, 31), tot1 = __shfl_sync(0xFFFFFFFFu, inc1, 31);
-      const uint32_t at[2] = {resv + inc0 - res[0], resv + tot0 + inc1 - res[1]};
-      resv += tot0 + tot1;
+      // reserved stage entries: a hit its ids, a miss its bytes, a long
+      // pre-token one placeholder; both slots in one scan (16 bits each)
+      const uint32_t r0 = kind[0] == kProbe ? cnt[0] : (kind[0] == kMiss ? len[0] : (kind[0] == kLong ? 1u : 0u));
+      const uint32_t r1 = kind[1] == kProbe ? cnt[1] : (kind[1] == kMiss ? len[1] : (kind[1] == kLong ? 1u : 0u));
+      const uint32_t incl = warp_scan_incl(r0 | r1 << 16);
+      const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      const uint32_t at[2] = {resv + (incl & 0xFFFFu) - r0, resv + (tot & 0xFFFFu) + (incl >> 16) - r1};
+      resv += (tot & 0xFFFFu) + (tot >> 16);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t kind = (info[h] >> 21) & 7u;
-        const uint32_t doc = (info[h] >> 24) & 1u ? kIdDoc : 0u;
-        if (kind == kProbe) {
-#pragma unroll
-          for (uint32_t q = 0; q < (uint32_t)kCacheMaxIds; ++q)
-            if (q < cnt2[h]) stage[at[h] + q] = idv[h][q] | (q == 0 ? doc : 0u);
-        } else if (kind == kLong) {
-          const uint32_t s = info[h] & 0x3FFu, len = (info[h] >> 10) & 0x7FFu;
+        if (kind[h] == kProbe) {
+          stage[at[h]] = idv[h][0] | doc[h];
+          if (cnt[h] > 1) stage[at[h] + 1] = idv[h][1];
+          if (cnt[h] > 2) stage[at[h] + 2] = idv[h][2];
+        } else if (kind[h] == kLong) {
+          const uint32_t end = (S.span[min(i0 + 32u * h + lane, n_spans) + 1] == kSpanNone) ? 0u : len[h];
           const unsigned long long gi = atomicAdd(&a.small->n_giants, 1ull);
           if ((int64_t)gi < a.giant_cap) {
-            a.giants[gi] = GiantRec{t0 + (int64_t)s, len ? t0 + (int64_t)(s + len) : -1, t, 0u, 0u};
-            stage[at[h]] = kIdSpecial | kIdLong | (uint32_t)gi | doc;
+            a.giants[gi] = GiantRec{t0 + (int64_t)s[h], end ? t0 + (int64_t)(s[h] + end) : -1, t, 0u, 0u};
+            stage[at[h]] = kIdSpecial | kIdLong | (uint32_t)gi | doc[h];
           } else {
             atomicOr(&a.small->status, kStInternal);
             stage[at[h]] = kIdHole;
           }
         }
-        const bool miss = kind == kMiss;
+        const bool miss = kind[h] == kMiss;
         const uint32_t mb = __ballot_sync(0xFFFFFFFFu, miss);
-        if (miss) {
-          const uint32_t len = (info[h] >> 10) & 0x7FFu;
-          S.miss[n_miss + __popc(mb & lanemask_lt())] =
-              (info[h] & 0x3FFu) | (len << 10) | (at[h] << 17) | (doc ? 1u << 28 : 0u);
-        }
+        if (miss)
+          S.miss[n_miss + __popc(mb & lanemask_lt())] = s[h] | (len[h] << kMissLenShift) |
+                                                         (at[h] << kMissAtShift) | (doc[h] ? 1u << kMissDocShift : 0u);
         n_miss += __popc(mb);
       }
       __syncwarp();
@@ -511,7 +535,6 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm) k_tiles(TileArgs
     if (n_miss) tile_hand_misses(S, n_miss, t, a);
     if (lane == 0) a.rec[t] = TileRec{D.k0, D.k1, resv, 0u, 0u, D.dup ? kTileDup : 0u};
     __syncwarp();
-    t = t_next;
   }
 }
 
@@ -598,14 +621,16 @@ __global__ void __launch_bounds__(kMissThreads, kMissBlocksPerSm) k_misses(const
   const uint64_t warps = (uint64_t)gridDim.x * (kMissThreads / 32);
   for (uint64_t q0 = ((uint64_t)blockIdx.x * (kMissThreads / 32) + (threadIdx.x >> 5)) * 32; q0 < n_q; q0 += warps * 32) {
     const uint64_t e = q0 + lane < n_q ? queue[q0 + lane] : 0ull;
-    const uint32_t len = q0 + lane < n_q ? (uint32_t)(e >> 10) & 0x7Fu : 0u;  // 0: no entry
+    const uint32_t len = q0 + lane < n_q ? (uint32_t)(e >> kMissLenShift) & 0x7Fu : 0u;  // 0: no entry
     // where a queue entry's bytes, ids and tile record are
-    auto src_of = [&](uint64_t x) { return bytes + (int64_t)(x >> 29) * kTileOwn + (int64_t)(x & 0x3FFu); };
-    auto out_of = [&](uint64_t x) { return stage + (int64_t)(x >> 29) * kTileBits + ((x >> 18) & 0x7FFu); };
+    auto src_of = [&](uint64_t x) { return bytes + (int64_t)(x >> 30) * kTileOwn + (int64_t)(x & 0x7FFu); };
+    auto out_of = [&](uint64_t x) {
+      return stage + (int64_t)(x >> 30) * kTileBits + ((x >> kMissAtShift) & 0x7FFu);
+    };
     auto finish = [&](uint64_t x, uint32_t n, uint32_t cnt, uint32_t* out) {
       for (uint32_t q = cnt; q < n; ++q) out[q] = kIdHole;
-      if ((x >> 17) & 1u) out[0] |= kIdDoc;
-      if (n > cnt) atomicAdd(&rec[(int64_t)(x >> 29)].holes, n - cnt);
+      if ((x >> kMissDocShift) & 1u) out[0] |= kIdDoc;
+      if (n > cnt) atomicAdd(&rec[(int64_t)(x >> 30)].holes, n - cnt);
     };
     uint32_t m8 = __ballot_sync(0xFFFFFFFFu, len > 8u && len <= (uint32_t)kCacheMaxLen);
     uint32_t m16 = __ballot_sync(0xFFFFFFFFu, len > (uint32_t)kCacheMaxLen && len <= 32u);
@@ -620,7 +645,7 @@ __global__ void __launch_bounds__(kMissThreads, kMissBlocksPerSm) k_misses(const
       const int src = on ? __ffs(mm) - 1 : 0;
       for (int x = 0; x < 32 / G; ++x) *mask &= *mask - 1u;
       const uint64_t ge = __shfl_sync(0xFFFFFFFFu, e, src);
-      const uint32_t n = on ? (uint32_t)(ge >> 10) & 0x7Fu : 0u;
+      const uint32_t n = on ? (uint32_t)(ge >> kMissLenShift) & 0x7Fu : 0u;
       uint32_t* out = out_of(ge);
       const uint32_t cnt = merge(src_of(ge), n, out);
       __syncwarp();
@@ -834,7 +859,8 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_tile_sums(uint64_t* block
 // offsets in shared memory, maps r to its documents. The documents at the
 // end of the last one get the tile's end.
 constexpr int kCompactWarps = 8;
-constexpr int kCompactChunks = 8;  // stage chunks of 32 entries a lane loads before it processes any
+constexpr int kCompactChunks = 16;  // stage chunks of 32 entries a lane loads before it processes any
+
 __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* rec, const uint32_t* stage,
                                                                 const uint64_t* tile_base, const uint64_t* block_sum,
                                                                 const GiantRec* giants, const int32_t* pool,
@@ -845,16 +871,25 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* r
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t warps = (int64_t)gridDim.x * kCompactWarps;
   bool over = false;
-  for (int64_t t = (int64_t)blockIdx.x * kCompactWarps + warp; t < n_tiles; t += warps) {
-    // Every load of the tile is issued before any result is used: the record,
-    // the offset and the first kCompactChunks chunks of the stage slot (a slot
-    // is always kTileBits entries, so the loads stay inside it).
+  int64_t t = (int64_t)blockIdx.x * kCompactWarps + warp;
+  // the record and offset of the warp's next tile are loaded a tile ahead
+  TileRec Rn{};
+  uint64_t base_n = 0;
+  if (t < n_tiles) {
+    Rn = rec[t];
+    base_n = tile_base[t] + block_sum[t / kScanThreads];
+  }
+  for (; t < n_tiles; t += warps) {
+    const TileRec R = Rn;
+    const uint64_t base = base_n;
     const uint32_t* src = stage + t * (int64_t)kTileBits;
     uint32_t v[kCompactChunks];
 #pragma unroll
-    for (int c = 0; c < kCompactChunks; ++c) v[c] = __ldcs(src + 32 * c + lane);
-    const TileRec R = rec[t];
-    const uint64_t base = tile_base[t] + block_sum[t / kScanThreads];
+    for (int c = 0; c < kCompactChunks; ++c) v[c] = 32u * c + lane < R.resv ? __ldcs(src + 32 * c + lane) : kIdHole;
+    if (t + warps < n_tiles) {
+      Rn = rec[t + warps];
+      base_n = tile_base[t + warps] + block_sum[(t + warps) / kScanThreads];
+    }
     const bool dup = (R.flags & kTileDup) != 0;
     if (dup) {
       // docq[r] = the last document at the r-th distinct start in the tile
@@ -871,35 +906,44 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* r
       }
       __syncwarp();
     }
-    uint64_t shift = 0;  // ids placed so far
+    uint64_t at0 = base;  // where the chunk's first id goes
     uint32_t nmark = 0;
-    auto chunk = [&](uint32_t q0, uint32_t x) {
-      const bool in = q0 + lane < R.resv;
-      const uint32_t e = in ? x : kIdHole;
+    // Documents whose first id is at output position `at` (mark rank r).
+    auto mark_docs = [&](uint32_t r, uint64_t at) {
+      if (!dup) {
+        const int64_t k = R.k0 + r;
+        if (k < R.k1) out_offsets[k] = (int64_t)at;
+        else atomicOr(&small->status, kStInternal);
+      } else {
+        const int64_t k_hi = R.k0 + (r < (uint32_t)(kTileOwn + 2) ? docq[warp][r] : 0);
+        const int64_t k_lo = r == 0 ? R.k0 : R.k0 + docq[warp][r - 1] + 1;
+        for (int64_t k = k_lo; k <= k_hi; ++k) out_offsets[k] = (int64_t)at;
+      }
+    };
+    auto chunk = [&](uint32_t e) {
+      const bool plain = (e & kIdSpecial) == 0;  // an id (no hole, no placeholder)
+      const uint32_t pb = __ballot_sync(0xFFFFFFFFu, plain);
+      const bool mark = (e & kIdDoc) != 0;
+      const uint32_t mb = __ballot_sync(0xFFFFFFFFu, mark);
+      if (pb == 0xFFFFFFFFu) {  // 32 ids in a row: no scan
+        const uint64_t at = at0 + lane;
+        if ((int64_t)at < capacity) out_ids[at] = (int32_t)(e & ~kIdDoc);
+        else over = true;
+        if (mark) mark_docs(nmark + __popc(mb & lanemask_lt()), at);
+        nmark += __popc(mb);
+        at0 += 32;
+        return;
+      }
       const bool valid = (e & (kIdSpecial | kIdLong)) != kIdSpecial;
-      const bool ph = valid && (e & kIdSpecial);
-      const uint32_t g_cnt = ph ? giants[e & kIdIndex].count : 1u;
-      const uint32_t n_ids = valid ? g_cnt : 0u;
-      const uint32_t incl = warp_incl_scan(n_ids);
-      const uint64_t at = base + shift + (incl - n_ids);
-      if (valid && !ph) {
+      const bool ph = valid && !plain;
+      const uint32_t n_ids = !valid ? 0u : (ph ? giants[e & kIdIndex].count : 1u);
+      const uint32_t incl = warp_scan_incl(n_ids);
+      const uint64_t at = at0 + (incl - n_ids);
+      if (plain) {
         if ((int64_t)at < capacity) out_ids[at] = (int32_t)(e & ~kIdDoc);
         else over = true;
       }
-      const bool mark = valid && (e & kIdDoc);
-      const uint32_t mb = __ballot_sync(0xFFFFFFFFu, mark);
-      if (mark) {
-        const uint32_t r = nmark + __popc(mb & lanemask_lt());
-        if (!dup) {
-          const int64_t k = R.k0 + r;
-          if (k < R.k1) out_offsets[k] = (int64_t)at;
-          else atomicOr(&small->status, kStInternal);
-        } else {
-          const int64_t k_hi = R.k0 + (r < (uint32_t)(kTileOwn + 2) ? docq[warp][r] : 0);
-          const int64_t k_lo = r == 0 ? R.k0 : R.k0 + docq[warp][r - 1] + 1;
-          for (int64_t k = k_lo; k <= k_hi; ++k) out_offsets[k] = (int64_t)at;
-        }
-      }
+      if (mark) mark_docs(nmark + __popc(mb & lanemask_lt()), at);
       uint32_t phm = __ballot_sync(0xFFFFFFFFu, ph);
       while (phm) {
         const int src_lane = __ffs(phm) - 1;
@@ -913,15 +957,17 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* r
         }
       }
       nmark += __popc(mb);
-      shift += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      at0 += __shfl_sync(0xFFFFFFFFu, incl, 31);
     };
+    // a chunk past the used entries holds only holes and changes nothing
 #pragma unroll
     for (int c = 0; c < kCompactChunks; ++c)
-      if (32u * c < R.resv) chunk(32u * c, v[c]);
-    for (uint32_t q0 = 32u * kCompactChunks; q0 < R.resv; q0 += 32) chunk(q0, __ldcs(src + q0 + lane));
+      if (32u * c < R.resv) chunk(v[c]);
+    for (uint32_t q0 = 32u * kCompactChunks; q0 < R.resv; q0 += 32)
+      chunk(q0 + lane < R.resv ? __ldcs(src + q0 + lane) : kIdHole);
     // documents with no mark: at the end of the last document
     const int64_t k_rest = !dup ? R.k0 + nmark : (nmark == 0 ? R.k0 : R.k0 + docq[warp][nmark - 1] + 1);
-    for (int64_t k = k_rest + lane; k < R.k1; k += 32) out_offsets[k] = (int64_t)(base + shift);
+    for (int64_t k = k_rest + lane; k < R.k1; k += 32) out_offsets[k] = (int64_t)at0;
     __syncwarp();
   }
   if (over) atomicOr(&small->status, kStCapacity);
@@ -959,14 +1005,20 @@ __global__ void __launch_bounds__(32 * kSplitWarps) k_split_tiles(const uint8_t*
   tile_load_docs(W, doc_offsets, n_docs, t0, kA, d_first, d_last);
   cp_async_wait_all();
   __syncwarp();
-  uint32_t m;
-  if (!ascii_split32(W, kHalo + 32 * lane, &m)) m = start_mask32(W, kHalo + 32 * lane);
-  const int64_t gw = t0 / 32 + lane, n_words = (n_bytes + 31) / 32;
-  if (lane < kTileLanes && gw < n_words) {
-    uint32_t v = m;
-    const int64_t first_bit = gw * 32;
-    if (first_bit + 32 > n_bytes) v &= (1u << (n_bytes - first_bit)) - 1u;
-    out_bits[gw] = v;
+  const int64_t n_words = (n_bytes + 31) / 32;
+#pragma unroll
+  for (int hw = 0; hw < 2; ++hw) {
+    const int word = 32 * hw + lane;
+    if (word >= kTileWords - 1) continue;  // the margin: the next tile's own bytes
+    const int p0 = kHalo + 32 * word;
+    uint32_t m;
+    if (!ascii_split32(W, p0, &m)) m = start_mask32(W, p0);
+    const int64_t gw = t0 / 32 + word;
+    if (gw < n_words) {
+      const int64_t first_bit = gw * 32;
+      if (first_bit + 32 > n_bytes) m &= (1u << (n_bytes - first_bit)) - 1u;
+      out_bits[gw] = m;
+    }
   }
 }
 
