@@ -1143,30 +1143,36 @@ int status_code(uint32_t s) {
   return BPE_OK;
 }
 
-// Word cache: the ids of every vocabulary string of 1..16 bytes, of every
+// Word cache: the ids of every vocabulary string of 2..16 bytes, of every
 // vocabulary string that starts with a space with that space removed (the
 // same word at the start of a line or document), and of every prefix of
 // those (a word cut off by the end of a document), computed on the device by
-// the merge loop, laid out as an open-addressed table (load at most 1/8,
-// linear probing).
+// the merge loop, laid out as an open-addressed table (load at most 1/16,
+// linear probing, keys of lower ids inserted first).
 int build_word_cache(bpe_handle* h, const uint8_t* vocab_bytes, const int64_t* vocab_offsets, int64_t n_vocab) {
   std::vector<uint8_t> strs;
   std::vector<int64_t> offs{0};
+  std::vector<uint64_t> prio;  // insertion order: a lower id (an earlier merge, a more frequent pair) first
   std::unordered_set<std::string> keys;
-  auto add = [&](const uint8_t* b, int64_t L) {
-    if (L < 1 || L > kCacheMaxLen || !keys.insert(std::string((const char*)b, (size_t)L)).second) return;
+  // Single bytes are left out: a one-byte pre-token is its own token.
+  auto add = [&](const uint8_t* b, int64_t L, uint64_t p) {
+    if (L < 2 || L > kCacheMaxLen || !keys.insert(std::string((const char*)b, (size_t)L)).second) return;
     strs.insert(strs.end(), b, b + L);
     offs.push_back((int64_t)strs.size());
+    prio.push_back(p);
   };
-  for (int64_t id = 0; id < n_vocab; ++id) add(vocab_bytes + vocab_offsets[id], vocab_offsets[id + 1] - vocab_offsets[id]);
+  for (int64_t id = 0; id < n_vocab; ++id)
+    add(vocab_bytes + vocab_offsets[id], vocab_offsets[id + 1] - vocab_offsets[id], (uint64_t)id << 2);
   for (int64_t id = 0; id < n_vocab; ++id) {
     const int64_t L = vocab_offsets[id + 1] - vocab_offsets[id];
-    if (L >= 2 && vocab_bytes[vocab_offsets[id]] == ' ') add(vocab_bytes + vocab_offsets[id] + 1, L - 1);
+    if (L >= 2 && vocab_bytes[vocab_offsets[id]] == ' ')
+      add(vocab_bytes + vocab_offsets[id] + 1, L - 1, (uint64_t)id << 2 | 1u);
   }
   // Prefixes of all of the above (a word cut off by the end of a document).
   for (int64_t i = 0, n0 = (int64_t)offs.size() - 1; i < n0; ++i) {
     const std::string w(strs.begin() + offs[i], strs.begin() + offs[i + 1]);  // copy: add() grows strs
-    for (size_t L = 1; L < w.size(); ++L) add(reinterpret_cast<const uint8_t*>(w.data()), (int64_t)L);
+    const uint64_t p = (prio[(size_t)i] & ~3ull) | 2u;
+    for (size_t L = 2; L < w.size(); ++L) add(reinterpret_cast<const uint8_t*>(w.data()), (int64_t)L, p);
   }
   const int64_t n = (int64_t)offs.size() - 1;
   uint8_t* d_strs = nullptr;
@@ -1193,12 +1199,16 @@ int build_word_cache(bpe_handle* h, const uint8_t* vocab_bytes, const int64_t* v
   }
   int64_t keep = 0;
   for (int64_t i = 0; i < n; ++i) keep += (vals[4 * i] >= 1 && vals[4 * i] <= (uint32_t)kCacheMaxIds);
-  // load factor at most 1/8: a probe that meets another key at the home slot
-  // costs the whole warp a second round trip
+  // Load at most 1/16, keys inserted by priority: a probe that meets another
+  // key at the home slot costs its whole warp a second round trip, so the
+  // keys of frequent pre-tokens should own their home slots.
   uint64_t slots = 16;
-  while (slots < (uint64_t)keep * 8) slots <<= 1;
+  while (slots < (uint64_t)keep * 16) slots <<= 1;
+  std::vector<int64_t> order((size_t)n);
+  for (int64_t i = 0; i < n; ++i) order[(size_t)i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int64_t x, int64_t y) { return prio[(size_t)x] < prio[(size_t)y]; });
   std::vector<uint4> table(slots * 2, make_uint4(0, 0, 0, 0));
-  for (int64_t i = 0; i < n; ++i) {
+  for (const int64_t i : order) {
     const uint32_t cnt = vals[4 * i];
     if (cnt < 1 || cnt > (uint32_t)kCacheMaxIds) continue;
     const uint32_t len = (uint32_t)(offs[i + 1] - offs[i]);

@@ -348,33 +348,31 @@ __device__ __forceinline__ CacheKey tile_key(const TileWin& W, int s, int len) {
 // Count of ids (1..3) for key K of len bytes given the entry {ea, eb} at its
 // home slot, 0 when the key is absent; the ids go to ids[0..2]. The home slot
 // settles almost every probe (the table is at most 1/8 full); the rest of the
-// probe chain is kept out of line.
-__device__ __noinline__ uint32_t cache_probe_chain(const Cache& C, const CacheKey& K, uint32_t len, uint32_t* ids) {
-  uint32_t slot = cache_slot(K, len, C);
-  for (uint32_t probe = 0; probe < C.mask; ++probe) {
-    slot = (slot + 1) & C.mask;
+// probe chain is kept out of line, and takes and returns values only, so the
+// caller's registers never need a memory address.
+__device__ __noinline__ uint4 cache_probe_chain(const uint4* e, uint32_t mask, uint32_t x0, uint32_t x1, uint32_t x2,
+                                                uint32_t x3, uint32_t len) {
+  uint32_t slot = cache_hash(x0, x1, x2, x3, len) & mask;
+  for (uint32_t probe = 0; probe < mask; ++probe) {
+    slot = (slot + 1) & mask;
     uint4 ea, eb;
-    ldg32(C.e + 2 * slot, ea, eb);
-    if (eb.x == 0) return 0;
-    if ((eb.x & 31u) == len && ea.x == K.x0 && ea.y == K.x1 && ea.z == K.x2 && ea.w == K.x3) {
-      ids[0] = eb.y;
-      ids[1] = eb.z;
-      ids[2] = eb.w;
-      return (eb.x >> 5) & 7u;
-    }
+    ldg32(e + 2 * slot, ea, eb);
+    if (eb.x == 0) break;
+    if ((eb.x & 31u) == len && ea.x == x0 && ea.y == x1 && ea.z == x2 && ea.w == x3)
+      return make_uint4((eb.x >> 5) & 7u, eb.y, eb.z, eb.w);
   }
-  return 0;
+  return make_uint4(0u, 0u, 0u, 0u);
 }
 
 __device__ __forceinline__ uint32_t tile_resolve(const Cache& C, const CacheKey& K, uint32_t len, const uint4& ea,
                                                  const uint4& eb, uint32_t* ids) {
   const bool same = (eb.x & 31u) == len && ((ea.x ^ K.x0) | (ea.y ^ K.x1) | (ea.z ^ K.x2) | (ea.w ^ K.x3)) == 0;
-  ids[0] = eb.y;
-  ids[1] = eb.z;
-  ids[2] = eb.w;
-  if (same) return (eb.x >> 5) & 7u;
-  if (eb.x == 0) return 0;
-  return cache_probe_chain(C, K, len, ids);
+  uint4 r = make_uint4(same ? (eb.x >> 5) & 7u : 0u, eb.y, eb.z, eb.w);
+  if (!same && eb.x != 0) r = cache_probe_chain(C.e, C.mask, K.x0, K.x1, K.x2, K.x3, len);
+  ids[0] = r.y;
+  ids[1] = r.z;
+  ids[2] = r.w;
+  return r.x;
 }
 
 // The held miss records of tile t into the GPU-wide queue (one atomic per
