@@ -92,7 +92,7 @@ struct __align__(16) TileSmem {
   uint16_t span[kTileOwn + 8];    // pre-token starts
   uint32_t miss[kMissCap];        // held miss records
 };
-constexpr size_t kTileSmemBytes = kTileWarps * sizeof(TileSmem);
+constexpr size_t kTileSmemBytes = 1024 + kTileWarps * sizeof(TileSmem);  // the CTA's byte map, then the warps
 static_assert(kTileCtasPerSm * (kTileSmemBytes + 1024) <= 228 * 1024, "the tile CTAs fit in an SM's shared memory");
 
 struct TileArgs {
@@ -345,11 +345,11 @@ __device__ __forceinline__ CacheKey tile_key(const TileWin& W, int s, int len) {
   return K;
 }
 
-// Count of ids (1..3) for key K of len bytes given the entry {ea, eb} at its
-// home slot, 0 when the key is absent; the ids go to ids[0..2]. The home slot
-// settles almost every probe (the table is at most 1/8 full); the rest of the
-// probe chain is kept out of line, and takes and returns values only, so the
-// caller's registers never need a memory address.
+// The rest of a word-cache probe chain past the home slot: {count, id0, id1,
+// id2} of key (x0..x3, len), count 0 when absent. The home slot settles
+// almost every probe (the table is at most 1/16 full), so this is kept out of
+// line, and takes and returns values only, so the caller's registers never
+// need a memory address.
 __device__ __noinline__ uint4 cache_probe_chain(const uint4* e, uint32_t mask, uint32_t x0, uint32_t x1, uint32_t x2,
                                                 uint32_t x3, uint32_t len) {
   uint32_t slot = cache_hash(x0, x1, x2, x3, len) & mask;
@@ -362,17 +362,6 @@ __device__ __noinline__ uint4 cache_probe_chain(const uint4* e, uint32_t mask, u
       return make_uint4((eb.x >> 5) & 7u, eb.y, eb.z, eb.w);
   }
   return make_uint4(0u, 0u, 0u, 0u);
-}
-
-__device__ __forceinline__ uint32_t tile_resolve(const Cache& C, const CacheKey& K, uint32_t len, const uint4& ea,
-                                                 const uint4& eb, uint32_t* ids) {
-  const bool same = (eb.x & 31u) == len && ((ea.x ^ K.x0) | (ea.y ^ K.x1) | (ea.z ^ K.x2) | (ea.w ^ K.x3)) == 0;
-  uint4 r = make_uint4(same ? (eb.x >> 5) & 7u : 0u, eb.y, eb.z, eb.w);
-  if (!same && eb.x != 0) r = cache_probe_chain(C.e, C.mask, K.x0, K.x1, K.x2, K.x3, len);
-  ids[0] = r.y;
-  ids[1] = r.z;
-  ids[2] = r.w;
-  return r.x;
 }
 
 // The held miss records of tile t into the GPU-wide queue (one atomic per
@@ -393,8 +382,11 @@ __device__ void tile_hand_misses(const TileSmem& S, int n_miss, int64_t t, const
 // Persistent: each warp takes tiles from a counter.
 __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm) k_tiles(TileArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  TileSmem& S = reinterpret_cast<TileSmem*>(smem_raw)[threadIdx.x >> 5];
+  int32_t* byte_id = reinterpret_cast<int32_t*>(smem_raw);
+  TileSmem& S = reinterpret_cast<TileSmem*>(smem_raw + 1024)[threadIdx.x >> 5];
   TileWin& W = S.w;
+  for (int i = threadIdx.x; i < 256; i += kTileThreads) byte_id[i] = a.T.byte_id[i];
+  __syncthreads();
   const int lane = threadIdx.x & 31;
   const bool aligned = (reinterpret_cast<uintptr_t>(a.bytes) & 15u) == 0;
   int64_t d_first = __ldg(a.doc_offsets), d_last = __ldg(a.doc_offsets + a.n_docs);
@@ -481,15 +473,25 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm) k_tiles(TileArgs
       uint32_t cnt[2], idv[2][kCacheMaxIds];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        cnt[h] = 0;
-        if (kind[h] == kProbe) {
-          cnt[h] = tile_resolve(a.C, K[h], len[h], ea[h], eb[h], idv[h]);
-          if (!cnt[h]) kind[h] = kMiss;
-        } else if (kind[h] == kOne) {  // a single byte is its own token
-          idv[h][0] = (uint32_t)__ldg(a.T.byte_id + W.win[kHalo + s[h]]);
-          cnt[h] = 1;
-          kind[h] = kProbe;
+        // a probe's answer from its home slot, a single byte's id from the
+        // byte map; the rest of a probe chain only when the home slot holds
+        // another key
+        const bool same = (eb[h].x & 31u) == len[h] &&
+                          ((ea[h].x ^ K[h].x0) | (ea[h].y ^ K[h].x1) | (ea[h].z ^ K[h].x2) | (ea[h].w ^ K[h].x3)) == 0;
+        const bool one = kind[h] == kOne;
+        cnt[h] = one ? 1u : (same ? (eb[h].x >> 5) & 7u : 0u);
+        idv[h][0] = one ? (uint32_t)byte_id[W.win[kHalo + s[h]]] : eb[h].y;
+        idv[h][1] = eb[h].z;
+        idv[h][2] = eb[h].w;
+        if (kind[h] == kProbe && !same && eb[h].x != 0) {
+          const uint4 r = cache_probe_chain(a.C.e, a.C.mask, K[h].x0, K[h].x1, K[h].x2, K[h].x3, len[h]);
+          cnt[h] = r.x;
+          idv[h][0] = r.y;
+          idv[h][1] = r.z;
+          idv[h][2] = r.w;
         }
+        if (one || (kind[h] == kProbe && cnt[h])) kind[h] = kProbe;
+        else if (kind[h] == kProbe) kind[h] = kMiss;
       }
       // reserved stage entries: a hit its ids, a miss its bytes, a long
       // pre-token one placeholder; both slots in one scan (16 bits each)
