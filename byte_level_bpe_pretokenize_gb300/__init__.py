@@ -59,7 +59,7 @@ _lib = None
 
 EXPORTS = ["bpe_build", "bpe_encode_batch", "bpe_encode_batch_host", "bpe_encode_batch_noalloc", "bpe_pretokenize_batch", "bpe_decode_batch", "bpe_set_word_cache",
            "bpe_set_timing_events", "bpe_sync_status", "bpe_table_info", "bpe_table_monotone", "bpe_merges_monotone",
-           "bpe_destroy", "bpe_last_error"]
+           "bpe_workspace_bytes", "bpe_destroy", "bpe_last_error"]
 
 
 def lib():
@@ -96,6 +96,8 @@ def lib():
             L.bpe_table_monotone.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
             L.bpe_merges_monotone.restype = ctypes.c_int
             L.bpe_merges_monotone.argtypes = [p, i64, i64, ctypes.POINTER(ctypes.c_int)]
+            L.bpe_workspace_bytes.restype = ctypes.c_int
+            L.bpe_workspace_bytes.argtypes = [p, ctypes.POINTER(i64)]
             L.bpe_destroy.restype = ctypes.c_int
             L.bpe_destroy.argtypes = [p]
             L.bpe_last_error.restype = ctypes.c_char_p
@@ -200,6 +202,13 @@ def bpe_merges_monotone(merges, n_vocab: int) -> bool:
     out = ctypes.c_int()
     _check(lib().bpe_merges_monotone(mm.ctypes.data if mm.size else None, len(mm), n_vocab, ctypes.byref(out)))
     return bool(out.value)
+
+
+def bpe_workspace_bytes(handle: int) -> int:
+    """Device workspace the handle holds now (0 until a call needs it)."""
+    b = ctypes.c_int64()
+    _check(lib().bpe_workspace_bytes(handle, ctypes.byref(b)))
+    return b.value
 
 
 def bpe_destroy(handle: int) -> None:

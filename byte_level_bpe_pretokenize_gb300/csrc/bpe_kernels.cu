@@ -1309,10 +1309,9 @@ Ws ws_carve(unsigned char* base, int64_t n_bytes) {
 
 // k_tiles' dynamic shared memory above the 48 KB default, once per device.
 int tiles_smem_setup() {
-  return cudaFuncSetAttribute(k_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTileSmemBytes) ==
-                 cudaSuccess
-             ? BPE_OK
-             : fail(BPE_ERR_CUDA, "cudaFuncSetAttribute(k_tiles) failed");
+  if (cudaFuncSetAttribute(k_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTileSmemBytes) != cudaSuccess)
+    return fail(BPE_ERR_CUDA, "cudaFuncSetAttribute(k_tiles) failed");
+  return BPE_OK;
 }
 
 // The per-call kernels on stream st: k_prep_docs, k_prep_long, k_tiles,
@@ -1558,6 +1557,12 @@ int bpe_table_info(const bpe_handle* h, int64_t* n_merges, int64_t* n_vocab) {
   if (!h) return fail(BPE_ERR_INVALID_ARG, "null handle");
   if (n_merges) *n_merges = h->n_merges;
   if (n_vocab) *n_vocab = h->n_vocab;
+  return BPE_OK;
+}
+
+int bpe_workspace_bytes(const bpe_handle* h, int64_t* bytes) {
+  if (!h || !bytes) return fail(BPE_ERR_INVALID_ARG, "bpe_workspace_bytes: bad arguments");
+  *bytes = (int64_t)h->ws_bytes;
   return BPE_OK;
 }
 

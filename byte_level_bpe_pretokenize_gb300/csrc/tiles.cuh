@@ -850,25 +850,37 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_tile_sums(uint64_t* block
   if (threadIdx.x == 0) small->total = (int64_t)carry;
 }
 
+constexpr int kCompactWarps = 8;
+
+// What k_compact keeps per tile while it walks the stage.
+struct CompactState {
+  uint64_t at0;    // output position of the chunk's first entry
+  uint32_t nmark;  // document marks so far
+};
+
 // A warp per tile: its stage entries to out_ids at the tile's offset without
 // the holes, each placeholder expanded to its deferred pre-token's ids from
-// the pool. The stage is read with streaming loads (it is not read again). A document mark (the first id of a document) gives document
-// offsets: the r-th mark of the tile belongs to the r-th distinct document
-// start in it, which is document k0 + r unless the tile has empty documents;
-// then a table of the last document at each distinct start, built from the
-// offsets in shared memory, maps r to its documents. The documents at the
-// end of the last one get the tile's end.
-constexpr int kCompactWarps = 8;
-constexpr int kCompactChunks = 16;  // stage chunks of 32 entries a lane loads before it processes any
-
+// the pool. The used part of the tile's stage slot is copied to shared memory
+// kCompactPart entries at a time with asynchronous 16-byte copies (all loads
+// of a part in flight at once), then walked in chunks of 32 entries by one
+// short loop. A chunk of 32 plain ids needs no scan; others take positions
+// from a scan of each entry's id count (0 for a hole). A document mark (the
+// first id of a document) gives document offsets: the r-th mark of the tile
+// belongs to the r-th distinct document start in it, which is document k0 + r
+// unless the tile has empty documents; then the marks are taken in order and
+// each gets the run of documents that start at the same byte as the next
+// document not yet placed. The documents at the end of the last one get the
+// tile's end.
+constexpr int kCompactPart = 512;
 __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* rec, const uint32_t* stage,
                                                                 const uint64_t* tile_base, const uint64_t* block_sum,
                                                                 const GiantRec* giants, const int32_t* pool,
                                                                 const int64_t* doc_offsets, int64_t n_tiles,
                                                                 int32_t* out_ids, int64_t capacity,
                                                                 int64_t* out_offsets, DevSmall* small) {
-  __shared__ uint16_t docq[kCompactWarps][kTileOwn + 2];  // per mark rank: its last document - k0 (tiles with empty documents)
+  __shared__ __align__(16) uint32_t ent_all[kCompactWarps][kCompactPart];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t* ent = ent_all[warp];
   const int64_t warps = (int64_t)gridDim.x * kCompactWarps;
   bool over = false;
   int64_t t = (int64_t)blockIdx.x * kCompactWarps + warp;
@@ -881,93 +893,86 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* r
   }
   for (; t < n_tiles; t += warps) {
     const TileRec R = Rn;
-    const uint64_t base = base_n;
     const uint32_t* src = stage + t * (int64_t)kTileBits;
-    uint32_t v[kCompactChunks];
-#pragma unroll
-    for (int c = 0; c < kCompactChunks; ++c) v[c] = 32u * c + lane < R.resv ? __ldcs(src + 32 * c + lane) : kIdHole;
+    const uint32_t first = min(R.resv, (uint32_t)kCompactPart);
+    for (uint32_t c = lane; 4 * c < first; c += 32) cp_async16(ent + 4 * c, src + 4 * c);
+    CompactState st{base_n, 0u};
     if (t + warps < n_tiles) {
       Rn = rec[t + warps];
       base_n = tile_base[t + warps] + block_sum[(t + warps) / kScanThreads];
     }
     const bool dup = (R.flags & kTileDup) != 0;
-    if (dup) {
-      // docq[r] = the last document at the r-th distinct start in the tile
-      uint32_t r = 0;
-      for (int64_t k = R.k0; k < R.k1; k += 32) {
-        const int64_t kk = k + lane;
-        const int64_t o = kk < R.k1 ? doc_offsets[kk] : INT64_MAX;
-        const int64_t o_next = kk + 1 < R.k1 ? doc_offsets[kk + 1] : INT64_MAX;
-        const bool last = kk < R.k1 && o_next != o;
-        const uint32_t lb = __ballot_sync(0xFFFFFFFFu, last);
-        const uint32_t rr = r + __popc(lb & lanemask_lt());
-        if (last && rr < (uint32_t)(kTileOwn + 2)) docq[warp][rr] = (uint16_t)(kk - R.k0);
-        r += __popc(lb);
+    int64_t k_next = R.k0;  // tiles with empty documents: the first document not yet placed
+    for (uint32_t p0 = 0; p0 < R.resv; p0 += kCompactPart) {
+      const uint32_t n_part = min(R.resv - p0, (uint32_t)kCompactPart);
+      if (p0 > 0) {
+        __syncwarp();  // the previous part is read
+        for (uint32_t c = lane; 4 * c < n_part; c += 32) cp_async16(ent + 4 * c, src + p0 + 4 * c);
       }
+      cp_async_wait_all();
       __syncwarp();
-    }
-    uint64_t at0 = base;  // where the chunk's first id goes
-    uint32_t nmark = 0;
-    // Documents whose first id is at output position `at` (mark rank r).
-    auto mark_docs = [&](uint32_t r, uint64_t at) {
-      if (!dup) {
-        const int64_t k = R.k0 + r;
-        if (k < R.k1) out_offsets[k] = (int64_t)at;
-        else atomicOr(&small->status, kStInternal);
-      } else {
-        const int64_t k_hi = R.k0 + (r < (uint32_t)(kTileOwn + 2) ? docq[warp][r] : 0);
-        const int64_t k_lo = r == 0 ? R.k0 : R.k0 + docq[warp][r - 1] + 1;
-        for (int64_t k = k_lo; k <= k_hi; ++k) out_offsets[k] = (int64_t)at;
-      }
-    };
-    auto chunk = [&](uint32_t e) {
-      const bool plain = (e & kIdSpecial) == 0;  // an id (no hole, no placeholder)
-      const uint32_t pb = __ballot_sync(0xFFFFFFFFu, plain);
-      const bool mark = (e & kIdDoc) != 0;
-      const uint32_t mb = __ballot_sync(0xFFFFFFFFu, mark);
-      if (pb == 0xFFFFFFFFu) {  // 32 ids in a row: no scan
-        const uint64_t at = at0 + lane;
-        if ((int64_t)at < capacity) out_ids[at] = (int32_t)(e & ~kIdDoc);
-        else over = true;
-        if (mark) mark_docs(nmark + __popc(mb & lanemask_lt()), at);
-        nmark += __popc(mb);
-        at0 += 32;
-        return;
-      }
-      const bool valid = (e & (kIdSpecial | kIdLong)) != kIdSpecial;
-      const bool ph = valid && !plain;
-      const uint32_t n_ids = !valid ? 0u : (ph ? giants[e & kIdIndex].count : 1u);
-      const uint32_t incl = warp_scan_incl(n_ids);
-      const uint64_t at = at0 + (incl - n_ids);
-      if (plain) {
-        if ((int64_t)at < capacity) out_ids[at] = (int32_t)(e & ~kIdDoc);
-        else over = true;
-      }
-      if (mark) mark_docs(nmark + __popc(mb & lanemask_lt()), at);
-      uint32_t phm = __ballot_sync(0xFFFFFFFFu, ph);
-      while (phm) {
-        const int src_lane = __ffs(phm) - 1;
-        phm &= phm - 1;
-        const uint32_t gv = __shfl_sync(0xFFFFFFFFu, e, src_lane);
-        const uint64_t gat = __shfl_sync(0xFFFFFFFFu, at, src_lane);
-        const GiantRec G = giants[gv & kIdIndex];
-        for (uint32_t q = lane; q < G.count; q += 32) {
-          if ((int64_t)(gat + q) < capacity) out_ids[gat + q] = pool[G.start + q];
+      for (uint32_t q0 = 0; q0 < n_part; q0 += 32) {
+        const uint32_t e = q0 + lane < n_part ? ent[q0 + lane] : kIdHole;
+        const bool plain = (e & kIdSpecial) == 0;  // an id (no hole, no placeholder)
+        const uint32_t pb = __ballot_sync(0xFFFFFFFFu, plain);
+        uint64_t at = st.at0 + lane;
+        uint32_t n_here = 32;  // ids this chunk places
+        bool ph = false;
+        if (pb != 0xFFFFFFFFu) {
+          const bool valid = (e & (kIdSpecial | kIdLong)) != kIdSpecial;
+          ph = valid && !plain;
+          const uint32_t n_ids = !valid ? 0u : (ph ? giants[e & kIdIndex].count : 1u);
+          const uint32_t incl = warp_scan_incl(n_ids);
+          at = st.at0 + (incl - n_ids);
+          n_here = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (plain) {
+          if ((int64_t)at < capacity) out_ids[at] = (int32_t)(e & ~kIdDoc);
           else over = true;
         }
+        const bool mark = (e & kIdDoc) != 0;
+        const uint32_t mb = __ballot_sync(0xFFFFFFFFu, mark);
+        if (!dup) {
+          if (mark) {
+            const int64_t k = R.k0 + st.nmark + __popc(mb & lanemask_lt());
+            if (k < R.k1) out_offsets[k] = (int64_t)at;
+            else atomicOr(&small->status, kStInternal);
+          }
+        } else {
+          uint32_t mm = mb;
+          while (mm) {  // marks in rank order: each takes the documents at its start
+            const int m_lane = __ffs(mm) - 1;
+            mm &= mm - 1;
+            const uint64_t at_m = __shfl_sync(0xFFFFFFFFu, at, m_lane);
+            const int64_t o0 = k_next < R.k1 ? doc_offsets[k_next] : INT64_MAX;
+            int64_t k = k_next;
+            while (k < R.k1 && doc_offsets[k] == o0) {
+              if (lane == 0) out_offsets[k] = (int64_t)at_m;
+              ++k;
+            }
+            if (k == k_next) atomicOr(&small->status, kStInternal);
+            k_next = k;
+          }
+        }
+        uint32_t phm = __ballot_sync(0xFFFFFFFFu, ph);
+        while (phm) {
+          const int src_lane = __ffs(phm) - 1;
+          phm &= phm - 1;
+          const uint32_t gv = __shfl_sync(0xFFFFFFFFu, e, src_lane);
+          const uint64_t gat = __shfl_sync(0xFFFFFFFFu, at, src_lane);
+          const GiantRec G = giants[gv & kIdIndex];
+          for (uint32_t q = lane; q < G.count; q += 32) {
+            if ((int64_t)(gat + q) < capacity) out_ids[gat + q] = pool[G.start + q];
+            else over = true;
+          }
+        }
+        st.nmark += __popc(mb);
+        st.at0 += n_here;
       }
-      nmark += __popc(mb);
-      at0 += __shfl_sync(0xFFFFFFFFu, incl, 31);
-    };
-    // a chunk past the used entries holds only holes and changes nothing
-#pragma unroll
-    for (int c = 0; c < kCompactChunks; ++c)
-      if (32u * c < R.resv) chunk(v[c]);
-    for (uint32_t q0 = 32u * kCompactChunks; q0 < R.resv; q0 += 32)
-      chunk(q0 + lane < R.resv ? __ldcs(src + q0 + lane) : kIdHole);
+    }
     // documents with no mark: at the end of the last document
-    const int64_t k_rest = !dup ? R.k0 + nmark : (nmark == 0 ? R.k0 : R.k0 + docq[warp][nmark - 1] + 1);
-    for (int64_t k = k_rest + lane; k < R.k1; k += 32) out_offsets[k] = (int64_t)at0;
+    const int64_t k_rest = !dup ? R.k0 + st.nmark : k_next;
+    for (int64_t k = k_rest + lane; k < R.k1; k += 32) out_offsets[k] = (int64_t)st.at0;
     __syncwarp();
   }
   if (over) atomicOr(&small->status, kStCapacity);

@@ -279,6 +279,11 @@ int bpe_merges_monotone(const int32_t* merges, int64_t n_merges, int64_t n_vocab
 /* bpe_merges_monotone of the table a handle was built from. */
 int bpe_table_monotone(const bpe_handle* h, int* monotone);
 
+/* Bytes of device workspace the handle holds now (0 until a call needs it):
+ * bpe_encode_batch, bpe_encode_batch_host and bpe_decode_batch grow it;
+ * bpe_encode_batch_noalloc never does. */
+int bpe_workspace_bytes(const bpe_handle* h, int64_t* bytes);
+
 /* Frees the handle's device memory. Waits for its device first. */
 int bpe_destroy(bpe_handle* h);
 

@@ -100,6 +100,8 @@ def test_limit_and_empty_batch(bpe, handle):
     with pytest.raises(bpe.BpeError) as err:
         _noalloc(bpe, handle, big, limit + 1)
     assert err.value.code == 1 and "4 MiB" in str(err.value)
+    # the limit in the message is the binding's constant
+    assert f"limit of {limit} bytes" in str(err.value)
     torch.cuda.synchronize()
     assert (big[2].cpu().numpy() == -7).all() and (big[3].cpu().numpy() == -7).all()
     # Empty batches.
@@ -107,3 +109,31 @@ def test_limit_and_empty_batch(bpe, handle):
         dev = _device(np.zeros(0, np.uint8), np.zeros(n_docs + 1, np.int64))
         assert _noalloc(bpe, handle, dev, 0) == 0
         assert (dev[3].cpu().numpy() == 0).all()
+
+
+def test_calls_allocate_no_device_memory(bpe):
+    """A fresh handle, used only through the no-alloc call: after the first
+    call (which looks up the scratch address once per device), further calls
+    leave the device's free memory unchanged, and the handle's own workspace
+    is never created."""
+    import torch
+    m, vb, vo = workloads.table(1)
+    h = bpe.bpe_build(m, vb, vo, 0)
+    try:
+        d, o = workloads.docs(5, 0, 3000)
+        dev = _device(d, o)
+        want = None
+        _noalloc(bpe, h, dev, d.size)
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        for _ in range(3):
+            total = _noalloc(bpe, h, dev, d.size)
+            got = (dev[2][:total].cpu().numpy(), dev[3].cpu().numpy())
+            if want is None:
+                want = got
+            assert_same_encoding(got, want, d, o, "repeat")
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0
+        assert bpe.bpe_workspace_bytes(h) == 0
+    finally:
+        bpe.bpe_destroy(h)
