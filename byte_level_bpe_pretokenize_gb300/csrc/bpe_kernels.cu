@@ -884,11 +884,30 @@ __device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, in
       uint32_t pos = block_excl_scan(cnt, L.red, &round_cnt);
       for (uint32_t j = 0; j < cnt; ++j) L.stage[pos + j] = y[j];
       cta_sync();
-      for (uint32_t q = tid; q < round_cnt; q += kThreads) {
-        uint32_t left = q == 0 ? prev_sym : L.stage[q - 1];
-        uint32_t right = L.stage[q];
-        if (left != kNone) local_min = min(local_min, lookup_rank(T, left, right));
-        scr[W + q] = (int32_t)right;
+      // the round's new pairs, kLongPerThread per thread with their home
+      // buckets loaded together
+      {
+        uint32_t lf[kLongPerThread], rt[kLongPerThread], bk[kLongPerThread];
+        uint4 u[kLongPerThread], v[kLongPerThread];
+#pragma unroll
+        for (int k = 0; k < kLongPerThread; ++k) {
+          const uint32_t q = (uint32_t)tid + (uint32_t)k * kThreads;
+          lf[k] = kNone;
+          rt[k] = 0;
+          if (q < round_cnt) {
+            lf[k] = q == 0 ? prev_sym : L.stage[q - 1];
+            rt[k] = L.stage[q];
+            scr[W + q] = (int32_t)rt[k];
+          }
+          bk[k] = pair_hash(lf[k], rt[k]) & T.hmask;
+          if (lf[k] != kNone) ldg32(T.ht + 2ull * bk[k], u[k], v[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < kLongPerThread; ++k) {
+          if (lf[k] == kNone) continue;
+          uint32_t nw;
+          local_min = min(local_min, lookup_pair_from(T, lf[k], rt[k], bk[k], u[k], v[k], &nw));
+        }
       }
       if (round_cnt > 0) prev_sym = L.stage[round_cnt - 1];
       W += round_cnt;
@@ -1392,7 +1411,7 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
   k_misses<<<(unsigned)(kMissBlocksPerSm * h->n_sms), kMissThreads, 0, st>>>(d_bytes, w.misses, w.miss_cap, w.stage,
                                                                             w.rec, a.T, h->d_small);
   CK(cudaGetLastError());
-  k_giants<<<(unsigned)(2 * h->n_sms), kGiantThreads, 0, st>>>(d_bytes, w.giants, w.giant_cap, w.first_start, n_tiles,
+  k_giants<<<(unsigned)(8 * h->n_sms), kGiantThreads, 0, st>>>(d_bytes, w.giants, w.giant_cap, w.first_start, n_tiles,
                                                             w.rec, w.pool, a.T, h->d_small);
   CK(cudaGetLastError());
   const int64_t n_blocks = (n_tiles + kScanThreads - 1) / kScanThreads;
