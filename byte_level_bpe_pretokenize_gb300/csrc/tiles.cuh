@@ -694,7 +694,8 @@ __global__ void k_prep_docs(const int64_t* doc_offsets, int64_t n_docs, int64_t 
     small->n_misses = 0;
     small->n_giants = 0;
     small->giant_ctr = 0;
-    small->n_ranges = 0;
+    // n_ranges is counted by this kernel's threads, so it starts the call at
+    // zero from the call before (k_scan_tile_sums) or from bpe_build
   }
   bool bad = false;
   for (int64_t k = t0; k <= n_docs + 1; k += stride) {
@@ -847,7 +848,10 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_tile_sums(uint64_t* block
     if (threadIdx.x == 0) carry += all;
     __syncthreads();
   }
-  if (threadIdx.x == 0) small->total = (int64_t)carry;
+  if (threadIdx.x == 0) {
+    small->total = (int64_t)carry;
+    small->n_ranges = 0;  // for the next call's k_prep_docs (k_prep_long has read it)
+  }
 }
 
 constexpr int kCompactWarps = 8;

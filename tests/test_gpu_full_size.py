@@ -38,11 +38,20 @@ def gpu_encode_whole(bpe, cfg):
         d_off = torch.from_numpy(offsets).cuda()
         d_ids = torch.empty(data.size, dtype=torch.int32, device="cuda")
         d_out = torch.empty(len(offsets), dtype=torch.int64, device="cuda")
-        total = bpe.bpe_encode_batch(h, d_data.data_ptr(), data.size, d_off.data_ptr(), len(offsets) - 1,
-                                     d_ids.data_ptr(), d_ids.numel(), d_out.data_ptr(), True,
-                                     torch.cuda.current_stream().cuda_stream)
+        def call():
+            return bpe.bpe_encode_batch(h, d_data.data_ptr(), data.size, d_off.data_ptr(), len(offsets) - 1,
+                                        d_ids.data_ptr(), d_ids.numel(), d_out.data_ptr(), True,
+                                        torch.cuda.current_stream().cuda_stream)
+        total = call()
         ids = d_ids[:total].cpu().numpy()
         out_off = d_out.cpu().numpy()
+        # the same handle again, twice (nothing of a call may leak into the next)
+        for _ in range(2):
+            d_ids.fill_(-7)
+            d_out.fill_(-7)
+            assert call() == total
+            assert np.array_equal(d_ids[:total].cpu().numpy(), ids), f"config {cfg}: a repeated call differs"
+            assert np.array_equal(d_out.cpu().numpy(), out_off), f"config {cfg}: a repeated call's offsets differ"
     finally:
         bpe.bpe_destroy(h)
     return data, offsets, (merges, vb, vo), ids, out_off
