@@ -35,11 +35,16 @@ METRIC = "encoded input MB/s and tokens/s on 1 GB300; achieved HBM GB/s vs peak"
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic_serving_batch.json")
 KERNEL_SPAN = "k_prep_docs..k_compact"
 LAUNCHES_PER_CALL = 8
-KERNEL_SRC = os.path.join(ROOT, "byte_level_bpe_pretokenize_gb300", "csrc", "bpe_kernels.cu")
+KERNEL_SRC = [os.path.join(ROOT, "byte_level_bpe_pretokenize_gb300", "csrc", f)
+              for f in ("bpe_kernels.cu", "tiles.cuh", "class_table.inc")]
 
 
 def kernel_hash() -> str:
-    return hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    """Hash of the kernel sources (the translation unit and what it includes)."""
+    h = hashlib.sha256()
+    for f in KERNEL_SRC:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def peaks():
@@ -348,6 +353,17 @@ def run_gpu(args, world, rank, local):
     step_ms = t_start.elapsed_time(t_end) / args.steps
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
 
+    if args.kernels_only:
+        if rank == 0:
+            print(json.dumps({"kernels_only": True, "workload": workloads.NAMES[cfg], "n_docs": n_docs,
+                              "n_bytes": n_bytes, "tokens": int(n_tokens), "ms_per_step": round(step_ms, 4),
+                              "kernel_ms": round(kern_ms, 4), "gpu_launches": LAUNCHES_PER_CALL * args.steps}),
+                  flush=True)
+        enc.close()
+        if dist:
+            dist.destroy_process_group()
+        return None
+
     # Secondary: the same calls with the word cache off (every pre-token runs
     # the merge loop), timed the same way, outside the headline region.
     bpe.bpe_set_word_cache(handle, False)
@@ -466,6 +482,9 @@ def main():
     ap.add_argument("--reference-slice-mib", type=int, default=64,
                     help="MiB of whole documents per --impl reference step")
     ap.add_argument("--no-configs", action="store_true", help="headline workload only (no C1-C4 lines, no full parity)")
+    ap.add_argument("--kernels-only", action="store_true",
+                    help="profiling runs: the warm-up and timed device calls only (no cache-off, e2e or oracle "
+                         "legs); prints a short line that is not a bench result")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":

@@ -357,10 +357,13 @@ __device__ __forceinline__ Ascii4 ascii_classes(uint32_t w) {
 // 0x80-per-byte mask of a word -> 4 bits (byte j -> bit j).
 __device__ __forceinline__ uint32_t movemask4(uint32_t m) { return ((m >> 7) * 0x01020408u) >> 24; }
 
-// A 32-bit shared-memory load the compiler must issue as written. Merging a
-// shift-or of two adjacent word loads into one load at a 2-byte offset is a
-// misaligned 32-bit shared access on the GPU (it faults), so every such
-// combination below reads its words through this.
+// A 32-bit shared-memory load the compiler must issue as written, at the
+// aligned word address given. The funnel shifts of adjacent words below read
+// their words through this, so that no load of theirs can become a wider or
+// shifted access. This is a guard, not a known fix: an earlier kernel that did
+// the split and the encode in one CTA raised "misaligned address", and the
+// cause was never found (a CPU emulation under address and undefined-behaviour
+// checks was clean); a compiler-merged unaligned shared load was one suspect.
 __device__ __forceinline__ uint32_t lds_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"((unsigned)__cvta_generic_to_shared(p)));
