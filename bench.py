@@ -33,8 +33,8 @@ import workloads  # noqa: E402
 
 METRIC = "encoded input MB/s and tokens/s on 1 GB300; achieved HBM GB/s vs peak"
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic_serving_batch.json")
-KERNEL_SPAN = "k_prep_docs..k_compact"
-LAUNCHES_PER_CALL = 8
+KERNEL_SPAN = "k_prep_docs..k_giant_copy"
+LAUNCHES_PER_CALL = 9
 KERNEL_SRC = [os.path.join(ROOT, "byte_level_bpe_pretokenize_gb300", "csrc", f)
               for f in ("bpe_kernels.cu", "tiles.cuh", "class_table.inc")]
 

@@ -1338,7 +1338,9 @@ int tiles_smem_setup() {
 
 // The per-call kernels on stream st: k_prep_docs, k_prep_long, k_tiles,
 // k_misses, k_giants (which returns at once when nothing was deferred), the
-// scan and k_compact. ev_start / ev_stop (may be null) bracket all of them.
+// scan, k_compact and k_giant_copy (which returns at once when no deferred
+// pre-token has more than kCompactInlineIds ids). ev_start / ev_stop (may be
+// null) bracket all of them.
 int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
                   int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets, cudaStream_t st,
                   cudaEvent_t ev_start, cudaEvent_t ev_stop);
@@ -1388,8 +1390,8 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
   k_prep_docs<<<prep_blocks, 256, 0, st>>>(d_doc_offsets, n_docs, n_bytes, n_tiles, w.first_doc, w.ranges,
                                            w.range_cap, h->d_small);
   CK(cudaGetLastError());
-  k_prep_long<<<(unsigned)std::min<int64_t>(2 * h->n_sms, w.range_cap), 256, 0, st>>>(w.ranges, w.first_doc,
-                                                                                    h->d_small);
+  k_prep_long<<<(unsigned)std::min<int64_t>(2 * h->n_sms, w.range_cap), 256, 0, st>>>(w.ranges, w.range_cap,
+                                                                                    w.first_doc, n_tiles, h->d_small);
   CK(cudaGetLastError());
   TileArgs a;
   a.bytes = d_bytes;
@@ -1423,8 +1425,11 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
   k_scan_tile_sums<<<1, kScanThreads, 0, st>>>(w.block_sum, n_blocks, h->d_small);
   CK(cudaGetLastError());
   k_compact<<<(unsigned)std::min<int64_t>((n_tiles + kCompactWarps - 1) / kCompactWarps, 8 * h->n_sms),
-              32 * kCompactWarps, 0, st>>>(w.rec, w.stage, w.tile_base, w.block_sum, w.giants, w.pool, d_doc_offsets,
-                                          n_tiles, d_out_ids, out_capacity, d_out_offsets, h->d_small);
+              32 * kCompactWarps, 0, st>>>(w.rec, w.stage, w.tile_base, w.block_sum, w.giants, w.giant_cap, w.pool,
+                                          d_doc_offsets, n_tiles, d_out_ids, out_capacity, d_out_offsets, h->d_small);
+  CK(cudaGetLastError());
+  k_giant_copy<<<(unsigned)(4 * h->n_sms), kCopyThreads, 0, st>>>(w.giants, w.giant_cap, w.pool, d_out_ids,
+                                                                  out_capacity, h->d_small);
   CK(cudaGetLastError());
   if (ev_stop) CK(cudaEventRecord(ev_stop, st));
   return BPE_OK;

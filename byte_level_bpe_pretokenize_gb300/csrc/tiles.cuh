@@ -61,14 +61,17 @@ constexpr uint32_t kIdIndex = 0x1FFFFFFFu;
 
 // A deferred pre-token (longer than kShortMax bytes, or running past its
 // tile's margin): k_giants finds its end when unknown (-1), merges it into
-// the pool at its own bytes and stores its id count.
+// the pool at its own bytes and stores its id count; k_compact stores its
+// output position when it leaves the copy to k_giant_copy.
 struct GiantRec {
   int64_t start;
   int64_t end;
   int64_t tile;
+  int64_t at;
   uint32_t count;
   uint32_t pad;
 };
+constexpr uint32_t kCompactInlineIds = 1024;  // more ids than this: copied by k_giant_copy
 
 // Per tile: its documents [k0, k1) (k = n_docs: the end of the last one),
 // stage entries used, holes left by merged misses, extra ids of its
@@ -511,7 +514,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm) k_tiles(TileArgs
           const uint32_t end = (S.span[min(i0 + 32u * h + lane, n_spans) + 1] == kSpanNone) ? 0u : len[h];
           const unsigned long long gi = atomicAdd(&a.small->n_giants, 1ull);
           if ((int64_t)gi < a.giant_cap) {
-            a.giants[gi] = GiantRec{t0 + (int64_t)s[h], end ? t0 + (int64_t)(s[h] + end) : -1, t, 0u, 0u};
+            a.giants[gi] = GiantRec{t0 + (int64_t)s[h], end ? t0 + (int64_t)(s[h] + end) : -1, t, -1, 0u, 0u};
             stage[at[h]] = kIdSpecial | kIdLong | (uint32_t)gi | doc[h];
           } else {
             atomicOr(&a.small->status, kStInternal);
@@ -669,7 +672,7 @@ __global__ void __launch_bounds__(kMissThreads, kMissBlocksPerSm) k_misses(const
 // ------------------------------------------------------------- preparation --
 
 // Per call, before k_tiles: counters reset, offsets validated, and
-// first_doc[t] = the first document k with doc_offsets[k] >= 992 t - 16
+// first_doc[t] = the first document k with doc_offsets[k] >= 2016 t - 16
 // (n_docs + 1 if none). Thread k writes the tiles whose window start lies in
 // (doc_offsets[k - 1], doc_offsets[k]]: at most kPrepSpan of them, and a
 // longer run goes to a list that k_prep_long fills.
@@ -722,12 +725,15 @@ __global__ void k_prep_docs(const int64_t* doc_offsets, int64_t n_docs, int64_t 
 
 // The long runs of tiles k_prep_docs listed, a CTA per run; skipped when the
 // offsets are malformed (the runs may then overlap without bound).
-__global__ void k_prep_long(const PrepRange* ranges, int64_t* first_doc, DevSmall* small) {
-  const unsigned long long n = small->n_ranges;
+__global__ void k_prep_long(const PrepRange* ranges, int64_t range_cap, int64_t* first_doc, int64_t n_tiles,
+                            DevSmall* small) {
+  const unsigned long long n_raw = small->n_ranges;
+  const unsigned long long n = n_raw < (unsigned long long)range_cap ? n_raw : (unsigned long long)range_cap;
   if (small->status & kStBadInput) return;
   for (unsigned long long r = blockIdx.x; r < n; r += gridDim.x) {
     const PrepRange R = ranges[r];
-    for (int64_t t = R.t_lo + threadIdx.x; t <= R.t_hi; t += blockDim.x) first_doc[t] = R.k;
+    const int64_t lo = R.t_lo < 0 ? 0 : R.t_lo, hi = R.t_hi < n_tiles ? R.t_hi : n_tiles - 1;
+    for (int64_t t = lo + threadIdx.x; t <= hi; t += blockDim.x) first_doc[t] = R.k;
   }
 }
 
@@ -878,12 +884,14 @@ struct CompactState {
 constexpr int kCompactPart = 512;
 __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* rec, const uint32_t* stage,
                                                                 const uint64_t* tile_base, const uint64_t* block_sum,
-                                                                const GiantRec* giants, const int32_t* pool,
+                                                                GiantRec* giants, int64_t giant_cap, const int32_t* pool,
                                                                 const int64_t* doc_offsets, int64_t n_tiles,
                                                                 int32_t* out_ids, int64_t capacity,
                                                                 int64_t* out_offsets, DevSmall* small) {
   __shared__ __align__(16) uint32_t ent_all[kCompactWarps][kCompactPart];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned long long n_giants = small->n_giants < (unsigned long long)giant_cap ? small->n_giants
+                                                                                      : (unsigned long long)giant_cap;
   uint32_t* ent = ent_all[warp];
   const int64_t warps = (int64_t)gridDim.x * kCompactWarps;
   bool over = false;
@@ -924,8 +932,9 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* r
         bool ph = false;
         if (pb != 0xFFFFFFFFu) {
           const bool valid = (e & (kIdSpecial | kIdLong)) != kIdSpecial;
-          ph = valid && !plain;
-          const uint32_t n_ids = !valid ? 0u : (ph ? giants[e & kIdIndex].count : 1u);
+          ph = valid && !plain && (e & kIdIndex) < n_giants;
+          if (valid && !plain && !ph) atomicOr(&small->status, kStInternal);
+          const uint32_t n_ids = (!valid || (!plain && !ph)) ? 0u : (ph ? giants[e & kIdIndex].count : 1u);
           const uint32_t incl = warp_scan_incl(n_ids);
           at = st.at0 + (incl - n_ids);
           n_here = __shfl_sync(0xFFFFFFFFu, incl, 31);
@@ -965,9 +974,25 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* r
           const uint32_t gv = __shfl_sync(0xFFFFFFFFu, e, src_lane);
           const uint64_t gat = __shfl_sync(0xFFFFFFFFu, at, src_lane);
           const GiantRec G = giants[gv & kIdIndex];
-          for (uint32_t q = lane; q < G.count; q += 32) {
-            if ((int64_t)(gat + q) < capacity) out_ids[gat + q] = pool[G.start + q];
-            else over = true;
+          if (G.count > kCompactInlineIds) {  // a CTA of k_giant_copy copies it
+            if (lane == 0) giants[gv & kIdIndex].at = (int64_t)gat;
+            continue;
+          }
+          for (uint32_t q0 = 0; q0 < G.count; q0 += 32 * 8) {  // eight loads in flight a lane
+            int32_t v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const uint32_t q = q0 + 32 * u + lane;
+              v[u] = q < G.count ? pool[G.start + q] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const uint32_t q = q0 + 32 * u + lane;
+              if (q < G.count) {
+                if ((int64_t)(gat + q) < capacity) out_ids[gat + q] = v[u];
+                else over = true;
+              }
+            }
           }
         }
         st.nmark += __popc(mb);
@@ -978,6 +1003,41 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* r
     const int64_t k_rest = !dup ? R.k0 + st.nmark : k_next;
     for (int64_t k = k_rest + lane; k < R.k1; k += 32) out_offsets[k] = (int64_t)st.at0;
     __syncwarp();
+  }
+  if (over) atomicOr(&small->status, kStCapacity);
+}
+
+// The ids of the deferred pre-tokens that k_compact left (more than
+// kCompactInlineIds of them), a CTA each: pool -> out_ids at the stored
+// position, eight loads in flight a thread.
+constexpr int kCopyThreads = 256;
+__global__ void __launch_bounds__(kCopyThreads) k_giant_copy(const GiantRec* giants, int64_t giant_cap,
+                                                               const int32_t* pool, int32_t* out_ids, int64_t capacity,
+                                                               DevSmall* small) {
+  const unsigned long long n = small->n_giants < (unsigned long long)giant_cap ? small->n_giants
+                                                                               : (unsigned long long)giant_cap;
+  bool over = false;
+  for (unsigned long long g = blockIdx.x; g < n; g += gridDim.x) {
+    const int64_t at = giants[g].at;
+    const uint32_t count = giants[g].count;
+    if (count <= kCompactInlineIds || at < 0) continue;
+    const int32_t* src = pool + giants[g].start;
+    for (uint32_t q0 = 0; q0 < count; q0 += kCopyThreads * 8) {
+      int32_t v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t q = q0 + kCopyThreads * u + threadIdx.x;
+        v[u] = q < count ? src[q] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t q = q0 + kCopyThreads * u + threadIdx.x;
+        if (q < count) {
+          if (at + (int64_t)q < capacity) out_ids[at + q] = v[u];
+          else over = true;
+        }
+      }
+    }
   }
   if (over) atomicOr(&small->status, kStCapacity);
 }
