@@ -609,40 +609,7 @@ __device__ uint32_t start_mask32(const SS& S, int p0) {
 
 // ----------------------------------------------------------- block helpers --
 
-__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    uint32_t o = __shfl_up_sync(0xFFFFFFFFu, v, d);
-    if (lane >= d) v += o;
-  }
-  return v;
-}
-
-// Exclusive scan over the CTA; *total gets the sum. One barrier: each warp
-// posts its total to red[0..kThreads/32) and every thread adds up the totals
-// of the warps before its own. SYNC_AFTER = false leaves out the closing
-// barrier that lets red be written again: for callers that pass another
-// barrier before their next use of red.
-template <bool SYNC_AFTER = true>
-__device__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t incl = warp_incl_scan(v);
-  if (lane == 31) red[warp] = incl;
-  cta_sync();
-  uint32_t before = 0, all = 0;
-#pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) {
-    const uint32_t x = red[w];
-    before += w < warp ? x : 0u;
-    all += x;
-  }
-  *total = all;
-  if (SYNC_AFTER) cta_sync();
-  return before + incl - v;
-}
-
-
+// Minimum over the CTA (two barriers; red is free again on return).
 __device__ uint32_t block_min(uint32_t v, uint32_t* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -651,40 +618,6 @@ __device__ uint32_t block_min(uint32_t v, uint32_t* red) {
   cta_sync();
   uint32_t r = red[0];
   for (int k = 1; k < kThreads / 32; ++k) r = min(r, red[k]);
-  cta_sync();
-  return r;
-}
-
-// Transfer functions {0,1} -> {0,1} packed as bit0 = f(0), bit1 = f(1).
-__device__ __forceinline__ uint32_t tf_apply(uint32_t f, uint32_t x) { return (f >> x) & 1u; }
-__device__ __forceinline__ uint32_t tf_then(uint32_t first, uint32_t second) {
-  return tf_apply(second, first & 1u) | (tf_apply(second, (first >> 1) & 1u) << 1);
-}
-
-// Exclusive scan of transfer functions over the CTA, applied to carry_in.
-__device__ uint32_t block_tf_input(uint32_t f, uint32_t carry_in, uint32_t* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t incl = f;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-    if (lane >= d) incl = tf_then(o, incl);
-  }
-  if (lane == 31) red[warp] = incl;
-  cta_sync();
-  if (threadIdx.x == 0) {
-    uint32_t acc = 2u;  // identity
-    for (int k = 0; k < kThreads / 32; ++k) {
-      uint32_t t = red[k];
-      red[k] = acc;
-      acc = tf_then(acc, t);
-    }
-  }
-  cta_sync();
-  uint32_t excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-  if (lane == 0) excl = 2u;
-  uint32_t before = tf_then(red[warp], excl);
-  uint32_t r = tf_apply(before, carry_in);
   cta_sync();
   return r;
 }
@@ -822,107 +755,174 @@ __device__ uint32_t merge_group(GroupScratch& W, const uint8_t* src, uint32_t n,
 }
 
 // ------------------------------------------------------------ merge: long --
-// The whole CTA merges one long pre-token in place in scr (the pool range of
-// its own bytes, read and written in rounds of kRound elements; a round writes
-// only below where it read). A step is one pass: the chosen pair is replaced
-// left to right without overlap — each thread runs that scan over its
-// kLongPerThread elements for both possible "first element already consumed"
-// inputs, a CTA scan composes the results in order — and the pass also probes
-// every new adjacent pair for the next step's lowest rank.
+// The whole CTA merges one long pre-token in place: its symbols in scr and
+// the rank of each symbol's pair with the next in srk (both the pool range
+// of its own bytes, read and written in rounds of kRound elements; a round
+// writes only below where it read). A step is one pass: the chosen pair is
+// replaced left to right without overlap, and only the pairs that touch a
+// new symbol are looked up again; every other pair keeps its rank. Within a
+// round each thread takes kLongPerThread elements; whether its first element
+// was consumed by the merge before it, and where its kept symbols go, come
+// from one CTA scan of (transfer function, kept count) elements.
+
+constexpr uint32_t kDirty = 0xFFFFFFFEu;  // a new symbol: its pairs are looked up again
 
 struct LongScratch {
-  uint32_t* stage;  // kRound
-  uint32_t* red;    // kThreads / 32 + 2
-  uint32_t* carry;  // 1
+  uint32_t* sym;   // [2][kRound]: a round's kept symbols (by round parity)
+  uint32_t* rk;    // [2][kRound]: their old pair ranks, or kDirty
+  uint32_t* red;   // [2][kThreads / 32]
+  uint32_t* mred;  // [kThreads / 32]
 };
 
-__device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, int32_t* scr, const Tables& T,
-                               const int32_t* byte_id, LongScratch L) {
-  const int tid = threadIdx.x;
+// One scan element: bit 0 = "next element consumed" after this part when
+// the part's first element was not consumed, bit 1 = the same when it was;
+// bits 2..12 and 13..23 = symbols the part keeps in either case.
+__device__ __forceinline__ uint32_t tfc_then(uint32_t a, uint32_t b) {
+  const uint32_t a0 = a & 1u, a1 = (a >> 1) & 1u;
+  const uint32_t b0 = (b >> 2) & 0x7FFu, b1 = (b >> 13) & 0x7FFu;
+  const uint32_t f = ((b >> a0) & 1u) | ((b >> a1) & 1u) << 1;
+  const uint32_t c0 = ((a >> 2) & 0x7FFu) + (a0 ? b1 : b0);
+  const uint32_t c1 = ((a >> 13) & 0x7FFu) + (a1 ? b1 : b0);
+  return f | c0 << 2 | c1 << 13;
+}
+constexpr uint32_t kTfcIdentity = 2u;
+static_assert(kRound < 2048, "round counts fit in 11 bits");
+
+__device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, int32_t* scr, uint32_t* srk,
+                               const Tables& T, const int32_t* byte_id, LongScratch L) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t len = n;
   bool first_pass = true;
-  uint32_t A = 0, B = 0, NW = 0;
+  uint32_t best = kInf, NW = 0;
+  uint32_t par = 0;
   for (;;) {
-    uint32_t W = 0, carry = 0, prev_sym = kNone, local_min = kInf;
-    for (uint32_t r0 = 0; r0 < len; r0 += kRound) {
-      uint32_t x[kLongPerThread + 1];
+    uint32_t W = 0, carry = 0, prev_sym = kNone, prev_rk = kDirty, local_min = kInf;
+    for (uint32_t r0 = 0; r0 < len; r0 += kRound, par ^= 1u) {
+      uint32_t x[kLongPerThread], r[kLongPerThread];
 #pragma unroll
-      for (int k = 0; k <= kLongPerThread; ++k) {
-        uint32_t idx = r0 + (uint32_t)tid * kLongPerThread + (uint32_t)k;
+      for (int k = 0; k < kLongPerThread; ++k) {
+        const uint32_t idx = r0 + (uint32_t)tid * kLongPerThread + (uint32_t)k;
         x[k] = kNone;
-        if (idx < len) x[k] = first_pass ? (uint32_t)byte_id[g_bytes[s + idx]] : (uint32_t)scr[idx];
+        r[k] = kInf;
+        if (idx < len) {
+          x[k] = first_pass ? (uint32_t)byte_id[g_bytes[s + idx]] : (uint32_t)scr[idx];
+          if (!first_pass && idx + 1 < len) r[k] = srk[idx];
+        }
       }
-      uint32_t f = 2u;
+      // this thread's part for both inputs: consumed out, symbols kept
+      uint32_t e = kTfcIdentity;
       if (!first_pass) {
-        f = 0;
+        e = 0;
 #pragma unroll
         for (uint32_t in = 0; in < 2; ++in) {
-          uint32_t consumed = in;
+          uint32_t consumed = in, kept = 0;
 #pragma unroll
           for (int k = 0; k < kLongPerThread; ++k) {
             if (x[k] == kNone) break;
-            if (consumed) consumed = 0;
-            else if (x[k] == A && x[k + 1] == B) consumed = 1;
+            if (consumed) {
+              consumed = 0;
+            } else {
+              ++kept;
+              consumed = r[k] == best;
+            }
           }
-          f |= consumed << in;
+          e |= consumed << in | kept << (in ? 13 : 2);
         }
+      } else {
+        uint32_t kept = 0;
+#pragma unroll
+        for (int k = 0; k < kLongPerThread; ++k) kept += x[k] != kNone;
+        e = kTfcIdentity | kept << 2 | kept << 13;
       }
-      uint32_t consumed = block_tf_input(f, carry, L.red);  // also orders all reads before writes
-      uint32_t y[kLongPerThread];
-      uint32_t cnt = 0;
+      // CTA scan of the parts, one barrier
+      uint32_t incl = e;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl = tfc_then(o, incl);
+      }
+      uint32_t* red = L.red + par * (kThreads / 32);
+      if (lane == 31) red[warp] = incl;
+      cta_sync();
+      uint32_t before = kTfcIdentity, all = kTfcIdentity;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) {
+        const uint32_t v = red[w];
+        if (w < warp) before = tfc_then(before, v);
+        all = tfc_then(all, v);
+      }
+      uint32_t ex = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+      if (lane == 0) ex = kTfcIdentity;
+      before = tfc_then(before, ex);
+      uint32_t consumed = (before >> carry) & 1u;
+      uint32_t pos = carry ? (before >> 13) & 0x7FFu : (before >> 2) & 0x7FFu;
+      const uint32_t round_cnt = carry ? (all >> 13) & 0x7FFu : (all >> 2) & 0x7FFu;
+      carry = (all >> carry) & 1u;
+      // kept symbols with their old pair ranks (kDirty for a new symbol)
+      uint32_t* st_sym = L.sym + par * kRound;
+      uint32_t* st_rk = L.rk + par * kRound;
 #pragma unroll
       for (int k = 0; k < kLongPerThread; ++k) {
         if (x[k] == kNone) break;
         if (consumed) {
           consumed = 0;
-        } else if (!first_pass && x[k] == A && x[k + 1] == B) {
-          y[cnt++] = NW;
+        } else if (!first_pass && r[k] == best) {
+          st_sym[pos] = NW;
+          st_rk[pos] = kDirty;
+          ++pos;
           consumed = 1;
         } else {
-          y[cnt++] = x[k];
+          st_sym[pos] = x[k];
+          st_rk[pos] = first_pass ? kDirty : r[k];
+          ++pos;
         }
       }
-      if (tid == kThreads - 1) L.carry[0] = consumed;
-      uint32_t round_cnt;
-      uint32_t pos = block_excl_scan(cnt, L.red, &round_cnt);
-      for (uint32_t j = 0; j < cnt; ++j) L.stage[pos + j] = y[j];
       cta_sync();
-      // the round's new pairs, kLongPerThread per thread with their home
-      // buckets loaded together
+      // pairs (q - 1, q) of the new sequence: a pair of two old symbols keeps
+      // its rank (they were adjacent before); the others are looked up, with
+      // their home buckets loaded together
       {
-        uint32_t lf[kLongPerThread], rt[kLongPerThread], bk[kLongPerThread];
+        uint32_t lf[kLongPerThread], rt[kLongPerThread], bk[kLongPerThread], rank[kLongPerThread];
+        bool need[kLongPerThread];
         uint4 u[kLongPerThread], v[kLongPerThread];
 #pragma unroll
         for (int k = 0; k < kLongPerThread; ++k) {
           const uint32_t q = (uint32_t)tid + (uint32_t)k * kThreads;
           lf[k] = kNone;
           rt[k] = 0;
+          rank[k] = kInf;
+          need[k] = false;
           if (q < round_cnt) {
-            lf[k] = q == 0 ? prev_sym : L.stage[q - 1];
-            rt[k] = L.stage[q];
+            lf[k] = q == 0 ? prev_sym : st_sym[q - 1];
+            const uint32_t lrk = q == 0 ? prev_rk : st_rk[q - 1];
+            rt[k] = st_sym[q];
             scr[W + q] = (int32_t)rt[k];
+            need[k] = lf[k] != kNone && (lrk == kDirty || st_rk[q] == kDirty);
+            rank[k] = lrk;
           }
           bk[k] = pair_hash(lf[k], rt[k]) & T.hmask;
-          if (lf[k] != kNone) ldg32(T.ht + 2ull * bk[k], u[k], v[k]);
+          if (need[k]) ldg32(T.ht + 2ull * bk[k], u[k], v[k]);
         }
 #pragma unroll
         for (int k = 0; k < kLongPerThread; ++k) {
           if (lf[k] == kNone) continue;
+          const uint32_t q = (uint32_t)tid + (uint32_t)k * kThreads;
           uint32_t nw;
-          local_min = min(local_min, lookup_pair_from(T, lf[k], rt[k], bk[k], u[k], v[k], &nw));
+          if (need[k]) rank[k] = lookup_pair_from(T, lf[k], rt[k], bk[k], u[k], v[k], &nw);
+          srk[W + q - 1] = rank[k];
+          local_min = min(local_min, rank[k]);
         }
       }
-      if (round_cnt > 0) prev_sym = L.stage[round_cnt - 1];
+      if (round_cnt > 0) {
+        prev_sym = st_sym[round_cnt - 1];
+        prev_rk = st_rk[round_cnt - 1];
+      }
       W += round_cnt;
-      carry = L.carry[0];
-      cta_sync();
     }
     len = W;
     first_pass = false;
-    uint32_t best = block_min(local_min, L.red);
+    best = block_min(local_min, L.mred);
     if (best == kInf) break;
-    A = (uint32_t)T.mrows[3 * best];
-    B = (uint32_t)T.mrows[3 * best + 1];
     NW = (uint32_t)T.mrows[3 * best + 2];
   }
   cta_sync();
@@ -1272,7 +1272,7 @@ struct WsSizes {
 constexpr WsSizes ws_sizes(int64_t n_bytes) {
   WsSizes z{};
   z.n_tiles = n_bytes / kTileOwn + 1;
-  z.miss_cap = n_bytes / 2 + 64;  // a miss has at least 2 bytes
+  z.miss_cap = n_bytes / 2 + 64;  // a miss has at least 2 bytes; k_giants reuses the queue as u32[n_bytes]
   z.giant_cap = n_bytes / (kShortMax + 1) + z.n_tiles + 16;
   z.range_cap = z.n_tiles / kPrepSpan + 16;
   z.first_doc = align256((size_t)z.n_tiles * sizeof(int64_t));
@@ -1338,9 +1338,8 @@ int tiles_smem_setup() {
 
 // The per-call kernels on stream st: k_prep_docs, k_prep_long, k_tiles,
 // k_misses, k_giants (which returns at once when nothing was deferred), the
-// scan, k_compact and k_giant_copy (which returns at once when no deferred
-// pre-token has more than kCompactInlineIds ids). ev_start / ev_stop (may be
-// null) bracket all of them.
+// scan, k_compact and k_giant_copy (which returns at once when nothing was
+// deferred). ev_start / ev_stop (may be null) bracket all of them.
 int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
                   int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets, cudaStream_t st,
                   cudaEvent_t ev_start, cudaEvent_t ev_stop);
@@ -1416,8 +1415,11 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
   k_misses<<<(unsigned)(kMissBlocksPerSm * h->n_sms), kMissThreads, 0, st>>>(d_bytes, w.misses, w.miss_cap, w.stage,
                                                                             w.rec, a.T, h->d_small);
   CK(cudaGetLastError());
+  // the miss queue is dead once k_misses has run: k_giants keeps its pair
+  // ranks there (u32 per input byte; the queue holds 8 bytes per 2)
   k_giants<<<(unsigned)(8 * h->n_sms), kGiantThreads, 0, st>>>(d_bytes, w.giants, w.giant_cap, w.first_start, n_tiles,
-                                                            w.rec, w.pool, a.T, h->d_small);
+                                                            w.rec, w.pool, reinterpret_cast<uint32_t*>(w.misses), a.T,
+                                                            h->d_small);
   CK(cudaGetLastError());
   const int64_t n_blocks = (n_tiles + kScanThreads - 1) / kScanThreads;
   k_scan_tiles<<<(unsigned)n_blocks, kScanThreads, 0, st>>>(w.rec, n_tiles, w.tile_base, w.block_sum);
@@ -1425,7 +1427,7 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
   k_scan_tile_sums<<<1, kScanThreads, 0, st>>>(w.block_sum, n_blocks, h->d_small);
   CK(cudaGetLastError());
   k_compact<<<(unsigned)std::min<int64_t>((n_tiles + kCompactWarps - 1) / kCompactWarps, 8 * h->n_sms),
-              32 * kCompactWarps, 0, st>>>(w.rec, w.stage, w.tile_base, w.block_sum, w.giants, w.giant_cap, w.pool,
+              32 * kCompactWarps, 0, st>>>(w.rec, w.stage, w.tile_base, w.block_sum, w.giants, w.giant_cap,
                                           d_doc_offsets, n_tiles, d_out_ids, out_capacity, d_out_offsets, h->d_small);
   CK(cudaGetLastError());
   k_giant_copy<<<(unsigned)(4 * h->n_sms), kCopyThreads, 0, st>>>(w.giants, w.giant_cap, w.pool, d_out_ids,

@@ -62,7 +62,7 @@ constexpr uint32_t kIdIndex = 0x1FFFFFFFu;
 // A deferred pre-token (longer than kShortMax bytes, or running past its
 // tile's margin): k_giants finds its end when unknown (-1), merges it into
 // the pool at its own bytes and stores its id count; k_compact stores its
-// output position when it leaves the copy to k_giant_copy.
+// output position, and k_giant_copy copies its ids there.
 struct GiantRec {
   int64_t start;
   int64_t end;
@@ -71,7 +71,6 @@ struct GiantRec {
   uint32_t count;
   uint32_t pad;
 };
-constexpr uint32_t kCompactInlineIds = 1024;  // more ids than this: copied by k_giant_copy
 
 // Per tile: its documents [k0, k1) (k = n_docs: the end of the last one),
 // stage entries used, holes left by merged misses, extra ids of its
@@ -746,18 +745,20 @@ __global__ void k_prep_long(const PrepRange* ranges, int64_t range_cap, int64_t*
 constexpr int kGiantThreads = kThreads;
 __global__ void __launch_bounds__(kGiantThreads) k_giants(const uint8_t* bytes, GiantRec* giants, int64_t giant_cap,
                                                           const int64_t* first_start, int64_t n_tiles, TileRec* rec,
-                                                          int32_t* pool, Tables T, DevSmall* small) {
+                                                          int32_t* pool, uint32_t* pool_rank, Tables T,
+                                                          DevSmall* small) {
   __shared__ int32_t byte_id[256];
-  __shared__ uint32_t stage[kRound];
-  __shared__ uint32_t red[kThreads / 32 + 2];
-  __shared__ uint32_t carry[2];
+  __shared__ uint32_t st_sym[2 * kRound];
+  __shared__ uint32_t st_rk[2 * kRound];
+  __shared__ uint32_t red[2 * (kThreads / 32)];
+  __shared__ uint32_t mred[kThreads / 32];
   __shared__ unsigned long long next;
   __shared__ int64_t end_at;
   const unsigned long long n = small->n_giants < (unsigned long long)giant_cap ? small->n_giants
                                                                                : (unsigned long long)giant_cap;
   if (n == 0) return;
   for (int i = threadIdx.x; i < 256; i += kGiantThreads) byte_id[i] = T.byte_id[i];
-  LongScratch L{stage, red, carry};
+  LongScratch L{st_sym, st_rk, red, mred};
   for (;;) {
     if (threadIdx.x == 0) next = atomicAdd(&small->giant_ctr, 1ull);
     __syncthreads();
@@ -782,7 +783,8 @@ __global__ void __launch_bounds__(kGiantThreads) k_giants(const uint8_t* bytes, 
         R.end = R.start + 1;
       }
     }
-    const uint32_t cnt = merge_long(bytes, R.start, (uint32_t)(R.end - R.start), pool + R.start, T, byte_id, L);
+    const uint32_t cnt =
+        merge_long(bytes, R.start, (uint32_t)(R.end - R.start), pool + R.start, pool_rank + R.start, T, byte_id, L);
     if (threadIdx.x == 0) {
       giants[g].count = cnt;
       atomicAdd(&rec[R.tile].extra, cnt - 1u);
@@ -869,8 +871,8 @@ struct CompactState {
 };
 
 // A warp per tile: its stage entries to out_ids at the tile's offset without
-// the holes, each placeholder expanded to its deferred pre-token's ids from
-// the pool. The used part of the tile's stage slot is copied to shared memory
+// the holes, each placeholder given its deferred pre-token's id count (the
+// ids are copied from the pool by k_giant_copy). The used part of the tile's stage slot is copied to shared memory
 // kCompactPart entries at a time with asynchronous 16-byte copies (all loads
 // of a part in flight at once), then walked in chunks of 32 entries by one
 // short loop. A chunk of 32 plain ids needs no scan; others take positions
@@ -882,9 +884,10 @@ struct CompactState {
 // document not yet placed. The documents at the end of the last one get the
 // tile's end.
 constexpr int kCompactPart = 512;
-__global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* rec, const uint32_t* stage,
+
+__global__ void __launch_bounds__(32 * kCompactWarps, 4) k_compact(const TileRec* rec, const uint32_t* stage,
                                                                 const uint64_t* tile_base, const uint64_t* block_sum,
-                                                                GiantRec* giants, int64_t giant_cap, const int32_t* pool,
+                                                                GiantRec* giants, int64_t giant_cap,
                                                                 const int64_t* doc_offsets, int64_t n_tiles,
                                                                 int32_t* out_ids, int64_t capacity,
                                                                 int64_t* out_offsets, DevSmall* small) {
@@ -973,27 +976,7 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* r
           phm &= phm - 1;
           const uint32_t gv = __shfl_sync(0xFFFFFFFFu, e, src_lane);
           const uint64_t gat = __shfl_sync(0xFFFFFFFFu, at, src_lane);
-          const GiantRec G = giants[gv & kIdIndex];
-          if (G.count > kCompactInlineIds) {  // a CTA of k_giant_copy copies it
-            if (lane == 0) giants[gv & kIdIndex].at = (int64_t)gat;
-            continue;
-          }
-          for (uint32_t q0 = 0; q0 < G.count; q0 += 32 * 8) {  // eight loads in flight a lane
-            int32_t v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint32_t q = q0 + 32 * u + lane;
-              v[u] = q < G.count ? pool[G.start + q] : 0;
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint32_t q = q0 + 32 * u + lane;
-              if (q < G.count) {
-                if ((int64_t)(gat + q) < capacity) out_ids[gat + q] = v[u];
-                else over = true;
-              }
-            }
-          }
+          if (lane == 0) giants[gv & kIdIndex].at = (int64_t)gat;  // k_giant_copy copies its ids
         }
         st.nmark += __popc(mb);
         st.at0 += n_here;
@@ -1007,9 +990,8 @@ __global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* r
   if (over) atomicOr(&small->status, kStCapacity);
 }
 
-// The ids of the deferred pre-tokens that k_compact left (more than
-// kCompactInlineIds of them), a CTA each: pool -> out_ids at the stored
-// position, eight loads in flight a thread.
+// The ids of the deferred pre-tokens, a CTA each: pool -> out_ids at the
+// position k_compact stored, eight loads in flight a thread.
 constexpr int kCopyThreads = 256;
 __global__ void __launch_bounds__(kCopyThreads) k_giant_copy(const GiantRec* giants, int64_t giant_cap,
                                                                const int32_t* pool, int32_t* out_ids, int64_t capacity,
@@ -1020,7 +1002,7 @@ __global__ void __launch_bounds__(kCopyThreads) k_giant_copy(const GiantRec* gia
   for (unsigned long long g = blockIdx.x; g < n; g += gridDim.x) {
     const int64_t at = giants[g].at;
     const uint32_t count = giants[g].count;
-    if (count <= kCompactInlineIds || at < 0) continue;
+    if (at < 0) continue;
     const int32_t* src = pool + giants[g].start;
     for (uint32_t q0 = 0; q0 < count; q0 += kCopyThreads * 8) {
       int32_t v[8];
