@@ -844,13 +844,16 @@ __device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, in
       uint32_t* red = L.red + par * (kThreads / 32);
       if (lane == 31) red[warp] = incl;
       cta_sync();
-      uint32_t before = kTfcIdentity, all = kTfcIdentity;
+      // every warp scans the warp totals on its first kThreads / 32 lanes
+      uint32_t wt = lane < kThreads / 32 ? red[lane] : kTfcIdentity;
 #pragma unroll
-      for (int w = 0; w < kThreads / 32; ++w) {
-        const uint32_t v = red[w];
-        if (w < warp) before = tfc_then(before, v);
-        all = tfc_then(all, v);
+      for (int d = 1; d < kThreads / 32; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, wt, d);
+        if (lane >= d) wt = tfc_then(o, wt);
       }
+      const uint32_t all = __shfl_sync(0xFFFFFFFFu, wt, kThreads / 32 - 1);
+      uint32_t before = __shfl_sync(0xFFFFFFFFu, wt, (warp + 31) & 31);
+      if (warp == 0) before = kTfcIdentity;
       uint32_t ex = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
       if (lane == 0) ex = kTfcIdentity;
       before = tfc_then(before, ex);
@@ -947,6 +950,7 @@ __device__ __forceinline__ uint32_t cache_slot(const CacheKey& K, uint32_t len, 
 }  // namespace
 
 #include "tiles.cuh"
+#include "decode.cuh"
 
 namespace {
 
@@ -978,90 +982,6 @@ __global__ void k_offsets_shift(int64_t* x, int64_t n, int64_t delta) {
 // same copy engine and hold up the next slice's kernels.
 __global__ void k_total_to_host(const DevSmall* small, int64_t* h_dst) {
   if (threadIdx.x == 0) *reinterpret_cast<volatile int64_t*>(h_dst) = small->total;
-}
-
-// ---------------------------------------------------------------- decoding --
-
-constexpr int kScanBlock = 1024;
-
-__global__ void k_dec_len(const int32_t* ids, int64_t n_ids, const int64_t* voffs, int64_t n_vocab, int64_t* lens,
-                          DevSmall* small) {
-  bool bad = false;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_ids; i += (int64_t)gridDim.x * blockDim.x) {
-    const int32_t id = ids[i];
-    int64_t L = 0;
-    if (id >= 0 && id < n_vocab) L = voffs[id + 1] - voffs[id];
-    else bad = true;
-    lens[i] = L;
-  }
-  if (bad) atomicOr(&small->status, kStBadInput);
-}
-
-// In-place exclusive scan of x[0..n) in blocks of kScanBlock; block sums to sums.
-__global__ void k_scan_blocks(int64_t* x, int64_t n, int64_t* sums) {
-  __shared__ int64_t s[kScanBlock];
-  const int64_t base = (int64_t)blockIdx.x * kScanBlock;
-  for (int i = threadIdx.x; i < kScanBlock; i += blockDim.x) s[i] = (base + i < n) ? x[base + i] : 0;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int64_t acc = 0;
-    for (int i = 0; i < kScanBlock; ++i) {
-      int64_t v = s[i];
-      s[i] = acc;
-      acc += v;
-    }
-    sums[blockIdx.x] = acc;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < kScanBlock; i += blockDim.x)
-    if (base + i < n) x[base + i] = s[i];
-}
-
-__global__ void k_scan_sums(int64_t* sums, int64_t n_blocks, DevSmall* small) {
-  if (threadIdx.x == 0 && blockIdx.x == 0) {
-    int64_t acc = 0;
-    for (int64_t b = 0; b < n_blocks; ++b) {
-      int64_t v = sums[b];
-      sums[b] = acc;
-      acc += v;
-    }
-    small->total = acc;
-  }
-}
-
-__global__ void k_dec_gather(const int32_t* ids, int64_t n_ids, int64_t* offs, const int64_t* sums,
-                             const uint8_t* vbytes, const int64_t* voffs, int64_t n_vocab, uint8_t* out,
-                             int64_t cap, DevSmall* small) {
-  bool over = false;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_ids; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t o = offs[i] + sums[i / kScanBlock];
-    const int32_t id = ids[i];
-    if (id < 0 || id >= n_vocab) continue;
-    const int64_t b0 = voffs[id], L = voffs[id + 1] - b0;
-    for (int64_t q = 0; q < L; ++q) {
-      if (o + q < cap) out[o + q] = vbytes[b0 + q];
-      else over = true;
-    }
-  }
-  if (over) atomicOr(&small->status, kStCapacity);
-}
-
-__global__ void k_dec_docs(const int64_t* id_offsets, int64_t n_docs, int64_t n_ids, const int64_t* offs,
-                           const int64_t* sums, int64_t* out_offsets, DevSmall* small) {
-  bool bad = false;
-  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k <= n_docs; k += (int64_t)gridDim.x * blockDim.x) {
-    int64_t i = id_offsets[k];
-    if (i < 0 || i > n_ids || (k < n_docs && id_offsets[k + 1] < i)) bad = true;
-    if (i < 0) i = 0;
-    if (i > n_ids) i = n_ids;
-    int64_t first = id_offsets[0];
-    if (first < 0) first = 0;
-    if (first > n_ids) first = n_ids;
-    const int64_t at = (i < n_ids) ? offs[i] + sums[i / kScanBlock] : small->total;
-    const int64_t base = (first < n_ids) ? offs[first] + sums[first / kScanBlock] : small->total;
-    out_offsets[k] = at - base;
-  }
-  if (bad) atomicOr(&small->status, kStBadInput);
 }
 
 // ------------------------------------------------------------------- host --
@@ -1109,6 +1029,7 @@ struct bpe_handle {
   int32_t* d_byte_id = nullptr;
   uint8_t* d_vbytes = nullptr;
   int64_t* d_voffs = nullptr;
+  uint4* d_vent = nullptr;  // per token: its first 12 bytes and its length (decoding)
   uint4* d_cache = nullptr;
   uint32_t cache_mask = 0;
   int64_t cache_entries = 0;
@@ -1530,6 +1451,17 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
   if (nvb) CKB(cudaMemcpy(h->d_vbytes, vocab_bytes, (size_t)nvb, cudaMemcpyHostToDevice));
   CKB(cudaMalloc(&h->d_voffs, (size_t)(n_vocab + 1) * sizeof(int64_t)));
   CKB(cudaMemcpy(h->d_voffs, vocab_offsets, (size_t)(n_vocab + 1) * sizeof(int64_t), cudaMemcpyHostToDevice));
+  {
+    std::vector<uint4> vent((size_t)n_vocab, make_uint4(0, 0, 0, 0));
+    for (int64_t id = 0; id < n_vocab; ++id) {
+      const int64_t b0 = vocab_offsets[id], L = vocab_offsets[id + 1] - b0;
+      uint32_t w[3] = {0, 0, 0};
+      for (int64_t q = 0; q < L && q < (int64_t)kDecInline; ++q) w[q >> 2] |= (uint32_t)vocab_bytes[b0 + q] << (8 * (q & 3));
+      vent[(size_t)id] = make_uint4(w[0], w[1], w[2], (uint32_t)L);
+    }
+    CKB(cudaMalloc(&h->d_vent, vent.size() * sizeof(uint4)));
+    CKB(cudaMemcpy(h->d_vent, vent.data(), vent.size() * sizeof(uint4), cudaMemcpyHostToDevice));
+  }
   CKB(cudaMalloc(&h->d_small, sizeof(DevSmall)));
   CKB(cudaMemset(h->d_small, 0, sizeof(DevSmall)));
   CKB(cudaMallocHost(&h->h_small, sizeof(DevSmall)));
@@ -1549,6 +1481,7 @@ int bpe_destroy(bpe_handle* h) {
   cudaFree(h->d_byte_id);
   cudaFree(h->d_vbytes);
   cudaFree(h->d_voffs);
+  cudaFree(h->d_vent);
   cudaFree(h->d_cache);
   cudaFree(h->d_small);
   cudaFree(h->d_ws);
@@ -1859,19 +1792,26 @@ int bpe_decode_batch(bpe_handle* h, const int32_t* d_ids, int64_t n_ids, const i
     return fail(BPE_ERR_INVALID_ARG, "bpe_decode_batch: offsets must be 8-byte and ids 4-byte aligned");
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
-  const int64_t n_blocks = n_ids / kScanBlock + 1;
-  int rc = ensure_ws(h, (size_t)(n_ids + 1 + n_blocks) * sizeof(int64_t));
+  const int64_t n_tiles = n_ids / kDecIds + 1;
+  const int64_t n_blocks = (n_tiles + kDecScanThreads - 1) / kDecScanThreads;
+  const size_t a1 = align256((size_t)n_tiles * sizeof(uint64_t)), a2 = align256((size_t)n_blocks * sizeof(uint64_t));
+  int rc = ensure_ws(h, a1 + a2 + align256((size_t)n_tiles * sizeof(int64_t)));
   if (rc) return rc;
-  int64_t* offs = (int64_t*)h->d_ws;
-  int64_t* sums = offs + n_ids + 1;
-  const int grid = (int)std::min<int64_t>(8192, n_ids / 256 + 1);
-  k_dec_len<<<grid, 256, 0, st>>>(d_ids, n_ids, h->d_voffs, h->n_vocab, offs, h->d_small);
-  k_scan_blocks<<<(unsigned)n_blocks, 256, 0, st>>>(offs, n_ids, sums);
-  k_scan_sums<<<1, 32, 0, st>>>(sums, n_blocks, h->d_small);
-  k_dec_gather<<<grid, 256, 0, st>>>(d_ids, n_ids, offs, sums, h->d_vbytes, h->d_voffs, h->n_vocab, d_out_bytes,
-                                     out_capacity, h->d_small);
-  const int dgrid = (int)std::min<int64_t>(8192, n_docs / 256 + 1);
-  k_dec_docs<<<dgrid, 256, 0, st>>>(d_id_offsets, n_docs, n_ids, offs, sums, d_out_byte_offsets, h->d_small);
+  uint64_t* tile_base = reinterpret_cast<uint64_t*>(h->d_ws);
+  uint64_t* block_sum = reinterpret_cast<uint64_t*>(static_cast<unsigned char*>(h->d_ws) + a1);
+  int64_t* first_doc = reinterpret_cast<int64_t*>(static_cast<unsigned char*>(h->d_ws) + a1 + a2);
+  const unsigned tile_grid = (unsigned)std::min<int64_t>((n_tiles + kDecWarps - 1) / kDecWarps, 8 * h->n_sms);
+  k_dec_count<<<tile_grid, 32 * kDecWarps, 0, st>>>(d_ids, n_ids, h->d_vent, h->n_vocab, n_tiles, tile_base,
+                                                    h->d_small);
+  k_dec_scan_tiles<<<(unsigned)n_blocks, kDecScanThreads, 0, st>>>(tile_base, n_tiles, block_sum);
+  k_scan_tile_sums<<<1, kScanThreads, 0, st>>>(block_sum, n_blocks, h->d_small);
+  const int64_t n_first = std::max<int64_t>(n_tiles, n_docs + 1);
+  k_dec_first_doc<<<(unsigned)std::min<int64_t>(4096, (n_first + 255) / 256), 256, 0, st>>>(d_id_offsets, n_docs, n_ids,
+                                                                                           n_tiles, first_doc,
+                                                                                           h->d_small);
+  k_dec_write<<<tile_grid, 32 * kDecWarps, 0, st>>>(d_ids, n_ids, h->d_vent, h->d_vbytes, h->d_voffs, h->n_vocab,
+                                                    tile_base, block_sum, first_doc, d_id_offsets, n_docs, n_tiles,
+                                                    d_out_bytes, out_capacity, d_out_byte_offsets, h->d_small);
   CK(cudaGetLastError());
   if (h_total_bytes) {
     DevSmall s;

@@ -79,3 +79,35 @@ def test_full_workload_equals_oracle(bpe, cfg):
         doc = int(np.searchsorted(out_off, k, side="right")) - 1
         raise AssertionError(f"config {cfg}: ids differ from the oracle first at token {k} (document {doc})")
     assert g_digest == o_digest
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_full_workload_decodes_back(bpe, cfg):
+    """decode(encode(x)) == x on every whole workload ("Tokenisierung",
+    section "Prüfe zuerst den Roundtrip"), byte for byte, with the document
+    offsets; the ids come from the GPU encoder (equal to the oracle's by the
+    test above)."""
+    import torch
+    data, offsets = workloads.docs(cfg)
+    merges, vb, vo = workloads.table(cfg)
+    h = bpe.bpe_build(merges, vb, vo, 0)
+    try:
+        s = torch.cuda.current_stream().cuda_stream
+        d_data = torch.from_numpy(data).cuda()
+        d_off = torch.from_numpy(offsets).cuda()
+        d_ids = torch.empty(data.size, dtype=torch.int32, device="cuda")
+        d_ioff = torch.empty(len(offsets), dtype=torch.int64, device="cuda")
+        total = bpe.bpe_encode_batch(h, d_data.data_ptr(), data.size, d_off.data_ptr(), len(offsets) - 1,
+                                     d_ids.data_ptr(), d_ids.numel(), d_ioff.data_ptr(), True, s)
+        del d_data
+        out = torch.full((data.size + 64,), 0xAB, dtype=torch.uint8, device="cuda")
+        out_off = torch.full((len(offsets),), -7, dtype=torch.int64, device="cuda")
+        for _ in range(2):  # twice on one handle
+            n = bpe.bpe_decode_batch(h, d_ids.data_ptr(), total, d_ioff.data_ptr(), len(offsets) - 1, out.data_ptr(),
+                                     out.numel(), out_off.data_ptr(), True, s)
+            assert n == data.size
+            assert np.array_equal(out[:n].cpu().numpy(), data), f"config {cfg}: decoded bytes differ"
+            assert (out[n:].cpu().numpy() == 0xAB).all()
+            assert np.array_equal(out_off.cpu().numpy(), offsets), f"config {cfg}: decoded offsets differ"
+    finally:
+        bpe.bpe_destroy(h)
