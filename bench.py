@@ -275,6 +275,27 @@ class Encoder:
         self.bpe.bpe_sync_status(self.handle, self.stream.cuda_stream)
         return [a.elapsed_time(b) for a, b in ev]
 
+    def kernel_ms(self, calls=3):
+        """Per-kernel CUDA-event time of a call (median over `calls`), from
+        events recorded before the first kernel and after each."""
+        import torch
+        bpe = self.bpe
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(bpe.ENCODE_LAUNCHES + 1)]
+        for e in evs:  # materialise the CUDA events
+            e.record(self.stream)
+        pe = bpe.PhaseEvents([e.cuda_event for e in evs])
+        per = []
+        try:
+            bpe.bpe_set_phase_events(self.handle, pe)
+            for _ in range(calls):
+                torch.cuda.synchronize()
+                self.step()
+                torch.cuda.synchronize()
+                per.append([evs[i].elapsed_time(evs[i + 1]) for i in range(bpe.ENCODE_LAUNCHES)])
+        finally:
+            bpe.bpe_set_phase_events(self.handle, None)
+        return {k: round(statistics.median(p[i] for p in per), 4) for i, k in enumerate(bpe.ENCODE_KERNELS)}
+
     def result(self):
         return self.d_ids[:self.n_tokens].cpu().numpy(), self.d_out.cpu().numpy()
 
@@ -300,6 +321,64 @@ def parity_line(enc: "Encoder", gpu_ids, gpu_off) -> tuple[dict, dict]:
     line = {"fnv1a64_gpu": f"{workloads.fnv1a64(gpu_ids):016x}", "fnv1a64_oracle": f"{workloads.fnv1a64(r['ids']):016x}",
             "docs_compared": enc.n_docs, "identical": same}
     return line, r
+
+
+def decode_line(bpe, enc: "Encoder", steps: int, peak: float) -> dict:
+    """bpe_decode_batch on the encoded batch (ids resident in HBM): CUDA-event
+    time per call (median after 3 warm-up calls), algorithmic bytes (ids and
+    id offsets read, bytes and byte offsets written), and whether the bytes
+    and offsets equal the input."""
+    import torch
+    dev = enc.d_ids.device
+    n_tok = int(enc.n_tokens)
+    out = torch.empty(enc.n_bytes + 64, dtype=torch.uint8, device=dev)
+    out_off = torch.empty(enc.n_docs + 1, dtype=torch.int64, device=dev)
+    s = enc.stream.cuda_stream
+
+    def call(want=False):
+        return bpe.bpe_decode_batch(enc.handle, enc.d_ids.data_ptr(), n_tok, enc.d_out.data_ptr(), enc.n_docs,
+                                    out.data_ptr(), out.numel(), out_off.data_ptr(), want, s)
+
+    total = call(True)
+    same = bool(total == enc.n_bytes and torch.equal(out[:total], enc.d_data)
+                and np.array_equal(out_off.cpu().numpy(), enc.offsets))
+    for _ in range(3):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(enc.stream)
+        call()
+        b.record(enc.stream)
+    torch.cuda.synchronize()
+    bpe.bpe_sync_status(enc.handle, s)
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    alg = 4 * n_tok + 8 * (enc.n_docs + 1) + enc.n_bytes + 8 * (enc.n_docs + 1)
+    ach = alg / (ms / 1e3) / 1e9
+    return {"ms_per_call": round(ms, 4), "output_mb_per_s": round(enc.n_bytes / (ms / 1e3) / 1e6, 3),
+            "tokens_per_s": round(n_tok / (ms / 1e3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(ach, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(ach / peak, 4), "algorithmic_bytes_per_launch": alg,
+                         "kernel": "k_dec_count..k_dec_write"},
+            "round_trip_identical": same, "gpu_launches_per_call": 5}
+
+
+def train_line(bpe, cfg: int, local: int) -> dict:
+    """bpe_train on the trainer word list of a workload's corpus: wall time of
+    the call (host arrays in, merge rows out), and whether its table equals
+    the host trainer's."""
+    import torch
+    data, offsets, counts = workloads.train_words(workloads.corpus(cfg))
+    want = workloads.table(cfg)[0]
+    bpe.bpe_train(data[:64], np.array([0, min(64, data.size)], np.int64), np.ones(1, np.int64), 4, local)  # warm-up
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    got = bpe.bpe_train(data, offsets, counts, workloads.n_merges(cfg), local)
+    wall = time.perf_counter() - t0
+    return {"workload": f"trainer word list of {workloads.NAMES[cfg]}'s corpus", "words": int(len(counts)),
+            "word_bytes": int(data.size), "merges": int(len(got)), "seconds": round(wall, 3),
+            "merges_per_s": round(len(got) / wall, 1),
+            "identical_to_host_trainer": bool(got.shape == want.shape and np.array_equal(got, want))}
 
 
 def run_gpu(args, world, rank, local):
@@ -368,6 +447,7 @@ def run_gpu(args, world, rank, local):
     # the merge loop), timed the same way, outside the headline region.
     bpe.bpe_set_word_cache(handle, False)
     nocache_ms = statistics.median(enc.time_calls(max(1, min(args.steps, 3)), 1))
+    nocache_kernels = enc.kernel_ms()
     bpe.bpe_set_word_cache(handle, True)
 
     # End to end through the C ABI's host-buffer call: page-locked host input,
@@ -391,6 +471,9 @@ def run_gpu(args, world, rank, local):
         host_step()
     e2e_s = (time.perf_counter() - e0) / e2e_steps
     del h_data, h_off, h_ids, h_out
+    dec = decode_line(bpe, enc, max(5, min(args.steps, 20)), peaks()[0]) if rank == 0 else None
+    trn = train_line(bpe, 2, local) if rank == 0 and world == 1 and args.n_docs is None and not args.no_configs \
+        else None
     (step_ms, kern_ms, e2e_s), (all_bytes, all_tokens, all_docs) = reduce_ranks(
         dist, dev, [step_ms, kern_ms, e2e_s], [n_bytes, n_tokens, n_docs])
 
@@ -411,6 +494,7 @@ def run_gpu(args, world, rank, local):
                 e = Encoder(bpe, c, dev, local)
                 ms = statistics.median(e.time_calls(max(10, min(args.steps, 20)), 3))
                 configs[f"C{c}"] = config_line(e, ms, peak)
+                configs[f"C{c}"]["kernel_ms"] = e.kernel_ms()
                 if not args.no_cpu_baseline:
                     ids_c, off_c = e.result()
                     configs[f"C{c}"]["parity"], _ = parity_line(e, ids_c, off_c)
@@ -418,6 +502,7 @@ def run_gpu(args, world, rank, local):
                 del e
                 torch.cuda.empty_cache()
             configs[f"C{cfg}"] = config_line(enc, kern_ms, peak)
+            configs[f"C{cfg}"]["kernel_ms"] = enc.kernel_ms()
             if not args.no_cpu_baseline:
                 par, r = parity_line(enc, head_ids, head_off)
                 configs[f"C{cfg}"]["parity"] = par
@@ -457,7 +542,10 @@ def run_gpu(args, world, rank, local):
                     "d2h_bytes_per_step": 4 * int(n_tokens) + 8 * (n_docs + 1)},
             "without_word_cache": {"value": round(n_bytes / (nocache_ms / 1e3) / 1e6, 3), "unit": "MB/s",
                                    "ms_per_step": round(nocache_ms, 4),
-                                   "hbm_frac": round(alg / (nocache_ms / 1e3) / 1e9 / peak, 4)},
+                                   "hbm_frac": round(alg / (nocache_ms / 1e3) / 1e9 / peak, 4),
+                                   "kernel_ms": nocache_kernels},
+            "decode": dec,
+            "train": trn,
             "configs": configs,
             "gpu_launches": LAUNCHES_PER_CALL * args.steps,
             "clocks": clk,

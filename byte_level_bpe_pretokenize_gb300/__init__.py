@@ -58,8 +58,8 @@ _lock = threading.Lock()
 _lib = None
 
 EXPORTS = ["bpe_build", "bpe_encode_batch", "bpe_encode_batch_host", "bpe_encode_batch_noalloc", "bpe_pretokenize_batch", "bpe_decode_batch", "bpe_set_word_cache",
-           "bpe_set_timing_events", "bpe_sync_status", "bpe_table_info", "bpe_table_monotone", "bpe_merges_monotone",
-           "bpe_workspace_bytes", "bpe_destroy", "bpe_last_error"]
+           "bpe_set_timing_events", "bpe_set_phase_events", "bpe_sync_status", "bpe_table_info", "bpe_table_monotone", "bpe_merges_monotone",
+           "bpe_workspace_bytes", "bpe_train", "bpe_destroy", "bpe_last_error"]
 
 
 def lib():
@@ -88,6 +88,8 @@ def lib():
             L.bpe_set_word_cache.argtypes = [p, ctypes.c_int]
             L.bpe_set_timing_events.restype = ctypes.c_int
             L.bpe_set_timing_events.argtypes = [p, p, p]
+            L.bpe_set_phase_events.restype = ctypes.c_int
+            L.bpe_set_phase_events.argtypes = [p, p, ctypes.c_int]
             L.bpe_sync_status.restype = ctypes.c_int
             L.bpe_sync_status.argtypes = [p, p]
             L.bpe_table_info.restype = ctypes.c_int
@@ -96,6 +98,8 @@ def lib():
             L.bpe_table_monotone.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
             L.bpe_merges_monotone.restype = ctypes.c_int
             L.bpe_merges_monotone.argtypes = [p, i64, i64, ctypes.POINTER(ctypes.c_int)]
+            L.bpe_train.restype = ctypes.c_int
+            L.bpe_train.argtypes = [p, p, p, i64, i64, ctypes.c_int, p, ctypes.POINTER(i64)]
             L.bpe_workspace_bytes.restype = ctypes.c_int
             L.bpe_workspace_bytes.argtypes = [p, ctypes.POINTER(i64)]
             L.bpe_destroy.restype = ctypes.c_int
@@ -175,9 +179,46 @@ def bpe_set_word_cache(handle: int, enable: bool) -> None:
     _check(lib().bpe_set_word_cache(handle, 1 if enable else 0))
 
 
+def bpe_train(word_bytes, word_offsets, word_counts, n_merges: int, device: int = 0):
+    """Merge rows int32[k, 3] (left, right, new_id) trained on the GPU from a
+    word list (host arrays: bytes, offsets[n + 1], counts[n])."""
+    wb = np.ascontiguousarray(word_bytes, dtype=np.uint8)
+    wo = np.ascontiguousarray(word_offsets, dtype=np.int64)
+    wc = np.ascontiguousarray(word_counts, dtype=np.int64)
+    out = np.zeros((max(1, n_merges), 3), dtype=np.int32)
+    made = ctypes.c_int64(0)
+    _check(lib().bpe_train(wb.ctypes.data if wb.size else None, wo.ctypes.data, wc.ctypes.data if wc.size else None,
+                           len(wo) - 1, n_merges, device, out.ctypes.data, ctypes.byref(made)))
+    return out[:made.value].copy()
+
+
 def bpe_set_timing_events(handle: int, ev_start: int | None, ev_stop: int | None) -> None:
-    """cudaEvent_t handles (ints) recorded around the main encode kernel."""
+    """cudaEvent_t handles (ints) recorded before the first and after the
+    last kernel of each encode call."""
     _check(lib().bpe_set_timing_events(handle, ev_start, ev_stop))
+
+
+ENCODE_LAUNCHES = 9
+ENCODE_KERNELS = ("k_prep_docs", "k_prep_long", "k_tiles", "k_misses", "k_giants", "k_scan_tiles",
+                  "k_scan_tile_sums", "k_compact", "k_giant_copy")
+
+
+class PhaseEvents:
+    """ENCODE_LAUNCHES + 1 cudaEvent_t handles (ints) held in a C array that
+    lives as long as this object; bpe_set_phase_events records them around
+    each kernel of the next encode calls."""
+
+    def __init__(self, events: list[int]):
+        if len(events) != ENCODE_LAUNCHES + 1:
+            raise ValueError(f"need {ENCODE_LAUNCHES + 1} events")
+        self.array = (ctypes.c_void_p * len(events))(*events)
+
+
+def bpe_set_phase_events(handle: int, events: "PhaseEvents | None") -> None:
+    if events is None:
+        _check(lib().bpe_set_phase_events(handle, None, 0))
+    else:
+        _check(lib().bpe_set_phase_events(handle, ctypes.cast(events.array, ctypes.c_void_p), len(events.array)))
 
 
 def bpe_sync_status(handle: int, stream: int) -> None:

@@ -755,21 +755,18 @@ __device__ uint32_t merge_group(GroupScratch& W, const uint8_t* src, uint32_t n,
 }
 
 // ------------------------------------------------------------ merge: long --
-// The whole CTA merges one long pre-token in place: its symbols in scr and
-// the rank of each symbol's pair with the next in srk (both the pool range
-// of its own bytes, read and written in rounds of kRound elements; a round
-// writes only below where it read). A step is one pass: the chosen pair is
-// replaced left to right without overlap, and only the pairs that touch a
-// new symbol are looked up again; every other pair keeps its rank. Within a
-// round each thread takes kLongPerThread elements; whether its first element
-// was consumed by the merge before it, and where its kept symbols go, come
-// from one CTA scan of (transfer function, kept count) elements.
-
-constexpr uint32_t kDirty = 0xFFFFFFFEu;  // a new symbol: its pairs are looked up again
+// The whole CTA merges one long pre-token in place in scr (the pool range of
+// its own bytes, read and written in rounds of kRound elements; a round
+// writes only below where it read). A step is one pass: the chosen pair
+// (A, B) is replaced left to right without overlap, and every pair of the
+// new sequence is looked up for the next step's lowest rank (four home
+// buckets in flight a thread). Within a round each thread takes
+// kLongPerThread elements; whether its first element was consumed by the
+// merge before it, and where its kept symbols go, come from one CTA scan of
+// (transfer function, kept count) elements.
 
 struct LongScratch {
   uint32_t* sym;   // [2][kRound]: a round's kept symbols (by round parity)
-  uint32_t* rk;    // [2][kRound]: their old pair ranks, or kDirty
   uint32_t* red;   // [2][kThreads / 32]
   uint32_t* mred;  // [kThreads / 32]
 };
@@ -788,51 +785,42 @@ __device__ __forceinline__ uint32_t tfc_then(uint32_t a, uint32_t b) {
 constexpr uint32_t kTfcIdentity = 2u;
 static_assert(kRound < 2048, "round counts fit in 11 bits");
 
-__device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, int32_t* scr, uint32_t* srk,
-                               const Tables& T, const int32_t* byte_id, LongScratch L) {
+__device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, int32_t* scr, const Tables& T,
+                               const int32_t* byte_id, LongScratch L) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t len = n;
   bool first_pass = true;
-  uint32_t best = kInf, NW = 0;
+  uint32_t A = kNone, B = kNone, NW = 0;  // the pair of this pass (none in the first)
   uint32_t par = 0;
   for (;;) {
-    uint32_t W = 0, carry = 0, prev_sym = kNone, prev_rk = kDirty, local_min = kInf;
+    uint32_t W = 0, carry = 0, prev_sym = kNone, local_min = kInf;
     for (uint32_t r0 = 0; r0 < len; r0 += kRound, par ^= 1u) {
-      uint32_t x[kLongPerThread], r[kLongPerThread];
+      uint32_t x[kLongPerThread + 1];
 #pragma unroll
-      for (int k = 0; k < kLongPerThread; ++k) {
+      for (int k = 0; k <= kLongPerThread; ++k) {
         const uint32_t idx = r0 + (uint32_t)tid * kLongPerThread + (uint32_t)k;
         x[k] = kNone;
-        r[k] = kInf;
-        if (idx < len) {
-          x[k] = first_pass ? (uint32_t)byte_id[g_bytes[s + idx]] : (uint32_t)scr[idx];
-          if (!first_pass && idx + 1 < len) r[k] = srk[idx];
-        }
+        if (idx < len) x[k] = first_pass ? (uint32_t)byte_id[g_bytes[s + idx]] : (uint32_t)scr[idx];
       }
+      bool hit[kLongPerThread];  // (x[k], x[k + 1]) is the pair of this pass
+#pragma unroll
+      for (int k = 0; k < kLongPerThread; ++k) hit[k] = !first_pass && x[k] == A && x[k + 1] == B;
       // this thread's part for both inputs: consumed out, symbols kept
-      uint32_t e = kTfcIdentity;
-      if (!first_pass) {
-        e = 0;
+      uint32_t e = 0;
 #pragma unroll
-        for (uint32_t in = 0; in < 2; ++in) {
-          uint32_t consumed = in, kept = 0;
+      for (uint32_t in = 0; in < 2; ++in) {
+        uint32_t consumed = in, kept = 0;
 #pragma unroll
-          for (int k = 0; k < kLongPerThread; ++k) {
-            if (x[k] == kNone) break;
-            if (consumed) {
-              consumed = 0;
-            } else {
-              ++kept;
-              consumed = r[k] == best;
-            }
+        for (int k = 0; k < kLongPerThread; ++k) {
+          if (x[k] == kNone) break;
+          if (consumed) {
+            consumed = 0;
+          } else {
+            ++kept;
+            consumed = hit[k];
           }
-          e |= consumed << in | kept << (in ? 13 : 2);
         }
-      } else {
-        uint32_t kept = 0;
-#pragma unroll
-        for (int k = 0; k < kLongPerThread; ++k) kept += x[k] != kNone;
-        e = kTfcIdentity | kept << 2 | kept << 13;
+        e |= consumed << in | kept << (in ? 13 : 2);
       }
       // CTA scan of the parts, one barrier
       uint32_t incl = e;
@@ -861,71 +849,56 @@ __device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, in
       uint32_t pos = carry ? (before >> 13) & 0x7FFu : (before >> 2) & 0x7FFu;
       const uint32_t round_cnt = carry ? (all >> 13) & 0x7FFu : (all >> 2) & 0x7FFu;
       carry = (all >> carry) & 1u;
-      // kept symbols with their old pair ranks (kDirty for a new symbol)
+      // the kept symbols, in order (a buffer per round parity, so the next
+      // round's writes need no barrier after this round's reads)
       uint32_t* st_sym = L.sym + par * kRound;
-      uint32_t* st_rk = L.rk + par * kRound;
 #pragma unroll
       for (int k = 0; k < kLongPerThread; ++k) {
         if (x[k] == kNone) break;
         if (consumed) {
           consumed = 0;
-        } else if (!first_pass && r[k] == best) {
-          st_sym[pos] = NW;
-          st_rk[pos] = kDirty;
-          ++pos;
+        } else if (hit[k]) {
+          st_sym[pos++] = NW;
           consumed = 1;
         } else {
-          st_sym[pos] = x[k];
-          st_rk[pos] = first_pass ? kDirty : r[k];
-          ++pos;
+          st_sym[pos++] = x[k];
         }
       }
       cta_sync();
-      // pairs (q - 1, q) of the new sequence: a pair of two old symbols keeps
-      // its rank (they were adjacent before); the others are looked up, with
-      // their home buckets loaded together
+      // the round's pairs (q - 1, q), kLongPerThread per thread with their
+      // home buckets loaded together
       {
-        uint32_t lf[kLongPerThread], rt[kLongPerThread], bk[kLongPerThread], rank[kLongPerThread];
-        bool need[kLongPerThread];
+        uint32_t lf[kLongPerThread], rt[kLongPerThread], bk[kLongPerThread];
         uint4 u[kLongPerThread], v[kLongPerThread];
 #pragma unroll
         for (int k = 0; k < kLongPerThread; ++k) {
           const uint32_t q = (uint32_t)tid + (uint32_t)k * kThreads;
           lf[k] = kNone;
           rt[k] = 0;
-          rank[k] = kInf;
-          need[k] = false;
           if (q < round_cnt) {
             lf[k] = q == 0 ? prev_sym : st_sym[q - 1];
-            const uint32_t lrk = q == 0 ? prev_rk : st_rk[q - 1];
             rt[k] = st_sym[q];
             scr[W + q] = (int32_t)rt[k];
-            need[k] = lf[k] != kNone && (lrk == kDirty || st_rk[q] == kDirty);
-            rank[k] = lrk;
           }
           bk[k] = pair_hash(lf[k], rt[k]) & T.hmask;
-          if (need[k]) ldg32(T.ht + 2ull * bk[k], u[k], v[k]);
+          if (lf[k] != kNone) ldg32(T.ht + 2ull * bk[k], u[k], v[k]);
         }
 #pragma unroll
         for (int k = 0; k < kLongPerThread; ++k) {
           if (lf[k] == kNone) continue;
-          const uint32_t q = (uint32_t)tid + (uint32_t)k * kThreads;
           uint32_t nw;
-          if (need[k]) rank[k] = lookup_pair_from(T, lf[k], rt[k], bk[k], u[k], v[k], &nw);
-          srk[W + q - 1] = rank[k];
-          local_min = min(local_min, rank[k]);
+          local_min = min(local_min, lookup_pair_from(T, lf[k], rt[k], bk[k], u[k], v[k], &nw));
         }
       }
-      if (round_cnt > 0) {
-        prev_sym = st_sym[round_cnt - 1];
-        prev_rk = st_rk[round_cnt - 1];
-      }
+      if (round_cnt > 0) prev_sym = st_sym[round_cnt - 1];
       W += round_cnt;
     }
     len = W;
     first_pass = false;
-    best = block_min(local_min, L.mred);
+    const uint32_t best = block_min(local_min, L.mred);
     if (best == kInf) break;
+    A = (uint32_t)T.mrows[3 * best];
+    B = (uint32_t)T.mrows[3 * best + 1];
     NW = (uint32_t)T.mrows[3 * best + 2];
   }
   cta_sync();
@@ -951,6 +924,7 @@ __device__ __forceinline__ uint32_t cache_slot(const CacheKey& K, uint32_t len, 
 
 #include "tiles.cuh"
 #include "decode.cuh"
+#include "train.cuh"
 
 namespace {
 
@@ -1040,6 +1014,7 @@ struct bpe_handle {
   size_t ws_bytes = 0;
   bool smem_set = false;
   cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
+  cudaEvent_t* ev_phase = nullptr;  // BPE_ENCODE_LAUNCHES + 1 caller-owned events, or null
   // bpe_encode_batch_host: kHostSlots slots of device buffers, copy streams,
   // events
   static constexpr int kHostSlots = 4;
@@ -1193,7 +1168,7 @@ struct WsSizes {
 constexpr WsSizes ws_sizes(int64_t n_bytes) {
   WsSizes z{};
   z.n_tiles = n_bytes / kTileOwn + 1;
-  z.miss_cap = n_bytes / 2 + 64;  // a miss has at least 2 bytes; k_giants reuses the queue as u32[n_bytes]
+  z.miss_cap = n_bytes / 2 + 64;  // a miss has at least 2 bytes
   z.giant_cap = n_bytes / (kShortMax + 1) + z.n_tiles + 16;
   z.range_cap = z.n_tiles / kPrepSpan + 16;
   z.first_doc = align256((size_t)z.n_tiles * sizeof(int64_t));
@@ -1260,10 +1235,11 @@ int tiles_smem_setup() {
 // The per-call kernels on stream st: k_prep_docs, k_prep_long, k_tiles,
 // k_misses, k_giants (which returns at once when nothing was deferred), the
 // scan, k_compact and k_giant_copy (which returns at once when nothing was
-// deferred). ev_start / ev_stop (may be null) bracket all of them.
+// deferred). ev_start / ev_stop (may be null) bracket all of them; ev_phase
+// (may be null) gets one event before the first and one after each.
 int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
                   int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets, cudaStream_t st,
-                  cudaEvent_t ev_start, cudaEvent_t ev_stop);
+                  cudaEvent_t ev_start, cudaEvent_t ev_stop, cudaEvent_t* ev_phase);
 }  // namespace
 
 // ---------------------------------------------- fixed scratch of the no-alloc encode --
@@ -1303,16 +1279,20 @@ int noalloc_setup(int dev, unsigned char** base) {
 namespace {
 int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_bytes, const int64_t* d_doc_offsets,
                   int64_t n_docs, int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets, cudaStream_t st,
-                  cudaEvent_t ev_start, cudaEvent_t ev_stop) {
+                  cudaEvent_t ev_start, cudaEvent_t ev_stop, cudaEvent_t* ev_phase) {
   if (ev_start) CK(cudaEventRecord(ev_start, st));
+  int phase = 0;  // bpe_set_phase_events
+  if (ev_phase) CK(cudaEventRecord(ev_phase[phase++], st));
   const int64_t n_tiles = w.n_tiles;
   const int prep_blocks = (int)std::min<int64_t>(4096, (n_docs + 2) / 256 + 1);
   k_prep_docs<<<prep_blocks, 256, 0, st>>>(d_doc_offsets, n_docs, n_bytes, n_tiles, w.first_doc, w.ranges,
                                            w.range_cap, h->d_small);
   CK(cudaGetLastError());
+  if (ev_phase) CK(cudaEventRecord(ev_phase[phase++], st));
   k_prep_long<<<(unsigned)std::min<int64_t>(2 * h->n_sms, w.range_cap), 256, 0, st>>>(w.ranges, w.range_cap,
                                                                                     w.first_doc, n_tiles, h->d_small);
   CK(cudaGetLastError());
+  if (ev_phase) CK(cudaEventRecord(ev_phase[phase++], st));
   TileArgs a;
   a.bytes = d_bytes;
   a.n_bytes = n_bytes;
@@ -1333,28 +1313,33 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
   const int64_t grid = std::min<int64_t>((int64_t)kTileCtasPerSm * h->n_sms, (n_tiles + kTileWarps - 1) / kTileWarps);
   k_tiles<<<(unsigned)grid, kTileThreads, kTileSmemBytes, st>>>(a);
   CK(cudaGetLastError());
+  if (ev_phase) CK(cudaEventRecord(ev_phase[phase++], st));
   k_misses<<<(unsigned)(kMissBlocksPerSm * h->n_sms), kMissThreads, 0, st>>>(d_bytes, w.misses, w.miss_cap, w.stage,
                                                                             w.rec, a.T, h->d_small);
   CK(cudaGetLastError());
-  // the miss queue is dead once k_misses has run: k_giants keeps its pair
-  // ranks there (u32 per input byte; the queue holds 8 bytes per 2)
+  if (ev_phase) CK(cudaEventRecord(ev_phase[phase++], st));
   k_giants<<<(unsigned)(8 * h->n_sms), kGiantThreads, 0, st>>>(d_bytes, w.giants, w.giant_cap, w.first_start, n_tiles,
-                                                            w.rec, w.pool, reinterpret_cast<uint32_t*>(w.misses), a.T,
-                                                            h->d_small);
+                                                            w.rec, w.pool, a.T, h->d_small);
   CK(cudaGetLastError());
+  if (ev_phase) CK(cudaEventRecord(ev_phase[phase++], st));
   const int64_t n_blocks = (n_tiles + kScanThreads - 1) / kScanThreads;
   k_scan_tiles<<<(unsigned)n_blocks, kScanThreads, 0, st>>>(w.rec, n_tiles, w.tile_base, w.block_sum);
   CK(cudaGetLastError());
+  if (ev_phase) CK(cudaEventRecord(ev_phase[phase++], st));
   k_scan_tile_sums<<<1, kScanThreads, 0, st>>>(w.block_sum, n_blocks, h->d_small);
   CK(cudaGetLastError());
+  if (ev_phase) CK(cudaEventRecord(ev_phase[phase++], st));
   k_compact<<<(unsigned)std::min<int64_t>((n_tiles + kCompactWarps - 1) / kCompactWarps, 8 * h->n_sms),
               32 * kCompactWarps, 0, st>>>(w.rec, w.stage, w.tile_base, w.block_sum, w.giants, w.giant_cap,
                                           d_doc_offsets, n_tiles, d_out_ids, out_capacity, d_out_offsets, h->d_small);
   CK(cudaGetLastError());
+  if (ev_phase) CK(cudaEventRecord(ev_phase[phase++], st));
   k_giant_copy<<<(unsigned)(4 * h->n_sms), kCopyThreads, 0, st>>>(w.giants, w.giant_cap, w.pool, d_out_ids,
                                                                   out_capacity, h->d_small);
   CK(cudaGetLastError());
+  if (ev_phase) CK(cudaEventRecord(ev_phase[phase++], st));
   if (ev_stop) CK(cudaEventRecord(ev_stop, st));
+  static_assert(BPE_ENCODE_LAUNCHES == 9, "the launches above");
   return BPE_OK;
 }
 }  // namespace
@@ -1515,6 +1500,13 @@ int bpe_set_timing_events(bpe_handle* h, void* ev_start, void* ev_stop) {
   return BPE_OK;
 }
 
+int bpe_set_phase_events(bpe_handle* h, void** events, int n) {
+  if (!h || (n != 0 && (n != BPE_ENCODE_LAUNCHES + 1 || !events)))
+    return fail(BPE_ERR_INVALID_ARG, "bpe_set_phase_events: n must be 0 or BPE_ENCODE_LAUNCHES + 1");
+  h->ev_phase = n ? reinterpret_cast<cudaEvent_t*>(events) : nullptr;
+  return BPE_OK;
+}
+
 int bpe_table_info(const bpe_handle* h, int64_t* n_merges, int64_t* n_vocab) {
   if (!h) return fail(BPE_ERR_INVALID_ARG, "null handle");
   if (n_merges) *n_merges = h->n_merges;
@@ -1585,7 +1577,7 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
     h->smem_set = true;
   }
   rc = launch_encode(h, ws_carve(static_cast<unsigned char*>(h->d_ws), n_bytes), d_bytes, n_bytes, d_doc_offsets,
-                     n_docs, d_out_ids, out_capacity, d_out_offsets, st, h->ev_start, h->ev_stop);
+                     n_docs, d_out_ids, out_capacity, d_out_offsets, st, h->ev_start, h->ev_stop, h->ev_phase);
   if (rc) return rc;
   if (h_total_tokens) {
     DevSmall s;
@@ -1617,7 +1609,7 @@ int bpe_encode_batch_noalloc(bpe_handle* h, const uint8_t* d_bytes, int64_t n_by
   if (rc) return rc;
   cudaStream_t st = (cudaStream_t)stream;
   rc = launch_encode(h, ws_carve(base, n_bytes), d_bytes, n_bytes, d_doc_offsets, n_docs, d_out_ids, out_capacity,
-                     d_out_offsets, st, nullptr, nullptr);
+                     d_out_offsets, st, nullptr, nullptr, nullptr);
   if (rc) return rc;
   if (h_total_tokens) {
     DevSmall s;
@@ -1730,7 +1722,7 @@ int bpe_encode_batch_host(bpe_handle* h, const uint8_t* h_bytes, int64_t n_bytes
     k_offsets_shift<<<(unsigned)std::min<int64_t>(1024, nd / 256 + 1), 256, 0, cs>>>(sl.offs, nd + 1, -b0);
     CK(cudaGetLastError());
     int r = launch_encode(h, ws_carve(static_cast<unsigned char*>(h->d_ws), nb), sl.bytes, nb, sl.offs, nd, sl.ids,
-                          nb, sl.out_offs, cs, nullptr, nullptr);
+                          nb, sl.out_offs, cs, nullptr, nullptr, nullptr);
     if (r) return r;
     k_total_to_host<<<1, 32, 0, cs>>>(h->d_small, h->d_totals + j);
     CK(cudaGetLastError());
@@ -1821,6 +1813,105 @@ int bpe_decode_batch(bpe_handle* h, const int32_t* d_ids, int64_t n_ids, const i
     if (s.status) return status_code(s.status);
     if (s.total > out_capacity) return fail(BPE_ERR_CAPACITY, "decoded bytes exceed out_capacity");
   }
+  return BPE_OK;
+}
+
+int bpe_train(const uint8_t* word_bytes, const int64_t* word_offsets, const int64_t* word_counts, int64_t n_words,
+              int64_t n_merges, int device, int32_t* merges_out, int64_t* n_made) {
+  if (n_words < 0 || n_merges < 0 || !word_offsets || (n_words > 0 && !word_counts) || !n_made ||
+      (n_merges > 0 && !merges_out) || (word_offsets[n_words] > 0 && !word_bytes) ||
+      n_merges > (int64_t)(1 << 20) - 256)
+    return fail(BPE_ERR_INVALID_ARG, "bpe_train: bad arguments");
+  if (word_offsets[0] != 0) return fail(BPE_ERR_INVALID_ARG, "bpe_train: word_offsets[0] must be 0");
+  int64_t n_pairs = 0;
+  std::vector<int32_t> len((size_t)std::max<int64_t>(1, n_words));
+  for (int64_t w = 0; w < n_words; ++w) {
+    const int64_t L = word_offsets[w + 1] - word_offsets[w];
+    if (L < 0 || L > INT32_MAX || word_counts[w] < 0)
+      return fail(BPE_ERR_INVALID_ARG, "bpe_train: offsets must not decrease and counts must be >= 0");
+    len[(size_t)w] = (int32_t)L;
+    n_pairs += L > 1 ? L - 1 : 0;
+  }
+  *n_made = 0;
+  if (n_words == 0 || n_merges == 0) return BPE_OK;
+  DeviceGuard g(device);
+  const int64_t n_sym = word_offsets[n_words];
+  std::vector<int32_t> sym((size_t)std::max<int64_t>(1, n_sym));
+  for (int64_t i = 0; i < n_sym; ++i) sym[(size_t)i] = word_bytes[i];  // byte b is symbol b
+  uint64_t n_slots = 1024;
+  while (n_slots < (uint64_t)n_pairs * 2) n_slots <<= 1;
+  int n_sms = 1;
+  CK(cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, device));
+  const unsigned word_grid = (unsigned)std::min<int64_t>((n_words + kTrainThreads - 1) / kTrainThreads, 8 * n_sms);
+  const unsigned slot_grid = (unsigned)std::min<uint64_t>((n_slots + kTrainThreads - 1) / kTrainThreads, 4 * n_sms);
+  const unsigned repl_grid = std::max(word_grid, slot_grid);
+  struct Dev {
+    int32_t* sym = nullptr;
+    int64_t* off = nullptr;
+    int32_t* len = nullptr;
+    int64_t* freq = nullptr;
+    uint64_t* keys = nullptr;
+    unsigned long long* counts = nullptr;
+    unsigned long long* bc = nullptr;
+    unsigned long long* bk = nullptr;
+    TrainState* st = nullptr;
+    int32_t* merges = nullptr;
+    cudaStream_t s = nullptr;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    ~Dev() {
+      if (exec) cudaGraphExecDestroy(exec);
+      if (graph) cudaGraphDestroy(graph);
+      if (s) cudaStreamDestroy(s);
+      cudaFree(sym); cudaFree(off); cudaFree(len); cudaFree(freq); cudaFree(keys); cudaFree(counts);
+      cudaFree(bc); cudaFree(bk); cudaFree(st); cudaFree(merges);
+    }
+  } d;
+  CK(cudaMalloc(&d.sym, sym.size() * sizeof(int32_t)));
+  CK(cudaMalloc(&d.off, (size_t)n_words * sizeof(int64_t)));
+  CK(cudaMalloc(&d.len, (size_t)n_words * sizeof(int32_t)));
+  CK(cudaMalloc(&d.freq, (size_t)n_words * sizeof(int64_t)));
+  CK(cudaMalloc(&d.keys, n_slots * sizeof(uint64_t)));
+  CK(cudaMalloc(&d.counts, n_slots * sizeof(unsigned long long)));
+  CK(cudaMalloc(&d.bc, slot_grid * sizeof(unsigned long long)));
+  CK(cudaMalloc(&d.bk, slot_grid * sizeof(unsigned long long)));
+  CK(cudaMalloc(&d.st, sizeof(TrainState)));
+  CK(cudaMalloc(&d.merges, (size_t)n_merges * 3 * sizeof(int32_t)));
+  CK(cudaStreamCreateWithFlags(&d.s, cudaStreamNonBlocking));
+  CK(cudaMemcpyAsync(d.sym, sym.data(), sym.size() * sizeof(int32_t), cudaMemcpyHostToDevice, d.s));
+  CK(cudaMemcpyAsync(d.off, word_offsets, (size_t)n_words * sizeof(int64_t), cudaMemcpyHostToDevice, d.s));
+  CK(cudaMemcpyAsync(d.len, len.data(), (size_t)n_words * sizeof(int32_t), cudaMemcpyHostToDevice, d.s));
+  CK(cudaMemcpyAsync(d.freq, word_counts, (size_t)n_words * sizeof(int64_t), cudaMemcpyHostToDevice, d.s));
+  CK(cudaMemsetAsync(d.keys, 0xFF, n_slots * sizeof(uint64_t), d.s));
+  CK(cudaMemsetAsync(d.counts, 0, n_slots * sizeof(unsigned long long), d.s));
+  CK(cudaMemsetAsync(d.st, 0, sizeof(TrainState), d.s));
+  // kSteps identical steps per graph launch
+  constexpr int kSteps = 64;
+  CK(cudaStreamBeginCapture(d.s, cudaStreamCaptureModeThreadLocal));
+  for (int k = 0; k < kSteps; ++k) {
+    k_train_count<<<word_grid, kTrainThreads, 0, d.s>>>(d.sym, d.off, d.len, d.freq, n_words, d.keys, d.counts,
+                                                         n_slots - 1, d.st);
+    k_train_best<<<slot_grid, kTrainThreads, 0, d.s>>>(d.keys, d.counts, n_slots, d.bc, d.bk, d.st, d.merges,
+                                                        n_merges);
+    k_train_replace<<<repl_grid, kTrainThreads, 0, d.s>>>(d.sym, d.off, d.len, n_words, d.keys, d.counts, n_slots,
+                                                           d.st);
+  }
+  CK(cudaStreamEndCapture(d.s, &d.graph));
+  CK(cudaGraphInstantiate(&d.exec, d.graph, 0));
+  TrainState hs{};
+  for (int64_t done_steps = 0; done_steps < n_merges;) {
+    // up to 16 graph launches between looks at the state
+    for (int r = 0; r < 16 && done_steps < n_merges; ++r, done_steps += kSteps) CK(cudaGraphLaunch(d.exec, d.s));
+    CK(cudaMemcpyAsync(&hs, d.st, sizeof(TrainState), cudaMemcpyDeviceToHost, d.s));
+    CK(cudaStreamSynchronize(d.s));
+    if (hs.done) break;
+  }
+  CK(cudaMemcpyAsync(&hs, d.st, sizeof(TrainState), cudaMemcpyDeviceToHost, d.s));
+  CK(cudaStreamSynchronize(d.s));
+  const int64_t made = std::min<int64_t>(hs.made, n_merges);
+  if (made > 0)
+    CK(cudaMemcpy(merges_out, d.merges, (size_t)made * 3 * sizeof(int32_t), cudaMemcpyDeviceToHost));
+  *n_made = made;
   return BPE_OK;
 }
 

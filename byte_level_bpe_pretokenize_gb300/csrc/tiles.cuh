@@ -745,11 +745,9 @@ __global__ void k_prep_long(const PrepRange* ranges, int64_t range_cap, int64_t*
 constexpr int kGiantThreads = kThreads;
 __global__ void __launch_bounds__(kGiantThreads) k_giants(const uint8_t* bytes, GiantRec* giants, int64_t giant_cap,
                                                           const int64_t* first_start, int64_t n_tiles, TileRec* rec,
-                                                          int32_t* pool, uint32_t* pool_rank, Tables T,
-                                                          DevSmall* small) {
+                                                          int32_t* pool, Tables T, DevSmall* small) {
   __shared__ int32_t byte_id[256];
   __shared__ uint32_t st_sym[2 * kRound];
-  __shared__ uint32_t st_rk[2 * kRound];
   __shared__ uint32_t red[2 * (kThreads / 32)];
   __shared__ uint32_t mred[kThreads / 32];
   __shared__ unsigned long long next;
@@ -758,7 +756,7 @@ __global__ void __launch_bounds__(kGiantThreads) k_giants(const uint8_t* bytes, 
                                                                                : (unsigned long long)giant_cap;
   if (n == 0) return;
   for (int i = threadIdx.x; i < 256; i += kGiantThreads) byte_id[i] = T.byte_id[i];
-  LongScratch L{st_sym, st_rk, red, mred};
+  LongScratch L{st_sym, red, mred};
   for (;;) {
     if (threadIdx.x == 0) next = atomicAdd(&small->giant_ctr, 1ull);
     __syncthreads();
@@ -783,8 +781,7 @@ __global__ void __launch_bounds__(kGiantThreads) k_giants(const uint8_t* bytes, 
         R.end = R.start + 1;
       }
     }
-    const uint32_t cnt =
-        merge_long(bytes, R.start, (uint32_t)(R.end - R.start), pool + R.start, pool_rank + R.start, T, byte_id, L);
+    const uint32_t cnt = merge_long(bytes, R.start, (uint32_t)(R.end - R.start), pool + R.start, T, byte_id, L);
     if (threadIdx.x == 0) {
       giants[g].count = cnt;
       atomicAdd(&rec[R.tile].extra, cnt - 1u);
@@ -885,7 +882,7 @@ struct CompactState {
 // tile's end.
 constexpr int kCompactPart = 512;
 
-__global__ void __launch_bounds__(32 * kCompactWarps, 4) k_compact(const TileRec* rec, const uint32_t* stage,
+__global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* rec, const uint32_t* stage,
                                                                 const uint64_t* tile_base, const uint64_t* block_sum,
                                                                 GiantRec* giants, int64_t giant_cap,
                                                                 const int64_t* doc_offsets, int64_t n_tiles,
@@ -893,8 +890,6 @@ __global__ void __launch_bounds__(32 * kCompactWarps, 4) k_compact(const TileRec
                                                                 int64_t* out_offsets, DevSmall* small) {
   __shared__ __align__(16) uint32_t ent_all[kCompactWarps][kCompactPart];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned long long n_giants = small->n_giants < (unsigned long long)giant_cap ? small->n_giants
-                                                                                      : (unsigned long long)giant_cap;
   uint32_t* ent = ent_all[warp];
   const int64_t warps = (int64_t)gridDim.x * kCompactWarps;
   bool over = false;
@@ -935,7 +930,8 @@ __global__ void __launch_bounds__(32 * kCompactWarps, 4) k_compact(const TileRec
         bool ph = false;
         if (pb != 0xFFFFFFFFu) {
           const bool valid = (e & (kIdSpecial | kIdLong)) != kIdSpecial;
-          ph = valid && !plain && (e & kIdIndex) < n_giants;
+          const unsigned long long n_giants = small->n_giants;  // records written: min(this, giant_cap)
+          ph = valid && !plain && (e & kIdIndex) < n_giants && (e & kIdIndex) < (unsigned long long)giant_cap;
           if (valid && !plain && !ph) atomicOr(&small->status, kStInternal);
           const uint32_t n_ids = (!valid || (!plain && !ph)) ? 0u : (ph ? giants[e & kIdIndex].count : 1u);
           const uint32_t incl = warp_scan_incl(n_ids);

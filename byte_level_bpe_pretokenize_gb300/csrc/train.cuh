@@ -1,0 +1,178 @@
+// Training: the merge table from a word list ("Tokenisierung", section "Byte
+// Pair Encoding schrittweise": count the adjacent pairs, take the most
+// frequent, ties to the smallest ids, replace it everywhere, count again).
+//
+// Included once by bpe_kernels.cu; not a standalone header.
+//
+// The words are the distinct pre-tokens of a corpus with their counts. Byte b
+// starts as symbol b; merge k makes symbol 256 + k and has rank k. One step,
+// all on the device and without a host round trip:
+//   * k_train_count: a thread per word adds the word's count to every
+//     adjacent pair of its symbols in an open-addressed pair histogram
+//     (64-bit key left << 32 | right, 64-bit count; atomicCAS claims a slot).
+//   * k_train_best: the histogram's most frequent pair, ties to the smallest
+//     (left, right): block reductions, then the last CTA to finish reduces
+//     the block results, appends the merge row and clears nothing else. With
+//     no pair left it sets the done flag and later steps return at once.
+//   * k_train_replace: a thread per word replaces the pair left to right
+//     without overlap and compacts the word in place; it also empties the
+//     histogram for the next step (grid-stride).
+// Every step is the same three launches with the same arguments, so the host
+// captures a run of steps in a CUDA graph once and replays it.
+
+namespace {
+
+constexpr uint64_t kTrainEmpty = ~0ull;
+constexpr int kTrainThreads = 256;
+
+struct TrainState {
+  unsigned long long best_count;
+  unsigned long long best_key;
+  unsigned int blocks_done;
+  int done;        // no pair left, or n_merges made: later steps return at once
+  int merged_now;  // this step made a merge (k_train_replace applies it)
+  long long made;
+};
+
+__device__ __forceinline__ uint32_t train_hash(uint64_t k) {
+  return mix32((uint32_t)k * 0x9E3779B1u ^ mix32((uint32_t)(k >> 32)));
+}
+
+// (count, key) order: larger count first, then smaller key.
+__device__ __forceinline__ bool train_better(uint64_t c1, uint64_t k1, uint64_t c2, uint64_t k2) {
+  return c1 > c2 || (c1 == c2 && k1 < k2);
+}
+
+__global__ void __launch_bounds__(kTrainThreads) k_train_count(const int32_t* sym, const int64_t* off,
+                                                               const int32_t* len, const int64_t* freq,
+                                                               int64_t n_words, uint64_t* keys,
+                                                               unsigned long long* counts, uint64_t mask,
+                                                               TrainState* st) {
+  if (st->done) return;
+  for (int64_t w = (int64_t)blockIdx.x * kTrainThreads + threadIdx.x; w < n_words;
+       w += (int64_t)gridDim.x * kTrainThreads) {
+    const int32_t* s = sym + off[w];
+    const int32_t n = len[w];
+    const unsigned long long f = (unsigned long long)freq[w];
+    for (int32_t i = 0; i + 1 < n; ++i) {
+      const uint64_t key = (uint64_t)(uint32_t)s[i] << 32 | (uint32_t)s[i + 1];
+      uint64_t h = train_hash(key) & mask;
+      for (uint64_t probe = 0; probe <= mask; ++probe) {
+        const unsigned long long prev =
+            atomicCAS(reinterpret_cast<unsigned long long*>(keys + h), (unsigned long long)kTrainEmpty,
+                      (unsigned long long)key);
+        if (prev == kTrainEmpty || prev == key) {
+          atomicAdd(counts + h, f);
+          break;
+        }
+        h = (h + 1) & mask;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTrainThreads) k_train_best(const uint64_t* keys, const unsigned long long* counts,
+                                                              uint64_t n_slots, unsigned long long* block_count,
+                                                              unsigned long long* block_key, TrainState* st,
+                                                              int32_t* merges, int64_t n_merges) {
+  __shared__ unsigned long long sc[kTrainThreads / 32], sk[kTrainThreads / 32];
+  __shared__ bool last;
+  if (st->done) return;
+  uint64_t bc = 0, bk = kTrainEmpty;
+  for (uint64_t i = (uint64_t)blockIdx.x * kTrainThreads + threadIdx.x; i < n_slots;
+       i += (uint64_t)gridDim.x * kTrainThreads) {
+    const uint64_t k = keys[i];
+    if (k == kTrainEmpty) continue;
+    const uint64_t c = counts[i];
+    if (train_better(c, k, bc, bk)) {
+      bc = c;
+      bk = k;
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    const uint64_t oc = __shfl_xor_sync(0xFFFFFFFFu, bc, d), ok = __shfl_xor_sync(0xFFFFFFFFu, bk, d);
+    if (train_better(oc, ok, bc, bk)) {
+      bc = oc;
+      bk = ok;
+    }
+  }
+  if (lane == 0) {
+    sc[warp] = bc;
+    sk[warp] = bk;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kTrainThreads / 32; ++w)
+      if (train_better(sc[w], sk[w], bc, bk)) {
+        bc = sc[w];
+        bk = sk[w];
+      }
+    block_count[blockIdx.x] = bc;
+    block_key[blockIdx.x] = bk;
+    __threadfence();
+    last = atomicAdd(&st->blocks_done, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last || threadIdx.x != 0) return;
+  // the last CTA: every block result is visible (each was fenced before its
+  // counter increment)
+  __threadfence();
+  bc = 0;
+  bk = kTrainEmpty;
+  for (unsigned b = 0; b < gridDim.x; ++b) {
+    const uint64_t c = *reinterpret_cast<volatile unsigned long long*>(block_count + b);
+    const uint64_t k = *reinterpret_cast<volatile unsigned long long*>(block_key + b);
+    if (train_better(c, k, bc, bk)) {
+      bc = c;
+      bk = k;
+    }
+  }
+  st->blocks_done = 0;
+  st->merged_now = 0;
+  if (bc == 0 || st->made >= n_merges) {
+    st->done = 1;
+    return;
+  }
+  const long long m = st->made;
+  merges[3 * m] = (int32_t)(bk >> 32);
+  merges[3 * m + 1] = (int32_t)(uint32_t)bk;
+  merges[3 * m + 2] = 256 + (int32_t)m;
+  st->best_count = bc;
+  st->best_key = bk;
+  st->made = m + 1;
+  st->merged_now = 1;
+}
+
+__global__ void __launch_bounds__(kTrainThreads) k_train_replace(int32_t* sym, const int64_t* off, int32_t* len,
+                                                                 int64_t n_words, uint64_t* keys,
+                                                                 unsigned long long* counts, uint64_t n_slots,
+                                                                 const TrainState* st) {
+  // the histogram is cleared for the next step (every step ends here)
+  for (uint64_t i = (uint64_t)blockIdx.x * kTrainThreads + threadIdx.x; i < n_slots;
+       i += (uint64_t)gridDim.x * kTrainThreads) {
+    keys[i] = kTrainEmpty;
+    counts[i] = 0;
+  }
+  if (!st->merged_now) return;  // no merge was made by this step
+  const int32_t a = (int32_t)(st->best_key >> 32), b = (int32_t)(uint32_t)st->best_key;
+  const int32_t nw = 256 + (int32_t)(st->made - 1);
+  for (int64_t w = (int64_t)blockIdx.x * kTrainThreads + threadIdx.x; w < n_words;
+       w += (int64_t)gridDim.x * kTrainThreads) {
+    int32_t* s = sym + off[w];
+    const int32_t n = len[w];
+    int32_t m = 0;
+    for (int32_t i = 0; i < n;) {
+      if (i + 1 < n && s[i] == a && s[i + 1] == b) {
+        s[m++] = nw;
+        i += 2;
+      } else {
+        s[m++] = s[i++];
+      }
+    }
+    len[w] = m;
+  }
+}
+
+}  // namespace

@@ -243,13 +243,52 @@ int bpe_set_word_cache(bpe_handle* h, int enable);
  * bpe_set_timing_events — measurement hook. ev_start and ev_stop are two
  * cudaEvent_t created by the caller on the handle's device. When they are
  * non-NULL, the next bpe_encode_batch calls record them on the call's stream:
- *   - ev_start right after the first (bookkeeping) kernel;
+ *   - ev_start right before the first kernel;
  *   - ev_stop right after the last kernel.
- * So the caller times the split, encode, miss-merge, scan and compaction
- * kernels together.
+ * So the caller times all BPE_ENCODE_LAUNCHES kernels of a call together.
  * NULL, NULL switches it off.
  */
 int bpe_set_timing_events(bpe_handle* h, void* ev_start, void* ev_stop);
+
+/*
+ * bpe_set_phase_events — measurement hook for the time of each kernel.
+ * events is an array of BPE_ENCODE_LAUNCHES + 1 cudaEvent_t created by the
+ * caller on the handle's device (the handle keeps the pointer, not a copy:
+ * the array must outlive its use). While set, bpe_encode_batch records
+ * events[0] before its first kernel and events[i] right after its i-th, in
+ * this order: k_prep_docs, k_prep_long, k_tiles, k_misses, k_giants,
+ * k_scan_tiles, k_scan_tile_sums, k_compact, k_giant_copy. n = 0 (events may
+ * be NULL) switches it off; any other n than BPE_ENCODE_LAUNCHES + 1 is
+ * BPE_ERR_INVALID_ARG.
+ */
+#define BPE_ENCODE_LAUNCHES 9
+int bpe_set_phase_events(bpe_handle* h, void** events, int n);
+
+/*
+ * bpe_train — the merge table of a word list, trained on the GPU
+ * ("Tokenisierung", section "Byte Pair Encoding schrittweise": count the
+ * adjacent pairs, take the most frequent, ties broken deterministically by
+ * the smallest ids, replace it, count again). Byte b is symbol b; merge k
+ * makes symbol 256 + k and has rank k. Each step counts every adjacent pair
+ * of every word, weighted by the word's count, in a device hash histogram,
+ * takes the pair with the largest count (ties: the smallest (left, right)),
+ * and replaces it in every word left to right without overlap. Training stops
+ * after n_merges merges or when no pair is left.
+ *
+ *   word_bytes     host uint8, the words back to back (the distinct
+ *                  pre-tokens of a corpus).
+ *   word_offsets   host int64[n_words + 1], word_offsets[0] = 0,
+ *                  non-decreasing.
+ *   word_counts    host int64[n_words] >= 0, occurrences of each word.
+ *   n_merges       merges wanted (<= 2^20 - 256).
+ *   device         CUDA device ordinal; the call allocates, runs on its own
+ *                  stream and frees everything before it returns.
+ *   merges_out     host int32[n_merges][3]: rows (left, right, new_id).
+ *   n_made         host int64*: merges made (<= n_merges).
+ * Errors: BPE_ERR_INVALID_ARG for bad arguments, BPE_ERR_CUDA.
+ */
+int bpe_train(const uint8_t* word_bytes, const int64_t* word_offsets, const int64_t* word_counts, int64_t n_words,
+              int64_t n_merges, int device, int32_t* merges_out, int64_t* n_made);
 
 /* Waits for the stream and returns (then clears) errors the kernels of
  * earlier calls on this handle recorded. */

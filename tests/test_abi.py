@@ -129,3 +129,17 @@ def test_merges_monotone_host_only(bpe):
     assert bpe.bpe_merges_monotone(m, len(vo) - 1)
     with pytest.raises(bpe.BpeError):
         bpe.bpe_merges_monotone(np.array([[1, 2, 999]], np.int32), 300)
+
+
+def test_measurement_hooks_check_their_arguments(bpe):
+    L = bpe.lib()
+    # a null handle, and a wrong event count, are rejected before anything is kept
+    assert L.bpe_set_phase_events(None, None, 0) == 1
+    assert L.bpe_set_timing_events(None, None, None) == 1
+    assert bpe.ENCODE_LAUNCHES == len(bpe.ENCODE_KERNELS)
+    hdr = open(os.path.join(ROOT, "include", "bpe_gb300.h")).read()
+    assert f"#define BPE_ENCODE_LAUNCHES {bpe.ENCODE_LAUNCHES}" in hdr
+    # the kernel order the header states is the binding's
+    assert ", ".join(bpe.ENCODE_KERNELS) in " ".join(hdr.replace("*", " ").split())
+    with pytest.raises(ValueError):
+        bpe.PhaseEvents([0] * 3)

@@ -95,3 +95,14 @@ def test_table_vocab_is_consistent():
     for a, b, c in m.tolist():
         assert toks[c] == toks[a] + toks[b]
         assert c == 256 + m.tolist().index([a, b, c])
+
+
+def test_train_words_tile_the_corpus():
+    text = workloads.corpus(2)[:200_000]
+    data, offsets, counts = workloads.train_words(text)
+    words = [bytes(data[offsets[i]:offsets[i + 1]]) for i in range(len(counts))]
+    assert len(set(words)) == len(words) and all(words)
+    assert int((np.diff(offsets) * counts).sum()) == text.size
+    # the host trainer on the corpus equals the naive recount on the word list
+    pieces = [w for w, c in zip(words, counts) for _ in range(int(c))]
+    assert workloads.train(text, 40).tolist() == naive_train(pieces, 40).tolist()

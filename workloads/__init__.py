@@ -74,6 +74,8 @@ def _load():
             lib.wl_docs.argtypes = [ctypes.c_int, ctypes.c_uint64, i64, i64, p, p]
             lib.wl_train.restype = i64
             lib.wl_train.argtypes = [p, i64, i64, p]
+            lib.wl_train_words.restype = i64
+            lib.wl_train_words.argtypes = [p, i64, ctypes.POINTER(i64), p, p, p]
             for f in ("wl_cfg_corpus_bytes", "wl_cfg_n_merges", "wl_cfg_n_docs"):
                 getattr(lib, f).restype = i64
                 getattr(lib, f).argtypes = [ctypes.c_int]
@@ -154,6 +156,21 @@ def docs(cfg: int, first: int = 0, count: int | None = None, seed: int | None = 
     if r < 0:
         raise RuntimeError("document generation failed")
     return data, offsets
+
+
+def train_words(text: np.ndarray) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """The trainer's word list of a corpus: (bytes uint8, offsets int64[n+1],
+    counts int64[n]) of its distinct pre-tokens, first-seen order."""
+    lib = _load()
+    text = np.ascontiguousarray(text, dtype=np.uint8)
+    total = ctypes.c_int64(0)
+    n = lib.wl_train_words(_ptr(text) if text.size else 0, text.size, ctypes.byref(total), None, None, None)
+    data = np.zeros(max(1, total.value), np.uint8)
+    offsets = np.zeros(n + 1, np.int64)
+    counts = np.zeros(max(1, n), np.int64)
+    lib.wl_train_words(_ptr(text) if text.size else 0, text.size, ctypes.byref(total), _ptr(data), _ptr(offsets),
+                       _ptr(counts))
+    return data[:total.value], offsets, counts[:n]
 
 
 def train(text: np.ndarray, merges: int) -> np.ndarray:

@@ -459,12 +459,15 @@ int64_t wl_docs(int cfg, uint64_t seed, int64_t k0, int64_t n, int64_t* lens, ui
   return bad ? -1 : total;
 }
 
-// BPE trainer over a corpus: writes up to n_merges rows (left, right, new_id)
-// to merges_out and returns the number of merges made.
-int64_t wl_train(const uint8_t* corpus, int64_t n, int64_t n_merges, int32_t* merges_out) {
+}  // extern "C"
+
+namespace {
+// The trainer's words: the distinct pre-tokens of the corpus (first-seen
+// order) as byte-symbol sequences, with how often each occurs.
+void trainer_words(const uint8_t* corpus, int64_t n, std::vector<std::vector<int32_t>>& words,
+                   std::vector<int64_t>& freq) {
   std::vector<Unit> u = trainer_units(corpus, n);
   std::unordered_map<std::string, int32_t> index;
-  Trainer t;
   size_t i = 0;
   while (i < u.size()) {
     size_t j = i;
@@ -484,17 +487,51 @@ int64_t wl_train(const uint8_t* corpus, int64_t n, int64_t n_merges, int32_t* me
     std::string w((const char*)corpus + a, (size_t)(b - a));
     auto it = index.find(w);
     if (it == index.end()) {
-      index.emplace(w, (int32_t)t.words.size());
+      index.emplace(w, (int32_t)words.size());
       std::vector<int32_t> syms;
       for (int64_t q = a; q < b; ++q) syms.push_back((int32_t)corpus[q]);
-      t.words.push_back(std::move(syms));
-      t.freq.push_back(1);
+      words.push_back(std::move(syms));
+      freq.push_back(1);
     } else {
-      t.freq[(size_t)it->second] += 1;
+      freq[(size_t)it->second] += 1;
     }
     i = j;
   }
+}
+}  // namespace
+
+extern "C" {
+
+// BPE trainer over a corpus: writes up to n_merges rows (left, right, new_id)
+// to merges_out and returns the number of merges made.
+int64_t wl_train(const uint8_t* corpus, int64_t n, int64_t n_merges, int32_t* merges_out) {
+  Trainer t;
+  trainer_words(corpus, n, t.words, t.freq);
   return t.run(n_merges, merges_out);
+}
+
+// The trainer's word list of a corpus: returns the number of words and sets
+// *total_bytes; when bytes is non-null also writes the words' bytes back to
+// back, offsets[n_words + 1] and counts[n_words] (size them from a first call
+// with bytes == nullptr).
+int64_t wl_train_words(const uint8_t* corpus, int64_t n, int64_t* total_bytes, uint8_t* bytes, int64_t* offsets,
+                       int64_t* counts) {
+  std::vector<std::vector<int32_t>> words;
+  std::vector<int64_t> freq;
+  trainer_words(corpus, n, words, freq);
+  int64_t total = 0;
+  for (const auto& w : words) total += (int64_t)w.size();
+  *total_bytes = total;
+  if (bytes) {
+    int64_t at = 0;
+    offsets[0] = 0;
+    for (size_t k = 0; k < words.size(); ++k) {
+      for (int32_t b : words[k]) bytes[at++] = (uint8_t)b;
+      offsets[k + 1] = at;
+      counts[k] = freq[k];
+    }
+  }
+  return (int64_t)words.size();
 }
 
 // FNV-1a 64 over n bytes, continuing from state h (start with
