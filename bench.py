@@ -445,9 +445,15 @@ def run_gpu(args, world, rank, local):
 
     # Secondary: the same calls with the word cache off (every pre-token runs
     # the merge loop), timed the same way, outside the headline region.
+    # With the cache off the per-call memo of the misses is on by default;
+    # the merge path alone is timed with the memo off too.
     bpe.bpe_set_word_cache(handle, False)
     nocache_ms = statistics.median(enc.time_calls(max(1, min(args.steps, 3)), 1))
     nocache_kernels = enc.kernel_ms()
+    bpe.bpe_set_call_memo(handle, bpe.MEMO_OFF)
+    nomemo_ms = statistics.median(enc.time_calls(max(1, min(args.steps, 3)), 1))
+    nomemo_kernels = enc.kernel_ms()
+    bpe.bpe_set_call_memo(handle, bpe.MEMO_AUTO)
     bpe.bpe_set_word_cache(handle, True)
 
     # End to end through the C ABI's host-buffer call: page-locked host input,
@@ -495,6 +501,10 @@ def run_gpu(args, world, rank, local):
                 ms = statistics.median(e.time_calls(max(10, min(args.steps, 20)), 3))
                 configs[f"C{c}"] = config_line(e, ms, peak)
                 configs[f"C{c}"]["kernel_ms"] = e.kernel_ms()
+                if c == 2:  # the per-call memo forced on where the misses are nearly all distinct
+                    bpe.bpe_set_call_memo(e.handle, bpe.MEMO_ON)
+                    configs["C2"]["memo_on_ms"] = round(statistics.median(e.time_calls(10, 3)), 4)
+                    bpe.bpe_set_call_memo(e.handle, bpe.MEMO_AUTO)
                 if not args.no_cpu_baseline:
                     ids_c, off_c = e.result()
                     configs[f"C{c}"]["parity"], _ = parity_line(e, ids_c, off_c)
@@ -543,7 +553,10 @@ def run_gpu(args, world, rank, local):
             "without_word_cache": {"value": round(n_bytes / (nocache_ms / 1e3) / 1e6, 3), "unit": "MB/s",
                                    "ms_per_step": round(nocache_ms, 4),
                                    "hbm_frac": round(alg / (nocache_ms / 1e3) / 1e9 / peak, 4),
-                                   "kernel_ms": nocache_kernels},
+                                   "per_call_memo": "on (the default with the cache off)",
+                                   "kernel_ms": nocache_kernels,
+                                   "memo_off": {"value": round(n_bytes / (nomemo_ms / 1e3) / 1e6, 3),
+                                                "ms_per_step": round(nomemo_ms, 4), "kernel_ms": nomemo_kernels}},
             "decode": dec,
             "train": trn,
             "configs": configs,

@@ -58,7 +58,7 @@ _lock = threading.Lock()
 _lib = None
 
 EXPORTS = ["bpe_build", "bpe_encode_batch", "bpe_encode_batch_host", "bpe_encode_batch_noalloc", "bpe_pretokenize_batch", "bpe_decode_batch", "bpe_set_word_cache",
-           "bpe_set_timing_events", "bpe_set_phase_events", "bpe_sync_status", "bpe_table_info", "bpe_table_monotone", "bpe_merges_monotone",
+           "bpe_set_timing_events", "bpe_set_phase_events", "bpe_set_call_memo", "bpe_sync_status", "bpe_table_info", "bpe_table_monotone", "bpe_merges_monotone",
            "bpe_workspace_bytes", "bpe_train", "bpe_destroy", "bpe_last_error"]
 
 
@@ -88,6 +88,8 @@ def lib():
             L.bpe_set_word_cache.argtypes = [p, ctypes.c_int]
             L.bpe_set_timing_events.restype = ctypes.c_int
             L.bpe_set_timing_events.argtypes = [p, p, p]
+            L.bpe_set_call_memo.restype = ctypes.c_int
+            L.bpe_set_call_memo.argtypes = [p, ctypes.c_int]
             L.bpe_set_phase_events.restype = ctypes.c_int
             L.bpe_set_phase_events.argtypes = [p, p, ctypes.c_int]
             L.bpe_sync_status.restype = ctypes.c_int
@@ -190,6 +192,15 @@ def bpe_train(word_bytes, word_offsets, word_counts, n_merges: int, device: int 
     _check(lib().bpe_train(wb.ctypes.data if wb.size else None, wo.ctypes.data, wc.ctypes.data if wc.size else None,
                            len(wo) - 1, n_merges, device, out.ctypes.data, ctypes.byref(made)))
     return out[:made.value].copy()
+
+
+MEMO_OFF, MEMO_ON, MEMO_AUTO = 0, 1, 2
+
+
+def bpe_set_call_memo(handle: int, mode: int) -> None:
+    """Per-call memo of word-cache misses: MEMO_OFF, MEMO_ON or MEMO_AUTO (on
+    exactly when the word cache is off)."""
+    _check(lib().bpe_set_call_memo(handle, mode))
 
 
 def bpe_set_timing_events(handle: int, ev_start: int | None, ev_stop: int | None) -> None:

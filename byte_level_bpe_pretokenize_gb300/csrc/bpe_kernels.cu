@@ -923,6 +923,7 @@ __device__ __forceinline__ uint32_t cache_slot(const CacheKey& K, uint32_t len, 
 }  // namespace
 
 #include "tiles.cuh"
+#include "memo.cuh"
 #include "decode.cuh"
 #include "train.cuh"
 
@@ -1008,6 +1009,7 @@ struct bpe_handle {
   uint32_t cache_mask = 0;
   int64_t cache_entries = 0;
   int cache_enabled = 1;
+  int call_memo = BPE_MEMO_AUTO;  // bpe_set_call_memo
   DevSmall* d_small = nullptr;
   DevSmall* h_small = nullptr;  // pinned
   void* d_ws = nullptr;
@@ -1161,11 +1163,16 @@ namespace {
 constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsSizes {
-  size_t first_doc, rec, first_start, tile_base, block_sum, stage, misses, giants, ranges, pool, total;
+  size_t first_doc, rec, first_start, tile_base, block_sum, stage, misses, giants, ranges, pool, memo, follow, total;
   int64_t n_tiles, miss_cap, giant_cap, range_cap;
+  uint64_t memo_slots;
 };
 
-constexpr WsSizes ws_sizes(int64_t n_bytes) {
+constexpr uint64_t kMemoMaxSlots = uint64_t(1) << 24;  // the per-call memo's table: at most 128 MiB
+
+// memo: room for the per-call memo of the misses (the table and the
+// follower of each queue entry)
+constexpr WsSizes ws_sizes(int64_t n_bytes, bool memo = false) {
   WsSizes z{};
   z.n_tiles = n_bytes / kTileOwn + 1;
   z.miss_cap = n_bytes / 2 + 64;  // a miss has at least 2 bytes
@@ -1181,8 +1188,16 @@ constexpr WsSizes ws_sizes(int64_t n_bytes) {
   z.giants = align256((size_t)z.giant_cap * sizeof(GiantRec));
   z.ranges = align256((size_t)z.range_cap * sizeof(PrepRange));
   z.pool = align256((size_t)(n_bytes + 4) * sizeof(int32_t));
+  z.memo_slots = 0;
+  z.memo = z.follow = 0;
+  if (memo) {
+    z.memo_slots = 1024;
+    while (z.memo_slots < kMemoMaxSlots && z.memo_slots < 2 * (uint64_t)z.miss_cap) z.memo_slots <<= 1;
+    z.memo = align256(z.memo_slots * sizeof(uint64_t));
+    z.follow = align256((size_t)z.miss_cap * sizeof(uint32_t));
+  }
   z.total = z.first_doc + z.rec + z.first_start + z.tile_base + z.block_sum + z.stage + z.misses + z.giants +
-            z.ranges + z.pool;
+            z.ranges + z.pool + z.memo + z.follow;
   return z;
 }
 
@@ -1198,10 +1213,13 @@ struct Ws {
   GiantRec* giants;
   PrepRange* ranges;
   int32_t* pool;
+  uint64_t* memo;   // null: no per-call memo
+  uint32_t* follow;
+  uint64_t memo_slots;
 };
 
-Ws ws_carve(unsigned char* base, int64_t n_bytes) {
-  const WsSizes z = ws_sizes(n_bytes);
+Ws ws_carve(unsigned char* base, int64_t n_bytes, bool memo = false) {
+  const WsSizes z = ws_sizes(n_bytes, memo);
   Ws w;
   w.n_tiles = z.n_tiles;
   w.miss_cap = z.miss_cap;
@@ -1222,6 +1240,9 @@ Ws ws_carve(unsigned char* base, int64_t n_bytes) {
   w.giants = reinterpret_cast<GiantRec*>(take(z.giants));
   w.ranges = reinterpret_cast<PrepRange*>(take(z.ranges));
   w.pool = reinterpret_cast<int32_t*>(take(z.pool));
+  w.memo = memo ? reinterpret_cast<uint64_t*>(take(z.memo)) : nullptr;
+  w.follow = memo ? reinterpret_cast<uint32_t*>(take(z.follow)) : nullptr;
+  w.memo_slots = z.memo_slots;
   return w;
 }
 
@@ -1314,8 +1335,19 @@ int launch_encode(bpe_handle* h, const Ws& w, const uint8_t* d_bytes, int64_t n_
   k_tiles<<<(unsigned)grid, kTileThreads, kTileSmemBytes, st>>>(a);
   CK(cudaGetLastError());
   if (ev_phase) CK(cudaEventRecord(ev_phase[phase++], st));
-  k_misses<<<(unsigned)(kMissBlocksPerSm * h->n_sms), kMissThreads, 0, st>>>(d_bytes, w.misses, w.miss_cap, w.stage,
-                                                                            w.rec, a.T, h->d_small);
+  if (w.memo) {  // the per-call memo: claims before the merge, copies after (counted with k_misses)
+    CK(cudaMemsetAsync(w.memo, 0xFF, w.memo_slots * sizeof(uint64_t), st));
+    k_memo_claim<<<(unsigned)(8 * h->n_sms), kMemoThreads, 0, st>>>(d_bytes, w.misses, w.miss_cap, w.memo,
+                                                                    w.memo_slots - 1, w.follow, h->d_small);
+    CK(cudaGetLastError());
+  }
+  k_misses<<<(unsigned)(kMissBlocksPerSm * h->n_sms), kMissThreads, 0, st>>>(d_bytes, w.misses, w.miss_cap, w.follow,
+                                                                            w.stage, w.rec, a.T, h->d_small);
+  if (w.memo) {
+    CK(cudaGetLastError());
+    k_memo_copy<<<(unsigned)(8 * h->n_sms), kMemoThreads, 0, st>>>(w.misses, w.miss_cap, w.follow, w.stage, w.rec,
+                                                                   h->d_small);
+  }
   CK(cudaGetLastError());
   if (ev_phase) CK(cudaEventRecord(ev_phase[phase++], st));
   k_giants<<<(unsigned)(8 * h->n_sms), kGiantThreads, 0, st>>>(d_bytes, w.giants, w.giant_cap, w.first_start, n_tiles,
@@ -1493,6 +1525,13 @@ int bpe_set_word_cache(bpe_handle* h, int enable) {
   return BPE_OK;
 }
 
+int bpe_set_call_memo(bpe_handle* h, int mode) {
+  if (!h || (mode != BPE_MEMO_OFF && mode != BPE_MEMO_ON && mode != BPE_MEMO_AUTO))
+    return fail(BPE_ERR_INVALID_ARG, "bpe_set_call_memo: mode must be BPE_MEMO_OFF, BPE_MEMO_ON or BPE_MEMO_AUTO");
+  h->call_memo = mode;
+  return BPE_OK;
+}
+
 int bpe_set_timing_events(bpe_handle* h, void* ev_start, void* ev_stop) {
   if (!h) return fail(BPE_ERR_INVALID_ARG, "null handle");
   h->ev_start = (cudaEvent_t)ev_start;
@@ -1570,14 +1609,19 @@ int bpe_encode_batch(bpe_handle* h, const uint8_t* d_bytes, int64_t n_bytes, con
     return fail(BPE_ERR_INVALID_ARG, "bpe_encode_batch: offsets must be 8-byte and ids 4-byte aligned");
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
-  int rc = ensure_ws(h, ws_sizes(n_bytes).total);
+  // the per-call memo: on request, or (by default) when the word cache is off
+  // and the misses are every pre-token; queue indices must fit in 32 bits
+  const bool memo = (h->call_memo == BPE_MEMO_ON || (h->call_memo == BPE_MEMO_AUTO && !h->cache_enabled)) &&
+                    ws_sizes(n_bytes).miss_cap < (int64_t)UINT32_MAX;
+  int rc = ensure_ws(h, ws_sizes(n_bytes, memo).total);
   if (rc) return rc;
   if (!h->smem_set) {
     if ((rc = tiles_smem_setup())) return rc;
     h->smem_set = true;
   }
-  rc = launch_encode(h, ws_carve(static_cast<unsigned char*>(h->d_ws), n_bytes), d_bytes, n_bytes, d_doc_offsets,
-                     n_docs, d_out_ids, out_capacity, d_out_offsets, st, h->ev_start, h->ev_stop, h->ev_phase);
+  rc = launch_encode(h, ws_carve(static_cast<unsigned char*>(h->d_ws), n_bytes, memo), d_bytes, n_bytes,
+                     d_doc_offsets, n_docs, d_out_ids, out_capacity, d_out_offsets, st, h->ev_start, h->ev_stop,
+                     h->ev_phase);
   if (rc) return rc;
   if (h_total_tokens) {
     DevSmall s;

@@ -608,8 +608,9 @@ __device__ uint32_t merge_thread(TinyScratch& Z, const uint8_t* src, uint32_t n,
 // on its first id, and adds its holes to its tile's record.
 constexpr int kMissBlocksPerSm = 5;
 __global__ void __launch_bounds__(kMissThreads, kMissBlocksPerSm) k_misses(const uint8_t* bytes, const uint64_t* queue,
-                                                                           int64_t queue_cap, uint32_t* stage,
-                                                                           TileRec* rec, Tables T, DevSmall* small) {
+                                                                           int64_t queue_cap, const uint32_t* follow,
+                                                                           uint32_t* stage, TileRec* rec, Tables T,
+                                                                           DevSmall* small) {
   __shared__ GroupScratch grp[kMissThreads / 32];
   __shared__ TinyScratch tiny;
   __shared__ int32_t byte_id[256];
@@ -622,8 +623,11 @@ __global__ void __launch_bounds__(kMissThreads, kMissBlocksPerSm) k_misses(const
   GroupScratch& W = grp[threadIdx.x >> 5];
   const uint64_t warps = (uint64_t)gridDim.x * (kMissThreads / 32);
   for (uint64_t q0 = ((uint64_t)blockIdx.x * (kMissThreads / 32) + (threadIdx.x >> 5)) * 32; q0 < n_q; q0 += warps * 32) {
+    // an entry another miss of the same bytes stands for (follow, the per-call
+    // memo) is left to k_memo_copy
+    const bool own = q0 + lane < n_q && (!follow || follow[q0 + lane] == (uint32_t)(q0 + lane));
     const uint64_t e = q0 + lane < n_q ? queue[q0 + lane] : 0ull;
-    const uint32_t len = q0 + lane < n_q ? (uint32_t)(e >> kMissLenShift) & 0x7Fu : 0u;  // 0: no entry
+    const uint32_t len = own ? (uint32_t)(e >> kMissLenShift) & 0x7Fu : 0u;  // 0: no entry
     // where a queue entry's bytes, ids and tile record are
     auto src_of = [&](uint64_t x) { return bytes + (int64_t)(x >> 30) * kTileOwn + (int64_t)(x & 0x7FFu); };
     auto out_of = [&](uint64_t x) {

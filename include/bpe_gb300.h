@@ -229,15 +229,38 @@ int bpe_decode_batch(bpe_handle* h, const int32_t* d_ids, int64_t n_ids, const i
  * The cache is the memo of "Hugging Face Tokenizers v1" (section on word
  * caching: a given pre-token always yields the same ids, so its ids can be
  * looked up instead of merged). bpe_build fills it once with strings of
- * 1..16 bytes: every vocabulary string, every vocabulary string that starts
+ * 2..16 bytes: every vocabulary string, every vocabulary string that starts
  * with a space with the space removed (the word at the start of a line or
  * document), and every prefix of those (a word cut off by the end of a
  * document). Each is run through the device merge loop and its ids (when at
- * most 3) are stored under its bytes. During encoding a pre-token of at most
- * 16 bytes found there takes the stored ids; every other pre-token runs the
- * merge loop. Either setting gives identical ids.
+ * most 3) are stored under its bytes. During encoding a pre-token of 2 to 16
+ * bytes found there takes the stored ids, a pre-token of one byte is its own
+ * token, and every other pre-token runs the merge loop. Either setting gives
+ * identical ids.
  */
 int bpe_set_word_cache(bpe_handle* h, int enable);
+
+/*
+ * bpe_set_call_memo — the per-call memo of the pre-tokens that miss the word
+ * cache ("Hugging Face Tokenizers v1", section on word caching: a pre-token
+ * always yields the same ids). When it is on, bpe_encode_batch hashes every
+ * miss of the call into a table, compares equal hashes byte for byte, merges
+ * one pre-token of each distinct string and copies its ids to the others.
+ *   BPE_MEMO_AUTO (default): on exactly when the word cache is off (then
+ *     every pre-token of two or more bytes is a miss, and they repeat);
+ *     with the cache on, the misses are strings the vocabulary does not
+ *     hold, nearly all distinct, and the memo would only add work.
+ *   BPE_MEMO_ON, BPE_MEMO_OFF: always, never.
+ * Either setting gives identical ids. Only bpe_encode_batch uses the memo
+ * (bpe_encode_batch_host and bpe_encode_batch_noalloc never do). The memo
+ * needs about 2 bytes of workspace per input byte and a table of at most
+ * 128 MiB; beyond 2^24 distinct misses the rest are merged one by one.
+ * Errors: BPE_ERR_INVALID_ARG for a null handle or another mode.
+ */
+#define BPE_MEMO_OFF 0
+#define BPE_MEMO_ON 1
+#define BPE_MEMO_AUTO 2
+int bpe_set_call_memo(bpe_handle* h, int mode);
 
 /*
  * bpe_set_timing_events — measurement hook. ev_start and ev_stop are two
@@ -257,7 +280,8 @@ int bpe_set_timing_events(bpe_handle* h, void* ev_start, void* ev_stop);
  * the array must outlive its use). While set, bpe_encode_batch records
  * events[0] before its first kernel and events[i] right after its i-th, in
  * this order: k_prep_docs, k_prep_long, k_tiles, k_misses, k_giants,
- * k_scan_tiles, k_scan_tile_sums, k_compact, k_giant_copy. n = 0 (events may
+ * k_scan_tiles, k_scan_tile_sums, k_compact, k_giant_copy (with the per-call
+ * memo on, its two kernels run in the k_misses interval). n = 0 (events may
  * be NULL) switches it off; any other n than BPE_ENCODE_LAUNCHES + 1 is
  * BPE_ERR_INVALID_ARG.
  */

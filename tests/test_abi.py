@@ -143,3 +143,11 @@ def test_measurement_hooks_check_their_arguments(bpe):
     assert ", ".join(bpe.ENCODE_KERNELS) in " ".join(hdr.replace("*", " ").split())
     with pytest.raises(ValueError):
         bpe.PhaseEvents([0] * 3)
+
+
+def test_call_memo_modes_checked(bpe):
+    L = bpe.lib()
+    assert L.bpe_set_call_memo(None, bpe.MEMO_AUTO) == 1
+    hdr = open(os.path.join(ROOT, "include", "bpe_gb300.h")).read()
+    for name, v in (("BPE_MEMO_OFF", bpe.MEMO_OFF), ("BPE_MEMO_ON", bpe.MEMO_ON), ("BPE_MEMO_AUTO", bpe.MEMO_AUTO)):
+        assert f"#define {name} {v}" in hdr

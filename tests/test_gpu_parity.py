@@ -43,14 +43,19 @@ def tiny(bpe):
 
 
 def check(handle, orc, data, offsets, label="", n_bytes=None):
-    """GPU ids with the word cache on and off, each equal to the oracle's."""
+    """GPU ids with the word cache on and off, and the per-call memo of the
+    misses on and off (by default it is on exactly when the cache is off),
+    each equal to the oracle's."""
     import byte_level_bpe_pretokenize_gb300 as bpe
     want = orc.encode_batch(data, offsets)
-    for cache in (True, False):
+    for cache, memo in ((True, bpe.MEMO_AUTO), (False, bpe.MEMO_AUTO), (True, bpe.MEMO_ON), (False, bpe.MEMO_OFF)):
         bpe.bpe_set_word_cache(handle, cache)
+        bpe.bpe_set_call_memo(handle, memo)
         got = gpu_encode(handle, data, offsets, n_bytes)
-        assert_same_encoding(got, want, data, offsets, f"{label} (word cache {'on' if cache else 'off'})")
+        assert_same_encoding(got, want, data, offsets,
+                             f"{label} (word cache {'on' if cache else 'off'}, memo mode {memo})")
     bpe.bpe_set_word_cache(handle, True)
+    bpe.bpe_set_call_memo(handle, bpe.MEMO_AUTO)
     return got
 
 
