@@ -25,6 +25,7 @@ constexpr int kDecWarps = 8;           // tiles in flight per CTA
 constexpr int kDecBuf = 8192;          // bytes a warp buffers before it stores them
 constexpr int kDecScanThreads = 1024;  // tiles per block of the tile scan
 constexpr uint32_t kDecInline = 12;    // token bytes held in its entry
+constexpr int kDecAhead = 4;           // rounds of 32 ids whose loads are issued together
 
 __device__ __forceinline__ uint4 dec_entry(const uint4* vent, int64_t n_vocab, int32_t id, bool* bad) {
   if (id < 0 || (int64_t)id >= n_vocab) {
@@ -44,10 +45,16 @@ __global__ void __launch_bounds__(32 * kDecWarps) k_dec_count(const int32_t* ids
     const int64_t i0 = t * kDecIds;
     const int64_t n = n_ids - i0 < kDecIds ? n_ids - i0 : kDecIds;
     uint32_t sum = 0;
-#pragma unroll 8
-    for (int j = 0; j < kDecIds / 32; ++j) {
-      const int64_t i = (int64_t)j * 32 + lane;
-      if (i < n) sum += dec_entry(vent, n_vocab, __ldcs(ids + i0 + i), &bad).w;
+    for (int j0 = 0; j0 < kDecIds / 32; j0 += 8) {  // eight ids, then their eight entries, in flight
+      int32_t id[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t i = (int64_t)(j0 + u) * 32 + lane;
+        id[u] = i < n ? __ldcs(ids + i0 + i) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if ((int64_t)(j0 + u) * 32 + lane < n) sum += dec_entry(vent, n_vocab, id[u], &bad).w;
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, d);
@@ -154,10 +161,24 @@ __global__ void __launch_bounds__(32 * kDecWarps) k_dec_write(const int32_t* ids
     int64_t g_lo = base;
     uint32_t lo = (uint32_t)(reinterpret_cast<uintptr_t>(out + base) & 15u), hi = lo;
     int64_t at = base;  // output position of the next token
-    for (int64_t r0 = 0; r0 < n; r0 += 32) {
-      const int64_t i = r0 + lane;
-      const int32_t id = i < n ? __ldcs(ids + i0 + i) : -1;
-      const uint4 e = i < n ? dec_entry(vent, n_vocab, id, &bad) : make_uint4(0, 0, 0, 0);
+    for (int64_t g0 = 0; g0 < n; g0 += 32 * kDecAhead) {
+     // the ids and token entries of kDecAhead rounds are loaded together
+     int32_t idg[kDecAhead];
+     uint4 eg[kDecAhead];
+#pragma unroll
+     for (int u = 0; u < kDecAhead; ++u) {
+       const int64_t i = g0 + 32 * u + lane;
+       idg[u] = i < n ? __ldcs(ids + i0 + i) : -1;
+     }
+#pragma unroll
+     for (int u = 0; u < kDecAhead; ++u)
+       eg[u] = g0 + 32 * u + lane < n ? dec_entry(vent, n_vocab, idg[u], &bad) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+     for (int u = 0; u < kDecAhead; ++u) {
+      const int64_t r0 = g0 + 32 * u;
+      if (r0 >= n) break;
+      const int32_t id = idg[u];
+      const uint4 e = eg[u];
       const uint32_t len = e.w;
       uint32_t incl = len;
 #pragma unroll
@@ -208,6 +229,7 @@ __global__ void __launch_bounds__(32 * kDecWarps) k_dec_write(const int32_t* ids
         hi += rtot;
       }
       at += rtot;
+     }
     }
     __syncwarp();
     over |= dec_flush(buf, lo, hi, out, g_lo, cap);
