@@ -1896,6 +1896,7 @@ int bpe_train(const uint8_t* word_bytes, const int64_t* word_offsets, const int6
     int64_t* freq = nullptr;
     uint64_t* keys = nullptr;
     unsigned long long* counts = nullptr;
+    uint32_t* occ = nullptr;
     unsigned long long* bc = nullptr;
     unsigned long long* bk = nullptr;
     TrainState* st = nullptr;
@@ -1907,7 +1908,7 @@ int bpe_train(const uint8_t* word_bytes, const int64_t* word_offsets, const int6
       if (exec) cudaGraphExecDestroy(exec);
       if (graph) cudaGraphDestroy(graph);
       if (s) cudaStreamDestroy(s);
-      cudaFree(sym); cudaFree(off); cudaFree(len); cudaFree(freq); cudaFree(keys); cudaFree(counts);
+      cudaFree(sym); cudaFree(off); cudaFree(len); cudaFree(freq); cudaFree(keys); cudaFree(counts); cudaFree(occ);
       cudaFree(bc); cudaFree(bk); cudaFree(st); cudaFree(merges);
     }
   } d;
@@ -1917,6 +1918,7 @@ int bpe_train(const uint8_t* word_bytes, const int64_t* word_offsets, const int6
   CK(cudaMalloc(&d.freq, (size_t)n_words * sizeof(int64_t)));
   CK(cudaMalloc(&d.keys, n_slots * sizeof(uint64_t)));
   CK(cudaMalloc(&d.counts, n_slots * sizeof(unsigned long long)));
+  CK(cudaMalloc(&d.occ, n_slots * sizeof(uint32_t)));
   CK(cudaMalloc(&d.bc, slot_grid * sizeof(unsigned long long)));
   CK(cudaMalloc(&d.bk, slot_grid * sizeof(unsigned long long)));
   CK(cudaMalloc(&d.st, sizeof(TrainState)));
@@ -1934,10 +1936,10 @@ int bpe_train(const uint8_t* word_bytes, const int64_t* word_offsets, const int6
   CK(cudaStreamBeginCapture(d.s, cudaStreamCaptureModeThreadLocal));
   for (int k = 0; k < kSteps; ++k) {
     k_train_count<<<word_grid, kTrainThreads, 0, d.s>>>(d.sym, d.off, d.len, d.freq, n_words, d.keys, d.counts,
-                                                         n_slots - 1, d.st);
-    k_train_best<<<slot_grid, kTrainThreads, 0, d.s>>>(d.keys, d.counts, n_slots, d.bc, d.bk, d.st, d.merges,
+                                                         n_slots - 1, d.occ, d.st);
+    k_train_best<<<slot_grid, kTrainThreads, 0, d.s>>>(d.keys, d.counts, d.occ, d.bc, d.bk, d.st, d.merges,
                                                         n_merges);
-    k_train_replace<<<repl_grid, kTrainThreads, 0, d.s>>>(d.sym, d.off, d.len, n_words, d.keys, d.counts, n_slots,
+    k_train_replace<<<repl_grid, kTrainThreads, 0, d.s>>>(d.sym, d.off, d.len, n_words, d.keys, d.counts, d.occ,
                                                            d.st);
   }
   CK(cudaStreamEndCapture(d.s, &d.graph));

@@ -886,7 +886,7 @@ struct CompactState {
 // tile's end.
 constexpr int kCompactPart = 512;
 
-__global__ void __launch_bounds__(32 * kCompactWarps) k_compact(const TileRec* rec, const uint32_t* stage,
+__global__ void __launch_bounds__(32 * kCompactWarps, 4) k_compact(const TileRec* rec, const uint32_t* stage,
                                                                 const uint64_t* tile_base, const uint64_t* block_sum,
                                                                 GiantRec* giants, int64_t giant_cap,
                                                                 const int64_t* doc_offsets, int64_t n_tiles,

@@ -9,14 +9,16 @@
 // all on the device and without a host round trip:
 //   * k_train_count: a thread per word adds the word's count to every
 //     adjacent pair of its symbols in an open-addressed pair histogram
-//     (64-bit key left << 32 | right, 64-bit count; atomicCAS claims a slot).
-//   * k_train_best: the histogram's most frequent pair, ties to the smallest
+//     (64-bit key left << 32 | right, 64-bit count; atomicCAS claims a slot,
+//     and a claimed slot is listed, so the other two kernels touch only the
+//     pairs that occur).
+//   * k_train_best: the most frequent listed pair, ties to the smallest
 //     (left, right): block reductions, then the last CTA to finish reduces
-//     the block results, appends the merge row and clears nothing else. With
-//     no pair left it sets the done flag and later steps return at once.
+//     the block results and appends the merge row. With no pair left it sets
+//     the done flag and later steps return at once.
 //   * k_train_replace: a thread per word replaces the pair left to right
 //     without overlap and compacts the word in place; it also empties the
-//     histogram for the next step (grid-stride).
+//     listed slots for the next step.
 // Every step is the same three launches with the same arguments, so the host
 // captures a run of steps in a CUDA graph once and replays it.
 
@@ -32,6 +34,8 @@ struct TrainState {
   int done;        // no pair left, or n_merges made: later steps return at once
   int merged_now;  // this step made a merge (k_train_replace applies it)
   long long made;
+  unsigned long long n_occ;    // histogram slots claimed in this step (listed in occ)
+  unsigned long long n_clear;  // slots k_train_replace empties (this step's n_occ)
 };
 
 __device__ __forceinline__ uint32_t train_hash(uint64_t k) {
@@ -47,7 +51,7 @@ __global__ void __launch_bounds__(kTrainThreads) k_train_count(const int32_t* sy
                                                                const int32_t* len, const int64_t* freq,
                                                                int64_t n_words, uint64_t* keys,
                                                                unsigned long long* counts, uint64_t mask,
-                                                               TrainState* st) {
+                                                               uint32_t* occ, TrainState* st) {
   if (st->done) return;
   for (int64_t w = (int64_t)blockIdx.x * kTrainThreads + threadIdx.x; w < n_words;
        w += (int64_t)gridDim.x * kTrainThreads) {
@@ -62,6 +66,7 @@ __global__ void __launch_bounds__(kTrainThreads) k_train_count(const int32_t* sy
             atomicCAS(reinterpret_cast<unsigned long long*>(keys + h), (unsigned long long)kTrainEmpty,
                       (unsigned long long)key);
         if (prev == kTrainEmpty || prev == key) {
+          if (prev == kTrainEmpty) occ[atomicAdd(&st->n_occ, 1ull)] = (uint32_t)h;
           atomicAdd(counts + h, f);
           break;
         }
@@ -72,17 +77,18 @@ __global__ void __launch_bounds__(kTrainThreads) k_train_count(const int32_t* sy
 }
 
 __global__ void __launch_bounds__(kTrainThreads) k_train_best(const uint64_t* keys, const unsigned long long* counts,
-                                                              uint64_t n_slots, unsigned long long* block_count,
+                                                              const uint32_t* occ, unsigned long long* block_count,
                                                               unsigned long long* block_key, TrainState* st,
                                                               int32_t* merges, int64_t n_merges) {
   __shared__ unsigned long long sc[kTrainThreads / 32], sk[kTrainThreads / 32];
   __shared__ bool last;
   if (st->done) return;
+  const uint64_t n_occ = st->n_occ;
   uint64_t bc = 0, bk = kTrainEmpty;
-  for (uint64_t i = (uint64_t)blockIdx.x * kTrainThreads + threadIdx.x; i < n_slots;
-       i += (uint64_t)gridDim.x * kTrainThreads) {
+  for (uint64_t j = (uint64_t)blockIdx.x * kTrainThreads + threadIdx.x; j < n_occ;
+       j += (uint64_t)gridDim.x * kTrainThreads) {
+    const uint32_t i = occ[j];
     const uint64_t k = keys[i];
-    if (k == kTrainEmpty) continue;
     const uint64_t c = counts[i];
     if (train_better(c, k, bc, bk)) {
       bc = c;
@@ -115,13 +121,13 @@ __global__ void __launch_bounds__(kTrainThreads) k_train_best(const uint64_t* ke
     last = atomicAdd(&st->blocks_done, 1u) == gridDim.x - 1;
   }
   __syncthreads();
-  if (!last || threadIdx.x != 0) return;
-  // the last CTA: every block result is visible (each was fenced before its
-  // counter increment)
+  if (!last || warp != 0) return;
+  // the last CTA's first warp: every block result is visible (each was
+  // fenced before its counter increment)
   __threadfence();
   bc = 0;
   bk = kTrainEmpty;
-  for (unsigned b = 0; b < gridDim.x; ++b) {
+  for (unsigned b = lane; b < gridDim.x; b += 32) {
     const uint64_t c = *reinterpret_cast<volatile unsigned long long*>(block_count + b);
     const uint64_t k = *reinterpret_cast<volatile unsigned long long*>(block_key + b);
     if (train_better(c, k, bc, bk)) {
@@ -129,8 +135,19 @@ __global__ void __launch_bounds__(kTrainThreads) k_train_best(const uint64_t* ke
       bk = k;
     }
   }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    const uint64_t oc = __shfl_xor_sync(0xFFFFFFFFu, bc, d), ok = __shfl_xor_sync(0xFFFFFFFFu, bk, d);
+    if (train_better(oc, ok, bc, bk)) {
+      bc = oc;
+      bk = ok;
+    }
+  }
+  if (lane != 0) return;
   st->blocks_done = 0;
   st->merged_now = 0;
+  st->n_clear = st->n_occ;  // every CTA has read n_occ
+  st->n_occ = 0;
   if (bc == 0 || st->made >= n_merges) {
     st->done = 1;
     return;
@@ -147,11 +164,13 @@ __global__ void __launch_bounds__(kTrainThreads) k_train_best(const uint64_t* ke
 
 __global__ void __launch_bounds__(kTrainThreads) k_train_replace(int32_t* sym, const int64_t* off, int32_t* len,
                                                                  int64_t n_words, uint64_t* keys,
-                                                                 unsigned long long* counts, uint64_t n_slots,
+                                                                 unsigned long long* counts, const uint32_t* occ,
                                                                  const TrainState* st) {
-  // the histogram is cleared for the next step (every step ends here)
-  for (uint64_t i = (uint64_t)blockIdx.x * kTrainThreads + threadIdx.x; i < n_slots;
-       i += (uint64_t)gridDim.x * kTrainThreads) {
+  // the slots this step claimed are emptied for the next step
+  const uint64_t n_clear = st->n_clear;
+  for (uint64_t j = (uint64_t)blockIdx.x * kTrainThreads + threadIdx.x; j < n_clear;
+       j += (uint64_t)gridDim.x * kTrainThreads) {
+    const uint32_t i = occ[j];
     keys[i] = kTrainEmpty;
     counts[i] = 0;
   }
