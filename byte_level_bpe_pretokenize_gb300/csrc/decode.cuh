@@ -173,63 +173,83 @@ __global__ void __launch_bounds__(32 * kDecWarps) k_dec_write(const int32_t* ids
 #pragma unroll
      for (int u = 0; u < kDecAhead; ++u)
        eg[u] = g0 + 32 * u + lane < n ? dec_entry(vent, n_vocab, idg[u], &bad) : make_uint4(0, 0, 0, 0);
+     // the group's kDecAhead scans together (independent chains)
+     uint32_t len[kDecAhead], incl[kDecAhead];
+#pragma unroll
+     for (int u = 0; u < kDecAhead; ++u) incl[u] = len[u] = eg[u].w;
+#pragma unroll
+     for (int d = 1; d < 32; d <<= 1) {
+#pragma unroll
+       for (int u = 0; u < kDecAhead; ++u) {
+         const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl[u], d);
+         if (lane >= (uint32_t)d) incl[u] += o;
+       }
+     }
+     uint32_t gb[kDecAhead];  // bytes of the group's rounds before round u
+     uint32_t gtot = 0;
 #pragma unroll
      for (int u = 0; u < kDecAhead; ++u) {
-      const int64_t r0 = g0 + 32 * u;
-      if (r0 >= n) break;
-      const int32_t id = idg[u];
-      const uint4 e = eg[u];
-      const uint32_t len = e.w;
-      uint32_t incl = len;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= (uint32_t)d) incl += o;
-      }
-      const uint32_t excl = incl - len, rtot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      // documents whose first id is in this round: the byte offset of that id
-      for (;;) {
-        const int64_t rel = doff - (i0 + r0);
-        const bool here = rel >= 0 && rel < 32 && r0 + rel < n;
-        const uint32_t pre = __shfl_sync(0xFFFFFFFFu, excl, here ? (uint32_t)rel : lane);
-        if (here) out_offsets[kb + lane] = at + pre;
-        const bool done = doff == INT64_MAX || (rel < 32 && r0 + rel < n);
-        if (!__all_sync(0xFFFFFFFFu, done) || kb + 32 > n_docs) break;
-        kb += 32;
-        doff = kb + lane <= n_docs ? __ldg(id_offsets + kb + lane) : INT64_MAX;
-      }
-      // bytes: flush first when the round does not fit; a round larger than
-      // the buffer goes straight to the output
-      if (hi + rtot > (uint32_t)kDecBuf) {
-        __syncwarp();
-        over |= dec_flush(buf, lo, hi, out, g_lo, cap);
-        __syncwarp();
-        g_lo = at;
-        lo = hi = (uint32_t)(reinterpret_cast<uintptr_t>(out + at) & 15u);
-      }
-      if (hi + rtot > (uint32_t)kDecBuf) {
-        const int64_t b0 = len > kDecInline ? voffs[id] : 0;
-        for (uint32_t q = 0; q < len; ++q) {
-          const int64_t g = at + excl + q;
-          const uint8_t v = q < kDecInline ? (uint8_t)((q < 4 ? e.x : q < 8 ? e.y : e.z) >> (8 * (q & 3))) : vbytes[b0 + q];
-          if (g < cap) out[g] = v;
-          else over = true;
-        }
-        g_lo = at + rtot;
-        lo = hi = (uint32_t)(reinterpret_cast<uintptr_t>(out + g_lo) & 15u);
-      } else {
-        uint8_t* d = buf + hi + excl;
-#pragma unroll
-        for (uint32_t q = 0; q < kDecInline; ++q)
-          if (q < len) d[q] = (uint8_t)((q < 4 ? e.x : q < 8 ? e.y : e.z) >> (8 * (q & 3)));
-        if (len > kDecInline) {
-          const uint8_t* src = vbytes + voffs[id];
-          for (uint32_t q = kDecInline; q < len; ++q) d[q] = src[q];
-        }
-        hi += rtot;
-      }
-      at += rtot;
+       gb[u] = gtot;
+       gtot += __shfl_sync(0xFFFFFFFFu, incl[u], 31);
      }
+     // documents whose first id is in the group: the byte offset of that id
+     const int64_t gn = n - g0 < 32 * kDecAhead ? n - g0 : 32 * kDecAhead;  // ids of the group
+     for (;;) {
+       const int64_t rel = doff - (i0 + g0);
+       const bool here = rel >= 0 && rel < gn;
+       const uint32_t src = here ? (uint32_t)(rel & 31) : lane;
+       uint32_t pre = 0;
+#pragma unroll
+       for (int u = 0; u < kDecAhead; ++u) {
+         const uint32_t x = __shfl_sync(0xFFFFFFFFu, incl[u] - len[u], src);
+         if (here && (rel >> 5) == u) pre = gb[u] + x;
+       }
+       if (here) out_offsets[kb + lane] = at + pre;
+       const bool done = doff == INT64_MAX || rel < gn;
+       if (!__all_sync(0xFFFFFFFFu, done) || kb + 32 > n_docs) break;
+       kb += 32;
+       doff = kb + lane <= n_docs ? __ldg(id_offsets + kb + lane) : INT64_MAX;
+     }
+     // bytes: flush first when the group does not fit; a group larger than
+     // the buffer goes straight to the output
+     if (hi + gtot > (uint32_t)kDecBuf) {
+       __syncwarp();
+       over |= dec_flush(buf, lo, hi, out, g_lo, cap);
+       __syncwarp();
+       g_lo = at;
+       lo = hi = (uint32_t)(reinterpret_cast<uintptr_t>(out + at) & 15u);
+     }
+     const bool direct = hi + gtot > (uint32_t)kDecBuf;
+#pragma unroll
+     for (int u = 0; u < kDecAhead; ++u) {
+       const uint4 e = eg[u];
+       const uint32_t L = len[u], off = gb[u] + incl[u] - L;
+       if (direct) {
+         const int64_t b0 = L > kDecInline ? voffs[idg[u]] : 0;
+         for (uint32_t q = 0; q < L; ++q) {
+           const int64_t g = at + off + q;
+           const uint8_t v = q < kDecInline ? (uint8_t)((q < 4 ? e.x : q < 8 ? e.y : e.z) >> (8 * (q & 3))) : vbytes[b0 + q];
+           if (g < cap) out[g] = v;
+           else over = true;
+         }
+       } else {
+         uint8_t* d = buf + hi + off;
+#pragma unroll
+         for (uint32_t q = 0; q < kDecInline; ++q)
+           if (q < L) d[q] = (uint8_t)((q < 4 ? e.x : q < 8 ? e.y : e.z) >> (8 * (q & 3)));
+         if (L > kDecInline) {
+           const uint8_t* src = vbytes + voffs[idg[u]];
+           for (uint32_t q = kDecInline; q < L; ++q) d[q] = src[q];
+         }
+       }
+     }
+     if (direct) {
+       g_lo = at + gtot;
+       lo = hi = (uint32_t)(reinterpret_cast<uintptr_t>(out + g_lo) & 15u);
+     } else {
+       hi += gtot;
+     }
+     at += gtot;
     }
     __syncwarp();
     over |= dec_flush(buf, lo, hi, out, g_lo, cap);

@@ -26,6 +26,7 @@ namespace {
 
 constexpr uint64_t kTrainEmpty = ~0ull;
 constexpr int kTrainThreads = 256;
+constexpr int kTrainLocal = 2048;  // claimed slots a CTA lists in shared memory
 
 struct TrainState {
   unsigned long long best_count;
@@ -52,7 +53,14 @@ __global__ void __launch_bounds__(kTrainThreads) k_train_count(const int32_t* sy
                                                                int64_t n_words, uint64_t* keys,
                                                                unsigned long long* counts, uint64_t mask,
                                                                uint32_t* occ, TrainState* st) {
+  // slots this CTA claims, listed in shared memory and appended to occ with
+  // one global atomic at the end (past kTrainLocal, one atomic each)
+  __shared__ uint32_t loc[kTrainLocal];
+  __shared__ unsigned int n_loc;
+  __shared__ unsigned long long base;
   if (st->done) return;
+  if (threadIdx.x == 0) n_loc = 0;
+  __syncthreads();
   for (int64_t w = (int64_t)blockIdx.x * kTrainThreads + threadIdx.x; w < n_words;
        w += (int64_t)gridDim.x * kTrainThreads) {
     const int32_t* s = sym + off[w];
@@ -66,7 +74,11 @@ __global__ void __launch_bounds__(kTrainThreads) k_train_count(const int32_t* sy
             atomicCAS(reinterpret_cast<unsigned long long*>(keys + h), (unsigned long long)kTrainEmpty,
                       (unsigned long long)key);
         if (prev == kTrainEmpty || prev == key) {
-          if (prev == kTrainEmpty) occ[atomicAdd(&st->n_occ, 1ull)] = (uint32_t)h;
+          if (prev == kTrainEmpty) {
+            const unsigned int j = atomicAdd(&n_loc, 1u);
+            if (j < (unsigned)kTrainLocal) loc[j] = (uint32_t)h;
+            else occ[atomicAdd(&st->n_occ, 1ull)] = (uint32_t)h;
+          }
           atomicAdd(counts + h, f);
           break;
         }
@@ -74,6 +86,11 @@ __global__ void __launch_bounds__(kTrainThreads) k_train_count(const int32_t* sy
       }
     }
   }
+  __syncthreads();
+  const unsigned int n = n_loc < (unsigned)kTrainLocal ? n_loc : (unsigned)kTrainLocal;
+  if (threadIdx.x == 0) base = n ? atomicAdd(&st->n_occ, (unsigned long long)n) : 0ull;
+  __syncthreads();
+  for (unsigned int j = threadIdx.x; j < n; j += kTrainThreads) occ[base + j] = loc[j];
 }
 
 __global__ void __launch_bounds__(kTrainThreads) k_train_best(const uint64_t* keys, const unsigned long long* counts,
