@@ -876,8 +876,7 @@ struct CompactState {
 // ids are copied from the pool by k_giant_copy). The used part of the tile's
 // stage slot is copied to shared memory kCompactPart entries at a time with
 // asynchronous 16-byte copies (all loads of a part in flight at once), then
-// walked 128 entries at a time while they are all plain ids (four coalesced
-// stores a lane, no scan), else in chunks of 32: a chunk of 32 plain ids
+// walked in chunks of 32 entries by one short loop. A chunk of 32 plain ids
 // needs no scan; others take positions from a scan of each entry's id count
 // (0 for a hole). A document mark (the
 // first id of a document) gives document offsets: the r-th mark of the tile
@@ -928,36 +927,6 @@ __global__ void __launch_bounds__(32 * kCompactWarps, 4) k_compact(const TileRec
       cp_async_wait_all();
       __syncwarp();
       for (uint32_t q0 = 0; q0 < n_part; q0 += 32) {
-        if (!dup && (q0 & 127u) == 0 && q0 + 128 <= n_part) {
-          // 128 entries at once when they are all plain ids (the common case):
-          // no scan, four coalesced stores a lane
-          uint32_t e4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) e4[u] = ent[q0 + 32 * u + lane];
-          const uint32_t any4 = e4[0] | e4[1] | e4[2] | e4[3];
-          if (!__any_sync(0xFFFFFFFFu, (any4 & kIdSpecial) != 0) && (int64_t)(st.at0 + 128) <= capacity) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) out_ids[st.at0 + 32 * u + lane] = (int32_t)(e4[u] & ~kIdDoc);
-            if (__any_sync(0xFFFFFFFFu, (any4 & kIdDoc) != 0)) {
-              uint32_t before = 0;
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const bool mark = (e4[u] & kIdDoc) != 0;
-                const uint32_t mb = __ballot_sync(0xFFFFFFFFu, mark);
-                if (mark) {
-                  const int64_t k = R.k0 + st.nmark + before + __popc(mb & lanemask_lt());
-                  if (k < R.k1) out_offsets[k] = (int64_t)(st.at0 + 32 * u + lane);
-                  else atomicOr(&small->status, kStInternal);
-                }
-                before += __popc(mb);
-              }
-              st.nmark += before;
-            }
-            st.at0 += 128;
-            q0 += 96;  // and 32 by the loop
-            continue;
-          }
-        }
         const uint32_t e = q0 + lane < n_part ? ent[q0 + lane] : kIdHole;
         const bool plain = (e & kIdSpecial) == 0;  // an id (no hole, no placeholder)
         const uint32_t pb = __ballot_sync(0xFFFFFFFFu, plain);
