@@ -557,14 +557,16 @@ __device__ __forceinline__ uint32_t ascii_starts32(const SS& S, int p0, const ui
 
 // Start bits of window positions [p0, p0 + 32), p0 a multiple of 16.
 template <class SS>
-__device__ uint32_t start_mask32(const SS& S, int p0) {
+__device__ uint32_t start_mask32(const SS& S, int p0, bool try_ascii = true) {
   const uint64_t D = bits64_at(S.docbits, p0 - 8), O = bits64_at(S.outbits, p0 - 8);
   if ((uint32_t)(O >> 8) == 0xFFFFFFFFu) return 0;
   // Ten aligned window words: bytes p0 - 4 .. p0 + 35. ASCII: every byte is a
-  // unit.
-  uint32_t any;
-  const uint32_t ascii = ascii_starts32(S, p0, reinterpret_cast<const uint32_t*>(S.win + p0) - 1, D, O, &any);
-  if (!(any & 0x80808080u)) return ascii;
+  // unit (skipped when the caller has already found a byte above 0x7F).
+  if (try_ascii) {
+    uint32_t any;
+    const uint32_t ascii = ascii_starts32(S, p0, reinterpret_cast<const uint32_t*>(S.win + p0) - 1, D, O, &any);
+    if (!(any & 0x80808080u)) return ascii;
+  }
   // General: scan the UTF-8 units of bytes [p0 - 7, p0 + 33); each byte
   // carries its unit's class. Units starting before p0 - 8 may be misread
   // only up to p0 - 5, and nothing before p0 - 4 is used.

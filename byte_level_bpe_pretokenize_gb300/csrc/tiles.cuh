@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm) k_tiles(TileArgs
       const int p0 = kHalo + 1024 * hw + 32 * lane;
       dw[hw] = bits32_at(W.docbits, p0);
       dso[hw] = dw[hw] & bits32_at(W.outbits, p0);
-      if (!ascii_split32(W, p0, &m[hw])) m[hw] = start_mask32(W, p0);
+      if (!ascii_split32(W, p0, &m[hw])) m[hw] = start_mask32(W, p0, false);  // a byte above 0x7F is near
       m[hw] |= dso[hw];
     }
     const bool own1 = lane < 31;  // lane 31's second word is the margin
@@ -1064,7 +1064,7 @@ __global__ void __launch_bounds__(32 * kSplitWarps) k_split_tiles(const uint8_t*
     if (word >= kTileWords - 1) continue;  // the margin: the next tile's own bytes
     const int p0 = kHalo + 32 * word;
     uint32_t m;
-    if (!ascii_split32(W, p0, &m)) m = start_mask32(W, p0);
+    if (!ascii_split32(W, p0, &m)) m = start_mask32(W, p0, false);
     const int64_t gw = t0 / 32 + word;
     if (gw < n_words) {
       const int64_t first_bit = gw * 32;
