@@ -432,6 +432,16 @@ def run_gpu(args, world, rank, local):
     step_ms = t_start.elapsed_time(t_end) / args.steps
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
 
+    if args.decode_only:
+        if rank == 0:
+            dec = decode_line(bpe, enc, args.steps, peaks()[0])
+            print(json.dumps({"decode_only": True, "workload": workloads.NAMES[cfg], "n_docs": n_docs,
+                              "n_bytes": n_bytes, "tokens": int(n_tokens), **dec}), flush=True)
+        enc.close()
+        if dist:
+            dist.destroy_process_group()
+        return None
+
     if args.kernels_only:
         if rank == 0:
             print(json.dumps({"kernels_only": True, "workload": workloads.NAMES[cfg], "n_docs": n_docs,
@@ -583,6 +593,9 @@ def main():
     ap.add_argument("--reference-slice-mib", type=int, default=64,
                     help="MiB of whole documents per --impl reference step")
     ap.add_argument("--no-configs", action="store_true", help="headline workload only (no C1-C4 lines, no full parity)")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="profiling runs: after the encode steps, only bpe_decode_batch of the encoded batch "
+                         "(3 warm-up calls, then --steps calls); prints a short line that is not a bench result")
     ap.add_argument("--kernels-only", action="store_true",
                     help="profiling runs: the warm-up and timed device calls only (no cache-off, e2e or oracle "
                          "legs); prints a short line that is not a bench result")

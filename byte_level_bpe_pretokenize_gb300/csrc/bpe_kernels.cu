@@ -1847,7 +1847,9 @@ int bpe_decode_batch(bpe_handle* h, const int32_t* d_ids, int64_t n_ids, const i
   k_dec_first_doc<<<(unsigned)std::min<int64_t>(4096, (n_first + 255) / 256), 256, 0, st>>>(d_id_offsets, n_docs, n_ids,
                                                                                            n_tiles, first_doc,
                                                                                            h->d_small);
-  k_dec_write<<<tile_grid, 32 * kDecWarps, 0, st>>>(d_ids, n_ids, h->d_vent, h->d_vbytes, h->d_voffs, h->n_vocab,
+  // k_dec_write: one wave (three CTAs fit an SM: registers and shared memory)
+  const unsigned write_grid = (unsigned)std::min<int64_t>((n_tiles + kDecWarps - 1) / kDecWarps, 3 * h->n_sms);
+  k_dec_write<<<write_grid, 32 * kDecWarps, 0, st>>>(d_ids, n_ids, h->d_vent, h->d_vbytes, h->d_voffs, h->n_vocab,
                                                     tile_base, block_sum, first_doc, d_id_offsets, n_docs, n_tiles,
                                                     d_out_bytes, out_capacity, d_out_byte_offsets, h->d_small);
   CK(cudaGetLastError());
