@@ -866,11 +866,6 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_tile_sums(uint64_t* block
 constexpr int kCompactWarps = 8;
 
 // What k_compact keeps per tile while it walks the stage.
-struct CompactState {
-  uint64_t at0;    // output position of the chunk's first entry
-  uint32_t nmark;  // document marks so far
-};
-
 // A warp per tile: its stage entries to out_ids at the tile's offset without
 // the holes, each placeholder given its deferred pre-token's id count (the
 // ids are copied from the pool by k_giant_copy). The used part of the tile's
@@ -911,11 +906,19 @@ __global__ void __launch_bounds__(32 * kCompactWarps, 4) k_compact(const TileRec
     const uint32_t* src = stage + t * (int64_t)kTileBits;
     const uint32_t first = min(R.resv, (uint32_t)kCompactPart);
     for (uint32_t c = lane; 4 * c < first; c += 32) cp_async16(ent + 4 * c, src + 4 * c);
-    CompactState st{base_n, 0u};
+    // positions within the tile are 32-bit: at < resv + extra ids of its
+    // deferred pre-tokens, ids of the tile's documents k - k0 < 2^31
+    const int64_t base = (int64_t)base_n;
+    int32_t* out_t = out_ids + base;
+    const int64_t room = capacity - base;  // ids of this tile that fit
+    const uint32_t cap_t = room <= 0 ? 0u : (room >= (int64_t)UINT32_MAX ? UINT32_MAX : (uint32_t)room);
+    int64_t* offs_t = out_offsets + R.k0;
+    const uint32_t n_k = (uint32_t)(R.k1 - R.k0);
     if (t + warps < n_tiles) {
       Rn = rec[t + warps];
       base_n = tile_base[t + warps] + block_sum[(t + warps) / kScanThreads];
     }
+    uint32_t at0 = 0, nmark = 0;  // the next chunk's first position, document marks so far
     const bool dup = (R.flags & kTileDup) != 0;
     int64_t k_next = R.k0;  // tiles with empty documents: the first document not yet placed
     for (uint32_t p0 = 0; p0 < R.resv; p0 += kCompactPart) {
@@ -930,7 +933,7 @@ __global__ void __launch_bounds__(32 * kCompactWarps, 4) k_compact(const TileRec
         const uint32_t e = q0 + lane < n_part ? ent[q0 + lane] : kIdHole;
         const bool plain = (e & kIdSpecial) == 0;  // an id (no hole, no placeholder)
         const uint32_t pb = __ballot_sync(0xFFFFFFFFu, plain);
-        uint64_t at = st.at0 + lane;
+        uint32_t at = at0 + lane;
         uint32_t n_here = 32;  // ids this chunk places
         bool ph = false;
         if (pb != 0xFFFFFFFFu) {
@@ -940,19 +943,19 @@ __global__ void __launch_bounds__(32 * kCompactWarps, 4) k_compact(const TileRec
           if (valid && !plain && !ph) atomicOr(&small->status, kStInternal);
           const uint32_t n_ids = (!valid || (!plain && !ph)) ? 0u : (ph ? giants[e & kIdIndex].count : 1u);
           const uint32_t incl = warp_scan_incl(n_ids);
-          at = st.at0 + (incl - n_ids);
+          at = at0 + (incl - n_ids);
           n_here = __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
         if (plain) {
-          if ((int64_t)at < capacity) out_ids[at] = (int32_t)(e & ~kIdDoc);
+          if (at < cap_t) out_t[at] = (int32_t)(e & ~kIdDoc);
           else over = true;
         }
         const bool mark = (e & kIdDoc) != 0;
         const uint32_t mb = __ballot_sync(0xFFFFFFFFu, mark);
         if (!dup) {
           if (mark) {
-            const int64_t k = R.k0 + st.nmark + __popc(mb & lanemask_lt());
-            if (k < R.k1) out_offsets[k] = (int64_t)at;
+            const uint32_t k = nmark + __popc(mb & lanemask_lt());
+            if (k < n_k) offs_t[k] = base + at;
             else atomicOr(&small->status, kStInternal);
           }
         } else {
@@ -960,11 +963,11 @@ __global__ void __launch_bounds__(32 * kCompactWarps, 4) k_compact(const TileRec
           while (mm) {  // marks in rank order: each takes the documents at its start
             const int m_lane = __ffs(mm) - 1;
             mm &= mm - 1;
-            const uint64_t at_m = __shfl_sync(0xFFFFFFFFu, at, m_lane);
+            const int64_t at_m = base + __shfl_sync(0xFFFFFFFFu, at, m_lane);
             const int64_t o0 = k_next < R.k1 ? doc_offsets[k_next] : INT64_MAX;
             int64_t k = k_next;
             while (k < R.k1 && doc_offsets[k] == o0) {
-              if (lane == 0) out_offsets[k] = (int64_t)at_m;
+              if (lane == 0) out_offsets[k] = at_m;
               ++k;
             }
             if (k == k_next) atomicOr(&small->status, kStInternal);
@@ -976,16 +979,16 @@ __global__ void __launch_bounds__(32 * kCompactWarps, 4) k_compact(const TileRec
           const int src_lane = __ffs(phm) - 1;
           phm &= phm - 1;
           const uint32_t gv = __shfl_sync(0xFFFFFFFFu, e, src_lane);
-          const uint64_t gat = __shfl_sync(0xFFFFFFFFu, at, src_lane);
-          if (lane == 0) giants[gv & kIdIndex].at = (int64_t)gat;  // k_giant_copy copies its ids
+          const uint32_t gat = __shfl_sync(0xFFFFFFFFu, at, src_lane);
+          if (lane == 0) giants[gv & kIdIndex].at = base + gat;  // k_giant_copy copies its ids
         }
-        st.nmark += __popc(mb);
-        st.at0 += n_here;
+        nmark += __popc(mb);
+        at0 += n_here;
       }
     }
     // documents with no mark: at the end of the last document
-    const int64_t k_rest = !dup ? R.k0 + st.nmark : k_next;
-    for (int64_t k = k_rest + lane; k < R.k1; k += 32) out_offsets[k] = (int64_t)st.at0;
+    const int64_t k_rest = !dup ? R.k0 + nmark : k_next;
+    for (int64_t k = k_rest + lane; k < R.k1; k += 32) out_offsets[k] = base + at0;
     __syncwarp();
   }
   if (over) atomicOr(&small->status, kStCapacity);
