@@ -36,14 +36,20 @@ TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic_serving_batch.json")
 KERNEL_SPAN = "k_prep_docs..k_giant_copy"
 LAUNCHES_PER_CALL = 9
 KERNEL_SRC = [os.path.join(ROOT, "byte_level_bpe_pretokenize_gb300", "csrc", f)
-              for f in ("bpe_kernels.cu", "tiles.cuh", "class_table.inc")]
+              for f in ("bpe_kernels.cu", "tiles.cuh", "memo.cuh", "decode.cuh", "train.cuh", "class_table.inc")]
 
 
 def kernel_hash() -> str:
-    """Hash of the kernel sources (the translation unit and what it includes)."""
+    """Hash of the kernel sources (the translation unit and what it includes),
+    comments and blank space left out, so that a change to a comment keeps a
+    profile taken on the same code."""
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SRC:
-        h.update(open(f, "rb").read())
+        text = open(f, encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

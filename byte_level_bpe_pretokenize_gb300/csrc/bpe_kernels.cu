@@ -10,11 +10,12 @@
 // Encoding schrittweise").
 //
 // GPU design (none of it is on the pages, whose engines are CPU code):
-//   * One pass over the input (k_tiles, tiles.cuh): a warp per 992-byte tile
-//     splits, probes the word cache, merges the misses and writes the ids;
-//     a decoupled look-back over the tiles' counts gives each tile its output
-//     offset.
-//   * Split (start_mask32): each lane takes 32 bytes.
+//   * One pass over the input (k_tiles, tiles.cuh): a warp per 2016-byte tile
+//     splits it, probes the word cache for every pre-token, and writes the
+//     tile's ids to its stage slot, reserving room for the misses (their
+//     byte length) and a placeholder for each pre-token over 64 bytes.
+//   * Split (ascii_split32 in tiles.cuh, start_mask32 here): each lane takes
+//     two words of 32 bytes.
 //     - When they and their context are ASCII, carry-free SWAR range tests
 //       give per-byte class masks, and the split rules are a dozen mask
 //       operations; each apostrophe resolves its contraction in place.
@@ -29,18 +30,25 @@
 //   * Word cache ("Hugging Face Tokenizers v1", section on word caching: the
 //     same pre-token always gives the same ids, so a memo from pre-token bytes
 //     to ids skips the merge loop).
-//     - bpe_build fills it once, by running the merge loop on strings of at
-//       most 16 bytes: vocabulary strings, space-stripped vocabulary words and
+//     - bpe_build fills it once, by running the merge loop on strings of 2 to
+//       16 bytes: vocabulary strings, space-stripped vocabulary words and
 //       prefixes of both.
-//     - A pre-token found there takes the stored ids.
-//   * Merges of cache misses (at most 64 bytes) by lane groups of 4 to 32
-//     lanes (merge_group): each step is a group-wide minimum, a ballot of the
-//     pair's positions and a run-parity mask for the non-overlapping
-//     left-to-right choice.
+//     - A pre-token found there takes the stored ids; one of a single byte is
+//       its own token.
+//   * Cache misses (at most 64 bytes) are merged GPU-wide (k_misses): a lane
+//     per miss of up to 8 bytes (merge_thread), groups of 8, 16 or 32 lanes
+//     for longer ones (merge_group: each step is a group-wide minimum, a
+//     ballot of the pair's positions and a run-parity mask for the
+//     non-overlapping left-to-right choice). memo.cuh adds a per-call memo of
+//     repeated misses.
 //   * Longer pre-tokens are merged by a whole CTA each (k_giants,
 //     merge_long) in a device pool indexed by input byte, so each owns the
-//     pool range of its own bytes; their tiles' ids are placed by the fix-up
-//     kernels after a scan of all tile counts.
+//     pool range of its own bytes.
+//   * A scan of the tiles' final counts, then k_compact (ids into place
+//     without the holes, document offsets) and k_giant_copy (the long
+//     pre-tokens' ids). No kernel waits on another CTA.
+//   * decode.cuh: ids back to bytes; train.cuh: the merge table trained on
+//     the GPU.
 
 #include <cuda_runtime.h>
 

@@ -29,8 +29,9 @@
 //   * Long pre-tokens (k_giants): a CTA each, in a pool at their own bytes.
 //   * Output: a two-level scan of the tiles' final counts (k_scan_tiles,
 //     k_scan_tile_sums), then k_compact moves every tile's ids into place
-//     without the holes, expanding the placeholders, and writes the document
-//     offsets. No kernel waits on another CTA.
+//     without the holes, gives each placeholder its output position, and
+//     writes the document offsets; k_giant_copy copies the long pre-tokens'
+//     ids there. No kernel waits on another CTA.
 
 namespace {
 
