@@ -770,7 +770,8 @@ __device__ uint32_t merge_group(GroupScratch& W, const uint8_t* src, uint32_t n,
 // writes only below where it read). A step is one pass: the chosen pair
 // (A, B) is replaced left to right without overlap, and every pair of the
 // new sequence is looked up for the next step's lowest rank (four home
-// buckets in flight a thread). Within a round each thread takes
+// buckets in flight a thread). The first pass merges nothing, so it only
+// maps bytes to symbols and looks up their pairs, without scans or barriers. Within a round each thread takes
 // kLongPerThread elements; whether its first element was consumed by the
 // merge before it, and where its kept symbols go, come from one CTA scan of
 // (transfer function, kept count) elements.
@@ -804,7 +805,32 @@ __device__ uint32_t merge_long(const uint8_t* g_bytes, int64_t s, uint32_t n, in
   uint32_t par = 0;
   for (;;) {
     uint32_t W = 0, carry = 0, prev_sym = kNone, local_min = kInf;
-    for (uint32_t r0 = 0; r0 < len; r0 += kRound, par ^= 1u) {
+    if (first_pass) {
+      // Nothing merges in the first pass: every byte's symbol stays where it
+      // is, so a thread looks up its own pairs (the next thread's first
+      // symbol read directly) with no scan and no barrier.
+      for (uint32_t r0 = 0; r0 < len; r0 += kRound) {
+        uint32_t x[kLongPerThread + 1], bk[kLongPerThread];
+        uint4 u[kLongPerThread], v[kLongPerThread];
+        const uint32_t i0 = r0 + (uint32_t)tid * kLongPerThread;
+#pragma unroll
+        for (int k = 0; k <= kLongPerThread; ++k) x[k] = i0 + k < len ? (uint32_t)byte_id[g_bytes[s + i0 + k]] : kNone;
+#pragma unroll
+        for (int k = 0; k < kLongPerThread; ++k) {
+          if (x[k] != kNone) scr[i0 + k] = (int32_t)x[k];
+          bk[k] = pair_hash(x[k], x[k + 1]) & T.hmask;
+          if (x[k + 1] != kNone) ldg32(T.ht + 2ull * bk[k], u[k], v[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < kLongPerThread; ++k) {
+          if (x[k + 1] == kNone) continue;
+          uint32_t nw;
+          local_min = min(local_min, lookup_pair_from(T, x[k], x[k + 1], bk[k], u[k], v[k], &nw));
+        }
+      }
+      W = len;
+    }
+    for (uint32_t r0 = 0; !first_pass && r0 < len; r0 += kRound, par ^= 1u) {
       uint32_t x[kLongPerThread + 1];
 #pragma unroll
       for (int k = 0; k <= kLongPerThread; ++k) {
