@@ -93,15 +93,17 @@ int bpe_build(const int32_t* merges, int64_t n_merges, const uint8_t* vocab_byte
  *                  the next bpe_sync_status() on the handle.
  *   stream         the CUDA stream to run on.
  *
- * Workspace: the handle keeps about 12.6 bytes per input byte:
- *   - a stage of 4.1 bytes per input byte (each 992-byte tile's ids at their
+ * Workspace: the handle keeps about 12.7 bytes per input byte:
+ *   - a stage of 4.1 bytes per input byte (each 2016-byte tile's ids at their
  *     reserved positions, before the tiles' offsets are known);
  *   - a queue of 4 bytes per input byte for the word-cache misses the tiles
  *     hand to the GPU-wide miss merge (a miss has at least 2 bytes);
  *   - a pool of 4 bytes per input byte (scratch for pre-tokens longer than
  *     64 bytes, each using the range of its own bytes);
- *   - about 48 bytes per tile (first document, record, first pre-token start,
- *     offset) and records of the long pre-tokens.
+ *   - about 56 bytes per tile (first document, record, first pre-token start,
+ *     offset) and records of the long pre-tokens (40 bytes each);
+ *   - with the per-call memo on (bpe_set_call_memo), 2 bytes per input byte
+ *     more and a table of at most 128 MiB.
  * The workspace grows (cudaFree of the old one, then cudaMalloc) the first
  * time a larger batch is seen. No kernel of the call waits on another CTA.
  */
