@@ -42,7 +42,7 @@ using TileWin = WindowSmem<kTileBits, 0, true>;    // window: 16 + 2048 + 16 byt
 static_assert(TileWin::kLen == kHalo + kTileBits + kHalo, "tile window");
 constexpr int kTileWarps = 8;                      // warps (tiles in flight) per CTA
 constexpr int kTileThreads = 32 * kTileWarps;
-constexpr int kTileCtasPerSm = 3;                  // resident CTAs (registers: 85 a thread)
+constexpr int kTileCtasPerSm = 3;                  // resident CTAs (registers: at most 85 a thread)
 constexpr int kMissCap = 128;                      // miss records a tile holds before it hands them on
 constexpr int kMissFlush = kMissCap - 64;          // hand on once this many are held (a round adds <= 64)
 
