@@ -362,6 +362,25 @@ __device__ __forceinline__ Ascii4 ascii_classes(uint32_t w) {
   return r;
 }
 
+// SWAR class flags of four ASCII bytes (0x80 in each byte that is a letter,
+// a digit, whitespace, or U+0020); bytes must be below 0x80 (no carries).
+struct Flags4 {
+  uint32_t L, N, S, SP;
+};
+
+__device__ __forceinline__ Flags4 ascii_flags(uint32_t w) {
+  const uint32_t H = 0x80808080u;
+  const uint32_t t = w | 0x20202020u;  // fold case
+  Flags4 f;
+  f.L = (t + 0x1F1F1F1Fu) & ~(t + 0x05050505u) & H;   // 'a' .. 'z'
+  f.N = (w + 0x50505050u) & ~(w + 0x46464646u) & H;   // '0' .. '9'
+  f.SP = ~((w ^ 0x20202020u) + 0x7F7F7F7Fu) & H;      // == 0x20
+  f.S = ((w + 0x77777777u) & ~(w + 0x72727272u) & H) | f.SP;  // 0x09 .. 0x0D or 0x20
+  return f;
+}
+
+// Eight 0x80 flags of words a, b -> 8 bits in byte order, in bits 24..31.
+__device__ __forceinline__ uint32_t gather8(uint32_t a, uint32_t b) { return ((a >> 4) | b) * 0x00204081u; }
 // 0x80-per-byte mask of a word -> 4 bits (byte j -> bit j).
 __device__ __forceinline__ uint32_t movemask4(uint32_t m) { return ((m >> 7) * 0x01020408u) >> 24; }
 
@@ -575,35 +594,59 @@ __device__ uint32_t start_mask32(const SS& S, int p0, bool try_ascii = true) {
     const uint32_t ascii = ascii_starts32(S, p0, reinterpret_cast<const uint32_t*>(S.win + p0) - 1, D, O, &any);
     if (!(any & 0x80808080u)) return ascii;
   }
-  // General: scan the UTF-8 units of bytes [p0 - 7, p0 + 33); each byte
-  // carries its unit's class. Units starting before p0 - 8 may be misread
-  // only up to p0 - 5, and nothing before p0 - 4 is used.
+  // General: the UTF-8 units of bytes [p0 - 7, p0 + 33); each byte carries
+  // its unit's class (bit k of the masks is byte p0 - 8 + k). Units starting
+  // before p0 - 8 may be misread only up to p0 - 5, and nothing before p0 - 4
+  // is used. ASCII bytes are units of their own, classed by the SWAR tests of
+  // twelve aligned words with every byte above 0x7F cleared first; only the
+  // bytes above 0x7F are walked, a unit at a time.
   const int base = p0 - 8;
-  uint64_t U = 0, Lm = 0, Nm = 0, Sm = 0, SPm = 0, APm = 0, MBS = 0;
-  int rem = 0, cls = kO;
-#pragma unroll 4
-  for (int k = 1; k < 41; ++k) {
-    const int q = base + k;
-    const uint32_t b = S.win[q];
-    const uint64_t bit = 1ull << k;
-    if (D & bit) rem = 0;
-    if (rem > 0) {
-      --rem;
-    } else {
-      U |= bit;
-      const uint32_t dn = (uint32_t)(D >> (k + 1)) & 7u;  // document edges at q + 1 .. q + 3
-      const int hi = dn ? q + __ffs(dn) : q + 4;
-      const int len = seq_len(S.win, hi, q);
-      cls = unit_class(S.win, q, len);
-      rem = (len > 1 ? len : 1) - 1;
-      if (cls == kS && len > 1) MBS |= bit;
-    }
-    Lm |= cls == kL ? bit : 0ull;
-    Nm |= cls == kN ? bit : 0ull;
-    Sm |= cls == kS ? bit : 0ull;
-    SPm |= b == 0x20u ? bit : 0ull;
-    APm |= b == 0x27u ? bit : 0ull;
+  const uint32_t* w32 = reinterpret_cast<const uint32_t*>(S.win + base);
+  uint64_t Lm = 0, Nm = 0, Sm = 0, SPm = 0, APm = 0, NA = 0;
+#pragma unroll
+  for (int i = 0; i < 6; ++i) {
+    uint32_t wa = lds_u32(w32 + 2 * i), wb = lds_u32(w32 + 2 * i + 1);
+    const uint32_t ha = wa & 0x80808080u, hb = wb & 0x80808080u;
+    wa &= ~((ha >> 7) * 0xFFu);  // bytes above 0x7F -> 0 (class O, no apostrophe)
+    wb &= ~((hb >> 7) * 0xFFu);
+    const Flags4 fa = ascii_flags(wa), fb = ascii_flags(wb);
+    const uint32_t xa = wa ^ 0x27272727u, xb = wb ^ 0x27272727u;
+    const uint32_t aa = ~(xa + 0x7F7F7F7Fu) & 0x80808080u, ab = ~(xb + 0x7F7F7F7Fu) & 0x80808080u;
+    const int sh = 8 * i;
+    Lm |= (uint64_t)(gather8(fa.L, fb.L) >> 24) << sh;
+    Nm |= (uint64_t)(gather8(fa.N, fb.N) >> 24) << sh;
+    Sm |= (uint64_t)(gather8(fa.S, fb.S) >> 24) << sh;
+    SPm |= (uint64_t)(gather8(fa.SP, fb.SP) >> 24) << sh;
+    APm |= (uint64_t)(gather8(aa, ab) >> 24) << sh;
+    NA |= (uint64_t)(gather8(ha, hb) >> 24) << sh;
   }
+  const uint64_t kSpan = 0x1FFFFFFFFFEull;  // bits 1 .. 40
+  uint64_t cons = 0, MBS = 0;                // continuation bytes of multi-byte units; multi-byte whitespace
+  uint64_t na = NA & kSpan;
+  while (na) {
+    const int k = __ffsll((long long)na) - 1;
+    na &= na - 1;
+    if ((cons >> k) & 1ull) continue;  // inside the unit before
+    const int q = base + k;
+    const uint32_t dn = (uint32_t)(D >> (k + 1)) & 7u;  // document edges at q + 1 .. q + 3
+    const int hi = dn ? q + __ffs(dn) : q + 4;
+    const int len = seq_len(S.win, hi, q);
+    const int cls = unit_class(S.win, q, len);
+    const uint64_t unit = ((len > 1 ? (1ull << len) : 2ull) - 1ull) << k;  // its bytes
+    if (len > 1) cons |= unit & ~(1ull << k);
+    if (cls == kL) Lm |= unit;
+    if (cls == kN) Nm |= unit;
+    if (cls == kS) {
+      Sm |= unit;
+      if (len > 1) MBS |= 1ull << k;
+    }
+  }
+  const uint64_t U = kSpan & ~cons;
+  Lm &= kSpan;
+  Nm &= kSpan;
+  Sm &= kSpan;
+  SPm &= kSpan;
+  APm &= kSpan;
   uint32_t res = boundaries32(S, p0, U, Lm, Nm, Sm, SPm, APm, D, O);
   // Whitespace of several bytes (B2 looks past the whole unit): the per-byte
   // predicate.

@@ -238,23 +238,6 @@ __device__ __forceinline__ uint4 lds_u128(const void* p) {
   return v;
 }
 
-struct Flags4 {
-  uint32_t L, N, S, SP;
-};
-
-__device__ __forceinline__ Flags4 ascii_flags(uint32_t w) {
-  const uint32_t H = 0x80808080u;
-  const uint32_t t = w | 0x20202020u;  // fold case
-  Flags4 f;
-  f.L = (t + 0x1F1F1F1Fu) & ~(t + 0x05050505u) & H;   // 'a' .. 'z'
-  f.N = (w + 0x50505050u) & ~(w + 0x46464646u) & H;   // '0' .. '9'
-  f.SP = ~((w ^ 0x20202020u) + 0x7F7F7F7Fu) & H;      // == 0x20
-  f.S = ((w + 0x77777777u) & ~(w + 0x72727272u) & H) | f.SP;  // 0x09 .. 0x0D or 0x20
-  return f;
-}
-
-// Eight 0x80 flags of words a, b -> 8 bits in byte order, in bits 24..31.
-__device__ __forceinline__ uint32_t gather8(uint32_t a, uint32_t b) { return ((a >> 4) | b) * 0x00204081u; }
 // Bits 24..31 of p0..p3 -> one word (p0's in byte 0).
 __device__ __forceinline__ uint32_t gather32(uint32_t p0, uint32_t p1, uint32_t p2, uint32_t p3) {
   return __byte_perm(__byte_perm(p0, p1, 0x0073u), __byte_perm(p2, p3, 0x0073u), 0x5410u);
